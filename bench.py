@@ -1,0 +1,578 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode hot path on GB300: prints ONE JSON line.
+
+A step is one decode step of one attention layer for the whole batch: the
+append of every sequence's new K/V row (kvc_append) followed by paged decode
+attention over the whole cache (kvc_decode_attention, whose split-K merge runs
+inside the same call). Inputs are resident in HBM; the L2 is flushed (a
+256 MiB write) between timed steps, outside the timed events.
+
+Default workload: a Llama-3-8B-shaped layer, 32 query / 8 kv heads, head dim
+128, bf16, batch 32, context lengths uniform in [512, 4096] (seed 43),
+block size 16, physical blocks randomly permuted in a pool with 10% spare.
+``value`` is decode-attention GB/s over the algorithmic bytes of a step (K/V
+rows actually attended, q, out, the table entries read, lengths, plus the
+append's reads and writes). The other shapes (all-4096 contexts, the shared-
+prefix MHA batch, the long-context split-K batch, MLA, the tiny fp32 model)
+are measured too and reported under ``variants``.
+
+--impl reference times the CPU oracle instead (bounded samples of the same
+workload on the host cores), for the driver's ratio.
+"""
+
+from __future__ import annotations
+
+import os
+
+# The oracle legs run NumPy single-threaded (their core count is reported as 1).
+for _v in ("OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "OMP_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention HBM GB/s (% of 8 TB/s roofline) and seq·layer steps/s on 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+MAIN = dict(name="gqa_llama3_8b_layer", batch=32, hq=32, hkv=8, d=128, bs=16, lens=(512, 4096), dtype="bf16",
+            seed=43)
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            j = json.load(open(p))
+            return float(j["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ workloads
+
+def step_bytes(case_lens, hq, hkv, d, bs, elt, out_elt, unique_kv_rows=None):
+    """Algorithmic bytes of one step (append + decode)."""
+    B = len(case_lens)
+    rows = sum(case_lens) if unique_kv_rows is None else unique_kv_rows
+    kv = rows * hkv * d * elt * 2
+    q = B * hq * d * elt
+    out = B * hq * d * out_elt
+    tables = sum(-(-n // bs) for n in case_lens) * 4
+    lens = B * 4
+    decode = kv + q + out + tables + lens
+    append = B * hkv * d * elt * 2 * 2 + B * 8
+    return decode, append
+
+
+class GqaStep:
+    """Device-resident inputs of one decode step plus the calls that run it."""
+
+    def __init__(self, kvc, case, out_dtype):
+        import torch
+        self.kvc = kvc
+        self.case = case
+        self.dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in case.items()}
+        lens = case["context_lens"].tolist()
+        self.lens = lens
+        self.B, self.hq, self.d = case["q"].shape
+        _, self.hkv, self.bs, _ = case["k_cache"].shape
+        self.slots = kvc.slots_from_tables(case["block_tables"], self.bs, list(range(self.B)),
+                                           [n - 1 for n in lens]).cuda()
+        self.out = torch.empty((self.B, self.hq, self.d), dtype=out_dtype, device="cuda")
+        n = kvc.decode_workspace_size(self.B, self.hq, self.hkv, self.d, self.bs, case["block_tables"].shape[1])
+        self.ws = torch.empty(max(1, n), dtype=torch.uint8, device="cuda")
+        self.scale = 1.0 / math.sqrt(self.d)
+
+    def append(self):
+        d = self.dev
+        self.kvc.append(d["k_new"], d["v_new"], self.slots, d["k_cache"], d["v_cache"])
+
+    def decode(self):
+        d = self.dev
+        self.kvc.decode_attention(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                                  self.scale, self.out, self.ws)
+
+
+def flush_buffer():
+    import torch
+    return torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+
+def time_steps(step, steps, warmup, flush, sampler=None):
+    """Per-step CUDA-event times (ms) of append and decode, L2 flushed between steps."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        step.append()
+        step.decode()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    if sampler:
+        sampler.start()
+        time.sleep(0.2)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step.append()
+        ev[i][1].record(stream)
+        step.decode()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop() if sampler else None
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(steps)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
+    return step_ms, dec_ms, wall, clocks
+
+
+def time_e2e(kvc, step, steps, warmup, flush):
+    """Same step through the public API from pinned host buffers: H2D of the step's
+    inputs (q, new k/v, slots, tables, lengths), append, decode, D2H of the output."""
+    import torch
+    c = step.case
+    host = {k: c[k].pin_memory() for k in ("q", "k_new", "v_new", "block_tables", "context_lens")}
+    host["slots"] = step.slots.cpu().pin_memory()
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    dev = step.dev
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        dev["q"].copy_(host["q"], non_blocking=True)
+        dev["k_new"].copy_(host["k_new"], non_blocking=True)
+        dev["v_new"].copy_(host["v_new"], non_blocking=True)
+        dev["block_tables"].copy_(host["block_tables"], non_blocking=True)
+        dev["context_lens"].copy_(host["context_lens"], non_blocking=True)
+        step.slots.copy_(host["slots"], non_blocking=True)
+        step.append()
+        step.decode()
+        out_h.copy_(step.out, non_blocking=True)
+
+    for _ in range(warmup):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one()
+        b.record(stream)
+        b.synchronize()  # the host needs the result before the next step
+        ts.append(a.elapsed_time(b))
+    return statistics.mean(ts), h2d, d2h
+
+
+# --------------------------------------------------------------- oracle
+
+def oracle_sample_seconds(case, seqs, units=None):
+    """Times the oracle (append + decode) on the given sequences of a case.
+
+    Returns (seconds, algorithmic bytes of that sample).
+    """
+    import numpy as np
+    import torch
+    from oracle import paged as OP
+
+    def f64(t):
+        return t.detach().cpu().to(torch.float64).numpy()
+
+    bs = case["block_size"]
+    tab = case["block_tables"]
+    hkv = case["k_cache"].shape[1]
+    hq, d = case["q"].shape[1], case["q"].shape[2]
+    lens = [int(case["context_lens"][i]) for i in seqs]
+    used = []
+    rows = []
+    for i, n in zip(seqs, lens):
+        nb = -(-n // bs)
+        rows.append(list(range(len(used), len(used) + nb)))
+        used.extend(int(x) for x in tab[i, :nb])
+    maxb = max(len(r) for r in rows)
+    table = np.zeros((len(seqs), maxb), dtype=np.int64)
+    for r, row in enumerate(rows):
+        table[r, :len(row)] = row
+    idx = torch.as_tensor(used, dtype=torch.long, device=case["k_cache"].device)
+    kc = f64(case["k_cache"][idx])
+    vc = f64(case["v_cache"][idx])
+    q = f64(case["q"][list(seqs)])
+    kn = f64(case["k_new"][list(seqs)])
+    vn = f64(case["v_new"][list(seqs)])
+    slots = np.array([table[r, (n - 1) // bs] * bs + (n - 1) % bs for r, n in enumerate(lens)], dtype=np.int64)
+    t0 = time.perf_counter()
+    kc2, vc2 = OP.append_to_paged(kn, vn, slots, kc, vc)
+    OP.paged_decode(q, kc2, vc2, table, lens, 1.0 / math.sqrt(d))
+    dt = time.perf_counter() - t0
+    elt = case["q"].element_size()
+    dec, app = step_bytes(lens, hq, hkv, d, bs, elt, elt)
+    return dt, dec + app
+
+
+def cpu_baseline(case, budget_s=12.0):
+    """Oracle GB/s on a growing sample of whole sequences (about budget_s of CPU work)."""
+    B = case["q"].shape[0]
+    seqs, tot_t, tot_b = [], 0.0, 0
+    i = 0
+    while tot_t < budget_s and i < B:
+        dt, by = oracle_sample_seconds(case, [i])
+        tot_t += dt
+        tot_b += by
+        seqs.append(i)
+        i += 1
+    return {"value": round(tot_b / tot_t / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"append + decode of sequences 0..{len(seqs) - 1} of the same workload "
+                      f"({len(seqs)} of {B} sequences, all heads), float64 NumPy, single thread; "
+                      f"{tot_t:.1f} s"}
+
+
+# --------------------------------------------------------------- variants
+
+def measure_gqa_case(kvc, case, steps, warmup, flush, unique_rows=None):
+    import torch
+    st = GqaStep(kvc, case, torch.bfloat16)
+    step_ms, dec_ms, _, _ = time_steps(st, steps, warmup, flush)
+    lens = st.lens
+    dec_b, app_b = step_bytes(lens, st.hq, st.hkv, st.d, st.bs, case["q"].element_size(), 2, unique_rows)
+    ms = statistics.mean(step_ms)
+    dms = statistics.mean(dec_ms)
+    res = {"ms_per_step": round(ms, 5), "gbps": round((dec_b + app_b) / ms / 1e6, 1),
+           "decode_ms": round(dms, 5), "decode_gbps": round(dec_b / dms / 1e6, 1),
+           "frac_of_8tbs": round(dec_b / dms / 1e6 / NOMINAL_HBM_GBS, 4),
+           "seq_layer_steps_per_s": round(len(lens) / (ms / 1e3), 1), "bytes_per_step": dec_b + app_b}
+    del st
+    torch.cuda.empty_cache()
+    return res
+
+
+def variants(kvc, flush, steps):
+    import torch
+    from paged_kv_cache_157_gb300 import workloads as W
+    out = {}
+    try:
+        c = W.gqa_case(32, 32, 8, 128, 16, [4096] * 32, "bf16", 43, device="cuda")
+        out["gqa_b32_ctx4096"] = measure_gqa_case(kvc, c, steps, 5, flush)
+        del c
+        c = W.shared_case(8, 8, 2048, 256, 32, 128, 16, "f16", 44, device="cuda")
+        unique = 8 * 2048 + 64 * 256
+        r = measure_gqa_case(kvc, c, steps, 5, flush, unique_rows=unique)
+        logical, _ = step_bytes(c["context_lens"].tolist(), 32, 32, 128, 16, 2, 2)
+        r["logical_decode_bytes"] = logical
+        r["note"] = "gbps counts each shared prompt block once (unique physical bytes)"
+        out["mha_shared_prefix_8x8"] = r
+        del c
+        c = W.gqa_case(4, 64, 8, 128, 16, [32768, 65536, 131072, 131072], "bf16", 45, device="cuda")
+        out["gqa_long_splitk"] = measure_gqa_case(kvc, c, max(5, steps // 4), 3, flush)
+        del c
+        torch.cuda.empty_cache()
+        c = W.gqa_case(3, 64, 8, 128, 16, [17, 31, 32], "bf16", 45, device="cuda")
+        out["gqa_ragged_17_31_32"] = measure_gqa_case(kvc, c, steps, 5, flush)
+        del c
+        out["tiny_mha_fp32"] = measure_tiny(kvc, flush, steps)
+        out["mla_deepseek_v2"] = measure_mla(kvc, flush, steps)
+    except Exception as e:  # report, do not hide, a failing variant
+        out["error"] = f"{type(e).__name__}: {e}"
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_tiny(kvc, flush, steps):
+    """1 sequence, 2 layers, 4 heads x 32, fp32: seq*layer decode steps per second (append + decode)."""
+    import torch
+    from paged_kv_cache_157_gb300 import workloads as W
+    res = []
+    for L in range(2):
+        c = W.gqa_case(1, 4, 4, 32, 16, [69], "f32", 42 + L, device="cuda")
+        st = GqaStep(kvc, c, torch.float32)
+        step_ms, _, _, _ = time_steps(st, steps, 5, flush)
+        res.append(statistics.mean(step_ms))
+    ms = sum(res)
+    return {"ms_per_step_2_layers": round(ms, 5), "seq_layer_steps_per_s": round(2 / (ms / 1e3), 1),
+            "note": "latency-bound: one sequence of 69 tokens"}
+
+
+def measure_mla(kvc, flush, steps):
+    import torch
+    from paged_kv_cache_157_gb300 import workloads as W
+    try:
+        kvc.decode_mla_workspace_size(64, 128, 512, 64, 64, 128)
+    except kvc.KvcError as e:
+        return {"unavailable": str(e)}
+    c = W.mla_case(64, 128, 512, 64, 64, (1024, 8192), "bf16", 46, device="cuda")
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in c.items()}
+    lens = c["context_lens"].tolist()
+    B = 64
+    slots = kvc.slots_from_tables(c["block_tables"], 64, list(range(B)), [n - 1 for n in lens]).cuda()
+    out = torch.empty((B, 128, 512), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(1, kvc.decode_mla_workspace_size(B, 128, 512, 64, 64, c["block_tables"].shape[1])),
+                     dtype=torch.uint8, device="cuda")
+    scale = 1.0 / 24.0
+
+    class S:
+        def append(self):
+            kvc.append_latent(d["c_new"], slots, d["latent_cache"], 512)
+
+        def decode(self):
+            kvc.decode_attention_mla(d["q"], d["latent_cache"], d["block_tables"], d["context_lens"], scale, 512,
+                                     out, ws)
+
+    step_ms, dec_ms, _, _ = time_steps(S(), steps, 5, flush)
+    rows = sum(lens)
+    dec_b = rows * 576 * 2 + B * 128 * 576 * 2 + B * 128 * 512 * 2 + sum(-(-n // 64) for n in lens) * 4 + B * 4
+    flops = rows * 128 * 2 * (576 + 512)
+    dms = statistics.mean(dec_ms)
+    return {"decode_ms": round(dms, 5), "decode_gbps": round(dec_b / dms / 1e6, 1),
+            "tflops": round(flops / dms / 1e9, 1), "frac_of_8tbs": round(dec_b / dms / 1e6 / NOMINAL_HBM_GBS, 4),
+            "ms_per_step": round(statistics.mean(step_ms), 5), "bytes_per_step": dec_b, "flops_per_step": flops}
+
+
+# ------------------------------------------------------------------- main
+
+def traffic_from_profile():
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if the
+    kernel source has not changed since it was taken; else None."""
+    p = os.path.join(ROOT, "profiles", "gqa_decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        j = json.load(open(p))
+        if j.get("source_sha256") != kernel_source_sha():
+            return None
+        return j.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("decode_gqa_impl.cuh", "decode_gqa.h", "kvc_device.cuh", "decode_gqa_api.cu", "decode_gqa_launch.cuh"):
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_157_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def run_kvc(args):
+    import torch
+    import torch.distributed as dist
+    import paged_kv_cache_157_gb300 as kvc
+    from paged_kv_cache_157_gb300 import build_lib
+    from paged_kv_cache_157_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    if rank == 0:
+        build_lib.build()
+    if world > 1:
+        dist.barrier()
+    kvc.raw()
+
+    m = MAIN
+    case = W.gqa_case(m["batch"], m["hq"], m["hkv"], m["d"], m["bs"], m["lens"], m["dtype"], m["seed"],
+                      device="cuda")
+    step = GqaStep(kvc, case, torch.bfloat16)
+    flush = flush_buffer()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms, dec_ms, wall, clocks = time_steps(step, args.steps, args.warmup, flush, sampler)
+    if world > 1:
+        dist.barrier()
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms, statistics.mean(dec_ms)], device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, dec_avg = float(t[0]), float(t[1])
+    ms = total_ms / args.steps
+    dec_b, app_b = step_bytes(step.lens, step.hq, step.hkv, step.d, step.bs, 2, 2)
+    per_step = dec_b + app_b
+    value = world * per_step / (ms / 1e3) / 1e9
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+    peak, peak_kind = peaks()
+    achieved = dec_b / (dec_avg / 1e3) / 1e9
+    e2e_ms, h2d, d2h = time_e2e(kvc, step, min(args.steps, 500), min(args.warmup, 10), flush)
+    e2e_value = per_step / (e2e_ms / 1e3) / 1e9
+    var = {} if args.no_variants else variants(kvc, flush, max(10, min(args.steps, 200)))
+    cpu = None if args.no_cpu_baseline else cpu_baseline(case)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/K/V, uniform lengths, permuted block pool)",
+        "config": {
+            "workload": "GQA decode, Llama-3-8B-shaped layer: batch 32, 32 q / 8 kv heads, head_dim 128, bf16, "
+                        "context lengths U[512,4096] (seed 43), block_size 16, permuted pool (+10% spare); "
+                        "step = kvc_append of 32 new tokens + kvc_decode_attention (bf16 out)",
+            "batch": m["batch"], "n_q_heads": m["hq"], "n_kv_heads": m["hkv"], "head_dim": m["d"],
+            "block_size": m["bs"], "context_lens": "U[512,4096]", "mean_context_len": statistics.mean(step.lens),
+            "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "frac_of_8tbs": round(value / NOMINAL_HBM_GBS, 4),
+        "seq_layer_steps_per_s": round(world * m["batch"] / (ms / 1e3), 1),
+        "bytes_per_step": per_step,
+        "roofline": {"bound": "hbm", "kernel": "kvc_decode_attention (gqa_decode_kernel + gqa_merge_kernel)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                     "traffic": traffic_from_profile(), "algorithmic_bytes_per_launch": dec_b},
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "timed_wall_s": round(wall, 4),
+        "cpu_baseline": cpu,
+        "variants": var,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle on the host cores: each step a bounded sample (one whole sequence) of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from paged_kv_cache_157_gb300 import workloads as W
+    m = MAIN
+    case = W.gqa_case(m["batch"], m["hq"], m["hkv"], m["d"], m["bs"], m["lens"], m["dtype"], m["seed"])
+    for i in range(args.warmup):
+        oracle_sample_seconds(case, [i % m["batch"]])
+    budget = 150.0
+    tot_t, tot_b, n = 0.0, 0, 0
+    t_start = time.perf_counter()
+    for i in range(args.steps):
+        dt, by = oracle_sample_seconds(case, [i % m["batch"]])
+        tot_t += dt
+        tot_b += by
+        n += 1
+        if time.perf_counter() - t_start > budget:
+            break
+    value = tot_b / tot_t / 1e9
+    ms = tot_t / n * 1e3
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": 1, "steps": n, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (same seeded workload)",
+        "config": {"workload": "same as the kvc arm; each step is one whole sequence (all heads) of it",
+                   "requested_steps": args.steps},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "append + decode of one sequence (all heads) per step, float64 NumPy, "
+                                   "single thread"},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
+    ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_kvc(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,227 @@
+/*
+ * kvc.h: C ABI of the paged KV-cache decode library for GB300 (sm_103a).
+ *
+ * What the library computes (source pages, by title and section):
+ *
+ *   "KV缓存原理与显存估算" (LLM Systems Wiki), knowledge point 2: one new
+ *   query per sequence attends over every cached row after the current K/V
+ *   has been appended: z_i = scale * q.k_i, a = softmax(z) with the maximum
+ *   subtracted, o = sum_i a_i v_i.
+ *   "KV Cache（键值缓存）" (llm-compass) section 2.3 (PagedAttention): the
+ *   cache of a sequence is cut into fixed-size blocks; a block table maps
+ *   logical block j to a physical block in a shared pool; section 2.2:
+ *   MHA / MQA / GQA head sharing and the MLA latent cache (d_c + d_R per
+ *   token, W^UK / W^UV absorbed into the query / output side).
+ *   "单请求 KV Cache" (mini-vllm step 07): preallocated storage written in
+ *   place at the new position, never copied.
+ *
+ * Conventions for every call:
+ *   - All calls return kvc_status; KVC_OK is 0. No C++ exception crosses
+ *     this boundary. kvc_last_error_message() gives a one-line reason for
+ *     the most recent failure on the calling thread.
+ *   - Device pointers are plain CUDA device addresses on the current device.
+ *     The caller owns every buffer; the library never allocates, frees or
+ *     retains device memory, and keeps no pointer after a call returns.
+ *   - Compute calls are asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) unless checked mode is on.
+ *   - Arguments are validated on the host first (KVC_ERR_INVALID_ARG,
+ *     KVC_ERR_UNSUPPORTED). Values that live in device memory (block ids,
+ *     context lengths, slots) are checked inside the kernels: an out-of-range
+ *     value is never dereferenced, the affected output is left as zeros or
+ *     skipped, and a bit is set in the device error word
+ *     (kvc_get_error_flags). No kernel traps, asserts or waits without a
+ *     bound.
+ *
+ * Layouts (row-major, element type given by a kvc_dtype):
+ *   k_cache, v_cache  [num_blocks, n_kv_heads, block_size, head_dim]
+ *   latent_cache      [num_blocks, block_size, d_c + d_r]
+ *   block_tables      int32 [batch, max_blocks_per_seq]; entry j of row i is
+ *                     the physical block holding logical positions
+ *                     j*block_size .. j*block_size+block_size-1 of sequence i
+ *   context_lens      int32 [batch]; rows attended by sequence i, including the
+ *                     token appended this step (must be >= 1)
+ *   slot_mapping      int64 [num_tokens]; slot = physical_block*block_size +
+ *                     position%block_size; a negative slot means "skip"
+ *   q, out            [batch, n_q_heads, head_dim]; query head h reads kv
+ *                     head h / (n_q_heads / n_kv_heads)
+ */
+#ifndef KVC_H_
+#define KVC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVC_ABI_VERSION 1
+
+typedef enum kvc_status {
+  KVC_OK = 0,
+  KVC_ERR_INVALID_ARG = 1,  /* a host-checkable argument is wrong */
+  KVC_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
+  KVC_ERR_NO_BLOCKS = 3,    /* block pool exhausted; nothing was allocated */
+  KVC_ERR_CUDA = 4,         /* a CUDA runtime call failed */
+  KVC_ERR_OUT_OF_RANGE = 5, /* checked mode: a kernel saw a bad device value */
+  KVC_ERR_WORKSPACE = 6     /* workspace smaller than the size query asked for */
+} kvc_status;
+
+typedef enum kvc_dtype { KVC_F32 = 0, KVC_F16 = 1, KVC_BF16 = 2 } kvc_dtype;
+
+/* Bits of the device error word. */
+#define KVC_FLAG_BAD_BLOCK 0x1u   /* block table entry outside [0, num_blocks) */
+#define KVC_FLAG_BAD_LEN 0x2u     /* context_len < 1 or > max_blocks_per_seq*block_size */
+#define KVC_FLAG_BAD_SLOT 0x4u    /* slot >= num_blocks*block_size */
+#define KVC_FLAG_TIMEOUT 0x8u     /* a bounded wait on an async copy gave up */
+
+typedef void* kvc_stream; /* cudaStream_t */
+
+/* ---------------------------------------------------------------- runtime */
+
+int kvc_abi_version(void);
+const char* kvc_status_string(kvc_status s);
+/* Reason for the last non-OK status returned on this thread ("" if none).
+ * The string stays valid until the next call on the same thread. */
+const char* kvc_last_error_message(void);
+
+typedef enum kvc_option {
+  /* 0 (default): calls are asynchronous. 1: every compute call synchronises
+   * its stream, reads the device error word of the current device, clears
+   * it, and returns KVC_ERR_OUT_OF_RANGE if any bit was set. */
+  KVC_OPT_CHECKED = 0,
+  /* Decode work split: 0 (default) = automatic. N > 0 = every CTA of the
+   * decode kernels takes about N cache blocks (used by tests to force many
+   * split-K partials). Process-wide. */
+  KVC_OPT_BLOCKS_PER_CTA = 1,
+  /* Upper bound on decode CTAs (0 = automatic, SM count x resident CTAs). */
+  KVC_OPT_MAX_CTAS = 2
+} kvc_option;
+kvc_status kvc_set_option(kvc_option opt, int64_t value);
+kvc_status kvc_get_option(kvc_option opt, int64_t* value);
+
+/* Synchronises `stream`, then returns (in *flags) and clears the error word
+ * of the current device. */
+kvc_status kvc_get_error_flags(kvc_stream stream, uint32_t* flags);
+
+/* ----------------------------------------------------------------- append */
+
+/* Writes token t's rows k[t, :, :] and v[t, :, :] (both [num_tokens,
+ * n_kv_heads, head_dim], dtype `dtype`) into k_cache / v_cache at
+ * slot_mapping[t], for every kv head: cache[slot/bs, h, slot%bs, :] = k[t,h,:].
+ * Bit-exact copy. Negative slots are skipped; slots >= num_blocks*block_size
+ * are skipped and set KVC_FLAG_BAD_SLOT. Two tokens mapped to the same slot
+ * race (the result is one of them). num_tokens == 0 is a no-op.
+ * Requires head_dim*element_size to be a multiple of 16 bytes and all
+ * pointers 16-byte aligned.
+ * Source: the in-place write at the current position ("单请求 KV Cache",
+ * production practice section) into PagedAttention blocks (llm-compass 2.3). */
+kvc_status kvc_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                      void* k_cache, void* v_cache, int64_t num_blocks, int block_size, int n_kv_heads,
+                      int head_dim, kvc_dtype dtype, kvc_stream stream);
+
+/* MLA form: writes row c[t, :] (width d_c + d_r) into
+ * latent_cache[slot/bs, slot%bs, :]. Same rules as kvc_append.
+ * Source: llm-compass section 2.2 (one shared latent plus decoupled RoPE part
+ * cached per token). */
+kvc_status kvc_append_latent(const void* c, const int64_t* slot_mapping, int64_t num_tokens,
+                             void* latent_cache, int64_t num_blocks, int block_size, int d_c, int d_r,
+                             kvc_dtype dtype, kvc_stream stream);
+
+/* ----------------------------------------------------------------- decode */
+
+/* Bytes of scratch that kvc_decode_attention needs for these shapes on the
+ * current device (split-K partial results). 0 is a valid answer. The size
+ * depends on the device's SM count and on KVC_OPT_MAX_CTAS. */
+kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                     int max_blocks_per_seq, size_t* bytes);
+
+/* Single-step paged decode attention (MHA, GQA, MQA).
+ *   out[i, h, :] = sum_t a_t v_t,  a = softmax_t(scale * q[i,h,:] . k_t)
+ * over t = 0 .. context_lens[i]-1, rows read through block_tables[i] from
+ * kv head h / (n_q_heads/n_kv_heads). Accumulation is fp32; `out` is written
+ * in out_dtype (F32, F16 or BF16).
+ * Supported: head_dim in {32, 64, 128, 256}; block_size a multiple of 16 up
+ * to 128; n_q_heads % n_kv_heads == 0; batch <= 4096.
+ * workspace: device scratch of at least kvc_decode_workspace_size() bytes,
+ * 256-byte aligned, no initial contents required; may be NULL with
+ * workspace_bytes 0 (then every (sequence, head group) is handled by one
+ * CTA, which balances less well on long contexts). The workspace must not
+ * be shared by calls that may run concurrently.
+ * Sources: knowledge point 2 of "KV缓存原理与显存估算"; head grouping from
+ * "KV-Cache——为什么AI回复越来越快" section 03 and llm-compass 2.2. */
+kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                                int batch, float scale, int n_q_heads, int n_kv_heads, int head_dim,
+                                int block_size, int64_t num_blocks, kvc_dtype dtype, void* out,
+                                kvc_dtype out_dtype, void* workspace, size_t workspace_bytes, kvc_stream stream);
+
+/* Scratch bytes for kvc_decode_attention_mla on the current device. */
+kvc_status kvc_decode_mla_workspace_size(int batch, int n_q_heads, int d_c, int d_r, int block_size,
+                                         int max_blocks_per_seq, size_t* bytes);
+
+/* MLA absorbed decode on tensor cores (tcgen05):
+ *   out[i, h, :] = sum_t a_t c_t[:d_c],  a = softmax_t(scale * q_absorbed[i,h,:] . c_t)
+ * where c_t is the cached row of width d_c + d_r (keys use the whole row,
+ * values its first d_c elements). The caller applies W^UV and the output
+ * projection to `out`. dtype must be BF16; out_dtype F32 or BF16.
+ * Supported: d_c = 512, d_r = 64, n_q_heads a multiple of 64 up to 128,
+ * block_size a multiple of 64. Source: llm-compass section 2.2. */
+kvc_status kvc_decode_attention_mla(const void* q_absorbed, const void* latent_cache, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens, int batch, float scale,
+                                    int n_q_heads, int d_c, int d_r, int block_size, int64_t num_blocks,
+                                    kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
+                                    size_t workspace_bytes, kvc_stream stream);
+
+/* ------------------------------------------------------------- block pool */
+
+/* Host-side refcounted block pool ("KV Cache（键值缓存）" 2.3: blocks on
+ * demand, shared blocks counted by reference; "KV缓存原理与显存估算",
+ * closing section: a block is reusable when its count reaches zero).
+ * Policy: a new block is the lowest-numbered free block; sequence ids are
+ * 0, 1, 2, ... and never reused. Not thread-safe: one thread per pool. */
+typedef struct kvc_pool kvc_pool;
+
+typedef struct kvc_pool_stats {
+  int64_t num_blocks;
+  int64_t free_blocks;
+  int64_t unique_blocks;   /* blocks with refcount > 0 */
+  int64_t table_entries;   /* sum over live sequences of their table lengths */
+  int64_t useful_tokens;   /* sum over live sequences of their lengths */
+  int64_t live_seqs;
+  int32_t block_size;
+} kvc_pool_stats;
+
+kvc_status kvc_pool_create(int64_t num_blocks, int block_size, kvc_pool** pool);
+void kvc_pool_destroy(kvc_pool* pool);
+kvc_status kvc_seq_add(kvc_pool* pool, int64_t* seq);
+/* New sequence sharing all of parent's blocks (each gains one reference). */
+kvc_status kvc_seq_fork(kvc_pool* pool, int64_t parent, int64_t* child);
+/* Extends `seq` by n_new tokens and writes their slots to slots_out[n_new].
+ * Allocates a block at every block boundary. KVC_ERR_NO_BLOCKS if the pool
+ * cannot supply them (nothing allocated, length unchanged).
+ * KVC_ERR_UNSUPPORTED if the last block is partly filled and shared
+ * (would need copy-on-write). */
+kvc_status kvc_seq_reserve(kvc_pool* pool, int64_t seq, int64_t n_new, int64_t* slots_out);
+/* Drops the sequence; each of its blocks loses one reference. */
+kvc_status kvc_seq_free(kvc_pool* pool, int64_t seq);
+kvc_status kvc_seq_length(kvc_pool* pool, int64_t seq, int64_t* length);
+kvc_status kvc_block_refcount(kvc_pool* pool, int64_t block, int32_t* refcount);
+/* Writes table rows (int32 [n, max_blocks], unused entries 0) and lengths
+ * (int32 [n]) for the given sequences, into host memory. */
+kvc_status kvc_build_block_tables(kvc_pool* pool, const int64_t* seqs, int n, int32_t* table_out,
+                                  int max_blocks, int32_t* lens_out);
+kvc_status kvc_pool_get_stats(kvc_pool* pool, kvc_pool_stats* stats);
+
+/* Host helper: slots of (row, position) pairs for an existing host-side
+ * block table (int32 [rows, max_blocks]). Out-of-table positions give
+ * KVC_ERR_INVALID_ARG. */
+kvc_status kvc_slots_from_tables(const int32_t* block_tables, int rows, int max_blocks, int block_size,
+                                 const int32_t* row_index, const int64_t* positions, int64_t n,
+                                 int64_t* slots_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H_ */

@@ -1,0 +1,90 @@
+// Append kernel: scatters the new tokens' K/V rows (or latent rows) to the
+// slots their slot mapping names. One thread moves one 16-byte chunk, so a
+// warp writes whole 512-byte spans of consecutive chunks of a row.
+//
+// Source: in-place write at the current position of a preallocated cache
+// ("单请求 KV Cache", production practice section), into fixed-size
+// PagedAttention blocks ("KV Cache（键值缓存）" section 2.3).
+#include "kvc_device.cuh"
+#include "kvc_internal.h"
+
+namespace kvc {
+
+// Copies rows src[t, h, :] (row_chunks 16-byte chunks each) into
+// dst[slot/bs, h, slot%bs, :] for n_src tensors (1 or 2).
+__global__ void __launch_bounds__(256) append_kernel(const uint4* __restrict__ src0, const uint4* __restrict__ src1,
+                                                     uint4* __restrict__ dst0, uint4* __restrict__ dst1,
+                                                     const int64_t* __restrict__ slots, int64_t num_tokens,
+                                                     int64_t num_slots, int block_size, int n_heads, int row_chunks,
+                                                     unsigned int* err) {
+  const int64_t per_token = static_cast<int64_t>(n_heads) * row_chunks;
+  const int64_t total = num_tokens * per_token;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / per_token;
+    const int64_t r = i - t * per_token;
+    const int h = static_cast<int>(r / row_chunks);
+    const int c = static_cast<int>(r - static_cast<int64_t>(h) * row_chunks);
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (h == 0 && c == 0) set_flag(err, 0x4u);
+      continue;
+    }
+    const int64_t blk = slot / block_size;
+    const int64_t off = slot - blk * block_size;
+    const int64_t d = ((blk * n_heads + h) * block_size + off) * row_chunks + c;
+    dst0[d] = __ldg(src0 + i);
+    if (src1 != nullptr) dst1[d] = __ldg(src1 + i);
+  }
+}
+
+static kvc_status launch_append(bool two, const void* s0, const void* s1, void* d0, void* d1, const int64_t* slots,
+                                 int64_t num_tokens, int64_t num_blocks, int block_size, int n_heads, int width,
+                                 kvc_dtype dtype, cudaStream_t stream) {
+  if (!dtype_ok(dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || n_heads < 1 || width < 1)
+    return fail(KVC_ERR_INVALID_ARG, "sizes must be positive (num_tokens >= 0)");
+  if (num_tokens == 0) return KVC_OK;
+  if (s0 == nullptr || d0 == nullptr || slots == nullptr || (two && (s1 == nullptr || d1 == nullptr)))
+    return fail(KVC_ERR_INVALID_ARG, "NULL pointer");
+  const size_t row_bytes = static_cast<size_t>(width) * dtype_size(dtype);
+  if (row_bytes % 16 != 0) return fail(KVC_ERR_UNSUPPORTED, "row width x element size must be a multiple of 16 bytes");
+  if (!aligned16(s0) || !aligned16(d0) || (s1 && !aligned16(s1)) || (d1 && !aligned16(d1)))
+    return fail(KVC_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  DeviceInfo* dev = nullptr;
+  kvc_status st = current_device(&dev);
+  if (st != KVC_OK) return st;
+  const int row_chunks = static_cast<int>(row_bytes / 16);
+  const int64_t total = num_tokens * n_heads * row_chunks;
+  const int64_t want = (total + 255) / 256;
+  const int grid = static_cast<int>(want < dev->num_sms * 16LL ? want : dev->num_sms * 16LL);
+  append_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(s0), static_cast<const uint4*>(s1),
+                                          static_cast<uint4*>(d0), static_cast<uint4*>(d1), slots, num_tokens,
+                                          num_blocks * block_size, block_size, n_heads, row_chunks,
+                                          dev->error_word);
+  return finish_call(stream);
+}
+
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                      void* v_cache, int64_t num_blocks, int block_size, int n_kv_heads, int head_dim,
+                      kvc_dtype dtype, kvc_stream stream) {
+  kvc::clear_error();
+  return kvc::launch_append(true, k, v, k_cache, v_cache, slot_mapping, num_tokens, num_blocks, block_size, n_kv_heads,
+                            head_dim, dtype, static_cast<cudaStream_t>(stream));
+}
+
+kvc_status kvc_append_latent(const void* c, const int64_t* slot_mapping, int64_t num_tokens, void* latent_cache,
+                             int64_t num_blocks, int block_size, int d_c, int d_r, kvc_dtype dtype,
+                             kvc_stream stream) {
+  kvc::clear_error();
+  if (d_c < 1 || d_r < 0) return kvc::fail(KVC_ERR_INVALID_ARG, "d_c must be >= 1 and d_r >= 0");
+  return kvc::launch_append(false, c, nullptr, latent_cache, nullptr, slot_mapping, num_tokens, num_blocks, block_size,
+                            1, d_c + d_r, dtype, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,196 @@
+// Host side of kvc_decode_attention: argument checks, work planning,
+// workspace carve-up and launch.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "decode_gqa.h"
+
+namespace kvc {
+
+namespace {
+
+constexpr size_t kStageBudget = 100 * 1024;  // shared memory for K/V stages, aims at 2 CTAs per SM
+constexpr int kMaxCtasPerSm = 4;
+constexpr int kMinBlocksPerCta = 2 * kGqaWarps;
+constexpr int kMaxBatch = 4096;
+
+struct GqaPlan {
+  int GH = 1, n_hsub = 1, stages = 2;
+  int64_t units = 0;
+  size_t smem = 0;
+  size_t rec_bytes_per_cta = 0;
+};
+
+int head_subgroup(int group) { return group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1); }
+
+kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, int elt, int max_smem, GqaPlan* pl) {
+  const int group = n_q_heads / n_kv_heads;
+  pl->GH = head_subgroup(group);
+  pl->n_hsub = group / pl->GH;
+  pl->units = static_cast<int64_t>(n_kv_heads) * batch * pl->n_hsub;
+  const size_t stage = 2ull * bs * D * elt;
+  int S = static_cast<int>(kStageBudget / (kGqaWarps * stage));
+  S = std::max(2, std::min(S, 8));
+  GqaSmem L = gqa_smem_layout(elt, D, pl->GH, bs, S, batch);
+  while (S > 2 && L.total > static_cast<size_t>(max_smem)) L = gqa_smem_layout(elt, D, pl->GH, bs, --S, batch);
+  if (L.total > static_cast<size_t>(max_smem))
+    return fail(KVC_ERR_UNSUPPORTED, "block_size %d x head_dim %d needs %zu bytes of shared memory (max %d)", bs, D,
+                L.total, max_smem);
+  pl->stages = S;
+  pl->smem = L.total;
+  pl->rec_bytes_per_cta = 2ull * pl->GH * (D + 2) * sizeof(float);
+  return KVC_OK;
+}
+
+// Number of CTAs for the balanced split: never more than the blocks allow,
+// at most kMaxCtasPerSm per SM unless the caller forced a block count.
+int64_t plan_ctas(const DeviceInfo* dev, int occ, int64_t units, int max_blocks) {
+  const int64_t upper = units * max_blocks;  // upper bound on cache blocks
+  int64_t G;
+  const int64_t forced = option(KVC_OPT_BLOCKS_PER_CTA);
+  if (forced > 0) {
+    G = (upper + forced - 1) / forced;
+  } else {
+    G = static_cast<int64_t>(dev->num_sms) * std::max(1, std::min(occ, kMaxCtasPerSm));
+    G = std::min(G, std::max<int64_t>(1, upper / kMinBlocksPerCta));
+  }
+  const int64_t cap = option(KVC_OPT_MAX_CTAS);
+  if (cap > 0) G = std::min(G, cap);
+  return std::max<int64_t>(1, std::min<int64_t>(G, 1 << 30));
+}
+
+kvc_status check_shapes(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size, int max_blocks) {
+  if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1 || block_size < 1 || max_blocks < 1)
+    return fail(KVC_ERR_INVALID_ARG, "batch, heads, head_dim, block_size and max_blocks_per_seq must be >= 1");
+  if (n_q_heads % n_kv_heads != 0)
+    return fail(KVC_ERR_INVALID_ARG, "n_q_heads (%d) must be a multiple of n_kv_heads (%d)", n_q_heads, n_kv_heads);
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(KVC_ERR_UNSUPPORTED, "head_dim %d (supported: 32, 64, 128, 256)", head_dim);
+  if (block_size % 16 != 0 || block_size > 128)
+    return fail(KVC_ERR_UNSUPPORTED, "block_size %d (supported: multiples of 16 up to 128)", block_size);
+  if (batch > kMaxBatch) return fail(KVC_ERR_UNSUPPORTED, "batch %d > %d", batch, kMaxBatch);
+  if (static_cast<int64_t>(max_blocks) * block_size > (1ll << 30))
+    return fail(KVC_ERR_UNSUPPORTED, "max_blocks_per_seq x block_size too large");
+  return KVC_OK;
+}
+
+template <typename T>
+kvc_status occupancy(const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
+  return gqa_dispatch<T>(p, D, pl.GH, 0, pl.smem, 0, 0, nullptr, 1, occ);
+}
+
+kvc_status occupancy_for(kvc_dtype dt, const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
+  switch (dt) {
+    case KVC_F32: return occupancy<float>(p, D, pl, occ);
+    case KVC_F16: return occupancy<__half>(p, D, pl, occ);
+    case KVC_BF16: return occupancy<__nv_bfloat16>(p, D, pl, occ);
+  }
+  return fail(KVC_ERR_INVALID_ARG, "dtype");
+}
+
+}  // namespace
+
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                     int max_blocks_per_seq, size_t* bytes) {
+  using namespace kvc;
+  clear_error();
+  if (bytes == nullptr) return fail(KVC_ERR_INVALID_ARG, "bytes is NULL");
+  kvc_status s = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq);
+  if (s != KVC_OK) return s;
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != KVC_OK) return s;
+  GqaPlan pl;
+  if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, 2, dev->max_smem_optin, &pl)) != KVC_OK)
+    return s;
+  const int64_t G = plan_ctas(dev, kMaxCtasPerSm, pl.units, max_blocks_per_seq);
+  *bytes = align_up(static_cast<size_t>(G) * pl.rec_bytes_per_cta, 256);
+  return KVC_OK;
+}
+
+kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens, int batch, float scale,
+                                int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
+                                size_t workspace_bytes, kvc_stream stream) {
+  using namespace kvc;
+  clear_error();
+  if (!dtype_ok(dtype) || !dtype_ok(out_dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype");
+  kvc_status s = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq);
+  if (s != KVC_OK) return s;
+  if (num_blocks < 1) return fail(KVC_ERR_INVALID_ARG, "num_blocks must be >= 1");
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_tables == nullptr || context_lens == nullptr ||
+      out == nullptr)
+    return fail(KVC_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(KVC_ERR_INVALID_ARG, "q and caches must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(KVC_ERR_INVALID_ARG, "scale must be finite");
+  if (workspace_bytes > 0 && workspace == nullptr) return fail(KVC_ERR_INVALID_ARG, "workspace is NULL");
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(KVC_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != KVC_OK) return s;
+  const int elt = static_cast<int>(dtype_size(dtype));
+  GqaPlan pl;
+  if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, elt, dev->max_smem_optin, &pl)) != KVC_OK)
+    return s;
+
+  GqaParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.err = dev->error_word;
+  p.num_blocks = num_blocks;
+  p.batch = batch;
+  p.n_q_heads = n_q_heads;
+  p.n_kv_heads = n_kv_heads;
+  p.group = n_q_heads / n_kv_heads;
+  p.n_hsub = pl.n_hsub;
+  p.block_size = block_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.out_dtype = static_cast<int>(out_dtype);
+  p.stages = pl.stages;
+  p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
+
+  int occ = 1;
+  if ((s = occupancy_for(dtype, p, head_dim, pl, &occ)) != KVC_OK) return s;
+  int64_t G = plan_ctas(dev, occ, pl.units, max_blocks_per_seq);
+  G = std::min<int64_t>(G, static_cast<int64_t>(workspace_bytes / pl.rec_bytes_per_cta));
+  int grid, merge_grid;
+  size_t merge_smem = 0;
+  if (G >= 1) {
+    p.unit_mode = 0;
+    p.rec_o = static_cast<float*>(workspace);
+    p.rec_ml = p.rec_o + static_cast<size_t>(G) * 2 * pl.GH * head_dim;
+    grid = static_cast<int>(G);
+    merge_grid = static_cast<int>(pl.units);
+    merge_smem = static_cast<size_t>(batch + 1 + 32) * 4;
+  } else {
+    p.unit_mode = 1;
+    grid = static_cast<int>(pl.units);
+    merge_grid = 0;
+  }
+  if (pl.units > (1ll << 31) - 1) return fail(KVC_ERR_UNSUPPORTED, "too many (sequence, head) units");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (dtype) {
+    case KVC_F32: s = gqa_dispatch<float>(p, head_dim, pl.GH, grid, pl.smem, merge_grid, merge_smem, st, 0, nullptr); break;
+    case KVC_F16: s = gqa_dispatch<__half>(p, head_dim, pl.GH, grid, pl.smem, merge_grid, merge_smem, st, 0, nullptr); break;
+    case KVC_BF16:
+      s = gqa_dispatch<__nv_bfloat16>(p, head_dim, pl.GH, grid, pl.smem, merge_grid, merge_smem, st, 0, nullptr);
+      break;
+  }
+  if (s != KVC_OK) return s;
+  return finish_call(st);
+}
+
+}  // extern "C"

@@ -5,10 +5,11 @@ uniform context lengths, and random physical block assignments. Nothing here
 computes attention, slots or byte counts; the library and the oracle each do
 that themselves from these inputs.
 
-Every tensor is produced on the CPU from a ``torch.Generator`` seeded with
-the given seed, as float32 N(0, 1) and then rounded to the storage dtype, so
-the library (after a copy to the device) and the oracle (after a widening to
-float64) see the same values.
+Every tensor is produced from a ``torch.Generator`` seeded with the given
+seed, as float32 N(0, 1) and then rounded to the storage dtype, so the library
+(after a copy to the device) and the oracle (after a widening to float64) see
+the same values. Parity tests draw on the CPU; the benchmark may draw the large
+value tensors on the GPU (``device="cuda"``) where they are needed anyway.
 """
 
 from __future__ import annotations
@@ -18,17 +19,29 @@ import torch
 DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
-def _gen(seed: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def _gen(seed: int, device: str = "cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     return g
 
 
 def normal(shape, dtype: str, gen: torch.Generator) -> torch.Tensor:
-    return torch.randn(*shape, generator=gen, dtype=torch.float32).to(DTYPES[dtype])
+    """N(0, 1) drawn as float32 on the generator's device, rounded to ``dtype``.
+
+    Large tensors are drawn in slices so the float32 staging copy stays small.
+    """
+    dev = gen.device
+    out = torch.empty(*shape, dtype=DTYPES[dtype], device=dev)
+    flat = out.view(-1)
+    step = 1 << 26
+    for a in range(0, flat.numel(), step):
+        b = min(flat.numel(), a + step)
+        flat[a:b] = torch.randn(b - a, generator=gen, dtype=torch.float32, device=dev).to(DTYPES[dtype])
+    return out
 
 
 def uniform_lengths(batch: int, lo: int, hi: int, gen: torch.Generator) -> torch.Tensor:
+    # lengths are always drawn on the CPU so a case has the same structure on every device
     return torch.randint(lo, hi + 1, (batch,), generator=gen, dtype=torch.int64).to(torch.int32)
 
 
@@ -89,14 +102,17 @@ def shared_prefix_block_tables(n_prompts: int, fanout: int, prompt_len: int, pri
 
 
 def gqa_case(batch, n_q_heads, n_kv_heads, head_dim, block_size, lens, dtype, seed,
-             spare_frac=0.10, permute=True):
+             spare_frac=0.10, permute=True, device="cpu"):
     """A paged GQA/MHA/MQA decode step.
 
     ``lens`` is a list of context lengths (each including the new token) or a
     (lo, hi) tuple for uniform random lengths. Draw order (fixed): lengths,
-    table permutation, K pool, V pool, q, new k, new v.
+    table permutation, K pool, V pool, q, new k, new v. Lengths and tables
+    always come from a CPU generator; values from a generator on ``device``
+    (the same seed gives different values on "cpu" and "cuda").
     """
     g = _gen(seed)
+    gv = g if device == "cpu" else _gen(seed, device)
     if isinstance(lens, tuple):
         lens_t = uniform_lengths(batch, lens[0], lens[1], g)
     else:
@@ -107,19 +123,21 @@ def gqa_case(batch, n_q_heads, n_kv_heads, head_dim, block_size, lens, dtype, se
         "context_lens": lens_t,
         "block_tables": table,
         "num_blocks": num_blocks,
-        "k_cache": normal(shape, dtype, g),
-        "v_cache": normal(shape, dtype, g),
-        "q": normal((batch, n_q_heads, head_dim), dtype, g),
-        "k_new": normal((batch, n_kv_heads, head_dim), dtype, g),
-        "v_new": normal((batch, n_kv_heads, head_dim), dtype, g),
+        "k_cache": normal(shape, dtype, gv),
+        "v_cache": normal(shape, dtype, gv),
+        "q": normal((batch, n_q_heads, head_dim), dtype, gv),
+        "k_new": normal((batch, n_kv_heads, head_dim), dtype, gv),
+        "v_new": normal((batch, n_kv_heads, head_dim), dtype, gv),
         "dtype": dtype,
         "block_size": block_size,
     }
 
 
-def shared_case(n_prompts, fanout, prompt_len, private_len, n_heads, head_dim, block_size, dtype, seed):
+def shared_case(n_prompts, fanout, prompt_len, private_len, n_heads, head_dim, block_size, dtype, seed,
+                device="cpu"):
     """MHA decode step where groups of sequences share their prompt blocks."""
     g = _gen(seed)
+    gv = g if device == "cpu" else _gen(seed, device)
     table, lens, num_blocks = shared_prefix_block_tables(n_prompts, fanout, prompt_len, private_len,
                                                          block_size, g)
     B = n_prompts * fanout
@@ -128,19 +146,20 @@ def shared_case(n_prompts, fanout, prompt_len, private_len, n_heads, head_dim, b
         "context_lens": lens,
         "block_tables": table,
         "num_blocks": num_blocks,
-        "k_cache": normal(shape, dtype, g),
-        "v_cache": normal(shape, dtype, g),
-        "q": normal((B, n_heads, head_dim), dtype, g),
-        "k_new": normal((B, n_heads, head_dim), dtype, g),
-        "v_new": normal((B, n_heads, head_dim), dtype, g),
+        "k_cache": normal(shape, dtype, gv),
+        "v_cache": normal(shape, dtype, gv),
+        "q": normal((B, n_heads, head_dim), dtype, gv),
+        "k_new": normal((B, n_heads, head_dim), dtype, gv),
+        "v_new": normal((B, n_heads, head_dim), dtype, gv),
         "dtype": dtype,
         "block_size": block_size,
     }
 
 
-def mla_case(batch, n_heads, d_c, d_r, block_size, lens, dtype, seed, spare_frac=0.10):
+def mla_case(batch, n_heads, d_c, d_r, block_size, lens, dtype, seed, spare_frac=0.10, device="cpu"):
     """An MLA absorbed decode step over a paged latent cache [num_blocks, bs, d_c + d_r]."""
     g = _gen(seed)
+    gv = g if device == "cpu" else _gen(seed, device)
     if isinstance(lens, tuple):
         lens_t = uniform_lengths(batch, lens[0], lens[1], g)
     else:
@@ -151,9 +170,9 @@ def mla_case(batch, n_heads, d_c, d_r, block_size, lens, dtype, seed, spare_frac
         "context_lens": lens_t,
         "block_tables": table,
         "num_blocks": num_blocks,
-        "latent_cache": normal((num_blocks, block_size, W), dtype, g),
-        "q": normal((batch, n_heads, W), dtype, g),
-        "c_new": normal((batch, W), dtype, g),
+        "latent_cache": normal((num_blocks, block_size, W), dtype, gv),
+        "q": normal((batch, n_heads, W), dtype, gv),
+        "c_new": normal((batch, W), dtype, gv),
         "dtype": dtype,
         "block_size": block_size,
     }

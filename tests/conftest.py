@@ -17,3 +17,13 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+@pytest.fixture(scope="session")
+def kvc():
+    """The product binding with libkvc.so built in place (nvcc cross-compiles without a GPU)."""
+    from paged_kv_cache_157_gb300 import build_lib
+    build_lib.build()
+    import paged_kv_cache_157_gb300 as k
+    k.raw()
+    return k

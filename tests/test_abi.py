@@ -1,0 +1,72 @@
+"""The C ABI library loads and exports every symbol include/kvc.h declares (no GPU needed)."""
+
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "kvc.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding(kvc):
+    assert declared_functions() == kvc.symbols()
+
+
+def test_library_exports_every_declared_symbol(kvc):
+    out = subprocess.run(["nm", "-D", "--defined-only", kvc.lib_path()], capture_output=True, text=True, check=True)
+    exported = set(re.findall(r"\b(kvc_[a-z0-9_]+)\b", out.stdout))
+    missing = [s for s in declared_functions() if s not in exported]
+    assert not missing, missing
+    lib = kvc.raw()
+    for s in declared_functions():
+        assert getattr(lib, s) is not None
+
+
+def test_status_strings_and_version(kvc):
+    lib = kvc.raw()
+    assert lib.kvc_abi_version() == 1
+    assert lib.kvc_status_string(0) == b"KVC_OK"
+    assert lib.kvc_status_string(3) == b"KVC_ERR_NO_BLOCKS"
+    assert lib.kvc_status_string(99) == b"KVC_ERR_UNKNOWN"
+
+
+def test_options_roundtrip(kvc):
+    kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, 7)
+    assert kvc.get_option(kvc.OPT_BLOCKS_PER_CTA) == 7
+    kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, 0)
+    with pytest.raises(kvc.KvcError):
+        kvc.set_option(kvc.OPT_CHECKED, 2)
+    with pytest.raises(kvc.KvcError):
+        kvc.set_option(9, 1)
+
+
+def test_host_validation_before_any_device_work(kvc):
+    import ctypes
+    lib = kvc.raw()
+    z = ctypes.c_void_p(0)
+    # n_q_heads not a multiple of n_kv_heads
+    s = lib.kvc_decode_attention(z, z, z, z, 4, z, 2, 0.1, 6, 4, 128, 16, 10, 2, z, 0, z, 0, z)
+    assert s == kvc.ERR_INVALID_ARG
+    assert b"multiple" in lib.kvc_last_error_message()
+    # unsupported head_dim
+    assert lib.kvc_decode_attention(z, z, z, z, 4, z, 2, 0.1, 8, 4, 96, 16, 10, 2, z, 0, z, 0, z) == kvc.ERR_UNSUPPORTED
+    # block size not a multiple of 16
+    assert lib.kvc_decode_attention(z, z, z, z, 4, z, 2, 0.1, 8, 4, 128, 8, 10, 2, z, 0, z, 0, z) == kvc.ERR_UNSUPPORTED
+    # empty batch
+    assert lib.kvc_decode_attention(z, z, z, z, 4, z, 0, 0.1, 8, 4, 128, 16, 10, 2, z, 0, z, 0, z) == kvc.ERR_INVALID_ARG
+    # append of zero tokens is a no-op that succeeds without touching the device
+    assert lib.kvc_append(z, z, z, 0, z, z, 10, 16, 8, 128, 2, z) == kvc.OK
+    # bad dtype
+    assert lib.kvc_append(z, z, z, 1, z, z, 10, 16, 8, 128, 7, z) == kvc.ERR_INVALID_ARG
+    # workspace query validates shapes too
+    n = ctypes.c_size_t()
+    assert lib.kvc_decode_workspace_size(2, 6, 4, 128, 16, 4, ctypes.byref(n)) == kvc.ERR_INVALID_ARG
