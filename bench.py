@@ -153,8 +153,8 @@ class GqaStep:
         self.slots = kvc.slots_from_tables(case["block_tables"], self.bs, list(range(self.B)),
                                            [n - 1 for n in lens]).cuda()
         self.out = torch.empty((self.B, self.hq, self.d), dtype=out_dtype, device="cuda")
-        n = kvc.decode_workspace_size(self.B, self.hq, self.hkv, self.d, self.bs, case["block_tables"].shape[1])
-        self.ws = torch.empty(max(1, n), dtype=torch.uint8, device="cuda")
+        self.ws = kvc.new_decode_workspace(self.B, self.hq, self.hkv, self.d, self.bs,
+                                           case["block_tables"].shape[1])
         self.scale = 1.0 / math.sqrt(self.d)
 
     def append(self):
@@ -207,7 +207,7 @@ def time_e2e(kvc, step, steps, warmup, flush):
     inputs (q, new k/v, slots, tables, lengths), append, decode, D2H of the output."""
     import torch
     c = step.case
-    host = {k: c[k].pin_memory() for k in ("q", "k_new", "v_new", "block_tables", "context_lens")}
+    host = {k: c[k].detach().to("cpu").pin_memory() for k in ("q", "k_new", "v_new", "block_tables", "context_lens")}
     host["slots"] = step.slots.cpu().pin_memory()
     out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     dev = step.dev

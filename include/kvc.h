@@ -74,6 +74,7 @@ typedef enum kvc_dtype { KVC_F32 = 0, KVC_F16 = 1, KVC_BF16 = 2 } kvc_dtype;
 #define KVC_FLAG_BAD_LEN 0x2u     /* context_len < 1 or > max_blocks_per_seq*block_size */
 #define KVC_FLAG_BAD_SLOT 0x4u    /* slot >= num_blocks*block_size */
 #define KVC_FLAG_TIMEOUT 0x8u     /* a bounded wait on an async copy gave up */
+#define KVC_FLAG_WORKSPACE 0x10u  /* decode workspace counters were not zero at entry */
 
 typedef void* kvc_stream; /* cudaStream_t */
 
@@ -144,10 +145,14 @@ kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, i
  * Supported: head_dim in {32, 64, 128, 256}; block_size a multiple of 16 up
  * to 128; n_q_heads % n_kv_heads == 0; batch <= 4096.
  * workspace: device scratch of at least kvc_decode_workspace_size() bytes,
- * 256-byte aligned, no initial contents required; may be NULL with
- * workspace_bytes 0 (then every (sequence, head group) is handled by one
- * CTA, which balances less well on long contexts). The workspace must not
- * be shared by calls that may run concurrently.
+ * 256-byte aligned. It must be zero-filled once before its first use (for
+ * example cudaMemset after allocation); every complete call leaves it zeroed
+ * again (it holds split-K partial results and one counter per (sequence,
+ * head group) that the kernel resets). If a call finds a counter that was not
+ * zero it sets KVC_FLAG_WORKSPACE and the affected outputs are not written:
+ * zero the workspace again. May be NULL with workspace_bytes 0 (then every
+ * (sequence, head group) is handled by one CTA, which balances less well on
+ * long contexts). Calls that may run concurrently must not share a workspace.
  * Sources: knowledge point 2 of "KV缓存原理与显存估算"; head grouping from
  * "KV-Cache——为什么AI回复越来越快" section 03 and llm-compass 2.2. */
 kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* v_cache,

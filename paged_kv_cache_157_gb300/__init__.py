@@ -21,7 +21,8 @@ __all__ = [
     "append", "append_latent", "decode_workspace_size", "decode_attention",
     "decode_mla_workspace_size", "decode_attention_mla", "set_option", "get_option",
     "get_error_flags", "BlockPool", "slots_from_tables",
-    "F32", "F16", "BF16", "FLAG_BAD_BLOCK", "FLAG_BAD_LEN", "FLAG_BAD_SLOT", "FLAG_TIMEOUT",
+    "F32", "F16", "BF16", "FLAG_BAD_BLOCK", "FLAG_BAD_LEN", "FLAG_BAD_SLOT", "FLAG_TIMEOUT", "FLAG_WORKSPACE",
+    "new_decode_workspace",
     "OPT_CHECKED", "OPT_BLOCKS_PER_CTA", "OPT_MAX_CTAS",
 ]
 
@@ -30,7 +31,7 @@ _LIB_PATH = os.path.join(_HERE, "libkvc.so")
 
 F32, F16, BF16 = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_BLOCKS, ERR_CUDA, ERR_OUT_OF_RANGE, ERR_WORKSPACE = range(7)
-FLAG_BAD_BLOCK, FLAG_BAD_LEN, FLAG_BAD_SLOT, FLAG_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+FLAG_BAD_BLOCK, FLAG_BAD_LEN, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLAG_WORKSPACE = 0x1, 0x2, 0x4, 0x8, 0x10
 OPT_CHECKED, OPT_BLOCKS_PER_CTA, OPT_MAX_CTAS = 0, 1, 2
 
 # Every exported symbol of include/kvc.h with (restype, argtypes).
@@ -209,9 +210,17 @@ def decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, block_size, ma
     return n.value
 
 
+def new_decode_workspace(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, device="cuda"):
+    """Zero-filled uint8 workspace of the size kvc_decode_workspace_size asks for."""
+    torch = _torch()
+    n = decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq)
+    return torch.zeros(max(n, 1), dtype=torch.uint8, device=device)
+
+
 def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace=None, stream=None):
     """kvc_decode_attention. q/out [B, Hq, D]; caches [num_blocks, Hkv, bs, D];
-    block_tables int32 [B, max_blocks]; context_lens int32 [B]; workspace uint8 tensor or None."""
+    block_tables int32 [B, max_blocks]; context_lens int32 [B]; workspace: a zero-filled uint8 tensor
+    (see new_decode_workspace) that later calls keep zeroed, or None."""
     torch = _torch()
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
         _require(t, n)

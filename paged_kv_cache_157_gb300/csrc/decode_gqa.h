@@ -20,6 +20,7 @@ struct GqaParams {
   void* out;
   float* rec_o;   // [G*2, GH, D] partial outputs (stream mode)
   float* rec_ml;  // [G*2, GH, 2] (max in log2 units, sum)
+  unsigned int* counters;  // [units] records seen per split unit; zero between calls
   unsigned int* err;
   int64_t num_blocks;
   int batch;
@@ -59,7 +60,7 @@ __host__ __device__ inline GqaSmem gqa_smem_layout(int elt_bytes, int D, int GH,
 }
 
 template <typename T>
-kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, int merge_grid,
-                        size_t merge_smem, cudaStream_t stream, int mode, int* occ);
+kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
+                        int* occ);
 
 }  // namespace kvc

@@ -24,6 +24,9 @@ struct GqaPlan {
   size_t rec_bytes_per_cta = 0;
 };
 
+// Workspace layout: [unit counters][record outputs][record (max, sum)].
+size_t counter_bytes(const GqaPlan& pl) { return align_up(static_cast<size_t>(pl.units) * 4, 256); }
+
 int head_subgroup(int group) { return group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1); }
 
 kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, int elt, int max_smem, GqaPlan* pl) {
@@ -33,9 +36,9 @@ kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, in
   pl->units = static_cast<int64_t>(n_kv_heads) * batch * pl->n_hsub;
   const size_t stage = 2ull * bs * D * elt;
   int S = static_cast<int>(kStageBudget / (kGqaWarps * stage));
-  S = std::max(2, std::min(S, 8));
+  S = std::max(1, std::min(S, 8));
   GqaSmem L = gqa_smem_layout(elt, D, pl->GH, bs, S, batch);
-  while (S > 2 && L.total > static_cast<size_t>(max_smem)) L = gqa_smem_layout(elt, D, pl->GH, bs, --S, batch);
+  while (S > 1 && L.total > static_cast<size_t>(max_smem)) L = gqa_smem_layout(elt, D, pl->GH, bs, --S, batch);
   if (L.total > static_cast<size_t>(max_smem))
     return fail(KVC_ERR_UNSUPPORTED, "block_size %d x head_dim %d needs %zu bytes of shared memory (max %d)", bs, D,
                 L.total, max_smem);
@@ -79,7 +82,7 @@ kvc_status check_shapes(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
 
 template <typename T>
 kvc_status occupancy(const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
-  return gqa_dispatch<T>(p, D, pl.GH, 0, pl.smem, 0, 0, nullptr, 1, occ);
+  return gqa_dispatch<T>(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ);
 }
 
 kvc_status occupancy_for(kvc_dtype dt, const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
@@ -110,7 +113,7 @@ kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, i
   if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, 2, dev->max_smem_optin, &pl)) != KVC_OK)
     return s;
   const int64_t G = plan_ctas(dev, kMaxCtasPerSm, pl.units, max_blocks_per_seq);
-  *bytes = align_up(static_cast<size_t>(G) * pl.rec_bytes_per_cta, 256);
+  *bytes = align_up(counter_bytes(pl) + static_cast<size_t>(G) * pl.rec_bytes_per_cta, 256);
   return KVC_OK;
 }
 
@@ -165,29 +168,27 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
   int occ = 1;
   if ((s = occupancy_for(dtype, p, head_dim, pl, &occ)) != KVC_OK) return s;
   int64_t G = plan_ctas(dev, occ, pl.units, max_blocks_per_seq);
-  G = std::min<int64_t>(G, static_cast<int64_t>(workspace_bytes / pl.rec_bytes_per_cta));
-  int grid, merge_grid;
-  size_t merge_smem = 0;
+  const size_t cbytes = counter_bytes(pl);
+  G = std::min<int64_t>(G, workspace_bytes > cbytes
+                               ? static_cast<int64_t>((workspace_bytes - cbytes) / pl.rec_bytes_per_cta)
+                               : 0);
+  int grid;
   if (G >= 1) {
     p.unit_mode = 0;
-    p.rec_o = static_cast<float*>(workspace);
+    p.counters = static_cast<unsigned int*>(workspace);
+    p.rec_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + cbytes);
     p.rec_ml = p.rec_o + static_cast<size_t>(G) * 2 * pl.GH * head_dim;
     grid = static_cast<int>(G);
-    merge_grid = static_cast<int>(pl.units);
-    merge_smem = static_cast<size_t>(batch + 1 + 32) * 4;
   } else {
     p.unit_mode = 1;
     grid = static_cast<int>(pl.units);
-    merge_grid = 0;
   }
   if (pl.units > (1ll << 31) - 1) return fail(KVC_ERR_UNSUPPORTED, "too many (sequence, head) units");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (dtype) {
-    case KVC_F32: s = gqa_dispatch<float>(p, head_dim, pl.GH, grid, pl.smem, merge_grid, merge_smem, st, 0, nullptr); break;
-    case KVC_F16: s = gqa_dispatch<__half>(p, head_dim, pl.GH, grid, pl.smem, merge_grid, merge_smem, st, 0, nullptr); break;
-    case KVC_BF16:
-      s = gqa_dispatch<__nv_bfloat16>(p, head_dim, pl.GH, grid, pl.smem, merge_grid, merge_smem, st, 0, nullptr);
-      break;
+    case KVC_F32: s = gqa_dispatch<float>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr); break;
+    case KVC_F16: s = gqa_dispatch<__half>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr); break;
+    case KVC_BF16: s = gqa_dispatch<__nv_bfloat16>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr); break;
   }
   if (s != KVC_OK) return s;
   return finish_call(st);

@@ -12,18 +12,22 @@
 // * Balanced split: the cache blocks of all units are laid end to end
 //   (kv head major, then sequence, then subgroup, so units that read the
 //   same pages sit next to each other) and CTA c takes blocks
-//   [c*N/G, (c+1)*N/G). A CTA finishes whole units itself and leaves at most
-//   two partial results (its first and last segment) as fp32 records; the
-//   merge kernel combines records with the log-sum-exp rule.
+//   [c*N/G, (c+1)*N/G). A CTA finishes whole units itself. A unit cut by a
+//   range boundary leaves one fp32 record (max, sum, unnormalised output) per
+//   CTA that touched it; the last of those CTAs to finish (a counter per unit
+//   in the workspace, reset to zero by that CTA) merges the records with the
+//   log-sum-exp rule. No CTA ever waits for another.
 // * Each warp streams its own pages: lane 0 issues 1-D bulk copies (TMA) of
 //   the K page and V page of a block into a per-warp ring of shared-memory
 //   stages, completion counted on an mbarrier; every wait is bounded.
 // * Per 16-row tile a lane owns 16 (or 8) head dimensions of TL-strided rows.
-//   Partial dot products are reduced across the lanes of a row with a
-//   reduce-scatter (each lane ends holding whole scores of one head), softmax
-//   runs online in the log2 domain with a lazy rescale (the reference maximum
-//   moves only when a score exceeds it by more than 8, i.e. a factor 256), and
-//   the weights are gathered back for the V accumulation in fp32.
+//   Products use the packed fp32x2 FMA of sm_100+ (two fp32 lanes per
+//   instruction, an IEEE fma in each). Partial dot products are reduced across
+//   the lanes of a row with a reduce-scatter (each lane ends holding whole
+//   scores of one head), softmax runs online in the log2 domain with a lazy
+//   rescale (the reference maximum moves only when a score exceeds it by more
+//   than 8, i.e. a factor 256), and the weights are gathered back for the V
+//   accumulation in fp32.
 #pragma once
 
 #include "decode_gqa.h"
@@ -35,6 +39,7 @@ template <typename T, int D, int GH>
 struct GqaCfg {
   static constexpr int NW = kGqaWarps;
   static constexpr int DPL = (D >= 64) ? 16 : 8;  // dims per lane
+  static constexpr int DP2 = DPL / 2;               // fp32 pairs per lane
   static constexpr int DL = D / DPL;                // lanes per row
   static constexpr int TL = 32 / DL;                // row groups per warp
   static constexpr int RT = 16 / TL;                // rows per lane per 16-row tile
@@ -71,7 +76,6 @@ __device__ inline void scan_blocks(const int32_t* lens, int B, int bs, int max_b
   const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
   int local = 0;
   for (int b = b0; b < b1; ++b) local += seq_blocks(lens, b, bs, max_blocks);
-  // inclusive warp scan of per-thread sums
   const int lane = tid & 31, wid = tid >> 5;
   int v = local;
 #pragma unroll
@@ -135,18 +139,25 @@ struct ReduceScatter {
 template <typename T, int D, int GH>
 struct WarpState {
   using C = GqaCfg<T, D, GH>;
-  float q[GH][C::DPL];
-  float o[GH][C::DPL];
-  float m[GH];
-  float l;  // partial sum of this lane's weights (head h_lane)
+  float2 q[GH][C::DP2];  // query, pre-scaled by scale*log2(e)
+  float2 o[GH][C::DP2];  // unnormalised output relative to m
+  float m[GH];           // reference maximum (log2 units), warp-uniform
+  float l;               // partial sum of this lane's weights (head h_lane)
 };
 
-template <typename T, int D, int GH>
+template <int GH>
 __device__ __forceinline__ float select_head(const float (&v)[GH], int h) {
   float r = v[0];
 #pragma unroll
   for (int i = 1; i < GH; ++i) r = (h == i) ? v[i] : r;
   return r;
+}
+
+template <typename T, int NCH, int DL, int VEC>
+__device__ __forceinline__ void load_pairs(const T* rp, int dq, float2* f) {
+#pragma unroll
+  for (int j = 0; j < NCH; ++j)
+    Elem<T>::unpack(lds128(rp + (dq + DL * j) * VEC), reinterpret_cast<float*>(f) + j * VEC);
 }
 
 // One 16-row tile of a page: scores, online softmax, V accumulation.
@@ -157,23 +168,21 @@ __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __re
   float s[C::NV];
 #pragma unroll
   for (int r = 0; r < C::RT; ++r) {
-    const T* rp = kp + (r * C::TL + tq) * D;
-    float kf[C::DPL];
-#pragma unroll
-    for (int j = 0; j < C::NCH; ++j) Elem<T>::unpack(lds128(rp + (dq + C::DL * j) * C::VEC), kf + j * C::VEC);
+    float2 kf[C::DP2];
+    load_pairs<T, C::NCH, C::DL, C::VEC>(kp + (r * C::TL + tq) * D, dq, kf);
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
-      float acc = 0.f;
+      float2 acc = fmul2(st.q[h][0], kf[0]);
 #pragma unroll
-      for (int e = 0; e < C::DPL; ++e) acc = fmaf(st.q[h][e], kf[e], acc);
-      s[h * C::RT + r] = acc;
+      for (int i = 1; i < C::DP2; ++i) acc = ffma2(st.q[h][i], kf[i], acc);
+      s[h * C::RT + r] = acc.x + acc.y;
     }
   }
   ReduceScatter<C::NV, C::DL / 2>::run(s, dq);
 
   // Score k of this lane has value index i = h*RT + r.
   const int base_i = C::NV >= C::DL ? C::NVF * dq : dq / C::DUP;
-  float m_l = select_head<T, D, GH>(st.m, h_lane);
+  float m_l = select_head<GH>(st.m, h_lane);
   bool need = false;
 #pragma unroll
   for (int k = 0; k < C::NVF; ++k) {
@@ -192,12 +201,13 @@ __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __re
       const float tmax = warp_max(h_lane == hh ? loc : kNegInf);
       const float mn = fmaxf(st.m[hh], tmax);
       const float alpha = fast_exp2(st.m[hh] - mn);
+      const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-      for (int e = 0; e < C::DPL; ++e) st.o[hh][e] *= alpha;
+      for (int i = 0; i < C::DP2; ++i) st.o[hh][i] = fmul2(st.o[hh][i], a2);
       if (h_lane == hh) st.l *= alpha;
       st.m[hh] = mn;
     }
-    m_l = select_head<T, D, GH>(st.m, h_lane);
+    m_l = select_head<GH>(st.m, h_lane);
   }
   float p[C::NVF];
 #pragma unroll
@@ -215,19 +225,75 @@ __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __re
   }
 #pragma unroll
   for (int r = 0; r < C::RT; ++r) {
-    const T* rp = vp + (r * C::TL + tq) * D;
-    float vf[C::DPL];
-#pragma unroll
-    for (int j = 0; j < C::NCH; ++j) Elem<T>::unpack(lds128(rp + (dq + C::DL * j) * C::VEC), vf + j * C::VEC);
+    float2 vf[C::DP2];
+    load_pairs<T, C::NCH, C::DL, C::VEC>(vp + (r * C::TL + tq) * D, dq, vf);
     if (PARTIAL && r * C::TL + tq >= valid) {
 #pragma unroll
-      for (int e = 0; e < C::DPL; ++e) vf[e] = 0.f;
+      for (int i = 0; i < C::DP2; ++i) vf[i] = make_float2(0.f, 0.f);
     }
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
+      const float2 pp = make_float2(pa[h * C::RT + r], pa[h * C::RT + r]);
 #pragma unroll
-      for (int e = 0; e < C::DPL; ++e) st.o[h][e] = fmaf(pa[h * C::RT + r], vf[e], st.o[h][e]);
+      for (int i = 0; i < C::DP2; ++i) st.o[h][i] = ffma2(pp, vf[i], st.o[h][i]);
     }
+  }
+}
+
+// Merges the records that CTAs c0..c1 left for one unit (blocks starting at
+// global index u0) and writes the normalised output. Record ids are staged in
+// s_rec in chunks of `cap` CTAs; pass 0 finds the maxima, pass 1 sums.
+template <int GH>
+__device__ void merge_records(const GqaParams& p, int D, int64_t u0, int64_t c0, int64_t c1, int64_t G, int64_t N,
+                              int seq, int h0, int* s_rec, int cap) {
+  constexpr int kMaxOwned = 8;  // GH * D <= 8 * blockDim for GH <= 4, D <= 256, 128 threads
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int span = static_cast<int>(c1 - c0 + 1);
+  float M[GH];
+#pragma unroll
+  for (int h = 0; h < GH; ++h) M[h] = kNegInf;
+  float O[kMaxOwned], Ls[kMaxOwned];
+#pragma unroll
+  for (int k = 0; k < kMaxOwned; ++k) O[k] = Ls[k] = 0.f;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int base = 0; base < span; base += cap) {
+      const int n = min(cap, span - base);
+      __syncthreads();
+      for (int t = tid; t < n; t += nt) {
+        const int64_t c = c0 + base + t;
+        const int64_t f0 = cta_range_start(c, G, N);
+        const int64_t f1 = cta_range_start(c + 1, G, N);
+        s_rec[t] = (f0 == f1) ? -1 : static_cast<int>(c * 2 + ((u0 > f0) ? 1 : 0));
+      }
+      __syncthreads();
+      for (int t = 0; t < n; ++t) {
+        const int64_t rec = s_rec[t];
+        if (rec < 0) continue;
+        if (pass == 0) {
+#pragma unroll
+          for (int h = 0; h < GH; ++h) M[h] = fmaxf(M[h], __ldcg(p.rec_ml + (rec * GH + h) * 2));
+        } else {
+#pragma unroll
+          for (int k = 0; k < kMaxOwned; ++k) {
+            const int idx = tid + k * nt;
+            if (idx >= GH * D) break;
+            const int h = idx / D, d = idx - (idx / D) * D;
+            const float mc = __ldcg(p.rec_ml + (rec * GH + h) * 2);
+            if (mc == kNegInf) continue;
+            const float f = fast_exp2(mc - select_head<GH>(M, h));
+            Ls[k] += f * __ldcg(p.rec_ml + (rec * GH + h) * 2 + 1);
+            O[k] += f * __ldcg(p.rec_o + (rec * GH + h) * D + d);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kMaxOwned; ++k) {
+    const int idx = tid + k * nt;
+    if (idx >= GH * D) break;
+    const int h = idx / D, d = idx - (idx / D) * D;
+    store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + h0 + h) * D + d, O[k] / Ls[k], p.out_dtype);
   }
 }
 
@@ -241,6 +307,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
   float* s_o = reinterpret_cast<float*>(smem + L.o_off);
   float* s_ml = reinterpret_cast<float*>(smem + L.ml_off);
   int* s_scan = reinterpret_cast<int*>(smem + L.scan_off);
+  __shared__ int s_last;
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int tq = lane / C::DL, dq = lane % C::DL;
@@ -259,6 +326,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
 
   // Block range of this CTA.
   int64_t lo, hi, slab = 0, N = 0;
+  const int64_t G = gridDim.x;
   if (p.unit_mode) {
     lo = 0;
     hi = 1;
@@ -267,17 +335,22 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
     scan_blocks(p.context_lens, B, bs, p.max_blocks, s_scan);
     slab = static_cast<int64_t>(p.n_hsub) * s_scan[B];
     N = slab * p.n_kv_heads;
-    lo = cta_range_start(blockIdx.x, gridDim.x, N);
-    hi = cta_range_start(blockIdx.x + 1, gridDim.x, N);
+    lo = cta_range_start(blockIdx.x, G, N);
+    hi = cta_range_start(blockIdx.x + 1, G, N);
   }
-  if (blockIdx.x == 0 && tid < B) {
-    const int n = __ldg(p.context_lens + tid);
-    if (n < 1 || n > bs * p.max_blocks) set_flag(p.err, 0x2u);
-  }
-  if (blockIdx.x == 0 && tid == 0) {
-    for (int b = kGqaWarps * 32; b < B; ++b) {
+  if (blockIdx.x == 0) {
+    // Validate every length once; in the split mode CTA 0 also writes the
+    // zero outputs of sequences whose length is invalid (no CTA visits them).
+    for (int b = tid; b < B; b += blockDim.x) {
       const int n = __ldg(p.context_lens + b);
       if (n < 1 || n > bs * p.max_blocks) set_flag(p.err, 0x2u);
+    }
+    if (!p.unit_mode) {
+      for (int b = 0; b < B; ++b) {
+        if (__ldg(p.context_lens + b) >= 1) continue;
+        for (int idx = tid; idx < p.n_q_heads * D; idx += blockDim.x)
+          store_out(p.out, static_cast<int64_t>(b) * p.n_q_heads * D + idx, 0.f, p.out_dtype);
+      }
     }
   }
 
@@ -296,7 +369,6 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
       nb = seq_blocks(p.context_lens, seq, bs, p.max_blocks);
       j0 = 0;
       seg_len = nb;
-      gb = hi;
     } else {
       kvh = static_cast<int>(gb / slab);
       const int64_t r = gb - kvh * slab;
@@ -315,7 +387,8 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
     }
     const bool whole = (j0 == 0 && seg_len == nb);
     const int which = (gb == lo) ? 0 : 1;
-    if (!p.unit_mode) gb += seg_len;
+    const int64_t u0 = gb - j0;  // global index of the unit's first block (split mode)
+    gb = p.unit_mode ? hi : gb + seg_len;
     const int h0 = kvh * p.group + hsub * GH;
     const int n_rows = seq_rows(p.context_lens, seq, bs, p.max_blocks);
 
@@ -333,16 +406,16 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
       const T* qp = static_cast<const T*>(p.q) + (static_cast<int64_t>(seq) * p.n_q_heads + h0) * D;
 #pragma unroll
       for (int h = 0; h < GH; ++h) {
+        float f[C::DPL];
 #pragma unroll
-        for (int j = 0; j < C::NCH; ++j) {
-          const uint4 u = __ldg(reinterpret_cast<const uint4*>(qp + h * D + (dq + C::DL * j) * C::VEC));
-          float f[C::VEC];
-          Elem<T>::unpack(u, f);
+        for (int j = 0; j < C::NCH; ++j)
+          Elem<T>::unpack(__ldg(reinterpret_cast<const uint4*>(qp + h * D + (dq + C::DL * j) * C::VEC)),
+                          f + j * C::VEC);
 #pragma unroll
-          for (int e = 0; e < C::VEC; ++e) st.q[h][j * C::VEC + e] = f[e] * p.qscale;
+        for (int i = 0; i < C::DP2; ++i) {
+          st.q[h][i] = make_float2(f[2 * i] * p.qscale, f[2 * i + 1] * p.qscale);
+          st.o[h][i] = make_float2(0.f, 0.f);
         }
-#pragma unroll
-        for (int e = 0; e < C::DPL; ++e) st.o[h][e] = 0.f;
         st.m[h] = kNegInf;
       }
       st.l = 0.f;
@@ -422,7 +495,10 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
 #pragma unroll
       for (int h = 0; h < GH; ++h) {
 #pragma unroll
-        for (int e = 0; e < C::DPL; ++e) st.o[h][e] += __shfl_xor_sync(0xffffffffu, st.o[h][e], msk);
+        for (int i = 0; i < C::DP2; ++i) {
+          st.o[h][i].x += __shfl_xor_sync(0xffffffffu, st.o[h][i].x, msk);
+          st.o[h][i].y += __shfl_xor_sync(0xffffffffu, st.o[h][i].y, msk);
+        }
       }
     }
     float lw[GH];
@@ -434,8 +510,11 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
 #pragma unroll
         for (int j = 0; j < C::NCH; ++j) {
 #pragma unroll
-          for (int e = 0; e < C::VEC; ++e)
-            s_o[(w * GH + h) * D + (dq + C::DL * j) * C::VEC + e] = st.o[h][j * C::VEC + e];
+          for (int e = 0; e < C::VEC; e += 2) {
+            const float2 v = st.o[h][(j * C::VEC + e) / 2];
+            s_o[(w * GH + h) * D + (dq + C::DL * j) * C::VEC + e] = v.x;
+            s_o[(w * GH + h) * D + (dq + C::DL * j) * C::VEC + e + 1] = v.y;
+          }
         }
       }
     }
@@ -472,56 +551,33 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
         }
       }
     }
+    if (!whole) {
+      // Publish this record, count it, and let the last contributor merge.
+      __threadfence();
+      __syncthreads();
+      const int64_t c0 = cta_of_block(u0, G, N), c1 = cta_of_block(u0 + nb - 1, G, N);
+      const int64_t unit = (static_cast<int64_t>(kvh) * B + seq) * p.n_hsub + hsub;
+      if (tid == 0) {
+        int contributors = 0;
+        for (int64_t c = c0; c <= c1; ++c)
+          contributors += (cta_range_start(c, G, N) != cta_range_start(c + 1, G, N)) ? 1 : 0;
+        const unsigned int old = atomicAdd(p.counters + unit, 1u);
+        s_last = 0;
+        if (old + 1 == static_cast<unsigned int>(contributors)) {
+          s_last = 1;
+        } else if (old + 1 > static_cast<unsigned int>(contributors)) {
+          set_flag(p.err, 0x10u);  // the workspace counters were not zero
+          atomicExch(p.counters + unit, 0u);
+        }
+      }
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        merge_records<GH>(p, D, u0, c0, c1, G, N, seq, h0, reinterpret_cast<int*>(s_o), kGqaWarps * GH * D);
+        if (tid == 0) p.counters[unit] = 0u;
+      }
+    }
     __syncthreads();
-  }
-}
-
-// Combines the partial records of units split across CTAs; writes zeros for
-// units whose length was invalid. One CTA per unit.
-template <int GH>
-__global__ void __launch_bounds__(128) gqa_merge_kernel(const GqaParams p, int D, int G) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  int* s_scan = reinterpret_cast<int*>(smem);
-  const int B = p.batch, bs = p.block_size;
-  scan_blocks(p.context_lens, B, bs, p.max_blocks, s_scan);
-  const int u = blockIdx.x;
-  const int hsub = u % p.n_hsub;
-  const int seq = (u / p.n_hsub) % B;
-  const int kvh = u / (p.n_hsub * B);
-  const int h0 = kvh * p.group + hsub * GH;
-  const int nb = s_scan[seq + 1] - s_scan[seq];
-  if (nb == 0) {
-    for (int idx = threadIdx.x; idx < GH * D; idx += blockDim.x)
-      store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + h0 + idx / D) * D + idx % D, 0.f, p.out_dtype);
-    return;
-  }
-  const int64_t slab = static_cast<int64_t>(p.n_hsub) * s_scan[B];
-  const int64_t N = slab * p.n_kv_heads;
-  const int64_t u0 = kvh * slab + static_cast<int64_t>(p.n_hsub) * s_scan[seq] + static_cast<int64_t>(hsub) * nb;
-  const int64_t u1 = u0 + nb;
-  const int64_t c0 = cta_of_block(u0, G, N), c1 = cta_of_block(u1 - 1, G, N);
-  if (c0 == c1) return;
-  for (int idx = threadIdx.x; idx < GH * D; idx += blockDim.x) {
-    const int h = idx / D, d = idx - (idx / D) * D;
-    float M = kNegInf;
-    for (int64_t c = c0; c <= c1; ++c) {
-      const int64_t f0 = cta_range_start(c, G, N);
-      if (f0 == cta_range_start(c + 1, G, N)) continue;
-      const int64_t rec = c * 2 + ((u0 > f0) ? 1 : 0);
-      M = fmaxf(M, p.rec_ml[(rec * GH + h) * 2]);
-    }
-    float Lsum = 0.f, O = 0.f;
-    for (int64_t c = c0; c <= c1; ++c) {
-      const int64_t f0 = cta_range_start(c, G, N);
-      if (f0 == cta_range_start(c + 1, G, N)) continue;
-      const int64_t rec = c * 2 + ((u0 > f0) ? 1 : 0);
-      const float mc = p.rec_ml[(rec * GH + h) * 2];
-      if (mc == kNegInf) continue;
-      const float f = fast_exp2(mc - M);
-      Lsum += f * p.rec_ml[(rec * GH + h) * 2 + 1];
-      O += f * p.rec_o[(rec * GH + h) * D + d];
-    }
-    store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + h0 + h) * D + d, O / Lsum, p.out_dtype);
   }
 }
 

@@ -7,15 +7,9 @@
 
 namespace kvc {
 
-// mode 0: launch main (+ merge when merge_grid > 0); mode 1: only report
-// the occupancy (CTAs per SM) of the main kernel in *occ.
-template <typename T>
-kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, int merge_grid,
-                        size_t merge_smem, cudaStream_t stream, int mode, int* occ);
-
+// mode 0: launch; mode 1: only report the occupancy (CTAs per SM) in *occ.
 template <typename T, int D, int GH>
-static kvc_status gqa_run(const GqaParams& p, int grid, size_t smem, int merge_grid, size_t merge_smem,
-                          cudaStream_t stream, int mode, int* occ) {
+static kvc_status gqa_run(const GqaParams& p, int grid, size_t smem, cudaStream_t stream, int mode, int* occ) {
   auto* k = gqa_decode_kernel<T, D, GH>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gqa)");
@@ -25,36 +19,28 @@ static kvc_status gqa_run(const GqaParams& p, int grid, size_t smem, int merge_g
     return KVC_OK;
   }
   k<<<grid, kGqaWarps * 32, smem, stream>>>(p);
-  if (merge_grid > 0) {
-    auto* mk = gqa_merge_kernel<GH>;
-    if (merge_smem > 48 * 1024) {
-      e = cudaFuncSetAttribute(mk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(merge_smem));
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge)");
-    }
-    mk<<<merge_grid, 128, merge_smem, stream>>>(p, D, grid);
-  }
   return KVC_OK;
 }
 
 template <typename T, int D>
-static kvc_status gqa_run_gh(const GqaParams& p, int GH, int grid, size_t smem, int merge_grid, size_t merge_smem,
-                             cudaStream_t stream, int mode, int* occ) {
+static kvc_status gqa_run_gh(const GqaParams& p, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
+                             int* occ) {
   switch (GH) {
-    case 1: return gqa_run<T, D, 1>(p, grid, smem, merge_grid, merge_smem, stream, mode, occ);
-    case 2: return gqa_run<T, D, 2>(p, grid, smem, merge_grid, merge_smem, stream, mode, occ);
-    case 4: return gqa_run<T, D, 4>(p, grid, smem, merge_grid, merge_smem, stream, mode, occ);
+    case 1: return gqa_run<T, D, 1>(p, grid, smem, stream, mode, occ);
+    case 2: return gqa_run<T, D, 2>(p, grid, smem, stream, mode, occ);
+    case 4: return gqa_run<T, D, 4>(p, grid, smem, stream, mode, occ);
   }
   return fail(KVC_ERR_UNSUPPORTED, "head subgroup %d", GH);
 }
 
 template <typename T>
-kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, int merge_grid,
-                        size_t merge_smem, cudaStream_t stream, int mode, int* occ) {
+kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
+                        int* occ) {
   switch (D) {
-    case 32: return gqa_run_gh<T, 32>(p, GH, grid, smem, merge_grid, merge_smem, stream, mode, occ);
-    case 64: return gqa_run_gh<T, 64>(p, GH, grid, smem, merge_grid, merge_smem, stream, mode, occ);
-    case 128: return gqa_run_gh<T, 128>(p, GH, grid, smem, merge_grid, merge_smem, stream, mode, occ);
-    case 256: return gqa_run_gh<T, 256>(p, GH, grid, smem, merge_grid, merge_smem, stream, mode, occ);
+    case 32: return gqa_run_gh<T, 32>(p, GH, grid, smem, stream, mode, occ);
+    case 64: return gqa_run_gh<T, 64>(p, GH, grid, smem, stream, mode, occ);
+    case 128: return gqa_run_gh<T, 128>(p, GH, grid, smem, stream, mode, occ);
+    case 256: return gqa_run_gh<T, 256>(p, GH, grid, smem, stream, mode, occ);
   }
   return fail(KVC_ERR_UNSUPPORTED, "head_dim %d (supported: 32, 64, 128, 256)", D);
 }

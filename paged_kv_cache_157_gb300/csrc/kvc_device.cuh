@@ -177,6 +177,30 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Packed fp32x2 arithmetic of sm_100+: one instruction, two independent
+// IEEE fp32 operations (round to nearest even).
+union F2U64 {
+  float2 f;
+  unsigned long long u;
+};
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  F2U64 A, Bv, Cv, R;
+  A.f = a;
+  Bv.f = b;
+  Cv.f = c;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(R.u) : "l"(A.u), "l"(Bv.u), "l"(Cv.u));
+  return R.f;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  F2U64 A, Bv, R;
+  A.f = a;
+  Bv.f = b;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(R.u) : "l"(A.u), "l"(Bv.u));
+  return R.f;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -30,8 +30,7 @@ def run_decode(kvc, dev, scale, out_dtype=torch.float32, workspace="auto"):
     out = torch.empty((B, Hq, D), dtype=out_dtype, device="cuda")
     ws = None
     if workspace == "auto":
-        n = kvc.decode_workspace_size(B, Hq, Hkv, D, bs, dev["block_tables"].shape[1])
-        ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+        ws = kvc.new_decode_workspace(B, Hq, Hkv, D, bs, dev["block_tables"].shape[1])
     elif workspace is not None:
         ws = workspace
     kvc.decode_attention(q, dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"], scale, out, ws)

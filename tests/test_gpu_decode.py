@@ -55,7 +55,7 @@ def test_config1_tiny_mha_fp32_every_step_vs_recompute(kvc):
     for l, lay in enumerate(layers):
         kvc.append(lay["k"][:5].cuda(), lay["v"][:5].cuda(), slots, *caches[l])
     scale = 1.0 / math.sqrt(D)
-    ws = torch.empty(kvc.decode_workspace_size(1, H, H, D, bs, 5), dtype=torch.uint8, device="cuda")
+    ws = kvc.new_decode_workspace(1, H, H, D, bs, 5)
     worst = 0.0
     for t in range(5, T):
         slot = torch.tensor(pool.reserve(sid, 1), dtype=torch.int64, device="cuda")
