@@ -166,16 +166,33 @@ __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __re
                                          WarpState<T, D, GH>& st, int tq, int dq, int lane, int h_lane) {
   using C = GqaCfg<T, D, GH>;
   float s[C::NV];
+  {
+    // All RT rows' raw K chunks first, then the RT*GH accumulators advance
+    // together over the lane's dims (independent FMA chains, unpacked lazily).
+    uint4 kr[C::RT][C::NCH];
 #pragma unroll
-  for (int r = 0; r < C::RT; ++r) {
-    float2 kf[C::DP2];
-    load_pairs<T, C::NCH, C::DL, C::VEC>(kp + (r * C::TL + tq) * D, dq, kf);
+    for (int r = 0; r < C::RT; ++r) {
 #pragma unroll
-    for (int h = 0; h < GH; ++h) {
-      float2 acc = fmul2(st.q[h][0], kf[0]);
+      for (int j = 0; j < C::NCH; ++j) kr[r][j] = lds128(kp + (r * C::TL + tq) * D + (dq + C::DL * j) * C::VEC);
+    }
+    float2 acc[C::RT][GH];
 #pragma unroll
-      for (int i = 1; i < C::DP2; ++i) acc = ffma2(st.q[h][i], kf[i], acc);
-      s[h * C::RT + r] = acc.x + acc.y;
+    for (int j = 0; j < C::NCH; ++j) {
+#pragma unroll
+      for (int c = 0; c < C::VEC / 2; ++c) {
+        const int i = j * (C::VEC / 2) + c;
+#pragma unroll
+        for (int r = 0; r < C::RT; ++r) {
+          const float2 kf = Elem<T>::pair(kr[r][j], c);
+#pragma unroll
+          for (int h = 0; h < GH; ++h) acc[r][h] = (i == 0) ? fmul2(st.q[h][0], kf) : ffma2(st.q[h][i], kf, acc[r][h]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < C::RT; ++r) {
+#pragma unroll
+      for (int h = 0; h < GH; ++h) s[h * C::RT + r] = acc[r][h].x + acc[r][h].y;
     }
   }
   ReduceScatter<C::NV, C::DL / 2>::run(s, dq);
@@ -426,10 +443,18 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
     T* wst = s_stage + static_cast<size_t>(w) * S * 2 * page_elems;
     uint64_t* wbar = s_bar + w * S;
 
-    auto issue = [&](int t) {
-      const int j = j0 + w + kGqaWarps * t;
+    // Block-table entries of this warp's tiles, 32 at a time: lane L holds the
+    // entry of tile 32*window + L (one coalesced load per window, issued a
+    // window ahead), handed to lane 0 by shuffles when it issues the copies.
+    auto load_window = [&](int win) -> int {
+      const int t = win * 32 + lane;
+      return t < nbw ? __ldg(bt + j0 + w + kGqaWarps * t) : -1;
+    };
+    int bt_cur = load_window(0);
+    int bt_nxt = nbw > 32 ? load_window(1) : -1;
+
+    auto issue = [&](int t, int phys) {
       const int slot = (ticket + t) % S;
-      const int phys = __ldg(bt + j);
       if (phys < 0 || phys >= p.num_blocks) {
         set_flag(p.err, 0x1u);
         mbar_arrive(wbar + slot);
@@ -442,8 +467,11 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
       }
     };
 
-    if (lane == 0 && !aborted) {
-      for (int t = 0; t < S && t < nbw; ++t) issue(t);
+    if (!aborted) {
+      for (int t = 0; t < S && t < nbw; ++t) {
+        const int ph = __shfl_sync(0xffffffffu, bt_cur, t);
+        if (lane == 0) issue(t, ph);
+      }
     }
     __syncwarp();
 
@@ -452,6 +480,13 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
       const int slot = (ticket + t) % S;
       const uint32_t parity = ((ticket + t) / S) & 1u;
       if (aborted) break;
+      if (t > 0 && (t & 31) == 0) {
+        bt_cur = bt_nxt;
+        bt_nxt = (t + 32 < nbw) ? load_window((t >> 5) + 1) : -1;
+      }
+      const int phys = __shfl_sync(0xffffffffu, bt_cur, t & 31);
+      const int tn = t + S;
+      const int phys_next = __shfl_sync(0xffffffffu, (tn >> 5) == (t >> 5) ? bt_cur : bt_nxt, tn & 31);
       const bool ok = mbar_wait_bounded(wbar + slot, parity);
       if (__any_sync(0xffffffffu, !ok)) {
         aborted = true;
@@ -460,7 +495,6 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
         break;
       }
       const int j = j0 + w + kGqaWarps * t;
-      const int phys = __ldg(bt + j);
       if (phys >= 0 && phys < p.num_blocks) {
         const T* kp = wst + static_cast<size_t>(slot) * 2 * page_elems;
         const T* vp = kp + page_elems;
@@ -474,11 +508,10 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
             gqa_tile<T, D, GH, true>(kp + tt * 16 * D, vp + tt * 16 * D, valid, st, tq, dq, lane, h_lane);
         }
       }
+      // Every shared-memory read of this stage fed an FMA issued before this
+      // point, so no read of it is outstanding when lane 0 refills it.
       __syncwarp();
-      if (lane == 0 && t + S < nbw) {
-        fence_proxy_async_smem();
-        issue(t + S);
-      }
+      if (lane == 0 && tn < nbw) issue(tn, phys_next);
       __syncwarp();
     }
     if (drain_from >= 0) {

@@ -31,6 +31,11 @@ template <> struct Elem<float> {
     f[3] = __uint_as_float(u.w);
   }
   __device__ __forceinline__ static float to_float(float x) { return x; }
+  // Elements 2c and 2c+1 of a 16-byte chunk as an fp32 pair.
+  __device__ __forceinline__ static float2 pair(const uint4& u, int c) {
+    return c == 0 ? make_float2(__uint_as_float(u.x), __uint_as_float(u.y))
+                  : make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+  }
 };
 template <> struct Elem<__nv_bfloat16> {
   static constexpr int kVec = 8;
@@ -46,6 +51,10 @@ template <> struct Elem<__nv_bfloat16> {
     unpack2(u.w, f + 6);
   }
   __device__ __forceinline__ static float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+  __device__ __forceinline__ static float2 pair(const uint4& u, int c) {
+    const uint32_t w = c == 0 ? u.x : (c == 1 ? u.y : (c == 2 ? u.z : u.w));
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
 };
 template <> struct Elem<__half> {
   static constexpr int kVec = 8;
@@ -62,6 +71,10 @@ template <> struct Elem<__half> {
     unpack2(u.w, f + 6);
   }
   __device__ __forceinline__ static float to_float(__half x) { return __half2float(x); }
+  __device__ __forceinline__ static float2 pair(const uint4& u, int c) {
+    uint32_t w = c == 0 ? u.x : (c == 1 ? u.y : (c == 2 ? u.z : u.w));
+    return __half22float2(*reinterpret_cast<__half2*>(&w));
+  }
 };
 
 // Stores one fp32 value as the output dtype (0 f32, 1 f16, 2 bf16).
