@@ -1,17 +1,847 @@
-// MLA absorbed decode (tensor cores). Placeholder until the tcgen05 kernel lands.
+// MLA absorbed decode on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// What is computed ("KV Cache（键值缓存）" section 2.2, with W^UK and W^UV
+// absorbed into the query and output side): for sequence i and head h,
+//     z_t = scale * q~_h . c_t          (c_t = cached row, d_c + d_r = 576 wide)
+//     a   = softmax(z) over the context_lens[i] cached rows (paged, block 64)
+//     o_h = sum_t a_t c_t[0 : d_c]      (d_c = 512)
+//
+// Design (sm_103a, one CTA per SM):
+// * A CTA works on 32-token tiles and one half (256) of the 512 output
+//   dimensions; its partner CTA (adjacent in the grid) takes the other half of
+//   the same tiles, so the latent tile is fetched from HBM once and the second
+//   read is served by L2. Both compute S = Q~ C^T in full: the O half
+//   (128 x 256 fp32) plus two S buffers (128 x 32 fp32 each) fit the 512 TMEM
+//   columns, which the whole O (128 x 512 fp32) alone would fill.
+// * Shared memory: Q~ [128 x 576] bf16 (147 KB) resident per sequence and two
+//   latent tile stages [32 x 576] (36 KB each),
+//   in the 128B-swizzled K-major layout that TMA writes and the UMMA
+//   descriptors read.
+// * Warp roles: warps 0-3 = softmax and epilogue (thread = head = TMEM lane),
+//   warp 4 = TMA producer, warp 5 = MMA issuer and TMEM owner.
+//   Per tile: S(t) = Q~ C_t^T (36 MMAs, K = 16 each, N = 32) -> softmax reads S
+//   from TMEM, updates the running max lazily (O in TMEM is rescaled only when
+//   the max grows by more than 2^8), writes P = exp2(s - m) into TMEM as two
+//   bf16 parts (hi = bf16(p), lo = bf16(p - hi), so hi + lo carries p to about
+//   2^-17) -> O += P_hi V_t + P_lo V_t (4 MMAs with A read from TMEM, N = 256,
+//   V = the first 512 columns of the same tile, read MN-major). The MMA of S(t+1) is issued before PV(t) so the tensor
+//   core works while the softmax runs.
+// * Work split: as in the GQA kernel, the tiles of all sequences are laid end
+//   to end and CTA pair c takes a contiguous range; a sequence cut by a range
+//   boundary leaves fp32 records (m, l, O) and the last contributing CTA of
+//   each (sequence, half) merges them with the log-sum-exp rule.
+// * Every mbarrier wait is bounded; a wait that gives up sets the error word
+//   and a shared abort flag that stops every role, which then drains and
+//   frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "kvc_device.cuh"
 #include "kvc_internal.h"
+
+namespace kvc {
+
+namespace mla {
+
+constexpr int kHeads = 128;          // M of every MMA
+constexpr int kDc = 512;             // latent (value) width
+constexpr int kW = 576;              // cached row width
+constexpr int kKB = kW / 64;         // 64-element (128 B) K blocks of a row: 9
+constexpr int kTile = 32;            // tokens per tile (MMA N for S)
+constexpr int kHalf = kDc / 2;       // output dims per CTA: 256
+constexpr int kStages = 2;           // latent tile stages
+constexpr int kThreads = 192;        // 6 warps
+constexpr int kMaxBatch = 256;
+
+constexpr uint32_t kQBytes = kHeads * kW * 2;        // 147456
+constexpr uint32_t kQSub = kHeads * 128;             // one 64-column block of Q~: 16384
+constexpr uint32_t kTileBytes = kTile * kW * 2;      // 36864
+constexpr uint32_t kTileSub = kTile * 128;           // one 64-column block of a tile: 4096
+
+// TMEM columns: O half at 0..255, S buffers at 256 and 288, P at 320: the
+// high bf16 part of the weights (16 columns = 32 bf16 per head) then the low
+// part (336..351).
+constexpr uint32_t kColO = 0;
+constexpr uint32_t kColS = 256;
+constexpr uint32_t kColP = 320;
+constexpr uint32_t kTmemCols = 512;
+
+// Shared memory carve-up (offsets from a 1024-byte aligned base).
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffC = kOffQ + kQBytes;
+constexpr uint32_t kOffBar = kOffC + kStages * kTileBytes;
+// barrier indices
+enum {
+  B_QFULL = 0, B_QEMPTY, B_CFULL0, B_CFULL1, B_CEMPTY0, B_CEMPTY1, B_SFULL0, B_SFULL1, B_SEMPTY0, B_SEMPTY1,
+  B_PFULL, B_PVDONE, B_OFREE, B_FINAL, B_COUNT
+};
+constexpr uint32_t kOffMisc = kOffBar + B_COUNT * 8;  // tmem address, abort flag, last flag
+constexpr uint32_t kOffScan = kOffMisc + 16;
+constexpr uint32_t smem_bytes(int batch) { return kOffScan + (batch + 1 + 32) * 4 + 1024; }
+
+struct Params {
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* out;
+  float* rec_o;   // [G * 2, 128, 256]
+  float* rec_ml;  // [G * 2, 128, 2]
+  unsigned int* counters;  // [batch * 2]
+  unsigned int* err;
+  int64_t num_blocks;
+  int batch;
+  int max_blocks;
+  int block_size;
+  int out_dtype;
+  int unit_mode;  // 1: CTA pair s handles all of sequence s
+  float qscale;   // scale * log2(e)
+};
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void arrive_expect(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           unsigned int* err) {
+  if (try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1; i < kWaitLimit; ++i) {
+    if (try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitNs) break;
+    }
+  }
+  *abort_flag = 1;
+  set_flag(err, 0x8u);
+  return false;
+}
+
+// UMMA shared-memory descriptor: start address, leading / stride byte offsets,
+// the fixed version bits of sm_100 descriptors and the swizzle mode
+// (2 = 128B, 4 = 64B).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+         (static_cast<uint64_t>(swizzle) << 61);
+}
+
+// Instruction descriptor of kind::f16: D fp32, A and B bf16, K- or MN-major.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Same MMA with the A operand read from tensor memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ------------------------------------------------------- work bookkeeping
+
+__device__ __forceinline__ int seq_tiles(const int32_t* lens, int b, int bs, int max_blocks) {
+  const int n = __ldg(lens + b);
+  if (n < 1) return 0;
+  const int cap = bs * max_blocks;
+  return ((n < cap ? n : cap) + kTile - 1) / kTile;
+}
+
+__device__ __forceinline__ int seq_rows(const int32_t* lens, int b, int bs, int max_blocks) {
+  const int n = __ldg(lens + b);
+  if (n < 1) return 0;
+  const int cap = bs * max_blocks;
+  return n < cap ? n : cap;
+}
+
+// Exclusive prefix sums of tiles per sequence (whole CTA participates).
+__device__ inline void scan_tiles(const int32_t* lens, int B, int bs, int max_blocks, int* s_scan) {
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    int run = 0;
+    for (int base = 0; base < B; base += 32) {
+      const int b = base + tid;
+      const int v = b < B ? seq_tiles(lens, b, bs, max_blocks) : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, x, o);
+        if (tid >= o) x += u;
+      }
+      if (b < B) s_scan[b] = run + x - v;
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (tid == 0) s_scan[B] = run;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ int64_t range_start(int64_t c, int64_t G, int64_t N) { return c * N / G; }
+__device__ __forceinline__ int64_t pair_of(int64_t t, int64_t G, int64_t N) { return ((t + 1) * G - 1) / N; }
+
+// A contiguous run of tiles of one sequence handled by this CTA.
+struct Segment {
+  int seq, t0, t1, ntiles;  // tiles [t0, t1) of the sequence's ntiles
+  int64_t u0;               // global index of the sequence's first tile
+  int which;                // record slot (0: segment starts the CTA range)
+};
+
+// Walks this CTA's segments: returns false when the range is exhausted.
+struct Walker {
+  int64_t pos, hi;
+  int64_t lo;
+  __device__ bool next(const Params& p, const int* s_scan, Segment& sg) {
+    if (p.unit_mode) {
+      if (pos >= hi) return false;
+      sg.seq = static_cast<int>(pos);
+      sg.ntiles = seq_tiles(p.context_lens, sg.seq, p.block_size, p.max_blocks);
+      sg.t0 = 0;
+      sg.t1 = sg.ntiles;
+      sg.u0 = 0;
+      sg.which = 0;
+      pos = hi;
+      return true;
+    }
+    if (pos >= hi) return false;
+    int a = 0, b = p.batch - 1;
+    while (a < b) {
+      const int mid = (a + b + 1) >> 1;
+      if (s_scan[mid] <= pos) a = mid; else b = mid - 1;
+    }
+    sg.seq = a;
+    sg.ntiles = s_scan[a + 1] - s_scan[a];
+    sg.u0 = s_scan[a];
+    sg.t0 = static_cast<int>(pos - sg.u0);
+    const int64_t end = sg.u0 + sg.ntiles < hi ? sg.u0 + sg.ntiles : hi;
+    sg.t1 = static_cast<int>(end - sg.u0);
+    sg.which = (pos == lo) ? 0 : 1;
+    pos = end;
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
+                      const Params p) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  unsigned char* sm = smem_raw + (base - raw_addr);
+  const uint32_t sQ = base + kOffQ, sC = base + kOffC;
+  const uint32_t bar0 = base + kOffBar;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(sm + kOffMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
+  volatile int* s_last = reinterpret_cast<volatile int*>(sm + kOffMisc + 8);
+  int* s_scan = reinterpret_cast<int*>(sm + kOffScan);
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hf = blockIdx.x & 1;  // output half of this CTA
+  const int64_t pair = blockIdx.x >> 1;
+  const int64_t G = gridDim.x >> 1;
+
+  if (tid == 0) {
+    *s_abort = 0;
+    const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 1, 4, 1};
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], counts[i]);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + kOffMisc),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (blockIdx.x == 0) {
+    for (int b = tid; b < p.batch; b += blockDim.x) {
+      const int n = __ldg(p.context_lens + b);
+      if (n < 1 || n > p.block_size * p.max_blocks) set_flag(p.err, 0x2u);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  Walker walk;
+  if (p.unit_mode) {
+    walk.lo = walk.pos = pair;
+    walk.hi = pair + 1;
+  } else {
+    scan_tiles(p.context_lens, p.batch, p.block_size, p.max_blocks, s_scan);
+    const int64_t N = s_scan[p.batch];
+    walk.lo = walk.pos = range_start(pair, G, N);
+    walk.hi = range_start(pair + 1, G, N);
+  }
+  // zero outputs of sequences with an invalid length (no CTA visits them)
+  if (blockIdx.x < 2) {
+    for (int b = 0; b < p.batch; ++b) {
+      if (__ldg(p.context_lens + b) >= 1) continue;
+      for (int idx = tid; idx < kHeads * kHalf; idx += blockDim.x) {
+        const int h = idx / kHalf, d = idx % kHalf;
+        store_out(p.out, (static_cast<int64_t>(b) * kHeads + h) * kDc + hf * kHalf + d, 0.f, p.out_dtype);
+      }
+    }
+  }
+  __syncthreads();
+
+  const int64_t N_all = p.unit_mode ? 0 : s_scan[p.batch];
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t g = 0, seg_i = 0;
+      uint32_t issued[kStages] = {0, 0};
+      bool q_pending = false;
+      Segment sg;
+      Walker w = walk;
+      while (!*s_abort && w.next(p, s_scan, sg)) {
+        if (sg.ntiles == 0) continue;
+        if (seg_i > 0 && !wait_phase(bar(B_QEMPTY), (seg_i - 1) & 1u, s_abort, p.err)) break;
+        arrive_expect(bar(B_QFULL), kQBytes);
+        for (int kb = 0; kb < kKB; ++kb) tma_load_3d(sQ + kb * kQSub, &tm_q, kb * 64, 0, sg.seq, bar(B_QFULL));
+        q_pending = true;
+        const int32_t* bt = p.block_tables + static_cast<int64_t>(sg.seq) * p.max_blocks;
+        bool ok = true;
+        for (int t = sg.t0; t < sg.t1; ++t, ++g) {
+          const int st = g & 1;
+          if (g >= kStages && !wait_phase(bar(B_CEMPTY0 + st), ((g >> 1) - 1) & 1u, s_abort, p.err)) {
+            ok = false;
+            break;
+          }
+          const int j = (t * kTile) / p.block_size;
+          int phys = __ldg(bt + j);
+          if (phys < 0 || phys >= p.num_blocks) {
+            set_flag(p.err, 0x1u);
+            phys = 0;  // keep the pipeline moving on valid memory; the output is flagged
+          }
+          const int row = phys * p.block_size + (t * kTile) % p.block_size;
+          arrive_expect(bar(B_CFULL0 + st), kTileBytes);
+          for (int kb = 0; kb < kKB; ++kb)
+            tma_load_2d(sC + st * kTileBytes + kb * kTileSub, &tm_c, kb * 64, row, bar(B_CFULL0 + st));
+          ++issued[st];
+        }
+        if (!ok) break;
+        ++seg_i;
+      }
+      if (*s_abort) {
+        // Copies still in flight must land before this shared memory goes away:
+        // wait (bounded) for the last phase of every barrier this warp armed.
+        for (int st = 0; st < kStages; ++st) {
+          if (issued[st] == 0) continue;
+          const uint64_t t0 = globaltimer_ns();
+          while (!try_wait(bar(B_CFULL0 + st), (issued[st] - 1) & 1u) && globaltimer_ns() - t0 < kWaitNs) {
+          }
+        }
+        if (q_pending && seg_i > 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!try_wait(bar(B_QFULL), (seg_i - 1) & 1u) && globaltimer_ns() - t0 < kWaitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = instr_desc(kHeads, kTile, 0, 0);
+      const uint32_t id_pv = instr_desc(kHeads, kHalf, 0, 1);
+      uint32_t g = 0, seg_i = 0, pv_i = 0;
+      Segment sg;
+      Walker w = walk;
+      bool ok = true;
+      while (ok && !*s_abort && w.next(p, s_scan, sg)) {
+        if (sg.ntiles == 0) continue;
+        if (!wait_phase(bar(B_QFULL), seg_i & 1u, s_abort, p.err)) break;
+        fence_after();
+        const uint32_t g_first = g;
+        auto issue_pv = [&](uint32_t gi) -> bool {
+          if (!wait_phase(bar(B_PFULL), pv_i & 1u, s_abort, p.err)) return false;
+          const bool first = (gi == g_first);
+          if (first && seg_i > 0 && !wait_phase(bar(B_OFREE), (seg_i - 1) & 1u, s_abort, p.err)) return false;
+          fence_after();
+          const uint32_t st = gi & 1u;
+          for (int part = 0; part < 2; ++part) {  // P_hi, then P_lo, against the same V rows
+            for (int ks = 0; ks < kTile / 16; ++ks) {
+              const uint64_t b = smem_desc(sC + st * kTileBytes + (4 * hf) * kTileSub + ks * 2048, 4096, 1024, 2);
+              mma_bf16_ts(tmem + kColO, tmem + kColP + part * (kTile / 2) + ks * 8, b, id_pv,
+                          (first && part == 0 && ks == 0) ? 0u : 1u);
+            }
+          }
+          mma_commit(bar(B_CEMPTY0 + st));
+          mma_commit(bar(B_PVDONE));
+          ++pv_i;
+          return true;
+        };
+        for (int t = sg.t0; t < sg.t1 && ok; ++t, ++g) {
+          const uint32_t st = g & 1u;
+          if (!wait_phase(bar(B_CFULL0 + st), (g >> 1) & 1u, s_abort, p.err)) { ok = false; break; }
+          if (g >= kStages && !wait_phase(bar(B_SEMPTY0 + st), ((g >> 1) - 1) & 1u, s_abort, p.err)) {
+            ok = false;
+            break;
+          }
+          fence_after();
+          for (int ks = 0; ks < kW / 16; ++ks) {
+            const int kb = ks >> 2, kin = ks & 3;
+            const uint64_t a = smem_desc(sQ + kb * kQSub + kin * 32, 16, 1024, 2);
+            const uint64_t b = smem_desc(sC + st * kTileBytes + kb * kTileSub + kin * 32, 16, 1024, 2);
+            mma_bf16(tmem + kColS + st * kTile, a, b, id_s, ks == 0 ? 0u : 1u);
+          }
+          mma_commit(bar(B_SFULL0 + st));
+          if (t == sg.t1 - 1) mma_commit(bar(B_QEMPTY));
+          if (t > sg.t0 && !issue_pv(g - 1)) { ok = false; break; }
+        }
+        if (ok && !issue_pv(g - 1)) ok = false;
+        ++seg_i;
+      }
+      // all MMAs of this CTA complete before TMEM is released
+      mma_commit(bar(B_FINAL));
+      const uint64_t t0 = globaltimer_ns();
+      while (!try_wait(bar(B_FINAL), 0) && globaltimer_ns() - t0 < kWaitNs) {
+      }
+    }
+  } else {
+    // ------------------------------------------------- softmax + epilogue
+    const int h = warp * 32 + lane;  // head = TMEM lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    uint32_t g = 0, seg_i = 0, pv_seen = 0;
+    Segment sg;
+    Walker w = walk;
+    bool ok = true;
+    while (ok && !*s_abort && w.next(p, s_scan, sg)) {
+      if (sg.ntiles == 0) continue;
+      const int n_rows = seq_rows(p.context_lens, sg.seq, p.block_size, p.max_blocks);
+      float m = -__builtin_huge_valf(), l = 0.f;
+      const uint32_t g_first = g;
+      for (int t = sg.t0; t < sg.t1; ++t, ++g) {
+        const uint32_t st = g & 1u;
+        if (!__all_sync(0xffffffffu, wait_phase(bar(B_SFULL0 + st), (g >> 1) & 1u, s_abort, p.err))) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        float s[kTile];
+        tmem_ld32(lane_addr + kColS + st * kTile, s);
+        fence_before();
+        __syncwarp();
+        if (lane == 0) arrive(bar(B_SEMPTY0 + st));
+        const int valid = n_rows - t * kTile;
+        float mt = -__builtin_huge_valf();
+#pragma unroll
+        for (int i = 0; i < kTile; ++i) {
+          s[i] = (i < valid) ? s[i] * p.qscale : -__builtin_huge_valf();
+          mt = fmaxf(mt, s[i]);
+        }
+        if (g > g_first) {
+          // P(t-1) must be consumed (and O stable) before P or O change.
+          if (!__all_sync(0xffffffffu, wait_phase(bar(B_PVDONE), pv_seen & 1u, s_abort, p.err))) {
+            ok = false;
+            break;
+          }
+          ++pv_seen;
+          fence_after();
+        }
+        // Lazy rescale, decided per warp: the TMEM accesses below are warp-wide.
+        if (__any_sync(0xffffffffu, mt > m + 8.0f)) {
+          const float m_new = fmaxf(m, mt);
+          const float alpha = fast_exp2(m - m_new);  // 0 on the first tile of a segment
+          if (g > g_first) {
+            // rescale O in TMEM (rare: the running max grew by more than 2^8)
+            for (int c = 0; c < kHalf; c += 32) {
+              float v[32];
+              tmem_ld32(lane_addr + kColO + c, v);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= alpha;
+              tmem_st32(lane_addr + kColO + c, v);
+            }
+          }
+          l *= alpha;
+          m = m_new;
+        }
+        // Row h of P in TMEM: 16 columns of bf16 pairs (hi), then 16 (lo).
+        uint32_t pk[kTile];
+#pragma unroll
+        for (int i = 0; i < kTile / 2; ++i) {
+          const float p0 = fast_exp2(s[2 * i] - m), p1 = fast_exp2(s[2 * i + 1] - m);
+          l += p0 + p1;
+          const uint32_t hi = pack_bf16(p0, p1);
+          pk[i] = hi;
+          pk[kTile / 2 + i] = pack_bf16(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
+        }
+        tmem_st32u(lane_addr + kColP, pk);
+        fence_before();
+        __syncwarp();
+        if (lane == 0) arrive(bar(B_PFULL));
+      }
+      if (!ok) break;
+      // ---- epilogue: wait for the last PV, read O, write output or record
+      if (!__all_sync(0xffffffffu, wait_phase(bar(B_PVDONE), pv_seen & 1u, s_abort, p.err))) break;
+      ++pv_seen;
+      fence_after();
+      const bool whole = (sg.t0 == 0 && sg.t1 == sg.ntiles);
+      const int64_t rec = (static_cast<int64_t>(blockIdx.x) * 2 + sg.which) * kHeads + h;
+      const float inv = 1.0f / l;
+      for (int c = 0; c < kHalf; c += 32) {
+        float v[32];
+        tmem_ld32(lane_addr + kColO + c, v);
+        if (whole) {
+          const int64_t o = (static_cast<int64_t>(sg.seq) * kHeads + h) * kDc + hf * kHalf + c;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) store_out(p.out, o + i, v[i] * inv, p.out_dtype);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.rec_o + rec * kHalf + c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+      }
+      if (!whole) {
+        p.rec_ml[rec * 2] = m;
+        p.rec_ml[rec * 2 + 1] = l;
+      }
+      fence_before();
+      __syncwarp();
+      if (lane == 0) arrive(bar(B_OFREE));
+      if (!whole) {
+        // count this record; the last contributor merges (softmax warpgroup only)
+        __threadfence();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const int64_t c0 = pair_of(sg.u0, G, N_all), c1 = pair_of(sg.u0 + sg.ntiles - 1, G, N_all);
+        const int64_t unit = static_cast<int64_t>(sg.seq) * 2 + hf;
+        if (tid == 0) {
+          int contributors = 0;
+          for (int64_t c = c0; c <= c1; ++c)
+            contributors += (range_start(c, G, N_all) != range_start(c + 1, G, N_all)) ? 1 : 0;
+          const unsigned int old = atomicAdd(p.counters + unit, 1u);
+          *s_last = 0;
+          if (old + 1 == static_cast<unsigned int>(contributors)) {
+            *s_last = 1;
+          } else if (old + 1 > static_cast<unsigned int>(contributors)) {
+            set_flag(p.err, 0x10u);
+            atomicExch(p.counters + unit, 0u);
+          }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (*s_last) {
+          __threadfence();
+          // merge: this thread owns head h, all 256 dims of this half
+          float M = -__builtin_huge_valf();
+          for (int64_t c = c0; c <= c1; ++c) {
+            const int64_t f0 = range_start(c, G, N_all);
+            if (f0 == range_start(c + 1, G, N_all)) continue;
+            const int64_t r = ((c * 2 + hf) * 2 + ((sg.u0 > f0) ? 1 : 0)) * kHeads + h;
+            M = fmaxf(M, __ldcg(p.rec_ml + r * 2));
+          }
+          float L = 0.f;
+          for (int64_t c = c0; c <= c1; ++c) {
+            const int64_t f0 = range_start(c, G, N_all);
+            if (f0 == range_start(c + 1, G, N_all)) continue;
+            const int64_t r = ((c * 2 + hf) * 2 + ((sg.u0 > f0) ? 1 : 0)) * kHeads + h;
+            const float mc = __ldcg(p.rec_ml + r * 2);
+            if (mc == -__builtin_huge_valf()) continue;
+            L += fast_exp2(mc - M) * __ldcg(p.rec_ml + r * 2 + 1);
+          }
+          const float invL = 1.0f / L;
+          for (int d0 = 0; d0 < kHalf; d0 += 32) {
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+            for (int64_t c = c0; c <= c1; ++c) {
+              const int64_t f0 = range_start(c, G, N_all);
+              if (f0 == range_start(c + 1, G, N_all)) continue;
+              const int64_t r = ((c * 2 + hf) * 2 + ((sg.u0 > f0) ? 1 : 0)) * kHeads + h;
+              const float mc = __ldcg(p.rec_ml + r * 2);
+              if (mc == -__builtin_huge_valf()) continue;
+              const float f = fast_exp2(mc - M);
+              const float4* src = reinterpret_cast<const float4*>(p.rec_o + r * kHalf + d0);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 x = __ldcg(src + i);
+                acc[4 * i] += f * x.x;
+                acc[4 * i + 1] += f * x.y;
+                acc[4 * i + 2] += f * x.z;
+                acc[4 * i + 3] += f * x.w;
+              }
+            }
+            const int64_t o = (static_cast<int64_t>(sg.seq) * kHeads + h) * kDc + hf * kHalf + d0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) store_out(p.out, o + i, acc[i] * invL, p.out_dtype);
+          }
+          if (tid == 0) p.counters[unit] = 0u;
+        }
+      }
+      ++seg_i;
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 5) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+int plan_pairs(const DeviceInfo* dev, int batch, int max_blocks, int block_size) {
+  const int64_t tiles_upper = static_cast<int64_t>(batch) * ((static_cast<int64_t>(max_blocks) * block_size + kTile - 1) / kTile);
+  int64_t G2 = dev->num_sms / 2;
+  const int64_t forced = option(KVC_OPT_BLOCKS_PER_CTA);
+  if (forced > 0) G2 = (tiles_upper * kTile / block_size + forced - 1) / forced;
+  const int64_t cap = option(KVC_OPT_MAX_CTAS);
+  if (cap > 0) G2 = std::min<int64_t>(G2, std::max<int64_t>(1, cap / 2));
+  G2 = std::min<int64_t>(G2, std::max<int64_t>(1, tiles_upper));
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(G2, 1 << 20)));
+}
+
+size_t counter_bytes(int batch) { return (static_cast<size_t>(batch) * 2 * 4 + 255) / 256 * 256; }
+size_t record_bytes_per_pair() { return 2ull * 2 * kHeads * (kHalf + 2) * sizeof(float); }
+
+kvc_status check(int batch, int n_q_heads, int d_c, int d_r, int block_size, int max_blocks) {
+  if (batch < 1 || max_blocks < 1 || block_size < 1) return fail(KVC_ERR_INVALID_ARG, "sizes must be >= 1");
+  if (n_q_heads != kHeads || d_c != kDc || d_r != kW - kDc)
+    return fail(KVC_ERR_UNSUPPORTED, "MLA decode supports n_q_heads 128, d_c 512, d_r 64 (got %d, %d, %d)",
+                n_q_heads, d_c, d_r);
+  if (block_size % kTile != 0 || block_size > 256)
+    return fail(KVC_ERR_UNSUPPORTED, "MLA block_size must be a multiple of 32 up to 256 (got %d)", block_size);
+  if (batch > kMaxBatch) return fail(KVC_ERR_UNSUPPORTED, "MLA batch %d > %d", batch, kMaxBatch);
+  return KVC_OK;
+}
+
+}  // namespace mla
+}  // namespace kvc
 
 extern "C" {
 
-kvc_status kvc_decode_mla_workspace_size(int, int, int, int, int, int, size_t* bytes) {
-  if (bytes) *bytes = 0;
-  return kvc::fail(KVC_ERR_UNSUPPORTED, "MLA decode not built yet");
+kvc_status kvc_decode_mla_workspace_size(int batch, int n_q_heads, int d_c, int d_r, int block_size,
+                                         int max_blocks_per_seq, size_t* bytes) {
+  using namespace kvc;
+  clear_error();
+  if (bytes == nullptr) return fail(KVC_ERR_INVALID_ARG, "bytes is NULL");
+  kvc_status s = mla::check(batch, n_q_heads, d_c, d_r, block_size, max_blocks_per_seq);
+  if (s != KVC_OK) return s;
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != KVC_OK) return s;
+  const int G2 = mla::plan_pairs(dev, batch, max_blocks_per_seq, block_size);
+  *bytes = mla::counter_bytes(batch) + static_cast<size_t>(G2) * mla::record_bytes_per_pair();
+  return KVC_OK;
 }
 
-kvc_status kvc_decode_attention_mla(const void*, const void*, const int32_t*, int, const int32_t*, int, float, int,
-                                    int, int, int, int64_t, kvc_dtype, void*, kvc_dtype, void*, size_t,
-                                    kvc_stream) {
-  return kvc::fail(KVC_ERR_UNSUPPORTED, "MLA decode not built yet");
+kvc_status kvc_decode_attention_mla(const void* q_absorbed, const void* latent_cache, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens, int batch, float scale,
+                                    int n_q_heads, int d_c, int d_r, int block_size, int64_t num_blocks,
+                                    kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
+                                    size_t workspace_bytes, kvc_stream stream) {
+  using namespace kvc;
+  clear_error();
+  kvc_status s = mla::check(batch, n_q_heads, d_c, d_r, block_size, max_blocks_per_seq);
+  if (s != KVC_OK) return s;
+  if (dtype != KVC_BF16) return fail(KVC_ERR_UNSUPPORTED, "MLA decode reads bf16 caches only");
+  if (!dtype_ok(out_dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown out dtype");
+  if (num_blocks < 1) return fail(KVC_ERR_INVALID_ARG, "num_blocks must be >= 1");
+  if (num_blocks * block_size > (1ll << 31) - 1) return fail(KVC_ERR_UNSUPPORTED, "latent pool too large");
+  if (q_absorbed == nullptr || latent_cache == nullptr || block_tables == nullptr || context_lens == nullptr ||
+      out == nullptr)
+    return fail(KVC_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(q_absorbed) || !aligned16(latent_cache)) return fail(KVC_ERR_INVALID_ARG, "16-byte alignment");
+  if (!std::isfinite(scale)) return fail(KVC_ERR_INVALID_ARG, "scale must be finite");
+  if (workspace_bytes > 0 && workspace == nullptr) return fail(KVC_ERR_INVALID_ARG, "workspace is NULL");
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(KVC_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != KVC_OK) return s;
+  const uint32_t smem = mla::smem_bytes(batch);
+  if (smem > static_cast<uint32_t>(dev->max_smem_optin))
+    return fail(KVC_ERR_UNSUPPORTED, "MLA kernel needs %u bytes of shared memory (device max %d)", smem,
+                dev->max_smem_optin);
+  auto encode = mla::encode_fn();
+  if (encode == nullptr) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+
+  CUtensorMap tq, tc;
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(mla::kW), static_cast<cuuint64_t>(mla::kHeads),
+                                static_cast<cuuint64_t>(batch)};
+    const cuuint64_t strides[2] = {mla::kW * 2ull, static_cast<cuuint64_t>(mla::kW) * 2 * mla::kHeads};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(mla::kHeads), 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = encode(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_absorbed), dims, strides, box,
+                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "tensor map for q_absorbed: CUresult %d", static_cast<int>(r));
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mla::kW), static_cast<cuuint64_t>(num_blocks * block_size)};
+    const cuuint64_t strides[1] = {mla::kW * 2ull};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(mla::kTile)};
+    const cuuint32_t es[2] = {1, 1};
+    CUresult r = encode(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(latent_cache), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "tensor map for latent_cache: CUresult %d", static_cast<int>(r));
+  }
+
+  mla::Params p{};
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.err = dev->error_word;
+  p.num_blocks = num_blocks;
+  p.batch = batch;
+  p.max_blocks = max_blocks_per_seq;
+  p.block_size = block_size;
+  p.out_dtype = static_cast<int>(out_dtype);
+  p.qscale = scale * 1.4426950408889634f;
+  int G2 = mla::plan_pairs(dev, batch, max_blocks_per_seq, block_size);
+  const size_t cb = mla::counter_bytes(batch);
+  const int64_t fit = workspace_bytes > cb ? static_cast<int64_t>((workspace_bytes - cb) / mla::record_bytes_per_pair()) : 0;
+  if (fit >= 1) {
+    G2 = static_cast<int>(std::min<int64_t>(G2, fit));
+    p.unit_mode = 0;
+    p.counters = static_cast<unsigned int*>(workspace);
+    p.rec_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + cb);
+    p.rec_ml = p.rec_o + static_cast<size_t>(G2) * 2 * 2 * mla::kHeads * mla::kHalf;
+  } else {
+    p.unit_mode = 1;
+    G2 = batch;
+  }
+  cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(mla)");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mla::mla_decode_kernel<<<2 * G2, mla::kThreads, smem, st>>>(tq, tc, p);
+  return finish_call(st);
 }
 
 }  // extern "C"
