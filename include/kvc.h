@@ -20,8 +20,11 @@
  *     this boundary. kvc_last_error_message() gives a one-line reason for
  *     the most recent failure on the calling thread.
  *   - Device pointers are plain CUDA device addresses on the current device.
- *     The caller owns every buffer; the library never allocates, frees or
- *     retains device memory, and keeps no pointer after a call returns.
+ *     The caller owns every buffer it passes; the library never allocates,
+ *     frees or retains device memory at run time and keeps no pointer after a
+ *     call returns. The only device memory of its own is static: a 4-byte
+ *     error word and the 8 MiB scratch of kvc_decode_attention_static, per
+ *     device that loads the library.
  *   - Compute calls are asynchronous on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) unless checked mode is on.
  *   - Arguments are validated on the host first (KVC_ERR_INVALID_ARG,
@@ -160,6 +163,36 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
                                 int batch, float scale, int n_q_heads, int n_kv_heads, int head_dim,
                                 int block_size, int64_t num_blocks, kvc_dtype dtype, void* out,
                                 kvc_dtype out_dtype, void* workspace, size_t workspace_bytes, kvc_stream stream);
+
+/* kvc_decode_attention for callers that cannot allocate device memory.
+ *
+ * There is no counterpart of this call on the source pages: it exists for
+ * callers that must not or cannot allocate on the decode path, such as a
+ * plugin that only receives its input and output buffers from a host
+ * framework, code running under a fixed device-memory budget or an allocator
+ * lock, or plain C code with no allocator of its own. It computes exactly what
+ * kvc_decode_attention computes (same arguments, minus the workspace) and
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *
+ * Its split-K scratch is one fixed 8 MiB array inside the library, reserved
+ * on every device that loads the library and held until the process exits.
+ * Shapes whose kvc_decode_workspace_size exceeds 8 MiB are refused with
+ * KVC_ERR_WORKSPACE and a message giving both sizes (use kvc_decode_attention
+ * with your own workspace for those).
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture. Every call then clears the counters at the start
+ * of the array with an asynchronous memset on `stream`; the array keeps the
+ * rest of the last call's contents. All calls share the one array, so calls
+ * whose kernels may overlap on the GPU (different streams, or several host
+ * threads) race: serialise them, or use kvc_decode_attention with one
+ * workspace per stream. */
+kvc_status kvc_decode_attention_static(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                       const int32_t* context_lens, int batch, float scale, int n_q_heads,
+                                       int n_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                       kvc_dtype dtype, void* out, kvc_dtype out_dtype, kvc_stream stream);
 
 /* Scratch bytes for kvc_decode_attention_mla on the current device. */
 kvc_status kvc_decode_mla_workspace_size(int batch, int n_q_heads, int d_c, int d_r, int block_size,

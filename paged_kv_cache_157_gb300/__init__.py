@@ -18,7 +18,7 @@ import threading
 
 __all__ = [
     "KvcError", "KvcLibraryMissing", "raw", "lib_path", "symbols",
-    "append", "append_latent", "decode_workspace_size", "decode_attention",
+    "append", "append_latent", "decode_workspace_size", "decode_attention", "decode_attention_static",
     "decode_mla_workspace_size", "decode_attention_mla", "set_option", "get_option",
     "get_error_flags", "BlockPool", "slots_from_tables",
     "F32", "F16", "BF16", "FLAG_BAD_BLOCK", "FLAG_BAD_LEN", "FLAG_BAD_SLOT", "FLAG_TIMEOUT", "FLAG_WORKSPACE",
@@ -58,6 +58,8 @@ SIGNATURES = {
     "kvc_decode_workspace_size": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _szp]),
     "kvc_decode_attention": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32, _i64, _i32,
                                     _vp, _i32, _vp, _sz, _vp]),
+    "kvc_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32, _i64,
+                                           _i32, _vp, _i32, _vp]),
     "kvc_decode_mla_workspace_size": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _szp]),
     "kvc_decode_attention_mla": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32, _i64, _i32, _vp,
                                         _i32, _vp, _sz, _vp]),
@@ -238,6 +240,25 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out
                                       block_tables.shape[1], _ptr(context_lens), B, float(scale), hq, hkv, d, bs, nb,
                                       _dtype_code(k_cache), _ptr(out), _dtype_code(out), ws_ptr, ws_bytes,
                                       _stream(stream)), "kvc_decode_attention")
+
+
+def decode_attention_static(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None):
+    """kvc_decode_attention_static: the same decode with the library's built-in scratch, for callers that
+    cannot allocate device memory (see include/kvc.h). Calls that may overlap on the GPU must not be issued
+    concurrently: they share one scratch array."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
+        _require(t, n)
+    _require(block_tables, "block_tables", torch.int32)
+    _require(context_lens, "context_lens", torch.int32)
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if d2 != d or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("shape mismatch")
+    _check(raw().kvc_decode_attention_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                             block_tables.shape[1], _ptr(context_lens), B, float(scale), hq, hkv, d,
+                                             bs, nb, _dtype_code(k_cache), _ptr(out), _dtype_code(out),
+                                             _stream(stream)), "kvc_decode_attention_static")
 
 
 def decode_mla_workspace_size(batch, n_q_heads, d_c, d_r, block_size, max_blocks_per_seq) -> int:

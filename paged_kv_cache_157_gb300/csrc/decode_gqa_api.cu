@@ -5,6 +5,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
+#include <vector>
 
 #include "decode_gqa.h"
 
@@ -192,6 +194,86 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
   }
   if (s != KVC_OK) return s;
   return finish_call(st);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------
+// Decode without any caller-provided scratch.
+//
+// Some callers cannot allocate device memory at the moment they decode: a
+// plugin or runtime that only receives pre-allocated input and output buffers
+// from its host framework, code that must not touch the allocator on the
+// decode path (fixed memory budgets, allocator locks), or a C caller that
+// has no CUDA allocator of its own. For them the split-K scratch lives in the
+// library itself: one fixed array per device, reserved when the library is
+// loaded and held until the process exits.
+
+namespace kvc {
+namespace {
+
+constexpr size_t kStaticScratchBytes = 8u << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mutex;
+std::vector<void*> g_static_ptr;  // device address of g_decode_scratch, per device
+
+// Looks up (once per device, with that device current) the device address of
+// the scratch array. Host code must not use the symbol itself as a pointer.
+kvc_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (dev >= static_cast<int>(g_static_ptr.size())) g_static_ptr.resize(dev + 1, nullptr);
+  if (g_static_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+    g_static_ptr[dev] = ptr;
+  }
+  *out = g_static_ptr[dev];
+  return KVC_OK;
+}
+
+}  // namespace
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_decode_attention_static(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                       const int32_t* context_lens, int batch, float scale, int n_q_heads,
+                                       int n_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                       kvc_dtype dtype, void* out, kvc_dtype out_dtype, kvc_stream stream) {
+  using namespace kvc;
+  clear_error();
+  if (!dtype_ok(dtype) || !dtype_ok(out_dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype");
+  size_t need = 0;
+  kvc_status s = kvc_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                           &need);
+  if (s != KVC_OK) return s;
+  if (need > kStaticScratchBytes)
+    return fail(KVC_ERR_WORKSPACE,
+                "these shapes need %zu bytes of decode scratch; the built-in scratch holds %zu bytes "
+                "(use kvc_decode_attention with a caller-provided workspace)",
+                need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  if ((s = static_scratch(&scratch)) != KVC_OK) return s;
+  // The array keeps the previous call's contents; only the per-unit counters
+  // at its start must be zero on entry.
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != KVC_OK) return s;
+  GqaPlan pl;
+  if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, static_cast<int>(dtype_size(dtype)),
+                     dev->max_smem_optin, &pl)) != KVC_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(scratch, 0, counter_bytes(pl), st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(decode scratch counters)");
+  return kvc_decode_attention(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale,
+                              n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, dtype, out, out_dtype, scratch,
+                              kStaticScratchBytes, stream);
 }
 
 }  // extern "C"

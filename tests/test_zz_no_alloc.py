@@ -1,0 +1,71 @@
+"""GPU: kvc_decode_attention_static, the decode entry point that allocates nothing.
+
+It exists for callers that cannot allocate device memory on the decode path
+(a plugin handed only its buffers, a fixed memory budget, plain C without an
+allocator). It must give the same results as kvc_decode_attention with a
+caller-provided workspace, on consecutive calls (the built-in scratch keeps
+the previous call's contents). This file is named to run after every other
+test file.
+"""
+
+import ctypes
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_157_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _c_abi_static(kvc, dev, scale, out):
+    lib = kvc.raw()
+    B, hq, d = dev["q"].shape
+    nb, hkv, bs, _ = dev["k_cache"].shape
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return lib.kvc_decode_attention_static(p(dev["q"]), p(dev["k_cache"]), p(dev["v_cache"]), p(dev["block_tables"]),
+                                           dev["block_tables"].shape[1], p(dev["context_lens"]), B, scale, hq, hkv,
+                                           d, bs, nb, kvc.BF16, p(out), kvc.F32, stream)
+
+
+def _reference(kvc, dev, scale):
+    B, hq, d = dev["q"].shape
+    _, hkv, bs, _ = dev["k_cache"].shape
+    ws = kvc.new_decode_workspace(B, hq, hkv, d, bs, dev["block_tables"].shape[1])
+    out = torch.empty((B, hq, d), device="cuda")
+    kvc.decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"], scale,
+                         out, ws)
+    return out
+
+
+def test_static_scratch_matches_workspace_path_twice(kvc):
+    for o in (kvc.OPT_BLOCKS_PER_CTA, kvc.OPT_MAX_CTAS, kvc.OPT_CHECKED):
+        kvc.set_option(o, 0)
+    scale = 1.0 / math.sqrt(128)
+    cases = [W.gqa_case(32, 32, 8, 128, 16, (512, 4096), "bf16", seed=43),
+             W.gqa_case(5, 32, 8, 128, 16, [1, 17, 300, 2000, 64], "bf16", seed=44)]
+    for case in cases:  # two calls in a row, different shapes, same scratch
+        dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in case.items()}
+        ref = _reference(kvc, dev, scale)
+        out = torch.full_like(ref, float("nan"))
+        assert _c_abi_static(kvc, dev, scale, out) == kvc.OK, kvc.raw().kvc_last_error_message()
+        torch.cuda.synchronize()
+        err = float((out - ref).abs().max())
+        assert err <= 2e-3, err
+        assert kvc.get_error_flags() == 0
+
+
+def test_static_scratch_refuses_oversized_shapes(kvc):
+    kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, 1)  # one cache block per CTA: far more records than 8 MiB hold
+    try:
+        case = W.gqa_case(8, 32, 8, 128, 16, [4096] * 8, "bf16", seed=45)
+        dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in case.items()}
+        out = torch.empty((8, 32, 128), device="cuda")
+        status = _c_abi_static(kvc, dev, 0.1, out)
+        assert status == kvc.ERR_WORKSPACE
+        assert b"built-in scratch" in kvc.raw().kvc_last_error_message()
+    finally:
+        kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, 0)
