@@ -288,21 +288,18 @@ def oracle_sample_seconds(case, seqs, units=None):
     return dt, dec + app
 
 
-def cpu_baseline(case, budget_s=12.0):
-    """Oracle GB/s on a growing sample of whole sequences (about budget_s of CPU work)."""
+def cpu_baseline(case, budget_s=10.0):
+    """Oracle GB/s on whole sequences of the workload, cycling over the batch until about budget_s of CPU work."""
     B = case["q"].shape[0]
-    seqs, tot_t, tot_b = [], 0.0, 0
-    i = 0
-    while tot_t < budget_s and i < B:
-        dt, by = oracle_sample_seconds(case, [i])
+    n_done, tot_t, tot_b = 0, 0.0, 0
+    while tot_t < budget_s and n_done < 50 * B:
+        dt, by = oracle_sample_seconds(case, [n_done % B])
         tot_t += dt
         tot_b += by
-        seqs.append(i)
-        i += 1
+        n_done += 1
     return {"value": round(tot_b / tot_t / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"append + decode of sequences 0..{len(seqs) - 1} of the same workload "
-                      f"({len(seqs)} of {B} sequences, all heads), float64 NumPy, single thread; "
-                      f"{tot_t:.1f} s"}
+            "sample": f"append + decode of {n_done} whole sequences (all heads) of the same workload, cycling "
+                      f"over its {B} sequences, float64 NumPy, single thread; {tot_t:.1f} s"}
 
 
 # --------------------------------------------------------------- variants
@@ -324,34 +321,46 @@ def measure_gqa_case(kvc, case, steps, warmup, flush, unique_rows=None):
     return res
 
 
-def variants(kvc, flush, steps):
+def run_variant(kvc, name, flush, steps):
     import torch
     from paged_kv_cache_157_gb300 import workloads as W
-    out = {}
-    try:
+    if name == "gqa_b32_ctx4096":
         c = W.gqa_case(32, 32, 8, 128, 16, [4096] * 32, "bf16", 43, device="cuda")
-        out["gqa_b32_ctx4096"] = measure_gqa_case(kvc, c, steps, 5, flush)
-        del c
+        return measure_gqa_case(kvc, c, steps, 5, flush)
+    if name == "mha_shared_prefix_8x8":
         c = W.shared_case(8, 8, 2048, 256, 32, 128, 16, "f16", 44, device="cuda")
         unique = 8 * 2048 + 64 * 256
         r = measure_gqa_case(kvc, c, steps, 5, flush, unique_rows=unique)
         logical, _ = step_bytes(c["context_lens"].tolist(), 32, 32, 128, 16, 2, 2)
         r["logical_decode_bytes"] = logical
         r["note"] = "gbps counts each shared prompt block once (unique physical bytes)"
-        out["mha_shared_prefix_8x8"] = r
-        del c
+        return r
+    if name == "gqa_long_splitk":
         c = W.gqa_case(4, 64, 8, 128, 16, [32768, 65536, 131072, 131072], "bf16", 45, device="cuda")
-        out["gqa_long_splitk"] = measure_gqa_case(kvc, c, max(5, steps // 4), 3, flush)
-        del c
-        torch.cuda.empty_cache()
+        return measure_gqa_case(kvc, c, max(5, steps // 4), 3, flush)
+    if name == "gqa_ragged_17_31_32":
         c = W.gqa_case(3, 64, 8, 128, 16, [17, 31, 32], "bf16", 45, device="cuda")
-        out["gqa_ragged_17_31_32"] = measure_gqa_case(kvc, c, steps, 5, flush)
-        del c
-        out["tiny_mha_fp32"] = measure_tiny(kvc, flush, steps)
-        out["mla_deepseek_v2"] = measure_mla(kvc, flush, steps)
-    except Exception as e:  # report, do not hide, a failing variant
-        out["error"] = f"{type(e).__name__}: {e}"
-    torch.cuda.empty_cache()
+        return measure_gqa_case(kvc, c, steps, 5, flush)
+    if name == "tiny_mha_fp32":
+        return measure_tiny(kvc, flush, steps)
+    if name == "mla_deepseek_v2":
+        return measure_mla(kvc, flush, steps)
+    raise ValueError(f"unknown workload {name}")
+
+
+VARIANTS = ("gqa_b32_ctx4096", "mha_shared_prefix_8x8", "gqa_long_splitk", "gqa_ragged_17_31_32", "tiny_mha_fp32",
+            "mla_deepseek_v2")
+
+
+def variants(kvc, flush, steps):
+    import torch
+    out = {}
+    for name in VARIANTS:
+        try:
+            out[name] = run_variant(kvc, name, flush, steps)
+        except Exception as e:  # report, do not hide, a failing variant
+            out[name] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
     return out
 
 
@@ -565,9 +574,18 @@ def main():
     ap.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=("main",) + VARIANTS, default="main",
+                    help="time one other workload alone (prints its measurement, not the contract line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload != "main":
+        import paged_kv_cache_157_gb300 as kvc
+        from paged_kv_cache_157_gb300 import build_lib
+        build_lib.build()
+        print(json.dumps({"workload": args.workload,
+                          **run_variant(kvc, args.workload, flush_buffer(), args.steps)}), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
