@@ -39,10 +39,15 @@ def nvcc() -> str:
     return exe
 
 
+def _extra_flags():
+    """Extra nvcc flags from KVC_NVCC_FLAGS (space separated), e.g. tuning macros."""
+    return os.environ.get("KVC_NVCC_FLAGS", "").split()
+
+
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
     cmd = [nvcc(), *ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-           "--expt-relaxed-constexpr", "-c", os.path.join(CSRC, src), "-o", obj]
+           "--expt-relaxed-constexpr", *_extra_flags(), "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)

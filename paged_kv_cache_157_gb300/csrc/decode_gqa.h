@@ -36,8 +36,21 @@ struct GqaParams {
   float qscale;   // scale * log2(e)
 };
 
-constexpr int kGqaWarps = 4;
+#ifndef KVC_GQA_PAIR_WARPS
+#define KVC_GQA_PAIR_WARPS 1
+#endif
+#ifndef KVC_GQA_WARPS
+#define KVC_GQA_WARPS 8
+#endif
+constexpr int kGqaWarps = KVC_GQA_WARPS;  // warps per CTA
 constexpr float kNegInf = -__builtin_huge_valf();
+
+// A unit's GH query heads are split over HW warps that share one stream of
+// K/V pages; each warp holds GH / HW heads. KVC_GQA_PAIR_WARPS selects
+// whether head groups of 2 or more are split over a warp pair (1) or kept in
+// one warp (0).
+__host__ __device__ constexpr int gqa_warps_per_stream(int GH) { return (KVC_GQA_PAIR_WARPS && GH >= 2) ? 2 : 1; }
+__host__ __device__ constexpr int gqa_streams(int GH) { return kGqaWarps / gqa_warps_per_stream(GH); }
 
 // Shared-memory carve-up, identical on host and device.
 struct GqaSmem {
@@ -50,11 +63,12 @@ __host__ __device__ inline GqaSmem gqa_smem_layout(int elt_bytes, int D, int GH,
                                                   int batch) {
   GqaSmem s;
   const size_t page = static_cast<size_t>(block_size) * D * elt_bytes;
+  const size_t np = static_cast<size_t>(gqa_streams(GH));
   s.stage_off = 0;
-  s.bar_off = align_up(s.stage_off + static_cast<size_t>(kGqaWarps) * stages * 2 * page, 16);
-  s.o_off = align_up(s.bar_off + static_cast<size_t>(kGqaWarps) * stages * 8, 16);
-  s.ml_off = s.o_off + static_cast<size_t>(kGqaWarps) * GH * D * 4;
-  s.scan_off = align_up(s.ml_off + static_cast<size_t>(kGqaWarps) * GH * 2 * 4, 16);
+  s.bar_off = align_up(s.stage_off + np * stages * 2 * page, 16);
+  s.o_off = align_up(s.bar_off + np * stages * 2 * 8, 16);  // full and empty barrier per stage
+  s.ml_off = s.o_off + np * GH * D * 4;                      // per stream: GH heads x D
+  s.scan_off = align_up(s.ml_off + np * GH * 2 * 4, 16);
   s.total = s.scan_off + static_cast<size_t>(batch + 1 + 32) * 4;
   return s;
 }

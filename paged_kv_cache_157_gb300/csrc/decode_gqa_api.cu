@@ -37,7 +37,7 @@ kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, in
   pl->n_hsub = group / pl->GH;
   pl->units = static_cast<int64_t>(n_kv_heads) * batch * pl->n_hsub;
   const size_t stage = 2ull * bs * D * elt;
-  int S = static_cast<int>(kStageBudget / (kGqaWarps * stage));
+  int S = static_cast<int>(kStageBudget / (gqa_streams(pl->GH) * stage));
   S = std::max(1, std::min(S, 8));
   GqaSmem L = gqa_smem_layout(elt, D, pl->GH, bs, S, batch);
   while (S > 1 && L.total > static_cast<size_t>(max_smem)) L = gqa_smem_layout(elt, D, pl->GH, bs, --S, batch);

@@ -8,7 +8,9 @@
 //
 // How (sm_103a):
 // * Work unit = (kv head, sequence, head subgroup of GH <= 4 query heads).
-//   All GH query heads of a unit share every K/V page that is loaded.
+//   All GH query heads of a unit share every K/V page that is loaded. A
+//   stream of pages is consumed by one warp (or, as a build option, by a warp
+//   pair that splits the heads).
 // * Balanced split: the cache blocks of all units are laid end to end
 //   (kv head major, then sequence, then subgroup, so units that read the
 //   same pages sit next to each other) and CTA c takes blocks
@@ -17,9 +19,11 @@
 //   CTA that touched it; the last of those CTAs to finish (a counter per unit
 //   in the workspace, reset to zero by that CTA) merges the records with the
 //   log-sum-exp rule. No CTA ever waits for another.
-// * Each warp streams its own pages: lane 0 issues 1-D bulk copies (TMA) of
-//   the K page and V page of a block into a per-warp ring of shared-memory
-//   stages, completion counted on an mbarrier; every wait is bounded.
+// * Each stream has its own ring of shared-memory stages: lane 0 of its
+//   first warp issues 1-D bulk copies (TMA) of the K page and V page of a
+//   block, completion counted on a "full" mbarrier (with a warp pair, both
+//   warps release a stage on an "empty" mbarrier before it is refilled);
+//   every wait is bounded. Stage and phase advance incrementally per tile.
 // * Per 16-row tile a lane owns 16 (or 8) head dimensions of TL-strided rows.
 //   Products use the packed fp32x2 FMA of sm_100+ (two fp32 lanes per
 //   instruction, an IEEE fma in each). Partial dot products are reduced across
@@ -37,7 +41,6 @@ namespace kvc {
 
 template <typename T, int D, int GH>
 struct GqaCfg {
-  static constexpr int NW = kGqaWarps;
   static constexpr int DPL = (D >= 64) ? 16 : 8;  // dims per lane
   static constexpr int DP2 = DPL / 2;               // fp32 pairs per lane
   static constexpr int DL = D / DPL;                // lanes per row
@@ -315,18 +318,23 @@ __device__ void merge_records(const GqaParams& p, int D, int64_t u0, int64_t c0,
 }
 
 template <typename T, int D, int GH>
-__global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaParams p) {
-  using C = GqaCfg<T, D, GH>;
+__global__ void __launch_bounds__(kGqaWarps * 32, 2) gqa_decode_kernel(const GqaParams p) {
+  constexpr int HW = gqa_warps_per_stream(GH);  // warps sharing one page stream
+  constexpr int GW = GH / HW;                    // query heads per warp
+  constexpr int NP = kGqaWarps / HW;             // page streams per CTA
+  using C = GqaCfg<T, D, GW>;
   extern __shared__ __align__(128) unsigned char smem[];
   const GqaSmem L = gqa_smem_layout(sizeof(T), D, GH, p.block_size, p.stages, p.batch);
   T* s_stage = reinterpret_cast<T*>(smem + L.stage_off);
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + L.bar_off);
-  float* s_o = reinterpret_cast<float*>(smem + L.o_off);
-  float* s_ml = reinterpret_cast<float*>(smem + L.ml_off);
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + L.bar_off);  // [NP * S] full, then [NP * S] empty
+  float* s_o = reinterpret_cast<float*>(smem + L.o_off);              // [kGqaWarps][GW][D]
+  float* s_ml = reinterpret_cast<float*>(smem + L.ml_off);            // [kGqaWarps][GW][2]
   int* s_scan = reinterpret_cast<int*>(smem + L.scan_off);
   __shared__ int s_last;
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int sp = w / HW, hw = w % HW;  // page stream of this warp, and its half of the heads
+  const bool issuer = (hw == 0);       // lane 0 of the stream's first warp issues the copies
   const int tq = lane / C::DL, dq = lane % C::DL;
   const int base_i = C::NV >= C::DL ? C::NVF * dq : dq / C::DUP;
   const int h_lane = base_i / C::RT;
@@ -338,7 +346,10 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
   const T* kc = static_cast<const T*>(p.k_cache);
   const T* vc = static_cast<const T*>(p.v_cache);
 
-  if (tid < kGqaWarps * S) mbar_init(s_bar + tid, 1);
+  if (tid < NP * S) {
+    mbar_init(s_bar + tid, 1);               // full: one arrive (with the copy bytes)
+    mbar_init(s_bar + NP * S + tid, HW);     // empty: every warp of the stream releases
+  }
   fence_barrier_init();
 
   // Block range of this CTA.
@@ -372,7 +383,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
   }
 
   const uint64_t pol = policy_evict_first();
-  uint32_t ticket = 0;  // tiles consumed by this warp so far (stage/parity bookkeeping)
+  uint32_t ticket = 0;  // tiles of this stream consumed so far (stage/parity bookkeeping)
   bool aborted = false;
 
   for (int64_t gb = lo; gb < hi;) {
@@ -406,7 +417,8 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
     const int which = (gb == lo) ? 0 : 1;
     const int64_t u0 = gb - j0;  // global index of the unit's first block (split mode)
     gb = p.unit_mode ? hi : gb + seg_len;
-    const int h0 = kvh * p.group + hsub * GH;
+    const int h0 = kvh * p.group + hsub * GH;  // first query head of the unit
+    const int hq0 = h0 + hw * GW;              // first query head of this warp
     const int n_rows = seq_rows(p.context_lens, seq, bs, p.max_blocks);
 
     if (nb == 0) {
@@ -418,11 +430,11 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
     }
 
     // ---- per-warp state
-    WarpState<T, D, GH> st;
+    WarpState<T, D, GW> st;
     {
-      const T* qp = static_cast<const T*>(p.q) + (static_cast<int64_t>(seq) * p.n_q_heads + h0) * D;
+      const T* qp = static_cast<const T*>(p.q) + (static_cast<int64_t>(seq) * p.n_q_heads + hq0) * D;
 #pragma unroll
-      for (int h = 0; h < GH; ++h) {
+      for (int h = 0; h < GW; ++h) {
         float f[C::DPL];
 #pragma unroll
         for (int j = 0; j < C::NCH; ++j)
@@ -438,47 +450,58 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
       st.l = 0.f;
     }
 
-    const int nbw = seg_len > w ? (seg_len - w + kGqaWarps - 1) / kGqaWarps : 0;  // this warp's blocks
+    const int nbw = seg_len > sp ? (seg_len - sp + NP - 1) / NP : 0;  // this stream's blocks
     const int32_t* bt = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks;
-    T* wst = s_stage + static_cast<size_t>(w) * S * 2 * page_elems;
-    uint64_t* wbar = s_bar + w * S;
+    T* wst = s_stage + static_cast<size_t>(sp) * S * 2 * page_elems;
+    uint64_t* fbar = s_bar + sp * S;
+    uint64_t* ebar = s_bar + NP * S + sp * S;
 
-    // Block-table entries of this warp's tiles, 32 at a time: lane L holds the
-    // entry of tile 32*window + L (one coalesced load per window, issued a
-    // window ahead), handed to lane 0 by shuffles when it issues the copies.
+    // Block-table entries of this stream's tiles, 32 at a time: lane L holds
+    // the entry of tile 32*window + L (one coalesced load per window, issued a
+    // window ahead), handed to the issuing lane by shuffles.
     auto load_window = [&](int win) -> int {
       const int t = win * 32 + lane;
-      return t < nbw ? __ldg(bt + j0 + w + kGqaWarps * t) : -1;
+      return t < nbw ? __ldg(bt + j0 + sp + NP * t) : -1;
     };
     int bt_cur = load_window(0);
     int bt_nxt = nbw > 32 ? load_window(1) : -1;
 
-    auto issue = [&](int t, int phys) {
-      const int slot = (ticket + t) % S;
+    // Stage bookkeeping without divisions: tile t of this segment sits in
+    // stage `slot`, whose barriers are in phase parity `par`; both advance by
+    // one tile per iteration.
+    const int stage_elems = 2 * bs * D;
+    const int slot0 = static_cast<int>(ticket % static_cast<uint32_t>(S));
+    const uint32_t par0 = (ticket / static_cast<uint32_t>(S)) & 1u;
+
+    auto issue = [&](int slot, int phys) {
       if (phys < 0 || phys >= p.num_blocks) {
         set_flag(p.err, 0x1u);
-        mbar_arrive(wbar + slot);
+        mbar_arrive(fbar + slot);
       } else {
         const size_t src = (static_cast<size_t>(phys) * p.n_kv_heads + kvh) * page_elems;
-        mbar_arrive_expect_tx(wbar + slot, 2 * page_bytes);
-        bulk_g2s(wst + static_cast<size_t>(slot) * 2 * page_elems, kc + src, page_bytes, wbar + slot, pol);
-        bulk_g2s(wst + static_cast<size_t>(slot) * 2 * page_elems + page_elems, vc + src, page_bytes, wbar + slot,
-                 pol);
+        T* dst = wst + slot * stage_elems;
+        mbar_arrive_expect_tx(fbar + slot, 2 * page_bytes);
+        bulk_g2s(dst, kc + src, page_bytes, fbar + slot, pol);
+        bulk_g2s(dst + page_elems, vc + src, page_bytes, fbar + slot, pol);
       }
     };
 
-    if (!aborted) {
+    // All stages are free here: every warp finished the previous segment
+    // before the CTA-wide barrier that ended it.
+    if (!aborted && issuer) {
+      int sl = slot0;
       for (int t = 0; t < S && t < nbw; ++t) {
         const int ph = __shfl_sync(0xffffffffu, bt_cur, t);
-        if (lane == 0) issue(t, ph);
+        if (lane == 0) issue(sl, ph);
+        sl = (sl + 1 == S) ? 0 : sl + 1;
       }
     }
     __syncwarp();
 
     int drain_from = -1;  // first tile not consumed when a wait gave up
+    int slot = slot0;
+    uint32_t par = par0;
     for (int t = 0; t < nbw; ++t) {
-      const int slot = (ticket + t) % S;
-      const uint32_t parity = ((ticket + t) / S) & 1u;
       if (aborted) break;
       if (t > 0 && (t & 31) == 0) {
         bt_cur = bt_nxt;
@@ -487,38 +510,61 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
       const int phys = __shfl_sync(0xffffffffu, bt_cur, t & 31);
       const int tn = t + S;
       const int phys_next = __shfl_sync(0xffffffffu, (tn >> 5) == (t >> 5) ? bt_cur : bt_nxt, tn & 31);
-      const bool ok = mbar_wait_bounded(wbar + slot, parity);
+      const bool ok = mbar_wait_bounded(fbar + slot, par);
       if (__any_sync(0xffffffffu, !ok)) {
         aborted = true;
         drain_from = t;
         if (lane == 0) set_flag(p.err, 0x8u);
         break;
       }
-      const int j = j0 + w + kGqaWarps * t;
+      const int j = j0 + sp + NP * t;
       if (phys >= 0 && phys < p.num_blocks) {
-        const T* kp = wst + static_cast<size_t>(slot) * 2 * page_elems;
+        const T* kp = wst + slot * stage_elems;
         const T* vp = kp + page_elems;
         const int vr = min(bs, n_rows - j * bs);
-        for (int tt = 0; tt < tiles_per_page; ++tt) {
-          const int valid = vr - tt * 16;
-          if (valid <= 0) break;
-          if (valid >= 16)
-            gqa_tile<T, D, GH, false>(kp + tt * 16 * D, vp + tt * 16 * D, 16, st, tq, dq, lane, h_lane);
-          else
-            gqa_tile<T, D, GH, true>(kp + tt * 16 * D, vp + tt * 16 * D, valid, st, tq, dq, lane, h_lane);
+        if (vr >= bs) {
+          for (int tt = 0; tt < tiles_per_page; ++tt)
+            gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, 16, st, tq, dq, lane, h_lane);
+        } else {
+          for (int tt = 0; tt < tiles_per_page; ++tt) {
+            const int valid = vr - tt * 16;
+            if (valid <= 0) break;
+            if (valid >= 16)
+              gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, 16, st, tq, dq, lane, h_lane);
+            else
+              gqa_tile<T, D, GW, true>(kp + tt * 16 * D, vp + tt * 16 * D, valid, st, tq, dq, lane, h_lane);
+          }
         }
       }
       // Every shared-memory read of this stage fed an FMA issued before this
-      // point, so no read of it is outstanding when lane 0 refills it.
+      // point, so no read of it is outstanding once the warp releases it.
       __syncwarp();
-      if (lane == 0 && tn < nbw) issue(tn, phys_next);
+      if (HW > 1 && lane == 0) mbar_arrive(ebar + slot);
+      if (issuer && tn < nbw) {
+        if (HW > 1) {
+          // Refill once every warp of the stream has released the stage.
+          bool ok2 = true;
+          if (lane == 0) ok2 = mbar_wait_bounded(ebar + slot, par);
+          if (!__shfl_sync(0xffffffffu, ok2 ? 1 : 0, 0)) {
+            aborted = true;
+            drain_from = t + 1;
+            if (lane == 0) set_flag(p.err, 0x8u);
+            break;
+          }
+        }
+        if (lane == 0) issue(slot, phys_next);
+      }
       __syncwarp();
+      if (++slot == S) {
+        slot = 0;
+        par ^= 1u;
+      }
     }
-    if (drain_from >= 0) {
+    if (drain_from >= 0 && issuer) {
       // Copies issued but not consumed (at most S) must land before this
       // shared memory is reused or the CTA exits.
       for (int t = drain_from; t < nbw && t < drain_from + S; ++t)
-        (void)mbar_wait_bounded(wbar + (ticket + t) % S, ((ticket + t) / S) & 1u);
+        (void)mbar_wait_bounded(fbar + (ticket + t) % S, ((ticket + t) / S) & 1u);
     }
     ticket += nbw;
 
@@ -526,7 +572,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
 #pragma unroll
     for (int msk = C::DL; msk < 32; msk <<= 1) {
 #pragma unroll
-      for (int h = 0; h < GH; ++h) {
+      for (int h = 0; h < GW; ++h) {
 #pragma unroll
         for (int i = 0; i < C::DP2; ++i) {
           st.o[h][i].x += __shfl_xor_sync(0xffffffffu, st.o[h][i].x, msk);
@@ -534,45 +580,48 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
         }
       }
     }
-    float lw[GH];
+    float lw[GW];
 #pragma unroll
-    for (int hh = 0; hh < GH; ++hh) lw[hh] = warp_sum(h_lane == hh ? st.l : 0.f) * (1.0f / C::DUP);
+    for (int hh = 0; hh < GW; ++hh) lw[hh] = warp_sum(h_lane == hh ? st.l : 0.f) * (1.0f / C::DUP);
     if (tq == 0) {
 #pragma unroll
-      for (int h = 0; h < GH; ++h) {
+      for (int h = 0; h < GW; ++h) {
 #pragma unroll
         for (int j = 0; j < C::NCH; ++j) {
 #pragma unroll
           for (int e = 0; e < C::VEC; e += 2) {
             const float2 v = st.o[h][(j * C::VEC + e) / 2];
-            s_o[(w * GH + h) * D + (dq + C::DL * j) * C::VEC + e] = v.x;
-            s_o[(w * GH + h) * D + (dq + C::DL * j) * C::VEC + e + 1] = v.y;
+            s_o[(w * GW + h) * D + (dq + C::DL * j) * C::VEC + e] = v.x;
+            s_o[(w * GW + h) * D + (dq + C::DL * j) * C::VEC + e + 1] = v.y;
           }
         }
       }
     }
     if (lane == 0) {
 #pragma unroll
-      for (int h = 0; h < GH; ++h) {
-        s_ml[(w * GH + h) * 2] = st.m[h];
-        s_ml[(w * GH + h) * 2 + 1] = lw[h];
+      for (int h = 0; h < GW; ++h) {
+        s_ml[(w * GW + h) * 2] = st.m[h];
+        s_ml[(w * GW + h) * 2 + 1] = lw[h];
       }
     }
     __syncthreads();
     const int64_t rec = static_cast<int64_t>(blockIdx.x) * 2 + which;
     for (int idx = tid; idx < GH * D; idx += blockDim.x) {
       const int h = idx / D, d = idx - (idx / D) * D;
+      // head h of the unit lives in warp (stream, h / GW), slot h % GW
+      const int hw_h = h / GW, jh = h - hw_h * GW;
       float M = kNegInf;
 #pragma unroll
-      for (int ww = 0; ww < kGqaWarps; ++ww) M = fmaxf(M, s_ml[(ww * GH + h) * 2]);
+      for (int ss = 0; ss < NP; ++ss) M = fmaxf(M, s_ml[((ss * HW + hw_h) * GW + jh) * 2]);
       float Lsum = 0.f, O = 0.f;
 #pragma unroll
-      for (int ww = 0; ww < kGqaWarps; ++ww) {
-        const float mw = s_ml[(ww * GH + h) * 2];
+      for (int ss = 0; ss < NP; ++ss) {
+        const int r = (ss * HW + hw_h) * GW + jh;
+        const float mw = s_ml[r * 2];
         if (mw == kNegInf) continue;
         const float f = fast_exp2(mw - M);
-        Lsum += f * s_ml[(ww * GH + h) * 2 + 1];
-        O += f * s_o[(ww * GH + h) * D + d];
+        Lsum += f * s_ml[r * 2 + 1];
+        O += f * s_o[r * D + d];
       }
       if (whole) {
         store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + h0 + h) * D + d, O / Lsum, p.out_dtype);
@@ -606,7 +655,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32) gqa_decode_kernel(const GqaPar
       __syncthreads();
       if (s_last) {
         __threadfence();
-        merge_records<GH>(p, D, u0, c0, c1, G, N, seq, h0, reinterpret_cast<int*>(s_o), kGqaWarps * GH * D);
+        merge_records<GH>(p, D, u0, c0, c1, G, N, seq, h0, reinterpret_cast<int*>(s_o), NP * GH * D);
         if (tid == 0) p.counters[unit] = 0u;
       }
     }
