@@ -7,23 +7,28 @@
 //     o_h = sum_t a_t c_t[0 : d_c]      (d_c = 512)
 //
 // Design (sm_103a, one CTA per SM):
-// * A CTA works on 32-token tiles and one half (256) of the 512 output
+// * A CTA works on 64-token tiles and one half (256) of the 512 output
 //   dimensions; its partner CTA (adjacent in the grid) takes the other half of
 //   the same tiles, so the latent tile is fetched from HBM once and the second
 //   read is served by L2. Both compute S = Q~ C^T in full: the O half
-//   (128 x 256 fp32) plus two S buffers (128 x 32 fp32 each) fit the 512 TMEM
+//   (128 x 256 fp32), S (128 x 64 fp32), P and part of Q~ fit the 512 TMEM
 //   columns, which the whole O (128 x 512 fp32) alone would fill.
-// * Shared memory: Q~ [128 x 576] bf16 (147 KB) resident per sequence and two
-//   latent tile stages [32 x 576] (36 KB each),
+// * Q~ [128 x 576] bf16 is split: columns 0..255 sit in TMEM (128 columns of
+//   bf16 pairs, written by the softmax warps) and feed the first 16 K steps of
+//   S as the A operand from tensor memory; columns 256..575 sit in shared
+//   memory (80 KB). That leaves room for two latent tile stages [64 x 576]
+//   (72 KB each),
 //   in the 128B-swizzled K-major layout that TMA writes and the UMMA
 //   descriptors read.
 // * Warp roles: warps 0-3 = softmax and epilogue (thread = head = TMEM lane),
 //   warp 4 = TMA producer, warp 5 = MMA issuer and TMEM owner.
-//   Per tile: S(t) = Q~ C_t^T (36 MMAs, K = 16 each, N = 32) -> softmax reads S
+//   Per tile: S(t) = Q~ C_t^T (36 MMAs, K = 16 each, N = 64: a wider N than
+//   32 halves how often each MMA re-reads its 128 x 16 slice of Q~, which
+//   bounded the issue rate) -> softmax reads S
 //   from TMEM, updates the running max lazily (O in TMEM is rescaled only when
 //   the max grows by more than 2^8), writes P = exp2(s - m) into TMEM as two
 //   bf16 parts (hi = bf16(p), lo = bf16(p - hi), so hi + lo carries p to about
-//   2^-17) -> O += P_hi V_t + P_lo V_t (4 MMAs with A read from TMEM, N = 256,
+//   2^-17) -> O += P_hi V_t + P_lo V_t (8 MMAs with A read from TMEM, N = 256,
 //   V = the first 512 columns of the same tile, read MN-major). The MMA of S(t+1) is issued before PV(t) so the tensor
 //   core works while the softmax runs.
 // * Work split: as in the GQA kernel, the tiles of all sequences are laid end
@@ -52,23 +57,29 @@ constexpr int kHeads = 128;          // M of every MMA
 constexpr int kDc = 512;             // latent (value) width
 constexpr int kW = 576;              // cached row width
 constexpr int kKB = kW / 64;         // 64-element (128 B) K blocks of a row: 9
-constexpr int kTile = 32;            // tokens per tile (MMA N for S)
+constexpr int kTile = 64;            // tokens per tile (MMA N for S)
 constexpr int kHalf = kDc / 2;       // output dims per CTA: 256
 constexpr int kStages = 2;           // latent tile stages
+constexpr int kSBufs = 1;            // S buffers in TMEM (released as soon as the softmax has read S)
 constexpr int kThreads = 192;        // 6 warps
 constexpr int kMaxBatch = 256;
 
-constexpr uint32_t kQBytes = kHeads * kW * 2;        // 147456
-constexpr uint32_t kQSub = kHeads * 128;             // one 64-column block of Q~: 16384
-constexpr uint32_t kTileBytes = kTile * kW * 2;      // 36864
-constexpr uint32_t kTileSub = kTile * 128;           // one 64-column block of a tile: 4096
+// Q~ is split: columns [0, 256) live in TMEM (the A operand of the first 16
+// K steps), columns [256, 576) in shared memory (5 blocks of 64 columns).
+constexpr int kQTmemK = 256;                          // Q~ columns held in TMEM
+constexpr int kQSmemKB0 = kQTmemK / 64;               // first 64-column block in shared memory: 4
+constexpr uint32_t kQSub = kHeads * 128;              // one 64-column block of Q~: 16384
+constexpr uint32_t kQBytes = (kKB - kQSmemKB0) * kQSub;  // 81920
+constexpr uint32_t kTileBytes = kTile * kW * 2;      // 73728
+constexpr uint32_t kTileSub = kTile * 128;           // one 64-column block of a tile: 8192
 
-// TMEM columns: O half at 0..255, S buffers at 256 and 288, P at 320: the
-// high bf16 part of the weights (16 columns = 32 bf16 per head) then the low
-// part (336..351).
+// TMEM columns: O half at 0..255, S at 256..319, P at 320..383: the high
+// bf16 part of the weights (32 columns = 64 bf16 per head) then the low part;
+// Q~ columns 0..255 as bf16 pairs at 384..511.
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS = 256;
 constexpr uint32_t kColP = 320;
+constexpr uint32_t kColQ = 384;
 constexpr uint32_t kTmemCols = 512;
 
 // Shared memory carve-up (offsets from a 1024-byte aligned base).
@@ -77,14 +88,15 @@ constexpr uint32_t kOffC = kOffQ + kQBytes;
 constexpr uint32_t kOffBar = kOffC + kStages * kTileBytes;
 // barrier indices
 enum {
-  B_QFULL = 0, B_QEMPTY, B_CFULL0, B_CFULL1, B_CEMPTY0, B_CEMPTY1, B_SFULL0, B_SFULL1, B_SEMPTY0, B_SEMPTY1,
-  B_PFULL, B_PVDONE, B_OFREE, B_FINAL, B_COUNT
+  B_QFULL = 0, B_QEMPTY, B_CFULL0, B_CEMPTY0 = B_CFULL0 + kStages, B_SFULL0 = B_CEMPTY0 + kStages,
+  B_SEMPTY0 = B_SFULL0 + kSBufs, B_PFULL = B_SEMPTY0 + kSBufs, B_PVDONE, B_OFREE, B_FINAL, B_COUNT
 };
 constexpr uint32_t kOffMisc = kOffBar + B_COUNT * 8;  // tmem address, abort flag, last flag
 constexpr uint32_t kOffScan = kOffMisc + 16;
 constexpr uint32_t smem_bytes(int batch) { return kOffScan + (batch + 1 + 32) * 4 + 1024; }
 
 struct Params {
+  const __nv_bfloat16* q;  // absorbed queries [batch, 128, 576]
   const int32_t* block_tables;
   const int32_t* context_lens;
   void* out;
@@ -140,13 +152,29 @@ __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
+// Non-blocking probe of a phase (never suspends the thread).
+__device__ __forceinline__ bool test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted. It
+// spins on the non-blocking test: the hand-offs between roles are on the
+// critical path of every tile, so a suspended waiter would add its wake-up
+// latency to each of them.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            unsigned int* err) {
-  if (try_wait(bar, parity)) return true;
+  if (test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1; i < kWaitLimit; ++i) {
-    if (try_wait(bar, parity)) return true;
+    if (test_wait(bar, parity)) return true;
     if ((i & 31u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kWaitNs) break;
@@ -361,8 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     *s_abort = 0;
-    const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 1, 4, 1};
-    for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], counts[i]);
+    for (int i = 0; i < B_COUNT; ++i) {
+      // Q~ full: the producer's copy plus the four softmax warps' TMEM stores;
+      // S empty, P full and O free: the four softmax warps; all others: one.
+      uint32_t c = 1;
+      if (i == B_QFULL) c = 5;
+      if ((i >= B_SEMPTY0 && i < B_SEMPTY0 + kSBufs) || i == B_PFULL || i == B_OFREE) c = 4;
+      mbar_init(&bars[i], c);
+    }
     fence_barrier_init();
   }
   if (warp == 5) {
@@ -410,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t g = 0, seg_i = 0;
-      uint32_t issued[kStages] = {0, 0};
+      uint32_t issued[kStages] = {};
       bool q_pending = false;
       Segment sg;
       Walker w = walk;
@@ -418,13 +452,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (sg.ntiles == 0) continue;
         if (seg_i > 0 && !wait_phase(bar(B_QEMPTY), (seg_i - 1) & 1u, s_abort, p.err)) break;
         arrive_expect(bar(B_QFULL), kQBytes);
-        for (int kb = 0; kb < kKB; ++kb) tma_load_3d(sQ + kb * kQSub, &tm_q, kb * 64, 0, sg.seq, bar(B_QFULL));
+        for (int kb = kQSmemKB0; kb < kKB; ++kb)
+          tma_load_3d(sQ + (kb - kQSmemKB0) * kQSub, &tm_q, kb * 64, 0, sg.seq, bar(B_QFULL));
         q_pending = true;
         const int32_t* bt = p.block_tables + static_cast<int64_t>(sg.seq) * p.max_blocks;
         bool ok = true;
         for (int t = sg.t0; t < sg.t1; ++t, ++g) {
-          const int st = g & 1;
-          if (g >= kStages && !wait_phase(bar(B_CEMPTY0 + st), ((g >> 1) - 1) & 1u, s_abort, p.err)) {
+          const int st = g % kStages;
+          if (g >= kStages && !wait_phase(bar(B_CEMPTY0 + st), (g / kStages - 1) & 1u, s_abort, p.err)) {
             ok = false;
             break;
           }
@@ -464,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id_s = instr_desc(kHeads, kTile, 0, 0);
       const uint32_t id_pv = instr_desc(kHeads, kHalf, 0, 1);
+      const uint64_t a_q0 = smem_desc(sQ, 16, 1024, 2);
       uint32_t g = 0, seg_i = 0, pv_i = 0;
       Segment sg;
       Walker w = walk;
@@ -478,11 +514,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool first = (gi == g_first);
           if (first && seg_i > 0 && !wait_phase(bar(B_OFREE), (seg_i - 1) & 1u, s_abort, p.err)) return false;
           fence_after();
-          const uint32_t st = gi & 1u;
+          const uint32_t st = gi % kStages;
+          const uint64_t bv0 = smem_desc(sC + st * kTileBytes + (4 * hf) * kTileSub, kTileSub, 1024, 2);
+#pragma unroll
           for (int part = 0; part < 2; ++part) {  // P_hi, then P_lo, against the same V rows
+#pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks) {
-              const uint64_t b = smem_desc(sC + st * kTileBytes + (4 * hf) * kTileSub + ks * 2048, 4096, 1024, 2);
-              mma_bf16_ts(tmem + kColO, tmem + kColP + part * (kTile / 2) + ks * 8, b, id_pv,
+              mma_bf16_ts(tmem + kColO, tmem + kColP + part * (kTile / 2) + ks * 8, bv0 + ((ks * 2048) >> 4), id_pv,
                           (first && part == 0 && ks == 0) ? 0u : 1u);
             }
           }
@@ -492,20 +530,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         for (int t = sg.t0; t < sg.t1 && ok; ++t, ++g) {
-          const uint32_t st = g & 1u;
-          if (!wait_phase(bar(B_CFULL0 + st), (g >> 1) & 1u, s_abort, p.err)) { ok = false; break; }
-          if (g >= kStages && !wait_phase(bar(B_SEMPTY0 + st), ((g >> 1) - 1) & 1u, s_abort, p.err)) {
+          const uint32_t st = g % kStages;  // latent stage
+          const uint32_t sb = g % kSBufs;   // S buffer
+          if (!wait_phase(bar(B_CFULL0 + st), (g / kStages) & 1u, s_abort, p.err)) { ok = false; break; }
+          if (g >= kSBufs && !wait_phase(bar(B_SEMPTY0 + sb), (g / kSBufs - 1) & 1u, s_abort, p.err)) {
             ok = false;
             break;
           }
           fence_after();
-          for (int ks = 0; ks < kW / 16; ++ks) {
-            const int kb = ks >> 2, kin = ks & 3;
-            const uint64_t a = smem_desc(sQ + kb * kQSub + kin * 32, 16, 1024, 2);
-            const uint64_t b = smem_desc(sC + st * kTileBytes + kb * kTileSub + kin * 32, 16, 1024, 2);
-            mma_bf16(tmem + kColS + st * kTile, a, b, id_s, ks == 0 ? 0u : 1u);
+          {
+            // Descriptors advance by constant offsets (in 16-byte units) from
+            // one base per operand, so each K step costs one add.
+            const uint64_t b0 = smem_desc(sC + st * kTileBytes, 16, 1024, 2);
+            const uint32_t d_s = tmem + kColS + sb * kTile;
+#pragma unroll
+            for (int ks = 0; ks < kW / 16; ++ks) {
+              const int kb = ks >> 2, kin = ks & 3;
+              const uint64_t b = b0 + static_cast<uint64_t>((kb * kTileSub + kin * 32) >> 4);
+              if (ks < kQTmemK / 16) {
+                mma_bf16_ts(d_s, tmem + kColQ + ks * 8, b, id_s, ks == 0 ? 0u : 1u);
+              } else {
+                const uint64_t a = a_q0 + static_cast<uint64_t>(((kb - kQSmemKB0) * kQSub + kin * 32) >> 4);
+                mma_bf16(d_s, a, b, id_s, 1u);
+              }
+            }
           }
-          mma_commit(bar(B_SFULL0 + st));
+          mma_commit(bar(B_SFULL0 + sb));
           if (t == sg.t1 - 1) mma_commit(bar(B_QEMPTY));
           if (t > sg.t0 && !issue_pv(g - 1)) { ok = false; break; }
         }
@@ -529,17 +579,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && !*s_abort && w.next(p, s_scan, sg)) {
       if (sg.ntiles == 0) continue;
       const int n_rows = seq_rows(p.context_lens, sg.seq, p.block_size, p.max_blocks);
+      // Columns [0, 320) of this head's Q~ row go to TMEM (the A operand of the
+      // first 20 K steps of S), once the previous segment's S MMAs are done.
+      if (seg_i > 0 &&
+          !__all_sync(0xffffffffu, wait_phase(bar(B_QEMPTY), (seg_i - 1) & 1u, s_abort, p.err))) {
+        ok = false;
+        break;
+      }
+      fence_after();
+      {
+        const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(sg.seq) * kHeads + h) * kW);
+        for (int c = 0; c < kQTmemK / 2; c += 32) {
+          uint32_t r[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 x = __ldg(qrow + c / 4 + i);
+            r[4 * i] = x.x;
+            r[4 * i + 1] = x.y;
+            r[4 * i + 2] = x.z;
+            r[4 * i + 3] = x.w;
+          }
+          tmem_st32u(lane_addr + kColQ + c, r);
+        }
+      }
+      fence_before();
+      __syncwarp();
+      if (lane == 0) arrive(bar(B_QFULL));
       float m = -__builtin_huge_valf(), l = 0.f;
       const uint32_t g_first = g;
       for (int t = sg.t0; t < sg.t1; ++t, ++g) {
-        const uint32_t st = g & 1u;
-        if (!__all_sync(0xffffffffu, wait_phase(bar(B_SFULL0 + st), (g >> 1) & 1u, s_abort, p.err))) {
+        const uint32_t st = g % kSBufs;
+        if (!__all_sync(0xffffffffu, wait_phase(bar(B_SFULL0 + st), (g / kSBufs) & 1u, s_abort, p.err))) {
           ok = false;
           break;
         }
         fence_after();
         float s[kTile];
-        tmem_ld32(lane_addr + kColS + st * kTile, s);
+#pragma unroll
+        for (int c = 0; c < kTile; c += 32) tmem_ld32(lane_addr + kColS + st * kTile + c, s + c);
         fence_before();
         __syncwarp();
         if (lane == 0) arrive(bar(B_SEMPTY0 + st));
@@ -586,7 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[i] = hi;
           pk[kTile / 2 + i] = pack_bf16(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
         }
-        tmem_st32u(lane_addr + kColP, pk);
+#pragma unroll
+        for (int c = 0; c < kTile; c += 32) tmem_st32u(lane_addr + kColP + c, pk + c);
         fence_before();
         __syncwarp();
         if (lane == 0) arrive(bar(B_PFULL));
@@ -735,7 +813,7 @@ kvc_status check(int batch, int n_q_heads, int d_c, int d_r, int block_size, int
     return fail(KVC_ERR_UNSUPPORTED, "MLA decode supports n_q_heads 128, d_c 512, d_r 64 (got %d, %d, %d)",
                 n_q_heads, d_c, d_r);
   if (block_size % kTile != 0 || block_size > 256)
-    return fail(KVC_ERR_UNSUPPORTED, "MLA block_size must be a multiple of 32 up to 256 (got %d)", block_size);
+    return fail(KVC_ERR_UNSUPPORTED, "MLA block_size must be a multiple of 64 up to 256 (got %d)", block_size);
   if (batch > kMaxBatch) return fail(KVC_ERR_UNSUPPORTED, "MLA batch %d > %d", batch, kMaxBatch);
   return KVC_OK;
 }
@@ -813,6 +891,7 @@ kvc_status kvc_decode_attention_mla(const void* q_absorbed, const void* latent_c
   }
 
   mla::Params p{};
+  p.q = static_cast<const __nv_bfloat16*>(q_absorbed);
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.out = out;
