@@ -512,13 +512,13 @@ def run_kvc(args):
         "frac_of_8tbs": round(value / NOMINAL_HBM_GBS, 4),
         "seq_layer_steps_per_s": round(world * m["batch"] / (ms / 1e3), 1),
         "bytes_per_step": per_step,
-        "roofline": {"bound": "hbm", "kernel": "kvc_decode_attention (gqa_decode_kernel + gqa_merge_kernel)",
+        "roofline": {"bound": "hbm", "kernel": "kvc_decode_attention (gqa_decode_kernel, split-K merge fused in)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "traffic": traffic_from_profile(), "algorithmic_bytes_per_launch": dec_b},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,  # kvc_append + kvc_decode_attention per step
         "clocks": clocks,
         "timed_wall_s": round(wall, 4),
         "cpu_baseline": cpu,

@@ -23,7 +23,7 @@
  *     The caller owns every buffer it passes; the library never allocates,
  *     frees or retains device memory at run time and keeps no pointer after a
  *     call returns. The only device memory of its own is static: a 4-byte
- *     error word and the 8 MiB scratch of kvc_decode_attention_static, per
+ *     error word and the 16 MiB scratch of kvc_decode_attention_static, per
  *     device that loads the library.
  *   - Compute calls are asynchronous on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) unless checked mode is on.
@@ -174,9 +174,9 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
  * kvc_decode_attention computes (same arguments, minus the workspace) and
  * allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
  *
- * Its split-K scratch is one fixed 8 MiB array inside the library, reserved
+ * Its split-K scratch is one fixed 16 MiB array inside the library, reserved
  * on every device that loads the library and held until the process exits.
- * Shapes whose kvc_decode_workspace_size exceeds 8 MiB are refused with
+ * Shapes whose kvc_decode_workspace_size exceeds 16 MiB are refused with
  * KVC_ERR_WORKSPACE and a message giving both sizes (use kvc_decode_attention
  * with your own workspace for those).
  *

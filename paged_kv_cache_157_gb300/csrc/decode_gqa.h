@@ -18,9 +18,9 @@ struct GqaParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   void* out;
-  float* rec_o;   // [G*2, GH, D] partial outputs (stream mode)
-  float* rec_ml;  // [G*2, GH, 2] (max in log2 units, sum)
-  unsigned int* counters;  // [units] records seen per split unit; zero between calls
+  float* rec_o;   // [W*2, GH, D] partial outputs of the W workers (split mode)
+  float* rec_ml;  // [W*2, GH, 2] (max in log2 units, sum)
+  unsigned int* counters;  // [units, warps per stream] records seen per split unit; zero between calls
   unsigned int* err;
   int64_t num_blocks;
   int batch;
@@ -32,15 +32,15 @@ struct GqaParams {
   int max_blocks;
   int out_dtype;
   int stages;
-  int unit_mode;  // 1: CTA u handles unit u completely (no records)
+  int unit_mode;  // 1: worker u handles unit u completely (no records)
   float qscale;   // scale * log2(e)
 };
 
 #ifndef KVC_GQA_PAIR_WARPS
-#define KVC_GQA_PAIR_WARPS 1
+#define KVC_GQA_PAIR_WARPS 0
 #endif
 #ifndef KVC_GQA_WARPS
-#define KVC_GQA_WARPS 8
+#define KVC_GQA_WARPS 4
 #endif
 constexpr int kGqaWarps = KVC_GQA_WARPS;  // warps per CTA
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -49,26 +49,30 @@ constexpr float kNegInf = -__builtin_huge_valf();
 // K/V pages; each warp holds GH / HW heads. KVC_GQA_PAIR_WARPS selects
 // whether head groups of 2 or more are split over a warp pair (1) or kept in
 // one warp (0).
-__host__ __device__ constexpr int gqa_warps_per_stream(int GH) { return (KVC_GQA_PAIR_WARPS && GH >= 2) ? 2 : 1; }
+__host__ __device__ constexpr int gqa_warps_per_stream(int GH) {
+  return GH > 4 ? GH / 4 : ((KVC_GQA_PAIR_WARPS && GH >= 2) ? 2 : 1);
+}
 __host__ __device__ constexpr int gqa_streams(int GH) { return kGqaWarps / gqa_warps_per_stream(GH); }
 
-// Shared-memory carve-up, identical on host and device.
+// Shared-memory carve-up, identical on host and device. Each page stream
+// has `stages` stages of [K page][V page][the unit's GH query rows].
 struct GqaSmem {
-  size_t stage_off, bar_off, o_off, ml_off, scan_off, total;
+  size_t stage_off, bar_off, scan_off, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+__host__ __device__ inline size_t gqa_stage_bytes(int elt_bytes, int D, int GH, int block_size) {
+  return (2ull * block_size * D + static_cast<size_t>(GH) * D) * elt_bytes;
+}
+
 __host__ __device__ inline GqaSmem gqa_smem_layout(int elt_bytes, int D, int GH, int block_size, int stages,
                                                   int batch) {
   GqaSmem s;
-  const size_t page = static_cast<size_t>(block_size) * D * elt_bytes;
   const size_t np = static_cast<size_t>(gqa_streams(GH));
   s.stage_off = 0;
-  s.bar_off = align_up(s.stage_off + np * stages * 2 * page, 16);
-  s.o_off = align_up(s.bar_off + np * stages * 2 * 8, 16);  // full and empty barrier per stage
-  s.ml_off = s.o_off + np * GH * D * 4;                      // per stream: GH heads x D
-  s.scan_off = align_up(s.ml_off + np * GH * 2 * 4, 16);
+  s.bar_off = align_up(np * stages * gqa_stage_bytes(elt_bytes, D, GH, block_size), 16);
+  s.scan_off = align_up(s.bar_off + np * stages * 2 * 8, 16);  // full and empty barrier per stage
   s.total = s.scan_off + static_cast<size_t>(batch + 1 + 32) * 4;
   return s;
 }

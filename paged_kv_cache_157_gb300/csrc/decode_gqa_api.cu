@@ -14,30 +14,43 @@ namespace kvc {
 
 namespace {
 
-constexpr size_t kStageBudget = 100 * 1024;  // shared memory for K/V stages, aims at 2 CTAs per SM
+constexpr size_t kStageBudget = 108 * 1024;  // shared memory per CTA for stages + scan: 2 CTAs per SM
 constexpr int kMaxCtasPerSm = 4;
 constexpr int kMinBlocksPerCta = 2 * kGqaWarps;
 constexpr int kMaxBatch = 4096;
 
 struct GqaPlan {
-  int GH = 1, n_hsub = 1, stages = 2;
+  int GH = 1, n_hsub = 1, stages = 2, streams = 1;
   int64_t units = 0;
   size_t smem = 0;
-  size_t rec_bytes_per_cta = 0;
+  size_t rec_bytes_per_cta = 0;  // two records per page stream (worker)
 };
 
-// Workspace layout: [unit counters][record outputs][record (max, sum)].
-size_t counter_bytes(const GqaPlan& pl) { return align_up(static_cast<size_t>(pl.units) * 4, 256); }
+// Workspace layout: [unit counters, one per warp of a stream][record
+// outputs][record (max, sum)].
+size_t counter_bytes(const GqaPlan& pl) {
+  return align_up(static_cast<size_t>(pl.units) * gqa_warps_per_stream(pl.GH) * 4, 256);
+}
 
-int head_subgroup(int group) { return group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1); }
+// Query heads per unit: the largest power of two up to 16 that divides the
+// group. Up to 4 heads share one warp; 8 and 16 split over 2 and 4 warps that
+// consume one stream of pages, so each page is loaded once for all of them.
+int head_subgroup(int group) {
+  for (int gh = 16; gh > 1; gh >>= 1)
+    if (group % gh == 0) return gh;
+  return 1;
+}
 
 kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, int elt, int max_smem, GqaPlan* pl) {
   const int group = n_q_heads / n_kv_heads;
   pl->GH = head_subgroup(group);
   pl->n_hsub = group / pl->GH;
   pl->units = static_cast<int64_t>(n_kv_heads) * batch * pl->n_hsub;
-  const size_t stage = 2ull * bs * D * elt;
-  int S = static_cast<int>(kStageBudget / (gqa_streams(pl->GH) * stage));
+  pl->streams = gqa_streams(pl->GH);
+  const size_t stage = gqa_stage_bytes(elt, D, pl->GH, bs);
+  const size_t scan = static_cast<size_t>(batch + 1 + 32) * 4;
+  const size_t budget = kStageBudget > scan + 1024 ? kStageBudget - scan - 1024 : 0;
+  int S = static_cast<int>(budget / (pl->streams * stage));
   S = std::max(1, std::min(S, 8));
   GqaSmem L = gqa_smem_layout(elt, D, pl->GH, bs, S, batch);
   while (S > 1 && L.total > static_cast<size_t>(max_smem)) L = gqa_smem_layout(elt, D, pl->GH, bs, --S, batch);
@@ -46,7 +59,7 @@ kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, in
                 L.total, max_smem);
   pl->stages = S;
   pl->smem = L.total;
-  pl->rec_bytes_per_cta = 2ull * pl->GH * (D + 2) * sizeof(float);
+  pl->rec_bytes_per_cta = static_cast<size_t>(pl->streams) * 2 * pl->GH * (D + 2) * sizeof(float);
   return KVC_OK;
 }
 
@@ -79,6 +92,8 @@ kvc_status check_shapes(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
   if (batch > kMaxBatch) return fail(KVC_ERR_UNSUPPORTED, "batch %d > %d", batch, kMaxBatch);
   if (static_cast<int64_t>(max_blocks) * block_size > (1ll << 30))
     return fail(KVC_ERR_UNSUPPORTED, "max_blocks_per_seq x block_size too large");
+  if (static_cast<int64_t>(batch) * n_q_heads * head_dim >= (1ll << 31))
+    return fail(KVC_ERR_UNSUPPORTED, "batch x n_q_heads x head_dim must be below 2^31");
   return KVC_OK;
 }
 
@@ -179,13 +194,15 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
     p.unit_mode = 0;
     p.counters = static_cast<unsigned int*>(workspace);
     p.rec_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + cbytes);
-    p.rec_ml = p.rec_o + static_cast<size_t>(G) * 2 * pl.GH * head_dim;
+    p.rec_ml = p.rec_o + static_cast<size_t>(G) * pl.streams * 2 * pl.GH * head_dim;
     grid = static_cast<int>(G);
   } else {
     p.unit_mode = 1;
-    grid = static_cast<int>(pl.units);
+    grid = static_cast<int>((pl.units + pl.streams - 1) / pl.streams);
   }
   if (pl.units > (1ll << 31) - 1) return fail(KVC_ERR_UNSUPPORTED, "too many (sequence, head) units");
+  if (pl.units * max_blocks_per_seq / (static_cast<int64_t>(grid) * pl.streams) + 1 >= (1ll << 31))
+    return fail(KVC_ERR_UNSUPPORTED, "too many cache blocks per page stream");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (dtype) {
     case KVC_F32: s = gqa_dispatch<float>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr); break;
@@ -212,7 +229,7 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
 namespace kvc {
 namespace {
 
-constexpr size_t kStaticScratchBytes = 8u << 20;  // 8 MiB
+constexpr size_t kStaticScratchBytes = 16u << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 std::mutex g_static_mutex;

@@ -7,10 +7,11 @@
 // table (PagedAttention, "KV Cache（键值缓存）" section 2.3).
 //
 // How (sm_103a):
-// * Work unit = (kv head, sequence, head subgroup of GH <= 4 query heads).
+// * Work unit = (kv head, sequence, head subgroup of GH <= 16 query heads).
 //   All GH query heads of a unit share every K/V page that is loaded. A
-//   stream of pages is consumed by one warp (or, as a build option, by a warp
-//   pair that splits the heads).
+//   stream of pages is consumed by one warp holding up to 4 heads; 8 or 16
+//   heads split over 2 or 4 warps that consume the same stream (as a build
+//   option, 2 or 4 heads split over a warp pair too).
 // * Balanced split: the cache blocks of all units are laid end to end
 //   (kv head major, then sequence, then subgroup, so units that read the
 //   same pages sit next to each other) and CTA c takes blocks
@@ -260,60 +261,94 @@ __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __re
   }
 }
 
-// Merges the records that CTAs c0..c1 left for one unit (blocks starting at
-// global index u0) and writes the normalised output. Record ids are staged in
-// s_rec in chunks of `cap` CTAs; pass 0 finds the maxima, pass 1 sums.
-template <int GH>
-__device__ void merge_records(const GqaParams& p, int D, int64_t u0, int64_t c0, int64_t c1, int64_t G, int64_t N,
-                              int seq, int h0, int* s_rec, int cap) {
-  constexpr int kMaxOwned = 8;  // GH * D <= 8 * blockDim for GH <= 4, D <= 256, 128 threads
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int span = static_cast<int>(c1 - c0 + 1);
-  float M[GH];
+// Worker whose block range [w*N/W, (w+1)*N/W) contains global block b, and
+// the first block of worker w's range.
+__device__ __forceinline__ int64_t worker_of_block(int64_t b, int64_t W, int64_t N) { return ((b + 1) * W - 1) / N; }
+__device__ __forceinline__ int64_t worker_range_start(int64_t w, int64_t W, int64_t N) { return w * N / W; }
+
+// Global block index -> (kv head, sequence, head subgroup, block of the
+// sequence). Blocks are numbered kv head major, then sequence, then subgroup;
+// s_scan holds the exclusive prefix sums of the per-sequence block counts.
+struct BlockPos {
+  int kvh, seq, hsub, j, nb;
+};
+
+__device__ __forceinline__ BlockPos locate_block(int64_t gb, int64_t slab, const int* s_scan, int B, int n_hsub) {
+  BlockPos r;
+  r.kvh = static_cast<int>(gb / slab);
+  const int64_t rem = gb - r.kvh * slab;
+  int a = 0, b = B - 1;  // largest sequence with n_hsub * S[seq] <= rem (skips empty ones)
+  while (a < b) {
+    const int mid = (a + b + 1) >> 1;
+    if (static_cast<int64_t>(n_hsub) * s_scan[mid] <= rem) a = mid; else b = mid - 1;
+  }
+  r.seq = a;
+  r.nb = s_scan[a + 1] - s_scan[a];
+  const int r2 = static_cast<int>(rem - static_cast<int64_t>(n_hsub) * s_scan[a]);
+  r.hsub = r2 / r.nb;
+  r.j = r2 - r.hsub * r.nb;
+  return r;
+}
+
+// Record slot that worker c left for the unit whose first block is u0: 2c
+// if the unit's part in c starts at c's first block, else 2c + 1. Returns
+// -1 for a worker with an empty range (only when N < W).
+__device__ __forceinline__ int64_t record_of(int64_t c, int64_t c0, int64_t u0, int64_t f00, int64_t W, int64_t N) {
+  if (N >= W) return 2 * c + ((c == c0 && u0 > f00) ? 1 : 0);
+  const int64_t f0 = worker_range_start(c, W, N), f1 = worker_range_start(c + 1, W, N);
+  if (f0 == f1) return -1;
+  return 2 * c + (u0 > f0 ? 1 : 0);
+}
+
+// One warp merges, for its GW heads of a unit (first block u0, nb blocks),
+// the records of every worker that touched the unit, with the log-sum-exp
+// rule, and writes the normalised output. Lanes own dims lane + 32k.
+template <int D, int GH, int GW>
+__device__ void merge_unit_warp(const GqaParams& p, int64_t u0, int nb, int64_t W, int64_t N, int seq, int hq0,
+                                int hoff, int lane) {
+  constexpr int DK = D / 32;
+  const int64_t c0 = worker_of_block(u0, W, N), c1 = worker_of_block(u0 + nb - 1, W, N);
+  const int64_t f00 = worker_range_start(c0, W, N);
+  float M[GW];
 #pragma unroll
-  for (int h = 0; h < GH; ++h) M[h] = kNegInf;
-  float O[kMaxOwned], Ls[kMaxOwned];
+  for (int h = 0; h < GW; ++h) M[h] = kNegInf;
+  for (int64_t c = c0 + lane; c <= c1; c += 32) {
+    const int64_t rec = record_of(c, c0, u0, f00, W, N);
+    if (rec < 0) continue;
 #pragma unroll
-  for (int k = 0; k < kMaxOwned; ++k) O[k] = Ls[k] = 0.f;
-  for (int pass = 0; pass < 2; ++pass) {
-    for (int base = 0; base < span; base += cap) {
-      const int n = min(cap, span - base);
-      __syncthreads();
-      for (int t = tid; t < n; t += nt) {
-        const int64_t c = c0 + base + t;
-        const int64_t f0 = cta_range_start(c, G, N);
-        const int64_t f1 = cta_range_start(c + 1, G, N);
-        s_rec[t] = (f0 == f1) ? -1 : static_cast<int>(c * 2 + ((u0 > f0) ? 1 : 0));
-      }
-      __syncthreads();
-      for (int t = 0; t < n; ++t) {
-        const int64_t rec = s_rec[t];
-        if (rec < 0) continue;
-        if (pass == 0) {
+    for (int h = 0; h < GW; ++h) M[h] = fmaxf(M[h], __ldcg(p.rec_ml + (rec * GH + hoff + h) * 2));
+  }
 #pragma unroll
-          for (int h = 0; h < GH; ++h) M[h] = fmaxf(M[h], __ldcg(p.rec_ml + (rec * GH + h) * 2));
-        } else {
+  for (int h = 0; h < GW; ++h) M[h] = warp_max(M[h]);
+  float Ls[GW], O[GW][DK];
 #pragma unroll
-          for (int k = 0; k < kMaxOwned; ++k) {
-            const int idx = tid + k * nt;
-            if (idx >= GH * D) break;
-            const int h = idx / D, d = idx - (idx / D) * D;
-            const float mc = __ldcg(p.rec_ml + (rec * GH + h) * 2);
-            if (mc == kNegInf) continue;
-            const float f = fast_exp2(mc - select_head<GH>(M, h));
-            Ls[k] += f * __ldcg(p.rec_ml + (rec * GH + h) * 2 + 1);
-            O[k] += f * __ldcg(p.rec_o + (rec * GH + h) * D + d);
-          }
-        }
-      }
+  for (int h = 0; h < GW; ++h) {
+    Ls[h] = 0.f;
+#pragma unroll
+    for (int k = 0; k < DK; ++k) O[h][k] = 0.f;
+  }
+  for (int64_t c = c0; c <= c1; ++c) {
+    const int64_t rec = record_of(c, c0, u0, f00, W, N);
+    if (rec < 0) continue;
+#pragma unroll
+    for (int h = 0; h < GW; ++h) {
+      const float* ml = p.rec_ml + (rec * GH + hoff + h) * 2;
+      const float mc = __ldcg(ml);
+      if (mc == kNegInf) continue;
+      const float f = fast_exp2(mc - M[h]);
+      Ls[h] += f * __ldcg(ml + 1);
+      const float* o = p.rec_o + (rec * GH + hoff + h) * D + lane;
+#pragma unroll
+      for (int k = 0; k < DK; ++k) O[h][k] += f * __ldcg(o + 32 * k);
     }
   }
 #pragma unroll
-  for (int k = 0; k < kMaxOwned; ++k) {
-    const int idx = tid + k * nt;
-    if (idx >= GH * D) break;
-    const int h = idx / D, d = idx - (idx / D) * D;
-    store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + h0 + h) * D + d, O[k] / Ls[k], p.out_dtype);
+  for (int h = 0; h < GW; ++h) {
+    const float inv = 1.0f / Ls[h];
+#pragma unroll
+    for (int k = 0; k < DK; ++k)
+      store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + hq0 + h) * D + lane + 32 * k, O[h][k] * inv,
+                p.out_dtype);
   }
 }
 
@@ -321,19 +356,18 @@ template <typename T, int D, int GH>
 __global__ void __launch_bounds__(kGqaWarps * 32, 2) gqa_decode_kernel(const GqaParams p) {
   constexpr int HW = gqa_warps_per_stream(GH);  // warps sharing one page stream
   constexpr int GW = GH / HW;                    // query heads per warp
-  constexpr int NP = kGqaWarps / HW;             // page streams per CTA
+  constexpr int NP = kGqaWarps / HW;             // page streams (workers) per CTA
   using C = GqaCfg<T, D, GW>;
+  static_assert(GW * HW == GH && kGqaWarps % HW == 0, "head split over the warps of a stream");
+  static_assert(D % 32 == 0, "merge lanes own D / 32 dims");
   extern __shared__ __align__(128) unsigned char smem[];
   const GqaSmem L = gqa_smem_layout(sizeof(T), D, GH, p.block_size, p.stages, p.batch);
   T* s_stage = reinterpret_cast<T*>(smem + L.stage_off);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + L.bar_off);  // [NP * S] full, then [NP * S] empty
-  float* s_o = reinterpret_cast<float*>(smem + L.o_off);              // [kGqaWarps][GW][D]
-  float* s_ml = reinterpret_cast<float*>(smem + L.ml_off);            // [kGqaWarps][GW][2]
   int* s_scan = reinterpret_cast<int*>(smem + L.scan_off);
-  __shared__ int s_last;
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int sp = w / HW, hw = w % HW;  // page stream of this warp, and its half of the heads
+  const int sp = w / HW, hw = w % HW;  // stream (worker) of this warp, and its share of the heads
   const bool issuer = (hw == 0);       // lane 0 of the stream's first warp issues the copies
   const int tq = lane / C::DL, dq = lane % C::DL;
   const int base_i = C::NV >= C::DL ? C::NVF * dq : dq / C::DUP;
@@ -341,34 +375,29 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 2) gqa_decode_kernel(const Gqa
   const int bs = p.block_size, S = p.stages;
   const int B = p.batch;
   const int tiles_per_page = bs / 16;
-  const size_t page_elems = static_cast<size_t>(bs) * D;
+  const int page_elems = bs * D;
+  const int stage_elems = 2 * page_elems + GH * D;  // K page, V page, the unit's query rows
   const uint32_t page_bytes = static_cast<uint32_t>(page_elems * sizeof(T));
+  const uint32_t q_bytes = static_cast<uint32_t>(GH * D * sizeof(T));
   const T* kc = static_cast<const T*>(p.k_cache);
   const T* vc = static_cast<const T*>(p.v_cache);
+  const T* qg = static_cast<const T*>(p.q);
+  const uint32_t full = 0xffffffffu;
 
   if (tid < NP * S) {
-    mbar_init(s_bar + tid, 1);               // full: one arrive (with the copy bytes)
-    mbar_init(s_bar + NP * S + tid, HW);     // empty: every warp of the stream releases
+    mbar_init(s_bar + tid, 1);            // full: one arrive (with the copy bytes)
+    mbar_init(s_bar + NP * S + tid, HW);  // empty: every warp of the stream releases
   }
   fence_barrier_init();
+  scan_blocks(p.context_lens, B, bs, p.max_blocks, s_scan);  // ends with a CTA barrier
+  const int64_t slab = static_cast<int64_t>(p.n_hsub) * s_scan[B];
+  const int64_t N = slab * p.n_kv_heads;
+  const int64_t W = static_cast<int64_t>(gridDim.x) * NP;
+  const int64_t wk = static_cast<int64_t>(blockIdx.x) * NP + sp;
 
-  // Block range of this CTA.
-  int64_t lo, hi, slab = 0, N = 0;
-  const int64_t G = gridDim.x;
-  if (p.unit_mode) {
-    lo = 0;
-    hi = 1;
-    __syncthreads();
-  } else {
-    scan_blocks(p.context_lens, B, bs, p.max_blocks, s_scan);
-    slab = static_cast<int64_t>(p.n_hsub) * s_scan[B];
-    N = slab * p.n_kv_heads;
-    lo = cta_range_start(blockIdx.x, G, N);
-    hi = cta_range_start(blockIdx.x + 1, G, N);
-  }
   if (blockIdx.x == 0) {
     // Validate every length once; in the split mode CTA 0 also writes the
-    // zero outputs of sequences whose length is invalid (no CTA visits them).
+    // zero outputs of sequences whose length is invalid (no worker visits them).
     for (int b = tid; b < B; b += blockDim.x) {
       const int n = __ldg(p.context_lens + b);
       if (n < 1 || n > bs * p.max_blocks) set_flag(p.err, 0x2u);
@@ -381,147 +410,143 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 2) gqa_decode_kernel(const Gqa
       }
     }
   }
+  // No CTA-wide barrier below this point: every stream runs on its own.
 
-  const uint64_t pol = policy_evict_first();
-  uint32_t ticket = 0;  // tiles of this stream consumed so far (stage/parity bookkeeping)
-  bool aborted = false;
-
-  for (int64_t gb = lo; gb < hi;) {
-    // ---- locate the unit containing global block gb
-    int kvh, seq, hsub, j0, nb, seg_len;
-    if (p.unit_mode) {
-      const int u = blockIdx.x;
-      hsub = u % p.n_hsub;
-      seq = (u / p.n_hsub) % B;
-      kvh = u / (p.n_hsub * B);
-      nb = seq_blocks(p.context_lens, seq, bs, p.max_blocks);
-      j0 = 0;
-      seg_len = nb;
-    } else {
-      kvh = static_cast<int>(gb / slab);
-      const int64_t r = gb - kvh * slab;
-      int a = 0, b = B - 1;  // largest seq with n_hsub*S[seq] <= r
-      while (a < b) {
-        const int mid = (a + b + 1) >> 1;
-        if (static_cast<int64_t>(p.n_hsub) * s_scan[mid] <= r) a = mid; else b = mid - 1;
-      }
-      seq = a;
-      nb = s_scan[seq + 1] - s_scan[seq];
-      const int64_t r2 = r - static_cast<int64_t>(p.n_hsub) * s_scan[seq];
-      hsub = static_cast<int>(r2 / nb);
-      j0 = static_cast<int>(r2 - static_cast<int64_t>(hsub) * nb);
-      const int64_t left = nb - j0;
-      seg_len = static_cast<int>((hi - gb) < left ? (hi - gb) : left);
-    }
-    const bool whole = (j0 == 0 && seg_len == nb);
-    const int which = (gb == lo) ? 0 : 1;
-    const int64_t u0 = gb - j0;  // global index of the unit's first block (split mode)
-    gb = p.unit_mode ? hi : gb + seg_len;
-    const int h0 = kvh * p.group + hsub * GH;  // first query head of the unit
-    const int hq0 = h0 + hw * GW;              // first query head of this warp
-    const int n_rows = seq_rows(p.context_lens, seq, bs, p.max_blocks);
-
+  int64_t lo, hi;
+  if (p.unit_mode) {
+    // worker u takes unit u = (kv head, sequence, subgroup) whole
+    const int64_t units = static_cast<int64_t>(p.n_kv_heads) * B * p.n_hsub;
+    if (wk >= units) return;
+    const int hsub = static_cast<int>(wk % p.n_hsub);
+    const int seq = static_cast<int>((wk / p.n_hsub) % B);
+    const int kvh = static_cast<int>(wk / (static_cast<int64_t>(p.n_hsub) * B));
+    const int nb = s_scan[seq + 1] - s_scan[seq];
     if (nb == 0) {
-      // invalid length: zero output (only reachable in unit mode)
-      for (int idx = tid; idx < GH * D; idx += blockDim.x)
-        store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + h0 + idx / D) * D + idx % D, 0.f,
-                  p.out_dtype);
-      continue;
+      // invalid length: zero output for this warp's heads
+      const int hq0 = kvh * p.group + hsub * GH + hw * GW;
+      for (int idx = lane; idx < GW * D; idx += 32)
+        store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + hq0) * D + idx, 0.f, p.out_dtype);
+      return;
     }
+    lo = kvh * slab + static_cast<int64_t>(p.n_hsub) * s_scan[seq] + static_cast<int64_t>(hsub) * nb;
+    hi = lo + nb;
+  } else {
+    lo = worker_range_start(wk, W, N);
+    hi = worker_range_start(wk + 1, W, N);
+  }
+  const int total = static_cast<int>(hi - lo);  // blocks (positions) of this worker
+  if (total <= 0) return;
 
-    // ---- per-warp state
+  T* wst = s_stage + static_cast<size_t>(sp) * S * stage_elems;
+  uint64_t* fbar = s_bar + sp * S;
+  uint64_t* ebar = s_bar + NP * S + sp * S;
+  const uint64_t pol = policy_evict_first();
+
+  // Positions lo + 32*win + lane, one per lane: the element offset of the
+  // K/V page (-1 if the table entry is out of range) and, for the first
+  // block of a segment, the element offset of the unit's query rows.
+  auto window = [&](int win, int64_t& src, int& qoff) {
+    const int64_t pos = lo + static_cast<int64_t>(win) * 32 + lane;
+    src = -1;
+    qoff = -1;
+    if (pos < hi) {
+      const BlockPos bp = locate_block(pos, slab, s_scan, B, p.n_hsub);
+      const int phys = __ldg(p.block_tables + static_cast<int64_t>(bp.seq) * p.max_blocks + bp.j);
+      if (phys >= 0 && phys < p.num_blocks)
+        src = (static_cast<int64_t>(phys) * p.n_kv_heads + bp.kvh) * page_elems;
+      if (pos == lo || bp.j == 0) qoff = (bp.seq * p.n_q_heads + bp.kvh * p.group + bp.hsub * GH) * D;
+    }
+  };
+  // Copies of position x into stage `slot` (lane 0 only).
+  auto issue = [&](int slot, int64_t src, int qoff) {
+    const uint32_t bytes = (src >= 0 ? 2 * page_bytes : 0u) + (qoff >= 0 ? q_bytes : 0u);
+    if (src < 0) set_flag(p.err, 0x1u);
+    if (bytes == 0) {
+      mbar_arrive(fbar + slot);
+      return;
+    }
+    T* dst = wst + slot * stage_elems;
+    mbar_arrive_expect_tx(fbar + slot, bytes);
+    if (src >= 0) {
+      bulk_g2s(dst, kc + src, page_bytes, fbar + slot, pol);
+      bulk_g2s(dst + page_elems, vc + src, page_bytes, fbar + slot, pol);
+    }
+    if (qoff >= 0) bulk_g2s(dst + 2 * page_elems, qg + qoff, q_bytes, fbar + slot, pol);
+  };
+
+  int64_t w_src0, w_src1 = -1;
+  int w_q0, w_q1 = -1;
+  window(0, w_src0, w_q0);
+  if (total > 32) window(1, w_src1, w_q1);
+
+  // The ring runs ahead across segment boundaries: position x always sits in
+  // stage x % S, and the copy of x + S is issued as soon as x is consumed.
+  const int n_first = total < S ? total : S;
+  if (issuer) {
+    for (int i = 0; i < n_first; ++i) {
+      const int64_t src = __shfl_sync(full, w_src0, i);
+      const int qo = __shfl_sync(full, w_q0, i);
+      if (lane == 0) issue(i, src, qo);
+    }
+  }
+  int issued = n_first;
+  __syncwarp();
+
+  int slot = 0;
+  uint32_t par = 0;
+  int c = 0;              // positions consumed
+  int drain_from = -1;    // first position not consumed when a wait gave up
+  int64_t gb = lo;
+  while (gb < hi) {
+    // ---- segment: the part of one unit inside [lo, hi)
+    const BlockPos sg = locate_block(gb, slab, s_scan, B, p.n_hsub);
+    const int seg_len = static_cast<int>(((sg.nb - sg.j) < (hi - gb)) ? (sg.nb - sg.j) : (hi - gb));
+    const int n_rows = seq_rows(p.context_lens, sg.seq, bs, p.max_blocks);
+    const int h0 = sg.kvh * p.group + sg.hsub * GH;  // first query head of the unit
+    const int hq0 = h0 + hw * GW;                    // first query head of this warp
+
     WarpState<T, D, GW> st;
-    {
-      const T* qp = static_cast<const T*>(p.q) + (static_cast<int64_t>(seq) * p.n_q_heads + hq0) * D;
-#pragma unroll
-      for (int h = 0; h < GW; ++h) {
-        float f[C::DPL];
-#pragma unroll
-        for (int j = 0; j < C::NCH; ++j)
-          Elem<T>::unpack(__ldg(reinterpret_cast<const uint4*>(qp + h * D + (dq + C::DL * j) * C::VEC)),
-                          f + j * C::VEC);
-#pragma unroll
-        for (int i = 0; i < C::DP2; ++i) {
-          st.q[h][i] = make_float2(f[2 * i] * p.qscale, f[2 * i + 1] * p.qscale);
-          st.o[h][i] = make_float2(0.f, 0.f);
-        }
-        st.m[h] = kNegInf;
+    for (int t = 0; t < seg_len; ++t, ++c) {
+      if (c > 0 && (c & 31) == 0) {
+        w_src0 = w_src1;
+        w_q0 = w_q1;
+        w_src1 = -1;
+        w_q1 = -1;
+        if (c + 32 < total) window((c >> 5) + 1, w_src1, w_q1);
       }
-      st.l = 0.f;
-    }
-
-    const int nbw = seg_len > sp ? (seg_len - sp + NP - 1) / NP : 0;  // this stream's blocks
-    const int32_t* bt = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks;
-    T* wst = s_stage + static_cast<size_t>(sp) * S * 2 * page_elems;
-    uint64_t* fbar = s_bar + sp * S;
-    uint64_t* ebar = s_bar + NP * S + sp * S;
-
-    // Block-table entries of this stream's tiles, 32 at a time: lane L holds
-    // the entry of tile 32*window + L (one coalesced load per window, issued a
-    // window ahead), handed to the issuing lane by shuffles.
-    auto load_window = [&](int win) -> int {
-      const int t = win * 32 + lane;
-      return t < nbw ? __ldg(bt + j0 + sp + NP * t) : -1;
-    };
-    int bt_cur = load_window(0);
-    int bt_nxt = nbw > 32 ? load_window(1) : -1;
-
-    // Stage bookkeeping without divisions: tile t of this segment sits in
-    // stage `slot`, whose barriers are in phase parity `par`; both advance by
-    // one tile per iteration.
-    const int stage_elems = 2 * bs * D;
-    const int slot0 = static_cast<int>(ticket % static_cast<uint32_t>(S));
-    const uint32_t par0 = (ticket / static_cast<uint32_t>(S)) & 1u;
-
-    auto issue = [&](int slot, int phys) {
-      if (phys < 0 || phys >= p.num_blocks) {
-        set_flag(p.err, 0x1u);
-        mbar_arrive(fbar + slot);
-      } else {
-        const size_t src = (static_cast<size_t>(phys) * p.n_kv_heads + kvh) * page_elems;
-        T* dst = wst + slot * stage_elems;
-        mbar_arrive_expect_tx(fbar + slot, 2 * page_bytes);
-        bulk_g2s(dst, kc + src, page_bytes, fbar + slot, pol);
-        bulk_g2s(dst + page_elems, vc + src, page_bytes, fbar + slot, pol);
-      }
-    };
-
-    // All stages are free here: every warp finished the previous segment
-    // before the CTA-wide barrier that ended it.
-    if (!aborted && issuer) {
-      int sl = slot0;
-      for (int t = 0; t < S && t < nbw; ++t) {
-        const int ph = __shfl_sync(0xffffffffu, bt_cur, t);
-        if (lane == 0) issue(sl, ph);
-        sl = (sl + 1 == S) ? 0 : sl + 1;
-      }
-    }
-    __syncwarp();
-
-    int drain_from = -1;  // first tile not consumed when a wait gave up
-    int slot = slot0;
-    uint32_t par = par0;
-    for (int t = 0; t < nbw; ++t) {
-      if (aborted) break;
-      if (t > 0 && (t & 31) == 0) {
-        bt_cur = bt_nxt;
-        bt_nxt = (t + 32 < nbw) ? load_window((t >> 5) + 1) : -1;
-      }
-      const int phys = __shfl_sync(0xffffffffu, bt_cur, t & 31);
-      const int tn = t + S;
-      const int phys_next = __shfl_sync(0xffffffffu, (tn >> 5) == (t >> 5) ? bt_cur : bt_nxt, tn & 31);
+      const int64_t src = __shfl_sync(full, w_src0, c & 31);
+      const int cn = c + S;
+      const bool in_cur = (cn >> 5) == (c >> 5);
+      const int64_t src_n = __shfl_sync(full, in_cur ? w_src0 : w_src1, cn & 31);
+      const int q_n = __shfl_sync(full, in_cur ? w_q0 : w_q1, cn & 31);
       const bool ok = mbar_wait_bounded(fbar + slot, par);
-      if (__any_sync(0xffffffffu, !ok)) {
-        aborted = true;
-        drain_from = t;
+      if (__any_sync(full, !ok)) {
+        drain_from = c;
         if (lane == 0) set_flag(p.err, 0x8u);
         break;
       }
-      const int j = j0 + sp + NP * t;
-      if (phys >= 0 && phys < p.num_blocks) {
-        const T* kp = wst + slot * stage_elems;
+      const T* kp = wst + slot * stage_elems;
+      if (t == 0) {
+        // the unit's query rows came with its first page
+        const T* qs = kp + 2 * page_elems + hw * GW * D;
+#pragma unroll
+        for (int h = 0; h < GW; ++h) {
+          float f[C::DPL];
+#pragma unroll
+          for (int j = 0; j < C::NCH; ++j)
+            Elem<T>::unpack(lds128(qs + h * D + (dq + C::DL * j) * C::VEC), f + j * C::VEC);
+#pragma unroll
+          for (int i = 0; i < C::DP2; ++i) {
+            st.q[h][i] = make_float2(f[2 * i] * p.qscale, f[2 * i + 1] * p.qscale);
+            st.o[h][i] = make_float2(0.f, 0.f);
+          }
+          st.m[h] = kNegInf;
+        }
+        st.l = 0.f;
+      }
+      if (src >= 0) {
         const T* vp = kp + page_elems;
-        const int vr = min(bs, n_rows - j * bs);
+        const int vr = min(bs, n_rows - (sg.j + t) * bs);
         if (vr >= bs) {
           for (int tt = 0; tt < tiles_per_page; ++tt)
             gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, 16, st, tq, dq, lane, h_lane);
@@ -536,23 +561,23 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 2) gqa_decode_kernel(const Gqa
           }
         }
       }
-      // Every shared-memory read of this stage fed an FMA issued before this
-      // point, so no read of it is outstanding once the warp releases it.
+      // Every shared-memory read of this stage fed an instruction issued
+      // before this point, so no read of it is outstanding once released.
       __syncwarp();
       if (HW > 1 && lane == 0) mbar_arrive(ebar + slot);
-      if (issuer && tn < nbw) {
+      if (issuer && cn < total) {
         if (HW > 1) {
-          // Refill once every warp of the stream has released the stage.
+          // refill once every warp of the stream has released the stage
           bool ok2 = true;
           if (lane == 0) ok2 = mbar_wait_bounded(ebar + slot, par);
-          if (!__shfl_sync(0xffffffffu, ok2 ? 1 : 0, 0)) {
-            aborted = true;
-            drain_from = t + 1;
+          if (!__shfl_sync(full, ok2 ? 1 : 0, 0)) {
+            drain_from = c + 1;
             if (lane == 0) set_flag(p.err, 0x8u);
             break;
           }
         }
-        if (lane == 0) issue(slot, phys_next);
+        if (lane == 0) issue(slot, src_n, q_n);
+        ++issued;
       }
       __syncwarp();
       if (++slot == S) {
@@ -560,106 +585,101 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 2) gqa_decode_kernel(const Gqa
         par ^= 1u;
       }
     }
-    if (drain_from >= 0 && issuer) {
-      // Copies issued but not consumed (at most S) must land before this
-      // shared memory is reused or the CTA exits.
-      for (int t = drain_from; t < nbw && t < drain_from + S; ++t)
-        (void)mbar_wait_bounded(fbar + (ticket + t) % S, ((ticket + t) / S) & 1u);
-    }
-    ticket += nbw;
+    if (drain_from >= 0) break;
 
-    // ---- combine the warps of this CTA
+    // ---- finish the segment: this warp holds every row of it for its heads
 #pragma unroll
     for (int msk = C::DL; msk < 32; msk <<= 1) {
 #pragma unroll
       for (int h = 0; h < GW; ++h) {
 #pragma unroll
         for (int i = 0; i < C::DP2; ++i) {
-          st.o[h][i].x += __shfl_xor_sync(0xffffffffu, st.o[h][i].x, msk);
-          st.o[h][i].y += __shfl_xor_sync(0xffffffffu, st.o[h][i].y, msk);
+          st.o[h][i].x += __shfl_xor_sync(full, st.o[h][i].x, msk);
+          st.o[h][i].y += __shfl_xor_sync(full, st.o[h][i].y, msk);
         }
       }
     }
     float lw[GW];
 #pragma unroll
     for (int hh = 0; hh < GW; ++hh) lw[hh] = warp_sum(h_lane == hh ? st.l : 0.f) * (1.0f / C::DUP);
-    if (tq == 0) {
+    const bool whole = (sg.j == 0 && seg_len == sg.nb);
+    if (whole) {
+      if (tq == 0) {
 #pragma unroll
-      for (int h = 0; h < GW; ++h) {
+        for (int h = 0; h < GW; ++h) {
+          const float inv = 1.0f / lw[h];
+          const int64_t ob = (static_cast<int64_t>(sg.seq) * p.n_q_heads + hq0 + h) * D;
 #pragma unroll
-        for (int j = 0; j < C::NCH; ++j) {
+          for (int j = 0; j < C::NCH; ++j) {
 #pragma unroll
-          for (int e = 0; e < C::VEC; e += 2) {
-            const float2 v = st.o[h][(j * C::VEC + e) / 2];
-            s_o[(w * GW + h) * D + (dq + C::DL * j) * C::VEC + e] = v.x;
-            s_o[(w * GW + h) * D + (dq + C::DL * j) * C::VEC + e + 1] = v.y;
+            for (int e = 0; e < C::VEC; e += 2) {
+              const float2 v = st.o[h][(j * C::VEC + e) / 2];
+              const int d = (dq + C::DL * j) * C::VEC + e;
+              store_out(p.out, ob + d, v.x * inv, p.out_dtype);
+              store_out(p.out, ob + d + 1, v.y * inv, p.out_dtype);
+            }
           }
         }
       }
-    }
-    if (lane == 0) {
+    } else {
+      // Record (max, sum, unnormalised output) for this warp's heads; the
+      // last worker of the unit to finish merges all of them.
+      const int64_t rec = wk * 2 + (gb == lo ? 0 : 1);
+      if (tq == 0) {
 #pragma unroll
-      for (int h = 0; h < GW; ++h) {
-        s_ml[(w * GW + h) * 2] = st.m[h];
-        s_ml[(w * GW + h) * 2 + 1] = lw[h];
-      }
-    }
-    __syncthreads();
-    const int64_t rec = static_cast<int64_t>(blockIdx.x) * 2 + which;
-    for (int idx = tid; idx < GH * D; idx += blockDim.x) {
-      const int h = idx / D, d = idx - (idx / D) * D;
-      // head h of the unit lives in warp (stream, h / GW), slot h % GW
-      const int hw_h = h / GW, jh = h - hw_h * GW;
-      float M = kNegInf;
+        for (int h = 0; h < GW; ++h) {
+          float* ro = p.rec_o + (rec * GH + hw * GW + h) * D;
 #pragma unroll
-      for (int ss = 0; ss < NP; ++ss) M = fmaxf(M, s_ml[((ss * HW + hw_h) * GW + jh) * 2]);
-      float Lsum = 0.f, O = 0.f;
+          for (int j = 0; j < C::NCH; ++j) {
 #pragma unroll
-      for (int ss = 0; ss < NP; ++ss) {
-        const int r = (ss * HW + hw_h) * GW + jh;
-        const float mw = s_ml[r * 2];
-        if (mw == kNegInf) continue;
-        const float f = fast_exp2(mw - M);
-        Lsum += f * s_ml[r * 2 + 1];
-        O += f * s_o[r * D + d];
-      }
-      if (whole) {
-        store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + h0 + h) * D + d, O / Lsum, p.out_dtype);
-      } else {
-        p.rec_o[(rec * GH + h) * D + d] = O;
-        if (d == 0) {
-          p.rec_ml[(rec * GH + h) * 2] = M;
-          p.rec_ml[(rec * GH + h) * 2 + 1] = Lsum;
+            for (int e = 0; e < C::VEC; e += 4) {
+              const float2 a = st.o[h][(j * C::VEC + e) / 2], b = st.o[h][(j * C::VEC + e) / 2 + 1];
+              *reinterpret_cast<float4*>(ro + (dq + C::DL * j) * C::VEC + e) = make_float4(a.x, a.y, b.x, b.y);
+            }
+          }
         }
       }
-    }
-    if (!whole) {
-      // Publish this record, count it, and let the last contributor merge.
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < GW; ++h) {
+          p.rec_ml[(rec * GH + hw * GW + h) * 2] = st.m[h];
+          p.rec_ml[(rec * GH + hw * GW + h) * 2 + 1] = lw[h];
+        }
+      }
       __threadfence();
-      __syncthreads();
-      const int64_t c0 = cta_of_block(u0, G, N), c1 = cta_of_block(u0 + nb - 1, G, N);
-      const int64_t unit = (static_cast<int64_t>(kvh) * B + seq) * p.n_hsub + hsub;
-      if (tid == 0) {
-        int contributors = 0;
-        for (int64_t c = c0; c <= c1; ++c)
-          contributors += (cta_range_start(c, G, N) != cta_range_start(c + 1, G, N)) ? 1 : 0;
-        const unsigned int old = atomicAdd(p.counters + unit, 1u);
-        s_last = 0;
+      __syncwarp();
+      const int64_t u0 = gb - sg.j;
+      const int64_t unit = (static_cast<int64_t>(sg.kvh) * B + sg.seq) * p.n_hsub + sg.hsub;
+      int last = 0;
+      if (lane == 0) {
+        const int64_t c0 = worker_of_block(u0, W, N), c1 = worker_of_block(u0 + sg.nb - 1, W, N);
+        int64_t contributors = c1 - c0 + 1;
+        if (N < W) {
+          contributors = 0;
+          for (int64_t x = c0; x <= c1; ++x)
+            contributors += (worker_range_start(x, W, N) != worker_range_start(x + 1, W, N)) ? 1 : 0;
+        }
+        unsigned int* ctr = p.counters + unit * HW + hw;
+        const unsigned int old = atomicAdd(ctr, 1u);
         if (old + 1 == static_cast<unsigned int>(contributors)) {
-          s_last = 1;
+          last = 1;
+          *ctr = 0u;  // every contributor has counted: reset for the next call
         } else if (old + 1 > static_cast<unsigned int>(contributors)) {
           set_flag(p.err, 0x10u);  // the workspace counters were not zero
-          atomicExch(p.counters + unit, 0u);
+          atomicExch(ctr, 0u);
         }
       }
-      __syncthreads();
-      if (s_last) {
+      if (__shfl_sync(full, last, 0)) {
         __threadfence();
-        merge_records<GH>(p, D, u0, c0, c1, G, N, seq, h0, reinterpret_cast<int*>(s_o), NP * GH * D);
-        if (tid == 0) p.counters[unit] = 0u;
+        merge_unit_warp<D, GH, GW>(p, u0, sg.nb, W, N, sg.seq, h0 + hw * GW, hw * GW, lane);
       }
     }
-    __syncthreads();
+    gb += seg_len;
+  }
+  if (drain_from >= 0 && issuer) {
+    // Copies issued but not consumed (at most S) must land before the CTA
+    // can exit and its shared memory be reused.
+    for (int x = drain_from; x < issued; ++x) (void)mbar_wait_bounded(fbar + x % S, (x / S) & 1u);
   }
 }
 

@@ -29,6 +29,8 @@ static kvc_status gqa_run_gh(const GqaParams& p, int GH, int grid, size_t smem, 
     case 1: return gqa_run<T, D, 1>(p, grid, smem, stream, mode, occ);
     case 2: return gqa_run<T, D, 2>(p, grid, smem, stream, mode, occ);
     case 4: return gqa_run<T, D, 4>(p, grid, smem, stream, mode, occ);
+    case 8: return gqa_run<T, D, 8>(p, grid, smem, stream, mode, occ);
+    case 16: return gqa_run<T, D, 16>(p, grid, smem, stream, mode, occ);
   }
   return fail(KVC_ERR_UNSUPPORTED, "head subgroup %d", GH);
 }

@@ -77,7 +77,8 @@ def test_config1_tiny_mha_fp32_every_step_vs_recompute(kvc):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("hq,hkv,D", [(32, 8, 128), (8, 8, 128), (8, 1, 128), (16, 2, 64), (6, 2, 64),
-                                      (16, 2, 256), (8, 4, 32), (64, 8, 128)])
+                                      (16, 2, 256), (8, 4, 32), (64, 8, 128), (32, 2, 128), (32, 1, 64),
+                                      (24, 2, 128), (32, 2, 256)])
 def test_small_batch_ragged(kvc, dtype, hq, hkv, D):
     lens = [1, 15, 16, 17, 31, 32, 33, 47, 200, 129]
     case = W.gqa_case(len(lens), hq, hkv, D, 16, lens, dtype, seed=7)
@@ -95,6 +96,14 @@ def test_forced_split_k(kvc, blocks_per_cta):
     kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, blocks_per_cta)
     case = W.gqa_case(5, 32, 8, 128, 16, [1, 17, 160, 333, 64], "bf16", seed=13)
     step_and_compare(kvc, case, 1.0 / math.sqrt(128), TOL["bf16"])
+
+
+@pytest.mark.parametrize("hq,hkv,D", [(64, 8, 128), (32, 2, 128), (32, 2, 256)])
+def test_forced_split_k_wide_groups(kvc, hq, hkv, D):
+    # 8 and 16 query heads per unit, split over warps that share one page stream
+    kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, 3)
+    case = W.gqa_case(4, hq, hkv, D, 16, [1, 90, 333, 17], "bf16", seed=14)
+    step_and_compare(kvc, case, 1.0 / math.sqrt(D), TOL["bf16"])
 
 
 def test_without_workspace_single_cta_per_unit(kvc):

@@ -59,7 +59,7 @@ def test_static_scratch_matches_workspace_path_twice(kvc):
 
 
 def test_static_scratch_refuses_oversized_shapes(kvc):
-    kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, 1)  # one cache block per CTA: far more records than 8 MiB hold
+    kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, 1)  # one cache block per CTA: far more records than 16 MiB hold
     try:
         case = W.gqa_case(8, 32, 8, 128, 16, [4096] * 8, "bf16", seed=45)
         dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in case.items()}
