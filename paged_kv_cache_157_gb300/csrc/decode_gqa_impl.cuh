@@ -302,53 +302,105 @@ __device__ __forceinline__ int64_t record_of(int64_t c, int64_t c0, int64_t u0, 
 
 // One warp merges, for its GW heads of a unit (first block u0, nb blocks),
 // the records of every worker that touched the unit, with the log-sum-exp
-// rule, and writes the normalised output. Lanes own dims lane + 32k.
+// rule, and writes the normalised output. Records are taken RG at a time:
+// lane r loads the (max, sum) pairs of record r while every lane loads its
+// chunks of the group's output rows, so one round trip serves the group.
+// Lane L owns the float4 chunks L + 32k of the warp's GW x D outputs.
 template <int D, int GH, int GW>
 __device__ void merge_unit_warp(const GqaParams& p, int64_t u0, int nb, int64_t W, int64_t N, int seq, int hq0,
                                 int hoff, int lane) {
-  constexpr int DK = D / 32;
+  constexpr int CH = D / 4;                  // float4 chunks per head
+  constexpr int NCK = (GW * CH + 31) / 32;   // chunks per lane
+  constexpr int RG = NCK <= 4 ? 8 : 4;       // records in flight together
   const int64_t c0 = worker_of_block(u0, W, N), c1 = worker_of_block(u0 + nb - 1, W, N);
   const int64_t f00 = worker_range_start(c0, W, N);
-  float M[GW];
-#pragma unroll
-  for (int h = 0; h < GW; ++h) M[h] = kNegInf;
-  for (int64_t c = c0 + lane; c <= c1; c += 32) {
-    const int64_t rec = record_of(c, c0, u0, f00, W, N);
-    if (rec < 0) continue;
-#pragma unroll
-    for (int h = 0; h < GW; ++h) M[h] = fmaxf(M[h], __ldcg(p.rec_ml + (rec * GH + hoff + h) * 2));
-  }
-#pragma unroll
-  for (int h = 0; h < GW; ++h) M[h] = warp_max(M[h]);
-  float Ls[GW], O[GW][DK];
+  const int span = static_cast<int>(c1 - c0 + 1);
+  const float* rbase = p.rec_o + static_cast<int64_t>(hoff) * D + 4 * lane;
+  float M[GW], Lp[GW];
+  float4 O[NCK];
 #pragma unroll
   for (int h = 0; h < GW; ++h) {
-    Ls[h] = 0.f;
-#pragma unroll
-    for (int k = 0; k < DK; ++k) O[h][k] = 0.f;
+    M[h] = kNegInf;
+    Lp[h] = 0.f;
   }
-  for (int64_t c = c0; c <= c1; ++c) {
-    const int64_t rec = record_of(c, c0, u0, f00, W, N);
-    if (rec < 0) continue;
+#pragma unroll
+  for (int k = 0; k < NCK; ++k) O[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < span; base += RG) {
+    const int n = min(RG, span - base);
+    // lanes r < n: (max, sum) of record base + r
+    const int64_t rec = (lane < n) ? record_of(c0 + base + lane, c0, u0, f00, W, N) : -1;
+    float mr[GW], lr[GW];
 #pragma unroll
     for (int h = 0; h < GW; ++h) {
       const float* ml = p.rec_ml + (rec * GH + hoff + h) * 2;
-      const float mc = __ldcg(ml);
-      if (mc == kNegInf) continue;
-      const float f = fast_exp2(mc - M[h]);
-      Ls[h] += f * __ldcg(ml + 1);
-      const float* o = p.rec_o + (rec * GH + hoff + h) * D + lane;
+      mr[h] = rec >= 0 ? __ldcg(ml) : kNegInf;
+      lr[h] = rec >= 0 ? __ldcg(ml + 1) : 0.f;
+    }
+    // every lane: its chunks of the group's output rows
+    float4 ov[RG][NCK];
 #pragma unroll
-      for (int k = 0; k < DK; ++k) O[h][k] += f * __ldcg(o + 32 * k);
+    for (int i = 0; i < RG; ++i) {
+      const int64_t rr = __shfl_sync(0xffffffffu, rec, i);
+#pragma unroll
+      for (int k = 0; k < NCK; ++k) {
+        const bool ok = i < n && rr >= 0 && lane + 32 * k < GW * CH;
+        ov[i][k] = ok ? __ldcg(reinterpret_cast<const float4*>(rbase + rr * GH * D + 128 * k))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float fr[GW];
+#pragma unroll
+    for (int h = 0; h < GW; ++h) {
+      const float mn = fmaxf(M[h], warp_max(mr[h]));
+      if (mn != M[h]) {
+        const float a = (M[h] == kNegInf) ? 0.f : fast_exp2(M[h] - mn);
+        Lp[h] *= a;
+#pragma unroll
+        for (int k = 0; k < NCK; ++k) {
+          if (((lane + 32 * k) / CH) == h) {
+            O[k].x *= a;
+            O[k].y *= a;
+            O[k].z *= a;
+            O[k].w *= a;
+          }
+        }
+        M[h] = mn;
+      }
+      fr[h] = (mr[h] == kNegInf) ? 0.f : fast_exp2(mr[h] - M[h]);
+      Lp[h] += fr[h] * lr[h];
+    }
+#pragma unroll
+    for (int i = 0; i < RG; ++i) {
+      float fh[GW];
+#pragma unroll
+      for (int h = 0; h < GW; ++h) fh[h] = __shfl_sync(0xffffffffu, fr[h], i);
+#pragma unroll
+      for (int k = 0; k < NCK; ++k) {
+        float f = 0.f;
+#pragma unroll
+        for (int h = 0; h < GW; ++h) f = ((lane + 32 * k) / CH == h) ? fh[h] : f;
+        O[k].x += f * ov[i][k].x;
+        O[k].y += f * ov[i][k].y;
+        O[k].z += f * ov[i][k].z;
+        O[k].w += f * ov[i][k].w;
+      }
     }
   }
+  float inv[GW];
 #pragma unroll
-  for (int h = 0; h < GW; ++h) {
-    const float inv = 1.0f / Ls[h];
+  for (int h = 0; h < GW; ++h) inv[h] = 1.0f / warp_sum(Lp[h]);
 #pragma unroll
-    for (int k = 0; k < DK; ++k)
-      store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + hq0 + h) * D + lane + 32 * k, O[h][k] * inv,
-                p.out_dtype);
+  for (int k = 0; k < NCK; ++k) {
+    const int idx = lane + 32 * k;
+    if (idx >= GW * CH) break;
+    float iv = 0.f;
+#pragma unroll
+    for (int h = 0; h < GW; ++h) iv = (idx / CH == h) ? inv[h] : iv;
+    const int64_t o = (static_cast<int64_t>(seq) * p.n_q_heads + hq0) * D + 4 * idx;
+    store_out(p.out, o, O[k].x * iv, p.out_dtype);
+    store_out(p.out, o + 1, O[k].y * iv, p.out_dtype);
+    store_out(p.out, o + 2, O[k].z * iv, p.out_dtype);
+    store_out(p.out, o + 3, O[k].w * iv, p.out_dtype);
   }
 }
 
@@ -491,6 +543,12 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 2) gqa_decode_kernel(const Gqa
   }
   int issued = n_first;
   __syncwarp();
+
+  // Partial segments (at most two: the one starting at lo, the one ending
+  // at hi) whose records wait to be counted.
+  bool pend0 = false, pend1 = false;
+  int64_t p0_u0 = 0, p1_u0 = 0, p0_unit = 0, p1_unit = 0;
+  int p0_nb = 0, p1_nb = 0, p0_seq = 0, p1_seq = 0, p0_h0 = 0, p1_h0 = 0;
 
   int slot = 0;
   uint32_t par = 0;
@@ -646,35 +704,57 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 2) gqa_decode_kernel(const Gqa
           p.rec_ml[(rec * GH + hw * GW + h) * 2 + 1] = lw[h];
         }
       }
-      __threadfence();
-      __syncwarp();
-      const int64_t u0 = gb - sg.j;
-      const int64_t unit = (static_cast<int64_t>(sg.kvh) * B + sg.seq) * p.n_hsub + sg.hsub;
-      int last = 0;
-      if (lane == 0) {
-        const int64_t c0 = worker_of_block(u0, W, N), c1 = worker_of_block(u0 + sg.nb - 1, W, N);
-        int64_t contributors = c1 - c0 + 1;
-        if (N < W) {
-          contributors = 0;
-          for (int64_t x = c0; x <= c1; ++x)
-            contributors += (worker_range_start(x, W, N) != worker_range_start(x + 1, W, N)) ? 1 : 0;
-        }
-        unsigned int* ctr = p.counters + unit * HW + hw;
-        const unsigned int old = atomicAdd(ctr, 1u);
-        if (old + 1 == static_cast<unsigned int>(contributors)) {
-          last = 1;
-          *ctr = 0u;  // every contributor has counted: reset for the next call
-        } else if (old + 1 > static_cast<unsigned int>(contributors)) {
-          set_flag(p.err, 0x10u);  // the workspace counters were not zero
-          atomicExch(ctr, 0u);
-        }
-      }
-      if (__shfl_sync(full, last, 0)) {
-        __threadfence();
-        merge_unit_warp<D, GH, GW>(p, u0, sg.nb, W, N, sg.seq, h0 + hw * GW, hw * GW, lane);
+      // counted (and merged, if this worker is the unit's last) once the
+      // whole range is done, so that no wait on the count stalls the stream
+      if (gb == lo) {
+        pend0 = true;
+        p0_u0 = gb - sg.j;
+        p0_nb = sg.nb;
+        p0_seq = sg.seq;
+        p0_h0 = h0;
+        p0_unit = (static_cast<int64_t>(sg.kvh) * B + sg.seq) * p.n_hsub + sg.hsub;
+      } else {
+        pend1 = true;
+        p1_u0 = gb - sg.j;
+        p1_nb = sg.nb;
+        p1_seq = sg.seq;
+        p1_h0 = h0;
+        p1_unit = (static_cast<int64_t>(sg.kvh) * B + sg.seq) * p.n_hsub + sg.hsub;
       }
     }
     gb += seg_len;
+  }
+  if (drain_from < 0 && (pend0 || pend1)) {
+    // Count this worker's records (lane 0: the segment at lo, lane 1: the
+    // one ending at hi); the add that completes a unit's count makes its
+    // caller the unit's merger and resets the counter for the next call.
+    __syncwarp();
+    int last = 0;
+    if (lane < 2 && (lane == 0 ? pend0 : pend1)) {
+      const int64_t u0 = lane == 0 ? p0_u0 : p1_u0;
+      const int nbu = lane == 0 ? p0_nb : p1_nb;
+      const int64_t unit = lane == 0 ? p0_unit : p1_unit;
+      const int64_t c0 = worker_of_block(u0, W, N), c1 = worker_of_block(u0 + nbu - 1, W, N);
+      int64_t contributors = c1 - c0 + 1;
+      if (N < W) {
+        contributors = 0;
+        for (int64_t x = c0; x <= c1; ++x)
+          contributors += (worker_range_start(x, W, N) != worker_range_start(x + 1, W, N)) ? 1 : 0;
+      }
+      unsigned int* ctr = p.counters + unit * HW + hw;
+      const unsigned int old = atomic_add_acq_rel_gpu(ctr, 1u);
+      if (old + 1 == static_cast<unsigned int>(contributors)) {
+        last = 1;
+        *ctr = 0u;
+      } else if (old + 1 > static_cast<unsigned int>(contributors)) {
+        set_flag(p.err, 0x10u);  // the workspace counters were not zero
+        atomicExch(ctr, 0u);
+      }
+    }
+    // the warp barrier orders the other lanes' record reads after the acquire
+    const int last0 = __shfl_sync(full, last, 0), last1 = __shfl_sync(full, last, 1);
+    if (last0) merge_unit_warp<D, GH, GW>(p, p0_u0, p0_nb, W, N, p0_seq, p0_h0 + hw * GW, hw * GW, lane);
+    if (last1) merge_unit_warp<D, GH, GW>(p, p1_u0, p1_nb, W, N, p1_seq, p1_h0 + hw * GW, hw * GW, lane);
   }
   if (drain_from >= 0 && issuer) {
     // Copies issued but not consumed (at most S) must land before the CTA

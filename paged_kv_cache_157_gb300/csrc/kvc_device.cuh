@@ -178,6 +178,16 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
 
 // ------------------------------------------------------------ reductions
 
+// Atomic add with acquire-release semantics at GPU scope: it publishes the
+// writes that precede it in this thread (or that a warp barrier ordered
+// before it) and makes the writes published by earlier such adds on the same
+// word visible to this thread's later reads.
+__device__ __forceinline__ unsigned int atomic_add_acq_rel_gpu(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
