@@ -18,61 +18,68 @@ struct GqaParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   void* out;
-  float* rec_o;   // [W*2, GH, D] partial outputs of the W workers (split mode)
-  float* rec_ml;  // [W*2, GH, 2] (max in log2 units, sum)
-  unsigned int* counters;  // [units, warps per stream] records seen per split unit; zero between calls
+  float* rec_o;   // [G*2, kGqaWarps/HW * GH, D] partial outputs of the G CTAs (split mode)
+  float* rec_ml;  // [G*2, kGqaWarps/HW * GH, 2] (max in log2 units, sum)
+  unsigned int* counters;  // [units] records seen per split unit; zero between calls
   unsigned int* err;
   int64_t num_blocks;
   int batch;
   int n_q_heads;
   int n_kv_heads;
-  int group;  // n_q_heads / n_kv_heads
-  int n_hsub;  // group / GH
+  int group;     // n_q_heads / n_kv_heads
+  int n_hsub;    // group / GH
+  int hc;        // kv heads per CTA (a chunk): consecutive heads of a block, read as one copy
+  int n_chunks;  // n_kv_heads / hc
   int block_size;
   int max_blocks;
   int out_dtype;
   int stages;
-  int unit_mode;  // 1: worker u handles unit u completely (no records)
+  int unit_mode;  // 1: CTA u handles unit u completely (no records)
   float qscale;   // scale * log2(e)
 };
 
-#ifndef KVC_GQA_PAIR_WARPS
-#define KVC_GQA_PAIR_WARPS 0
-#endif
 #ifndef KVC_GQA_WARPS
 #define KVC_GQA_WARPS 4
 #endif
-constexpr int kGqaWarps = KVC_GQA_WARPS;  // warps per CTA
+#ifndef KVC_GQA_CTAS_PER_SM
+#define KVC_GQA_CTAS_PER_SM 2
+#endif
+constexpr int kGqaWarps = KVC_GQA_WARPS;            // warps per CTA
+constexpr int kGqaCtasPerSm = KVC_GQA_CTAS_PER_SM;  // resident CTAs the register and shared-memory budgets aim at
 constexpr float kNegInf = -__builtin_huge_valf();
 
-// A unit's GH query heads are split over HW warps that share one stream of
-// K/V pages; each warp holds GH / HW heads. KVC_GQA_PAIR_WARPS selects
-// whether head groups of 2 or more are split over a warp pair (1) or kept in
-// one warp (0).
-__host__ __device__ constexpr int gqa_warps_per_stream(int GH) {
-  return GH > 4 ? GH / 4 : ((KVC_GQA_PAIR_WARPS && GH >= 2) ? 2 : 1);
-}
-__host__ __device__ constexpr int gqa_streams(int GH) { return kGqaWarps / gqa_warps_per_stream(GH); }
+// The GH query heads of a kv head are split over HW warps (GH / HW <= 4
+// heads per warp); a CTA covers kGqaWarps / HW kv heads at most.
+__host__ __device__ constexpr int gqa_warps_per_kvhead(int GH) { return GH > 4 ? GH / 4 : 1; }
+__host__ __device__ constexpr int gqa_max_chunk(int GH) { return kGqaWarps / gqa_warps_per_kvhead(GH); }
 
-// Shared-memory carve-up, identical on host and device. Each page stream
-// has `stages` stages of [K page][V page][the unit's GH query rows].
+// Shared-memory carve-up, identical on host and device. The CTA has one ring
+// of `stages` stages, each [K chunk: hc pages][V chunk: hc pages][query rows
+// of the unit: hc x GH]; every warp has a [heads of the warp][16 rows] fp32
+// buffer for the softmax weights of its current tile.
 struct GqaSmem {
-  size_t stage_off, bar_off, scan_off, total;
+  size_t stage_off, p_off, bar_off, rel_off, misc_off, scan_off, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline size_t gqa_stage_bytes(int elt_bytes, int D, int GH, int block_size) {
-  return (2ull * block_size * D + static_cast<size_t>(GH) * D) * elt_bytes;
+__host__ __device__ inline size_t gqa_stage_bytes(int elt_bytes, int D, int GH, int block_size, int hc) {
+  return (2ull * hc * block_size * D + static_cast<size_t>(hc) * GH * D) * elt_bytes;
 }
 
-__host__ __device__ inline GqaSmem gqa_smem_layout(int elt_bytes, int D, int GH, int block_size, int stages,
+__host__ __device__ inline size_t gqa_p_bytes_per_warp(int GH) {
+  return static_cast<size_t>(GH / gqa_warps_per_kvhead(GH)) * 16 * 4;
+}
+
+__host__ __device__ inline GqaSmem gqa_smem_layout(int elt_bytes, int D, int GH, int block_size, int hc, int stages,
                                                   int batch) {
   GqaSmem s;
-  const size_t np = static_cast<size_t>(gqa_streams(GH));
   s.stage_off = 0;
-  s.bar_off = align_up(np * stages * gqa_stage_bytes(elt_bytes, D, GH, block_size), 16);
-  s.scan_off = align_up(s.bar_off + np * stages * 2 * 8, 16);  // full and empty barrier per stage
+  s.p_off = align_up(static_cast<size_t>(stages) * gqa_stage_bytes(elt_bytes, D, GH, block_size, hc), 16);
+  s.bar_off = align_up(s.p_off + kGqaWarps * gqa_p_bytes_per_warp(GH), 16);
+  s.rel_off = s.bar_off + static_cast<size_t>(stages) * 8;  // one "full" mbarrier per stage
+  s.misc_off = align_up(s.rel_off + static_cast<size_t>(stages) * 8, 16);  // release and issue counts per stage
+  s.scan_off = s.misc_off + 16;  // [abort flag, last flags]
   s.total = s.scan_off + static_cast<size_t>(batch + 1 + 32) * 4;
   return s;
 }

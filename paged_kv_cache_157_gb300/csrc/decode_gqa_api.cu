@@ -14,27 +14,29 @@ namespace kvc {
 
 namespace {
 
-constexpr size_t kStageBudget = 108 * 1024;  // shared memory per CTA for stages + scan: 2 CTAs per SM
+// Shared memory per CTA (stages, weights, barriers, scan) so that
+// kGqaCtasPerSm CTAs fit the 228 KB of an SM (1 KB of it reserved per CTA).
+constexpr size_t kStageBudget = (228 * 1024) / kGqaCtasPerSm - 1024;
 constexpr int kMaxCtasPerSm = 4;
 constexpr int kMinBlocksPerCta = 2 * kGqaWarps;
 constexpr int kMaxBatch = 4096;
 
 struct GqaPlan {
-  int GH = 1, n_hsub = 1, stages = 2, streams = 1;
+  int GH = 1, n_hsub = 1, stages = 2, hc = 1, n_chunks = 1;
   int64_t units = 0;
   size_t smem = 0;
-  size_t rec_bytes_per_cta = 0;  // two records per page stream (worker)
+  size_t rec_bytes_per_cta = 0;  // two records per CTA
 };
 
-// Workspace layout: [unit counters, one per warp of a stream][record
-// outputs][record (max, sum)].
-size_t counter_bytes(const GqaPlan& pl) {
-  return align_up(static_cast<size_t>(pl.units) * gqa_warps_per_stream(pl.GH) * 4, 256);
+// Workspace layout: [unit counters][record outputs][record (max, sum)]. The
+// counters are sized for one kv head per unit, the most units any plan uses.
+size_t counter_bytes(int batch, int n_kv_heads, const GqaPlan& pl) {
+  return align_up(static_cast<size_t>(batch) * n_kv_heads * pl.n_hsub * 4, 256);
 }
 
 // Query heads per unit: the largest power of two up to 16 that divides the
 // group. Up to 4 heads share one warp; 8 and 16 split over 2 and 4 warps that
-// consume one stream of pages, so each page is loaded once for all of them.
+// read the same pages, so each page is loaded once for all of them.
 int head_subgroup(int group) {
   for (int gh = 16; gh > 1; gh >>= 1)
     if (group % gh == 0) return gh;
@@ -45,21 +47,33 @@ kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, in
   const int group = n_q_heads / n_kv_heads;
   pl->GH = head_subgroup(group);
   pl->n_hsub = group / pl->GH;
-  pl->units = static_cast<int64_t>(n_kv_heads) * batch * pl->n_hsub;
-  pl->streams = gqa_streams(pl->GH);
-  const size_t stage = gqa_stage_bytes(elt, D, pl->GH, bs);
+  // kv heads per CTA: the largest power of two the CTA's warps can hold that
+  // divides n_kv_heads; their pages of a block are adjacent, so one copy
+  // moves all of them
+  int hc = 1;
+  while (hc * 2 <= gqa_max_chunk(pl->GH) && n_kv_heads % (hc * 2) == 0) hc *= 2;
   const size_t scan = static_cast<size_t>(batch + 1 + 32) * 4;
-  const size_t budget = kStageBudget > scan + 1024 ? kStageBudget - scan - 1024 : 0;
-  int S = static_cast<int>(budget / (pl->streams * stage));
-  S = std::max(1, std::min(S, 8));
-  GqaSmem L = gqa_smem_layout(elt, D, pl->GH, bs, S, batch);
-  while (S > 1 && L.total > static_cast<size_t>(max_smem)) L = gqa_smem_layout(elt, D, pl->GH, bs, --S, batch);
+  const size_t fixed = scan + kGqaWarps * gqa_p_bytes_per_warp(pl->GH) + 8 * 16 + 16 + 512;
+  const size_t budget = kStageBudget > fixed ? kStageBudget - fixed : 0;
+  int S = 1;
+  for (;;) {
+    const size_t stage = gqa_stage_bytes(elt, D, pl->GH, bs, hc);
+    S = std::max(1, std::min(static_cast<int>(budget / stage), 8));
+    if (S >= 2 || hc == 1) break;
+    hc /= 2;  // keep at least two stages in flight
+  }
+  GqaSmem L = gqa_smem_layout(elt, D, pl->GH, bs, hc, S, batch);
+  while (S > 1 && L.total > static_cast<size_t>(max_smem)) L = gqa_smem_layout(elt, D, pl->GH, bs, hc, --S, batch);
   if (L.total > static_cast<size_t>(max_smem))
     return fail(KVC_ERR_UNSUPPORTED, "block_size %d x head_dim %d needs %zu bytes of shared memory (max %d)", bs, D,
                 L.total, max_smem);
+  pl->hc = hc;
+  pl->n_chunks = n_kv_heads / hc;
+  pl->units = static_cast<int64_t>(batch) * pl->n_chunks * pl->n_hsub;
   pl->stages = S;
   pl->smem = L.total;
-  pl->rec_bytes_per_cta = static_cast<size_t>(pl->streams) * 2 * pl->GH * (D + 2) * sizeof(float);
+  pl->rec_bytes_per_cta =
+      2ull * gqa_max_chunk(pl->GH) * pl->GH * (static_cast<size_t>(D) + 2) * sizeof(float);
   return KVC_OK;
 }
 
@@ -129,8 +143,9 @@ kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, i
   GqaPlan pl;
   if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, 2, dev->max_smem_optin, &pl)) != KVC_OK)
     return s;
-  const int64_t G = plan_ctas(dev, kMaxCtasPerSm, pl.units, max_blocks_per_seq);
-  *bytes = align_up(counter_bytes(pl) + static_cast<size_t>(G) * pl.rec_bytes_per_cta, 256);
+  const int64_t G = plan_ctas(dev, kMaxCtasPerSm, static_cast<int64_t>(batch) * n_kv_heads * pl.n_hsub,
+                             max_blocks_per_seq);
+  *bytes = align_up(counter_bytes(batch, n_kv_heads, pl) + static_cast<size_t>(G) * pl.rec_bytes_per_cta, 256);
   return KVC_OK;
 }
 
@@ -176,6 +191,8 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
   p.n_kv_heads = n_kv_heads;
   p.group = n_q_heads / n_kv_heads;
   p.n_hsub = pl.n_hsub;
+  p.hc = pl.hc;
+  p.n_chunks = pl.n_chunks;
   p.block_size = block_size;
   p.max_blocks = max_blocks_per_seq;
   p.out_dtype = static_cast<int>(out_dtype);
@@ -185,24 +202,27 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
   int occ = 1;
   if ((s = occupancy_for(dtype, p, head_dim, pl, &occ)) != KVC_OK) return s;
   int64_t G = plan_ctas(dev, occ, pl.units, max_blocks_per_seq);
-  const size_t cbytes = counter_bytes(pl);
+  const size_t cbytes = counter_bytes(batch, n_kv_heads, pl);
   G = std::min<int64_t>(G, workspace_bytes > cbytes
                                ? static_cast<int64_t>((workspace_bytes - cbytes) / pl.rec_bytes_per_cta)
                                : 0);
+  const int HS = gqa_max_chunk(pl.GH) * pl.GH;  // query heads per record
   int grid;
   if (G >= 1) {
     p.unit_mode = 0;
     p.counters = static_cast<unsigned int*>(workspace);
     p.rec_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + cbytes);
-    p.rec_ml = p.rec_o + static_cast<size_t>(G) * pl.streams * 2 * pl.GH * head_dim;
+    p.rec_ml = p.rec_o + static_cast<size_t>(G) * 2 * HS * head_dim;
     grid = static_cast<int>(G);
   } else {
     p.unit_mode = 1;
-    grid = static_cast<int>((pl.units + pl.streams - 1) / pl.streams);
+    grid = static_cast<int>(pl.units);
   }
-  if (pl.units > (1ll << 31) - 1) return fail(KVC_ERR_UNSUPPORTED, "too many (sequence, head) units");
-  if (pl.units * max_blocks_per_seq / (static_cast<int64_t>(grid) * pl.streams) + 1 >= (1ll << 31))
-    return fail(KVC_ERR_UNSUPPORTED, "too many cache blocks per page stream");
+  if (pl.units > (1ll << 31) - 1) return fail(KVC_ERR_UNSUPPORTED, "too many (sequence, kv-head chunk) units");
+  if (pl.units * max_blocks_per_seq / grid + 1 >= (1ll << 31))
+    return fail(KVC_ERR_UNSUPPORTED, "too many cache blocks per CTA");
+  if (num_blocks * n_kv_heads >= (1ll << 31))
+    return fail(KVC_ERR_UNSUPPORTED, "num_blocks x n_kv_heads must be below 2^31");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (dtype) {
     case KVC_F32: s = gqa_dispatch<float>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr); break;
@@ -286,7 +306,7 @@ kvc_status kvc_decode_attention_static(const void* q, const void* k_cache, const
                      dev->max_smem_optin, &pl)) != KVC_OK)
     return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(scratch, 0, counter_bytes(pl), st);
+  cudaError_t e = cudaMemsetAsync(scratch, 0, counter_bytes(batch, n_kv_heads, pl), st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(decode scratch counters)");
   return kvc_decode_attention(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale,
                               n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, dtype, out, out_dtype, scratch,

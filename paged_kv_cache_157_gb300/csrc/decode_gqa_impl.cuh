@@ -40,21 +40,33 @@
 
 namespace kvc {
 
-template <typename T, int D, int GH>
+template <typename T, int D, int GW>
 struct GqaCfg {
-  static constexpr int DPL = (D >= 64) ? 16 : 8;  // dims per lane
+  // Scores: a lane owns DPL head dimensions of RT rows of a 16-row tile.
+  static constexpr int DPL = (D >= 64) ? 16 : 8;   // dims per lane
   static constexpr int DP2 = DPL / 2;               // fp32 pairs per lane
   static constexpr int DL = D / DPL;                // lanes per row
   static constexpr int TL = 32 / DL;                // row groups per warp
-  static constexpr int RT = 16 / TL;                // rows per lane per 16-row tile
+  static constexpr int RT = 16 / TL;                // rows per lane per tile
   static constexpr int VEC = Elem<T>::kVec;         // elements per 16-byte chunk
   static constexpr int NCH = DPL / VEC;             // chunks per lane per row
-  static constexpr int NV = RT * GH;                // partial scores per lane per tile
-  static constexpr int NVF = NV >= DL ? NV / DL : 1;  // whole scores per lane after reduce-scatter
+  // The RT rows are reduced in NS sets of SR rows: SR * GW partial scores
+  // per set are reduce-scattered over the DL lanes of a row group.
+  static constexpr int SR0 = DL / GW > 2 ? DL / GW : 2;
+  static constexpr int SR = SR0 < RT ? SR0 : RT;    // rows per set
+  static constexpr int NS = RT / SR;                // sets per tile
+  static constexpr int NV = SR * GW;                // partial scores per set
+  static constexpr int NVF = NV >= DL ? NV / DL : 1;  // whole scores per lane per set
   static constexpr int DUP = NV >= DL ? 1 : DL / NV;  // lanes holding the same score
+  // Weighted sum of V: a lane owns VD dims of every row of its row group.
+  static constexpr int VL = D >= 64 ? 32 : D / 2;   // lanes per V row
+  static constexpr int VG = 32 / VL;                // V row groups
+  static constexpr int VD = D / VL;                 // dims per lane: 2, 4 or 8
+  static constexpr int NPAIR = 8 / VG;              // row pairs per lane per tile
   static_assert(DL * DPL == D && TL * DL == 32 && RT * TL == 16, "lane layout");
   static_assert(NCH * VEC == DPL, "chunking");
-  static_assert(RT % NVF == 0, "a lane's scores must belong to one head");
+  static_assert(NS * SR == RT && SR % NVF == 0, "a lane's scores must belong to one head");
+  static_assert(VL * VD == D && VG * VL == 32, "V lane layout");
 };
 
 // Number of cache blocks sequence b contributes (0 if its length is invalid).
@@ -116,147 +128,231 @@ __device__ __forceinline__ int64_t cta_of_block(int64_t b, int64_t G, int64_t N)
 __device__ __forceinline__ int64_t cta_range_start(int64_t c, int64_t G, int64_t N) { return c * N / G; }
 
 // Reduce-scatter of CUR partial values across the lanes of a row group
-// (xor masks B, B/2, ..., 1). Upper lanes keep the upper half at each step;
-// once one value is left the remaining steps all-reduce it.
+// (xor masks B, B/2, ..., 1) without selects: every lane keeps the lower
+// half of its registers and sends the upper half. This is correct because a
+// lane whose mask bit is set stores its partial values with the two halves
+// swapped at that level (register slot p holds logical value p ^ (NVF * dq)),
+// so the partner's upper half is exactly the logical half this lane keeps.
+// Once one value is left the remaining steps all-reduce it.
 template <int CUR, int B>
 struct ReduceScatter {
-  __device__ __forceinline__ static void run(float* s, int dq) {
+  __device__ __forceinline__ static void run(float* s) {
     if constexpr (B >= 1) {
       if constexpr (CUR > 1) {
         constexpr int H = CUR / 2;
-        const bool up = (dq & B) != 0;
 #pragma unroll
-        for (int t = 0; t < H; ++t) {
-          const float send = up ? s[t] : s[t + H];
-          const float keep = up ? s[t + H] : s[t];
-          s[t] = keep + __shfl_xor_sync(0xffffffffu, send, B);
-        }
-        ReduceScatter<H, B / 2>::run(s, dq);
+        for (int t = 0; t < H; ++t) s[t] += __shfl_xor_sync(0xffffffffu, s[t + H], B);
+        ReduceScatter<H, B / 2>::run(s);
       } else {
         s[0] += __shfl_xor_sync(0xffffffffu, s[0], B);
-        ReduceScatter<1, B / 2>::run(s, dq);
+        ReduceScatter<1, B / 2>::run(s);
       }
     }
   }
 };
 
-template <typename T, int D, int GH>
-struct WarpState {
-  using C = GqaCfg<T, D, GH>;
-  float2 q[GH][C::DP2];  // query, pre-scaled by scale*log2(e)
-  float2 o[GH][C::DP2];  // unnormalised output relative to m
-  float m[GH];           // reference maximum (log2 units), warp-uniform
-  float l;               // partial sum of this lane's weights (head h_lane)
+// Per-lane geometry of the tile loops, fixed for the whole kernel.
+template <typename T, int D, int GW>
+struct LaneGeo {
+  using C = GqaCfg<T, D, GW>;
+  int kofs[C::SR];  // element offset of the K row held in register slot r (set 0), plus the lane's dims
+  int mh;           // query-head permutation: register slot h holds head h ^ mh
+  int h_lane;       // head of the whole scores this lane holds after the reduction
+  int prow[C::NVF]; // tile row of score k of set 0 (set s adds s)
+  int vofs;         // element offset of the lane's V dims in row 0 of its row group
+  int vg;           // V row group
+  __device__ __forceinline__ void init(int lane) {
+    const int tq = lane / C::DL, dq = lane % C::DL;
+    const int M = C::NVF * (dq / C::DUP);  // logical index of register slot p is p ^ M
+    const int mr = M % C::SR;
+    mh = M / C::SR;
+    h_lane = mh;
+#pragma unroll
+    for (int r = 0; r < C::SR; ++r) kofs[r] = (tq * C::RT + (r ^ mr) * C::NS) * D + dq * C::VEC;
+#pragma unroll
+    for (int k = 0; k < C::NVF; ++k) prow[k] = tq * C::RT + (mr + k) * C::NS;
+    vg = lane / C::VL;
+    vofs = (lane % C::VL) * C::VD;
+  }
 };
 
-template <int GH>
-__device__ __forceinline__ float select_head(const float (&v)[GH], int h) {
+template <typename T, int D, int GW>
+struct WarpState {
+  using C = GqaCfg<T, D, GW>;
+  float2 q[GW][C::DP2];      // query slot h = head h ^ mh, pre-scaled by scale*log2(e)
+  float2 o[GW][C::VD];       // unnormalised output of head h, dim vofs+d: (even rows, odd rows)
+  float m[GW];               // reference maximum (log2 units), warp-uniform
+  float l;                   // partial sum of this lane's weights (head h_lane)
+};
+
+template <int GW>
+__device__ __forceinline__ float select_head(const float (&v)[GW], int h) {
   float r = v[0];
 #pragma unroll
-  for (int i = 1; i < GH; ++i) r = (h == i) ? v[i] : r;
+  for (int i = 1; i < GW; ++i) r = (h == i) ? v[i] : r;
   return r;
 }
 
-template <typename T, int NCH, int DL, int VEC>
-__device__ __forceinline__ void load_pairs(const T* rp, int dq, float2* f) {
+// VD consecutive elements of T as raw 32-bit words.
+template <typename T, int VD>
+struct VRow {
+  static constexpr int NW = (VD * static_cast<int>(sizeof(T)) + 3) / 4;
+  uint32_t w[NW];
+  __device__ __forceinline__ void load(const T* p) {
+    if constexpr (NW == 1) {
+      w[0] = *reinterpret_cast<const uint32_t*>(p);
+    } else if constexpr (NW == 2) {
+      const uint2 u = *reinterpret_cast<const uint2*>(p);
+      w[0] = u.x;
+      w[1] = u.y;
+    } else {
 #pragma unroll
-  for (int j = 0; j < NCH; ++j)
-    Elem<T>::unpack(lds128(rp + (dq + DL * j) * VEC), reinterpret_cast<float*>(f) + j * VEC);
-}
+      for (int i = 0; i < NW; i += 4) {
+        const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint32_t*>(p) + i);
+        w[i] = u.x;
+        w[i + 1] = u.y;
+        w[i + 2] = u.z;
+        w[i + 3] = u.w;
+      }
+    }
+  }
+  __device__ __forceinline__ float get(int d) const {
+    if constexpr (sizeof(T) == 4) {
+      return __uint_as_float(w[d]);
+    } else {
+      const uint32_t x = w[d / 2];
+      return Elem<T>::half_to_float(x, d & 1);
+    }
+  }
+};
 
 // One 16-row tile of a page: scores, online softmax, V accumulation.
-template <typename T, int D, int GH, bool PARTIAL>
-__device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __restrict__ vp, int valid,
-                                         WarpState<T, D, GH>& st, int tq, int dq, int lane, int h_lane) {
-  using C = GqaCfg<T, D, GH>;
-  float s[C::NV];
-  {
-    // All RT rows' raw K chunks first, then the RT*GH accumulators advance
-    // together over the lane's dims (independent FMA chains, unpacked lazily).
-    uint4 kr[C::RT][C::NCH];
+// sp is this warp's [GW][16] fp32 weight buffer.
+template <typename T, int D, int GW, bool PARTIAL>
+__device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __restrict__ vp, float* sp, int valid,
+                                         WarpState<T, D, GW>& st, const LaneGeo<T, D, GW>& g) {
+  using C = GqaCfg<T, D, GW>;
+  float sc[C::NS][C::NVF];
 #pragma unroll
-    for (int r = 0; r < C::RT; ++r) {
+  for (int set = 0; set < C::NS; ++set) {
+    // The SR rows' raw K chunks first, then the SR*GW accumulators advance
+    // together over the lane's dims (independent FMA chains).
+    uint4 kr[C::SR][C::NCH];
 #pragma unroll
-      for (int j = 0; j < C::NCH; ++j) kr[r][j] = lds128(kp + (r * C::TL + tq) * D + (dq + C::DL * j) * C::VEC);
+    for (int r = 0; r < C::SR; ++r) {
+#pragma unroll
+      for (int j = 0; j < C::NCH; ++j) kr[r][j] = lds128(kp + g.kofs[r] + set * D + C::DL * j * C::VEC);
     }
-    float2 acc[C::RT][GH];
+    float2 acc[C::SR][GW];
 #pragma unroll
     for (int j = 0; j < C::NCH; ++j) {
 #pragma unroll
       for (int c = 0; c < C::VEC / 2; ++c) {
         const int i = j * (C::VEC / 2) + c;
 #pragma unroll
-        for (int r = 0; r < C::RT; ++r) {
+        for (int r = 0; r < C::SR; ++r) {
           const float2 kf = Elem<T>::pair(kr[r][j], c);
 #pragma unroll
-          for (int h = 0; h < GH; ++h) acc[r][h] = (i == 0) ? fmul2(st.q[h][0], kf) : ffma2(st.q[h][i], kf, acc[r][h]);
+          for (int h = 0; h < GW; ++h) acc[r][h] = (i == 0) ? fmul2(st.q[h][0], kf) : ffma2(st.q[h][i], kf, acc[r][h]);
         }
       }
     }
+    float s[C::NV];
 #pragma unroll
-    for (int r = 0; r < C::RT; ++r) {
+    for (int h = 0; h < GW; ++h) {
 #pragma unroll
-      for (int h = 0; h < GH; ++h) s[h * C::RT + r] = acc[r][h].x + acc[r][h].y;
+      for (int r = 0; r < C::SR; ++r) s[h * C::SR + r] = acc[r][h].x + acc[r][h].y;
     }
+    ReduceScatter<C::NV, C::DL / 2>::run(s);
+#pragma unroll
+    for (int k = 0; k < C::NVF; ++k) sc[set][k] = s[k];
   }
-  ReduceScatter<C::NV, C::DL / 2>::run(s, dq);
 
-  // Score k of this lane has value index i = h*RT + r.
-  const int base_i = C::NV >= C::DL ? C::NVF * dq : dq / C::DUP;
-  float m_l = select_head<GH>(st.m, h_lane);
+  float m_l = select_head<GW>(st.m, g.h_lane);
   bool need = false;
 #pragma unroll
-  for (int k = 0; k < C::NVF; ++k) {
-    if (PARTIAL) {
-      const int r = (base_i + k) % C::RT;
-      if (r * C::TL + tq >= valid) s[k] = kNegInf;
+  for (int set = 0; set < C::NS; ++set) {
+#pragma unroll
+    for (int k = 0; k < C::NVF; ++k) {
+      if (PARTIAL && g.prow[k] + set >= valid) sc[set][k] = kNegInf;
+      need |= sc[set][k] > m_l + 8.0f;
     }
-    need |= s[k] > m_l + 8.0f;
   }
   if (__any_sync(0xffffffffu, need)) {
-    float loc = s[0];
+    float loc = kNegInf;
 #pragma unroll
-    for (int k = 1; k < C::NVF; ++k) loc = fmaxf(loc, s[k]);
+    for (int set = 0; set < C::NS; ++set) {
 #pragma unroll
-    for (int hh = 0; hh < GH; ++hh) {
-      const float tmax = warp_max(h_lane == hh ? loc : kNegInf);
+      for (int k = 0; k < C::NVF; ++k) loc = fmaxf(loc, sc[set][k]);
+    }
+#pragma unroll
+    for (int hh = 0; hh < GW; ++hh) {
+      const float tmax = warp_max(g.h_lane == hh ? loc : kNegInf);
       const float mn = fmaxf(st.m[hh], tmax);
       const float alpha = fast_exp2(st.m[hh] - mn);
       const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-      for (int i = 0; i < C::DP2; ++i) st.o[hh][i] = fmul2(st.o[hh][i], a2);
-      if (h_lane == hh) st.l *= alpha;
+      for (int d = 0; d < C::VD; ++d) st.o[hh][d] = fmul2(st.o[hh][d], a2);
+      if (g.h_lane == hh) st.l *= alpha;
       st.m[hh] = mn;
     }
-    m_l = select_head<GH>(st.m, h_lane);
+    m_l = select_head<GW>(st.m, g.h_lane);
   }
-  float p[C::NVF];
+  __syncwarp();  // the previous tile's reads of sp are done
 #pragma unroll
-  for (int k = 0; k < C::NVF; ++k) {
-    p[k] = fast_exp2(s[k] - m_l);
-    st.l += p[k];
-  }
-  float pa[C::NV];
-  const int grp = lane & ~(C::DL - 1);
+  for (int set = 0; set < C::NS; ++set) {
 #pragma unroll
-  for (int i = 0; i < C::NV; ++i) {
-    const int src = C::NV >= C::DL ? i / C::NVF : i * C::DUP;
-    const int k = C::NV >= C::DL ? i % C::NVF : 0;
-    pa[i] = __shfl_sync(0xffffffffu, p[k], grp | src);
-  }
-#pragma unroll
-  for (int r = 0; r < C::RT; ++r) {
-    float2 vf[C::DP2];
-    load_pairs<T, C::NCH, C::DL, C::VEC>(vp + (r * C::TL + tq) * D, dq, vf);
-    if (PARTIAL && r * C::TL + tq >= valid) {
-#pragma unroll
-      for (int i = 0; i < C::DP2; ++i) vf[i] = make_float2(0.f, 0.f);
+    for (int k = 0; k < C::NVF; ++k) {
+      const float pv = fast_exp2(sc[set][k] - m_l);
+      st.l += pv;
+      sc[set][k] = pv;
     }
+  }
+  if constexpr (C::NVF == 1 && C::NS == 2) {
+    // the lane's two weights are adjacent rows
+    *reinterpret_cast<float2*>(sp + g.h_lane * 16 + g.prow[0]) = make_float2(sc[0][0], sc[1][0]);
+  } else {
 #pragma unroll
-    for (int h = 0; h < GH; ++h) {
-      const float2 pp = make_float2(pa[h * C::RT + r], pa[h * C::RT + r]);
+    for (int set = 0; set < C::NS; ++set) {
 #pragma unroll
-      for (int i = 0; i < C::DP2; ++i) st.o[h][i] = ffma2(pp, vf[i], st.o[h][i]);
+      for (int k = 0; k < C::NVF; ++k) sp[g.h_lane * 16 + g.prow[k] + set] = sc[set][k];
+    }
+  }
+  __syncwarp();
+
+  // o[h][d] += (p[h][2k], p[h][2k+1]) * (v[2k][d], v[2k+1][d]): one packed
+  // FMA covers a row pair, so no weight or value needs duplicating.
+  float4 p4[GW];
+#pragma unroll
+  for (int kk = 0; kk < C::NPAIR; ++kk) {
+    const int k = kk * C::VG + g.vg;  // row pair
+    VRow<T, C::VD> va, vb;
+    va.load(vp + (2 * k) * D + g.vofs);
+    vb.load(vp + (2 * k + 1) * D + g.vofs);
+    float2 pp[GW];
+    if constexpr (C::VG == 1) {
+      // weights of row pairs k and k + 1 in one 16-byte load (sp is 16-byte aligned)
+      if ((kk & 1) == 0) {
+#pragma unroll
+        for (int h = 0; h < GW; ++h) p4[h] = *reinterpret_cast<const float4*>(sp + h * 16 + 2 * k);
+      }
+#pragma unroll
+      for (int h = 0; h < GW; ++h) pp[h] = (kk & 1) ? make_float2(p4[h].z, p4[h].w) : make_float2(p4[h].x, p4[h].y);
+    } else {
+#pragma unroll
+      for (int h = 0; h < GW; ++h) pp[h] = *reinterpret_cast<const float2*>(sp + h * 16 + 2 * k);
+    }
+    const bool za = PARTIAL && 2 * k >= valid, zb = PARTIAL && 2 * k + 1 >= valid;
+#pragma unroll
+    for (int d = 0; d < C::VD; ++d) {
+      float2 v = make_float2(va.get(d), vb.get(d));
+      if (PARTIAL) {
+        // rows past the context may hold anything (even NaN): their weight is 0
+        if (za) v.x = 0.f;
+        if (zb) v.y = 0.f;
+      }
+#pragma unroll
+      for (int h = 0; h < GW; ++h) st.o[h][d] = ffma2(pp[h], v, st.o[h][d]);
     }
   }
 }
@@ -266,27 +362,29 @@ __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __re
 __device__ __forceinline__ int64_t worker_of_block(int64_t b, int64_t W, int64_t N) { return ((b + 1) * W - 1) / N; }
 __device__ __forceinline__ int64_t worker_range_start(int64_t w, int64_t W, int64_t N) { return w * N / W; }
 
-// Global block index -> (kv head, sequence, head subgroup, block of the
-// sequence). Blocks are numbered kv head major, then sequence, then subgroup;
-// s_scan holds the exclusive prefix sums of the per-sequence block counts.
+// Global position -> (sequence, kv-head chunk, head subgroup, block of the
+// sequence). Positions are numbered sequence major, then chunk, then
+// subgroup, then block: gb = HN * scan[seq] + (chunk * n_hsub + hsub) * nb + j
+// with HN = n_chunks * n_hsub; s_scan holds the exclusive prefix sums of the
+// per-sequence block counts.
 struct BlockPos {
-  int kvh, seq, hsub, j, nb;
+  int chunk, seq, hsub, j, nb;
 };
 
-__device__ __forceinline__ BlockPos locate_block(int64_t gb, int64_t slab, const int* s_scan, int B, int n_hsub) {
+__device__ __forceinline__ BlockPos locate_block(int64_t gb, int HN, const int* s_scan, int B, int n_hsub) {
   BlockPos r;
-  r.kvh = static_cast<int>(gb / slab);
-  const int64_t rem = gb - r.kvh * slab;
-  int a = 0, b = B - 1;  // largest sequence with n_hsub * S[seq] <= rem (skips empty ones)
+  int a = 0, b = B - 1;  // largest sequence with HN * S[seq] <= gb (skips empty ones)
   while (a < b) {
     const int mid = (a + b + 1) >> 1;
-    if (static_cast<int64_t>(n_hsub) * s_scan[mid] <= rem) a = mid; else b = mid - 1;
+    if (static_cast<int64_t>(HN) * s_scan[mid] <= gb) a = mid; else b = mid - 1;
   }
   r.seq = a;
   r.nb = s_scan[a + 1] - s_scan[a];
-  const int r2 = static_cast<int>(rem - static_cast<int64_t>(n_hsub) * s_scan[a]);
-  r.hsub = r2 / r.nb;
-  r.j = r2 - r.hsub * r.nb;
+  const int r2 = static_cast<int>(gb - static_cast<int64_t>(HN) * s_scan[a]);
+  const int idx = r2 / r.nb;
+  r.chunk = idx / n_hsub;
+  r.hsub = idx - r.chunk * n_hsub;
+  r.j = r2 - idx * r.nb;
   return r;
 }
 
@@ -306,7 +404,7 @@ __device__ __forceinline__ int64_t record_of(int64_t c, int64_t c0, int64_t u0, 
 // lane r loads the (max, sum) pairs of record r while every lane loads its
 // chunks of the group's output rows, so one round trip serves the group.
 // Lane L owns the float4 chunks L + 32k of the warp's GW x D outputs.
-template <int D, int GH, int GW>
+template <int D, int HS, int GW>
 __device__ void merge_unit_warp(const GqaParams& p, int64_t u0, int nb, int64_t W, int64_t N, int seq, int hq0,
                                 int hoff, int lane) {
   constexpr int CH = D / 4;                  // float4 chunks per head
@@ -332,7 +430,7 @@ __device__ void merge_unit_warp(const GqaParams& p, int64_t u0, int nb, int64_t 
     float mr[GW], lr[GW];
 #pragma unroll
     for (int h = 0; h < GW; ++h) {
-      const float* ml = p.rec_ml + (rec * GH + hoff + h) * 2;
+      const float* ml = p.rec_ml + (rec * HS + hoff + h) * 2;
       mr[h] = rec >= 0 ? __ldcg(ml) : kNegInf;
       lr[h] = rec >= 0 ? __ldcg(ml + 1) : 0.f;
     }
@@ -344,7 +442,7 @@ __device__ void merge_unit_warp(const GqaParams& p, int64_t u0, int nb, int64_t 
 #pragma unroll
       for (int k = 0; k < NCK; ++k) {
         const bool ok = i < n && rr >= 0 && lane + 32 * k < GW * CH;
-        ov[i][k] = ok ? __ldcg(reinterpret_cast<const float4*>(rbase + rr * GH * D + 128 * k))
+        ov[i][k] = ok ? __ldcg(reinterpret_cast<const float4*>(rbase + rr * HS * D + 128 * k))
                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
@@ -404,52 +502,73 @@ __device__ void merge_unit_warp(const GqaParams& p, int64_t u0, int nb, int64_t 
   }
 }
 
+// Shared-memory atomic add with acquire-release semantics at CTA scope: the
+// reads of a stage that precede it (ordered by a warp barrier) happen before
+// the refill that the last releasing warp issues after it.
+__device__ __forceinline__ unsigned int atomic_add_acq_rel_cta_smem(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_addr(p)), "r"(v) : "memory");
+  return old;
+}
+
 template <typename T, int D, int GH>
-__global__ void __launch_bounds__(kGqaWarps * 32, 2) gqa_decode_kernel(const GqaParams p) {
-  constexpr int HW = gqa_warps_per_stream(GH);  // warps sharing one page stream
+__global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kernel(const GqaParams p) {
+  constexpr int HW = gqa_warps_per_kvhead(GH);  // warps per kv head
   constexpr int GW = GH / HW;                    // query heads per warp
-  constexpr int NP = kGqaWarps / HW;             // page streams (workers) per CTA
+  constexpr int HCM = kGqaWarps / HW;            // kv heads per CTA at most
+  constexpr int HS = HCM * GH;                   // query heads per record
   using C = GqaCfg<T, D, GW>;
-  static_assert(GW * HW == GH && kGqaWarps % HW == 0, "head split over the warps of a stream");
+  static_assert(GW * HW == GH && kGqaWarps % HW == 0, "head split over the warps of a kv head");
   static_assert(D % 32 == 0, "merge lanes own D / 32 dims");
   extern __shared__ __align__(128) unsigned char smem[];
-  const GqaSmem L = gqa_smem_layout(sizeof(T), D, GH, p.block_size, p.stages, p.batch);
+  const int hc = p.hc;
+  const GqaSmem L = gqa_smem_layout(sizeof(T), D, GH, p.block_size, hc, p.stages, p.batch);
   T* s_stage = reinterpret_cast<T*>(smem + L.stage_off);
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + L.bar_off);  // [NP * S] full, then [NP * S] empty
+  uint64_t* fbar = reinterpret_cast<uint64_t*>(smem + L.bar_off);  // [S] full
+  unsigned int* s_rel = reinterpret_cast<unsigned int*>(smem + L.rel_off);  // [S] releases seen
+  unsigned int* s_iss = s_rel + p.stages;  // [S] fills issued
+  volatile int* s_misc = reinterpret_cast<volatile int*>(smem + L.misc_off);  // [abort, last0, last1]
   int* s_scan = reinterpret_cast<int*>(smem + L.scan_off);
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int sp = w / HW, hw = w % HW;  // stream (worker) of this warp, and its share of the heads
-  const bool issuer = (hw == 0);       // lane 0 of the stream's first warp issues the copies
-  const int tq = lane / C::DL, dq = lane % C::DL;
-  const int base_i = C::NV >= C::DL ? C::NVF * dq : dq / C::DUP;
-  const int h_lane = base_i / C::RT;
+  const int kh = w / HW, hw = w % HW;  // kv head of the chunk and share of its query heads
+  const int nact = hc * HW;            // warps with work
+  const bool active = w < nact;
+  LaneGeo<T, D, GW> geo;
+  geo.init(lane);
   const int bs = p.block_size, S = p.stages;
   const int B = p.batch;
   const int tiles_per_page = bs / 16;
   const int page_elems = bs * D;
-  const int stage_elems = 2 * page_elems + GH * D;  // K page, V page, the unit's query rows
-  const uint32_t page_bytes = static_cast<uint32_t>(page_elems * sizeof(T));
-  const uint32_t q_bytes = static_cast<uint32_t>(GH * D * sizeof(T));
+  const int chunk_elems = hc * page_elems;
+  const int stage_elems = 2 * chunk_elems + hc * GH * D;  // K chunk, V chunk, the unit's query rows
+  const uint32_t chunk_bytes = static_cast<uint32_t>(chunk_elems * sizeof(T));
   const T* kc = static_cast<const T*>(p.k_cache);
   const T* vc = static_cast<const T*>(p.v_cache);
   const T* qg = static_cast<const T*>(p.q);
   const uint32_t full = 0xffffffffu;
+  const int HN = p.n_chunks * p.n_hsub;
+  const bool q_contig = (GH == p.group);  // the chunk's query rows are one contiguous run
 
-  if (tid < NP * S) {
-    mbar_init(s_bar + tid, 1);            // full: one arrive (with the copy bytes)
-    mbar_init(s_bar + NP * S + tid, HW);  // empty: every warp of the stream releases
+  if (tid < S) {
+    mbar_init(fbar + tid, 1);  // one arrive (with the copy bytes) per fill
+    s_rel[tid] = 0u;
+    s_iss[tid] = 0u;
+  }
+  if (tid == 0) {
+    s_misc[0] = 0;
+    s_misc[1] = 0;
+    s_misc[2] = 0;
   }
   fence_barrier_init();
   scan_blocks(p.context_lens, B, bs, p.max_blocks, s_scan);  // ends with a CTA barrier
-  const int64_t slab = static_cast<int64_t>(p.n_hsub) * s_scan[B];
-  const int64_t N = slab * p.n_kv_heads;
-  const int64_t W = static_cast<int64_t>(gridDim.x) * NP;
-  const int64_t wk = static_cast<int64_t>(blockIdx.x) * NP + sp;
+  const int64_t N = static_cast<int64_t>(HN) * s_scan[B];
+  const int64_t G = gridDim.x;
+  const int64_t c = blockIdx.x;
 
   if (blockIdx.x == 0) {
     // Validate every length once; in the split mode CTA 0 also writes the
-    // zero outputs of sequences whose length is invalid (no worker visits them).
+    // zero outputs of sequences whose length is invalid (no CTA visits them).
     for (int b = tid; b < B; b += blockDim.x) {
       const int n = __ldg(p.context_lens + b);
       if (n < 1 || n > bs * p.max_blocks) set_flag(p.err, 0x2u);
@@ -462,287 +581,279 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 2) gqa_decode_kernel(const Gqa
       }
     }
   }
-  // No CTA-wide barrier below this point: every stream runs on its own.
 
   int64_t lo, hi;
   if (p.unit_mode) {
-    // worker u takes unit u = (kv head, sequence, subgroup) whole
-    const int64_t units = static_cast<int64_t>(p.n_kv_heads) * B * p.n_hsub;
-    if (wk >= units) return;
-    const int hsub = static_cast<int>(wk % p.n_hsub);
-    const int seq = static_cast<int>((wk / p.n_hsub) % B);
-    const int kvh = static_cast<int>(wk / (static_cast<int64_t>(p.n_hsub) * B));
+    // CTA u takes unit u = (sequence, chunk, subgroup) whole
+    const int seq = static_cast<int>(c / HN);
+    const int idx = static_cast<int>(c - static_cast<int64_t>(seq) * HN);
     const int nb = s_scan[seq + 1] - s_scan[seq];
     if (nb == 0) {
-      // invalid length: zero output for this warp's heads
-      const int hq0 = kvh * p.group + hsub * GH + hw * GW;
-      for (int idx = lane; idx < GW * D; idx += 32)
-        store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + hq0) * D + idx, 0.f, p.out_dtype);
+      // invalid length: zero output for this CTA's heads
+      if (active) {
+        const int chunk = idx / p.n_hsub, hsub = idx - chunk * p.n_hsub;
+        const int hq0 = (chunk * hc + kh) * p.group + hsub * GH + hw * GW;
+        for (int i = lane; i < GW * D; i += 32)
+          store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + hq0) * D + i, 0.f, p.out_dtype);
+      }
       return;
     }
-    lo = kvh * slab + static_cast<int64_t>(p.n_hsub) * s_scan[seq] + static_cast<int64_t>(hsub) * nb;
+    lo = static_cast<int64_t>(HN) * s_scan[seq] + static_cast<int64_t>(idx) * nb;
     hi = lo + nb;
   } else {
-    lo = worker_range_start(wk, W, N);
-    hi = worker_range_start(wk + 1, W, N);
+    lo = cta_range_start(c, G, N);
+    hi = cta_range_start(c + 1, G, N);
   }
-  const int total = static_cast<int>(hi - lo);  // blocks (positions) of this worker
-  if (total <= 0) return;
+  const int total = static_cast<int>(hi - lo);  // positions of this CTA
+  if (total <= 0) return;                       // uniform over the CTA
 
-  T* wst = s_stage + static_cast<size_t>(sp) * S * stage_elems;
-  uint64_t* fbar = s_bar + sp * S;
-  uint64_t* ebar = s_bar + NP * S + sp * S;
+  T* my_k = s_stage + kh * page_elems;                       // + slot * stage_elems
+  T* my_v = s_stage + chunk_elems + kh * page_elems;
+  float* wp = reinterpret_cast<float*>(smem + L.p_off) + w * GW * 16;  // this warp's weights
   const uint64_t pol = policy_evict_first();
 
-  // Positions lo + 32*win + lane, one per lane: the element offset of the
-  // K/V page (-1 if the table entry is out of range) and, for the first
-  // block of a segment, the element offset of the unit's query rows.
-  auto window = [&](int win, int64_t& src, int& qoff) {
+  // Positions lo + 32*win + lane, one per lane: the page index (block *
+  // n_kv_heads + first kv head of the chunk; -1 if the table entry is out of
+  // range) and, for the first block of a segment, the element offset of the
+  // unit's first query row (-1 otherwise).
+  auto window = [&](int win, int& src, int& qoff) {
     const int64_t pos = lo + static_cast<int64_t>(win) * 32 + lane;
     src = -1;
     qoff = -1;
     if (pos < hi) {
-      const BlockPos bp = locate_block(pos, slab, s_scan, B, p.n_hsub);
+      const BlockPos bp = locate_block(pos, HN, s_scan, B, p.n_hsub);
       const int phys = __ldg(p.block_tables + static_cast<int64_t>(bp.seq) * p.max_blocks + bp.j);
-      if (phys >= 0 && phys < p.num_blocks)
-        src = (static_cast<int64_t>(phys) * p.n_kv_heads + bp.kvh) * page_elems;
-      if (pos == lo || bp.j == 0) qoff = (bp.seq * p.n_q_heads + bp.kvh * p.group + bp.hsub * GH) * D;
+      if (phys >= 0 && phys < p.num_blocks) src = phys * p.n_kv_heads + bp.chunk * hc;
+      if (pos == lo || bp.j == 0)
+        qoff = (bp.seq * p.n_q_heads + bp.chunk * hc * p.group + bp.hsub * GH) * D;
     }
   };
-  // Copies of position x into stage `slot` (lane 0 only).
-  auto issue = [&](int slot, int64_t src, int qoff) {
-    const uint32_t bytes = (src >= 0 ? 2 * page_bytes : 0u) + (qoff >= 0 ? q_bytes : 0u);
+  // Copies of one position into stage `slot` (one thread).
+  auto issue = [&](int slot, int src, int qoff) {
+    const uint32_t q_bytes = static_cast<uint32_t>(hc * GH * D * sizeof(T));
+    const uint32_t bytes = (src >= 0 ? 2 * chunk_bytes : 0u) + (qoff >= 0 ? q_bytes : 0u);
     if (src < 0) set_flag(p.err, 0x1u);
+    atomicAdd(s_iss + slot, 1u);
     if (bytes == 0) {
       mbar_arrive(fbar + slot);
       return;
     }
-    T* dst = wst + slot * stage_elems;
+    T* dst = s_stage + static_cast<size_t>(slot) * stage_elems;
     mbar_arrive_expect_tx(fbar + slot, bytes);
     if (src >= 0) {
-      bulk_g2s(dst, kc + src, page_bytes, fbar + slot, pol);
-      bulk_g2s(dst + page_elems, vc + src, page_bytes, fbar + slot, pol);
+      const int64_t e = static_cast<int64_t>(src) * page_elems;
+      bulk_g2s(dst, kc + e, chunk_bytes, fbar + slot, pol);
+      bulk_g2s(dst + chunk_elems, vc + e, chunk_bytes, fbar + slot, pol);
     }
-    if (qoff >= 0) bulk_g2s(dst + 2 * page_elems, qg + qoff, q_bytes, fbar + slot, pol);
+    if (qoff >= 0) {
+      if (q_contig) {
+        bulk_g2s(dst + 2 * chunk_elems, qg + qoff, q_bytes, fbar + slot, pol);
+      } else {
+        const uint32_t rb = static_cast<uint32_t>(GH * D * sizeof(T));
+        for (int h = 0; h < hc; ++h)
+          bulk_g2s(dst + 2 * chunk_elems + h * GH * D, qg + qoff + h * p.group * D, rb, fbar + slot, pol);
+      }
+    }
   };
 
-  int64_t w_src0, w_src1 = -1;
-  int w_q0, w_q1 = -1;
+  int w_src0, w_src1 = -1, w_q0, w_q1 = -1;
   window(0, w_src0, w_q0);
   if (total > 32) window(1, w_src1, w_q1);
 
-  // The ring runs ahead across segment boundaries: position x always sits in
-  // stage x % S, and the copy of x + S is issued as soon as x is consumed.
+  // Warp 0 fills the first S stages; after that the warp that releases a
+  // stage last (its release count reaches nact per fill) refills it, so no
+  // warp waits for another except through the "full" barriers.
   const int n_first = total < S ? total : S;
-  if (issuer) {
+  if (w == 0) {
     for (int i = 0; i < n_first; ++i) {
-      const int64_t src = __shfl_sync(full, w_src0, i);
+      const int src = __shfl_sync(full, w_src0, i);
       const int qo = __shfl_sync(full, w_q0, i);
       if (lane == 0) issue(i, src, qo);
     }
   }
-  int issued = n_first;
   __syncwarp();
 
   // Partial segments (at most two: the one starting at lo, the one ending
   // at hi) whose records wait to be counted.
   bool pend0 = false, pend1 = false;
-  int64_t p0_u0 = 0, p1_u0 = 0, p0_unit = 0, p1_unit = 0;
-  int p0_nb = 0, p1_nb = 0, p0_seq = 0, p1_seq = 0, p0_h0 = 0, p1_h0 = 0;
+  bool aborted = false;
 
-  int slot = 0;
-  uint32_t par = 0;
-  int c = 0;              // positions consumed
-  int drain_from = -1;    // first position not consumed when a wait gave up
-  int64_t gb = lo;
-  while (gb < hi) {
-    // ---- segment: the part of one unit inside [lo, hi)
-    const BlockPos sg = locate_block(gb, slab, s_scan, B, p.n_hsub);
-    const int seg_len = static_cast<int>(((sg.nb - sg.j) < (hi - gb)) ? (sg.nb - sg.j) : (hi - gb));
-    const int n_rows = seq_rows(p.context_lens, sg.seq, bs, p.max_blocks);
-    const int h0 = sg.kvh * p.group + sg.hsub * GH;  // first query head of the unit
-    const int hq0 = h0 + hw * GW;                    // first query head of this warp
+  if (active) {
+    int slot = 0;
+    uint32_t par = 0, fill = 0;  // phase parity and fill number of `slot`
+    int cpos = 0;                // positions consumed
+    int64_t gb = lo;
+    while (gb < hi) {
+      // ---- segment: the part of one unit inside [lo, hi)
+      const BlockPos sg = locate_block(gb, HN, s_scan, B, p.n_hsub);
+      const int seg_len = static_cast<int>(((sg.nb - sg.j) < (hi - gb)) ? (sg.nb - sg.j) : (hi - gb));
+      const int n_rows = seq_rows(p.context_lens, sg.seq, bs, p.max_blocks);
+      const int hq0 = (sg.chunk * hc + kh) * p.group + sg.hsub * GH + hw * GW;  // first query head of this warp
 
-    WarpState<T, D, GW> st;
-    for (int t = 0; t < seg_len; ++t, ++c) {
-      if (c > 0 && (c & 31) == 0) {
-        w_src0 = w_src1;
-        w_q0 = w_q1;
-        w_src1 = -1;
-        w_q1 = -1;
-        if (c + 32 < total) window((c >> 5) + 1, w_src1, w_q1);
-      }
-      const int64_t src = __shfl_sync(full, w_src0, c & 31);
-      const int cn = c + S;
-      const bool in_cur = (cn >> 5) == (c >> 5);
-      const int64_t src_n = __shfl_sync(full, in_cur ? w_src0 : w_src1, cn & 31);
-      const int q_n = __shfl_sync(full, in_cur ? w_q0 : w_q1, cn & 31);
-      const bool ok = mbar_wait_bounded(fbar + slot, par);
-      if (__any_sync(full, !ok)) {
-        drain_from = c;
-        if (lane == 0) set_flag(p.err, 0x8u);
-        break;
-      }
-      const T* kp = wst + slot * stage_elems;
-      if (t == 0) {
-        // the unit's query rows came with its first page
-        const T* qs = kp + 2 * page_elems + hw * GW * D;
-#pragma unroll
-        for (int h = 0; h < GW; ++h) {
-          float f[C::DPL];
-#pragma unroll
-          for (int j = 0; j < C::NCH; ++j)
-            Elem<T>::unpack(lds128(qs + h * D + (dq + C::DL * j) * C::VEC), f + j * C::VEC);
-#pragma unroll
-          for (int i = 0; i < C::DP2; ++i) {
-            st.q[h][i] = make_float2(f[2 * i] * p.qscale, f[2 * i + 1] * p.qscale);
-            st.o[h][i] = make_float2(0.f, 0.f);
-          }
-          st.m[h] = kNegInf;
+      WarpState<T, D, GW> st;
+      for (int t = 0; t < seg_len; ++t, ++cpos) {
+        if (cpos > 0 && (cpos & 31) == 0) {
+          w_src0 = w_src1;
+          w_q0 = w_q1;
+          w_src1 = -1;
+          w_q1 = -1;
+          if (cpos + 32 < total) window((cpos >> 5) + 1, w_src1, w_q1);
         }
-        st.l = 0.f;
-      }
-      if (src >= 0) {
-        const T* vp = kp + page_elems;
-        const int vr = min(bs, n_rows - (sg.j + t) * bs);
-        if (vr >= bs) {
-          for (int tt = 0; tt < tiles_per_page; ++tt)
-            gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, 16, st, tq, dq, lane, h_lane);
-        } else {
-          for (int tt = 0; tt < tiles_per_page; ++tt) {
-            const int valid = vr - tt * 16;
-            if (valid <= 0) break;
-            if (valid >= 16)
-              gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, 16, st, tq, dq, lane, h_lane);
-            else
-              gqa_tile<T, D, GW, true>(kp + tt * 16 * D, vp + tt * 16 * D, valid, st, tq, dq, lane, h_lane);
+        const int src = __shfl_sync(full, w_src0, cpos & 31);
+        const int cn = cpos + S;
+        const bool in_cur = (cn >> 5) == (cpos >> 5);
+        const int src_n = __shfl_sync(full, in_cur ? w_src0 : w_src1, cn & 31);
+        const int q_n = __shfl_sync(full, in_cur ? w_q0 : w_q1, cn & 31);
+        const bool ok = mbar_wait_bounded(fbar + slot, par);
+        if (__any_sync(full, !ok) || s_misc[0]) {
+          if (lane == 0) {
+            set_flag(p.err, 0x8u);
+            s_misc[0] = 1;
           }
+          aborted = true;
+          break;
         }
-      }
-      // Every shared-memory read of this stage fed an instruction issued
-      // before this point, so no read of it is outstanding once released.
-      __syncwarp();
-      if (HW > 1 && lane == 0) mbar_arrive(ebar + slot);
-      if (issuer && cn < total) {
-        if (HW > 1) {
-          // refill once every warp of the stream has released the stage
-          bool ok2 = true;
-          if (lane == 0) ok2 = mbar_wait_bounded(ebar + slot, par);
-          if (!__shfl_sync(full, ok2 ? 1 : 0, 0)) {
-            drain_from = c + 1;
-            if (lane == 0) set_flag(p.err, 0x8u);
-            break;
+        const T* stg = s_stage + static_cast<size_t>(slot) * stage_elems;
+        if (t == 0) {
+          // The unit's query rows came with its first position. Register slot
+          // h holds head h ^ mh (the lane's reduction order).
+          const T* qs = stg + 2 * chunk_elems + (kh * GH + hw * GW) * D + (geo.kofs[0] % D);
+#pragma unroll
+          for (int h = 0; h < GW; ++h) {
+            float f[C::DPL];
+            const T* qh = qs + (h ^ geo.mh) * D;
+#pragma unroll
+            for (int j = 0; j < C::NCH; ++j) Elem<T>::unpack(lds128(qh + C::DL * j * C::VEC), f + j * C::VEC);
+#pragma unroll
+            for (int i = 0; i < C::DP2; ++i) st.q[h][i] = make_float2(f[2 * i] * p.qscale, f[2 * i + 1] * p.qscale);
+#pragma unroll
+            for (int d = 0; d < C::VD; ++d) st.o[h][d] = make_float2(0.f, 0.f);
+            st.m[h] = kNegInf;
+          }
+          st.l = 0.f;
+        }
+        if (src >= 0) {
+          const T* kp = my_k + static_cast<size_t>(slot) * stage_elems;
+          const T* vp = my_v + static_cast<size_t>(slot) * stage_elems;
+          const int vr = min(bs, n_rows - (sg.j + t) * bs);
+          if (vr >= bs) {
+            for (int tt = 0; tt < tiles_per_page; ++tt)
+              gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, 16, st, geo);
+          } else {
+            for (int tt = 0; tt < tiles_per_page; ++tt) {
+              const int valid = vr - tt * 16;
+              if (valid <= 0) break;
+              if (valid >= 16)
+                gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, 16, st, geo);
+              else
+                gqa_tile<T, D, GW, true>(kp + tt * 16 * D, vp + tt * 16 * D, wp, valid, st, geo);
+            }
           }
         }
-        if (lane == 0) issue(slot, src_n, q_n);
-        ++issued;
+        // Every shared-memory read of this stage fed an instruction issued
+        // before this barrier, so none is outstanding once it is released.
+        __syncwarp();
+        if (lane == 0) {
+          const unsigned int old = atomic_add_acq_rel_cta_smem(s_rel + slot, 1u);
+          if (old + 1 == static_cast<unsigned int>(nact) * (fill + 1) && cn < total) issue(slot, src_n, q_n);
+        }
+        __syncwarp();
+        if (++slot == S) {
+          slot = 0;
+          par ^= 1u;
+          ++fill;
+        }
       }
-      __syncwarp();
-      if (++slot == S) {
-        slot = 0;
-        par ^= 1u;
-      }
-    }
-    if (drain_from >= 0) break;
+      if (aborted) break;
 
-    // ---- finish the segment: this warp holds every row of it for its heads
-#pragma unroll
-    for (int msk = C::DL; msk < 32; msk <<= 1) {
+      // ---- finish the segment: this warp holds every row of it for its heads
+      float ov[GW][C::VD];
 #pragma unroll
       for (int h = 0; h < GW; ++h) {
 #pragma unroll
-        for (int i = 0; i < C::DP2; ++i) {
-          st.o[h][i].x += __shfl_xor_sync(full, st.o[h][i].x, msk);
-          st.o[h][i].y += __shfl_xor_sync(full, st.o[h][i].y, msk);
+        for (int d = 0; d < C::VD; ++d) {
+          float v = st.o[h][d].x + st.o[h][d].y;
+#pragma unroll
+          for (int msk = C::VL; msk < 32; msk <<= 1) v += __shfl_xor_sync(full, v, msk);
+          ov[h][d] = v;
         }
       }
-    }
-    float lw[GW];
+      float lw[GW];
 #pragma unroll
-    for (int hh = 0; hh < GW; ++hh) lw[hh] = warp_sum(h_lane == hh ? st.l : 0.f) * (1.0f / C::DUP);
-    const bool whole = (sg.j == 0 && seg_len == sg.nb);
-    if (whole) {
-      if (tq == 0) {
+      for (int hh = 0; hh < GW; ++hh) lw[hh] = warp_sum(geo.h_lane == hh ? st.l : 0.f) * (1.0f / C::DUP);
+      const bool whole = (sg.j == 0 && seg_len == sg.nb);
+      if (whole) {
+        if (geo.vg == 0) {
 #pragma unroll
-        for (int h = 0; h < GW; ++h) {
-          const float inv = 1.0f / lw[h];
-          const int64_t ob = (static_cast<int64_t>(sg.seq) * p.n_q_heads + hq0 + h) * D;
+          for (int h = 0; h < GW; ++h) {
+            const float inv = 1.0f / lw[h];
+            const int64_t ob = (static_cast<int64_t>(sg.seq) * p.n_q_heads + hq0 + h) * D + geo.vofs;
 #pragma unroll
-          for (int j = 0; j < C::NCH; ++j) {
-#pragma unroll
-            for (int e = 0; e < C::VEC; e += 2) {
-              const float2 v = st.o[h][(j * C::VEC + e) / 2];
-              const int d = (dq + C::DL * j) * C::VEC + e;
-              store_out(p.out, ob + d, v.x * inv, p.out_dtype);
-              store_out(p.out, ob + d + 1, v.y * inv, p.out_dtype);
-            }
+            for (int d = 0; d < C::VD; ++d) ov[h][d] *= inv;
+            store_out_vec<C::VD>(p.out, ob, ov[h], p.out_dtype);
           }
         }
-      }
-    } else {
-      // Record (max, sum, unnormalised output) for this warp's heads; the
-      // last worker of the unit to finish merges all of them.
-      const int64_t rec = wk * 2 + (gb == lo ? 0 : 1);
-      if (tq == 0) {
-#pragma unroll
-        for (int h = 0; h < GW; ++h) {
-          float* ro = p.rec_o + (rec * GH + hw * GW + h) * D;
-#pragma unroll
-          for (int j = 0; j < C::NCH; ++j) {
-#pragma unroll
-            for (int e = 0; e < C::VEC; e += 4) {
-              const float2 a = st.o[h][(j * C::VEC + e) / 2], b = st.o[h][(j * C::VEC + e) / 2 + 1];
-              *reinterpret_cast<float4*>(ro + (dq + C::DL * j) * C::VEC + e) = make_float4(a.x, a.y, b.x, b.y);
-            }
-          }
-        }
-      }
-      if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < GW; ++h) {
-          p.rec_ml[(rec * GH + hw * GW + h) * 2] = st.m[h];
-          p.rec_ml[(rec * GH + hw * GW + h) * 2 + 1] = lw[h];
-        }
-      }
-      // counted (and merged, if this worker is the unit's last) once the
-      // whole range is done, so that no wait on the count stalls the stream
-      if (gb == lo) {
-        pend0 = true;
-        p0_u0 = gb - sg.j;
-        p0_nb = sg.nb;
-        p0_seq = sg.seq;
-        p0_h0 = h0;
-        p0_unit = (static_cast<int64_t>(sg.kvh) * B + sg.seq) * p.n_hsub + sg.hsub;
       } else {
-        pend1 = true;
-        p1_u0 = gb - sg.j;
-        p1_nb = sg.nb;
-        p1_seq = sg.seq;
-        p1_h0 = h0;
-        p1_unit = (static_cast<int64_t>(sg.kvh) * B + sg.seq) * p.n_hsub + sg.hsub;
+        // Record (max, sum, unnormalised output) for this warp's heads; the
+        // last CTA of the unit to finish merges all of them.
+        const int64_t rec = c * 2 + (gb == lo ? 0 : 1);
+        const int hr = kh * GH + hw * GW;  // first head of this warp within the record
+        if (geo.vg == 0) {
+#pragma unroll
+          for (int h = 0; h < GW; ++h) {
+            float* ro = p.rec_o + (rec * HS + hr + h) * D + geo.vofs;
+#pragma unroll
+            for (int d = 0; d < C::VD; d += 2) *reinterpret_cast<float2*>(ro + d) = make_float2(ov[h][d], ov[h][d + 1]);
+          }
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < GW; ++h) {
+            p.rec_ml[(rec * HS + hr + h) * 2] = st.m[h];
+            p.rec_ml[(rec * HS + hr + h) * 2 + 1] = lw[h];
+          }
+        }
+        if (gb == lo) pend0 = true; else pend1 = true;
       }
+      gb += seg_len;
     }
-    gb += seg_len;
+  } else {
+    // idle warp: still walk the segments so that pend0 / pend1 agree
+    int64_t gb = lo;
+    while (gb < hi) {
+      const BlockPos sg = locate_block(gb, HN, s_scan, B, p.n_hsub);
+      const int seg_len = static_cast<int>(((sg.nb - sg.j) < (hi - gb)) ? (sg.nb - sg.j) : (hi - gb));
+      if (!(sg.j == 0 && seg_len == sg.nb)) {
+        if (gb == lo) pend0 = true; else pend1 = true;
+      }
+      gb += seg_len;
+    }
   }
-  if (drain_from < 0 && (pend0 || pend1)) {
-    // Count this worker's records (lane 0: the segment at lo, lane 1: the
-    // one ending at hi); the add that completes a unit's count makes its
-    // caller the unit's merger and resets the counter for the next call.
-    __syncwarp();
-    int last = 0;
-    if (lane < 2 && (lane == 0 ? pend0 : pend1)) {
+
+  // Records are complete once every warp passes this barrier; one thread
+  // counts them per unit, and the add that completes a unit's count makes
+  // this CTA the unit's merger (it then resets the counter for the next call).
+  __threadfence();
+  __syncthreads();
+  const bool any_abort = s_misc[0] != 0;
+  if (!any_abort && (pend0 || pend1)) {
+    const BlockPos q0 = locate_block(lo, HN, s_scan, B, p.n_hsub);
+    const BlockPos q1 = locate_block(hi - 1, HN, s_scan, B, p.n_hsub);
+    const int64_t p0_u0 = lo - q0.j, p1_u0 = hi - 1 - q1.j;
+    if (w == 0 && lane < 2 && (lane == 0 ? pend0 : pend1)) {
+      const BlockPos& qq = lane == 0 ? q0 : q1;
       const int64_t u0 = lane == 0 ? p0_u0 : p1_u0;
-      const int nbu = lane == 0 ? p0_nb : p1_nb;
-      const int64_t unit = lane == 0 ? p0_unit : p1_unit;
-      const int64_t c0 = worker_of_block(u0, W, N), c1 = worker_of_block(u0 + nbu - 1, W, N);
+      const int64_t c0 = worker_of_block(u0, G, N), c1 = worker_of_block(u0 + qq.nb - 1, G, N);
       int64_t contributors = c1 - c0 + 1;
-      if (N < W) {
+      if (N < G) {
         contributors = 0;
         for (int64_t x = c0; x <= c1; ++x)
-          contributors += (worker_range_start(x, W, N) != worker_range_start(x + 1, W, N)) ? 1 : 0;
+          contributors += (worker_range_start(x, G, N) != worker_range_start(x + 1, G, N)) ? 1 : 0;
       }
-      unsigned int* ctr = p.counters + unit * HW + hw;
+      const int64_t unit = (static_cast<int64_t>(qq.seq) * p.n_chunks + qq.chunk) * p.n_hsub + qq.hsub;
+      unsigned int* ctr = p.counters + unit;
       const unsigned int old = atomic_add_acq_rel_gpu(ctr, 1u);
+      int last = 0;
       if (old + 1 == static_cast<unsigned int>(contributors)) {
         last = 1;
         *ctr = 0u;
@@ -750,16 +861,29 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 2) gqa_decode_kernel(const Gqa
         set_flag(p.err, 0x10u);  // the workspace counters were not zero
         atomicExch(ctr, 0u);
       }
+      s_misc[1 + lane] = last;
     }
-    // the warp barrier orders the other lanes' record reads after the acquire
-    const int last0 = __shfl_sync(full, last, 0), last1 = __shfl_sync(full, last, 1);
-    if (last0) merge_unit_warp<D, GH, GW>(p, p0_u0, p0_nb, W, N, p0_seq, p0_h0 + hw * GW, hw * GW, lane);
-    if (last1) merge_unit_warp<D, GH, GW>(p, p1_u0, p1_nb, W, N, p1_seq, p1_h0 + hw * GW, hw * GW, lane);
+    __syncthreads();
+    if (active) {
+      // the barrier orders every warp's record reads after thread 0's acquire
+      if (s_misc[1]) {
+        const int h0 = (q0.chunk * hc + kh) * p.group + q0.hsub * GH + hw * GW;
+        merge_unit_warp<D, HS, GW>(p, p0_u0, q0.nb, G, N, q0.seq, h0, kh * GH + hw * GW, lane);
+      }
+      if (s_misc[2]) {
+        const int h1 = (q1.chunk * hc + kh) * p.group + q1.hsub * GH + hw * GW;
+        merge_unit_warp<D, HS, GW>(p, p1_u0, q1.nb, G, N, q1.seq, h1, kh * GH + hw * GW, lane);
+      }
+    }
   }
-  if (drain_from >= 0 && issuer) {
-    // Copies issued but not consumed (at most S) must land before the CTA
-    // can exit and its shared memory be reused.
-    for (int x = drain_from; x < issued; ++x) (void)mbar_wait_bounded(fbar + x % S, (x / S) & 1u);
+  if (any_abort && tid == 0) {
+    // Copies that may still be in flight must land before the CTA exits and
+    // its shared memory is reused: wait (bounded) for the latest issued fill
+    // of every stage.
+    for (int x = 0; x < S; ++x) {
+      const unsigned int n = s_iss[x];
+      if (n > 0) (void)mbar_wait_bounded(fbar + x, (n - 1) & 1u);
+    }
   }
 }
 

@@ -51,6 +51,10 @@ template <> struct Elem<__nv_bfloat16> {
     unpack2(u.w, f + 6);
   }
   __device__ __forceinline__ static float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+  // Element `hi` (0: low half, 1: high half) of a 32-bit word of two bf16.
+  __device__ __forceinline__ static float half_to_float(uint32_t w, int hi) {
+    return hi ? __uint_as_float(w & 0xffff0000u) : __uint_as_float(w << 16);
+  }
   __device__ __forceinline__ static float2 pair(const uint4& u, int c) {
     const uint32_t w = c == 0 ? u.x : (c == 1 ? u.y : (c == 2 ? u.z : u.w));
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
@@ -71,6 +75,9 @@ template <> struct Elem<__half> {
     unpack2(u.w, f + 6);
   }
   __device__ __forceinline__ static float to_float(__half x) { return __half2float(x); }
+  __device__ __forceinline__ static float half_to_float(uint32_t w, int hi) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(hi ? (w >> 16) : (w & 0xffffu))));
+  }
   __device__ __forceinline__ static float2 pair(const uint4& u, int c) {
     uint32_t w = c == 0 ? u.x : (c == 1 ? u.y : (c == 2 ? u.z : u.w));
     return __half22float2(*reinterpret_cast<__half2*>(&w));
@@ -86,6 +93,63 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int o
   } else {
     static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
   }
+}
+
+// Stores N consecutive fp32 values as the output dtype, with one vector
+// store when the destination is aligned for it.
+template <int N>
+__device__ __forceinline__ void store_out_vec(void* out, int64_t idx, const float* v, int out_dtype) {
+  if (out_dtype == 0) {
+    float* dst = static_cast<float*>(out) + idx;
+    if constexpr (N % 4 == 0) {
+      if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        return;
+      }
+    } else if constexpr (N % 2 == 0) {
+      if ((reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i += 2) *reinterpret_cast<float2*>(dst + i) = make_float2(v[i], v[i + 1]);
+        return;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) dst[i] = v[i];
+    return;
+  }
+  uint32_t w[(N + 1) / 2];
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    const float b = (i + 1 < N) ? v[i + 1] : 0.f;
+    if (out_dtype == 1) {
+      __half2 h = __floats2half2_rn(v[i], b);
+      w[i / 2] = *reinterpret_cast<uint32_t*>(&h);
+    } else {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[i], b);
+      w[i / 2] = *reinterpret_cast<uint32_t*>(&h);
+    }
+  }
+  unsigned short* dst = static_cast<unsigned short*>(out) + idx;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+  if constexpr (N == 8) {
+    if ((a & 15u) == 0) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      return;
+    }
+  } else if constexpr (N == 4) {
+    if ((a & 7u) == 0) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+      return;
+    }
+  } else if constexpr (N == 2) {
+    if ((a & 3u) == 0) {
+      *reinterpret_cast<uint32_t*>(dst) = w[0];
+      return;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) dst[i] = static_cast<unsigned short>(i & 1 ? (w[i / 2] >> 16) : (w[i / 2] & 0xffffu));
 }
 
 // ----------------------------------------------------------------- mbarrier
