@@ -28,10 +28,11 @@ struct GqaPlan {
   size_t rec_bytes_per_cta = 0;  // two records per CTA
 };
 
-// Workspace layout: [unit counters][record outputs][record (max, sum)]. The
-// counters are sized for one kv head per unit, the most units any plan uses.
+// Workspace layout: [counters, one per unit and warp slot][record
+// outputs][record (max, sum)]. A unit of hc kv heads has hc * HW warp slots, so
+// batch * n_kv_heads * n_hsub * HW counters cover every plan.
 size_t counter_bytes(int batch, int n_kv_heads, const GqaPlan& pl) {
-  return align_up(static_cast<size_t>(batch) * n_kv_heads * pl.n_hsub * 4, 256);
+  return align_up(static_cast<size_t>(batch) * n_kv_heads * pl.n_hsub * gqa_warps_per_kvhead(pl.GH) * 4, 256);
 }
 
 // Query heads per unit: the largest power of two up to 16 that divides the

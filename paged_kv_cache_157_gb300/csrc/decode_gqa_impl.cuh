@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   uint64_t* fbar = reinterpret_cast<uint64_t*>(smem + L.bar_off);  // [S] full
   unsigned int* s_rel = reinterpret_cast<unsigned int*>(smem + L.rel_off);  // [S] releases seen
   unsigned int* s_iss = s_rel + p.stages;  // [S] fills issued
-  volatile int* s_misc = reinterpret_cast<volatile int*>(smem + L.misc_off);  // [abort, last0, last1]
+  volatile int* s_misc = reinterpret_cast<volatile int*>(smem + L.misc_off);  // [abort flag]
   int* s_scan = reinterpret_cast<int*>(smem + L.scan_off);
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -561,6 +561,16 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     s_misc[2] = 0;
   }
   fence_barrier_init();
+  if (tid < 2 && !p.unit_mode) {
+    // Warm L2 with the block-table line this CTA most likely reads first (a
+    // guess that assumes equal lengths; it only overlaps the length scan).
+    const int64_t Gc = gridDim.x;
+    const int64_t per_seq = static_cast<int64_t>(HN) * p.max_blocks;
+    const int64_t pos = static_cast<int64_t>(blockIdx.x) * B * per_seq / Gc;
+    const int seq = static_cast<int>(pos / per_seq);
+    const int j = static_cast<int>((pos - seq * per_seq) % p.max_blocks) + tid * 32;
+    if (seq < B && j < p.max_blocks) prefetch_l2(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks + j);
+  }
   scan_blocks(p.context_lens, B, bs, p.max_blocks, s_scan);  // ends with a CTA barrier
   const int64_t N = static_cast<int64_t>(HN) * s_scan[B];
   const int64_t G = gridDim.x;
@@ -676,6 +686,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   // Partial segments (at most two: the one starting at lo, the one ending
   // at hi) whose records wait to be counted.
   bool pend0 = false, pend1 = false;
+  unsigned int old0 = 0, old1 = 0;  // the counts seen by this warp's adds (lane 0)
   bool aborted = false;
 
   if (active) {
@@ -813,67 +824,65 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
             p.rec_ml[(rec * HS + hr + h) * 2 + 1] = lw[h];
           }
         }
-        if (gb == lo) pend0 = true; else pend1 = true;
-      }
-      gb += seg_len;
-    }
-  } else {
-    // idle warp: still walk the segments so that pend0 / pend1 agree
-    int64_t gb = lo;
-    while (gb < hi) {
-      const BlockPos sg = locate_block(gb, HN, s_scan, B, p.n_hsub);
-      const int seg_len = static_cast<int>(((sg.nb - sg.j) < (hi - gb)) ? (sg.nb - sg.j) : (hi - gb));
-      if (!(sg.j == 0 && seg_len == sg.nb)) {
+        // Count the record (one counter per unit and warp slot): the warp
+        // barrier orders the lanes' record writes before lane 0's release.
+        // The first segment is counted now and its result only read at the
+        // end, so the add's round trip never stalls the stream.
+        __syncwarp();
+        if (lane == 0) {
+          const int64_t unit = (static_cast<int64_t>(sg.seq) * p.n_chunks + sg.chunk) * p.n_hsub + sg.hsub;
+          const unsigned int old = atomic_add_acq_rel_gpu(p.counters + unit * nact + w, 1u);
+          if (gb == lo) old0 = old; else old1 = old;
+        }
         if (gb == lo) pend0 = true; else pend1 = true;
       }
       gb += seg_len;
     }
   }
 
-  // Records are complete once every warp passes this barrier; one thread
-  // counts them per unit, and the add that completes a unit's count makes
-  // this CTA the unit's merger (it then resets the counter for the next call).
-  __threadfence();
+  // The warp whose add completes a unit's count (one add per contributing
+  // CTA) merges the records of its heads and resets the counter for the next
+  // call. No warp waits for another warp or CTA.
   __syncthreads();
   const bool any_abort = s_misc[0] != 0;
-  if (!any_abort && (pend0 || pend1)) {
+  if (active && !any_abort && (pend0 || pend1)) {
     const BlockPos q0 = locate_block(lo, HN, s_scan, B, p.n_hsub);
     const BlockPos q1 = locate_block(hi - 1, HN, s_scan, B, p.n_hsub);
     const int64_t p0_u0 = lo - q0.j, p1_u0 = hi - 1 - q1.j;
-    if (w == 0 && lane < 2 && (lane == 0 ? pend0 : pend1)) {
-      const BlockPos& qq = lane == 0 ? q0 : q1;
-      const int64_t u0 = lane == 0 ? p0_u0 : p1_u0;
-      const int64_t c0 = worker_of_block(u0, G, N), c1 = worker_of_block(u0 + qq.nb - 1, G, N);
-      int64_t contributors = c1 - c0 + 1;
-      if (N < G) {
-        contributors = 0;
-        for (int64_t x = c0; x <= c1; ++x)
-          contributors += (worker_range_start(x, G, N) != worker_range_start(x + 1, G, N)) ? 1 : 0;
+    int last = 0;  // bit 0: the segment at lo, bit 1: the segment ending at hi
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (!(k == 0 ? pend0 : pend1)) continue;
+        const BlockPos& qq = k == 0 ? q0 : q1;
+        const int64_t u0 = k == 0 ? p0_u0 : p1_u0;
+        const int64_t c0 = worker_of_block(u0, G, N), c1 = worker_of_block(u0 + qq.nb - 1, G, N);
+        int64_t contributors = c1 - c0 + 1;
+        if (N < G) {
+          contributors = 0;
+          for (int64_t x = c0; x <= c1; ++x)
+            contributors += (worker_range_start(x, G, N) != worker_range_start(x + 1, G, N)) ? 1 : 0;
+        }
+        const int64_t unit = (static_cast<int64_t>(qq.seq) * p.n_chunks + qq.chunk) * p.n_hsub + qq.hsub;
+        unsigned int* ctr = p.counters + unit * nact + w;
+        const unsigned int old = k == 0 ? old0 : old1;
+        if (old + 1 == static_cast<unsigned int>(contributors)) {
+          last |= 1 << k;
+          *ctr = 0u;
+        } else if (old + 1 > static_cast<unsigned int>(contributors)) {
+          set_flag(p.err, 0x10u);  // the workspace counters were not zero
+          atomicExch(ctr, 0u);
+        }
       }
-      const int64_t unit = (static_cast<int64_t>(qq.seq) * p.n_chunks + qq.chunk) * p.n_hsub + qq.hsub;
-      unsigned int* ctr = p.counters + unit;
-      const unsigned int old = atomic_add_acq_rel_gpu(ctr, 1u);
-      int last = 0;
-      if (old + 1 == static_cast<unsigned int>(contributors)) {
-        last = 1;
-        *ctr = 0u;
-      } else if (old + 1 > static_cast<unsigned int>(contributors)) {
-        set_flag(p.err, 0x10u);  // the workspace counters were not zero
-        atomicExch(ctr, 0u);
-      }
-      s_misc[1 + lane] = last;
     }
-    __syncthreads();
-    if (active) {
-      // the barrier orders every warp's record reads after thread 0's acquire
-      if (s_misc[1]) {
-        const int h0 = (q0.chunk * hc + kh) * p.group + q0.hsub * GH + hw * GW;
-        merge_unit_warp<D, HS, GW>(p, p0_u0, q0.nb, G, N, q0.seq, h0, kh * GH + hw * GW, lane);
-      }
-      if (s_misc[2]) {
-        const int h1 = (q1.chunk * hc + kh) * p.group + q1.hsub * GH + hw * GW;
-        merge_unit_warp<D, HS, GW>(p, p1_u0, q1.nb, G, N, q1.seq, h1, kh * GH + hw * GW, lane);
-      }
+    last = __shfl_sync(full, last, 0);
+    if (last & 1) {
+      const int h0 = (q0.chunk * hc + kh) * p.group + q0.hsub * GH + hw * GW;
+      merge_unit_warp<D, HS, GW>(p, p0_u0, q0.nb, G, N, q0.seq, h0, kh * GH + hw * GW, lane);
+    }
+    if (last & 2) {
+      const int h1 = (q1.chunk * hc + kh) * p.group + q1.hsub * GH + hw * GW;
+      merge_unit_warp<D, HS, GW>(p, p1_u0, q1.nb, G, N, q1.seq, h1, kh * GH + hw * GW, lane);
     }
   }
   if (any_abort && tid == 0) {

@@ -236,6 +236,10 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
