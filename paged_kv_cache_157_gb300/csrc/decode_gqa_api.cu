@@ -87,8 +87,11 @@ int64_t plan_ctas(const DeviceInfo* dev, int occ, int64_t units, int max_blocks)
   if (forced > 0) {
     G = (upper + forced - 1) / forced;
   } else {
+    // at least kMinBlocksPerCta blocks per CTA, but never fewer CTAs than
+    // units: small batches are latency-bound, and a CTA per unit finishes
+    // them without any split-K merge
     G = static_cast<int64_t>(dev->num_sms) * std::max(1, std::min(occ, kMaxCtasPerSm));
-    G = std::min(G, std::max<int64_t>(1, upper / kMinBlocksPerCta));
+    G = std::min(G, std::max<int64_t>({1, upper / kMinBlocksPerCta, units}));
   }
   const int64_t cap = option(KVC_OPT_MAX_CTAS);
   if (cap > 0) G = std::min(G, cap);

@@ -7,30 +7,30 @@
 //     o_h = sum_t a_t c_t[0 : d_c]      (d_c = 512)
 //
 // Design (sm_103a, one CTA per SM):
-// * A CTA works on 64-token tiles and one half (256) of the 512 output
+// * A CTA works on 32-token tiles and one half (256) of the 512 output
 //   dimensions; its partner CTA (adjacent in the grid) takes the other half of
 //   the same tiles, so the latent tile is fetched from HBM once and the second
 //   read is served by L2. Both compute S = Q~ C^T in full: the O half
-//   (128 x 256 fp32), S (128 x 64 fp32), P and part of Q~ fit the 512 TMEM
-//   columns, which the whole O (128 x 512 fp32) alone would fill.
+//   (128 x 256 fp32), two S buffers (128 x 32 fp32), two P buffers and part
+//   of Q~ fit the 512 TMEM columns, which the whole O (128 x 512 fp32) alone
+//   would fill.
 // * Q~ [128 x 576] bf16 is split: columns 0..255 sit in TMEM (128 columns of
 //   bf16 pairs, written by the softmax warps) and feed the first 16 K steps of
 //   S as the A operand from tensor memory; columns 256..575 sit in shared
-//   memory (80 KB). That leaves room for two latent tile stages [64 x 576]
-//   (72 KB each),
-//   in the 128B-swizzled K-major layout that TMA writes and the UMMA
-//   descriptors read.
+//   memory (80 KB). That leaves room for four latent tile stages [32 x 576]
+//   (36 KB each) in the 128B-swizzled K-major layout that TMA writes and the
+//   UMMA descriptors read: a stage is held from S(t) until PV(t), and the
+//   other two stages keep the next tiles' copies in flight meanwhile.
 // * Warp roles: warps 0-3 = softmax and epilogue (thread = head = TMEM lane),
 //   warp 4 = TMA producer, warp 5 = MMA issuer and TMEM owner.
-//   Per tile: S(t) = Q~ C_t^T (36 MMAs, K = 16 each, N = 64: a wider N than
-//   32 halves how often each MMA re-reads its 128 x 16 slice of Q~, which
-//   bounded the issue rate) -> softmax reads S
-//   from TMEM, updates the running max lazily (O in TMEM is rescaled only when
-//   the max grows by more than 2^8), writes P = exp2(s - m) into TMEM as two
-//   bf16 parts (hi = bf16(p), lo = bf16(p - hi), so hi + lo carries p to about
-//   2^-17) -> O += P_hi V_t + P_lo V_t (8 MMAs with A read from TMEM, N = 256,
-//   V = the first 512 columns of the same tile, read MN-major). The MMA of S(t+1) is issued before PV(t) so the tensor
-//   core works while the softmax runs.
+//   Per tile: S(t) = Q~ C_t^T (36 MMAs, K = 16 each, N = 32) -> softmax reads
+//   S from TMEM, updates the running max lazily (O in TMEM is rescaled only
+//   when the max grows by more than 2^8, after waiting for the previous PV),
+//   writes P = exp2(s - m) into TMEM as two bf16 parts (hi = bf16(p), lo =
+//   bf16(p - hi), so hi + lo carries p to about 2^-17) -> O += P_hi V_t +
+//   P_lo V_t (4 MMAs with A read from TMEM, N = 256, V = the first 512 columns
+//   of the same tile, read MN-major). S and P are double buffered and S(t+1)
+//   is queued before PV(t), so the tensor core works while the softmax runs.
 // * Work split: as in the GQA kernel, the tiles of all sequences are laid end
 //   to end and CTA pair c takes a contiguous range; a sequence cut by a range
 //   boundary leaves fp32 records (m, l, O) and the last contributing CTA of
@@ -57,10 +57,11 @@ constexpr int kHeads = 128;          // M of every MMA
 constexpr int kDc = 512;             // latent (value) width
 constexpr int kW = 576;              // cached row width
 constexpr int kKB = kW / 64;         // 64-element (128 B) K blocks of a row: 9
-constexpr int kTile = 64;            // tokens per tile (MMA N for S)
+constexpr int kTile = 32;            // tokens per tile (MMA N for S)
 constexpr int kHalf = kDc / 2;       // output dims per CTA: 256
-constexpr int kStages = 2;           // latent tile stages
-constexpr int kSBufs = 1;            // S buffers in TMEM (released as soon as the softmax has read S)
+constexpr int kStages = 4;           // latent tile stages
+constexpr int kSBufs = 2;            // S buffers in TMEM
+constexpr int kPBufs = 2;            // P buffers in TMEM
 constexpr int kThreads = 192;        // 6 warps
 constexpr int kMaxBatch = 256;
 
@@ -70,12 +71,13 @@ constexpr int kQTmemK = 256;                          // Q~ columns held in TMEM
 constexpr int kQSmemKB0 = kQTmemK / 64;               // first 64-column block in shared memory: 4
 constexpr uint32_t kQSub = kHeads * 128;              // one 64-column block of Q~: 16384
 constexpr uint32_t kQBytes = (kKB - kQSmemKB0) * kQSub;  // 81920
-constexpr uint32_t kTileBytes = kTile * kW * 2;      // 73728
-constexpr uint32_t kTileSub = kTile * 128;           // one 64-column block of a tile: 8192
+constexpr uint32_t kTileBytes = kTile * kW * 2;      // 36864
+constexpr uint32_t kTileSub = kTile * 128;           // one 64-column block of a tile: 4096
 
-// TMEM columns: O half at 0..255, S at 256..319, P at 320..383: the high
-// bf16 part of the weights (32 columns = 64 bf16 per head) then the low part;
-// Q~ columns 0..255 as bf16 pairs at 384..511.
+// TMEM columns: O half at 0..255, two S buffers (32 columns each) at
+// 256..319, two P buffers at 320..383 (each: the high bf16 part of the
+// weights, 16 columns = 32 bf16 per head, then the low part), Q~ columns
+// 0..255 as bf16 pairs at 384..511.
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS = 256;
 constexpr uint32_t kColP = 320;
@@ -89,7 +91,8 @@ constexpr uint32_t kOffBar = kOffC + kStages * kTileBytes;
 // barrier indices
 enum {
   B_QFULL = 0, B_QEMPTY, B_CFULL0, B_CEMPTY0 = B_CFULL0 + kStages, B_SFULL0 = B_CEMPTY0 + kStages,
-  B_SEMPTY0 = B_SFULL0 + kSBufs, B_PFULL = B_SEMPTY0 + kSBufs, B_PVDONE, B_OFREE, B_FINAL, B_COUNT
+  B_SEMPTY0 = B_SFULL0 + kSBufs, B_PFULL0 = B_SEMPTY0 + kSBufs, B_PEMPTY0 = B_PFULL0 + kPBufs,
+  B_OFREE = B_PEMPTY0 + kPBufs, B_FINAL, B_COUNT
 };
 constexpr uint32_t kOffMisc = kOffBar + B_COUNT * 8;  // tmem address, abort flag, last flag
 constexpr uint32_t kOffScan = kOffMisc + 16;
@@ -394,7 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S empty, P full and O free: the four softmax warps; all others: one.
       uint32_t c = 1;
       if (i == B_QFULL) c = 5;
-      if ((i >= B_SEMPTY0 && i < B_SEMPTY0 + kSBufs) || i == B_PFULL || i == B_OFREE) c = 4;
+      if ((i >= B_SEMPTY0 && i < B_SEMPTY0 + kSBufs) || (i >= B_PFULL0 && i < B_PFULL0 + kPBufs) || i == B_OFREE)
+        c = 4;
       mbar_init(&bars[i], c);
     }
     fence_barrier_init();
@@ -496,11 +500,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------- MMA issuer
+    // Tensor-pipe order per segment: S(t0), S(t0+1), PV(t0), S(t0+2), PV(t0+1),
+    // ...: S of the next tile is always queued before PV of the tile whose
+    // weights the softmax warps are computing, and both S and P are double
+    // buffered, so the tensor core works while the softmax runs.
     if (lane == 0) {
       const uint32_t id_s = instr_desc(kHeads, kTile, 0, 0);
       const uint32_t id_pv = instr_desc(kHeads, kHalf, 0, 1);
       const uint64_t a_q0 = smem_desc(sQ, 16, 1024, 2);
-      uint32_t g = 0, seg_i = 0, pv_i = 0;
+      uint32_t g = 0, seg_i = 0;  // g: tiles issued so far (all segments)
       Segment sg;
       Walker w = walk;
       bool ok = true;
@@ -509,8 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_phase(bar(B_QFULL), seg_i & 1u, s_abort, p.err)) break;
         fence_after();
         const uint32_t g_first = g;
+        // PV of global tile gi: O (+)= P_hi V + P_lo V with A = P from TMEM and
+        // B = this CTA's half of the tile's first 512 columns, read MN-major.
         auto issue_pv = [&](uint32_t gi) -> bool {
-          if (!wait_phase(bar(B_PFULL), pv_i & 1u, s_abort, p.err)) return false;
+          const uint32_t pb = gi % kPBufs;
+          if (!wait_phase(bar(B_PFULL0 + pb), (gi / kPBufs) & 1u, s_abort, p.err)) return false;
           const bool first = (gi == g_first);
           if (first && seg_i > 0 && !wait_phase(bar(B_OFREE), (seg_i - 1) & 1u, s_abort, p.err)) return false;
           fence_after();
@@ -520,13 +531,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int part = 0; part < 2; ++part) {  // P_hi, then P_lo, against the same V rows
 #pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks) {
-              mma_bf16_ts(tmem + kColO, tmem + kColP + part * (kTile / 2) + ks * 8, bv0 + ((ks * 2048) >> 4), id_pv,
-                          (first && part == 0 && ks == 0) ? 0u : 1u);
+              mma_bf16_ts(tmem + kColO, tmem + kColP + pb * kTile + part * (kTile / 2) + ks * 8,
+                          bv0 + ((ks * 2048) >> 4), id_pv, (first && part == 0 && ks == 0) ? 0u : 1u);
             }
           }
           mma_commit(bar(B_CEMPTY0 + st));
-          mma_commit(bar(B_PVDONE));
-          ++pv_i;
+          mma_commit(bar(B_PEMPTY0 + pb));
           return true;
         };
         for (int t = sg.t0; t < sg.t1 && ok; ++t, ++g) {
@@ -572,15 +582,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------- softmax + epilogue
     const int h = warp * 32 + lane;  // head = TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    uint32_t g = 0, seg_i = 0, pv_seen = 0;
+    uint32_t g = 0, seg_i = 0;
     Segment sg;
     Walker w = walk;
     bool ok = true;
     while (ok && !*s_abort && w.next(p, s_scan, sg)) {
       if (sg.ntiles == 0) continue;
       const int n_rows = seq_rows(p.context_lens, sg.seq, p.block_size, p.max_blocks);
-      // Columns [0, 320) of this head's Q~ row go to TMEM (the A operand of the
-      // first 20 K steps of S), once the previous segment's S MMAs are done.
+      // Columns [0, 256) of this head's Q~ row go to TMEM (the A operand of the
+      // first 16 K steps of S), once the previous segment's S MMAs are done.
       if (seg_i > 0 &&
           !__all_sync(0xffffffffu, wait_phase(bar(B_QEMPTY), (seg_i - 1) & 1u, s_abort, p.err))) {
         ok = false;
@@ -608,18 +618,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -__builtin_huge_valf(), l = 0.f;
       const uint32_t g_first = g;
       for (int t = sg.t0; t < sg.t1; ++t, ++g) {
-        const uint32_t st = g % kSBufs;
-        if (!__all_sync(0xffffffffu, wait_phase(bar(B_SFULL0 + st), (g / kSBufs) & 1u, s_abort, p.err))) {
+        const uint32_t sb = g % kSBufs, pb = g % kPBufs;
+        if (!__all_sync(0xffffffffu, wait_phase(bar(B_SFULL0 + sb), (g / kSBufs) & 1u, s_abort, p.err))) {
           ok = false;
           break;
         }
         fence_after();
         float s[kTile];
-#pragma unroll
-        for (int c = 0; c < kTile; c += 32) tmem_ld32(lane_addr + kColS + st * kTile + c, s + c);
+        tmem_ld32(lane_addr + kColS + sb * kTile, s);
         fence_before();
         __syncwarp();
-        if (lane == 0) arrive(bar(B_SEMPTY0 + st));
+        if (lane == 0) arrive(bar(B_SEMPTY0 + sb));
         const int valid = n_rows - t * kTile;
         float mt = -__builtin_huge_valf();
 #pragma unroll
@@ -627,21 +636,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           s[i] = (i < valid) ? s[i] * p.qscale : -__builtin_huge_valf();
           mt = fmaxf(mt, s[i]);
         }
-        if (g > g_first) {
-          // P(t-1) must be consumed (and O stable) before P or O change.
-          if (!__all_sync(0xffffffffu, wait_phase(bar(B_PVDONE), pv_seen & 1u, s_abort, p.err))) {
-            ok = false;
-            break;
-          }
-          ++pv_seen;
-          fence_after();
+        // This P buffer was last read by PV(g - 2), long done in the steady state.
+        if (g >= kPBufs &&
+            !__all_sync(0xffffffffu, wait_phase(bar(B_PEMPTY0 + pb), (g / kPBufs - 1) & 1u, s_abort, p.err))) {
+          ok = false;
+          break;
         }
         // Lazy rescale, decided per warp: the TMEM accesses below are warp-wide.
         if (__any_sync(0xffffffffu, mt > m + 8.0f)) {
           const float m_new = fmaxf(m, mt);
           const float alpha = fast_exp2(m - m_new);  // 0 on the first tile of a segment
           if (g > g_first) {
-            // rescale O in TMEM (rare: the running max grew by more than 2^8)
+            // O must hold PV(g - 1) before it is rescaled (rare: the running
+            // max grew by more than 2^8)
+            const uint32_t gp = g - 1;
+            if (!__all_sync(0xffffffffu,
+                            wait_phase(bar(B_PEMPTY0 + gp % kPBufs), (gp / kPBufs) & 1u, s_abort, p.err))) {
+              ok = false;
+              break;
+            }
+            fence_after();
             for (int c = 0; c < kHalf; c += 32) {
               float v[32];
               tmem_ld32(lane_addr + kColO + c, v);
@@ -663,16 +677,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[i] = hi;
           pk[kTile / 2 + i] = pack_bf16(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
         }
-#pragma unroll
-        for (int c = 0; c < kTile; c += 32) tmem_st32u(lane_addr + kColP + c, pk + c);
+        tmem_st32u(lane_addr + kColP + pb * kTile, pk);
         fence_before();
         __syncwarp();
-        if (lane == 0) arrive(bar(B_PFULL));
+        if (lane == 0) arrive(bar(B_PFULL0 + pb));
       }
       if (!ok) break;
       // ---- epilogue: wait for the last PV, read O, write output or record
-      if (!__all_sync(0xffffffffu, wait_phase(bar(B_PVDONE), pv_seen & 1u, s_abort, p.err))) break;
-      ++pv_seen;
+      {
+        const uint32_t gl = g - 1;
+        if (!__all_sync(0xffffffffu, wait_phase(bar(B_PEMPTY0 + gl % kPBufs), (gl / kPBufs) & 1u, s_abort, p.err)))
+          break;
+      }
       fence_after();
       const bool whole = (sg.t0 == 0 && sg.t1 == sg.ntiles);
       const int64_t rec = (static_cast<int64_t>(blockIdx.x) * 2 + sg.which) * kHeads + h;
