@@ -107,5 +107,45 @@ def paged_decode_one(q_row, k_cache, v_cache, table_row, n, kv_head, scale):
     return attend_rows(q_row, K, V, scale)
 
 
+def window_start(n: int, window: int) -> int:
+    """First visible row of a sequence of n cached rows under a sliding window of W rows.
+
+    "KV-Cache——为什么AI回复越来越快" section 08 (Window Attention / Sliding
+    Window): only the most recent W tokens' K/V are kept and attended; the
+    closing section of "KV缓存原理与显存估算" notes that this drops the
+    out-of-window state because the visible range itself is redefined.
+    Reading: the newest row is the current token, so the visible rows are
+    [max(0, n - W), n); W >= n is full attention.
+    """
+    if window < 1:
+        raise ValueError("window must be >= 1")
+    return max(0, n - window)
+
+
+def paged_decode_window_lse(q, k_cache, v_cache, block_tables, context_lens, scale, window):
+    """Sliding-window decode: as paged_decode_lse, over the last ``window`` rows only."""
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    g = Hq // Hkv
+    out = np.zeros((B, Hq, v_cache.shape[3]), dtype=np.float64)
+    lse = np.zeros((B, Hq), dtype=np.float64)
+    for i in range(B):
+        n = int(context_lens[i])
+        if n < 1:
+            raise ValueError("context_len must be >= 1 (the new token is always attended)")
+        s0 = window_start(n, window)
+        for kvh in range(Hkv):
+            K = gather_logical(k_cache, block_tables[i], n, kvh)[s0:]
+            V = gather_logical(v_cache, block_tables[i], n, kvh)[s0:]
+            for h in range(kvh * g, (kvh + 1) * g):
+                out[i, h], lse[i, h] = attend_rows(q[i, h], K, V, scale)
+    return out, lse
+
+
+def paged_decode_window(q, k_cache, v_cache, block_tables, context_lens, scale, window):
+    return paged_decode_window_lse(q, k_cache, v_cache, block_tables, context_lens, scale, window)[0]
+
+
 def default_scale(head_dim: int) -> float:
     return 1.0 / math.sqrt(head_dim)
