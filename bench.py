@@ -141,10 +141,11 @@ def step_bytes(case_lens, hq, hkv, d, bs, elt, out_elt, unique_kv_rows=None):
 class GqaStep:
     """Device-resident inputs of one decode step plus the calls that run it."""
 
-    def __init__(self, kvc, case, out_dtype):
+    def __init__(self, kvc, case, out_dtype, window=None):
         import torch
         self.kvc = kvc
         self.case = case
+        self.window = window
         self.dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in case.items()}
         lens = case["context_lens"].tolist()
         self.lens = lens
@@ -164,7 +165,7 @@ class GqaStep:
     def decode(self):
         d = self.dev
         self.kvc.decode_attention(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
-                                  self.scale, self.out, self.ws)
+                                  self.scale, self.out, self.ws, window=self.window)
 
 
 class L2Flush:
@@ -320,11 +321,11 @@ def cpu_baseline(case, budget_s=10.0):
 
 # --------------------------------------------------------------- variants
 
-def measure_gqa_case(kvc, case, steps, warmup, flush, unique_rows=None):
+def measure_gqa_case(kvc, case, steps, warmup, flush, unique_rows=None, window=None):
     import torch
-    st = GqaStep(kvc, case, torch.bfloat16)
+    st = GqaStep(kvc, case, torch.bfloat16, window)
     step_ms, dec_ms, _, _ = time_steps(st, steps, warmup, flush)
-    lens = st.lens
+    lens = st.lens if window is None else [min(n, window) for n in st.lens]  # rows actually read
     dec_b, app_b = step_bytes(lens, st.hq, st.hkv, st.d, st.bs, case["q"].element_size(), 2, unique_rows)
     ms = statistics.mean(step_ms)
     dms = statistics.mean(dec_ms)
@@ -354,6 +355,11 @@ def run_variant(kvc, name, flush, steps):
     if name == "gqa_long_splitk":
         c = W.gqa_case(4, 64, 8, 128, 16, [32768, 65536, 131072, 131072], "bf16", 45, device="cuda")
         return measure_gqa_case(kvc, c, max(5, steps // 4), 3, flush)
+    if name == "gqa_window_b32_ctx4096_w1024":
+        c = W.gqa_case(32, 32, 8, 128, 16, [4096] * 32, "bf16", 43, device="cuda")
+        r = measure_gqa_case(kvc, c, steps, 5, flush, window=1024)
+        r["note"] = "sliding window of 1024 rows: bytes count the visible rows only"
+        return r
     if name == "gqa_ragged_17_31_32":
         c = W.gqa_case(3, 64, 8, 128, 16, [17, 31, 32], "bf16", 45, device="cuda")
         return measure_gqa_case(kvc, c, steps, 5, flush)
@@ -365,7 +371,7 @@ def run_variant(kvc, name, flush, steps):
 
 
 VARIANTS = ("gqa_b32_ctx4096", "mha_shared_prefix_8x8", "gqa_long_splitk", "gqa_ragged_17_31_32", "tiny_mha_fp32",
-            "mla_deepseek_v2")
+            "mla_deepseek_v2", "gqa_window_b32_ctx4096_w1024")
 
 
 def variants(kvc, flush, steps):

@@ -164,6 +164,24 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
                                 int block_size, int64_t num_blocks, kvc_dtype dtype, void* out,
                                 kvc_dtype out_dtype, void* workspace, size_t workspace_bytes, kvc_stream stream);
 
+/* Sliding-window decode: as kvc_decode_attention, but sequence i attends only
+ * its newest `window` rows, t = max(0, n_i - window) .. n_i - 1 with
+ * n_i = context_lens[i] (the token appended this step is the newest row).
+ * window >= n_i is full attention; window < 1 is KVC_ERR_INVALID_ARG. Table
+ * entries before the block that holds row n_i - window are never read, so a
+ * caller may drop (free) those blocks. Same arguments, workspace and error
+ * rules as kvc_decode_attention (the same workspace size query applies).
+ * Source: "KV-Cache——为什么AI回复越来越快" section 08 (Window Attention /
+ * Sliding Window: only the most recent W tokens' K/V are kept) and the
+ * closing section of "KV缓存原理与显存估算" (the dropped state is outside the
+ * model's visible range). */
+kvc_status kvc_decode_attention_window(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                       const int32_t* context_lens, int batch, float scale, int n_q_heads,
+                                       int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, int window,
+                                       kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
+                                       size_t workspace_bytes, kvc_stream stream);
+
 /* kvc_decode_attention for callers that cannot allocate device memory.
  *
  * There is no counterpart of this call on the source pages: it exists for

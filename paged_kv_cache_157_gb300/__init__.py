@@ -19,6 +19,7 @@ import threading
 __all__ = [
     "KvcError", "KvcLibraryMissing", "raw", "lib_path", "symbols",
     "append", "append_latent", "decode_workspace_size", "decode_attention", "decode_attention_static",
+    "decode_attention_window",
     "decode_mla_workspace_size", "decode_attention_mla", "set_option", "get_option",
     "get_error_flags", "BlockPool", "slots_from_tables",
     "F32", "F16", "BF16", "FLAG_BAD_BLOCK", "FLAG_BAD_LEN", "FLAG_BAD_SLOT", "FLAG_TIMEOUT", "FLAG_WORKSPACE",
@@ -60,6 +61,8 @@ SIGNATURES = {
                                     _vp, _i32, _vp, _sz, _vp]),
     "kvc_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32, _i64,
                                            _i32, _vp, _i32, _vp]),
+    "kvc_decode_attention_window": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32, _i64,
+                                           _i32, _i32, _vp, _i32, _vp, _sz, _vp]),
     "kvc_decode_mla_workspace_size": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _szp]),
     "kvc_decode_attention_mla": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32, _i64, _i32, _vp,
                                         _i32, _vp, _sz, _vp]),
@@ -219,10 +222,12 @@ def new_decode_workspace(batch, n_q_heads, n_kv_heads, head_dim, block_size, max
     return torch.zeros(max(n, 1), dtype=torch.uint8, device=device)
 
 
-def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace=None, stream=None):
-    """kvc_decode_attention. q/out [B, Hq, D]; caches [num_blocks, Hkv, bs, D];
-    block_tables int32 [B, max_blocks]; context_lens int32 [B]; workspace: a zero-filled uint8 tensor
-    (see new_decode_workspace) that later calls keep zeroed, or None."""
+def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace=None, stream=None,
+                     window=None):
+    """kvc_decode_attention (or kvc_decode_attention_window when ``window`` is given). q/out [B, Hq, D];
+    caches [num_blocks, Hkv, bs, D]; block_tables int32 [B, max_blocks]; context_lens int32 [B]; workspace:
+    a zero-filled uint8 tensor (see new_decode_workspace) that later calls keep zeroed, or None; window:
+    attend only the newest ``window`` rows of every sequence."""
     torch = _torch()
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
         _require(t, n)
@@ -236,6 +241,13 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out
     if workspace is not None:
         _require(workspace, "workspace")
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    if window is not None:
+        _check(raw().kvc_decode_attention_window(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                                 block_tables.shape[1], _ptr(context_lens), B, float(scale), hq, hkv,
+                                                 d, bs, nb, int(window), _dtype_code(k_cache), _ptr(out),
+                                                 _dtype_code(out), ws_ptr, ws_bytes, _stream(stream)),
+               "kvc_decode_attention_window")
+        return
     _check(raw().kvc_decode_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                       block_tables.shape[1], _ptr(context_lens), B, float(scale), hq, hkv, d, bs, nb,
                                       _dtype_code(k_cache), _ptr(out), _dtype_code(out), ws_ptr, ws_bytes,
@@ -369,3 +381,9 @@ def slots_from_tables(block_tables, block_size: int, rows, positions):
     _check(raw().kvc_slots_from_tables(_ptr(bt), bt.shape[0], bt.shape[1], block_size, _ptr(r), _ptr(p), p.numel(),
                                        _ptr(out)), "kvc_slots_from_tables")
     return out
+
+
+def decode_attention_window(q, k_cache, v_cache, block_tables, context_lens, scale, window, out, workspace=None,
+                            stream=None):
+    """kvc_decode_attention_window: decode over the newest ``window`` rows of every sequence."""
+    decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace, stream, window=window)

@@ -35,6 +35,7 @@ struct GqaParams {
   int out_dtype;
   int stages;
   int unit_mode;  // 1: CTA u handles unit u completely (no records)
+  int window;     // sliding window: attend the newest `window` rows (0: all rows)
   float qscale;   // scale * log2(e)
 };
 

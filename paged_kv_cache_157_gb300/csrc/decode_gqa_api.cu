@@ -153,13 +153,16 @@ kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, i
   return KVC_OK;
 }
 
-kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                                int max_blocks_per_seq, const int32_t* context_lens, int batch, float scale,
-                                int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks,
-                                kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
-                                size_t workspace_bytes, kvc_stream stream) {
-  using namespace kvc;
-  clear_error();
+}  // extern "C"
+
+namespace kvc {
+namespace {
+
+// Decode over the newest `window` rows of every sequence (window 0: all rows).
+kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                       int max_blocks_per_seq, const int32_t* context_lens, int batch, float scale, int n_q_heads,
+                       int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, int window, kvc_dtype dtype,
+                       void* out, kvc_dtype out_dtype, void* workspace, size_t workspace_bytes, kvc_stream stream) {
   if (!dtype_ok(dtype) || !dtype_ok(out_dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype");
   kvc_status s = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq);
   if (s != KVC_OK) return s;
@@ -201,6 +204,7 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
   p.max_blocks = max_blocks_per_seq;
   p.out_dtype = static_cast<int>(out_dtype);
   p.stages = pl.stages;
+  p.window = window;
   p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
 
   int occ = 1;
@@ -235,6 +239,35 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
   }
   if (s != KVC_OK) return s;
   return finish_call(st);
+}
+
+}  // namespace
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens, int batch, float scale,
+                                int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
+                                size_t workspace_bytes, kvc_stream stream) {
+  kvc::clear_error();
+  return kvc::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale, n_q_heads,
+                          n_kv_heads, head_dim, block_size, num_blocks, 0, dtype, out, out_dtype, workspace,
+                          workspace_bytes, stream);
+}
+
+kvc_status kvc_decode_attention_window(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                       const int32_t* context_lens, int batch, float scale, int n_q_heads,
+                                       int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, int window,
+                                       kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
+                                       size_t workspace_bytes, kvc_stream stream) {
+  kvc::clear_error();
+  if (window < 1) return kvc::fail(KVC_ERR_INVALID_ARG, "window must be >= 1 (got %d)", window);
+  return kvc::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale, n_q_heads,
+                          n_kv_heads, head_dim, block_size, num_blocks, window, dtype, out, out_dtype, workspace,
+                          workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -69,14 +69,8 @@ struct GqaCfg {
   static_assert(VL * VD == D && VG * VL == 32, "V lane layout");
 };
 
-// Number of cache blocks sequence b contributes (0 if its length is invalid).
-__device__ __forceinline__ int seq_blocks(const int32_t* lens, int b, int bs, int max_blocks) {
-  const int n = __ldg(lens + b);
-  if (n < 1) return 0;
-  const int nb = (n + bs - 1) / bs;
-  return nb < max_blocks ? nb : max_blocks;
-}
-
+// Rows of sequence b that are cached (capped by the table width; 0 if its
+// length is invalid).
 __device__ __forceinline__ int seq_rows(const int32_t* lens, int b, int bs, int max_blocks) {
   const int n = __ldg(lens + b);
   if (n < 1) return 0;
@@ -84,14 +78,28 @@ __device__ __forceinline__ int seq_rows(const int32_t* lens, int b, int bs, int 
   return n < cap ? n : cap;
 }
 
+// First visible row of a sequence of `rows` cached rows: with a sliding
+// window of W rows (W > 0) the newest W rows, [rows - W, rows), are attended.
+__device__ __forceinline__ int first_row(int rows, int window) {
+  return (window > 0 && rows > window) ? rows - window : 0;
+}
+
+// Number of cache blocks sequence b contributes: the blocks holding visible
+// rows (0 if its length is invalid).
+__device__ __forceinline__ int seq_blocks(const int32_t* lens, int b, int bs, int max_blocks, int window) {
+  const int rows = seq_rows(lens, b, bs, max_blocks);
+  if (rows == 0) return 0;
+  return (rows + bs - 1) / bs - first_row(rows, window) / bs;
+}
+
 // Exclusive prefix sums of seq_blocks over the batch into s_scan[0..B];
 // the whole CTA participates. s_scan needs B + 1 + 32 ints.
-__device__ inline void scan_blocks(const int32_t* lens, int B, int bs, int max_blocks, int* s_scan) {
+__device__ inline void scan_blocks(const int32_t* lens, int B, int bs, int max_blocks, int window, int* s_scan) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int per = (B + nt - 1) / nt;
   const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
   int local = 0;
-  for (int b = b0; b < b1; ++b) local += seq_blocks(lens, b, bs, max_blocks);
+  for (int b = b0; b < b1; ++b) local += seq_blocks(lens, b, bs, max_blocks, window);
   const int lane = tid & 31, wid = tid >> 5;
   int v = local;
 #pragma unroll
@@ -116,7 +124,7 @@ __device__ inline void scan_blocks(const int32_t* lens, int B, int bs, int max_b
   int run = v - local + (wid > 0 ? wsum[wid - 1] : 0);
   for (int b = b0; b < b1; ++b) {
     s_scan[b] = run;
-    run += seq_blocks(lens, b, bs, max_blocks);
+    run += seq_blocks(lens, b, bs, max_blocks, window);
   }
   if (b1 == B && b0 < B) s_scan[B] = run;
   if (B == 0 && tid == 0) s_scan[0] = 0;
@@ -228,8 +236,10 @@ struct VRow {
 
 // One 16-row tile of a page: scores, online softmax, V accumulation.
 // sp is this warp's [GW][16] fp32 weight buffer.
+// PARTIAL tiles attend only rows [lo_valid, valid) of the 16.
 template <typename T, int D, int GW, bool PARTIAL>
-__device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __restrict__ vp, float* sp, int valid,
+__device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __restrict__ vp, float* sp, int lo_valid,
+                                         int valid,
                                          WarpState<T, D, GW>& st, const LaneGeo<T, D, GW>& g) {
   using C = GqaCfg<T, D, GW>;
   float sc[C::NS][C::NVF];
@@ -274,7 +284,7 @@ __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __re
   for (int set = 0; set < C::NS; ++set) {
 #pragma unroll
     for (int k = 0; k < C::NVF; ++k) {
-      if (PARTIAL && g.prow[k] + set >= valid) sc[set][k] = kNegInf;
+      if (PARTIAL && (g.prow[k] + set >= valid || g.prow[k] + set < lo_valid)) sc[set][k] = kNegInf;
       need |= sc[set][k] > m_l + 8.0f;
     }
   }
@@ -342,7 +352,8 @@ __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __re
 #pragma unroll
       for (int h = 0; h < GW; ++h) pp[h] = *reinterpret_cast<const float2*>(sp + h * 16 + 2 * k);
     }
-    const bool za = PARTIAL && 2 * k >= valid, zb = PARTIAL && 2 * k + 1 >= valid;
+    const bool za = PARTIAL && (2 * k >= valid || 2 * k < lo_valid);
+    const bool zb = PARTIAL && (2 * k + 1 >= valid || 2 * k + 1 < lo_valid);
 #pragma unroll
     for (int d = 0; d < C::VD; ++d) {
       float2 v = make_float2(va.get(d), vb.get(d));
@@ -571,7 +582,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     const int j = static_cast<int>((pos - seq * per_seq) % p.max_blocks) + tid * 32;
     if (seq < B && j < p.max_blocks) prefetch_l2(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks + j);
   }
-  scan_blocks(p.context_lens, B, bs, p.max_blocks, s_scan);  // ends with a CTA barrier
+  scan_blocks(p.context_lens, B, bs, p.max_blocks, p.window, s_scan);  // ends with a CTA barrier
   const int64_t N = static_cast<int64_t>(HN) * s_scan[B];
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
@@ -632,7 +643,9 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     qoff = -1;
     if (pos < hi) {
       const BlockPos bp = locate_block(pos, HN, s_scan, B, p.n_hsub);
-      const int phys = __ldg(p.block_tables + static_cast<int64_t>(bp.seq) * p.max_blocks + bp.j);
+      // bp.j counts the sequence's visible blocks; the table is indexed from block 0
+      const int j0 = first_row(seq_rows(p.context_lens, bp.seq, bs, p.max_blocks), p.window) / bs;
+      const int phys = __ldg(p.block_tables + static_cast<int64_t>(bp.seq) * p.max_blocks + j0 + bp.j);
       if (phys >= 0 && phys < p.num_blocks) src = phys * p.n_kv_heads + bp.chunk * hc;
       if (pos == lo || bp.j == 0)
         qoff = (bp.seq * p.n_q_heads + bp.chunk * hc * p.group + bp.hsub * GH) * D;
@@ -699,6 +712,8 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
       const BlockPos sg = locate_block(gb, HN, s_scan, B, p.n_hsub);
       const int seg_len = static_cast<int>(((sg.nb - sg.j) < (hi - gb)) ? (sg.nb - sg.j) : (hi - gb));
       const int n_rows = seq_rows(p.context_lens, sg.seq, bs, p.max_blocks);
+      const int r0 = first_row(n_rows, p.window);  // first visible row
+      const int j0 = r0 / bs;                      // table index of the first visible block
       const int hq0 = (sg.chunk * hc + kh) * p.group + sg.hsub * GH + hw * GW;  // first query head of this warp
 
       WarpState<T, D, GW> st;
@@ -746,18 +761,21 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
         if (src >= 0) {
           const T* kp = my_k + static_cast<size_t>(slot) * stage_elems;
           const T* vp = my_v + static_cast<size_t>(slot) * stage_elems;
-          const int vr = min(bs, n_rows - (sg.j + t) * bs);
-          if (vr >= bs) {
+          const int jb = j0 + sg.j + t;                          // table index of this block
+          const int vr = min(bs, n_rows - jb * bs);              // rows of the block before the end
+          const int lr = (jb == j0) ? r0 - j0 * bs : 0;          // rows of the block before the window
+          if (vr >= bs && lr == 0) {
             for (int tt = 0; tt < tiles_per_page; ++tt)
-              gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, 16, st, geo);
+              gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, 0, 16, st, geo);
           } else {
             for (int tt = 0; tt < tiles_per_page; ++tt) {
-              const int valid = vr - tt * 16;
+              const int valid = vr - tt * 16, lo_valid = lr - tt * 16;
               if (valid <= 0) break;
-              if (valid >= 16)
-                gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, 16, st, geo);
+              if (lo_valid >= 16) continue;
+              if (valid >= 16 && lo_valid <= 0)
+                gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, 0, 16, st, geo);
               else
-                gqa_tile<T, D, GW, true>(kp + tt * 16 * D, vp + tt * 16 * D, wp, valid, st, geo);
+                gqa_tile<T, D, GW, true>(kp + tt * 16 * D, vp + tt * 16 * D, wp, lo_valid, valid, st, geo);
             }
           }
         }
