@@ -59,6 +59,19 @@ def append_to_paged(k, v, slot_mapping, k_cache, v_cache):
     return kc, vc
 
 
+def copy_blocks(cache, pairs):
+    """Copy-on-write step: block dst becomes a copy of block src for every (src, dst) pair.
+
+    PagedAttention sharing ("KV Cache（键值缓存）" section 2.3): a block held by
+    several sequences is copied before one of them writes into it. cache is a
+    pool [num_blocks, ...]; returns a new array (the input is not modified).
+    """
+    out = np.array(cache, copy=True)
+    for src, dst in pairs:
+        out[int(dst)] = cache[int(src)]
+    return out
+
+
 def gather_logical(cache, block_table_row, n: int, kv_head: int) -> np.ndarray:
     """Rows 0..n-1 of one sequence and one kv head, in logical order: [n, D]."""
     bs = cache.shape[2]

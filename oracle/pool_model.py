@@ -17,8 +17,12 @@ Readings where the pages are silent:
 * sequence ids are handed out 0, 1, 2, ... and never reused;
 * forking copies the parent's table and length and adds one reference to
   each of its blocks;
-* appending into a partly filled block that has more than one holder would
-  need copy-on-write, which this pool does not do: the request is refused;
+* appending into a partly filled block that has more than one holder needs
+  copy-on-write: ``reserve`` refuses it, ``reserve_cow`` gives the writer a
+  fresh block (lowest free id), drops the writer's reference to the shared
+  one and reports the pair (shared block, fresh block) whose contents the
+  caller copies before the new rows are written. The copy is of the whole
+  block; only its first ``length % block_size`` rows are live;
 * a reservation that needs more blocks than are free allocates nothing;
 * unused table entries are padded with 0.
 """
@@ -92,6 +96,26 @@ class PoolModel:
             slots.append(blocks[pos // bs] * bs + pos % bs)
         self.seqs[sid][1] = n + n_new
         return slots
+
+    def reserve_cow(self, sid: int, n_new: int):
+        """As ``reserve``, but a shared partly filled last block is first replaced
+        by a private copy. Returns (slots, copy) with copy = (src, dst) or None."""
+        blocks, n = self.seqs[sid]
+        bs = self.block_size
+        if n_new < 0:
+            raise ValueError("n_new must be >= 0")
+        copy = None
+        if n_new > 0 and n % bs != 0 and self.ref[blocks[-1]] > 1:
+            # the fresh block and the new tail blocks must all be available up front
+            need = 1 + (-(-(n + n_new) // bs) - len(blocks))
+            if need > self.free_blocks():
+                raise NoBlocks("pool exhausted")
+            old = blocks[-1]
+            new = self._take_free()
+            self.ref[old] -= 1
+            blocks[-1] = new
+            copy = (old, new)
+        return self.reserve(sid, n_new), copy
 
     def free(self, sid: int):
         blocks, _ = self.seqs.pop(sid)
