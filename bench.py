@@ -360,6 +360,8 @@ def run_variant(kvc, name, flush, steps):
         r = measure_gqa_case(kvc, c, steps, 5, flush, window=1024)
         r["note"] = "sliding window of 1024 rows: bytes count the visible rows only"
         return r
+    if name == "cow_copy_blocks_2048":
+        return measure_copy_blocks(kvc, flush, steps)
     if name == "gqa_ragged_17_31_32":
         c = W.gqa_case(3, 64, 8, 128, 16, [17, 31, 32], "bf16", 45, device="cuda")
         return measure_gqa_case(kvc, c, steps, 5, flush)
@@ -371,7 +373,7 @@ def run_variant(kvc, name, flush, steps):
 
 
 VARIANTS = ("gqa_b32_ctx4096", "mha_shared_prefix_8x8", "gqa_long_splitk", "gqa_ragged_17_31_32", "tiny_mha_fp32",
-            "mla_deepseek_v2", "gqa_window_b32_ctx4096_w1024")
+            "mla_deepseek_v2", "gqa_window_b32_ctx4096_w1024", "cow_copy_blocks_2048")
 
 
 def variants(kvc, flush, steps):
@@ -399,6 +401,34 @@ def measure_tiny(kvc, flush, steps):
     ms = sum(res)
     return {"ms_per_step_2_layers": round(ms, 5), "seq_layer_steps_per_s": round(2 / (ms / 1e3), 1),
             "note": "latency-bound: one sequence of 69 tokens"}
+
+
+def measure_copy_blocks(kvc, flush, steps):
+    """Copy-on-write: 2048 (shared, fresh) block pairs copied in the K and the V pool of the Llama-3-8B layer
+    (8 kv heads x 16 rows x 128 dims bf16 = 32 KB per block and pool); bytes = read + write."""
+    import torch
+    from paged_kv_cache_157_gb300 import workloads as W
+    nblk, n_pairs = 16384, 2048
+    g = torch.Generator(device="cuda")
+    g.manual_seed(71)
+    kc = W.normal((nblk, 8, 16, 128), "bf16", g)
+    vc = W.normal((nblk, 8, 16, 128), "bf16", g)
+    perm = torch.randperm(nblk, generator=torch.Generator().manual_seed(72))[:2 * n_pairs]
+    pairs = perm.view(n_pairs, 2).to(torch.int64).cuda()
+
+    class S:
+        def append(self):
+            pass
+
+        def decode(self):
+            kvc.copy_blocks(kc, pairs)
+            kvc.copy_blocks(vc, pairs)
+
+    _, dec_ms, _, _ = time_steps(S(), steps, 5, flush)
+    moved = 2 * 2 * n_pairs * kc[0].numel() * kc.element_size()
+    dms = statistics.mean(dec_ms)
+    return {"ms": round(dms, 5), "gbps": round(moved / dms / 1e6, 1), "bytes_per_step": moved,
+            "note": "read + write bytes of two kvc_copy_blocks calls (K and V pools)"}
 
 
 def measure_mla(kvc, flush, steps):

@@ -132,6 +132,19 @@ kvc_status kvc_append_latent(const void* c, const int64_t* slot_mapping, int64_t
                              void* latent_cache, int64_t num_blocks, int block_size, int d_c, int d_r,
                              kvc_dtype dtype, kvc_stream stream);
 
+/* Copy-on-write block copy inside one pool: for i < n_pairs, block
+ * pairs[2i + 1] becomes a byte copy of block pairs[2i]. cache: device pool of
+ * num_blocks blocks of block_bytes bytes each (for a K or V pool,
+ * n_kv_heads * block_size * head_dim * element size; for a latent pool,
+ * block_size * (d_c + d_r) * element size), 16-byte aligned; block_bytes a
+ * multiple of 16. pairs: int64 [n_pairs, 2] in device memory. Destination
+ * blocks must be distinct and must not be sources in the same call (copies
+ * run concurrently). Pairs naming a block outside the pool are skipped and set
+ * KVC_FLAG_BAD_BLOCK. Asynchronous on `stream`.
+ * Source: llm-compass 2.3 (copy-on-write of shared PagedAttention blocks). */
+kvc_status kvc_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes, const int64_t* pairs,
+                           int64_t n_pairs, kvc_stream stream);
+
 /* ----------------------------------------------------------------- decode */
 
 /* Bytes of scratch that kvc_decode_attention needs for these shapes on the
@@ -259,6 +272,17 @@ kvc_status kvc_seq_fork(kvc_pool* pool, int64_t parent, int64_t* child);
  * KVC_ERR_UNSUPPORTED if the last block is partly filled and shared
  * (would need copy-on-write). */
 kvc_status kvc_seq_reserve(kvc_pool* pool, int64_t seq, int64_t n_new, int64_t* slots_out);
+/* kvc_seq_reserve with copy-on-write: if the sequence's last block is partly
+ * filled and held by other sequences too, the sequence first gets a fresh
+ * block (the lowest free id) in its place, drops its reference to the shared
+ * block, and copy_pair (2 entries, host memory) receives (shared, fresh):
+ * the caller must run kvc_copy_blocks on every pool (K and V, or the latent
+ * pool) with that pair before it writes the new rows. copy_pair is (-1, -1)
+ * when nothing has to be copied. KVC_ERR_NO_BLOCKS if the fresh block and
+ * the new tail blocks are not all free (then nothing changes).
+ * Source: llm-compass 2.3 (blocks shared by reference count are copied
+ * before a holder writes into them: parallel sampling, beam search). */
+kvc_status kvc_seq_reserve_cow(kvc_pool* pool, int64_t seq, int64_t n_new, int64_t* slots_out, int64_t* copy_pair);
 /* Drops the sequence; each of its blocks loses one reference. */
 kvc_status kvc_seq_free(kvc_pool* pool, int64_t seq);
 kvc_status kvc_seq_length(kvc_pool* pool, int64_t seq, int64_t* length);

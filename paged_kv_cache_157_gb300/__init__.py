@@ -19,7 +19,7 @@ import threading
 __all__ = [
     "KvcError", "KvcLibraryMissing", "raw", "lib_path", "symbols",
     "append", "append_latent", "decode_workspace_size", "decode_attention", "decode_attention_static",
-    "decode_attention_window",
+    "decode_attention_window", "copy_blocks",
     "decode_mla_workspace_size", "decode_attention_mla", "set_option", "get_option",
     "get_error_flags", "BlockPool", "slots_from_tables",
     "F32", "F16", "BF16", "FLAG_BAD_BLOCK", "FLAG_BAD_LEN", "FLAG_BAD_SLOT", "FLAG_TIMEOUT", "FLAG_WORKSPACE",
@@ -71,6 +71,8 @@ SIGNATURES = {
     "kvc_seq_add": (_i32, [_vp, _i64p]),
     "kvc_seq_fork": (_i32, [_vp, _i64, _i64p]),
     "kvc_seq_reserve": (_i32, [_vp, _i64, _i64, _vp]),
+    "kvc_seq_reserve_cow": (_i32, [_vp, _i64, _i64, _vp, _vp]),
+    "kvc_copy_blocks": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp]),
     "kvc_seq_free": (_i32, [_vp, _i64]),
     "kvc_seq_length": (_i32, [_vp, _i64, _i64p]),
     "kvc_block_refcount": (_i32, [_vp, _i64, _i32p]),
@@ -342,6 +344,14 @@ class BlockPool:
         _check(self._lib.kvc_seq_reserve(self._h, seq, n_new, buf), "kvc_seq_reserve")
         return list(buf[:n_new])
 
+    def reserve_cow(self, seq: int, n_new: int):
+        """kvc_seq_reserve_cow: (slots, copy) with copy = (shared block, fresh block) or None."""
+        buf = (ctypes.c_int64 * max(1, n_new))()
+        pair = (ctypes.c_int64 * 2)()
+        _check(self._lib.kvc_seq_reserve_cow(self._h, seq, n_new, buf, pair), "kvc_seq_reserve_cow")
+        copy = None if pair[0] < 0 else (int(pair[0]), int(pair[1]))
+        return [int(buf[i]) for i in range(n_new)], copy
+
     def free(self, seq: int):
         _check(self._lib.kvc_seq_free(self._h, seq), "kvc_seq_free")
 
@@ -387,3 +397,17 @@ def decode_attention_window(q, k_cache, v_cache, block_tables, context_lens, sca
                             stream=None):
     """kvc_decode_attention_window: decode over the newest ``window`` rows of every sequence."""
     decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace, stream, window=window)
+
+
+def copy_blocks(cache, pairs, stream=None):
+    """kvc_copy_blocks: block pairs[i, 1] of ``cache`` (a pool tensor [num_blocks, ...]) becomes a copy of
+    block pairs[i, 0]. pairs: int64 device tensor [n, 2]."""
+    torch = _torch()
+    _require(cache, "cache")
+    _require(pairs, "pairs", torch.int64)
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be [n, 2]")
+    nb = cache.shape[0]
+    block_bytes = cache[0].numel() * cache.element_size()
+    _check(raw().kvc_copy_blocks(_ptr(cache), nb, block_bytes, _ptr(pairs), pairs.shape[0], _stream(stream)),
+           "kvc_copy_blocks")

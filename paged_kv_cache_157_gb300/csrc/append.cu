@@ -66,6 +66,27 @@ static kvc_status launch_append(bool two, const void* s0, const void* s1, void* 
   return finish_call(stream);
 }
 
+// Copy-on-write: block pairs[2i] -> block pairs[2i + 1] inside one pool,
+// block_chunks 16-byte chunks per block. Pairs with a block id outside the
+// pool are skipped and flagged; src == dst is a no-op.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* cache, const int64_t* __restrict__ pairs,
+                                                          int64_t n_pairs, int64_t num_blocks, int64_t block_chunks,
+                                                          unsigned int* err) {
+  const int64_t total = n_pairs * block_chunks;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t pr = i / block_chunks;
+    const int64_t c = i - pr * block_chunks;
+    const int64_t src = __ldg(pairs + 2 * pr), dst = __ldg(pairs + 2 * pr + 1);
+    if (src < 0 || dst < 0 || src >= num_blocks || dst >= num_blocks) {
+      if (c == 0) set_flag(err, 0x1u);
+      continue;
+    }
+    if (src == dst) continue;
+    cache[dst * block_chunks + c] = cache[src * block_chunks + c];
+  }
+}
+
 }  // namespace kvc
 
 extern "C" {
@@ -85,6 +106,27 @@ kvc_status kvc_append_latent(const void* c, const int64_t* slot_mapping, int64_t
   if (d_c < 1 || d_r < 0) return kvc::fail(KVC_ERR_INVALID_ARG, "d_c must be >= 1 and d_r >= 0");
   return kvc::launch_append(false, c, nullptr, latent_cache, nullptr, slot_mapping, num_tokens, num_blocks, block_size,
                             1, d_c + d_r, dtype, static_cast<cudaStream_t>(stream));
+}
+
+kvc_status kvc_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes, const int64_t* pairs, int64_t n_pairs,
+                           kvc_stream stream) {
+  using namespace kvc;
+  clear_error();
+  if (num_blocks < 1 || block_bytes < 16 || block_bytes % 16 != 0 || n_pairs < 0)
+    return fail(KVC_ERR_INVALID_ARG, "num_blocks >= 1, block_bytes a positive multiple of 16, n_pairs >= 0");
+  if (n_pairs == 0) return KVC_OK;
+  if (cache == nullptr || pairs == nullptr) return fail(KVC_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(cache)) return fail(KVC_ERR_INVALID_ARG, "cache must be 16-byte aligned");
+  DeviceInfo* dev = nullptr;
+  kvc_status st = current_device(&dev);
+  if (st != KVC_OK) return st;
+  const int64_t chunks = block_bytes / 16;
+  const int64_t want = (n_pairs * chunks + 255) / 256;
+  const int grid = static_cast<int>(want < dev->num_sms * 16LL ? want : dev->num_sms * 16LL);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  copy_blocks_kernel<<<grid, 256, 0, s>>>(static_cast<uint4*>(cache), pairs, n_pairs, num_blocks, chunks,
+                                          dev->error_word);
+  return finish_call(s);
 }
 
 }  // extern "C"

@@ -8,8 +8,9 @@
 //
 // Policy: the free set is a min-heap, so a new block is always the lowest
 // free id; sequence ids count up from 0 and are never reused. Appending into
-// a partly filled block that another sequence also holds would need
-// copy-on-write, which is not implemented: such a request is refused.
+// a partly filled block that another sequence also holds needs copy-on-write:
+// kvc_seq_reserve refuses it, kvc_seq_reserve_cow first gives the writer a
+// fresh block and reports the (shared, fresh) pair for kvc_copy_blocks.
 #include <cstdint>
 #include <functional>
 #include <new>
@@ -117,6 +118,35 @@ kvc_status kvc_seq_reserve(kvc_pool* pool, int64_t seq, int64_t n_new, int64_t* 
   }
   sq->length = n + n_new;
   return KVC_OK;
+}
+
+kvc_status kvc_seq_reserve_cow(kvc_pool* pool, int64_t seq, int64_t n_new, int64_t* slots_out, int64_t* copy_pair) {
+  kvc::clear_error();
+  kvc_pool::Seq* sq = nullptr;
+  kvc_status s = find_seq(pool, seq, &sq);
+  if (s != KVC_OK) return s;
+  if (copy_pair == nullptr) return kvc::fail(KVC_ERR_INVALID_ARG, "copy_pair is NULL");
+  if (n_new < 0) return kvc::fail(KVC_ERR_INVALID_ARG, "n_new must be >= 0");
+  copy_pair[0] = -1;
+  copy_pair[1] = -1;
+  const int64_t bs = pool->block_size;
+  const int64_t n = sq->length;
+  if (n_new > 0 && n % bs != 0 && pool->ref[static_cast<size_t>(sq->blocks.back())] > 1) {
+    // the fresh copy and every new tail block must be available up front
+    const int64_t need = 1 + (n + n_new + bs - 1) / bs - static_cast<int64_t>(sq->blocks.size());
+    if (need > static_cast<int64_t>(pool->free_heap.size()))
+      return kvc::fail(KVC_ERR_NO_BLOCKS, "need %lld blocks, %zu free", static_cast<long long>(need),
+                       pool->free_heap.size());
+    const int64_t old = sq->blocks.back();
+    const int64_t fresh = pool->free_heap.top();
+    pool->free_heap.pop();
+    pool->ref[static_cast<size_t>(fresh)] = 1;
+    pool->ref[static_cast<size_t>(old)] -= 1;
+    sq->blocks.back() = fresh;
+    copy_pair[0] = old;
+    copy_pair[1] = fresh;
+  }
+  return kvc_seq_reserve(pool, seq, n_new, slots_out);
 }
 
 kvc_status kvc_seq_free(kvc_pool* pool, int64_t seq) {

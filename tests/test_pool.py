@@ -50,6 +50,21 @@ def test_random_operations_match_model(kvc, seed):
             pool.free(sid)
             model.free(sid)
             live.remove(sid)
+        elif op < 0.55:
+            # copy-on-write reservation: same slots and the same (shared, fresh) pair as the model
+            sid = rng.choice(live)
+            n = rng.choice([1, 2, bs, 2 * bs + 3])
+            try:
+                expect = model.reserve_cow(sid, n)
+                err = None
+            except NoBlocks as e:
+                expect, err = None, e
+            if err is None:
+                assert pool.reserve_cow(sid, n) == expect
+            else:
+                with pytest.raises(kvc.KvcError) as ei:
+                    pool.reserve_cow(sid, n)
+                assert ei.value.status == kvc.ERR_NO_BLOCKS
         else:
             sid = rng.choice(live)
             n = rng.choice([1, 1, 2, 5, bs, 3 * bs + 1])
