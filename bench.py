@@ -360,6 +360,8 @@ def run_variant(kvc, name, flush, steps):
         r = measure_gqa_case(kvc, c, steps, 5, flush, window=1024)
         r["note"] = "sliding window of 1024 rows: bytes count the visible rows only"
         return r
+    if name == "gqa_fp8_b32_ctx4096":
+        return measure_fp8(kvc, flush, steps)
     if name == "cow_copy_blocks_2048":
         return measure_copy_blocks(kvc, flush, steps)
     if name == "gqa_ragged_17_31_32":
@@ -373,7 +375,7 @@ def run_variant(kvc, name, flush, steps):
 
 
 VARIANTS = ("gqa_b32_ctx4096", "mha_shared_prefix_8x8", "gqa_long_splitk", "gqa_ragged_17_31_32", "tiny_mha_fp32",
-            "mla_deepseek_v2", "gqa_window_b32_ctx4096_w1024", "cow_copy_blocks_2048")
+            "mla_deepseek_v2", "gqa_window_b32_ctx4096_w1024", "cow_copy_blocks_2048", "gqa_fp8_b32_ctx4096")
 
 
 def variants(kvc, flush, steps):
@@ -401,6 +403,41 @@ def measure_tiny(kvc, flush, steps):
     ms = sum(res)
     return {"ms_per_step_2_layers": round(ms, 5), "seq_layer_steps_per_s": round(2 / (ms / 1e3), 1),
             "note": "latency-bound: one sequence of 69 tokens"}
+
+
+def measure_fp8(kvc, flush, steps):
+    """Llama-3-8B-shaped layer over an FP8 e4m3 cache (batch 32, lengths 4096): kvc_append_fp8 of the new tokens +
+    kvc_decode_attention_fp8 (bf16 queries and output). Bytes: 1 per cached K/V element + 4 per (row, kv head) of
+    V scales, plus q, out, tables, lengths."""
+    import torch
+    from paged_kv_cache_157_gb300 import workloads as W
+    c = W.fp8_case(32, 32, 8, 128, 16, [4096] * 32, 94, device="cuda")
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in c.items()}
+    lens = c["context_lens"].tolist()
+    B, hq, hkv, D, bs = 32, 32, 8, 128, 16
+    slots = kvc.slots_from_tables(c["block_tables"], bs, list(range(B)), [n - 1 for n in lens]).cuda()
+    out = torch.empty((B, hq, D), dtype=torch.bfloat16, device="cuda")
+    ws = kvc.new_decode_workspace(B, hq, hkv, D, bs, c["block_tables"].shape[1])
+    scale = 1.0 / math.sqrt(D)
+
+    class S:
+        def append(self):
+            kvc.append_fp8(d["k_new"], d["v_new"], slots, d["k_cache"], d["v_cache"], d["v_scale"], d["k_scale"])
+
+        def decode(self):
+            kvc.decode_attention_fp8(d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
+                                     d["block_tables"], d["context_lens"], scale, out, ws)
+
+    step_ms, dec_ms, _, _ = time_steps(S(), steps, 5, flush)
+    rows = sum(lens)
+    dec_b = rows * hkv * (2 * D + 4) + 2 * B * hq * D * 2 + sum(-(-n // bs) for n in lens) * 4 + B * 4
+    dms = statistics.mean(dec_ms)
+    bf16_equiv = rows * hkv * D * 2 * 2
+    return {"decode_ms": round(dms, 5), "decode_gbps": round(dec_b / dms / 1e6, 1),
+            "frac_of_8tbs": round(dec_b / dms / 1e6 / NOMINAL_HBM_GBS, 4),
+            "bf16_equivalent_gbps": round(bf16_equiv / dms / 1e6, 1),
+            "ms_per_step": round(statistics.mean(step_ms), 5), "bytes_per_step": dec_b,
+            "note": "bf16_equivalent_gbps counts the bytes the same rows take in bf16"}
 
 
 def measure_copy_blocks(kvc, flush, steps):

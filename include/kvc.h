@@ -132,6 +132,23 @@ kvc_status kvc_append_latent(const void* c, const int64_t* slot_mapping, int64_t
                              void* latent_cache, int64_t num_blocks, int block_size, int d_c, int d_r,
                              kvc_dtype dtype, kvc_stream stream);
 
+/* FP8 KV cache append: quantises token t's K/V rows (k, v: [num_tokens,
+ * n_kv_heads, head_dim] in `dtype`, F32/F16/BF16) and writes them at
+ * slot_mapping[t] (negative: skipped; >= num_blocks*block_size: skipped and
+ * KVC_FLAG_BAD_SLOT) into k_cache / v_cache: uint8 e4m3 codes
+ * [num_blocks, n_kv_heads, block_size, head_dim]. K code = e4m3(k /
+ * k_scale[h, d]) with the caller's per-channel scales k_scale [n_kv_heads,
+ * head_dim] fp32; V code = e4m3(v / s) with one scale per (token, kv head)
+ * s = max_d |v| / 448 (1 for an all-zero row), written to v_scale
+ * [num_blocks, n_kv_heads, block_size] fp32. Divisions are fp32, correctly
+ * rounded; e4m3 rounding is to nearest, ties to even, saturating at +-448.
+ * head_dim must be even. Source: "KV-Cache——为什么AI回复越来越快" section 08
+ * (KV-Cache quantisation to FP8: per-token scales for V, per-channel scales
+ * for K). */
+kvc_status kvc_append_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                          void* k_cache, void* v_cache, float* v_scale, const float* k_scale, int64_t num_blocks,
+                          int block_size, int n_kv_heads, int head_dim, kvc_dtype dtype, kvc_stream stream);
+
 /* Copy-on-write block copy inside one pool: for i < n_pairs, block
  * pairs[2i + 1] becomes a byte copy of block pairs[2i]. cache: device pool of
  * num_blocks blocks of block_bytes bytes each (for a K or V pool,
@@ -194,6 +211,21 @@ kvc_status kvc_decode_attention_window(const void* q, const void* k_cache, const
                                        int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, int window,
                                        kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
                                        size_t workspace_bytes, kvc_stream stream);
+
+/* FP8 KV cache decode: as kvc_decode_attention over the caches written by
+ * kvc_append_fp8, attending k = e4m3value(code) * k_scale[h, d] and
+ * v = e4m3value(code) * v_scale[row] (the scales fold into the query and into
+ * the softmax weights, so the kernel reads one byte per cached element). q is
+ * bf16 [batch, n_q_heads, head_dim]; head_dim 64, 128 or 256; k_scale and
+ * v_scale 16-byte aligned. Same tables, lengths, workspace (size query:
+ * kvc_decode_workspace_size) and error rules as kvc_decode_attention.
+ * Source: "KV-Cache——为什么AI回复越来越快" section 08 (FP8 KV cache). */
+kvc_status kvc_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                                    const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int batch, float scale, int n_q_heads,
+                                    int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, void* out,
+                                    kvc_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                    kvc_stream stream);
 
 /* kvc_decode_attention for callers that cannot allocate device memory.
  *

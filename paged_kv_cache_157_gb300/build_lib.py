@@ -27,6 +27,7 @@ SOURCES = [
     "decode_gqa_f32.cu",
     "decode_gqa_f16.cu",
     "decode_gqa_bf16.cu",
+    "decode_gqa_fp8.cu",
     "decode_mla.cu",
     "pool.cpp",
 ]

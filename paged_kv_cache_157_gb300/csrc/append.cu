@@ -66,6 +66,50 @@ static kvc_status launch_append(bool two, const void* s0, const void* s1, void* 
   return finish_call(stream);
 }
 
+// FP8 append: one warp per (token, kv head). K is divided by its
+// per-channel scale, V by its row's scale s = max |v| / 448 (1 for an all-zero
+// row), both in fp32 with correctly rounded division, and rounded to e4m3
+// (nearest, ties to even, saturating at +-448). Codes go to the pools, s to
+// the V-scale pool [num_blocks, n_heads, block_size].
+template <typename T>
+__global__ void __launch_bounds__(256) append_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v,
+                                                         const int64_t* __restrict__ slots, int64_t num_tokens,
+                                                         int n_heads, int D, int block_size, int64_t num_slots,
+                                                         const float* __restrict__ k_scale, unsigned char* kc,
+                                                         unsigned char* vc, float* vs, unsigned int* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t wi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; wi < num_tokens * n_heads;
+       wi += warps) {
+    const int64_t t = wi / n_heads;
+    const int h = static_cast<int>(wi - t * n_heads);
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (lane == 0) set_flag(err, 0x4u);
+      continue;
+    }
+    const int64_t blk = slot / block_size, off = slot - blk * block_size;
+    const T* kr = k + wi * D;
+    const T* vr = v + wi * D;
+    float vmax = 0.f;
+    for (int d = 2 * lane; d < D; d += 64)
+      vmax = fmaxf(vmax, fmaxf(fabsf(Elem<T>::to_float(vr[d])), fabsf(Elem<T>::to_float(vr[d + 1]))));
+    vmax = warp_max(vmax);
+    const float s = vmax > 0.f ? __fdiv_rn(vmax, 448.0f) : 1.0f;
+    const int64_t row = ((blk * n_heads + h) * block_size + off) * D;
+    for (int d = 2 * lane; d < D; d += 64) {
+      const float k0 = __fdiv_rn(Elem<T>::to_float(kr[d]), __ldg(k_scale + h * D + d));
+      const float k1 = __fdiv_rn(Elem<T>::to_float(kr[d + 1]), __ldg(k_scale + h * D + d + 1));
+      const float v0 = __fdiv_rn(Elem<T>::to_float(vr[d]), s);
+      const float v1 = __fdiv_rn(Elem<T>::to_float(vr[d + 1]), s);
+      *reinterpret_cast<unsigned short*>(kc + row + d) = float2_to_fp8x2(k0, k1);
+      *reinterpret_cast<unsigned short*>(vc + row + d) = float2_to_fp8x2(v0, v1);
+    }
+    if (lane == 0) vs[(blk * n_heads + h) * block_size + off] = s;
+  }
+}
+
 // Copy-on-write: block pairs[2i] -> block pairs[2i + 1] inside one pool,
 // block_chunks 16-byte chunks per block. Pairs with a block id outside the
 // pool are skipped and flagged; src == dst is a no-op.
@@ -106,6 +150,48 @@ kvc_status kvc_append_latent(const void* c, const int64_t* slot_mapping, int64_t
   if (d_c < 1 || d_r < 0) return kvc::fail(KVC_ERR_INVALID_ARG, "d_c must be >= 1 and d_r >= 0");
   return kvc::launch_append(false, c, nullptr, latent_cache, nullptr, slot_mapping, num_tokens, num_blocks, block_size,
                             1, d_c + d_r, dtype, static_cast<cudaStream_t>(stream));
+}
+
+kvc_status kvc_append_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                          void* v_cache, float* v_scale, const float* k_scale, int64_t num_blocks, int block_size,
+                          int n_kv_heads, int head_dim, kvc_dtype dtype, kvc_stream stream) {
+  using namespace kvc;
+  clear_error();
+  if (!dtype_ok(dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || n_kv_heads < 1 || head_dim < 2 || head_dim % 2 != 0)
+    return fail(KVC_ERR_INVALID_ARG, "sizes must be positive (num_tokens >= 0, head_dim even)");
+  if (num_tokens == 0) return KVC_OK;
+  if (k == nullptr || v == nullptr || slot_mapping == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      v_scale == nullptr || k_scale == nullptr)
+    return fail(KVC_ERR_INVALID_ARG, "NULL pointer");
+  DeviceInfo* dev = nullptr;
+  kvc_status st = current_device(&dev);
+  if (st != KVC_OK) return st;
+  const int64_t warps = num_tokens * n_kv_heads;
+  const int64_t want = (warps + 7) / 8;
+  const int grid = static_cast<int>(want < dev->num_sms * 16LL ? want : dev->num_sms * 16LL);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* kc = static_cast<unsigned char*>(k_cache);
+  unsigned char* vc = static_cast<unsigned char*>(v_cache);
+  const int64_t num_slots = num_blocks * block_size;
+  switch (dtype) {
+    case KVC_F32:
+      append_fp8_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(k), static_cast<const float*>(v),
+                                                    slot_mapping, num_tokens, n_kv_heads, head_dim, block_size,
+                                                    num_slots, k_scale, kc, vc, v_scale, dev->error_word);
+      break;
+    case KVC_F16:
+      append_fp8_kernel<__half><<<grid, 256, 0, s>>>(static_cast<const __half*>(k), static_cast<const __half*>(v),
+                                                     slot_mapping, num_tokens, n_kv_heads, head_dim, block_size,
+                                                     num_slots, k_scale, kc, vc, v_scale, dev->error_word);
+      break;
+    case KVC_BF16:
+      append_fp8_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), slot_mapping, num_tokens,
+          n_kv_heads, head_dim, block_size, num_slots, k_scale, kc, vc, v_scale, dev->error_word);
+      break;
+  }
+  return finish_call(s);
 }
 
 kvc_status kvc_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes, const int64_t* pairs, int64_t n_pairs,

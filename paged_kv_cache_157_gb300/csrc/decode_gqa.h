@@ -36,6 +36,8 @@ struct GqaParams {
   int stages;
   int unit_mode;  // 1: CTA u handles unit u completely (no records)
   int window;     // sliding window: attend the newest `window` rows (0: all rows)
+  const float* k_scale;  // FP8 caches: per-channel K scales [n_kv_heads, head_dim]
+  const float* v_scale;  // FP8 caches: per-token V scales [num_blocks, n_kv_heads, block_size]
   float qscale;   // scale * log2(e)
 };
 
@@ -56,27 +58,34 @@ __host__ __device__ constexpr int gqa_max_chunk(int GH) { return kGqaWarps / gqa
 
 // Shared-memory carve-up, identical on host and device. The CTA has one ring
 // of `stages` stages, each [K chunk: hc pages][V chunk: hc pages][query rows
-// of the unit: hc x GH]; every warp has a [heads of the warp][16 rows] fp32
-// buffer for the softmax weights of its current tile.
+// of the unit: hc x GH][FP8 caches only: the chunk's per-token V scales,
+// hc x block_size fp32]; every warp has a [heads of the warp][16 rows] fp32
+// buffer for the softmax weights of its current tile. elt_bytes is the cache
+// element size, q_bytes the query element size, vs_bytes 4 for FP8 caches
+// (one scale per row) and 0 otherwise.
 struct GqaSmem {
   size_t stage_off, p_off, bar_off, rel_off, misc_off, scan_off, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline size_t gqa_stage_bytes(int elt_bytes, int D, int GH, int block_size, int hc) {
-  return (2ull * hc * block_size * D + static_cast<size_t>(hc) * GH * D) * elt_bytes;
+__host__ __device__ inline size_t gqa_stage_bytes(int elt_bytes, int q_bytes, int vs_bytes, int D, int GH,
+                                                  int block_size, int hc) {
+  return 2ull * hc * block_size * D * elt_bytes + static_cast<size_t>(hc) * GH * D * q_bytes +
+         static_cast<size_t>(hc) * block_size * vs_bytes;
 }
 
 __host__ __device__ inline size_t gqa_p_bytes_per_warp(int GH) {
   return static_cast<size_t>(GH / gqa_warps_per_kvhead(GH)) * 16 * 4;
 }
 
-__host__ __device__ inline GqaSmem gqa_smem_layout(int elt_bytes, int D, int GH, int block_size, int hc, int stages,
-                                                  int batch) {
+__host__ __device__ inline GqaSmem gqa_smem_layout(int elt_bytes, int q_bytes, int vs_bytes, int D, int GH,
+                                                  int block_size, int hc, int stages, int batch) {
   GqaSmem s;
   s.stage_off = 0;
-  s.p_off = align_up(static_cast<size_t>(stages) * gqa_stage_bytes(elt_bytes, D, GH, block_size, hc), 16);
+  s.p_off = align_up(static_cast<size_t>(stages) *
+                         align_up(gqa_stage_bytes(elt_bytes, q_bytes, vs_bytes, D, GH, block_size, hc), 16),
+                     16);
   s.bar_off = align_up(s.p_off + kGqaWarps * gqa_p_bytes_per_warp(GH), 16);
   s.rel_off = s.bar_off + static_cast<size_t>(stages) * 8;  // one "full" mbarrier per stage
   s.misc_off = align_up(s.rel_off + static_cast<size_t>(stages) * 8, 16);  // release and issue counts per stage
@@ -88,5 +97,8 @@ __host__ __device__ inline GqaSmem gqa_smem_layout(int elt_bytes, int D, int GH,
 template <typename T>
 kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
                         int* occ);
+// FP8 e4m3 caches with bf16 queries (head_dim 64, 128 or 256).
+kvc_status gqa_dispatch_fp8(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
+                            int* occ);
 
 }  // namespace kvc

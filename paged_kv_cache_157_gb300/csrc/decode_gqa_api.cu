@@ -44,7 +44,10 @@ int head_subgroup(int group) {
   return 1;
 }
 
-kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, int elt, int max_smem, GqaPlan* pl) {
+// elt: cache element bytes; q_elt: query element bytes; vsb: V-scale bytes
+// per cached row (4 for FP8 caches, else 0).
+kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, int elt, int q_elt, int vsb, int max_smem,
+                     GqaPlan* pl) {
   const int group = n_q_heads / n_kv_heads;
   pl->GH = head_subgroup(group);
   pl->n_hsub = group / pl->GH;
@@ -58,13 +61,14 @@ kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, in
   const size_t budget = kStageBudget > fixed ? kStageBudget - fixed : 0;
   int S = 1;
   for (;;) {
-    const size_t stage = gqa_stage_bytes(elt, D, pl->GH, bs, hc);
+    const size_t stage = align_up(gqa_stage_bytes(elt, q_elt, vsb, D, pl->GH, bs, hc), 16);
     S = std::max(1, std::min(static_cast<int>(budget / stage), 8));
     if (S >= 2 || hc == 1) break;
     hc /= 2;  // keep at least two stages in flight
   }
-  GqaSmem L = gqa_smem_layout(elt, D, pl->GH, bs, hc, S, batch);
-  while (S > 1 && L.total > static_cast<size_t>(max_smem)) L = gqa_smem_layout(elt, D, pl->GH, bs, hc, --S, batch);
+  GqaSmem L = gqa_smem_layout(elt, q_elt, vsb, D, pl->GH, bs, hc, S, batch);
+  while (S > 1 && L.total > static_cast<size_t>(max_smem))
+    L = gqa_smem_layout(elt, q_elt, vsb, D, pl->GH, bs, hc, --S, batch);
   if (L.total > static_cast<size_t>(max_smem))
     return fail(KVC_ERR_UNSUPPORTED, "block_size %d x head_dim %d needs %zu bytes of shared memory (max %d)", bs, D,
                 L.total, max_smem);
@@ -120,8 +124,10 @@ kvc_status occupancy(const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
   return gqa_dispatch<T>(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ);
 }
 
-kvc_status occupancy_for(kvc_dtype dt, const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
-  switch (dt) {
+// dt < 0: FP8 caches with bf16 queries
+kvc_status occupancy_for(int dt, const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
+  if (dt < 0) return gqa_dispatch_fp8(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ);
+  switch (static_cast<kvc_dtype>(dt)) {
     case KVC_F32: return occupancy<float>(p, D, pl, occ);
     case KVC_F16: return occupancy<__half>(p, D, pl, occ);
     case KVC_BF16: return occupancy<__nv_bfloat16>(p, D, pl, occ);
@@ -145,7 +151,8 @@ kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, i
   DeviceInfo* dev = nullptr;
   if ((s = current_device(&dev)) != KVC_OK) return s;
   GqaPlan pl;
-  if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, 2, dev->max_smem_optin, &pl)) != KVC_OK)
+  if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, 2, 2, 0, dev->max_smem_optin, &pl)) !=
+      KVC_OK)
     return s;
   const int64_t G = plan_ctas(dev, kMaxCtasPerSm, static_cast<int64_t>(batch) * n_kv_heads * pl.n_hsub,
                              max_blocks_per_seq);
@@ -159,11 +166,19 @@ namespace kvc {
 namespace {
 
 // Decode over the newest `window` rows of every sequence (window 0: all rows).
+// k_scale / v_scale non-NULL: FP8 e4m3 caches with bf16 queries (dtype is
+// then the query dtype and must be BF16).
 kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                        int max_blocks_per_seq, const int32_t* context_lens, int batch, float scale, int n_q_heads,
                        int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, int window, kvc_dtype dtype,
-                       void* out, kvc_dtype out_dtype, void* workspace, size_t workspace_bytes, kvc_stream stream) {
+                       void* out, kvc_dtype out_dtype, void* workspace, size_t workspace_bytes, kvc_stream stream,
+                       const float* k_scale = nullptr, const float* v_scale = nullptr) {
+  const bool fp8 = k_scale != nullptr;
   if (!dtype_ok(dtype) || !dtype_ok(out_dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype");
+  if (fp8 && dtype != KVC_BF16) return fail(KVC_ERR_UNSUPPORTED, "FP8 decode takes bf16 queries");
+  if (fp8 && head_dim == 32) return fail(KVC_ERR_UNSUPPORTED, "FP8 decode head_dim 32 (supported: 64, 128, 256)");
+  if (fp8 && (v_scale == nullptr || !aligned16(k_scale) || !aligned16(v_scale)))
+    return fail(KVC_ERR_INVALID_ARG, "k_scale and v_scale must be non-NULL and 16-byte aligned");
   kvc_status s = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq);
   if (s != KVC_OK) return s;
   if (num_blocks < 1) return fail(KVC_ERR_INVALID_ARG, "num_blocks must be >= 1");
@@ -179,9 +194,11 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
 
   DeviceInfo* dev = nullptr;
   if ((s = current_device(&dev)) != KVC_OK) return s;
-  const int elt = static_cast<int>(dtype_size(dtype));
+  const int q_elt = static_cast<int>(dtype_size(dtype));
+  const int elt = fp8 ? 1 : q_elt;
   GqaPlan pl;
-  if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, elt, dev->max_smem_optin, &pl)) != KVC_OK)
+  if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, elt, q_elt, fp8 ? 4 : 0,
+                     dev->max_smem_optin, &pl)) != KVC_OK)
     return s;
 
   GqaParams p{};
@@ -205,10 +222,12 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   p.out_dtype = static_cast<int>(out_dtype);
   p.stages = pl.stages;
   p.window = window;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
 
   int occ = 1;
-  if ((s = occupancy_for(dtype, p, head_dim, pl, &occ)) != KVC_OK) return s;
+  if ((s = occupancy_for(fp8 ? -1 : static_cast<int>(dtype), p, head_dim, pl, &occ)) != KVC_OK) return s;
   int64_t G = plan_ctas(dev, occ, pl.units, max_blocks_per_seq);
   const size_t cbytes = counter_bytes(batch, n_kv_heads, pl);
   G = std::min<int64_t>(G, workspace_bytes > cbytes
@@ -232,6 +251,11 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   if (num_blocks * n_kv_heads >= (1ll << 31))
     return fail(KVC_ERR_UNSUPPORTED, "num_blocks x n_kv_heads must be below 2^31");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (fp8) {
+    s = gqa_dispatch_fp8(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr);
+    if (s != KVC_OK) return s;
+    return finish_call(st);
+  }
   switch (dtype) {
     case KVC_F32: s = gqa_dispatch<float>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr); break;
     case KVC_F16: s = gqa_dispatch<__half>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr); break;
@@ -255,6 +279,19 @@ kvc_status kvc_decode_attention(const void* q, const void* k_cache, const void* 
   return kvc::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale, n_q_heads,
                           n_kv_heads, head_dim, block_size, num_blocks, 0, dtype, out, out_dtype, workspace,
                           workspace_bytes, stream);
+}
+
+kvc_status kvc_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                                    const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int batch, float scale, int n_q_heads,
+                                    int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, void* out,
+                                    kvc_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                    kvc_stream stream) {
+  kvc::clear_error();
+  if (k_scale == nullptr || v_scale == nullptr) return kvc::fail(KVC_ERR_INVALID_ARG, "k_scale / v_scale is NULL");
+  return kvc::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale, n_q_heads,
+                          n_kv_heads, head_dim, block_size, num_blocks, 0, KVC_BF16, out, out_dtype, workspace,
+                          workspace_bytes, stream, k_scale, v_scale);
 }
 
 kvc_status kvc_decode_attention_window(const void* q, const void* k_cache, const void* v_cache,
@@ -339,8 +376,9 @@ kvc_status kvc_decode_attention_static(const void* q, const void* k_cache, const
   DeviceInfo* dev = nullptr;
   if ((s = current_device(&dev)) != KVC_OK) return s;
   GqaPlan pl;
-  if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, static_cast<int>(dtype_size(dtype)),
-                     dev->max_smem_optin, &pl)) != KVC_OK)
+  const int elt_s = static_cast<int>(dtype_size(dtype));
+  if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, elt_s, elt_s, 0, dev->max_smem_optin, &pl)) !=
+      KVC_OK)
     return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(scratch, 0, counter_bytes(batch, n_kv_heads, pl), st);

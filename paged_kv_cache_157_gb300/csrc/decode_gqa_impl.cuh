@@ -201,13 +201,17 @@ __device__ __forceinline__ float select_head(const float (&v)[GW], int h) {
   return r;
 }
 
-// VD consecutive elements of T as raw 32-bit words.
+// VD consecutive elements of T (VD even) as raw words; pair(i) returns
+// elements 2i and 2i+1 as fp32.
 template <typename T, int VD>
 struct VRow {
-  static constexpr int NW = (VD * static_cast<int>(sizeof(T)) + 3) / 4;
+  static constexpr int BYTES = VD * static_cast<int>(sizeof(T));
+  static constexpr int NW = (BYTES + 3) / 4;
   uint32_t w[NW];
   __device__ __forceinline__ void load(const T* p) {
-    if constexpr (NW == 1) {
+    if constexpr (BYTES == 2) {
+      w[0] = *reinterpret_cast<const unsigned short*>(p);
+    } else if constexpr (NW == 1) {
       w[0] = *reinterpret_cast<const uint32_t*>(p);
     } else if constexpr (NW == 2) {
       const uint2 u = *reinterpret_cast<const uint2*>(p);
@@ -224,22 +228,25 @@ struct VRow {
       }
     }
   }
-  __device__ __forceinline__ float get(int d) const {
+  __device__ __forceinline__ float2 pair(int i) const {
     if constexpr (sizeof(T) == 4) {
-      return __uint_as_float(w[d]);
+      return make_float2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
+    } else if constexpr (sizeof(T) == 2) {
+      return make_float2(Elem<T>::half_to_float(w[i], 0), Elem<T>::half_to_float(w[i], 1));
     } else {
-      const uint32_t x = w[d / 2];
-      return Elem<T>::half_to_float(x, d & 1);
+      return fp8x2_to_float2(w[i >> 1] >> (16 * (i & 1)));
     }
   }
 };
 
 // One 16-row tile of a page: scores, online softmax, V accumulation.
 // sp is this warp's [GW][16] fp32 weight buffer.
-// PARTIAL tiles attend only rows [lo_valid, valid) of the 16.
+// PARTIAL tiles attend only rows [lo_valid, valid) of the 16. For FP8
+// caches vsp holds the tile's 16 per-token V scales: they multiply the
+// weights that feed the V accumulation (the sum l keeps the unscaled ones).
 template <typename T, int D, int GW, bool PARTIAL>
-__device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __restrict__ vp, float* sp, int lo_valid,
-                                         int valid,
+__device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __restrict__ vp, float* sp,
+                                         const float* __restrict__ vsp, int lo_valid, int valid,
                                          WarpState<T, D, GW>& st, const LaneGeo<T, D, GW>& g) {
   using C = GqaCfg<T, D, GW>;
   float sc[C::NS][C::NVF];
@@ -316,6 +323,7 @@ __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __re
       const float pv = fast_exp2(sc[set][k] - m_l);
       st.l += pv;
       sc[set][k] = pv;
+      if constexpr (sizeof(T) == 1) sc[set][k] = pv * vsp[g.prow[k] + set];
     }
   }
   if constexpr (C::NVF == 1 && C::NS == 2) {
@@ -355,15 +363,20 @@ __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __re
     const bool za = PARTIAL && (2 * k >= valid || 2 * k < lo_valid);
     const bool zb = PARTIAL && (2 * k + 1 >= valid || 2 * k + 1 < lo_valid);
 #pragma unroll
-    for (int d = 0; d < C::VD; ++d) {
-      float2 v = make_float2(va.get(d), vb.get(d));
-      if (PARTIAL) {
-        // rows past the context may hold anything (even NaN): their weight is 0
-        if (za) v.x = 0.f;
-        if (zb) v.y = 0.f;
-      }
+    for (int dp = 0; dp < C::VD / 2; ++dp) {
+      const float2 a = va.pair(dp), b = vb.pair(dp);
 #pragma unroll
-      for (int h = 0; h < GW; ++h) st.o[h][d] = ffma2(pp[h], v, st.o[h][d]);
+      for (int e = 0; e < 2; ++e) {
+        const int d = 2 * dp + e;
+        float2 v = e == 0 ? make_float2(a.x, b.x) : make_float2(a.y, b.y);
+        if (PARTIAL) {
+          // rows outside the attended range may hold anything (even NaN): their weight is 0
+          if (za) v.x = 0.f;
+          if (zb) v.y = 0.f;
+        }
+#pragma unroll
+        for (int h = 0; h < GW; ++h) st.o[h][d] = ffma2(pp[h], v, st.o[h][d]);
+      }
     }
   }
 }
@@ -522,7 +535,7 @@ __device__ __forceinline__ unsigned int atomic_add_acq_rel_cta_smem(unsigned int
   return old;
 }
 
-template <typename T, int D, int GH>
+template <typename T, int D, int GH, typename TQ>
 __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kernel(const GqaParams p) {
   constexpr int HW = gqa_warps_per_kvhead(GH);  // warps per kv head
   constexpr int GW = GH / HW;                    // query heads per warp
@@ -533,8 +546,10 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   static_assert(D % 32 == 0, "merge lanes own D / 32 dims");
   extern __shared__ __align__(128) unsigned char smem[];
   const int hc = p.hc;
-  const GqaSmem L = gqa_smem_layout(sizeof(T), D, GH, p.block_size, hc, p.stages, p.batch);
-  T* s_stage = reinterpret_cast<T*>(smem + L.stage_off);
+  constexpr bool kFp8 = sizeof(T) == 1;
+  constexpr int VSB = kFp8 ? 4 : 0;  // V-scale bytes per cached row
+  const GqaSmem L = gqa_smem_layout(sizeof(T), sizeof(TQ), VSB, D, GH, p.block_size, hc, p.stages, p.batch);
+  unsigned char* s_stage = smem + L.stage_off;
   uint64_t* fbar = reinterpret_cast<uint64_t*>(smem + L.bar_off);  // [S] full
   unsigned int* s_rel = reinterpret_cast<unsigned int*>(smem + L.rel_off);  // [S] releases seen
   unsigned int* s_iss = s_rel + p.stages;  // [S] fills issued
@@ -552,11 +567,15 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   const int tiles_per_page = bs / 16;
   const int page_elems = bs * D;
   const int chunk_elems = hc * page_elems;
-  const int stage_elems = 2 * chunk_elems + hc * GH * D;  // K chunk, V chunk, the unit's query rows
+  // stage: [K chunk][V chunk][the unit's query rows (TQ)][FP8: the chunk's V scales]
+  const uint32_t page_bytes = static_cast<uint32_t>(page_elems * sizeof(T));
   const uint32_t chunk_bytes = static_cast<uint32_t>(chunk_elems * sizeof(T));
+  const uint32_t q_bytes = static_cast<uint32_t>(hc * GH * D * sizeof(TQ));
+  const uint32_t vs_bytes = static_cast<uint32_t>(hc * bs * VSB);
+  const size_t stage_bytes = align_up(2 * chunk_bytes + q_bytes + vs_bytes, 16);
   const T* kc = static_cast<const T*>(p.k_cache);
   const T* vc = static_cast<const T*>(p.v_cache);
-  const T* qg = static_cast<const T*>(p.q);
+  const TQ* qg = static_cast<const TQ*>(p.q);
   const uint32_t full = 0xffffffffu;
   const int HN = p.n_chunks * p.n_hsub;
   const bool q_contig = (GH == p.group);  // the chunk's query rows are one contiguous run
@@ -628,8 +647,8 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   const int total = static_cast<int>(hi - lo);  // positions of this CTA
   if (total <= 0) return;                       // uniform over the CTA
 
-  T* my_k = s_stage + kh * page_elems;                       // + slot * stage_elems
-  T* my_v = s_stage + chunk_elems + kh * page_elems;
+  unsigned char* my_k = s_stage + kh * page_bytes;  // + slot * stage_bytes
+  unsigned char* my_v = s_stage + chunk_bytes + kh * page_bytes;
   float* wp = reinterpret_cast<float*>(smem + L.p_off) + w * GW * 16;  // this warp's weights
   const uint64_t pol = policy_evict_first();
 
@@ -653,28 +672,30 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   };
   // Copies of one position into stage `slot` (one thread).
   auto issue = [&](int slot, int src, int qoff) {
-    const uint32_t q_bytes = static_cast<uint32_t>(hc * GH * D * sizeof(T));
-    const uint32_t bytes = (src >= 0 ? 2 * chunk_bytes : 0u) + (qoff >= 0 ? q_bytes : 0u);
+    const uint32_t bytes = (src >= 0 ? 2 * chunk_bytes + vs_bytes : 0u) + (qoff >= 0 ? q_bytes : 0u);
     if (src < 0) set_flag(p.err, 0x1u);
     atomicAdd(s_iss + slot, 1u);
     if (bytes == 0) {
       mbar_arrive(fbar + slot);
       return;
     }
-    T* dst = s_stage + static_cast<size_t>(slot) * stage_elems;
+    unsigned char* dst = s_stage + static_cast<size_t>(slot) * stage_bytes;
     mbar_arrive_expect_tx(fbar + slot, bytes);
     if (src >= 0) {
       const int64_t e = static_cast<int64_t>(src) * page_elems;
       bulk_g2s(dst, kc + e, chunk_bytes, fbar + slot, pol);
-      bulk_g2s(dst + chunk_elems, vc + e, chunk_bytes, fbar + slot, pol);
+      bulk_g2s(dst + chunk_bytes, vc + e, chunk_bytes, fbar + slot, pol);
+      if constexpr (kFp8)  // the V scales of the chunk's rows: [hc heads][bs rows]
+        bulk_g2s(dst + 2 * chunk_bytes + q_bytes, p.v_scale + static_cast<int64_t>(src) * bs, vs_bytes, fbar + slot,
+                 pol);
     }
     if (qoff >= 0) {
       if (q_contig) {
-        bulk_g2s(dst + 2 * chunk_elems, qg + qoff, q_bytes, fbar + slot, pol);
+        bulk_g2s(dst + 2 * chunk_bytes, qg + qoff, q_bytes, fbar + slot, pol);
       } else {
-        const uint32_t rb = static_cast<uint32_t>(GH * D * sizeof(T));
+        const uint32_t rb = static_cast<uint32_t>(GH * D * sizeof(TQ));
         for (int h = 0; h < hc; ++h)
-          bulk_g2s(dst + 2 * chunk_elems + h * GH * D, qg + qoff + h * p.group * D, rb, fbar + slot, pol);
+          bulk_g2s(dst + 2 * chunk_bytes + h * rb, qg + qoff + h * p.group * D, rb, fbar + slot, pol);
       }
     }
   };
@@ -739,19 +760,43 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
           aborted = true;
           break;
         }
-        const T* stg = s_stage + static_cast<size_t>(slot) * stage_elems;
+        const unsigned char* stg = s_stage + static_cast<size_t>(slot) * stage_bytes;
         if (t == 0) {
           // The unit's query rows came with its first position. Register slot
-          // h holds head h ^ mh (the lane's reduction order).
-          const T* qs = stg + 2 * chunk_elems + (kh * GH + hw * GW) * D + (geo.kofs[0] % D);
+          // h holds head h ^ mh (the lane's reduction order); the lane's dims
+          // are C::VEC-element runs at (dq + DL * j) * C::VEC. FP8 caches fold
+          // the per-channel K scales into the query.
+          const int d0 = geo.kofs[0] % D;  // first dim of the lane's first run
+          const TQ* qs = reinterpret_cast<const TQ*>(stg + 2 * chunk_bytes) + (kh * GH + hw * GW) * D + d0;
+          constexpr int QV = Elem<TQ>::kVec;  // query elements per 16-byte load
+          float ksc[C::DPL];
+#pragma unroll
+          for (int i = 0; i < C::DPL; ++i) ksc[i] = p.qscale;
+          if constexpr (kFp8) {
+            const float* ks = p.k_scale + static_cast<int64_t>(sg.chunk * hc + kh) * D + d0;
+#pragma unroll
+            for (int j = 0; j < C::NCH; ++j) {
+#pragma unroll
+              for (int e = 0; e < C::VEC; e += 4) {
+                const float4 k4 = __ldg(reinterpret_cast<const float4*>(ks + C::DL * j * C::VEC + e));
+                ksc[j * C::VEC + e] *= k4.x;
+                ksc[j * C::VEC + e + 1] *= k4.y;
+                ksc[j * C::VEC + e + 2] *= k4.z;
+                ksc[j * C::VEC + e + 3] *= k4.w;
+              }
+            }
+          }
 #pragma unroll
           for (int h = 0; h < GW; ++h) {
             float f[C::DPL];
-            const T* qh = qs + (h ^ geo.mh) * D;
+            const TQ* qh = qs + (h ^ geo.mh) * D;
 #pragma unroll
-            for (int j = 0; j < C::NCH; ++j) Elem<T>::unpack(lds128(qh + C::DL * j * C::VEC), f + j * C::VEC);
+            for (int j = 0; j < C::NCH; ++j) {
 #pragma unroll
-            for (int i = 0; i < C::DP2; ++i) st.q[h][i] = make_float2(f[2 * i] * p.qscale, f[2 * i + 1] * p.qscale);
+              for (int e = 0; e < C::VEC; e += QV) Elem<TQ>::unpack(lds128(qh + C::DL * j * C::VEC + e), f + j * C::VEC + e);
+            }
+#pragma unroll
+            for (int i = 0; i < C::DP2; ++i) st.q[h][i] = make_float2(f[2 * i] * ksc[2 * i], f[2 * i + 1] * ksc[2 * i + 1]);
 #pragma unroll
             for (int d = 0; d < C::VD; ++d) st.o[h][d] = make_float2(0.f, 0.f);
             st.m[h] = kNegInf;
@@ -759,23 +804,25 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
           st.l = 0.f;
         }
         if (src >= 0) {
-          const T* kp = my_k + static_cast<size_t>(slot) * stage_elems;
-          const T* vp = my_v + static_cast<size_t>(slot) * stage_elems;
+          const T* kp = reinterpret_cast<const T*>(my_k + static_cast<size_t>(slot) * stage_bytes);
+          const T* vp = reinterpret_cast<const T*>(my_v + static_cast<size_t>(slot) * stage_bytes);
+          const float* vsp = reinterpret_cast<const float*>(stg + 2 * chunk_bytes + q_bytes) + kh * bs;
           const int jb = j0 + sg.j + t;                          // table index of this block
           const int vr = min(bs, n_rows - jb * bs);              // rows of the block before the end
           const int lr = (jb == j0) ? r0 - j0 * bs : 0;          // rows of the block before the window
           if (vr >= bs && lr == 0) {
             for (int tt = 0; tt < tiles_per_page; ++tt)
-              gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, 0, 16, st, geo);
+              gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, vsp + tt * 16, 0, 16, st, geo);
           } else {
             for (int tt = 0; tt < tiles_per_page; ++tt) {
               const int valid = vr - tt * 16, lo_valid = lr - tt * 16;
               if (valid <= 0) break;
               if (lo_valid >= 16) continue;
               if (valid >= 16 && lo_valid <= 0)
-                gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, 0, 16, st, geo);
+                gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, vsp + tt * 16, 0, 16, st, geo);
               else
-                gqa_tile<T, D, GW, true>(kp + tt * 16 * D, vp + tt * 16 * D, wp, lo_valid, valid, st, geo);
+                gqa_tile<T, D, GW, true>(kp + tt * 16 * D, vp + tt * 16 * D, wp, vsp + tt * 16, lo_valid, valid, st,
+                                         geo);
             }
           }
         }

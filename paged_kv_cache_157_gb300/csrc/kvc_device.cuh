@@ -84,6 +84,38 @@ template <> struct Elem<__half> {
   }
 };
 
+// FP8 e4m3 cache element (1 byte; no infinities, largest finite 448).
+struct fp8e4m3 {
+  unsigned char bits;
+};
+
+// Two e4m3 values (low byte first) as an fp32 pair, through the hardware
+// e4m3x2 -> f16x2 conversion (exact: every e4m3 value is an f16 value).
+__device__ __forceinline__ float2 fp8x2_to_float2(uint32_t two) {
+  uint32_t h2;
+  const unsigned short in = static_cast<unsigned short>(two & 0xffffu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return __half22float2(*reinterpret_cast<__half2*>(&h2));
+}
+
+// Rounds two fp32 values to e4m3 (nearest, ties to even, saturating at +-448;
+// NaN stays NaN); returns them packed, a in the low byte.
+__device__ __forceinline__ unsigned short float2_to_fp8x2(float a, float b) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+template <> struct Elem<fp8e4m3> {
+  static constexpr int kVec = 16;
+  // Elements 2c and 2c+1 of a 16-byte chunk (c in [0, 8)) as an fp32 pair.
+  __device__ __forceinline__ static float2 pair(const uint4& u, int c) {
+    const int wi = c >> 1;
+    const uint32_t w = wi == 0 ? u.x : (wi == 1 ? u.y : (wi == 2 ? u.z : u.w));
+    return fp8x2_to_float2((c & 1) ? (w >> 16) : w);
+  }
+};
+
 // Stores one fp32 value as the output dtype (0 f32, 1 f16, 2 bf16).
 __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int out_dtype) {
   if (out_dtype == 0) {
