@@ -94,7 +94,8 @@ __host__ __device__ inline GqaSmem gqa_smem_layout(int elt_bytes, int q_bytes, i
   return s;
 }
 
-template <typename T>
+// WIN: kernels with the sliding window compiled in (p.window > 0).
+template <typename T, bool WIN>
 kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
                         int* occ);
 // FP8 e4m3 caches with bf16 queries (head_dim 64, 128 or 256).

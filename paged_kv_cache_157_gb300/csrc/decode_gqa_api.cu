@@ -121,7 +121,8 @@ kvc_status check_shapes(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
 
 template <typename T>
 kvc_status occupancy(const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
-  return gqa_dispatch<T>(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ);
+  return p.window > 0 ? gqa_dispatch<T, true>(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ)
+                      : gqa_dispatch<T, false>(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ);
 }
 
 // dt < 0: FP8 caches with bf16 queries
@@ -256,10 +257,20 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
     if (s != KVC_OK) return s;
     return finish_call(st);
   }
+  const bool win = window > 0;
   switch (dtype) {
-    case KVC_F32: s = gqa_dispatch<float>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr); break;
-    case KVC_F16: s = gqa_dispatch<__half>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr); break;
-    case KVC_BF16: s = gqa_dispatch<__nv_bfloat16>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr); break;
+    case KVC_F32:
+      s = win ? gqa_dispatch<float, true>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr)
+              : gqa_dispatch<float, false>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr);
+      break;
+    case KVC_F16:
+      s = win ? gqa_dispatch<__half, true>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr)
+              : gqa_dispatch<__half, false>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr);
+      break;
+    case KVC_BF16:
+      s = win ? gqa_dispatch<__nv_bfloat16, true>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr)
+              : gqa_dispatch<__nv_bfloat16, false>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr);
+      break;
   }
   if (s != KVC_OK) return s;
   return finish_call(st);

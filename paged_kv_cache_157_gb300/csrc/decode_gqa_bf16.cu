@@ -2,5 +2,6 @@
 #include "decode_gqa_launch.cuh"
 
 namespace kvc {
-template kvc_status gqa_dispatch<__nv_bfloat16>(const GqaParams&, int, int, int, size_t, cudaStream_t, int, int*);
+template kvc_status gqa_dispatch<__nv_bfloat16, false>(const GqaParams&, int, int, int, size_t, cudaStream_t, int,
+                                                         int*);
 }  // namespace kvc

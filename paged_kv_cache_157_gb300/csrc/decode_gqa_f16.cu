@@ -2,5 +2,6 @@
 #include "decode_gqa_launch.cuh"
 
 namespace kvc {
-template kvc_status gqa_dispatch<__half>(const GqaParams&, int, int, int, size_t, cudaStream_t, int, int*);
+template kvc_status gqa_dispatch<__half, false>(const GqaParams&, int, int, int, size_t, cudaStream_t, int,
+                                                         int*);
 }  // namespace kvc

@@ -1,0 +1,7 @@
+// Explicit instantiation of the sliding-window GQA decode kernels for float storage.
+#include "decode_gqa_launch.cuh"
+
+namespace kvc {
+template kvc_status gqa_dispatch<float, true>(const GqaParams&, int, int, int, size_t, cudaStream_t, int,
+                                                         int*);
+}  // namespace kvc

@@ -7,9 +7,9 @@ namespace kvc {
 kvc_status gqa_dispatch_fp8(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
                             int* occ) {
   switch (D) {
-    case 64: return gqa_run_gh<fp8e4m3, 64, __nv_bfloat16>(p, GH, grid, smem, stream, mode, occ);
-    case 128: return gqa_run_gh<fp8e4m3, 128, __nv_bfloat16>(p, GH, grid, smem, stream, mode, occ);
-    case 256: return gqa_run_gh<fp8e4m3, 256, __nv_bfloat16>(p, GH, grid, smem, stream, mode, occ);
+    case 64: return gqa_run_gh<fp8e4m3, 64, __nv_bfloat16, false>(p, GH, grid, smem, stream, mode, occ);
+    case 128: return gqa_run_gh<fp8e4m3, 128, __nv_bfloat16, false>(p, GH, grid, smem, stream, mode, occ);
+    case 256: return gqa_run_gh<fp8e4m3, 256, __nv_bfloat16, false>(p, GH, grid, smem, stream, mode, occ);
   }
   return fail(KVC_ERR_UNSUPPORTED, "FP8 decode head_dim %d (supported: 64, 128, 256)", D);
 }

@@ -535,7 +535,9 @@ __device__ __forceinline__ unsigned int atomic_add_acq_rel_cta_smem(unsigned int
   return old;
 }
 
-template <typename T, int D, int GH, typename TQ>
+// WIN: the sliding window is compiled in only where it is used, so the
+// full-attention kernel keeps no per-block window bookkeeping.
+template <typename T, int D, int GH, typename TQ, bool WIN>
 __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kernel(const GqaParams p) {
   constexpr int HW = gqa_warps_per_kvhead(GH);  // warps per kv head
   constexpr int GW = GH / HW;                    // query heads per warp
@@ -547,6 +549,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   extern __shared__ __align__(128) unsigned char smem[];
   const int hc = p.hc;
   constexpr bool kFp8 = sizeof(T) == 1;
+  const int wnd = WIN ? p.window : 0;  // sliding window rows (0: all)
   constexpr int VSB = kFp8 ? 4 : 0;  // V-scale bytes per cached row
   const GqaSmem L = gqa_smem_layout(sizeof(T), sizeof(TQ), VSB, D, GH, p.block_size, hc, p.stages, p.batch);
   unsigned char* s_stage = smem + L.stage_off;
@@ -601,7 +604,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     const int j = static_cast<int>((pos - seq * per_seq) % p.max_blocks) + tid * 32;
     if (seq < B && j < p.max_blocks) prefetch_l2(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks + j);
   }
-  scan_blocks(p.context_lens, B, bs, p.max_blocks, p.window, s_scan);  // ends with a CTA barrier
+  scan_blocks(p.context_lens, B, bs, p.max_blocks, wnd, s_scan);  // ends with a CTA barrier
   const int64_t N = static_cast<int64_t>(HN) * s_scan[B];
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
@@ -663,7 +666,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     if (pos < hi) {
       const BlockPos bp = locate_block(pos, HN, s_scan, B, p.n_hsub);
       // bp.j counts the sequence's visible blocks; the table is indexed from block 0
-      const int j0 = first_row(seq_rows(p.context_lens, bp.seq, bs, p.max_blocks), p.window) / bs;
+      const int j0 = first_row(seq_rows(p.context_lens, bp.seq, bs, p.max_blocks), wnd) / bs;
       const int phys = __ldg(p.block_tables + static_cast<int64_t>(bp.seq) * p.max_blocks + j0 + bp.j);
       if (phys >= 0 && phys < p.num_blocks) src = phys * p.n_kv_heads + bp.chunk * hc;
       if (pos == lo || bp.j == 0)
@@ -733,7 +736,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
       const BlockPos sg = locate_block(gb, HN, s_scan, B, p.n_hsub);
       const int seg_len = static_cast<int>(((sg.nb - sg.j) < (hi - gb)) ? (sg.nb - sg.j) : (hi - gb));
       const int n_rows = seq_rows(p.context_lens, sg.seq, bs, p.max_blocks);
-      const int r0 = first_row(n_rows, p.window);  // first visible row
+      const int r0 = first_row(n_rows, wnd);  // first visible row
       const int j0 = r0 / bs;                      // table index of the first visible block
       const int hq0 = (sg.chunk * hc + kh) * p.group + sg.hsub * GH + hw * GW;  // first query head of this warp
 
