@@ -160,5 +160,25 @@ def paged_decode_window(q, k_cache, v_cache, block_tables, context_lens, scale, 
     return paged_decode_window_lse(q, k_cache, v_cache, block_tables, context_lens, scale, window)[0]
 
 
+def paged_decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale):
+    """Several new query tokens per sequence attending the paged cache causally.
+
+    q: [B, T, Hq, D]; context_lens count every cached row including the T new
+    ones (already appended). Query token t of sequence i sits at position
+    n_i - T + t and sees rows 0 .. n_i - T + t: the prefill/decode mask rule of
+    "单请求 KV Cache" (a query row i of a chunk sees columns up to past_len + i),
+    applied through the block table. Returns [B, T, Hq, D].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, T = q.shape[0], q.shape[1]
+    out = np.zeros(q.shape[:3] + (v_cache.shape[3],), dtype=np.float64)
+    lens = np.asarray(context_lens).reshape(-1)
+    if np.any(lens < T):
+        raise ValueError("every context must hold the T new rows")
+    for t in range(T):
+        out[:, t] = paged_decode(q[:, t], k_cache, v_cache, block_tables, lens - T + t + 1, scale)
+    return out
+
+
 def default_scale(head_dim: int) -> float:
     return 1.0 / math.sqrt(head_dim)
