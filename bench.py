@@ -362,6 +362,8 @@ def run_variant(kvc, name, flush, steps):
         return r
     if name == "gqa_fp8_b32_ctx4096":
         return measure_fp8(kvc, flush, steps)
+    if name == "gqa_spec4_b32_ctx4096":
+        return measure_multi(kvc, flush, steps, 4)
     if name == "cow_copy_blocks_2048":
         return measure_copy_blocks(kvc, flush, steps)
     if name == "gqa_ragged_17_31_32":
@@ -375,7 +377,8 @@ def run_variant(kvc, name, flush, steps):
 
 
 VARIANTS = ("gqa_b32_ctx4096", "mha_shared_prefix_8x8", "gqa_long_splitk", "gqa_ragged_17_31_32", "tiny_mha_fp32",
-            "mla_deepseek_v2", "gqa_window_b32_ctx4096_w1024", "cow_copy_blocks_2048", "gqa_fp8_b32_ctx4096")
+            "mla_deepseek_v2", "gqa_window_b32_ctx4096_w1024", "cow_copy_blocks_2048", "gqa_fp8_b32_ctx4096",
+            "gqa_spec4_b32_ctx4096")
 
 
 def variants(kvc, flush, steps):
@@ -438,6 +441,41 @@ def measure_fp8(kvc, flush, steps):
             "bf16_equivalent_gbps": round(bf16_equiv / dms / 1e6, 1),
             "ms_per_step": round(statistics.mean(step_ms), 5), "bytes_per_step": dec_b,
             "note": "bf16_equivalent_gbps counts the bytes the same rows take in bf16"}
+
+
+def measure_multi(kvc, flush, steps, T=4):
+    """Llama-3-8B-shaped layer verifying T speculated tokens per sequence (batch 32, lengths 4096 after the
+    append): kvc_append of the B*T new rows + kvc_decode_attention_multi (bf16). Bytes: every cached K/V row
+    once (all T tokens share each page), plus q, out, tables, lengths."""
+    import torch
+    from paged_kv_cache_157_gb300 import workloads as W
+    B, hq, hkv, D, bs = 32, 32, 8, 128, 16
+    c = W.multi_case(B, T, hq, hkv, D, bs, [4096] * B, "bf16", 95, device="cuda")
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in c.items()}
+    lens = c["context_lens"].tolist()
+    slots = kvc.slots_from_tables(c["block_tables"], bs, [i for i in range(B) for _ in range(T)],
+                                  [n - T + t for n in lens for t in range(T)]).cuda()
+    out = torch.empty((B, T, hq, D), dtype=torch.bfloat16, device="cuda")
+    ws = kvc.new_multi_workspace(B, T, hq, hkv, D, bs, c["block_tables"].shape[1])
+    scale = 1.0 / math.sqrt(D)
+    kn, vn = d["k_new"].reshape(B * T, hkv, D), d["v_new"].reshape(B * T, hkv, D)
+
+    class S:
+        def append(self):
+            kvc.append(kn, vn, slots, d["k_cache"], d["v_cache"])
+
+        def decode(self):
+            kvc.decode_attention_multi(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                                       scale, out, ws)
+
+    step_ms, dec_ms, _, _ = time_steps(S(), steps, 5, flush)
+    dec_b = sum(lens) * hkv * D * 2 * 2 + 2 * B * T * hq * D * 2 + sum(-(-n // bs) for n in lens) * 4 + B * 4
+    dms = statistics.mean(dec_ms)
+    return {"decode_ms": round(dms, 5), "decode_gbps": round(dec_b / dms / 1e6, 1),
+            "frac_of_8tbs": round(dec_b / dms / 1e6 / NOMINAL_HBM_GBS, 4),
+            "query_tokens_per_s": round(B * T / (dms / 1e3), 1),
+            "ms_per_step": round(statistics.mean(step_ms), 5), "bytes_per_step": dec_b,
+            "note": f"{T} new tokens per sequence attend causally in one pass over the pages"}
 
 
 def measure_copy_blocks(kvc, flush, steps):

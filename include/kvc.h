@@ -74,7 +74,7 @@ typedef enum kvc_dtype { KVC_F32 = 0, KVC_F16 = 1, KVC_BF16 = 2 } kvc_dtype;
 
 /* Bits of the device error word. */
 #define KVC_FLAG_BAD_BLOCK 0x1u   /* block table entry outside [0, num_blocks) */
-#define KVC_FLAG_BAD_LEN 0x2u     /* context_len < 1 or > max_blocks_per_seq*block_size */
+#define KVC_FLAG_BAD_LEN 0x2u     /* context_len < 1 (multi-token: < n_tokens) or > max_blocks_per_seq*block_size */
 #define KVC_FLAG_BAD_SLOT 0x4u    /* slot >= num_blocks*block_size */
 #define KVC_FLAG_TIMEOUT 0x8u     /* a bounded wait on an async copy gave up */
 #define KVC_FLAG_WORKSPACE 0x10u  /* decode workspace counters were not zero at entry */
@@ -211,6 +211,32 @@ kvc_status kvc_decode_attention_window(const void* q, const void* k_cache, const
                                        int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, int window,
                                        kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
                                        size_t workspace_bytes, kvc_stream stream);
+
+/* Several new query tokens per sequence (chunked prefill of a prompt
+ * continuation, or verification of n_tokens speculated tokens), attending
+ * the paged cache causally in one pass over each sequence's pages:
+ *   out[i, t, h, :] = softmax-weighted sum over rows 0 .. n_i - n_tokens + t
+ * with n_i = context_lens[i], which counts every cached row including the
+ * n_tokens new ones (append them first, e.g. with kvc_append). Token t sits
+ * at position n_i - n_tokens + t and sees itself and every earlier row.
+ * q: [batch, n_tokens, n_q_heads, head_dim] contiguous, dtype; out: the same
+ * shape in out_dtype. 1 <= n_tokens <= 256 (n_tokens 1 is
+ * kvc_decode_attention); a context with fewer than n_tokens rows is invalid
+ * (KVC_FLAG_BAD_LEN, zero outputs). Every page is read once for all
+ * n_tokens x (n_q_heads / n_kv_heads) queries of its kv head.
+ * workspace: at least kvc_decode_workspace_size(batch, n_tokens * n_q_heads,
+ * n_kv_heads, head_dim, block_size, max_blocks_per_seq) bytes; otherwise the
+ * arguments, workspace and error rules of kvc_decode_attention. F32, F16 and
+ * BF16 caches; not combined with a window or an FP8 cache.
+ * Source: the prefill/decode mask rule of "单请求 KV Cache" (query row i of a
+ * chunk sees columns up to past_len + i) applied through the block table of
+ * "KV缓存原理与显存估算" knowledge point 2. */
+kvc_status kvc_decode_attention_multi(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int batch, int n_tokens, float scale,
+                                      int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                      kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
+                                      size_t workspace_bytes, kvc_stream stream);
 
 /* FP8 KV cache decode: as kvc_decode_attention over the caches written by
  * kvc_append_fp8, attending k = e4m3value(code) * k_scale[h, d] and

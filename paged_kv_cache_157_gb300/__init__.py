@@ -63,6 +63,8 @@ SIGNATURES = {
                                            _i32, _vp, _i32, _vp]),
     "kvc_decode_attention_window": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32, _i64,
                                            _i32, _i32, _vp, _i32, _vp, _sz, _vp]),
+    "kvc_decode_attention_multi": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _i32, _i32, _i32, _i32,
+                                          _i64, _i32, _vp, _i32, _vp, _sz, _vp]),
     "kvc_decode_mla_workspace_size": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _szp]),
     "kvc_decode_attention_mla": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32, _i64, _i32, _vp,
                                         _i32, _vp, _sz, _vp]),
@@ -257,6 +259,37 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out
                                       block_tables.shape[1], _ptr(context_lens), B, float(scale), hq, hkv, d, bs, nb,
                                       _dtype_code(k_cache), _ptr(out), _dtype_code(out), ws_ptr, ws_bytes,
                                       _stream(stream)), "kvc_decode_attention")
+
+
+def new_multi_workspace(batch, n_tokens, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                        device="cuda"):
+    """Zero-filled workspace for decode_attention_multi (the decode size query with n_tokens * n_q_heads)."""
+    return new_decode_workspace(batch, n_tokens * n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                device)
+
+
+def decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace=None,
+                           stream=None):
+    """kvc_decode_attention_multi: q/out [B, T, Hq, D], the T newest rows of every sequence are its new tokens
+    (already appended; context_lens count them) and token t attends rows 0 .. n - T + t. Workspace: a
+    zero-filled uint8 tensor from new_multi_workspace, or None."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
+        _require(t, n)
+    _require(block_tables, "block_tables", torch.int32)
+    _require(context_lens, "context_lens", torch.int32)
+    B, T, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if d2 != d or tuple(out.shape) != (B, T, hq, d) or block_tables.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("shape mismatch")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        _require(workspace, "workspace")
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    _check(raw().kvc_decode_attention_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                            block_tables.shape[1], _ptr(context_lens), B, T, float(scale), hq, hkv,
+                                            d, bs, nb, _dtype_code(k_cache), _ptr(out), _dtype_code(out), ws_ptr,
+                                            ws_bytes, _stream(stream)), "kvc_decode_attention_multi")
 
 
 def decode_attention_static(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None):

@@ -27,9 +27,9 @@ SOURCES = [
     "decode_gqa_f32.cu",
     "decode_gqa_f16.cu",
     "decode_gqa_bf16.cu",
-    "decode_gqa_f32_win.cu",
-    "decode_gqa_f16_win.cu",
-    "decode_gqa_bf16_win.cu",
+    "decode_gqa_f32_ext.cu",
+    "decode_gqa_f16_ext.cu",
+    "decode_gqa_bf16_ext.cu",
     "decode_gqa_fp8.cu",
     "decode_mla.cu",
     "pool.cpp",

@@ -36,6 +36,7 @@ struct GqaParams {
   int stages;
   int unit_mode;  // 1: CTA u handles unit u completely (no records)
   int window;     // sliding window: attend the newest `window` rows (0: all rows)
+  int n_tok;      // new query tokens per sequence (q and out are [batch, n_tok, n_q_heads, D])
   const float* k_scale;  // FP8 caches: per-channel K scales [n_kv_heads, head_dim]
   const float* v_scale;  // FP8 caches: per-token V scales [num_blocks, n_kv_heads, block_size]
   float qscale;   // scale * log2(e)
@@ -94,8 +95,8 @@ __host__ __device__ inline GqaSmem gqa_smem_layout(int elt_bytes, int q_bytes, i
   return s;
 }
 
-// WIN: kernels with the sliding window compiled in (p.window > 0).
-template <typename T, bool WIN>
+// EXT: kernels with the extensions compiled in (p.window > 0 or p.n_tok > 1).
+template <typename T, bool EXT>
 kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
                         int* occ);
 // FP8 e4m3 caches with bf16 queries (head_dim 64, 128 or 256).

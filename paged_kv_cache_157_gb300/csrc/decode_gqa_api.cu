@@ -20,6 +20,7 @@ constexpr size_t kStageBudget = (228 * 1024) / kGqaCtasPerSm - 1024;
 constexpr int kMaxCtasPerSm = 4;
 constexpr int kMinBlocksPerCta = 2 * kGqaWarps;
 constexpr int kMaxBatch = 4096;
+constexpr int kMaxTokens = 256;  // new tokens per sequence in one multi-token call
 
 struct GqaPlan {
   int GH = 1, n_hsub = 1, stages = 2, hc = 1, n_chunks = 1;
@@ -45,10 +46,11 @@ int head_subgroup(int group) {
 }
 
 // elt: cache element bytes; q_elt: query element bytes; vsb: V-scale bytes
-// per cached row (4 for FP8 caches, else 0).
+// per cached row (4 for FP8 caches, else 0). n_tok new tokens per sequence
+// give each kv head n_tok * group (virtual) query heads that share its pages.
 kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, int elt, int q_elt, int vsb, int max_smem,
-                     GqaPlan* pl) {
-  const int group = n_q_heads / n_kv_heads;
+                     GqaPlan* pl, int n_tok = 1) {
+  const int group = n_tok * (n_q_heads / n_kv_heads);
   pl->GH = head_subgroup(group);
   pl->n_hsub = group / pl->GH;
   // kv heads per CTA: the largest power of two the CTA's warps can hold that
@@ -119,10 +121,13 @@ kvc_status check_shapes(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
   return KVC_OK;
 }
 
+// The extension kernels serve a sliding window or several new tokens.
+bool uses_ext(const GqaParams& p) { return p.window > 0 || p.n_tok > 1; }
+
 template <typename T>
 kvc_status occupancy(const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
-  return p.window > 0 ? gqa_dispatch<T, true>(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ)
-                      : gqa_dispatch<T, false>(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ);
+  return uses_ext(p) ? gqa_dispatch<T, true>(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ)
+                     : gqa_dispatch<T, false>(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ);
 }
 
 // dt < 0: FP8 caches with bf16 queries
@@ -168,13 +173,18 @@ namespace {
 
 // Decode over the newest `window` rows of every sequence (window 0: all rows).
 // k_scale / v_scale non-NULL: FP8 e4m3 caches with bf16 queries (dtype is
-// then the query dtype and must be BF16).
+// then the query dtype and must be BF16). n_tok > 1: that many new tokens per
+// sequence, q and out [batch, n_tok, n_q_heads, head_dim], causal among them.
 kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                        int max_blocks_per_seq, const int32_t* context_lens, int batch, float scale, int n_q_heads,
                        int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, int window, kvc_dtype dtype,
                        void* out, kvc_dtype out_dtype, void* workspace, size_t workspace_bytes, kvc_stream stream,
-                       const float* k_scale = nullptr, const float* v_scale = nullptr) {
+                       const float* k_scale = nullptr, const float* v_scale = nullptr, int n_tok = 1) {
   const bool fp8 = k_scale != nullptr;
+  if (n_tok < 1 || n_tok > kMaxTokens)
+    return fail(KVC_ERR_INVALID_ARG, "n_tokens %d (supported: 1 to %d)", n_tok, kMaxTokens);
+  if (n_tok > 1 && (fp8 || window > 0))
+    return fail(KVC_ERR_UNSUPPORTED, "several new tokens with an FP8 cache or a sliding window");
   if (!dtype_ok(dtype) || !dtype_ok(out_dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype");
   if (fp8 && dtype != KVC_BF16) return fail(KVC_ERR_UNSUPPORTED, "FP8 decode takes bf16 queries");
   if (fp8 && head_dim == 32) return fail(KVC_ERR_UNSUPPORTED, "FP8 decode head_dim 32 (supported: 64, 128, 256)");
@@ -182,6 +192,8 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
     return fail(KVC_ERR_INVALID_ARG, "k_scale and v_scale must be non-NULL and 16-byte aligned");
   kvc_status s = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq);
   if (s != KVC_OK) return s;
+  if (static_cast<int64_t>(batch) * n_tok * n_q_heads * head_dim >= (1ll << 31))
+    return fail(KVC_ERR_UNSUPPORTED, "batch x n_tokens x n_q_heads x head_dim must be below 2^31");
   if (num_blocks < 1) return fail(KVC_ERR_INVALID_ARG, "num_blocks must be >= 1");
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_tables == nullptr || context_lens == nullptr ||
       out == nullptr)
@@ -199,7 +211,7 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   const int elt = fp8 ? 1 : q_elt;
   GqaPlan pl;
   if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, elt, q_elt, fp8 ? 4 : 0,
-                     dev->max_smem_optin, &pl)) != KVC_OK)
+                     dev->max_smem_optin, &pl, n_tok)) != KVC_OK)
     return s;
 
   GqaParams p{};
@@ -223,6 +235,7 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   p.out_dtype = static_cast<int>(out_dtype);
   p.stages = pl.stages;
   p.window = window;
+  p.n_tok = n_tok;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
@@ -257,7 +270,7 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
     if (s != KVC_OK) return s;
     return finish_call(st);
   }
-  const bool win = window > 0;
+  const bool win = uses_ext(p);
   switch (dtype) {
     case KVC_F32:
       s = win ? gqa_dispatch<float, true>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr)
@@ -316,6 +329,18 @@ kvc_status kvc_decode_attention_window(const void* q, const void* k_cache, const
   return kvc::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale, n_q_heads,
                           n_kv_heads, head_dim, block_size, num_blocks, window, dtype, out, out_dtype, workspace,
                           workspace_bytes, stream);
+}
+
+kvc_status kvc_decode_attention_multi(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int batch, int n_tokens, float scale,
+                                      int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                      kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
+                                      size_t workspace_bytes, kvc_stream stream) {
+  kvc::clear_error();
+  return kvc::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale, n_q_heads,
+                          n_kv_heads, head_dim, block_size, num_blocks, 0, dtype, out, out_dtype, workspace,
+                          workspace_bytes, stream, nullptr, nullptr, n_tokens);
 }
 
 }  // extern "C"

@@ -1,4 +1,5 @@
-// Explicit instantiation of the sliding-window GQA decode kernels for __nv_bfloat16 storage.
+// Explicit instantiation of the GQA decode kernels with the extensions
+// (sliding window, several new tokens per sequence) for __nv_bfloat16 storage.
 #include "decode_gqa_launch.cuh"
 
 namespace kvc {

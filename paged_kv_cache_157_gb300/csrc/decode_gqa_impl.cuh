@@ -70,10 +70,10 @@ struct GqaCfg {
 };
 
 // Rows of sequence b that are cached (capped by the table width; 0 if its
-// length is invalid).
-__device__ __forceinline__ int seq_rows(const int32_t* lens, int b, int bs, int max_blocks) {
+// length is invalid, i.e. below min_len: 1, or the number of new query tokens).
+__device__ __forceinline__ int seq_rows(const int32_t* lens, int b, int bs, int max_blocks, int min_len = 1) {
   const int n = __ldg(lens + b);
-  if (n < 1) return 0;
+  if (n < min_len || n < 1) return 0;
   const int cap = bs * max_blocks;
   return n < cap ? n : cap;
 }
@@ -86,20 +86,22 @@ __device__ __forceinline__ int first_row(int rows, int window) {
 
 // Number of cache blocks sequence b contributes: the blocks holding visible
 // rows (0 if its length is invalid).
-__device__ __forceinline__ int seq_blocks(const int32_t* lens, int b, int bs, int max_blocks, int window) {
-  const int rows = seq_rows(lens, b, bs, max_blocks);
+__device__ __forceinline__ int seq_blocks(const int32_t* lens, int b, int bs, int max_blocks, int window,
+                                          int min_len) {
+  const int rows = seq_rows(lens, b, bs, max_blocks, min_len);
   if (rows == 0) return 0;
   return (rows + bs - 1) / bs - first_row(rows, window) / bs;
 }
 
 // Exclusive prefix sums of seq_blocks over the batch into s_scan[0..B];
 // the whole CTA participates. s_scan needs B + 1 + 32 ints.
-__device__ inline void scan_blocks(const int32_t* lens, int B, int bs, int max_blocks, int window, int* s_scan) {
+__device__ inline void scan_blocks(const int32_t* lens, int B, int bs, int max_blocks, int window, int min_len,
+                                   int* s_scan) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int per = (B + nt - 1) / nt;
   const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
   int local = 0;
-  for (int b = b0; b < b1; ++b) local += seq_blocks(lens, b, bs, max_blocks, window);
+  for (int b = b0; b < b1; ++b) local += seq_blocks(lens, b, bs, max_blocks, window, min_len);
   const int lane = tid & 31, wid = tid >> 5;
   int v = local;
 #pragma unroll
@@ -124,7 +126,7 @@ __device__ inline void scan_blocks(const int32_t* lens, int B, int bs, int max_b
   int run = v - local + (wid > 0 ? wsum[wid - 1] : 0);
   for (int b = b0; b < b1; ++b) {
     s_scan[b] = run;
-    run += seq_blocks(lens, b, bs, max_blocks, window);
+    run += seq_blocks(lens, b, bs, max_blocks, window, min_len);
   }
   if (b1 == B && b0 < B) s_scan[B] = run;
   if (B == 0 && tid == 0) s_scan[0] = 0;
@@ -241,12 +243,14 @@ struct VRow {
 
 // One 16-row tile of a page: scores, online softmax, V accumulation.
 // sp is this warp's [GW][16] fp32 weight buffer.
-// PARTIAL tiles attend only rows [lo_valid, valid) of the 16. For FP8
+// PARTIAL tiles attend only rows [lo_valid, valid) of the 16, and the lane's
+// head only those below vis (<= valid: with several new tokens an earlier
+// token does not see the later ones' rows). For FP8
 // caches vsp holds the tile's 16 per-token V scales: they multiply the
 // weights that feed the V accumulation (the sum l keeps the unscaled ones).
 template <typename T, int D, int GW, bool PARTIAL>
 __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __restrict__ vp, float* sp,
-                                         const float* __restrict__ vsp, int lo_valid, int valid,
+                                         const float* __restrict__ vsp, int lo_valid, int valid, int vis,
                                          WarpState<T, D, GW>& st, const LaneGeo<T, D, GW>& g) {
   using C = GqaCfg<T, D, GW>;
   float sc[C::NS][C::NVF];
@@ -291,7 +295,7 @@ __device__ __forceinline__ void gqa_tile(const T* __restrict__ kp, const T* __re
   for (int set = 0; set < C::NS; ++set) {
 #pragma unroll
     for (int k = 0; k < C::NVF; ++k) {
-      if (PARTIAL && (g.prow[k] + set >= valid || g.prow[k] + set < lo_valid)) sc[set][k] = kNegInf;
+      if (PARTIAL && (g.prow[k] + set >= vis || g.prow[k] + set < lo_valid)) sc[set][k] = kNegInf;
       need |= sc[set][k] > m_l + 8.0f;
     }
   }
@@ -412,6 +416,15 @@ __device__ __forceinline__ BlockPos locate_block(int64_t gb, int HN, const int* 
   return r;
 }
 
+// Row of `out` ([batch, n_tok, n_q_heads, D], flattened over rows) that holds
+// virtual query head v of kv head kvh: with several new tokens per sequence
+// the n_tok * group queries of a kv head are its virtual heads, v = t * group
+// + j (token t, query head j of the group).
+__device__ __forceinline__ int64_t out_row(const GqaParams& p, int seq, int kvh, int v) {
+  const int t = v / p.group, j = v - t * p.group;
+  return (static_cast<int64_t>(seq) * p.n_tok + t) * p.n_q_heads + kvh * p.group + j;
+}
+
 // Record slot that worker c left for the unit whose first block is u0: 2c
 // if the unit's part in c starts at c's first block, else 2c + 1. Returns
 // -1 for a worker with an empty range (only when N < W).
@@ -428,8 +441,8 @@ __device__ __forceinline__ int64_t record_of(int64_t c, int64_t c0, int64_t u0, 
 // lane r loads the (max, sum) pairs of record r while every lane loads its
 // chunks of the group's output rows, so one round trip serves the group.
 // Lane L owns the float4 chunks L + 32k of the warp's GW x D outputs.
-template <int D, int HS, int GW>
-__device__ void merge_unit_warp(const GqaParams& p, int64_t u0, int nb, int64_t W, int64_t N, int seq, int hq0,
+template <int D, int HS, int GW, bool EXT>
+__device__ void merge_unit_warp(const GqaParams& p, int64_t u0, int nb, int64_t W, int64_t N, int seq, int kvh, int v0,
                                 int hoff, int lane) {
   constexpr int CH = D / 4;                  // float4 chunks per head
   constexpr int NCK = (GW * CH + 31) / 32;   // chunks per lane
@@ -518,7 +531,8 @@ __device__ void merge_unit_warp(const GqaParams& p, int64_t u0, int nb, int64_t 
     float iv = 0.f;
 #pragma unroll
     for (int h = 0; h < GW; ++h) iv = (idx / CH == h) ? inv[h] : iv;
-    const int64_t o = (static_cast<int64_t>(seq) * p.n_q_heads + hq0) * D + 4 * idx;
+    const int64_t o = EXT ? out_row(p, seq, kvh, v0 + idx / CH) * D + 4 * (idx % CH)
+                          : (static_cast<int64_t>(seq) * p.n_q_heads + kvh * p.group + v0) * D + 4 * idx;
     store_out(p.out, o, O[k].x * iv, p.out_dtype);
     store_out(p.out, o + 1, O[k].y * iv, p.out_dtype);
     store_out(p.out, o + 2, O[k].z * iv, p.out_dtype);
@@ -535,9 +549,15 @@ __device__ __forceinline__ unsigned int atomic_add_acq_rel_cta_smem(unsigned int
   return old;
 }
 
-// WIN: the sliding window is compiled in only where it is used, so the
-// full-attention kernel keeps no per-block window bookkeeping.
-template <typename T, int D, int GH, typename TQ, bool WIN>
+// EXT: the extensions (sliding window, several new query tokens per
+// sequence) are compiled in only where they are used, so the single-token
+// full-attention kernel keeps no per-block bookkeeping for them.
+//
+// With n_tok new tokens the queries of a kv head are its n_tok * group
+// "virtual heads" v = t * group + j; they share every page. Token t sits at
+// position n - n_tok + t of a sequence of n cached rows and attends rows
+// [0, n - n_tok + t], so virtual head v hides the last n_tok - 1 - t rows.
+template <typename T, int D, int GH, typename TQ, bool EXT>
 __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kernel(const GqaParams p) {
   constexpr int HW = gqa_warps_per_kvhead(GH);  // warps per kv head
   constexpr int GW = GH / HW;                    // query heads per warp
@@ -549,7 +569,10 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   extern __shared__ __align__(128) unsigned char smem[];
   const int hc = p.hc;
   constexpr bool kFp8 = sizeof(T) == 1;
-  const int wnd = WIN ? p.window : 0;  // sliding window rows (0: all)
+  const int wnd = EXT ? p.window : 0;   // sliding window rows (0: all)
+  const int n_tok = EXT ? p.n_tok : 1;  // new query tokens per sequence
+  const int tm = n_tok - 1;             // rows hidden from the first of them
+  const bool multi = EXT && n_tok > 1;
   constexpr int VSB = kFp8 ? 4 : 0;  // V-scale bytes per cached row
   const GqaSmem L = gqa_smem_layout(sizeof(T), sizeof(TQ), VSB, D, GH, p.block_size, hc, p.stages, p.batch);
   unsigned char* s_stage = smem + L.stage_off;
@@ -604,7 +627,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     const int j = static_cast<int>((pos - seq * per_seq) % p.max_blocks) + tid * 32;
     if (seq < B && j < p.max_blocks) prefetch_l2(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks + j);
   }
-  scan_blocks(p.context_lens, B, bs, p.max_blocks, wnd, s_scan);  // ends with a CTA barrier
+  scan_blocks(p.context_lens, B, bs, p.max_blocks, wnd, n_tok, s_scan);  // ends with a CTA barrier
   const int64_t N = static_cast<int64_t>(HN) * s_scan[B];
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
@@ -614,13 +637,14 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     // zero outputs of sequences whose length is invalid (no CTA visits them).
     for (int b = tid; b < B; b += blockDim.x) {
       const int n = __ldg(p.context_lens + b);
-      if (n < 1 || n > bs * p.max_blocks) set_flag(p.err, 0x2u);
+      if (n < n_tok || n > bs * p.max_blocks) set_flag(p.err, 0x2u);
     }
     if (!p.unit_mode) {
+      const int rows = n_tok * p.n_q_heads * D;  // outputs of one sequence
       for (int b = 0; b < B; ++b) {
-        if (__ldg(p.context_lens + b) >= 1) continue;
-        for (int idx = tid; idx < p.n_q_heads * D; idx += blockDim.x)
-          store_out(p.out, static_cast<int64_t>(b) * p.n_q_heads * D + idx, 0.f, p.out_dtype);
+        if (__ldg(p.context_lens + b) >= n_tok) continue;
+        for (int idx = tid; idx < rows; idx += blockDim.x)
+          store_out(p.out, static_cast<int64_t>(b) * rows + idx, 0.f, p.out_dtype);
       }
     }
   }
@@ -635,9 +659,12 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
       // invalid length: zero output for this CTA's heads
       if (active) {
         const int chunk = idx / p.n_hsub, hsub = idx - chunk * p.n_hsub;
-        const int hq0 = (chunk * hc + kh) * p.group + hsub * GH + hw * GW;
-        for (int i = lane; i < GW * D; i += 32)
-          store_out(p.out, (static_cast<int64_t>(seq) * p.n_q_heads + hq0) * D + i, 0.f, p.out_dtype);
+        const int kvh = chunk * hc + kh, v0 = hsub * GH + hw * GW;
+        for (int i = lane; i < GW * D; i += 32) {
+          const int64_t o = EXT ? out_row(p, seq, kvh, v0 + i / D) * D + i % D
+                                : (static_cast<int64_t>(seq) * p.n_q_heads + kvh * p.group + v0) * D + i;
+          store_out(p.out, o, 0.f, p.out_dtype);
+        }
       }
       return;
     }
@@ -658,7 +685,8 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   // Positions lo + 32*win + lane, one per lane: the page index (block *
   // n_kv_heads + first kv head of the chunk; -1 if the table entry is out of
   // range) and, for the first block of a segment, the element offset of the
-  // unit's first query row (-1 otherwise).
+  // unit's first query row, or with several new tokens the unit's index
+  // (-1 otherwise).
   auto window = [&](int win, int& src, int& qoff) {
     const int64_t pos = lo + static_cast<int64_t>(win) * 32 + lane;
     src = -1;
@@ -666,11 +694,12 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     if (pos < hi) {
       const BlockPos bp = locate_block(pos, HN, s_scan, B, p.n_hsub);
       // bp.j counts the sequence's visible blocks; the table is indexed from block 0
-      const int j0 = first_row(seq_rows(p.context_lens, bp.seq, bs, p.max_blocks), wnd) / bs;
+      const int j0 = first_row(seq_rows(p.context_lens, bp.seq, bs, p.max_blocks, n_tok), wnd) / bs;
       const int phys = __ldg(p.block_tables + static_cast<int64_t>(bp.seq) * p.max_blocks + j0 + bp.j);
       if (phys >= 0 && phys < p.num_blocks) src = phys * p.n_kv_heads + bp.chunk * hc;
       if (pos == lo || bp.j == 0)
-        qoff = (bp.seq * p.n_q_heads + bp.chunk * hc * p.group + bp.hsub * GH) * D;
+        qoff = multi ? (bp.seq * p.n_chunks + bp.chunk) * p.n_hsub + bp.hsub
+                     : (bp.seq * p.n_q_heads + bp.chunk * hc * p.group + bp.hsub * GH) * D;
     }
   };
   // Copies of one position into stage `slot` (one thread).
@@ -693,7 +722,24 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
                  pol);
     }
     if (qoff >= 0) {
-      if (q_contig) {
+      if (multi) {
+        // The unit's GH virtual heads of each kv head, v = t * group + j, are
+        // query rows (seq, t, kv head * group + j): one copy per run of one token.
+        const int hs = qoff % p.n_hsub, rest = qoff / p.n_hsub;
+        const int ch = rest % p.n_chunks, sq = rest / p.n_chunks;
+        const uint32_t rowb = static_cast<uint32_t>(D * sizeof(TQ));
+        for (int h = 0; h < hc; ++h) {
+          const int kvh = ch * hc + h;
+          for (int v = hs * GH, ve = v + GH; v < ve;) {
+            const int t = v / p.group, j = v - t * p.group;
+            const int len = min(p.group - j, ve - v);
+            const int64_t row = (static_cast<int64_t>(sq) * n_tok + t) * p.n_q_heads + kvh * p.group + j;
+            bulk_g2s(dst + 2 * chunk_bytes + (h * GH + v - hs * GH) * rowb, qg + row * D, len * rowb, fbar + slot,
+                     pol);
+            v += len;
+          }
+        }
+      } else if (q_contig) {
         bulk_g2s(dst + 2 * chunk_bytes, qg + qoff, q_bytes, fbar + slot, pol);
       } else {
         const uint32_t rb = static_cast<uint32_t>(GH * D * sizeof(TQ));
@@ -735,10 +781,13 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
       // ---- segment: the part of one unit inside [lo, hi)
       const BlockPos sg = locate_block(gb, HN, s_scan, B, p.n_hsub);
       const int seg_len = static_cast<int>(((sg.nb - sg.j) < (hi - gb)) ? (sg.nb - sg.j) : (hi - gb));
-      const int n_rows = seq_rows(p.context_lens, sg.seq, bs, p.max_blocks);
+      const int n_rows = seq_rows(p.context_lens, sg.seq, bs, p.max_blocks, n_tok);
       const int r0 = first_row(n_rows, wnd);  // first visible row
       const int j0 = r0 / bs;                      // table index of the first visible block
-      const int hq0 = (sg.chunk * hc + kh) * p.group + sg.hsub * GH + hw * GW;  // first query head of this warp
+      const int kvh = sg.chunk * hc + kh;          // kv head of this warp
+      const int v0 = sg.hsub * GH + hw * GW;       // first (virtual) query head of this warp
+      const int hq0 = kvh * p.group + v0;          // its query head (single token)
+      const int dh = EXT ? tm - (v0 + geo.h_lane) / p.group : 0;  // last rows the lane's head may not see
 
       WarpState<T, D, GW> st;
       for (int t = 0; t < seg_len; ++t, ++cpos) {
@@ -802,7 +851,9 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
             for (int i = 0; i < C::DP2; ++i) st.q[h][i] = make_float2(f[2 * i] * ksc[2 * i], f[2 * i + 1] * ksc[2 * i + 1]);
 #pragma unroll
             for (int d = 0; d < C::VD; ++d) st.o[h][d] = make_float2(0.f, 0.f);
-            st.m[h] = kNegInf;
+            // With several tokens a head may meet only rows it may not see in
+            // a segment; a finite start keeps exp2(score - max) at 0 there.
+            st.m[h] = EXT ? -1e30f : kNegInf;
           }
           st.l = 0.f;
         }
@@ -811,21 +862,23 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
           const T* vp = reinterpret_cast<const T*>(my_v + static_cast<size_t>(slot) * stage_bytes);
           const float* vsp = reinterpret_cast<const float*>(stg + 2 * chunk_bytes + q_bytes) + kh * bs;
           const int jb = j0 + sg.j + t;                          // table index of this block
-          const int vr = min(bs, n_rows - jb * bs);              // rows of the block before the end
+          const int rb = n_rows - jb * bs;                       // rows from the block's first to the end
+          const int vr = min(bs, rb);                            // rows of the block before the end
           const int lr = (jb == j0) ? r0 - j0 * bs : 0;          // rows of the block before the window
-          if (vr >= bs && lr == 0) {
+          if (rb - tm >= bs && lr == 0) {
             for (int tt = 0; tt < tiles_per_page; ++tt)
-              gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, vsp + tt * 16, 0, 16, st, geo);
+              gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, vsp + tt * 16, 0, 16, 16, st, geo);
           } else {
             for (int tt = 0; tt < tiles_per_page; ++tt) {
               const int valid = vr - tt * 16, lo_valid = lr - tt * 16;
+              const int rt = rb - tt * 16;  // rows from the tile's first to the end
               if (valid <= 0) break;
               if (lo_valid >= 16) continue;
-              if (valid >= 16 && lo_valid <= 0)
-                gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, vsp + tt * 16, 0, 16, st, geo);
+              if (rt - tm >= 16 && lo_valid <= 0)
+                gqa_tile<T, D, GW, false>(kp + tt * 16 * D, vp + tt * 16 * D, wp, vsp + tt * 16, 0, 16, 16, st, geo);
               else
-                gqa_tile<T, D, GW, true>(kp + tt * 16 * D, vp + tt * 16 * D, wp, vsp + tt * 16, lo_valid, valid, st,
-                                         geo);
+                gqa_tile<T, D, GW, true>(kp + tt * 16 * D, vp + tt * 16 * D, wp, vsp + tt * 16, lo_valid, valid,
+                                         EXT ? min(valid, rt - dh) : valid, st, geo);
             }
           }
         }
@@ -866,7 +919,8 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
 #pragma unroll
           for (int h = 0; h < GW; ++h) {
             const float inv = 1.0f / lw[h];
-            const int64_t ob = (static_cast<int64_t>(sg.seq) * p.n_q_heads + hq0 + h) * D + geo.vofs;
+            const int64_t ob = (EXT ? out_row(p, sg.seq, kvh, v0 + h)
+                                    : static_cast<int64_t>(sg.seq) * p.n_q_heads + hq0 + h) * D + geo.vofs;
 #pragma unroll
             for (int d = 0; d < C::VD; ++d) ov[h][d] *= inv;
             store_out_vec<C::VD>(p.out, ob, ov[h], p.out_dtype);
@@ -944,14 +998,12 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
       }
     }
     last = __shfl_sync(full, last, 0);
-    if (last & 1) {
-      const int h0 = (q0.chunk * hc + kh) * p.group + q0.hsub * GH + hw * GW;
-      merge_unit_warp<D, HS, GW>(p, p0_u0, q0.nb, G, N, q0.seq, h0, kh * GH + hw * GW, lane);
-    }
-    if (last & 2) {
-      const int h1 = (q1.chunk * hc + kh) * p.group + q1.hsub * GH + hw * GW;
-      merge_unit_warp<D, HS, GW>(p, p1_u0, q1.nb, G, N, q1.seq, h1, kh * GH + hw * GW, lane);
-    }
+    if (last & 1)
+      merge_unit_warp<D, HS, GW, EXT>(p, p0_u0, q0.nb, G, N, q0.seq, q0.chunk * hc + kh, q0.hsub * GH + hw * GW,
+                                      kh * GH + hw * GW, lane);
+    if (last & 2)
+      merge_unit_warp<D, HS, GW, EXT>(p, p1_u0, q1.nb, G, N, q1.seq, q1.chunk * hc + kh, q1.hsub * GH + hw * GW,
+                                      kh * GH + hw * GW, lane);
   }
   if (any_abort && tid == 0) {
     // Copies that may still be in flight must land before the CTA exits and

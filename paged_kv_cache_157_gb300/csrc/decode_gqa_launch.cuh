@@ -8,9 +8,9 @@
 namespace kvc {
 
 // mode 0: launch; mode 1: only report the occupancy (CTAs per SM) in *occ.
-template <typename T, int D, int GH, typename TQ, bool WIN>
+template <typename T, int D, int GH, typename TQ, bool EXT>
 static kvc_status gqa_run(const GqaParams& p, int grid, size_t smem, cudaStream_t stream, int mode, int* occ) {
-  auto* k = gqa_decode_kernel<T, D, GH, TQ, WIN>;
+  auto* k = gqa_decode_kernel<T, D, GH, TQ, EXT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gqa)");
   if (mode == 1) {
@@ -22,27 +22,27 @@ static kvc_status gqa_run(const GqaParams& p, int grid, size_t smem, cudaStream_
   return KVC_OK;
 }
 
-template <typename T, int D, typename TQ, bool WIN>
+template <typename T, int D, typename TQ, bool EXT>
 static kvc_status gqa_run_gh(const GqaParams& p, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
                              int* occ) {
   switch (GH) {
-    case 1: return gqa_run<T, D, 1, TQ, WIN>(p, grid, smem, stream, mode, occ);
-    case 2: return gqa_run<T, D, 2, TQ, WIN>(p, grid, smem, stream, mode, occ);
-    case 4: return gqa_run<T, D, 4, TQ, WIN>(p, grid, smem, stream, mode, occ);
-    case 8: return gqa_run<T, D, 8, TQ, WIN>(p, grid, smem, stream, mode, occ);
-    case 16: return gqa_run<T, D, 16, TQ, WIN>(p, grid, smem, stream, mode, occ);
+    case 1: return gqa_run<T, D, 1, TQ, EXT>(p, grid, smem, stream, mode, occ);
+    case 2: return gqa_run<T, D, 2, TQ, EXT>(p, grid, smem, stream, mode, occ);
+    case 4: return gqa_run<T, D, 4, TQ, EXT>(p, grid, smem, stream, mode, occ);
+    case 8: return gqa_run<T, D, 8, TQ, EXT>(p, grid, smem, stream, mode, occ);
+    case 16: return gqa_run<T, D, 16, TQ, EXT>(p, grid, smem, stream, mode, occ);
   }
   return fail(KVC_ERR_UNSUPPORTED, "head subgroup %d", GH);
 }
 
-template <typename T, bool WIN>
+template <typename T, bool EXT>
 kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
                         int* occ) {
   switch (D) {
-    case 32: return gqa_run_gh<T, 32, T, WIN>(p, GH, grid, smem, stream, mode, occ);
-    case 64: return gqa_run_gh<T, 64, T, WIN>(p, GH, grid, smem, stream, mode, occ);
-    case 128: return gqa_run_gh<T, 128, T, WIN>(p, GH, grid, smem, stream, mode, occ);
-    case 256: return gqa_run_gh<T, 256, T, WIN>(p, GH, grid, smem, stream, mode, occ);
+    case 32: return gqa_run_gh<T, 32, T, EXT>(p, GH, grid, smem, stream, mode, occ);
+    case 64: return gqa_run_gh<T, 64, T, EXT>(p, GH, grid, smem, stream, mode, occ);
+    case 128: return gqa_run_gh<T, 128, T, EXT>(p, GH, grid, smem, stream, mode, occ);
+    case 256: return gqa_run_gh<T, 256, T, EXT>(p, GH, grid, smem, stream, mode, occ);
   }
   return fail(KVC_ERR_UNSUPPORTED, "head_dim %d (supported: 32, 64, 128, 256)", D);
 }

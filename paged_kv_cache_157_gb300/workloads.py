@@ -226,3 +226,20 @@ def fp8_case(batch, n_q_heads, n_kv_heads, head_dim, block_size, lens, seed, spa
         "v_new": normal((batch, n_kv_heads, head_dim), "bf16", gv),
         "block_size": block_size,
     }
+
+
+def multi_case(batch, n_tok, n_q_heads, n_kv_heads, head_dim, block_size, lens, dtype, seed, spare_frac=0.10,
+               device="cpu"):
+    """A paged step with ``n_tok`` new query tokens per sequence (chunked prefill or speculative verification).
+
+    ``lens`` count every row including the n_tok new ones (each at least n_tok). The cache part is
+    ``gqa_case`` with the same seed; then, from a second generator seeded ``seed + 1``, in this order:
+    q [B, n_tok, Hq, D], new k and new v [B, n_tok, Hkv, D] (the rows of positions n - n_tok .. n - 1).
+    """
+    c = gqa_case(batch, n_q_heads, n_kv_heads, head_dim, block_size, lens, dtype, seed, spare_frac, True, device)
+    g2 = _gen(seed + 1, device if device != "cpu" else "cpu")
+    c["q"] = normal((batch, n_tok, n_q_heads, head_dim), dtype, g2)
+    c["k_new"] = normal((batch, n_tok, n_kv_heads, head_dim), dtype, g2)
+    c["v_new"] = normal((batch, n_tok, n_kv_heads, head_dim), dtype, g2)
+    c["n_tok"] = n_tok
+    return c
