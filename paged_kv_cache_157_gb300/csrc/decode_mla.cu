@@ -95,7 +95,9 @@ enum {
   B_OFREE = B_PEMPTY0 + kPBufs, B_FINAL, B_COUNT
 };
 constexpr uint32_t kOffMisc = kOffBar + B_COUNT * 8;  // tmem address, abort flag, last flag
-constexpr uint32_t kOffScan = kOffMisc + 16;
+constexpr int kMergeChunk = 64;  // record slots the merging warpgroup lists in shared memory at a time
+constexpr uint32_t kOffRec = kOffMisc + 16;
+constexpr uint32_t kOffScan = kOffRec + kMergeChunk * 4;
 constexpr uint32_t smem_bytes(int batch) { return kOffScan + (batch + 1 + 32) * 4 + 1024; }
 
 struct Params {
@@ -430,8 +432,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     walk.lo = walk.pos = range_start(pair, G, N);
     walk.hi = range_start(pair + 1, G, N);
   }
-  // zero outputs of sequences with an invalid length (no CTA visits them)
+  // zero outputs of sequences with an invalid length (no CTA visits them);
+  // the lengths are checked in parallel first, so the common case costs one pass
+  bool any_bad = false;
   if (blockIdx.x < 2) {
+    int bad = 0;
+    for (int b = tid; b < p.batch; b += blockDim.x) bad |= (__ldg(p.context_lens + b) < 1) ? 1 : 0;
+    any_bad = __syncthreads_or(bad) != 0;
+  }
+  if (any_bad) {
     for (int b = 0; b < p.batch; ++b) {
       if (__ldg(p.context_lens + b) >= 1) continue;
       for (int idx = tid; idx < kHeads * kHalf; idx += blockDim.x) {
@@ -697,9 +706,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[32];
         tmem_ld32(lane_addr + kColO + c, v);
         if (whole) {
+          // this head's 32 consecutive output dims: 16-byte stores
           const int64_t o = (static_cast<int64_t>(sg.seq) * kHeads + h) * kDc + hf * kHalf + c;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) store_out(p.out, o + i, v[i] * inv, p.out_dtype);
+          for (int i = 0; i < 32; ++i) v[i] *= inv;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) store_out_vec<8>(p.out, o + i, v + i, p.out_dtype);
         } else {
           float4* dst = reinterpret_cast<float4*>(p.rec_o + rec * kHalf + c);
 #pragma unroll
@@ -735,48 +747,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (*s_last) {
           __threadfence();
-          // merge: this thread owns head h, all 256 dims of this half
-          float M = -__builtin_huge_valf();
-          for (int64_t c = c0; c <= c1; ++c) {
-            const int64_t f0 = range_start(c, G, N_all);
-            if (f0 == range_start(c + 1, G, N_all)) continue;
-            const int64_t r = ((c * 2 + hf) * 2 + ((sg.u0 > f0) ? 1 : 0)) * kHeads + h;
-            M = fmaxf(M, __ldcg(p.rec_ml + r * 2));
-          }
-          float L = 0.f;
-          for (int64_t c = c0; c <= c1; ++c) {
-            const int64_t f0 = range_start(c, G, N_all);
-            if (f0 == range_start(c + 1, G, N_all)) continue;
-            const int64_t r = ((c * 2 + hf) * 2 + ((sg.u0 > f0) ? 1 : 0)) * kHeads + h;
-            const float mc = __ldcg(p.rec_ml + r * 2);
-            if (mc == -__builtin_huge_valf()) continue;
-            L += fast_exp2(mc - M) * __ldcg(p.rec_ml + r * 2 + 1);
+          // Merge the unit's records with the log-sum-exp rule. The record
+          // slots of the contributors are listed in shared memory (kMergeChunk
+          // at a time, computed in parallel); pass 1 gives every head (thread
+          // h) its maximum and sum, pass 2 lets each half warp read one head's
+          // 256-float record rows as contiguous 1 KB runs and write its output
+          // row with 16-byte stores.
+          int* s_rec = reinterpret_cast<int*>(sm + kOffRec);
+          const int span = static_cast<int>(c1 - c0 + 1);
+          auto list_records = [&](int base, int nc) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // earlier readers of the list are done
+            if (tid < nc) {
+              const int64_t c = c0 + base + tid;
+              const int64_t f0 = range_start(c, G, N_all);
+              s_rec[tid] = (f0 == range_start(c + 1, G, N_all))
+                               ? -1
+                               : static_cast<int>((c * 2 + hf) * 2 + ((sg.u0 > f0) ? 1 : 0));
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+          };
+          float M = -__builtin_huge_valf(), L = 0.f;
+          for (int base = 0; base < span; base += kMergeChunk) {
+            const int nc = min(kMergeChunk, span - base);
+            list_records(base, nc);
+#pragma unroll 4
+            for (int i = 0; i < nc; ++i) {
+              const int rs = s_rec[i];
+              if (rs < 0) continue;
+              const int64_t r = static_cast<int64_t>(rs) * kHeads + h;
+              const float mc = __ldcg(p.rec_ml + r * 2), lc = __ldcg(p.rec_ml + r * 2 + 1);
+              if (mc == -__builtin_huge_valf()) continue;
+              const float mn = fmaxf(M, mc);
+              L = L * fast_exp2(M - mn) + lc * fast_exp2(mc - mn);  // M = -inf: L is 0 and stays 0
+              M = mn;
+            }
           }
           const float invL = 1.0f / L;
-          for (int d0 = 0; d0 < kHalf; d0 += 32) {
-            float acc[32];
+          const int half = lane >> 4, l16 = lane & 15;
+          for (int jj = 0; jj < 16; ++jj) {
+            const int src = 2 * jj + half;  // lane (head) of the warp this half warp serves
+            const int hj = warp * 32 + src;
+            const float Mj = __shfl_sync(0xffffffffu, M, src);
+            const float iLj = __shfl_sync(0xffffffffu, invL, src);
+            float acc[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-            for (int64_t c = c0; c <= c1; ++c) {
-              const int64_t f0 = range_start(c, G, N_all);
-              if (f0 == range_start(c + 1, G, N_all)) continue;
-              const int64_t r = ((c * 2 + hf) * 2 + ((sg.u0 > f0) ? 1 : 0)) * kHeads + h;
-              const float mc = __ldcg(p.rec_ml + r * 2);
-              if (mc == -__builtin_huge_valf()) continue;
-              const float f = fast_exp2(mc - M);
-              const float4* src = reinterpret_cast<const float4*>(p.rec_o + r * kHalf + d0);
+            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+            for (int base = 0; base < span; base += kMergeChunk) {
+              const int nc = min(kMergeChunk, span - base);
+              if (span > kMergeChunk) list_records(base, nc);  // uniform over the warpgroup
+#pragma unroll 2
+              for (int i = 0; i < nc; ++i) {
+                const int rs = s_rec[i];
+                if (rs < 0) continue;
+                const int64_t r = static_cast<int64_t>(rs) * kHeads + hj;
+                const float mc = __ldcg(p.rec_ml + r * 2);
+                const float4* srcp = reinterpret_cast<const float4*>(p.rec_o + r * kHalf) + l16 * 4;
+                float4 x[4];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float4 x = __ldcg(src + i);
-                acc[4 * i] += f * x.x;
-                acc[4 * i + 1] += f * x.y;
-                acc[4 * i + 2] += f * x.z;
-                acc[4 * i + 3] += f * x.w;
+                for (int k = 0; k < 4; ++k) x[k] = __ldcg(srcp + k);
+                const float f = (mc == -__builtin_huge_valf()) ? 0.f : fast_exp2(mc - Mj);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  acc[4 * k] += f * x[k].x;
+                  acc[4 * k + 1] += f * x[k].y;
+                  acc[4 * k + 2] += f * x[k].z;
+                  acc[4 * k + 3] += f * x[k].w;
+                }
               }
             }
-            const int64_t o = (static_cast<int64_t>(sg.seq) * kHeads + h) * kDc + hf * kHalf + d0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) store_out(p.out, o + i, acc[i] * invL, p.out_dtype);
+            for (int i = 0; i < 16; ++i) acc[i] *= iLj;
+            const int64_t o = (static_cast<int64_t>(sg.seq) * kHeads + hj) * kDc + hf * kHalf + l16 * 16;
+            store_out_vec<8>(p.out, o, acc, p.out_dtype);
+            store_out_vec<8>(p.out, o + 8, acc + 8, p.out_dtype);
           }
           if (tid == 0) p.counters[unit] = 0u;
         }

@@ -96,6 +96,24 @@ def test_mla_forced_split(kvc, blocks_per_cta):
     assert kvc.get_error_flags() == 0
 
 
+def test_mla_merge_of_more_than_64_records(kvc):
+    # one block per CTA pair: the 6400-row sequence is cut into 100 parts, so the merging warpgroup lists the
+    # record slots in two chunks (64 + 36); bf16 output takes the vector stores of the merge
+    kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, 1)
+    lens = [6400, 300]
+    case = W.mla_case(len(lens), H, D_C, D_R, 64, lens, "bf16", seed=49)
+    out, slots = run_mla(kvc, case)
+    ref = oracle_mla(case, slots)
+    err = float(np.max(np.abs(f64(out) - ref)))
+    assert err <= TOL, err
+    assert kvc.get_error_flags() == 0
+    out16, _ = run_mla(kvc, case, out_dtype=torch.bfloat16)  # a fresh device copy, the same append
+    # bf16 rounding of the same result
+    excess = np.abs(f64(out16) - ref) - (TOL + 2.0 ** -8 * np.abs(ref))
+    assert float(np.max(excess)) <= 0.0
+    assert kvc.get_error_flags() == 0
+
+
 def test_mla_without_workspace(kvc):
     lens = [300, 5, 129]
     case = W.mla_case(len(lens), H, D_C, D_R, 64, lens, "bf16", seed=48)
