@@ -687,6 +687,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[kTile / 2 + i] = pack_bf16(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
         }
         tmem_st32u(lane_addr + kColP + pb * kTile, pk);
+        if (valid < kTile) {
+          // Rows past the end of the sequence (the rest of its last block) may
+          // hold anything, NaN included; their weight is 0, but 0 x NaN is NaN,
+          // so this CTA's value columns of those rows are zeroed before PV
+          // reads them (whole 128-byte rows: the swizzle only permutes within
+          // a row). The proxy fence hands the writes to the tensor core.
+          const int r0 = valid > 0 ? valid : 0;
+          const int n16 = (kTile - r0) * 4 * 8;  // 16-byte chunks: rows x 4 value blocks x 8
+          unsigned char* stg = sm + kOffC + (g % kStages) * kTileBytes + (4 * hf) * kTileSub;
+          for (int i = tid; i < n16; i += 128) {
+            const int row = r0 + i / 32, blk = (i / 8) % 4, c = i % 8;
+            *reinterpret_cast<uint4*>(stg + blk * kTileSub + row * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
         fence_before();
         __syncwarp();
         if (lane == 0) arrive(bar(B_PFULL0 + pb));

@@ -114,6 +114,22 @@ def test_mla_merge_of_more_than_64_records(kvc):
     assert kvc.get_error_flags() == 0
 
 
+def test_mla_nan_in_unused_rows_of_the_last_block(kvc):
+    # the rows of a sequence's last block past its length may hold anything; NaN there must not reach the output
+    lens = [1, 33, 100, 64, 65]
+    case = W.mla_case(len(lens), H, D_C, D_R, 64, lens, "bf16", seed=50)
+    bs = case["block_size"]
+    for i, n in enumerate(lens):
+        blk = int(case["block_tables"][i, (n - 1) // bs])
+        case["latent_cache"][blk, n % bs if n % bs else bs:, :] = float("nan")
+    out, slots = run_mla(kvc, case)
+    ref = oracle_mla(case, slots)
+    assert torch.isfinite(out).all()
+    err = float(np.max(np.abs(f64(out) - ref)))
+    assert err <= TOL, err
+    assert kvc.get_error_flags() == 0
+
+
 def test_mla_without_workspace(kvc):
     lens = [300, 5, 129]
     case = W.mla_case(len(lens), H, D_C, D_R, 64, lens, "bf16", seed=48)
