@@ -220,44 +220,75 @@ def time_steps(step, steps, warmup, flush, sampler=None):
 
 
 def time_e2e(kvc, step, steps, warmup, flush):
-    """Same step through the public API from pinned host buffers: H2D of the step's
-    inputs (q, new k/v, slots, tables, lengths), append, decode, D2H of the output."""
+    """Same step through the public API from pinned host memory: one H2D copy of the step's inputs (q, new
+    k/v, tables, lengths, slots, packed at 256-byte offsets in one pinned staging buffer; the library calls
+    take device views into its device copy), kvc_append, kvc_decode_attention, and a D2H copy of the output.
+    The four operations are captured once in a CUDA graph and replayed every step (the host waits for each
+    step's result before the next). Returns (ms per step, H2D bytes, D2H bytes, whether a graph was used)."""
     import torch
     c = step.case
-    host = {k: c[k].detach().to("cpu").pin_memory() for k in ("q", "k_new", "v_new", "block_tables", "context_lens")}
-    host["slots"] = step.slots.cpu().pin_memory()
-    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    parts = [("q", c["q"]), ("k_new", c["k_new"]), ("v_new", c["v_new"]), ("block_tables", c["block_tables"]),
+             ("context_lens", c["context_lens"]), ("slots", step.slots.cpu())]
+    offs, total = {}, 0
+    for name, t in parts:
+        offs[name] = total
+        total += -(-t.numel() * t.element_size() // 256) * 256
+    host = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device="cuda")
+    v = {}
+    for name, t in parts:
+        t = t.detach().to("cpu").contiguous()
+        nb = t.numel() * t.element_size()
+        host[offs[name]:offs[name] + nb].copy_(t.view(-1).view(torch.uint8))
+        v[name] = dev_buf[offs[name]:offs[name] + nb].view(t.dtype).view(t.shape)
     dev = step.dev
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    out = torch.empty_like(step.out)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     d2h = out_h.numel() * out_h.element_size()
-    stream = torch.cuda.current_stream()
 
     def one():
-        dev["q"].copy_(host["q"], non_blocking=True)
-        dev["k_new"].copy_(host["k_new"], non_blocking=True)
-        dev["v_new"].copy_(host["v_new"], non_blocking=True)
-        dev["block_tables"].copy_(host["block_tables"], non_blocking=True)
-        dev["context_lens"].copy_(host["context_lens"], non_blocking=True)
-        step.slots.copy_(host["slots"], non_blocking=True)
-        step.append()
-        step.decode()
-        out_h.copy_(step.out, non_blocking=True)
+        dev_buf.copy_(host, non_blocking=True)
+        kvc.append(v["k_new"], v["v_new"], v["slots"], dev["k_cache"], dev["v_cache"])
+        kvc.decode_attention(v["q"], dev["k_cache"], dev["v_cache"], v["block_tables"], v["context_lens"],
+                             step.scale, out, step.ws)
+        out_h.copy_(out, non_blocking=True)
 
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(max(3, warmup)):
+            one()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            one()
+        graph = g
+    except Exception as e:  # report it; the same calls then run eagerly
+        print(f"e2e: CUDA graph capture failed ({type(e).__name__}: {e}); timing eager calls", file=sys.stderr)
+        torch.cuda.synchronize()
+    run = graph.replay if graph is not None else one
     for _ in range(warmup):
         flush.run()
-        one()
+        run()
     torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
     ts = []
     for _ in range(steps):
         flush.run()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        one()
+        run()
         b.record(stream)
         b.synchronize()  # the host needs the result before the next step
         ts.append(a.elapsed_time(b))
-    return statistics.mean(ts), h2d, d2h
+    ok = bool(torch.equal(out_h, out.cpu()))
+    if not ok:
+        print("e2e: the host copy of the output differs from the device output", file=sys.stderr)
+    return statistics.mean(ts), total, d2h, graph is not None
 
 
 # --------------------------------------------------------------- oracle
@@ -610,7 +641,7 @@ def run_kvc(args):
         return
     peak, peak_kind = peaks()
     achieved = dec_b / (dec_avg / 1e3) / 1e9
-    e2e_ms, h2d, d2h = time_e2e(kvc, step, min(args.steps, 500), min(args.warmup, 10), flush)
+    e2e_ms, h2d, d2h, e2e_graph = time_e2e(kvc, step, min(args.steps, 500), min(args.warmup, 10), flush)
     e2e_value = per_step / (e2e_ms / 1e3) / 1e9
     var = {} if args.no_variants else variants(kvc, flush, max(10, min(args.steps, 200)))
     cpu = None if args.no_cpu_baseline else cpu_baseline(case)
@@ -645,7 +676,9 @@ def run_kvc(args):
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "traffic": traffic_from_profile(), "algorithmic_bytes_per_launch": dec_b},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 5)},
+                "ms_per_step": round(e2e_ms, 5),
+                "how": ("one packed H2D copy + kvc_append + kvc_decode_attention + D2H of the output, "
+                        + ("replayed as one CUDA graph" if e2e_graph else "eager calls (graph capture failed)"))},
         "gpu_launches": 2 * args.steps,  # kvc_append + kvc_decode_attention per step
         "clocks": clocks,
         "timed_wall_s": round(wall, 4),
