@@ -99,7 +99,12 @@ typedef enum kvc_option {
    * split-K partials). Process-wide. */
   KVC_OPT_BLOCKS_PER_CTA = 1,
   /* Upper bound on decode CTAs (0 = automatic, SM count x resident CTAs). */
-  KVC_OPT_MAX_CTAS = 2
+  KVC_OPT_MAX_CTAS = 2,
+  /* GQA decode engine: 0 (default) = automatic (the tensor-core kernel for
+   * bf16/f16 caches, head_dim 128, block sizes 16/32/64/128, no window, when
+   * a kv head has 8 to 32 queries: n_tokens x n_q_heads / n_kv_heads);
+   * 1 = always the CUDA-core kernel. */
+  KVC_OPT_GQA_ENGINE = 3
 } kvc_option;
 kvc_status kvc_set_option(kvc_option opt, int64_t value);
 kvc_status kvc_get_option(kvc_option opt, int64_t* value);

@@ -95,6 +95,29 @@ __host__ __device__ inline GqaSmem gqa_smem_layout(int elt_bytes, int q_bytes, i
   return s;
 }
 
+// Tensor-core decode for kv heads with 8 to 32 queries (n_tok x group):
+// bf16/f16 caches, head_dim 128, block size 16/32/64/128, no window.
+struct WideArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* out;
+  void* workspace;
+  size_t workspace_bytes;
+  int64_t num_blocks;
+  int batch, n_q_heads, n_kv_heads, block_size, max_blocks, n_tok;
+  kvc_dtype dtype, out_dtype;
+  float scale;
+  cudaStream_t stream;
+};
+bool wide_supported(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size, int n_tok,
+                    kvc_dtype dtype);
+size_t wide_workspace_bytes(const DeviceInfo* dev, int batch, int n_q_heads, int n_kv_heads, int block_size,
+                            int max_blocks, int n_tok);
+kvc_status wide_decode(const WideArgs& a, DeviceInfo* dev);
+
 // EXT: kernels with the extensions compiled in (p.window > 0 or p.n_tok > 1).
 template <typename T, bool EXT>
 kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,

@@ -163,6 +163,12 @@ kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, i
   const int64_t G = plan_ctas(dev, kMaxCtasPerSm, static_cast<int64_t>(batch) * n_kv_heads * pl.n_hsub,
                              max_blocks_per_seq);
   *bytes = align_up(counter_bytes(batch, n_kv_heads, pl) + static_cast<size_t>(G) * pl.rec_bytes_per_cta, 256);
+  // the tensor-core kernel for wide groups (any dtype it takes) may need more
+  // (n_q_heads here already counts every new token of a multi-token call)
+  if (wide_supported(batch, n_q_heads, n_kv_heads, head_dim, block_size, 1, KVC_BF16))
+    *bytes = std::max(*bytes, align_up(wide_workspace_bytes(dev, batch, n_q_heads, n_kv_heads, block_size,
+                                                            max_blocks_per_seq, 1),
+                                       256));
   return KVC_OK;
 }
 
@@ -207,6 +213,30 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
 
   DeviceInfo* dev = nullptr;
   if ((s = current_device(&dev)) != KVC_OK) return s;
+  if (!fp8 && window == 0 &&
+      wide_supported(batch, n_q_heads, n_kv_heads, head_dim, block_size, n_tok, dtype)) {
+    WideArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.out = out;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.num_blocks = num_blocks;
+    a.batch = batch;
+    a.n_q_heads = n_q_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.block_size = block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.n_tok = n_tok;
+    a.dtype = dtype;
+    a.out_dtype = out_dtype;
+    a.scale = scale;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return wide_decode(a, dev);
+  }
   const int q_elt = static_cast<int>(dtype_size(dtype));
   const int elt = fp8 ? 1 : q_elt;
   GqaPlan pl;

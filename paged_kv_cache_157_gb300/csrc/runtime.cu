@@ -62,7 +62,7 @@ kvc_status current_device(DeviceInfo** out) {
   return KVC_OK;
 }
 
-static int64_t g_options[3] = {0, 0, 0};
+static int64_t g_options[4] = {0, 0, 0, 0};
 
 int64_t option(kvc_option opt) { return g_options[static_cast<int>(opt)]; }
 
@@ -119,16 +119,17 @@ const char* kvc_last_error_message(void) { return kvc::t_message.c_str(); }
 
 kvc_status kvc_set_option(kvc_option opt, int64_t value) {
   int o = static_cast<int>(opt);
-  if (o < 0 || o > 2) return kvc::fail(KVC_ERR_INVALID_ARG, "unknown option %d", o);
+  if (o < 0 || o > 3) return kvc::fail(KVC_ERR_INVALID_ARG, "unknown option %d", o);
   if (value < 0) return kvc::fail(KVC_ERR_INVALID_ARG, "option value must be >= 0");
   if (opt == KVC_OPT_CHECKED && value > 1) return kvc::fail(KVC_ERR_INVALID_ARG, "checked mode is 0 or 1");
+  if (opt == KVC_OPT_GQA_ENGINE && value > 1) return kvc::fail(KVC_ERR_INVALID_ARG, "GQA engine is 0 or 1");
   kvc::g_options[o] = value;
   return KVC_OK;
 }
 
 kvc_status kvc_get_option(kvc_option opt, int64_t* value) {
   int o = static_cast<int>(opt);
-  if (o < 0 || o > 2 || value == nullptr) return kvc::fail(KVC_ERR_INVALID_ARG, "bad option query");
+  if (o < 0 || o > 3 || value == nullptr) return kvc::fail(KVC_ERR_INVALID_ARG, "bad option query");
   *value = kvc::g_options[o];
   return KVC_OK;
 }
