@@ -484,8 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = sg.t0; t < sg.t1; ++t, ++g) {
         const uint32_t sb = g & 1u;
         // S^T(g) is in TMEM, and PV(g - 1) is done with P and O^T
-        bool got = wait_phase(bar(B_SFULL0 + sb), (g >> 1) & 1u, s_abort, p.err);
-        got = got && (g == 0 || wait_phase(bar(B_PEMPTY), (g - 1) & 1u, s_abort, p.err));
+        bool got = wait_phase_suspend(bar(B_SFULL0 + sb), (g >> 1) & 1u, s_abort, p.err);
+        got = got && (g == 0 || wait_phase_suspend(bar(B_PEMPTY), (g - 1) & 1u, s_abort, p.err));
         if (block_any128(!got || *s_abort)) {
           ok = false;
           break;
@@ -596,9 +596,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
 #pragma unroll
         for (int q = 0; q < NQ; ++q) p.rec_o[(rec * NQ + q) * kD + r] = o[q];
-        if (r == 0) {
 #pragma unroll
-          for (int q = 0; q < NQ; ++q) {
+        for (int q = 0; q < NQ; ++q) {
+          if (r == q) {  // thread q writes query q's (max, sum)
             p.rec_ml[(rec * NQ + q) * 2] = m[q];
             p.rec_ml[(rec * NQ + q) * 2 + 1] = l[q];
           }

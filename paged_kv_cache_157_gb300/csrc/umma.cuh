@@ -70,6 +70,25 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   return false;
 }
 
+// Same bound, but each probe may suspend the thread (try_wait) instead of
+// spinning, so a waiting warp leaves its scheduler's issue slots to the
+// warps that drive the copies and the tensor core.
+__device__ __forceinline__ bool wait_phase_suspend(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                   unsigned int* err) {
+  if (try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1; i < kWaitLimit; ++i) {
+    if (try_wait(bar, parity)) return true;
+    if ((i & 7u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitNs) break;
+    }
+  }
+  *abort_flag = 1;
+  set_flag(err, 0x8u);
+  return false;
+}
+
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets, the fixed version bits and the swizzle mode (2 = 128B).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
