@@ -287,6 +287,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// OR of `pred` over the 128 softmax threads (named barrier 1).
+__device__ __forceinline__ bool block_any128(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
 // ------------------------------------------------------- work bookkeeping
 
 __device__ __forceinline__ int seq_tiles(const int32_t* lens, int b, int bs, int max_blocks) {
@@ -591,19 +605,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------- softmax + epilogue
     const int h = warp * 32 + lane;  // head = TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // The four warps meet at named barriers (the record count and the merge),
+    // so they leave together: a failed wait ends only the tile loop, and a
+    // barrier vote before each shared step turns any failure into a common exit.
     uint32_t g = 0, seg_i = 0;
     Segment sg;
     Walker w = walk;
     bool ok = true;
-    while (ok && !*s_abort && w.next(p, s_scan, sg)) {
+    while (ok && w.next(p, s_scan, sg)) {
       if (sg.ntiles == 0) continue;
       const int n_rows = seq_rows(p.context_lens, sg.seq, p.block_size, p.max_blocks);
       // Columns [0, 256) of this head's Q~ row go to TMEM (the A operand of the
       // first 16 K steps of S), once the previous segment's S MMAs are done.
-      if (seg_i > 0 &&
-          !__all_sync(0xffffffffu, wait_phase(bar(B_QEMPTY), (seg_i - 1) & 1u, s_abort, p.err))) {
-        ok = false;
-        break;
+      {
+        const bool got = seg_i == 0 ||
+                         __all_sync(0xffffffffu, wait_phase(bar(B_QEMPTY), (seg_i - 1) & 1u, s_abort, p.err));
+        if (block_any128(!got || *s_abort)) {
+          ok = false;
+          break;
+        }
       }
       fence_after();
       {
@@ -706,12 +726,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) arrive(bar(B_PFULL0 + pb));
       }
-      if (!ok) break;
       // ---- epilogue: wait for the last PV, read O, write output or record
       {
         const uint32_t gl = g - 1;
-        if (!__all_sync(0xffffffffu, wait_phase(bar(B_PEMPTY0 + gl % kPBufs), (gl / kPBufs) & 1u, s_abort, p.err)))
+        const bool got = ok && __all_sync(0xffffffffu, wait_phase(bar(B_PEMPTY0 + gl % kPBufs), (gl / kPBufs) & 1u,
+                                                                  s_abort, p.err));
+        if (block_any128(!got || *s_abort)) {
+          ok = false;
           break;
+        }
       }
       fence_after();
       const bool whole = (sg.t0 == 0 && sg.t1 == sg.ntiles);
