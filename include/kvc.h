@@ -243,6 +243,39 @@ kvc_status kvc_decode_attention_multi(const void* q, const void* k_cache, const 
                                       kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
                                       size_t workspace_bytes, kvc_stream stream);
 
+/* Scratch bytes kvc_decode_attention_shared_prefix needs for these shapes
+ * (256-byte aligned, zero-filled once before first use; complete calls leave
+ * its counters zeroed again). */
+kvc_status kvc_decode_shared_prefix_workspace_size(int batch, int group_size, int n_q_heads, int n_kv_heads,
+                                                   int head_dim, int block_size, int max_blocks_per_seq,
+                                                   size_t* bytes);
+
+/* Decode for sequences that share a prefix (forks of one prompt: parallel
+ * sampling, beam search): the same result as kvc_decode_attention, but each
+ * shared block is read once per group instead of once per sequence.
+ * Sequences [g * group_size, (g + 1) * group_size) form group g; their first
+ * prefix_lens[g] rows (device int32 [batch / group_size]) must hold the same
+ * keys and values in every member (shared blocks, or copies of them), with
+ * 1 <= prefix_lens[g] <= each member's context length (KVC_FLAG_BAD_LEN
+ * otherwise). Runs three kernels on `stream`: the shared rows once per group
+ * (the group's queries of a kv head as virtual heads over the first member's
+ * table row), each sequence's rows from prefix_lens[g] on, and a merge of the
+ * two softmax states by their log-sum-exp. workspace: at least
+ * kvc_decode_shared_prefix_workspace_size() bytes (KVC_ERR_WORKSPACE if
+ * smaller or NULL). Other arguments, dtypes and errors as
+ * kvc_decode_attention. 1 <= group_size <= 256.
+ * Source: the shared physical blocks of "KV缓存原理与显存估算" (closing
+ * section: logical blocks of several sequences pointing at one physical block)
+ * and "KV Cache（键值缓存）" section 2.3 (sharing and copy-on-write of forks);
+ * the result is the decode of knowledge point 2 of the former. */
+kvc_status kvc_decode_attention_shared_prefix(const void* q, const void* k_cache, const void* v_cache,
+                                              const int32_t* block_tables, int max_blocks_per_seq,
+                                              const int32_t* context_lens, int batch, int group_size,
+                                              const int32_t* prefix_lens, float scale, int n_q_heads,
+                                              int n_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                              kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
+                                              size_t workspace_bytes, kvc_stream stream);
+
 /* FP8 KV cache decode: as kvc_decode_attention over the caches written by
  * kvc_append_fp8, attending k = e4m3value(code) * k_scale[h, d] and
  * v = e4m3value(code) * v_scale[row] (the scales fold into the query and into

@@ -65,6 +65,9 @@ SIGNATURES = {
                                            _i32, _i32, _vp, _i32, _vp, _sz, _vp]),
     "kvc_decode_attention_multi": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _i32, _i32, _i32, _i32,
                                           _i64, _i32, _vp, _i32, _vp, _sz, _vp]),
+    "kvc_decode_shared_prefix_workspace_size": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _szp]),
+    "kvc_decode_attention_shared_prefix": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _vp, _f32, _i32,
+                                                  _i32, _i32, _i32, _i64, _i32, _vp, _i32, _vp, _sz, _vp]),
     "kvc_decode_mla_workspace_size": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _szp]),
     "kvc_decode_attention_mla": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32, _i64, _i32, _vp,
                                         _i32, _vp, _sz, _vp]),
@@ -290,6 +293,42 @@ def decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens, scal
                                             block_tables.shape[1], _ptr(context_lens), B, T, float(scale), hq, hkv,
                                             d, bs, nb, _dtype_code(k_cache), _ptr(out), _dtype_code(out), ws_ptr,
                                             ws_bytes, _stream(stream)), "kvc_decode_attention_multi")
+
+
+def shared_prefix_workspace(batch, group_size, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                            device="cuda"):
+    """Zero-filled uint8 workspace of the size kvc_decode_shared_prefix_workspace_size asks for."""
+    torch = _torch()
+    n = ctypes.c_size_t()
+    _check(raw().kvc_decode_shared_prefix_workspace_size(batch, group_size, n_q_heads, n_kv_heads, head_dim,
+                                                         block_size, max_blocks_per_seq, ctypes.byref(n)),
+           "kvc_decode_shared_prefix_workspace_size")
+    return torch.zeros(max(n.value, 1), dtype=torch.uint8, device=device)
+
+
+def decode_attention_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, group_size, prefix_lens, scale,
+                                   out, workspace, stream=None):
+    """kvc_decode_attention_shared_prefix: q/out [B, Hq, D]; sequences [g*group_size, (g+1)*group_size) share
+    their first prefix_lens[g] rows (int32 device tensor [B / group_size]); workspace from
+    shared_prefix_workspace."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out"), (workspace, "workspace")):
+        _require(t, n)
+    _require(block_tables, "block_tables", torch.int32)
+    _require(context_lens, "context_lens", torch.int32)
+    _require(prefix_lens, "prefix_lens", torch.int32)
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if d2 != d or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("shape mismatch")
+    if prefix_lens.numel() * group_size != B:
+        raise ValueError("prefix_lens must hold one entry per group of group_size sequences")
+    _check(raw().kvc_decode_attention_shared_prefix(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                                    block_tables.shape[1], _ptr(context_lens), B, int(group_size),
+                                                    _ptr(prefix_lens), float(scale), hq, hkv, d, bs, nb,
+                                                    _dtype_code(k_cache), _ptr(out), _dtype_code(out),
+                                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                                    _stream(stream)), "kvc_decode_attention_shared_prefix")
 
 
 def decode_attention_static(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None):

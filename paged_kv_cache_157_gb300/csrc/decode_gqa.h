@@ -37,6 +37,10 @@ struct GqaParams {
   int unit_mode;  // 1: CTA u handles unit u completely (no records)
   int window;     // sliding window: attend the newest `window` rows (0: all rows)
   int n_tok;      // new query tokens per sequence (q and out are [batch, n_tok, n_q_heads, D])
+  int causal;     // n_tok > 1: 1 = token t sees rows up to n - n_tok + t; 0 = every row (a shared-prefix pass)
+  float* lse;     // non-NULL: log2 of each output row's softmax denominator plus its max (log2 units) [rows]
+  const int32_t* row_start;  // row_div > 0: sequence b attends rows from row_start[b / row_div]
+  int row_div;
   const float* k_scale;  // FP8 caches: per-channel K scales [n_kv_heads, head_dim]
   const float* v_scale;  // FP8 caches: per-token V scales [num_blocks, n_kv_heads, block_size]
   float qscale;   // scale * log2(e)
@@ -108,6 +112,8 @@ struct WideArgs {
   size_t workspace_bytes;
   int64_t num_blocks;
   int batch, n_q_heads, n_kv_heads, block_size, max_blocks, n_tok;
+  int causal;  // several tokens: 1 = causal among them, 0 = every row (a shared-prefix pass)
+  float* lse;  // non-NULL: per output row, max + log2(sum) (log2 units)
   kvc_dtype dtype, out_dtype;
   float scale;
   cudaStream_t stream;
@@ -118,7 +124,8 @@ size_t wide_workspace_bytes(const DeviceInfo* dev, int batch, int n_q_heads, int
                             int max_blocks, int n_tok);
 kvc_status wide_decode(const WideArgs& a, DeviceInfo* dev);
 
-// EXT: kernels with the extensions compiled in (p.window > 0 or p.n_tok > 1).
+// EXT: kernels with the extensions compiled in (window, several tokens,
+// start rows, LSE output).
 template <typename T, bool EXT>
 kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
                         int* occ);

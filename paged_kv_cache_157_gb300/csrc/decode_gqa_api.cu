@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "decode_gqa.h"
+#include "kvc_device.cuh"
 
 namespace kvc {
 
@@ -121,8 +122,17 @@ kvc_status check_shapes(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
   return KVC_OK;
 }
 
-// The extension kernels serve a sliding window or several new tokens.
-bool uses_ext(const GqaParams& p) { return p.window > 0 || p.n_tok > 1; }
+// The extension kernels serve a sliding window, several new tokens, start
+// rows or the LSE output.
+bool uses_ext(const GqaParams& p) { return p.window > 0 || p.n_tok > 1 || p.row_div > 0 || p.lse != nullptr; }
+
+// Options of the passes of a shared-prefix decode.
+struct DecodeExtra {
+  int causal = 1;
+  float* lse = nullptr;
+  const int32_t* row_start = nullptr;
+  int row_div = 0;
+};
 
 template <typename T>
 kvc_status occupancy(const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
@@ -185,7 +195,10 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
                        int max_blocks_per_seq, const int32_t* context_lens, int batch, float scale, int n_q_heads,
                        int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, int window, kvc_dtype dtype,
                        void* out, kvc_dtype out_dtype, void* workspace, size_t workspace_bytes, kvc_stream stream,
-                       const float* k_scale = nullptr, const float* v_scale = nullptr, int n_tok = 1) {
+                       const float* k_scale = nullptr, const float* v_scale = nullptr, int n_tok = 1,
+                       const DecodeExtra* ex = nullptr) {
+  const DecodeExtra none;
+  if (ex == nullptr) ex = &none;
   const bool fp8 = k_scale != nullptr;
   if (n_tok < 1 || n_tok > kMaxTokens)
     return fail(KVC_ERR_INVALID_ARG, "n_tokens %d (supported: 1 to %d)", n_tok, kMaxTokens);
@@ -213,7 +226,7 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
 
   DeviceInfo* dev = nullptr;
   if ((s = current_device(&dev)) != KVC_OK) return s;
-  if (!fp8 && window == 0 &&
+  if (!fp8 && window == 0 && ex->row_div == 0 &&
       wide_supported(batch, n_q_heads, n_kv_heads, head_dim, block_size, n_tok, dtype)) {
     WideArgs a{};
     a.q = q;
@@ -231,6 +244,8 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
     a.block_size = block_size;
     a.max_blocks = max_blocks_per_seq;
     a.n_tok = n_tok;
+    a.causal = ex->causal;
+    a.lse = ex->lse;
     a.dtype = dtype;
     a.out_dtype = out_dtype;
     a.scale = scale;
@@ -266,6 +281,10 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   p.stages = pl.stages;
   p.window = window;
   p.n_tok = n_tok;
+  p.causal = ex->causal;
+  p.lse = ex->lse;
+  p.row_start = ex->row_start;
+  p.row_div = ex->row_div;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
@@ -452,6 +471,149 @@ kvc_status kvc_decode_attention_static(const void* q, const void* k_cache, const
   return kvc_decode_attention(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale,
                               n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, dtype, out, out_dtype, scratch,
                               kStaticScratchBytes, stream);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------
+// Decode with shared prefixes (sequences forked from one prompt).
+//
+// Sequences [g * group_size, (g + 1) * group_size) hold the same first
+// prefix_lens[g] rows (the shared blocks of a fork). Reading those rows once
+// per sequence reads every shared block group_size times; instead the decode
+// runs in two passes whose softmax states are merged:
+//   1. the shared rows, once per group: the group's group_size x group
+//      queries of a kv head are its virtual heads over the group's first
+//      table row (the multi-token path without the causal rule),
+//   2. each sequence's own rows, [prefix_lens[g], n), through its table,
+// each writing its normalised output and log-sum-exp, then
+//   out = (o1 2^(lse1 - M) + o2 2^(lse2 - M)) / (2^(lse1 - M) + 2^(lse2 - M)),
+// M = max(lse1, lse2), which is the softmax over all n rows.
+
+namespace kvc {
+namespace {
+
+__global__ void lse_combine_kernel(const float* __restrict__ o1, const float* __restrict__ lse1,
+                                   const float* __restrict__ o2, const float* __restrict__ lse2, void* out,
+                                   int out_dtype, int64_t rows, int D) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const float a = lse1[row], b = lse2[row];
+  const float m = fmaxf(a, b);
+  float wa = 0.f, wb = 0.f;
+  if (m != kNegInf) {
+    wa = fast_exp2(a - m);  // a = -inf (no row in that pass): 0
+    wb = fast_exp2(b - m);
+  }
+  const float inv = (wa + wb) > 0.f ? 1.0f / (wa + wb) : 0.f;
+  for (int d = lane * 4; d < D; d += 128) {
+    const float4 x = *reinterpret_cast<const float4*>(o1 + row * D + d);
+    const float4 y = *reinterpret_cast<const float4*>(o2 + row * D + d);
+    const float v[4] = {(x.x * wa + y.x * wb) * inv, (x.y * wa + y.y * wb) * inv, (x.z * wa + y.z * wb) * inv,
+                        (x.w * wa + y.w * wb) * inv};
+    store_out_vec<4>(out, row * D + d, v, out_dtype);
+  }
+}
+
+struct PrefixLayout {
+  size_t inner, o1, o2, l1, l2, total;
+};
+
+kvc_status prefix_layout(int batch, int group_size, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                         int max_blocks, PrefixLayout* L) {
+  if (group_size < 1 || batch % group_size != 0)
+    return fail(KVC_ERR_INVALID_ARG, "batch (%d) must be a multiple of group_size (%d >= 1)", batch, group_size);
+  if (group_size > kMaxTokens) return fail(KVC_ERR_UNSUPPORTED, "group_size %d > %d", group_size, kMaxTokens);
+  if (static_cast<int64_t>(max_blocks) * group_size > (1 << 30))
+    return fail(KVC_ERR_UNSUPPORTED, "max_blocks_per_seq x group_size too large");
+  size_t w1 = 0, w2 = 0;
+  kvc_status s = kvc_decode_workspace_size(batch / group_size, group_size * n_q_heads, n_kv_heads, head_dim,
+                                           block_size, group_size * max_blocks, &w1);
+  if (s != KVC_OK) return s;
+  if ((s = kvc_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks, &w2)) != KVC_OK)
+    return s;
+  const size_t rows = static_cast<size_t>(batch) * n_q_heads;
+  L->inner = 0;
+  L->o1 = align_up(std::max(w1, w2), 256);
+  L->o2 = L->o1 + align_up(rows * head_dim * 4, 256);
+  L->l1 = L->o2 + align_up(rows * head_dim * 4, 256);
+  L->l2 = L->l1 + align_up(rows * 4, 256);
+  L->total = L->l2 + align_up(rows * 4, 256);
+  return KVC_OK;
+}
+
+}  // namespace
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_decode_shared_prefix_workspace_size(int batch, int group_size, int n_q_heads, int n_kv_heads,
+                                                   int head_dim, int block_size, int max_blocks_per_seq,
+                                                   size_t* bytes) {
+  using namespace kvc;
+  clear_error();
+  if (bytes == nullptr) return fail(KVC_ERR_INVALID_ARG, "bytes is NULL");
+  kvc_status s = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq);
+  if (s != KVC_OK) return s;
+  PrefixLayout L;
+  if ((s = prefix_layout(batch, group_size, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, &L)) !=
+      KVC_OK)
+    return s;
+  *bytes = L.total;
+  return KVC_OK;
+}
+
+kvc_status kvc_decode_attention_shared_prefix(const void* q, const void* k_cache, const void* v_cache,
+                                              const int32_t* block_tables, int max_blocks_per_seq,
+                                              const int32_t* context_lens, int batch, int group_size,
+                                              const int32_t* prefix_lens, float scale, int n_q_heads,
+                                              int n_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                              kvc_dtype dtype, void* out, kvc_dtype out_dtype, void* workspace,
+                                              size_t workspace_bytes, kvc_stream stream) {
+  using namespace kvc;
+  clear_error();
+  if (!dtype_ok(dtype) || !dtype_ok(out_dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype");
+  if (prefix_lens == nullptr) return fail(KVC_ERR_INVALID_ARG, "prefix_lens is NULL");
+  kvc_status s = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq);
+  if (s != KVC_OK) return s;
+  PrefixLayout L;
+  if ((s = prefix_layout(batch, group_size, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, &L)) !=
+      KVC_OK)
+    return s;
+  if (workspace == nullptr || workspace_bytes < L.total)
+    return fail(KVC_ERR_WORKSPACE, "shared-prefix decode needs %zu bytes of workspace (got %zu)", L.total,
+                workspace_bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(KVC_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  char* ws = static_cast<char*>(workspace);
+  float* o1 = reinterpret_cast<float*>(ws + L.o1);
+  float* o2 = reinterpret_cast<float*>(ws + L.o2);
+  float* l1 = reinterpret_cast<float*>(ws + L.l1);
+  float* l2 = reinterpret_cast<float*>(ws + L.l2);
+  // pass 1: the shared rows once per group (q, o1 viewed as [groups, group_size, n_q_heads, D])
+  DecodeExtra e1;
+  e1.causal = 0;
+  e1.lse = l1;
+  s = decode_impl(q, k_cache, v_cache, block_tables, group_size * max_blocks_per_seq, prefix_lens,
+                  batch / group_size, scale, n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, 0, dtype, o1,
+                  KVC_F32, ws + L.inner, L.o1, stream, nullptr, nullptr, group_size, &e1);
+  if (s != KVC_OK) return s;
+  // pass 2: each sequence's own rows
+  DecodeExtra e2;
+  e2.lse = l2;
+  e2.row_start = prefix_lens;
+  e2.row_div = group_size;
+  s = decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale, n_q_heads,
+                  n_kv_heads, head_dim, block_size, num_blocks, 0, dtype, o2, KVC_F32, ws + L.inner, L.o1, stream,
+                  nullptr, nullptr, 1, &e2);
+  if (s != KVC_OK) return s;
+  const int64_t rows = static_cast<int64_t>(batch) * n_q_heads;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  lse_combine_kernel<<<static_cast<unsigned int>((rows + 7) / 8), 256, 0, st>>>(o1, l1, o2, l2, out,
+                                                                               static_cast<int>(out_dtype), rows,
+                                                                               head_dim);
+  return finish_call(st);
 }
 
 }  // extern "C"

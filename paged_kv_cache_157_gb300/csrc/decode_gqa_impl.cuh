@@ -84,24 +84,37 @@ __device__ __forceinline__ int first_row(int rows, int window) {
   return (window > 0 && rows > window) ? rows - window : 0;
 }
 
+// First visible row of sequence b: from the window, or, when row_div > 0,
+// the start row row_start[b / row_div] (a shared prefix that another pass
+// covers), capped at `rows`.
+__device__ __forceinline__ int start_row(int rows, int window, const int32_t* row_start, int row_div, int b) {
+  if (row_div > 0) {
+    const int r = __ldg(row_start + b / row_div);
+    return r < 0 ? 0 : (r < rows ? r : rows);
+  }
+  return first_row(rows, window);
+}
+
 // Number of cache blocks sequence b contributes: the blocks holding visible
-// rows (0 if its length is invalid).
+// rows (0 if its length is invalid or no row is visible).
 __device__ __forceinline__ int seq_blocks(const int32_t* lens, int b, int bs, int max_blocks, int window,
-                                          int min_len) {
+                                          int min_len, const int32_t* row_start, int row_div) {
   const int rows = seq_rows(lens, b, bs, max_blocks, min_len);
   if (rows == 0) return 0;
-  return (rows + bs - 1) / bs - first_row(rows, window) / bs;
+  const int r0 = start_row(rows, window, row_start, row_div, b);
+  if (r0 >= rows) return 0;
+  return (rows + bs - 1) / bs - r0 / bs;
 }
 
 // Exclusive prefix sums of seq_blocks over the batch into s_scan[0..B];
 // the whole CTA participates. s_scan needs B + 1 + 32 ints.
 __device__ inline void scan_blocks(const int32_t* lens, int B, int bs, int max_blocks, int window, int min_len,
-                                   int* s_scan) {
+                                   const int32_t* row_start, int row_div, int* s_scan) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int per = (B + nt - 1) / nt;
   const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
   int local = 0;
-  for (int b = b0; b < b1; ++b) local += seq_blocks(lens, b, bs, max_blocks, window, min_len);
+  for (int b = b0; b < b1; ++b) local += seq_blocks(lens, b, bs, max_blocks, window, min_len, row_start, row_div);
   const int lane = tid & 31, wid = tid >> 5;
   int v = local;
 #pragma unroll
@@ -126,7 +139,7 @@ __device__ inline void scan_blocks(const int32_t* lens, int B, int bs, int max_b
   int run = v - local + (wid > 0 ? wsum[wid - 1] : 0);
   for (int b = b0; b < b1; ++b) {
     s_scan[b] = run;
-    run += seq_blocks(lens, b, bs, max_blocks, window, min_len);
+    run += seq_blocks(lens, b, bs, max_blocks, window, min_len, row_start, row_div);
   }
   if (b1 == B && b0 < B) s_scan[B] = run;
   if (B == 0 && tid == 0) s_scan[0] = 0;
@@ -523,7 +536,11 @@ __device__ void merge_unit_warp(const GqaParams& p, int64_t u0, int nb, int64_t 
   }
   float inv[GW];
 #pragma unroll
-  for (int h = 0; h < GW; ++h) inv[h] = 1.0f / warp_sum(Lp[h]);
+  for (int h = 0; h < GW; ++h) {
+    const float lsum = warp_sum(Lp[h]);
+    inv[h] = 1.0f / lsum;
+    if (EXT && p.lse != nullptr && lane == 0) p.lse[out_row(p, seq, kvh, v0 + h)] = M[h] + __log2f(lsum);
+  }
 #pragma unroll
   for (int k = 0; k < NCK; ++k) {
     const int idx = lane + 32 * k;
@@ -571,8 +588,12 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   constexpr bool kFp8 = sizeof(T) == 1;
   const int wnd = EXT ? p.window : 0;   // sliding window rows (0: all)
   const int n_tok = EXT ? p.n_tok : 1;  // new query tokens per sequence
-  const int tm = n_tok - 1;             // rows hidden from the first of them
+  const bool causal = !EXT || p.causal != 0;
+  const int tm = causal ? n_tok - 1 : 0;  // rows hidden from the first of them
+  const int min_len = causal ? n_tok : 1;  // shortest valid context
   const bool multi = EXT && n_tok > 1;
+  const int32_t* row_start = EXT ? p.row_start : nullptr;
+  const int row_div = EXT ? p.row_div : 0;
   constexpr int VSB = kFp8 ? 4 : 0;  // V-scale bytes per cached row
   const GqaSmem L = gqa_smem_layout(sizeof(T), sizeof(TQ), VSB, D, GH, p.block_size, hc, p.stages, p.batch);
   unsigned char* s_stage = smem + L.stage_off;
@@ -627,24 +648,31 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     const int j = static_cast<int>((pos - seq * per_seq) % p.max_blocks) + tid * 32;
     if (seq < B && j < p.max_blocks) prefetch_l2(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks + j);
   }
-  scan_blocks(p.context_lens, B, bs, p.max_blocks, wnd, n_tok, s_scan);  // ends with a CTA barrier
+  scan_blocks(p.context_lens, B, bs, p.max_blocks, wnd, min_len, row_start, row_div, s_scan);  // ends with a CTA barrier
   const int64_t N = static_cast<int64_t>(HN) * s_scan[B];
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
 
   if (blockIdx.x == 0) {
     // Validate every length once; in the split mode CTA 0 also writes the
-    // zero outputs of sequences whose length is invalid (no CTA visits them).
+    // zero outputs of sequences with no visible row (an invalid length, or
+    // every row before the start row): no CTA visits them.
+    int empty = 0;
     for (int b = tid; b < B; b += blockDim.x) {
       const int n = __ldg(p.context_lens + b);
-      if (n < n_tok || n > bs * p.max_blocks) set_flag(p.err, 0x2u);
+      if (n < min_len || n > bs * p.max_blocks) set_flag(p.err, 0x2u);
+      if (row_div > 0 && __ldg(row_start + b / row_div) > n) set_flag(p.err, 0x2u);
+      empty |= (s_scan[b + 1] == s_scan[b]) ? 1 : 0;
     }
-    if (!p.unit_mode) {
+    if (__syncthreads_or(empty) && !p.unit_mode) {
       const int rows = n_tok * p.n_q_heads * D;  // outputs of one sequence
       for (int b = 0; b < B; ++b) {
-        if (__ldg(p.context_lens + b) >= n_tok) continue;
+        if (s_scan[b + 1] != s_scan[b]) continue;
         for (int idx = tid; idx < rows; idx += blockDim.x)
           store_out(p.out, static_cast<int64_t>(b) * rows + idx, 0.f, p.out_dtype);
+        if (EXT && p.lse != nullptr)
+          for (int idx = tid; idx < n_tok * p.n_q_heads; idx += blockDim.x)
+            p.lse[static_cast<int64_t>(b) * n_tok * p.n_q_heads + idx] = kNegInf;
       }
     }
   }
@@ -656,7 +684,8 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     const int idx = static_cast<int>(c - static_cast<int64_t>(seq) * HN);
     const int nb = s_scan[seq + 1] - s_scan[seq];
     if (nb == 0) {
-      // invalid length: zero output for this CTA's heads
+      // no visible row (invalid length, or all before the start row): zero
+      // output for this CTA's heads
       if (active) {
         const int chunk = idx / p.n_hsub, hsub = idx - chunk * p.n_hsub;
         const int kvh = chunk * hc + kh, v0 = hsub * GH + hw * GW;
@@ -665,6 +694,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
                                 : (static_cast<int64_t>(seq) * p.n_q_heads + kvh * p.group + v0) * D + i;
           store_out(p.out, o, 0.f, p.out_dtype);
         }
+        if (EXT && p.lse != nullptr && lane < GW) p.lse[out_row(p, seq, kvh, v0 + lane)] = kNegInf;
       }
       return;
     }
@@ -694,7 +724,9 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     if (pos < hi) {
       const BlockPos bp = locate_block(pos, HN, s_scan, B, p.n_hsub);
       // bp.j counts the sequence's visible blocks; the table is indexed from block 0
-      const int j0 = first_row(seq_rows(p.context_lens, bp.seq, bs, p.max_blocks, n_tok), wnd) / bs;
+      const int j0 =
+          start_row(seq_rows(p.context_lens, bp.seq, bs, p.max_blocks, min_len), wnd, row_start, row_div, bp.seq) /
+          bs;
       const int phys = __ldg(p.block_tables + static_cast<int64_t>(bp.seq) * p.max_blocks + j0 + bp.j);
       if (phys >= 0 && phys < p.num_blocks) src = phys * p.n_kv_heads + bp.chunk * hc;
       if (pos == lo || bp.j == 0)
@@ -781,13 +813,13 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
       // ---- segment: the part of one unit inside [lo, hi)
       const BlockPos sg = locate_block(gb, HN, s_scan, B, p.n_hsub);
       const int seg_len = static_cast<int>(((sg.nb - sg.j) < (hi - gb)) ? (sg.nb - sg.j) : (hi - gb));
-      const int n_rows = seq_rows(p.context_lens, sg.seq, bs, p.max_blocks, n_tok);
-      const int r0 = first_row(n_rows, wnd);  // first visible row
+      const int n_rows = seq_rows(p.context_lens, sg.seq, bs, p.max_blocks, min_len);
+      const int r0 = start_row(n_rows, wnd, row_start, row_div, sg.seq);  // first visible row
       const int j0 = r0 / bs;                      // table index of the first visible block
       const int kvh = sg.chunk * hc + kh;          // kv head of this warp
       const int v0 = sg.hsub * GH + hw * GW;       // first (virtual) query head of this warp
       const int hq0 = kvh * p.group + v0;          // its query head (single token)
-      const int dh = EXT ? tm - (v0 + geo.h_lane) / p.group : 0;  // last rows the lane's head may not see
+      const int dh = (EXT && causal) ? tm - (v0 + geo.h_lane) / p.group : 0;  // last rows the lane's head may not see
 
       WarpState<T, D, GW> st;
       for (int t = 0; t < seg_len; ++t, ++cpos) {
@@ -925,6 +957,10 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
             for (int d = 0; d < C::VD; ++d) ov[h][d] *= inv;
             store_out_vec<C::VD>(p.out, ob, ov[h], p.out_dtype);
           }
+        }
+        if (EXT && p.lse != nullptr && lane == 0) {
+#pragma unroll
+          for (int h = 0; h < GW; ++h) p.lse[out_row(p, sg.seq, kvh, v0 + h)] = st.m[h] + __log2f(lw[h]);
         }
       } else {
         // Record (max, sum, unnormalised output) for this warp's heads; the

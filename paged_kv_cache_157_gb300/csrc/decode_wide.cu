@@ -97,6 +97,8 @@ struct Params {
   int64_t num_blocks;
   int batch, n_q_heads, n_kv_heads, group, n_tok, qn;  // qn = n_tok * group queries per kv head
   int block_size, max_blocks, out_dtype, unit_mode;
+  int causal;                    // n_tok > 1: token t sees rows up to n - n_tok + t (0: every row)
+  float* lse;                    // non-NULL: per output row, max + log2(sum) in log2 units
   float qscale;                  // scale * log2(e)
 };
 
@@ -104,7 +106,7 @@ struct Params {
 
 __device__ __forceinline__ int seq_rows(const Params& p, int b) {
   const int n = __ldg(p.context_lens + b);
-  if (n < p.n_tok || n < 1) return 0;
+  if ((p.causal && n < p.n_tok) || n < 1) return 0;
   const int cap = p.block_size * p.max_blocks;
   return n < cap ? n : cap;
 }
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (blockIdx.x == 0) {
     for (int b = tid; b < p.batch; b += blockDim.x) {
       const int n = __ldg(p.context_lens + b);
-      if (n < p.n_tok || n < 1 || n > bs * p.max_blocks) set_flag(p.err, 0x2u);
+      if ((p.causal && n < p.n_tok) || n < 1 || n > bs * p.max_blocks) set_flag(p.err, 0x2u);
     }
   }
   fence_before();
@@ -302,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (seq_tiles(p, seq) == 0) {
         for (int i = tid; i < p.qn * kD; i += blockDim.x)
           store_out(p.out, out_row(p, seq, kvh, i / kD) * kD + i % kD, 0.f, p.out_dtype);
+        if (p.lse != nullptr && tid < p.qn) p.lse[out_row(p, seq, kvh, tid)] = -__builtin_huge_valf();
       }
     } else if (blockIdx.x == 0) {
       int bad = 0;
@@ -311,6 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (seq_tiles(p, b) != 0) continue;
           for (int i = tid; i < row_elems; i += blockDim.x)
             store_out(p.out, static_cast<int64_t>(b) * row_elems + i, 0.f, p.out_dtype);
+          if (p.lse != nullptr)
+            for (int i = tid; i < p.n_tok * p.n_q_heads; i += blockDim.x)
+              p.lse[static_cast<int64_t>(b) * p.n_tok * p.n_q_heads + i] = -__builtin_huge_valf();
         }
       }
     }
@@ -502,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
           const int tok = q / p.group;
-          const bool vis = q < p.qn && r < rows_left - (p.n_tok - 1 - tok);
+          const bool vis = q < p.qn && r < rows_left - (p.causal ? p.n_tok - 1 - tok : 0);
           s[q] = vis ? s[q] * p.qscale : -__builtin_huge_valf();
           need |= s[q] > m[q] + 8.0f;
         }
@@ -591,8 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t rec = c * 2 + sg.which;
       if (whole) {
 #pragma unroll
-        for (int q = 0; q < NQ; ++q)
+        for (int q = 0; q < NQ; ++q) {
           if (q < p.qn) store_out(p.out, out_row(p, sg.seq, sg.kvh, q) * kD + r, o[q] / l[q], p.out_dtype);
+          if (p.lse != nullptr && r == q && q < p.qn) p.lse[out_row(p, sg.seq, sg.kvh, q)] = m[q] + __log2f(l[q]);
+        }
       } else {
 #pragma unroll
         for (int q = 0; q < NQ; ++q) p.rec_o[(rec * NQ + q) * kD + r] = o[q];
@@ -661,8 +669,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
 #pragma unroll
-          for (int q = 0; q < NQ; ++q)
+          for (int q = 0; q < NQ; ++q) {
             if (q < p.qn) store_out(p.out, out_row(p, sg.seq, sg.kvh, q) * kD + r, O[q] / L[q], p.out_dtype);
+            if (p.lse != nullptr && r == q && q < p.qn) p.lse[out_row(p, sg.seq, sg.kvh, q)] = M[q] + __log2f(L[q]);
+          }
           if (tid == 0) p.counters[unit] = 0u;
         }
       }
@@ -771,6 +781,8 @@ kvc_status wide_decode(const WideArgs& a, DeviceInfo* dev) {
   p.group = group;
   p.n_tok = a.n_tok;
   p.qn = qn;
+  p.causal = a.causal;
+  p.lse = a.lse;
   p.block_size = a.block_size;
   p.max_blocks = a.max_blocks;
   p.out_dtype = static_cast<int>(a.out_dtype);
