@@ -393,6 +393,8 @@ def run_variant(kvc, name, flush, steps):
         return r
     if name == "gqa_fp8_b32_ctx4096":
         return measure_fp8(kvc, flush, steps)
+    if name == "mha_shared_prefix_8x8_cascade":
+        return measure_shared_prefix(kvc, flush, steps)
     if name == "gqa_spec4_b32_ctx4096":
         return measure_multi(kvc, flush, steps, 4)
     if name == "cow_copy_blocks_2048":
@@ -409,7 +411,7 @@ def run_variant(kvc, name, flush, steps):
 
 VARIANTS = ("gqa_b32_ctx4096", "mha_shared_prefix_8x8", "gqa_long_splitk", "gqa_ragged_17_31_32", "tiny_mha_fp32",
             "mla_deepseek_v2", "gqa_window_b32_ctx4096_w1024", "cow_copy_blocks_2048", "gqa_fp8_b32_ctx4096",
-            "gqa_spec4_b32_ctx4096")
+            "gqa_spec4_b32_ctx4096", "mha_shared_prefix_8x8_cascade")
 
 
 def variants(kvc, flush, steps):
@@ -507,6 +509,40 @@ def measure_multi(kvc, flush, steps, T=4):
             "query_tokens_per_s": round(B * T / (dms / 1e3), 1),
             "ms_per_step": round(statistics.mean(step_ms), 5), "bytes_per_step": dec_b,
             "note": f"{T} new tokens per sequence attend causally in one pass over the pages"}
+
+
+def measure_shared_prefix(kvc, flush, steps):
+    """Config 3 through kvc_decode_attention_shared_prefix: 8 prompts x 2048 tokens forked 8 ways + 256 private
+    tokens each, 32 heads x 128, fp16; the step appends the 64 new tokens (private blocks) and decodes; bytes
+    count each shared block once (unique physical bytes)."""
+    import torch
+    from paged_kv_cache_157_gb300 import workloads as W
+    c = W.shared_case(8, 8, 2048, 256, 32, 128, 16, "f16", 44, device="cuda")
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in c.items()}
+    lens = c["context_lens"].tolist()
+    B = 64
+    slots = kvc.slots_from_tables(c["block_tables"], 16, list(range(B)), [n - 1 for n in lens]).cuda()
+    out = torch.empty((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    ws = kvc.shared_prefix_workspace(B, 8, 32, 32, 128, 16, c["block_tables"].shape[1])
+    prefix = torch.full((8,), 2048, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(128)
+
+    class S:
+        def append(self):
+            kvc.append(d["k_new"], d["v_new"], slots, d["k_cache"], d["v_cache"])
+
+        def decode(self):
+            kvc.decode_attention_shared_prefix(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                               d["context_lens"], 8, prefix, scale, out, ws)
+
+    step_ms, dec_ms, _, _ = time_steps(S(), steps, 5, flush)
+    unique = 8 * 2048 + 64 * 256
+    dec_b, _ = step_bytes(lens, 32, 32, 128, 16, 2, 2, unique)
+    dms = statistics.mean(dec_ms)
+    return {"decode_ms": round(dms, 5), "decode_gbps": round(dec_b / dms / 1e6, 1),
+            "frac_of_8tbs": round(dec_b / dms / 1e6 / NOMINAL_HBM_GBS, 4),
+            "ms_per_step": round(statistics.mean(step_ms), 5), "bytes_per_step": dec_b,
+            "note": "kvc_decode_attention_shared_prefix (shared prompt rows read once per group); unique bytes"}
 
 
 def measure_copy_blocks(kvc, flush, steps):
