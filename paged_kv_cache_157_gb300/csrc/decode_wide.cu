@@ -77,7 +77,8 @@ enum {
   B_QFULL = 0, B_QEMPTY, B_FULL0, B_EMPTY0 = B_FULL0 + kStages, B_SFULL0 = B_EMPTY0 + kStages,
   B_SEMPTY0 = B_SFULL0 + 2, B_PFULL = B_SEMPTY0 + 2, B_PEMPTY, B_OFREE, B_FINAL, B_COUNT
 };
-__host__ __device__ constexpr uint32_t off_bar(int nq) { return off_red(nq) + 4 * nq * 4; }
+__host__ __device__ constexpr uint32_t off_hide(int nq) { return off_red(nq) + 4 * nq * 4; }
+__host__ __device__ constexpr uint32_t off_bar(int nq) { return off_hide(nq) + nq * 4; }
 __host__ __device__ constexpr uint32_t off_misc(int nq) { return off_bar(nq) + B_COUNT * 8; }
 __host__ __device__ constexpr uint32_t off_rec(int nq) { return off_misc(nq) + 16; }
 __host__ __device__ constexpr uint32_t off_scan(int nq) { return off_rec(nq) + kMergeChunk * 4; }
@@ -243,6 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sm = smem_raw + (base - raw_addr);
   const uint32_t sStage = base + kOffStage, sQ = base + kOffQ, sP = base + off_p(NQ);
   float* s_red = reinterpret_cast<float*>(sm + off_red(NQ));  // [4][NQ]
+  // per query: rows it may not see at the end of a sequence (its later new
+  // tokens), or a huge value for padding queries
+  int* s_hide = reinterpret_cast<int*>(sm + off_hide(NQ));
   const uint32_t bar0 = base + off_bar(NQ);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + off_bar(NQ));
   volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(sm + off_misc(NQ));
@@ -257,6 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t c = blockIdx.x;
   const int bs = p.block_size;
 
+  if (tid < NQ)
+    s_hide[tid] = tid < p.qn ? (p.causal ? p.n_tok - 1 - tid / p.group : 0) : (1 << 30);
   if (tid == 0) {
     *s_abort = 0;
     for (int i = 0; i < B_COUNT; ++i) {
@@ -507,8 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool need = false;
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-          const int tok = q / p.group;
-          const bool vis = q < p.qn && r < rows_left - (p.causal ? p.n_tok - 1 - tok : 0);
+          const bool vis = r + s_hide[q] < rows_left;
           s[q] = vis ? s[q] * p.qscale : -__builtin_huge_valf();
           need |= s[q] > m[q] + 8.0f;
         }
