@@ -17,6 +17,9 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4* __restrict__ s
                                                      const int64_t* __restrict__ slots, int64_t num_tokens,
                                                      int64_t num_slots, int block_size, int n_heads, int row_chunks,
                                                      unsigned int* err) {
+  // a decode launched behind this kernel may start its prologue now; it
+  // waits for this grid to finish before it reads any cached row
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t per_token = static_cast<int64_t>(n_heads) * row_chunks;
   const int64_t total = num_tokens * per_token;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;

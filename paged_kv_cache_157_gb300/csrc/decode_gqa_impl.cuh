@@ -790,6 +790,10 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   // warp waits for another except through the "full" barriers.
   const int n_first = total < S ? total : S;
   if (w == 0) {
+    // Launched right behind the append of this step (programmatic stream
+    // serialisation), the prologue above overlapped it; the cached rows are
+    // read only after it has finished. Every later copy follows these.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = 0; i < n_first; ++i) {
       const int src = __shfl_sync(full, w_src0, i);
       const int qo = __shfl_sync(full, w_q0, i);

@@ -18,7 +18,20 @@ static kvc_status gqa_run(const GqaParams& p, int grid, size_t smem, cudaStream_
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
     return KVC_OK;
   }
-  k<<<grid, kGqaWarps * 32, smem, stream>>>(p);
+  // The kernel may start while the previous kernel in the stream (the append
+  // of this step) is still running; it waits for it before reading the cache.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGqaWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k, p);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gqa)");
   return KVC_OK;
 }
 

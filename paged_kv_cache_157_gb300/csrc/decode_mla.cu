@@ -470,6 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // launched behind the append of this step: read cached rows only after it
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       uint32_t g = 0, seg_i = 0;
       uint32_t issued[kStages] = {};
       bool q_pending = false;
@@ -1016,7 +1018,19 @@ kvc_status kvc_decode_attention_mla(const void* q_absorbed, const void* latent_c
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(mla)");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  mla::mla_decode_kernel<<<2 * G2, mla::kThreads, smem, st>>>(tq, tc, p);
+  // may start while the append of this step still runs (it waits before reading the cache)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * G2);
+  cfg.blockDim = dim3(mla::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel, tq, tc, p);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(mla)");
   return finish_call(st);
 }
 

@@ -333,7 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     // The whole warp: lane i reads the table entry of page i of the next tile
     // before the stage is free (hiding that load), lane 0 arms the stage's
-    // barrier, then lane i issues the four copies of page i.
+    // barrier, then lane i issues the four copies of page i. Launched behind
+    // the append of this step, the kernel reads cached rows only once that
+    // grid has finished.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     uint32_t g = 0;
     uint32_t issued[kStages] = {};
     Segment sg;
@@ -812,7 +815,18 @@ kvc_status wide_decode(const WideArgs& a, DeviceInfo* dev) {
   auto launch = [&](auto kernel) -> kvc_status {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(wide)");
-    kernel<<<grid, kThreads, smem, a.stream>>>(tk, tv, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, tk, tv, p);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(wide)");
     return KVC_OK;
   };
   kvc_status s;
