@@ -1,4 +1,4 @@
-"""FP8 (e4m3) KV-cache quantisation (oracle; test infrastructure only).
+"""FP8 (e4m3) and INT8 KV-cache quantisation (oracle; test infrastructure only).
 
 "KV-Cache——为什么AI回复越来越快" section 08 (KV-Cache quantisation): the FP16
 K and V matrices are stored as FP8 (1 byte), halving the cache; V is
@@ -126,4 +126,71 @@ def dequantized_pools(k_cache, v_cache, v_scale_pool, k_scale):
     """float64 K and V pools the quantised cache stands for."""
     K = decode_e4m3(k_cache) * np.asarray(k_scale, dtype=np.float64)[None, :, None, :]
     V = decode_e4m3(v_cache) * np.asarray(v_scale_pool, dtype=np.float64)[..., None]
+    return K, V
+
+
+# ---------------------------------------------------------------- INT8
+#
+# The same section names INT8 next to FP8 (one byte per element, V scaled per
+# token, K per channel). Readings where the page fixes nothing:
+#
+# * symmetric codes in [-127, 127] (-128 is never produced, so the range is
+#   symmetric like the scales), code = round(x) with ties to even, values
+#   beyond +-127 saturate;
+# * K: code = int8(k / k_scale[h, d]) with caller-given per-channel scales;
+#   V: s = max_d |v[d]| / 127 per (token, kv head) (1.0 for an all-zero row),
+#   code = int8(v / s); divisions in float32;
+# * decode attends over k = code * k_scale and v = code * s.
+
+MAX_INT8 = 127.0
+
+
+def encode_int8(x) -> np.ndarray:
+    """Round float32 values to int8 codes: nearest, ties to even, saturating at +-127."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    return np.clip(np.rint(x), -MAX_INT8, MAX_INT8).astype(np.int8)
+
+
+def quantize_k_int8(k, k_scale) -> np.ndarray:
+    """k [T, Hkv, D], k_scale [Hkv, D] -> int8 codes [T, Hkv, D]."""
+    q = np.asarray(k, dtype=np.float32) / np.asarray(k_scale, dtype=np.float32)[None]
+    return encode_int8(q.astype(np.float32))
+
+
+def v_token_scale_int8(v) -> np.ndarray:
+    """v [T, Hkv, D] -> per (token, kv head) scale [T, Hkv] = max |v| / 127 (float32; 1 for zero rows)."""
+    m = np.max(np.abs(np.asarray(v, dtype=np.float32)), axis=-1)
+    s = (m / np.float32(MAX_INT8)).astype(np.float32)
+    return np.where(m > 0, s, np.float32(1.0)).astype(np.float32)
+
+
+def quantize_v_int8(v, s) -> np.ndarray:
+    q = np.asarray(v, dtype=np.float32) / np.asarray(s, dtype=np.float32)[..., None]
+    return encode_int8(q.astype(np.float32))
+
+
+def append_int8(k, v, slot_mapping, k_cache, v_cache, v_scale_pool, k_scale):
+    """Quantise and write token t's K/V at slot_mapping[t] (negative: skip); int8 pools, float32 V scales."""
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    vs = np.array(v_scale_pool, copy=True)
+    bs = kc.shape[2]
+    kq = quantize_k_int8(k, k_scale)
+    s = v_token_scale_int8(v)
+    vq = quantize_v_int8(v, s)
+    for t, slot in enumerate(np.asarray(slot_mapping).reshape(-1)):
+        slot = int(slot)
+        if slot < 0:
+            continue
+        blk, off = slot // bs, slot % bs
+        kc[blk, :, off, :] = kq[t]
+        vc[blk, :, off, :] = vq[t]
+        vs[blk, :, off] = s[t]
+    return kc, vc, vs
+
+
+def dequantized_pools_int8(k_cache, v_cache, v_scale_pool, k_scale):
+    """float64 K and V pools the int8 cache stands for."""
+    K = np.asarray(k_cache, dtype=np.int8).astype(np.float64) * np.asarray(k_scale, dtype=np.float64)[None, :, None, :]
+    V = np.asarray(v_cache, dtype=np.int8).astype(np.float64) * np.asarray(v_scale_pool, dtype=np.float64)[..., None]
     return K, V

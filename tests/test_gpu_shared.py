@@ -158,3 +158,28 @@ def test_prefix_longer_than_a_member_is_flagged(kvc):
                                        dev["context_lens"], 4, torch.full((1,), 100, dtype=torch.int32).cuda(),
                                        0.1, out, ws)
     assert kvc.get_error_flags() & kvc.FLAG_BAD_LEN
+
+
+def test_config3_full_size_sampled_against_oracle(kvc):
+    # 8 prompts x 2048 tokens forked 8 ways + 256 private tokens, 32 heads x 128, fp16: both the plain decode and
+    # the shared-prefix decode against the oracle on sampled (sequence, head) pairs
+    from gpu_helpers import oracle_decode_sampled
+    case = W.shared_case(8, 8, 2048, 256, 32, 128, 16, "f16", 44)
+    dev = device_case(case)
+    B = 64
+    scale = 1.0 / math.sqrt(128)
+    plain = torch.empty((B, 32, 128), dtype=torch.float32, device="cuda")
+    kvc.decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"], scale,
+                         plain, kvc.new_decode_workspace(B, 32, 32, 128, 16, case["block_tables"].shape[1]))
+    shared = torch.empty_like(plain)
+    ws = kvc.shared_prefix_workspace(B, 8, 32, 32, 128, 16, case["block_tables"].shape[1])
+    kvc.decode_attention_shared_prefix(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                                       dev["context_lens"], 8, torch.full((8,), 2048, dtype=torch.int32).cuda(),
+                                       scale, shared, ws)
+    torch.cuda.synchronize()
+    pairs = [(0, 0), (7, 31), (8, 5), (33, 17), (63, 30)]
+    ref = oracle_decode_sampled(case, scale, pairs)
+    for (i, h), r in ref.items():
+        assert float(np.max(np.abs(f64(plain[i, h]) - r))) <= TOL["f16"], ("plain", i, h)
+        assert float(np.max(np.abs(f64(shared[i, h]) - r))) <= TOL["f16"], ("shared", i, h)
+    assert kvc.get_error_flags() == 0

@@ -133,3 +133,17 @@ def test_wide_long_context_sampled(kvc):
     for (i, h), r in ref.items():
         assert float(np.max(np.abs(f64(out[i, h]) - r))) <= TOL["bf16"]
     assert kvc.get_error_flags() == 0
+
+
+def test_config4_long_splitk_full_size_sampled(kvc):
+    # the long split-K configuration at full size, in the launch configuration bench.py times: batch 4, 64 q / 8 kv
+    # heads, contexts 32768 / 65536 / 131072 / 131072, block 16 (tensor-core kernel, many split-K records per unit)
+    lens = [32768, 65536, 131072, 131072]
+    case = W.gqa_case(4, 64, 8, 128, 16, lens, "bf16", seed=45)
+    dev = device_case(case)
+    out = run_decode(kvc, dev, 1.0 / math.sqrt(128))
+    pairs = [(0, 0), (1, 31), (2, 8), (3, 63), (3, 1)]
+    ref = oracle_decode_sampled(case, 1.0 / math.sqrt(128), pairs)
+    for (i, h), r in ref.items():
+        assert float(np.max(np.abs(f64(out[i, h]) - r))) <= TOL["bf16"], (i, h)
+    assert kvc.get_error_flags() == 0
