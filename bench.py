@@ -402,6 +402,8 @@ def run_variant(kvc, name, flush, steps):
         return r
     if name == "gqa_fp8_b32_ctx4096":
         return measure_fp8(kvc, flush, steps)
+    if name == "gqa_int8_b32_ctx4096":
+        return measure_fp8(kvc, flush, steps, int8=True)
     if name == "mha_shared_prefix_8x8_cascade":
         return measure_shared_prefix(kvc, flush, steps)
     if name == "gqa_spec4_b32_ctx4096":
@@ -420,7 +422,7 @@ def run_variant(kvc, name, flush, steps):
 
 VARIANTS = ("gqa_b32_ctx4096", "mha_shared_prefix_8x8", "gqa_long_splitk", "gqa_ragged_17_31_32", "tiny_mha_fp32",
             "mla_deepseek_v2", "gqa_window_b32_ctx4096_w1024", "cow_copy_blocks_2048", "gqa_fp8_b32_ctx4096",
-            "gqa_spec4_b32_ctx4096", "mha_shared_prefix_8x8_cascade")
+            "gqa_int8_b32_ctx4096", "gqa_spec4_b32_ctx4096", "mha_shared_prefix_8x8_cascade")
 
 
 def variants(kvc, flush, steps):
@@ -450,13 +452,15 @@ def measure_tiny(kvc, flush, steps):
             "note": "latency-bound: one sequence of 69 tokens"}
 
 
-def measure_fp8(kvc, flush, steps):
-    """Llama-3-8B-shaped layer over an FP8 e4m3 cache (batch 32, lengths 4096): kvc_append_fp8 of the new tokens +
-    kvc_decode_attention_fp8 (bf16 queries and output). Bytes: 1 per cached K/V element + 4 per (row, kv head) of
-    V scales, plus q, out, tables, lengths."""
+def measure_fp8(kvc, flush, steps, int8=False):
+    """Llama-3-8B-shaped layer over a one-byte cache, FP8 e4m3 or INT8 (batch 32, lengths 4096): the quantising
+    append of the new tokens + the one-byte decode (bf16 queries and output). Bytes: 1 per cached K/V element + 4
+    per (row, kv head) of V scales, plus q, out, tables, lengths."""
     import torch
     from paged_kv_cache_157_gb300 import workloads as W
-    c = W.fp8_case(32, 32, 8, 128, 16, [4096] * 32, 94, device="cuda")
+    c = (W.int8_case if int8 else W.fp8_case)(32, 32, 8, 128, 16, [4096] * 32, 94, device="cuda")
+    append_fn = kvc.append_int8 if int8 else kvc.append_fp8
+    decode_fn = kvc.decode_attention_int8 if int8 else kvc.decode_attention_fp8
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in c.items()}
     lens = c["context_lens"].tolist()
     B, hq, hkv, D, bs = 32, 32, 8, 128, 16
@@ -467,11 +471,11 @@ def measure_fp8(kvc, flush, steps):
 
     class S:
         def append(self):
-            kvc.append_fp8(d["k_new"], d["v_new"], slots, d["k_cache"], d["v_cache"], d["v_scale"], d["k_scale"])
+            append_fn(d["k_new"], d["v_new"], slots, d["k_cache"], d["v_cache"], d["v_scale"], d["k_scale"])
 
         def decode(self):
-            kvc.decode_attention_fp8(d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
-                                     d["block_tables"], d["context_lens"], scale, out, ws)
+            decode_fn(d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"], d["block_tables"],
+                      d["context_lens"], scale, out, ws)
 
     step_ms, dec_ms, _, _ = time_steps(S(), steps, 5, flush)
     rows = sum(lens)

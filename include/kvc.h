@@ -154,6 +154,18 @@ kvc_status kvc_append_fp8(const void* k, const void* v, const int64_t* slot_mapp
                           void* k_cache, void* v_cache, float* v_scale, const float* k_scale, int64_t num_blocks,
                           int block_size, int n_kv_heads, int head_dim, kvc_dtype dtype, kvc_stream stream);
 
+/* INT8 KV cache append: as kvc_append_fp8 with int8 codes (int8 pools
+ * [num_blocks, n_kv_heads, block_size, head_dim]): K code = q(k / k_scale[h, d]),
+ * V code = q(v / s) with s = max_d |v| / 127 (1 for an all-zero row) written
+ * to v_scale [num_blocks, n_kv_heads, block_size] fp32; q rounds an fp32 value
+ * to the nearest integer, ties to even, and saturates at +-127 (symmetric:
+ * -128 is never written). Divisions are fp32, correctly rounded. Same slot,
+ * flag and error rules as kvc_append_fp8. Source: "KV-Cache——为什么AI回复越来越快"
+ * section 08 (KV-Cache quantisation, INT8 named beside FP8). */
+kvc_status kvc_append_int8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                           void* k_cache, void* v_cache, float* v_scale, const float* k_scale, int64_t num_blocks,
+                           int block_size, int n_kv_heads, int head_dim, kvc_dtype dtype, kvc_stream stream);
+
 /* Copy-on-write block copy inside one pool: for i < n_pairs, block
  * pairs[2i + 1] becomes a byte copy of block pairs[2i]. cache: device pool of
  * num_blocks blocks of block_bytes bytes each (for a K or V pool,
@@ -290,6 +302,19 @@ kvc_status kvc_decode_attention_fp8(const void* q, const void* k_cache, const vo
                                     int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, void* out,
                                     kvc_dtype out_dtype, void* workspace, size_t workspace_bytes,
                                     kvc_stream stream);
+
+/* INT8 KV cache decode: as kvc_decode_attention_fp8 over the caches written
+ * by kvc_append_int8, attending k = code * k_scale[h, d] and
+ * v = code * v_scale[row]. q is bf16 [batch, n_q_heads, head_dim]; head_dim
+ * 64, 128 or 256; k_scale and v_scale 16-byte aligned. Same tables, lengths,
+ * workspace and error rules as kvc_decode_attention. Source:
+ * "KV-Cache——为什么AI回复越来越快" section 08 (KV-Cache quantisation). */
+kvc_status kvc_decode_attention_int8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                                     const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int batch, float scale, int n_q_heads,
+                                     int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, void* out,
+                                     kvc_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                     kvc_stream stream);
 
 /* kvc_decode_attention for callers that cannot allocate device memory.
  *

@@ -20,6 +20,7 @@ __all__ = [
     "KvcError", "KvcLibraryMissing", "raw", "lib_path", "symbols",
     "append", "append_latent", "decode_workspace_size", "decode_attention", "decode_attention_static",
     "decode_attention_window", "copy_blocks", "append_fp8", "decode_attention_fp8",
+    "append_int8", "decode_attention_int8",
     "decode_mla_workspace_size", "decode_attention_mla", "set_option", "get_option",
     "get_error_flags", "BlockPool", "slots_from_tables",
     "F32", "F16", "BF16", "FLAG_BAD_BLOCK", "FLAG_BAD_LEN", "FLAG_BAD_SLOT", "FLAG_TIMEOUT", "FLAG_WORKSPACE",
@@ -81,6 +82,9 @@ SIGNATURES = {
     "kvc_append_fp8": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp]),
     "kvc_decode_attention_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32,
                                         _i64, _vp, _i32, _vp, _sz, _vp]),
+    "kvc_append_int8": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp]),
+    "kvc_decode_attention_int8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32,
+                                         _i64, _vp, _i32, _vp, _sz, _vp]),
     "kvc_seq_free": (_i32, [_vp, _i64]),
     "kvc_seq_length": (_i32, [_vp, _i64, _i64p]),
     "kvc_block_refcount": (_i32, [_vp, _i64, _i32p]),
@@ -488,34 +492,30 @@ def copy_blocks(cache, pairs, stream=None):
            "kvc_copy_blocks")
 
 
-def append_fp8(k, v, slot_mapping, k_cache, v_cache, v_scale, k_scale, stream=None):
-    """kvc_append_fp8. k/v [T, Hkv, D] (f32/f16/bf16); k_cache/v_cache uint8 [num_blocks, Hkv, bs, D];
-    v_scale fp32 [num_blocks, Hkv, bs] (written); k_scale fp32 [Hkv, D]."""
+def _append_q8(fn, code_dtype, k, v, slot_mapping, k_cache, v_cache, v_scale, k_scale, stream):
     torch = _torch()
     for t, n in ((k, "k"), (v, "v")):
         _require(t, n)
     _require(slot_mapping, "slot_mapping", torch.int64)
-    _require(k_cache, "k_cache", torch.uint8)
-    _require(v_cache, "v_cache", torch.uint8)
+    _require(k_cache, "k_cache", code_dtype)
+    _require(v_cache, "v_cache", code_dtype)
     _require(v_scale, "v_scale", torch.float32)
     _require(k_scale, "k_scale", torch.float32)
     T, hkv, d = k.shape
     nb, hkv2, bs, d2 = k_cache.shape
     if (hkv2, d2) != (hkv, d) or tuple(v_scale.shape) != (nb, hkv, bs) or tuple(k_scale.shape) != (hkv, d):
         raise ValueError("shape mismatch")
-    _check(raw().kvc_append_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
-                                _ptr(v_scale), _ptr(k_scale), nb, bs, hkv, d, _dtype_code(k), _stream(stream)),
-           "kvc_append_fp8")
+    _check(getattr(raw(), fn)(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache), _ptr(v_scale),
+                              _ptr(k_scale), nb, bs, hkv, d, _dtype_code(k), _stream(stream)), fn)
 
 
-def decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
-                         workspace=None, stream=None):
-    """kvc_decode_attention_fp8: q bf16 [B, Hq, D] over FP8 caches written by append_fp8."""
+def _decode_q8(fn, code_dtype, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
+               workspace, stream):
     torch = _torch()
     _require(q, "q", torch.bfloat16)
     _require(out, "out")
-    _require(k_cache, "k_cache", torch.uint8)
-    _require(v_cache, "v_cache", torch.uint8)
+    _require(k_cache, "k_cache", code_dtype)
+    _require(v_cache, "v_cache", code_dtype)
     _require(k_scale, "k_scale", torch.float32)
     _require(v_scale, "v_scale", torch.float32)
     _require(block_tables, "block_tables", torch.int32)
@@ -528,7 +528,32 @@ def decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, co
     if workspace is not None:
         _require(workspace, "workspace")
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
-    _check(raw().kvc_decode_attention_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                                          _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B,
-                                          float(scale), hq, hkv, d, bs, nb, _ptr(out), _dtype_code(out), ws_ptr,
-                                          ws_bytes, _stream(stream)), "kvc_decode_attention_fp8")
+    _check(getattr(raw(), fn)(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                              _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, float(scale), hq, hkv,
+                              d, bs, nb, _ptr(out), _dtype_code(out), ws_ptr, ws_bytes, _stream(stream)), fn)
+
+
+def append_fp8(k, v, slot_mapping, k_cache, v_cache, v_scale, k_scale, stream=None):
+    """kvc_append_fp8. k/v [T, Hkv, D] (f32/f16/bf16); k_cache/v_cache uint8 [num_blocks, Hkv, bs, D];
+    v_scale fp32 [num_blocks, Hkv, bs] (written); k_scale fp32 [Hkv, D]."""
+    _append_q8("kvc_append_fp8", _torch().uint8, k, v, slot_mapping, k_cache, v_cache, v_scale, k_scale, stream)
+
+
+def decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
+                         workspace=None, stream=None):
+    """kvc_decode_attention_fp8: q bf16 [B, Hq, D] over FP8 caches written by append_fp8."""
+    _decode_q8("kvc_decode_attention_fp8", _torch().uint8, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+               context_lens, scale, out, workspace, stream)
+
+
+def append_int8(k, v, slot_mapping, k_cache, v_cache, v_scale, k_scale, stream=None):
+    """kvc_append_int8. k/v [T, Hkv, D] (f32/f16/bf16); k_cache/v_cache int8 [num_blocks, Hkv, bs, D];
+    v_scale fp32 [num_blocks, Hkv, bs] (written); k_scale fp32 [Hkv, D]."""
+    _append_q8("kvc_append_int8", _torch().int8, k, v, slot_mapping, k_cache, v_cache, v_scale, k_scale, stream)
+
+
+def decode_attention_int8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
+                          workspace=None, stream=None):
+    """kvc_decode_attention_int8: q bf16 [B, Hq, D] over INT8 caches written by append_int8."""
+    _decode_q8("kvc_decode_attention_int8", _torch().int8, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+               context_lens, scale, out, workspace, stream)

@@ -31,6 +31,7 @@ SOURCES = [
     "decode_gqa_f16_ext.cu",
     "decode_gqa_bf16_ext.cu",
     "decode_gqa_fp8.cu",
+    "decode_gqa_int8.cu",
     "decode_wide.cu",
     "decode_mla.cu",
     "pool.cpp",

@@ -69,12 +69,18 @@ static kvc_status launch_append(bool two, const void* s0, const void* s1, void* 
   return finish_call(stream);
 }
 
-// FP8 append: one warp per (token, kv head). K is divided by its
-// per-channel scale, V by its row's scale s = max |v| / 448 (1 for an all-zero
-// row), both in fp32 with correctly rounded division, and rounded to e4m3
-// (nearest, ties to even, saturating at +-448). Codes go to the pools, s to
-// the V-scale pool [num_blocks, n_heads, block_size].
-template <typename T>
+// One-byte append: one warp per (token, kv head). K is divided by its
+// per-channel scale, V by its row's scale s = max |v| / QMAX (1 for an
+// all-zero row), both in fp32 with correctly rounded division, and rounded to
+// the code format: e4m3 (QMAX 448; nearest, ties to even, saturating) or, with
+// INT8, symmetric int8 (QMAX 127; nearest, ties to even, saturating at +-127).
+// Codes go to the pools, s to the V-scale pool [num_blocks, n_heads, block_size].
+__device__ __forceinline__ unsigned short encode_pair(float a, float b, bool int8) {
+  if (!int8) return float2_to_fp8x2(a, b);
+  return static_cast<unsigned short>((float_to_s8(a) & 0xff) | ((float_to_s8(b) & 0xff) << 8));
+}
+
+template <typename T, bool INT8>
 __global__ void __launch_bounds__(256) append_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v,
                                                          const int64_t* __restrict__ slots, int64_t num_tokens,
                                                          int n_heads, int D, int block_size, int64_t num_slots,
@@ -99,15 +105,15 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const T* __restrict__ k
     for (int d = 2 * lane; d < D; d += 64)
       vmax = fmaxf(vmax, fmaxf(fabsf(Elem<T>::to_float(vr[d])), fabsf(Elem<T>::to_float(vr[d + 1]))));
     vmax = warp_max(vmax);
-    const float s = vmax > 0.f ? __fdiv_rn(vmax, 448.0f) : 1.0f;
+    const float s = vmax > 0.f ? __fdiv_rn(vmax, INT8 ? 127.0f : 448.0f) : 1.0f;
     const int64_t row = ((blk * n_heads + h) * block_size + off) * D;
     for (int d = 2 * lane; d < D; d += 64) {
       const float k0 = __fdiv_rn(Elem<T>::to_float(kr[d]), __ldg(k_scale + h * D + d));
       const float k1 = __fdiv_rn(Elem<T>::to_float(kr[d + 1]), __ldg(k_scale + h * D + d + 1));
       const float v0 = __fdiv_rn(Elem<T>::to_float(vr[d]), s);
       const float v1 = __fdiv_rn(Elem<T>::to_float(vr[d + 1]), s);
-      *reinterpret_cast<unsigned short*>(kc + row + d) = float2_to_fp8x2(k0, k1);
-      *reinterpret_cast<unsigned short*>(vc + row + d) = float2_to_fp8x2(v0, v1);
+      *reinterpret_cast<unsigned short*>(kc + row + d) = encode_pair(k0, k1, INT8);
+      *reinterpret_cast<unsigned short*>(vc + row + d) = encode_pair(v0, v1, INT8);
     }
     if (lane == 0) vs[(blk * n_heads + h) * block_size + off] = s;
   }
@@ -136,6 +142,65 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* cache, const in
 
 }  // namespace kvc
 
+namespace kvc {
+
+template <bool INT8>
+static void launch_q8(int grid, cudaStream_t s, kvc_dtype dtype, const void* k, const void* v,
+                      const int64_t* slot_mapping, int64_t num_tokens, int n_kv_heads, int head_dim, int block_size,
+                      int64_t num_slots, const float* k_scale, unsigned char* kc, unsigned char* vc, float* v_scale,
+                      unsigned int* err) {
+  switch (dtype) {
+    case KVC_F32:
+      append_fp8_kernel<float, INT8><<<grid, 256, 0, s>>>(static_cast<const float*>(k), static_cast<const float*>(v),
+                                                          slot_mapping, num_tokens, n_kv_heads, head_dim, block_size,
+                                                          num_slots, k_scale, kc, vc, v_scale, err);
+      break;
+    case KVC_F16:
+      append_fp8_kernel<__half, INT8><<<grid, 256, 0, s>>>(static_cast<const __half*>(k),
+                                                           static_cast<const __half*>(v), slot_mapping, num_tokens,
+                                                           n_kv_heads, head_dim, block_size, num_slots, k_scale, kc,
+                                                           vc, v_scale, err);
+      break;
+    case KVC_BF16:
+      append_fp8_kernel<__nv_bfloat16, INT8><<<grid, 256, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), slot_mapping, num_tokens,
+          n_kv_heads, head_dim, block_size, num_slots, k_scale, kc, vc, v_scale, err);
+      break;
+  }
+}
+
+// Quantising append to one-byte codes (e4m3 or int8).
+kvc_status append_q8(bool int8, const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                     void* k_cache, void* v_cache, float* v_scale, const float* k_scale, int64_t num_blocks,
+                     int block_size, int n_kv_heads, int head_dim, kvc_dtype dtype, kvc_stream stream) {
+  if (!dtype_ok(dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || n_kv_heads < 1 || head_dim < 2 || head_dim % 2 != 0)
+    return fail(KVC_ERR_INVALID_ARG, "sizes must be positive (num_tokens >= 0, head_dim even)");
+  if (num_tokens == 0) return KVC_OK;
+  if (k == nullptr || v == nullptr || slot_mapping == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      v_scale == nullptr || k_scale == nullptr)
+    return fail(KVC_ERR_INVALID_ARG, "NULL pointer");
+  DeviceInfo* dev = nullptr;
+  kvc_status st = current_device(&dev);
+  if (st != KVC_OK) return st;
+  const int64_t warps = num_tokens * n_kv_heads;
+  const int64_t want = (warps + 7) / 8;
+  const int grid = static_cast<int>(want < dev->num_sms * 16LL ? want : dev->num_sms * 16LL);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* kc = static_cast<unsigned char*>(k_cache);
+  unsigned char* vc = static_cast<unsigned char*>(v_cache);
+  const int64_t num_slots = num_blocks * block_size;
+  if (int8)
+    launch_q8<true>(grid, s, dtype, k, v, slot_mapping, num_tokens, n_kv_heads, head_dim, block_size, num_slots,
+                    k_scale, kc, vc, v_scale, dev->error_word);
+  else
+    launch_q8<false>(grid, s, dtype, k, v, slot_mapping, num_tokens, n_kv_heads, head_dim, block_size, num_slots,
+                     k_scale, kc, vc, v_scale, dev->error_word);
+  return finish_call(s);
+}
+
+}  // namespace kvc
+
 extern "C" {
 
 kvc_status kvc_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
@@ -158,43 +223,17 @@ kvc_status kvc_append_latent(const void* c, const int64_t* slot_mapping, int64_t
 kvc_status kvc_append_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
                           void* v_cache, float* v_scale, const float* k_scale, int64_t num_blocks, int block_size,
                           int n_kv_heads, int head_dim, kvc_dtype dtype, kvc_stream stream) {
-  using namespace kvc;
-  clear_error();
-  if (!dtype_ok(dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
-  if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || n_kv_heads < 1 || head_dim < 2 || head_dim % 2 != 0)
-    return fail(KVC_ERR_INVALID_ARG, "sizes must be positive (num_tokens >= 0, head_dim even)");
-  if (num_tokens == 0) return KVC_OK;
-  if (k == nullptr || v == nullptr || slot_mapping == nullptr || k_cache == nullptr || v_cache == nullptr ||
-      v_scale == nullptr || k_scale == nullptr)
-    return fail(KVC_ERR_INVALID_ARG, "NULL pointer");
-  DeviceInfo* dev = nullptr;
-  kvc_status st = current_device(&dev);
-  if (st != KVC_OK) return st;
-  const int64_t warps = num_tokens * n_kv_heads;
-  const int64_t want = (warps + 7) / 8;
-  const int grid = static_cast<int>(want < dev->num_sms * 16LL ? want : dev->num_sms * 16LL);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  unsigned char* kc = static_cast<unsigned char*>(k_cache);
-  unsigned char* vc = static_cast<unsigned char*>(v_cache);
-  const int64_t num_slots = num_blocks * block_size;
-  switch (dtype) {
-    case KVC_F32:
-      append_fp8_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(k), static_cast<const float*>(v),
-                                                    slot_mapping, num_tokens, n_kv_heads, head_dim, block_size,
-                                                    num_slots, k_scale, kc, vc, v_scale, dev->error_word);
-      break;
-    case KVC_F16:
-      append_fp8_kernel<__half><<<grid, 256, 0, s>>>(static_cast<const __half*>(k), static_cast<const __half*>(v),
-                                                     slot_mapping, num_tokens, n_kv_heads, head_dim, block_size,
-                                                     num_slots, k_scale, kc, vc, v_scale, dev->error_word);
-      break;
-    case KVC_BF16:
-      append_fp8_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), slot_mapping, num_tokens,
-          n_kv_heads, head_dim, block_size, num_slots, k_scale, kc, vc, v_scale, dev->error_word);
-      break;
-  }
-  return finish_call(s);
+  kvc::clear_error();
+  return kvc::append_q8(false, k, v, slot_mapping, num_tokens, k_cache, v_cache, v_scale, k_scale, num_blocks,
+                        block_size, n_kv_heads, head_dim, dtype, stream);
+}
+
+kvc_status kvc_append_int8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                           void* k_cache, void* v_cache, float* v_scale, const float* k_scale, int64_t num_blocks,
+                           int block_size, int n_kv_heads, int head_dim, kvc_dtype dtype, kvc_stream stream) {
+  kvc::clear_error();
+  return kvc::append_q8(true, k, v, slot_mapping, num_tokens, k_cache, v_cache, v_scale, k_scale, num_blocks,
+                        block_size, n_kv_heads, head_dim, dtype, stream);
 }
 
 kvc_status kvc_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes, const int64_t* pairs, int64_t n_pairs,

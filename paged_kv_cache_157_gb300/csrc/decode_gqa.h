@@ -132,5 +132,8 @@ kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem
 // FP8 e4m3 caches with bf16 queries (head_dim 64, 128 or 256).
 kvc_status gqa_dispatch_fp8(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
                             int* occ);
+// INT8 caches with bf16 queries (head_dim 64, 128 or 256).
+kvc_status gqa_dispatch_int8(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
+                             int* occ);
 
 }  // namespace kvc

@@ -132,6 +132,7 @@ struct DecodeExtra {
   float* lse = nullptr;
   const int32_t* row_start = nullptr;
   int row_div = 0;
+  bool int8 = false;  // with k_scale / v_scale: INT8 codes instead of e4m3
 };
 
 template <typename T>
@@ -140,9 +141,10 @@ kvc_status occupancy(const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
                      : gqa_dispatch<T, false>(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ);
 }
 
-// dt < 0: FP8 caches with bf16 queries
+// dt -1: FP8 caches, -2: INT8 caches (both with bf16 queries)
 kvc_status occupancy_for(int dt, const GqaParams& p, int D, const GqaPlan& pl, int* occ) {
-  if (dt < 0) return gqa_dispatch_fp8(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ);
+  if (dt == -1) return gqa_dispatch_fp8(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ);
+  if (dt == -2) return gqa_dispatch_int8(p, D, pl.GH, 0, pl.smem, nullptr, 1, occ);
   switch (static_cast<kvc_dtype>(dt)) {
     case KVC_F32: return occupancy<float>(p, D, pl, occ);
     case KVC_F16: return occupancy<__half>(p, D, pl, occ);
@@ -188,8 +190,8 @@ namespace kvc {
 namespace {
 
 // Decode over the newest `window` rows of every sequence (window 0: all rows).
-// k_scale / v_scale non-NULL: FP8 e4m3 caches with bf16 queries (dtype is
-// then the query dtype and must be BF16). n_tok > 1: that many new tokens per
+// k_scale / v_scale non-NULL: one-byte caches (e4m3, or int8 with
+// ex->int8) with bf16 queries (dtype is then the query dtype and must be BF16). n_tok > 1: that many new tokens per
 // sequence, q and out [batch, n_tok, n_q_heads, head_dim], causal among them.
 kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                        int max_blocks_per_seq, const int32_t* context_lens, int batch, float scale, int n_q_heads,
@@ -199,14 +201,15 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
                        const DecodeExtra* ex = nullptr) {
   const DecodeExtra none;
   if (ex == nullptr) ex = &none;
-  const bool fp8 = k_scale != nullptr;
+  const bool fp8 = k_scale != nullptr;  // one-byte codes, e4m3 or int8
   if (n_tok < 1 || n_tok > kMaxTokens)
     return fail(KVC_ERR_INVALID_ARG, "n_tokens %d (supported: 1 to %d)", n_tok, kMaxTokens);
   if (n_tok > 1 && (fp8 || window > 0))
-    return fail(KVC_ERR_UNSUPPORTED, "several new tokens with an FP8 cache or a sliding window");
+    return fail(KVC_ERR_UNSUPPORTED, "several new tokens with a one-byte cache or a sliding window");
   if (!dtype_ok(dtype) || !dtype_ok(out_dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype");
-  if (fp8 && dtype != KVC_BF16) return fail(KVC_ERR_UNSUPPORTED, "FP8 decode takes bf16 queries");
-  if (fp8 && head_dim == 32) return fail(KVC_ERR_UNSUPPORTED, "FP8 decode head_dim 32 (supported: 64, 128, 256)");
+  if (fp8 && dtype != KVC_BF16) return fail(KVC_ERR_UNSUPPORTED, "one-byte cache decode takes bf16 queries");
+  if (fp8 && head_dim == 32)
+    return fail(KVC_ERR_UNSUPPORTED, "one-byte cache decode head_dim 32 (supported: 64, 128, 256)");
   if (fp8 && (v_scale == nullptr || !aligned16(k_scale) || !aligned16(v_scale)))
     return fail(KVC_ERR_INVALID_ARG, "k_scale and v_scale must be non-NULL and 16-byte aligned");
   kvc_status s = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq);
@@ -290,7 +293,8 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
 
   int occ = 1;
-  if ((s = occupancy_for(fp8 ? -1 : static_cast<int>(dtype), p, head_dim, pl, &occ)) != KVC_OK) return s;
+  if ((s = occupancy_for(fp8 ? (ex->int8 ? -2 : -1) : static_cast<int>(dtype), p, head_dim, pl, &occ)) != KVC_OK)
+    return s;
   int64_t G = plan_ctas(dev, occ, pl.units, max_blocks_per_seq);
   const size_t cbytes = counter_bytes(batch, n_kv_heads, pl);
   G = std::min<int64_t>(G, workspace_bytes > cbytes
@@ -315,7 +319,8 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
     return fail(KVC_ERR_UNSUPPORTED, "num_blocks x n_kv_heads must be below 2^31");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (fp8) {
-    s = gqa_dispatch_fp8(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr);
+    s = ex->int8 ? gqa_dispatch_int8(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr)
+                 : gqa_dispatch_fp8(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr);
     if (s != KVC_OK) return s;
     return finish_call(st);
   }
@@ -365,6 +370,21 @@ kvc_status kvc_decode_attention_fp8(const void* q, const void* k_cache, const vo
   return kvc::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale, n_q_heads,
                           n_kv_heads, head_dim, block_size, num_blocks, 0, KVC_BF16, out, out_dtype, workspace,
                           workspace_bytes, stream, k_scale, v_scale);
+}
+
+kvc_status kvc_decode_attention_int8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                                     const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int batch, float scale, int n_q_heads,
+                                     int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, void* out,
+                                     kvc_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                     kvc_stream stream) {
+  kvc::clear_error();
+  if (k_scale == nullptr || v_scale == nullptr) return kvc::fail(KVC_ERR_INVALID_ARG, "k_scale / v_scale is NULL");
+  kvc::DecodeExtra ex;
+  ex.int8 = true;
+  return kvc::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale, n_q_heads,
+                          n_kv_heads, head_dim, block_size, num_blocks, 0, KVC_BF16, out, out_dtype, workspace,
+                          workspace_bytes, stream, k_scale, v_scale, 1, &ex);
 }
 
 kvc_status kvc_decode_attention_window(const void* q, const void* k_cache, const void* v_cache,

@@ -35,6 +35,8 @@
 //   accumulation in fp32.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_gqa.h"
 #include "kvc_device.cuh"
 
@@ -248,6 +250,8 @@ struct VRow {
       return make_float2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
     } else if constexpr (sizeof(T) == 2) {
       return make_float2(Elem<T>::half_to_float(w[i], 0), Elem<T>::half_to_float(w[i], 1));
+    } else if constexpr (std::is_same<T, s8q>::value) {
+      return s8x2_to_float2(w[i >> 1] >> (16 * (i & 1)));
     } else {
       return fp8x2_to_float2(w[i >> 1] >> (16 * (i & 1)));
     }

@@ -106,6 +106,39 @@ __device__ __forceinline__ unsigned short float2_to_fp8x2(float a, float b) {
   return r;
 }
 
+// INT8 cache element (symmetric codes in [-127, 127]).
+struct s8q {
+  signed char bits;
+};
+
+// Two int8 codes (low byte first) as an fp32 pair (exact). Flipping the sign
+// bit turns code c into the byte c + 128; placed in the low mantissa byte of
+// 2^23 that gives the float 2^23 + c + 128, and one subtraction leaves c.
+// (Integer-to-float conversion runs at a quarter of the FMA rate; this is a
+// byte permute, an XOR and a float add.)
+__device__ __forceinline__ float2 s8x2_to_float2(uint32_t two) {
+  const uint32_t u = two ^ 0x8080u;
+  const float a = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440));
+  const float b = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441));
+  return make_float2(a - 8388736.0f, b - 8388736.0f);
+}
+
+// Rounds an fp32 value to an int8 code: nearest, ties to even, saturating at
+// +-127 (-128 is never produced).
+__device__ __forceinline__ int float_to_s8(float x) {
+  const int r = __float2int_rn(x);
+  return r < -127 ? -127 : (r > 127 ? 127 : r);
+}
+
+template <> struct Elem<s8q> {
+  static constexpr int kVec = 16;
+  __device__ __forceinline__ static float2 pair(const uint4& u, int c) {
+    const int wi = c >> 1;
+    const uint32_t w = wi == 0 ? u.x : (wi == 1 ? u.y : (wi == 2 ? u.z : u.w));
+    return s8x2_to_float2((c & 1) ? (w >> 16) : w);
+  }
+};
+
 template <> struct Elem<fp8e4m3> {
   static constexpr int kVec = 16;
   // Elements 2c and 2c+1 of a 16-byte chunk (c in [0, 8)) as an fp32 pair.

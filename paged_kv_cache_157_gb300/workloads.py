@@ -228,6 +228,41 @@ def fp8_case(batch, n_q_heads, n_kv_heads, head_dim, block_size, lens, seed, spa
     }
 
 
+def int8_case(batch, n_q_heads, n_kv_heads, head_dim, block_size, lens, seed, spare_frac=0.10, device="cpu"):
+    """A paged decode step over an INT8 cache: codes uniform in [-127, 127], per-channel K scales [Hkv, D] and a
+    per-token V-scale pool [num_blocks, Hkv, bs] (positive, around 4/127 as for N(0,1) data), bf16 queries and
+    bf16 new K/V rows. Draw order: lengths, table permutation, K codes, V codes, K scales, V scales, q, new k,
+    new v."""
+    g = _gen(seed)
+    gv = g if device == "cpu" else _gen(seed, device)
+    if isinstance(lens, tuple):
+        lens_t = uniform_lengths(batch, lens[0], lens[1], g)
+    else:
+        lens_t = torch.tensor([int(x) for x in lens], dtype=torch.int32)
+    table, num_blocks = random_block_tables(lens_t.tolist(), block_size, spare_frac, g, True)
+    shape = (num_blocks, n_kv_heads, block_size, head_dim)
+
+    def codes():
+        return torch.randint(-127, 128, shape, generator=gv, dtype=torch.int32, device=gv.device).to(torch.int8)
+
+    kc, vc = codes(), codes()
+    k_scale = ((0.5 + torch.rand((n_kv_heads, head_dim), generator=gv, device=gv.device)) * (4.0 / 127.0)).float()
+    v_scale = ((0.5 + torch.rand(shape[:3], generator=gv, device=gv.device)) * (4.0 / 127.0)).float()
+    return {
+        "context_lens": lens_t,
+        "block_tables": table,
+        "num_blocks": num_blocks,
+        "k_cache": kc,
+        "v_cache": vc,
+        "k_scale": k_scale,
+        "v_scale": v_scale,
+        "q": normal((batch, n_q_heads, head_dim), "bf16", gv),
+        "k_new": normal((batch, n_kv_heads, head_dim), "bf16", gv),
+        "v_new": normal((batch, n_kv_heads, head_dim), "bf16", gv),
+        "block_size": block_size,
+    }
+
+
 def multi_case(batch, n_tok, n_q_heads, n_kv_heads, head_dim, block_size, lens, dtype, seed, spare_frac=0.10,
                device="cpu"):
     """A paged step with ``n_tok`` new query tokens per sequence (chunked prefill or speculative verification).
