@@ -111,16 +111,33 @@ struct s8q {
   signed char bits;
 };
 
-// Two int8 codes (low byte first) as an fp32 pair (exact). Flipping the sign
-// bit turns code c into the byte c + 128; placed in the low mantissa byte of
-// 2^23 that gives the float 2^23 + c + 128, and one subtraction leaves c.
-// (Integer-to-float conversion runs at a quarter of the FMA rate; this is a
-// byte permute, an XOR and a float add.)
+// int8 codes to fp32 without the integer-to-float unit (a quarter-rate
+// pipe). Flipping the sign bits (s8_flip) turns code c into the byte c + 128;
+// placed in the low mantissa byte of the float 2^23 (s8_biased) that byte
+// gives 2^23 + c + 128, and one packed subtraction of 2^23 + 128 leaves c
+// exactly (s8_unbias).
+__device__ __forceinline__ uint32_t s8_flip(uint32_t w) { return w ^ 0x80808080u; }
+
+// Byte `b` (0..3) of a flipped word as the float 2^23 + c + 128.
+__device__ __forceinline__ float s8_biased(uint32_t flipped, int b) {
+  return __uint_as_float(__byte_perm(flipped, 0x4B000000u, 0x7440u | static_cast<unsigned>(b)));
+}
+
+__device__ __forceinline__ float2 s8_unbias(float2 x) {
+  union {
+    float2 f;
+    unsigned long long u;
+  } a, c, r;
+  a.f = x;
+  c.f = make_float2(-8388736.0f, -8388736.0f);
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.u) : "l"(a.u), "l"(c.u));
+  return r.f;
+}
+
+// Two int8 codes (low byte first) as an fp32 pair (exact).
 __device__ __forceinline__ float2 s8x2_to_float2(uint32_t two) {
-  const uint32_t u = two ^ 0x8080u;
-  const float a = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440));
-  const float b = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441));
-  return make_float2(a - 8388736.0f, b - 8388736.0f);
+  const uint32_t u = s8_flip(two);
+  return s8_unbias(make_float2(s8_biased(u, 0), s8_biased(u, 1)));
 }
 
 // Rounds an fp32 value to an int8 code: nearest, ties to even, saturating at
@@ -134,8 +151,9 @@ template <> struct Elem<s8q> {
   static constexpr int kVec = 16;
   __device__ __forceinline__ static float2 pair(const uint4& u, int c) {
     const int wi = c >> 1;
-    const uint32_t w = wi == 0 ? u.x : (wi == 1 ? u.y : (wi == 2 ? u.z : u.w));
-    return s8x2_to_float2((c & 1) ? (w >> 16) : w);
+    const uint32_t w = s8_flip(wi == 0 ? u.x : (wi == 1 ? u.y : (wi == 2 ? u.z : u.w)));
+    const int b = 2 * (c & 1);  // bytes b and b + 1 of the word
+    return s8_unbias(make_float2(s8_biased(w, b), s8_biased(w, b + 1)));
   }
 };
 
