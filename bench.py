@@ -645,6 +645,21 @@ def kernel_source_sha():
     return h.hexdigest()
 
 
+def max_over_ranks(values, world, device):
+    """Each value's maximum over the ranks (the slowest replica sets the time); one rank returns them as is."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def replica_gbps(world, bytes_per_step, ms_per_step):
+    """Whole-job GB/s of `world` replicas that each move bytes_per_step per step in ms_per_step."""
+    return world * bytes_per_step / (ms_per_step / 1e3) / 1e9
+
+
 def run_kvc(args):
     import torch
     import torch.distributed as dist
@@ -676,15 +691,11 @@ def run_kvc(args):
     step_ms, dec_ms, wall, clocks = time_steps(step, args.steps, args.warmup, flush, sampler)
     if world > 1:
         dist.barrier()
-    total_ms = sum(step_ms)
-    t = torch.tensor([total_ms, statistics.mean(dec_ms)], device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, dec_avg = float(t[0]), float(t[1])
+    total_ms, dec_avg = max_over_ranks([sum(step_ms), statistics.mean(dec_ms)], world, "cuda")
     ms = total_ms / args.steps
     dec_b, app_b = step_bytes(step.lens, step.hq, step.hkv, step.d, step.bs, 2, 2)
     per_step = dec_b + app_b
-    value = world * per_step / (ms / 1e3) / 1e9
+    value = replica_gbps(world, per_step, ms)
     if rank != 0:
         dist.destroy_process_group()
         return
