@@ -797,8 +797,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=("main",) + VARIANTS, default="main",
                     help="time one other workload alone (prints its measurement, not the contract line)")
-    ap.add_argument("--gqa-engine", choices=("auto", "cuda-core"), default="auto",
-                    help="with --workload: 'cuda-core' keeps wide query groups off the tensor-core kernel")
+    ap.add_argument("--gqa-engine", choices=("auto", "cuda-core", "tensor-core"), default="auto",
+                    help="with --workload: 'cuda-core' keeps wide query groups off the tensor-core kernel, "
+                         "'tensor-core' puts them on it at any size")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -806,7 +807,7 @@ def main():
         import paged_kv_cache_157_gb300 as kvc
         from paged_kv_cache_157_gb300 import build_lib
         build_lib.build()
-        kvc.set_option(kvc.OPT_GQA_ENGINE, 1 if args.gqa_engine == "cuda-core" else 0)
+        kvc.set_option(kvc.OPT_GQA_ENGINE, {"auto": 0, "cuda-core": 1, "tensor-core": 2}[args.gqa_engine])
         print(json.dumps({"workload": args.workload, "gqa_engine": args.gqa_engine,
                           **run_variant(kvc, args.workload, flush_buffer(), args.steps)}), flush=True)
         return

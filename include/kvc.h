@@ -100,10 +100,14 @@ typedef enum kvc_option {
   KVC_OPT_BLOCKS_PER_CTA = 1,
   /* Upper bound on decode CTAs (0 = automatic, SM count x resident CTAs). */
   KVC_OPT_MAX_CTAS = 2,
-  /* GQA decode engine: 0 (default) = automatic (the tensor-core kernel for
-   * bf16/f16 caches, head_dim 128, block sizes 16/32/64/128, no window, when
-   * a kv head has 8 to 32 queries: n_tokens x n_q_heads / n_kv_heads);
-   * 1 = always the CUDA-core kernel. */
+  /* GQA decode engine. The tensor-core kernel takes bf16/f16 caches,
+   * head_dim 128, block sizes 16/32/64/128, no window, and kv heads with 8 to
+   * 32 queries (qn = n_tokens x n_q_heads / n_kv_heads). 0 (default) =
+   * automatic: that kernel where it applies and the cache it may read
+   * (batch x n_kv_heads x max_blocks_per_seq x block_size rows of K and V) is
+   * at least 512 MiB / qn, else the CUDA-core kernel, whose fixed cost per
+   * call is lower; 1 = always the CUDA-core kernel; 2 = the tensor-core
+   * kernel wherever it applies, at any size. */
   KVC_OPT_GQA_ENGINE = 3
 } kvc_option;
 kvc_status kvc_set_option(kvc_option opt, int64_t value);

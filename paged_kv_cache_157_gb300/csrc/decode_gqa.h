@@ -118,8 +118,12 @@ struct WideArgs {
   float scale;
   cudaStream_t stream;
 };
+// Whether the tensor-core kernel takes these shapes (and the engine option
+// allows it), and whether the automatic choice picks it (large enough work).
 bool wide_supported(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size, int n_tok,
                     kvc_dtype dtype);
+bool wide_preferred(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size, int max_blocks,
+                    int n_tok, kvc_dtype dtype);
 size_t wide_workspace_bytes(const DeviceInfo* dev, int batch, int n_q_heads, int n_kv_heads, int block_size,
                             int max_blocks, int n_tok);
 kvc_status wide_decode(const WideArgs& a, DeviceInfo* dev);

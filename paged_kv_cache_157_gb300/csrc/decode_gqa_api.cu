@@ -230,7 +230,7 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   DeviceInfo* dev = nullptr;
   if ((s = current_device(&dev)) != KVC_OK) return s;
   if (!fp8 && window == 0 && ex->row_div == 0 &&
-      wide_supported(batch, n_q_heads, n_kv_heads, head_dim, block_size, n_tok, dtype)) {
+      wide_preferred(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, n_tok, dtype)) {
     WideArgs a{};
     a.q = q;
     a.k_cache = k_cache;

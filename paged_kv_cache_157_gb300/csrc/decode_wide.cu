@@ -732,6 +732,21 @@ int64_t plan_ctas(const DeviceInfo* dev, int64_t units, int max_blocks, int bloc
 
 }  // namespace wide
 
+bool wide_preferred(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size, int max_blocks,
+                    int n_tok, kvc_dtype dtype) {
+  if (!wide_supported(batch, n_q_heads, n_kv_heads, head_dim, block_size, n_tok, dtype)) return false;
+  if (option(KVC_OPT_GQA_ENGINE) == 2) return true;
+  // Fixed cost per call ~31 us against ~14 us for the CUDA-core kernel, whose
+  // streaming rate falls with the queries per kv head (~3.5 TB/s at 8, ~1.6 at
+  // 16) where this kernel keeps ~6.1 TB/s: it pays from ~140 MB of cache at 8
+  // queries and ~40 MB at 16. The bound below uses the table width, the most
+  // the host knows about the lengths.
+  const int qn = n_tok * (n_q_heads / n_kv_heads);
+  const double rows = static_cast<double>(batch) * n_kv_heads * max_blocks * block_size;
+  const double bytes = rows * head_dim * 2.0 * 2.0;  // K and V, 2-byte elements
+  return bytes >= (512.0 * 1024.0 * 1024.0) / qn;
+}
+
 bool wide_supported(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size, int n_tok,
                     kvc_dtype dtype) {
   if (option(KVC_OPT_GQA_ENGINE) == 1) return false;

@@ -122,7 +122,7 @@ kvc_status kvc_set_option(kvc_option opt, int64_t value) {
   if (o < 0 || o > 3) return kvc::fail(KVC_ERR_INVALID_ARG, "unknown option %d", o);
   if (value < 0) return kvc::fail(KVC_ERR_INVALID_ARG, "option value must be >= 0");
   if (opt == KVC_OPT_CHECKED && value > 1) return kvc::fail(KVC_ERR_INVALID_ARG, "checked mode is 0 or 1");
-  if (opt == KVC_OPT_GQA_ENGINE && value > 1) return kvc::fail(KVC_ERR_INVALID_ARG, "GQA engine is 0 or 1");
+  if (opt == KVC_OPT_GQA_ENGINE && value > 2) return kvc::fail(KVC_ERR_INVALID_ARG, "GQA engine is 0, 1 or 2");
   kvc::g_options[o] = value;
   return KVC_OK;
 }

@@ -68,8 +68,11 @@ def shared_step(kvc, case, fanout, prefix, tol, append=True, out_dtype=torch.flo
 
 @pytest.mark.parametrize("hq,hkv,dtype", [(8, 8, "f16"), (16, 4, "bf16"), (32, 4, "bf16"), (16, 16, "bf16")])
 @pytest.mark.parametrize("fanout", [1, 4, 8])
-def test_shared_prefix_equals_decode(kvc, hq, hkv, dtype, fanout):
-    # the prefix pass has fanout x group queries per kv head: 1 to 64, both engines
+@pytest.mark.parametrize("engine", [0, 2])
+def test_shared_prefix_equals_decode(kvc, hq, hkv, dtype, fanout, engine):
+    # the prefix pass has fanout x group queries per kv head: 1 to 64; engine 2 puts the 8-32 query passes on
+    # the tensor-core kernel at these small sizes
+    kvc.set_option(kvc.OPT_GQA_ENGINE, engine)
     case = forked_case(3, fanout, 64, 37, hq, hkv, 128, 16, dtype, seed=140 + hq + fanout)
     shared_step(kvc, case, fanout, [64] * 3, TOL[dtype])
     assert kvc.get_error_flags() == 0
@@ -90,7 +93,7 @@ def test_no_private_rows(kvc):
 
 
 @pytest.mark.parametrize("blocks_per_cta", [1, 3])
-@pytest.mark.parametrize("engine", [0, 1])
+@pytest.mark.parametrize("engine", [0, 1, 2])
 def test_shared_prefix_split_k_and_engines(kvc, blocks_per_cta, engine):
     kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, blocks_per_cta)
     kvc.set_option(kvc.OPT_GQA_ENGINE, engine)

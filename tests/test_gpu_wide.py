@@ -1,5 +1,6 @@
 """GPU parity: the tensor-core decode for kv heads with 8 to 32 queries, against the oracle and against the
-CUDA-core kernel (KVC_OPT_GQA_ENGINE = 1 forces the latter on the same inputs)."""
+CUDA-core kernel. KVC_OPT_GQA_ENGINE = 2 forces the tensor-core kernel at any size (the automatic choice keeps
+small caches on the CUDA-core kernel), 1 forces the CUDA-core kernel on the same inputs."""
 
 import math
 
@@ -21,12 +22,13 @@ def _reset_options(kvc):
     opts = (kvc.OPT_BLOCKS_PER_CTA, kvc.OPT_MAX_CTAS, kvc.OPT_CHECKED, kvc.OPT_GQA_ENGINE)
     for o in opts:
         kvc.set_option(o, 0)
+    kvc.set_option(kvc.OPT_GQA_ENGINE, 2)
     yield
     for o in opts:
         kvc.set_option(o, 0)
 
 
-def decode_and_compare(kvc, case, tol, workspace="auto", engine=0):
+def decode_and_compare(kvc, case, tol, workspace="auto", engine=2):
     kvc.set_option(kvc.OPT_GQA_ENGINE, engine)
     dev = device_case(case)
     slots = last_position_slots(kvc, case)
@@ -46,7 +48,7 @@ def decode_and_compare(kvc, case, tol, workspace="auto", engine=0):
 LENS = [1, 15, 16, 17, 127, 128, 129, 255, 256, 257, 1000]
 
 
-@pytest.mark.parametrize("engine", [0, 1])
+@pytest.mark.parametrize("engine", [0, 1, 2])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("hq,hkv", [(64, 8), (32, 2), (32, 1), (24, 2), (8, 1)])
 def test_wide_groups_both_engines(kvc, engine, dtype, hq, hkv):
@@ -57,7 +59,7 @@ def test_wide_groups_both_engines(kvc, engine, dtype, hq, hkv):
 
 def test_engines_agree(kvc):
     case = W.gqa_case(6, 64, 8, 128, 16, (1, 3000), "bf16", seed=121)
-    a = decode_and_compare(kvc, case, TOL["bf16"], engine=0)
+    a = decode_and_compare(kvc, case, TOL["bf16"], engine=2)
     b = decode_and_compare(kvc, case, TOL["bf16"], engine=1)
     assert float((a - b).abs().max()) <= 2e-3
 
