@@ -75,3 +75,27 @@ def test_host_validation_before_any_device_work(kvc):
     # workspace query validates shapes too
     n = ctypes.c_size_t()
     assert lib.kvc_decode_workspace_size(2, 6, 4, 128, 16, 4, ctypes.byref(n)) == kvc.ERR_INVALID_ARG
+
+
+def test_one_byte_cache_entries_validate_on_the_host(kvc):
+    import ctypes
+    lib = kvc.raw()
+    z = ctypes.c_void_p(0)
+    p16 = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails before any device work
+    for name in ("kvc_decode_attention_fp8", "kvc_decode_attention_int8"):
+        fn = getattr(lib, name)
+        # NULL scales
+        assert fn(z, z, z, z, z, z, 4, z, 2, 0.1, 8, 4, 128, 16, 10, z, 0, z, 0, z) == kvc.ERR_INVALID_ARG
+        # head_dim 32 is not instantiated for one-byte caches
+        assert fn(z, z, z, p16, p16, z, 4, z, 2, 0.1, 8, 4, 32, 16, 10, z, 0, z, 0, z) == kvc.ERR_UNSUPPORTED
+        # unaligned scales
+        odd = ctypes.c_void_p(0x1004)
+        assert fn(z, z, z, odd, p16, z, 4, z, 2, 0.1, 8, 4, 128, 16, 10, z, 0, z, 0, z) == kvc.ERR_INVALID_ARG
+    for name in ("kvc_append_fp8", "kvc_append_int8"):
+        fn = getattr(lib, name)
+        # zero tokens: a no-op; a bad dtype or an odd head_dim: invalid
+        assert fn(z, z, z, 0, z, z, z, z, 10, 16, 8, 128, 2, z) == kvc.OK
+        assert fn(z, z, z, 1, z, z, z, z, 10, 16, 8, 128, 7, z) == kvc.ERR_INVALID_ARG
+        assert fn(z, z, z, 1, z, z, z, z, 10, 16, 8, 127, 2, z) == kvc.ERR_INVALID_ARG
+        # NULL scale pointers with tokens to write
+        assert fn(p16, p16, p16, 1, p16, p16, z, z, 10, 16, 8, 128, 2, z) == kvc.ERR_INVALID_ARG
