@@ -438,18 +438,51 @@ def variants(kvc, flush, steps):
 
 
 def measure_tiny(kvc, flush, steps):
-    """1 sequence, 2 layers, 4 heads x 32, fp32: seq*layer decode steps per second (append + decode)."""
+    """1 sequence, 2 layers, 4 heads x 32, fp32: seq*layer decode steps per second (append + decode). Eager
+    calls, and the same four calls (append and decode of both layers) captured once as a CUDA graph and
+    replayed per step, as a latency-bound serving loop would run them (L2 flushed between steps either way)."""
     import torch
     from paged_kv_cache_157_gb300 import workloads as W
-    res = []
+    res, sts = [], []
     for L in range(2):
         c = W.gqa_case(1, 4, 4, 32, 16, [69], "f32", 42 + L, device="cuda")
         st = GqaStep(kvc, c, torch.float32)
         step_ms, _, _, _ = time_steps(st, steps, 5, flush)
         res.append(statistics.mean(step_ms))
+        sts.append(st)
     ms = sum(res)
-    return {"ms_per_step_2_layers": round(ms, 5), "seq_layer_steps_per_s": round(2 / (ms / 1e3), 1),
-            "note": "latency-bound: one sequence of 69 tokens"}
+    out = {"ms_per_step_2_layers": round(ms, 5), "seq_layer_steps_per_s": round(2 / (ms / 1e3), 1),
+           "note": "latency-bound: one sequence of 69 tokens"}
+    try:
+        cur = torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            for st in sts:
+                st.append()
+                st.decode()
+        cur.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for st in sts:
+                st.append()
+                st.decode()
+        for _ in range(5):
+            flush.run()
+            g.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            flush.run()
+            a.record(cur)
+            g.replay()
+            b.record(cur)
+        torch.cuda.synchronize()
+        gms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        out["graph_ms_per_step_2_layers"] = round(gms, 5)
+        out["graph_seq_layer_steps_per_s"] = round(2 / (gms / 1e3), 1)
+    except RuntimeError as e:  # report, do not hide, a failed capture
+        out["graph_error"] = str(e)[:200]
+    return out
 
 
 def measure_fp8(kvc, flush, steps, int8=False):
