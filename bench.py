@@ -359,6 +359,45 @@ def cpu_baseline(case, budget_s=10.0):
                       f"over its {B} sequences, float64 NumPy, single thread; {tot_t:.1f} s"}
 
 
+_POOL_CASE = None
+
+
+def _pool_init(args):
+    """Pool worker start: rebuild the seeded workload on the CPU (not timed)."""
+    global _POOL_CASE
+    from paged_kv_cache_157_gb300 import workloads as W
+    _POOL_CASE = W.gqa_case(*args)
+
+
+def _pool_ready(_):
+    time.sleep(0.2)  # spreads these tasks over the workers, each past its start-up
+    return os.getpid()
+
+
+def _pool_task(i):
+    return oracle_sample_seconds(_POOL_CASE, [i])
+
+
+def cpu_baseline_pool(tasks_per_core=48):
+    """The same oracle on all host cores: a process pool (spawn start) over the sequences of the workload, each
+    worker with its own copy of it; value = algorithmic bytes of all tasks / wall time of the pool run."""
+    import multiprocessing as mp
+    m = MAIN
+    cores = len(os.sched_getaffinity(0))
+    args = (m["batch"], m["hq"], m["hkv"], m["d"], m["bs"], m["lens"], m["dtype"], m["seed"])
+    with mp.get_context("spawn").Pool(cores, initializer=_pool_init, initargs=(args,)) as pool:
+        pool.map(_pool_ready, range(2 * cores), chunksize=1)
+        n = cores * tasks_per_core
+        t0 = time.perf_counter()
+        res = pool.map(_pool_task, [i % m["batch"] for i in range(n)], chunksize=1)
+        wall = time.perf_counter() - t0
+    by = sum(b for _, b in res)
+    return {"value": round(by / wall / 1e9, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"append + decode of {n} whole sequences (all heads), cycling over the {m['batch']} "
+                      f"sequences, float64 NumPy, a spawn process pool of {cores} workers over sequences; "
+                      f"{wall:.1f} s wall"}
+
+
 # --------------------------------------------------------------- variants
 
 def measure_gqa_case(kvc, case, steps, warmup, flush, unique_rows=None, window=None):
@@ -738,6 +777,7 @@ def run_kvc(args):
     e2e_value = per_step / (e2e_ms / 1e3) / 1e9
     var = {} if args.no_variants else variants(kvc, flush, max(10, min(args.steps, 200)))
     cpu = None if args.no_cpu_baseline else cpu_baseline(case)
+    cpu_pool = None if args.no_cpu_baseline else cpu_baseline_pool()
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -776,6 +816,7 @@ def run_kvc(args):
         "clocks": clocks,
         "timed_wall_s": round(wall, 4),
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_pool,
         "variants": var,
     }
     print(json.dumps(line), flush=True)
