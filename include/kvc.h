@@ -187,7 +187,10 @@ kvc_status kvc_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes,
 
 /* Bytes of scratch that kvc_decode_attention needs for these shapes on the
  * current device (split-K partial results). 0 is a valid answer. The size
- * depends on the device's SM count and on KVC_OPT_MAX_CTAS. */
+ * depends on the device's SM count and on KVC_OPT_MAX_CTAS. Errors: the
+ * shape checks of kvc_decode_attention (KVC_ERR_INVALID_ARG /
+ * KVC_ERR_UNSUPPORTED). The split itself is this library's; the pages define
+ * only the result it must equal ("KV缓存原理与显存估算", knowledge point 2). */
 kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
                                      int max_blocks_per_seq, size_t* bytes);
 
@@ -261,7 +264,7 @@ kvc_status kvc_decode_attention_multi(const void* q, const void* k_cache, const 
 
 /* Scratch bytes kvc_decode_attention_shared_prefix needs for these shapes
  * (256-byte aligned, zero-filled once before first use; complete calls leave
- * its counters zeroed again). */
+ * its counters zeroed again). Same shape errors as the call it sizes. */
 kvc_status kvc_decode_shared_prefix_workspace_size(int batch, int group_size, int n_q_heads, int n_kv_heads,
                                                    int head_dim, int block_size, int max_blocks_per_seq,
                                                    size_t* bytes);
@@ -350,7 +353,8 @@ kvc_status kvc_decode_attention_static(const void* q, const void* k_cache, const
                                        int n_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                                        kvc_dtype dtype, void* out, kvc_dtype out_dtype, kvc_stream stream);
 
-/* Scratch bytes for kvc_decode_attention_mla on the current device. */
+/* Scratch bytes for kvc_decode_attention_mla on the current device (split-K
+ * records; 0 is a valid answer). Same shape errors as that call. */
 kvc_status kvc_decode_mla_workspace_size(int batch, int n_q_heads, int d_c, int d_r, int block_size,
                                          int max_blocks_per_seq, size_t* bytes);
 
@@ -389,13 +393,16 @@ typedef struct kvc_pool_stats {
 kvc_status kvc_pool_create(int64_t num_blocks, int block_size, kvc_pool** pool);
 void kvc_pool_destroy(kvc_pool* pool);
 kvc_status kvc_seq_add(kvc_pool* pool, int64_t* seq);
-/* New sequence sharing all of parent's blocks (each gains one reference). */
+/* New sequence sharing all of parent's blocks (each gains one reference);
+ * KVC_ERR_INVALID_ARG for an unknown parent. Source: "KV Cache（键值缓存）"
+ * 2.3 (blocks shared between sequences by reference count). */
 kvc_status kvc_seq_fork(kvc_pool* pool, int64_t parent, int64_t* child);
 /* Extends `seq` by n_new tokens and writes their slots to slots_out[n_new].
  * Allocates a block at every block boundary. KVC_ERR_NO_BLOCKS if the pool
  * cannot supply them (nothing allocated, length unchanged).
  * KVC_ERR_UNSUPPORTED if the last block is partly filled and shared
- * (would need copy-on-write). */
+ * (would need copy-on-write). slots_out is host memory owned by the caller.
+ * Source: "KV Cache（键值缓存）" 2.3 (fixed-size blocks allocated on demand). */
 kvc_status kvc_seq_reserve(kvc_pool* pool, int64_t seq, int64_t n_new, int64_t* slots_out);
 /* kvc_seq_reserve with copy-on-write: if the sequence's last block is partly
  * filled and held by other sequences too, the sequence first gets a fresh
@@ -408,19 +415,26 @@ kvc_status kvc_seq_reserve(kvc_pool* pool, int64_t seq, int64_t n_new, int64_t* 
  * Source: llm-compass 2.3 (blocks shared by reference count are copied
  * before a holder writes into them: parallel sampling, beam search). */
 kvc_status kvc_seq_reserve_cow(kvc_pool* pool, int64_t seq, int64_t n_new, int64_t* slots_out, int64_t* copy_pair);
-/* Drops the sequence; each of its blocks loses one reference. */
+/* Drops the sequence; each of its blocks loses one reference and returns to
+ * the free list at zero. KVC_ERR_INVALID_ARG for an unknown sequence.
+ * Source: "KV Cache（键值缓存）" 2.3. */
 kvc_status kvc_seq_free(kvc_pool* pool, int64_t seq);
 kvc_status kvc_seq_length(kvc_pool* pool, int64_t seq, int64_t* length);
 kvc_status kvc_block_refcount(kvc_pool* pool, int64_t block, int32_t* refcount);
 /* Writes table rows (int32 [n, max_blocks], unused entries 0) and lengths
- * (int32 [n]) for the given sequences, into host memory. */
+ * (int32 [n]) for the given sequences, into caller-owned host memory.
+ * KVC_ERR_INVALID_ARG for an unknown sequence or one with more blocks than
+ * max_blocks. Source: "KV Cache（键值缓存）" 2.3 (the per-sequence block table
+ * from logical to physical blocks). */
 kvc_status kvc_build_block_tables(kvc_pool* pool, const int64_t* seqs, int n, int32_t* table_out,
                                   int max_blocks, int32_t* lens_out);
 kvc_status kvc_pool_get_stats(kvc_pool* pool, kvc_pool_stats* stats);
 
 /* Host helper: slots of (row, position) pairs for an existing host-side
- * block table (int32 [rows, max_blocks]). Out-of-table positions give
- * KVC_ERR_INVALID_ARG. */
+ * block table (int32 [rows, max_blocks]): slot = table[row][pos / block_size]
+ * * block_size + pos % block_size. All pointers are caller-owned host memory.
+ * Out-of-table positions give KVC_ERR_INVALID_ARG. Source: "KV Cache（键值缓存）"
+ * 2.3 (block table lookup); the slot encoding is this library's. */
 kvc_status kvc_slots_from_tables(const int32_t* block_tables, int rows, int max_blocks, int block_size,
                                  const int32_t* row_index, const int64_t* positions, int64_t n,
                                  int64_t* slots_out);
