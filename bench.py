@@ -454,6 +454,8 @@ def run_variant(kvc, name, flush, steps):
         return measure_gqa_case(kvc, c, steps, 5, flush)
     if name == "tiny_mha_fp32":
         return measure_tiny(kvc, flush, steps)
+    if name == "host_pool_shared_8x8":
+        return measure_host_pool(kvc, steps)
     if name == "mla_deepseek_v2":
         return measure_mla(kvc, flush, steps)
     raise ValueError(f"unknown workload {name}")
@@ -461,7 +463,8 @@ def run_variant(kvc, name, flush, steps):
 
 VARIANTS = ("gqa_b32_ctx4096", "mha_shared_prefix_8x8", "gqa_long_splitk", "gqa_ragged_17_31_32", "tiny_mha_fp32",
             "mla_deepseek_v2", "gqa_window_b32_ctx4096_w1024", "cow_copy_blocks_2048", "gqa_fp8_b32_ctx4096",
-            "gqa_int8_b32_ctx4096", "gqa_spec4_b32_ctx4096", "mha_shared_prefix_8x8_cascade")
+            "gqa_int8_b32_ctx4096", "gqa_spec4_b32_ctx4096", "mha_shared_prefix_8x8_cascade",
+            "host_pool_shared_8x8")
 
 
 def variants(kvc, flush, steps):
@@ -474,6 +477,56 @@ def variants(kvc, flush, steps):
             out[name] = {"error": f"{type(e).__name__}: {e}"}
         torch.cuda.empty_cache()
     return out
+
+
+def measure_host_pool(kvc, steps):
+    """The host step of the sharing workload: 8 prompts of 2048 tokens, each forked 8 ways (64 sequences,
+    prompt blocks at refcount 8) with 256 private tokens; per step every sequence reserves one slot
+    (kvc_seq_reserve, one call per sequence, or kvc_seq_reserve_batch, one call for all) and the 64 table rows
+    are rebuilt (kvc_build_block_tables). Timed on the host through ctypes with preallocated buffers, so the
+    figures include the per-call binding overhead."""
+    import ctypes
+    lib = kvc.raw()
+    bs, max_blocks = 16, 160
+    pool = kvc.BlockPool(4096, bs)
+    seqs = []
+    for _ in range(8):
+        p = pool.add()
+        pool.reserve(p, 2048)
+        seqs.extend(pool.fork(p) for _ in range(8))
+        pool.free(p)
+    for sq in seqs:
+        pool.reserve(sq, 256)
+    n = len(seqs)
+    ids = (ctypes.c_int64 * n)(*seqs)
+    tab = (ctypes.c_int32 * (n * max_blocks))()
+    lens = (ctypes.c_int32 * n)()
+    slot = (ctypes.c_int64 * n)()
+    h = pool._h
+    steps = min(steps, (max_blocks * bs - 2304) // 4)  # two loops, each adds `steps` tokens per sequence
+    t_res = t_batch = t_tab = 0.0
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        for sq in seqs:
+            if lib.kvc_seq_reserve(h, sq, 1, slot) != 0:
+                raise RuntimeError("kvc_seq_reserve failed")
+        t1 = time.perf_counter()
+        if lib.kvc_build_block_tables(h, ids, n, tab, max_blocks, lens) != 0:
+            raise RuntimeError("kvc_build_block_tables failed")
+        t_tab += time.perf_counter() - t1
+        t_res += t1 - t0
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        if lib.kvc_seq_reserve_batch(h, ids, n, 1, slot) != 0:
+            raise RuntimeError("kvc_seq_reserve_batch failed")
+        t_batch += time.perf_counter() - t0
+    st = pool.stats()
+    pool.close()
+    return {"us_per_step": round((t_batch + t_tab) / steps * 1e6, 2),
+            "reserve_batch_64_us": round(t_batch / steps * 1e6, 2),
+            "reserve_64_calls_us": round(t_res / steps * 1e6, 2),
+            "build_tables_64x160_us": round(t_tab / steps * 1e6, 2), "steps": steps, "final_stats": st,
+            "note": "host CPU only, through ctypes; us_per_step = one batch reserve + one table build"}
 
 
 def measure_tiny(kvc, flush, steps):

@@ -404,6 +404,15 @@ kvc_status kvc_seq_fork(kvc_pool* pool, int64_t parent, int64_t* child);
  * (would need copy-on-write). slots_out is host memory owned by the caller.
  * Source: "KV Cache（键值缓存）" 2.3 (fixed-size blocks allocated on demand). */
 kvc_status kvc_seq_reserve(kvc_pool* pool, int64_t seq, int64_t n_new, int64_t* slots_out);
+/* kvc_seq_reserve for n distinct sequences in one call (a decode step's host
+ * work): each of seqs[0..n) gains n_new tokens, in that order, and
+ * slots_out[i * n_new + t] receives sequence i's slot for its token t (host
+ * memory, caller-owned, n * n_new entries). All or nothing: an unknown or
+ * repeated id (KVC_ERR_INVALID_ARG), a sequence whose partly filled last
+ * block is shared (KVC_ERR_UNSUPPORTED) or too few free blocks for the whole
+ * batch (KVC_ERR_NO_BLOCKS) changes nothing. The result equals n calls of
+ * kvc_seq_reserve in order. Source: "KV Cache（键值缓存）" 2.3. */
+kvc_status kvc_seq_reserve_batch(kvc_pool* pool, const int64_t* seqs, int n, int64_t n_new, int64_t* slots_out);
 /* kvc_seq_reserve with copy-on-write: if the sequence's last block is partly
  * filled and held by other sequences too, the sequence first gets a fresh
  * block (the lowest free id) in its place, drops its reference to the shared

@@ -78,6 +78,7 @@ SIGNATURES = {
     "kvc_seq_fork": (_i32, [_vp, _i64, _i64p]),
     "kvc_seq_reserve": (_i32, [_vp, _i64, _i64, _vp]),
     "kvc_seq_reserve_cow": (_i32, [_vp, _i64, _i64, _vp, _vp]),
+    "kvc_seq_reserve_batch": (_i32, [_vp, _vp, _i32, _i64, _vp]),
     "kvc_copy_blocks": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp]),
     "kvc_append_fp8": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp]),
     "kvc_decode_attention_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _f32, _i32, _i32, _i32, _i32,
@@ -422,6 +423,15 @@ class BlockPool:
         buf = (ctypes.c_int64 * max(1, n_new))()
         _check(self._lib.kvc_seq_reserve(self._h, seq, n_new, buf), "kvc_seq_reserve")
         return list(buf[:n_new])
+
+    def reserve_batch(self, seqs, n_new: int):
+        """kvc_seq_reserve_batch: n_new slots for each of the distinct sequences `seqs`, all or nothing.
+        Returns one list of slots per sequence."""
+        n = len(seqs)
+        ids = (ctypes.c_int64 * max(1, n))(*seqs)
+        buf = (ctypes.c_int64 * max(1, n * n_new))()
+        _check(self._lib.kvc_seq_reserve_batch(self._h, ids, n, n_new, buf), "kvc_seq_reserve_batch")
+        return [list(buf[i * n_new:(i + 1) * n_new]) for i in range(n)]
 
     def reserve_cow(self, seq: int, n_new: int):
         """kvc_seq_reserve_cow: (slots, copy) with copy = (shared block, fresh block) or None."""

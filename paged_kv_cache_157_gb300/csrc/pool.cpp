@@ -120,6 +120,50 @@ kvc_status kvc_seq_reserve(kvc_pool* pool, int64_t seq, int64_t n_new, int64_t* 
   return KVC_OK;
 }
 
+kvc_status kvc_seq_reserve_batch(kvc_pool* pool, const int64_t* seqs, int n, int64_t n_new, int64_t* slots_out) {
+  kvc::clear_error();
+  if (pool == nullptr) return kvc::fail(KVC_ERR_INVALID_ARG, "pool is NULL");
+  if (n < 0 || n_new < 0) return kvc::fail(KVC_ERR_INVALID_ARG, "n and n_new must be >= 0");
+  if (n == 0 || n_new == 0) return KVC_OK;
+  if (seqs == nullptr || slots_out == nullptr) return kvc::fail(KVC_ERR_INVALID_ARG, "NULL argument");
+  // check everything first, so that a refused batch changes nothing
+  const int64_t bs = pool->block_size;
+  std::vector<kvc_pool::Seq*> ss(static_cast<size_t>(n));
+  std::unordered_map<int64_t, int> seen;
+  int64_t need = 0;
+  for (int i = 0; i < n; ++i) {
+    kvc_status s = find_seq(pool, seqs[i], &ss[static_cast<size_t>(i)]);
+    if (s != KVC_OK) return s;
+    if (!seen.emplace(seqs[i], i).second)
+      return kvc::fail(KVC_ERR_INVALID_ARG, "sequence %lld appears twice", static_cast<long long>(seqs[i]));
+    const kvc_pool::Seq* sq = ss[static_cast<size_t>(i)];
+    if (sq->length % bs != 0 && pool->ref[static_cast<size_t>(sq->blocks.back())] > 1)
+      return kvc::fail(KVC_ERR_UNSUPPORTED, "sequence %lld: append into a shared, partly filled block needs "
+                       "copy-on-write", static_cast<long long>(seqs[i]));
+    need += (sq->length + n_new + bs - 1) / bs - static_cast<int64_t>(sq->blocks.size());
+  }
+  if (need > static_cast<int64_t>(pool->free_heap.size()))
+    return kvc::fail(KVC_ERR_NO_BLOCKS, "need %lld blocks, %zu free", static_cast<long long>(need),
+                     pool->free_heap.size());
+  for (int i = 0; i < n; ++i) {
+    kvc_pool::Seq* sq = ss[static_cast<size_t>(i)];
+    int64_t* out = slots_out + static_cast<int64_t>(i) * n_new;
+    const int64_t len = sq->length;
+    for (int64_t t = 0; t < n_new; ++t) {
+      const int64_t pos = len + t;
+      if (pos % bs == 0) {
+        const int64_t b = pool->free_heap.top();
+        pool->free_heap.pop();
+        pool->ref[static_cast<size_t>(b)] = 1;
+        sq->blocks.push_back(b);
+      }
+      out[t] = sq->blocks[static_cast<size_t>(pos / bs)] * bs + pos % bs;
+    }
+    sq->length = len + n_new;
+  }
+  return KVC_OK;
+}
+
 kvc_status kvc_seq_reserve_cow(kvc_pool* pool, int64_t seq, int64_t n_new, int64_t* slots_out, int64_t* copy_pair) {
   kvc::clear_error();
   kvc_pool::Seq* sq = nullptr;

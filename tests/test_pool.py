@@ -157,3 +157,54 @@ def test_config3_sharing_layout(kvc):
     rows, lens = pool.tables(seqs, 144)
     assert all(n == 2304 for n in lens)
     assert pool.refcount(rows[0][0]) == 8 and pool.refcount(rows[0][130]) == 1
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_reserve_batch_equals_sequential_reserves(kvc, seed):
+    # the batch call on one pool, single reserves (the model's) on the other: same slots, same state
+    rng = random.Random(100 + seed)
+    nblk, bs = 64, rng.choice([4, 16])
+    pool = kvc.BlockPool(nblk, bs)
+    model = PoolModel(nblk, bs)
+    live = []
+    for _ in range(6):
+        a, b = pool.add(), model.add()
+        assert a == b
+        live.append(a)
+    for _ in range(40):
+        batch = rng.sample(live, rng.randint(1, len(live)))
+        n_new = rng.choice([1, 2, bs - 1, bs + 1])
+        try:
+            expect = [model.reserve(s, n_new) for s in batch]
+            ok = True
+        except NoBlocks:
+            ok = False
+        if ok:
+            assert pool.reserve_batch(batch, n_new) == expect
+        else:
+            # the model may have served part of the batch before it ran out: rebuild it from the pool's state
+            before = pool.stats()
+            with pytest.raises(kvc.KvcError) as e:
+                pool.reserve_batch(batch, n_new)
+            assert e.value.status == kvc.ERR_NO_BLOCKS
+            assert pool.stats() == before  # all or nothing
+            break
+        _same_state(pool, model, live, nblk)
+
+
+def test_reserve_batch_refusals_change_nothing(kvc):
+    pool = kvc.BlockPool(8, 16)
+    a = pool.add()
+    pool.reserve(a, 20)
+    b = pool.fork(a)  # shares a's partly filled second block
+    c = pool.add()
+    before = pool.stats()
+    for seqs, n_new, status in (([c, c], 1, kvc.ERR_INVALID_ARG), ([c, 999], 1, kvc.ERR_INVALID_ARG),
+                                ([c, b], 1, kvc.ERR_UNSUPPORTED), ([c], 16 * 7 + 1, kvc.ERR_NO_BLOCKS)):
+        with pytest.raises(kvc.KvcError) as e:
+            pool.reserve_batch(seqs, n_new)
+        assert e.value.status == status
+        assert pool.stats() == before
+        assert pool.length(c) == 0
+    assert pool.reserve_batch([], 3) == [] and pool.reserve_batch([c], 0) == [[]]
+    assert pool.reserve_batch([c], 2) == [[2 * 16, 2 * 16 + 1]]  # lowest free block is 2
