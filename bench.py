@@ -467,12 +467,21 @@ VARIANTS = ("gqa_b32_ctx4096", "mha_shared_prefix_8x8", "gqa_long_splitk", "gqa_
             "host_pool_shared_8x8")
 
 
+def with_measured_fraction(r):
+    """Adds the decode's fraction of the measured (or fallback) HBM copy peak to a variant's record."""
+    peak, kind = peaks()
+    g = r.get("decode_gbps", r.get("gbps")) if isinstance(r, dict) else None
+    if g is not None and "error" not in r:
+        r[f"frac_of_{kind}_hbm"] = round(g / peak, 4)
+    return r
+
+
 def variants(kvc, flush, steps):
     import torch
     out = {}
     for name in VARIANTS:
         try:
-            out[name] = run_variant(kvc, name, flush, steps)
+            out[name] = with_measured_fraction(run_variant(kvc, name, flush, steps))
         except Exception as e:  # report, do not hide, a failing variant
             out[name] = {"error": f"{type(e).__name__}: {e}"}
         torch.cuda.empty_cache()
@@ -936,7 +945,8 @@ def main():
         build_lib.build()
         kvc.set_option(kvc.OPT_GQA_ENGINE, {"auto": 0, "cuda-core": 1, "tensor-core": 2}[args.gqa_engine])
         print(json.dumps({"workload": args.workload, "gqa_engine": args.gqa_engine,
-                          **run_variant(kvc, args.workload, flush_buffer(), args.steps)}), flush=True)
+                          **with_measured_fraction(run_variant(kvc, args.workload, flush_buffer(), args.steps))}),
+              flush=True)
         return
     if args.impl == "reference":
         run_reference(args)

@@ -81,7 +81,7 @@ __device__ __forceinline__ unsigned short encode_pair(float a, float b, bool int
 }
 
 template <typename T, bool INT8>
-__global__ void __launch_bounds__(256) append_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v,
+__global__ void __launch_bounds__(256) append_q8_kernel(const T* __restrict__ k, const T* __restrict__ v,
                                                          const int64_t* __restrict__ slots, int64_t num_tokens,
                                                          int n_heads, int D, int block_size, int64_t num_slots,
                                                          const float* __restrict__ k_scale, unsigned char* kc,
@@ -151,18 +151,18 @@ static void launch_q8(int grid, cudaStream_t s, kvc_dtype dtype, const void* k, 
                       unsigned int* err) {
   switch (dtype) {
     case KVC_F32:
-      append_fp8_kernel<float, INT8><<<grid, 256, 0, s>>>(static_cast<const float*>(k), static_cast<const float*>(v),
+      append_q8_kernel<float, INT8><<<grid, 256, 0, s>>>(static_cast<const float*>(k), static_cast<const float*>(v),
                                                           slot_mapping, num_tokens, n_kv_heads, head_dim, block_size,
                                                           num_slots, k_scale, kc, vc, v_scale, err);
       break;
     case KVC_F16:
-      append_fp8_kernel<__half, INT8><<<grid, 256, 0, s>>>(static_cast<const __half*>(k),
+      append_q8_kernel<__half, INT8><<<grid, 256, 0, s>>>(static_cast<const __half*>(k),
                                                            static_cast<const __half*>(v), slot_mapping, num_tokens,
                                                            n_kv_heads, head_dim, block_size, num_slots, k_scale, kc,
                                                            vc, v_scale, err);
       break;
     case KVC_BF16:
-      append_fp8_kernel<__nv_bfloat16, INT8><<<grid, 256, 0, s>>>(
+      append_q8_kernel<__nv_bfloat16, INT8><<<grid, 256, 0, s>>>(
           static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), slot_mapping, num_tokens,
           n_kv_heads, head_dim, block_size, num_slots, k_scale, kc, vc, v_scale, err);
       break;
