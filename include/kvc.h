@@ -112,6 +112,12 @@ typedef enum kvc_option {
 } kvc_option;
 kvc_status kvc_set_option(kvc_option opt, int64_t value);
 kvc_status kvc_get_option(kvc_option opt, int64_t* value);
+/* Checked mode on (enabled != 0) or off: the same as
+ * kvc_set_option(KVC_OPT_CHECKED, enabled != 0). The checks follow the input
+ * validation of the cached_attention listing of "KV缓存原理与显存估算"
+ * (knowledge point 2: non-empty input, in-range data) for the values that live
+ * in device memory. */
+kvc_status kvc_set_checked(int enabled);
 
 /* Synchronises `stream`, then returns (in *flags) and clears the error word
  * of the current device. */
@@ -341,7 +347,8 @@ kvc_status kvc_decode_attention_int8(const void* q, const void* k_cache, const v
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture. Every call then clears the counters at the start
+ * before any stream capture. The address is looked up again when the
+ * device's current context is a new one (after cudaDeviceReset, say). Every call then clears the counters at the start
  * of the array with an asynchronous memset on `stream`; the array keeps the
  * rest of the last call's contents. All calls share the one array, so calls
  * whose kernels may overlap on the GPU (different streams, or several host
@@ -390,8 +397,14 @@ typedef struct kvc_pool_stats {
   int32_t block_size;
 } kvc_pool_stats;
 
+/* A pool of num_blocks blocks of block_size token rows, all free; *pool
+ * receives a handle the caller releases with kvc_pool_destroy. Source:
+ * "KV Cache（键值缓存）" 2.3 (a shared pool of fixed-size physical blocks). */
 kvc_status kvc_pool_create(int64_t num_blocks, int block_size, kvc_pool** pool);
 void kvc_pool_destroy(kvc_pool* pool);
+/* A new empty sequence (length 0, no blocks); *seq receives its id. Source:
+ * "KV Cache（键值缓存）" 2.3 (each sequence owns a block table, empty until its
+ * first token). */
 kvc_status kvc_seq_add(kvc_pool* pool, int64_t* seq);
 /* New sequence sharing all of parent's blocks (each gains one reference);
  * KVC_ERR_INVALID_ARG for an unknown parent. Source: "KV Cache（键值缓存）"
@@ -428,7 +441,12 @@ kvc_status kvc_seq_reserve_cow(kvc_pool* pool, int64_t seq, int64_t n_new, int64
  * the free list at zero. KVC_ERR_INVALID_ARG for an unknown sequence.
  * Source: "KV Cache（键值缓存）" 2.3. */
 kvc_status kvc_seq_free(kvc_pool* pool, int64_t seq);
+/* Tokens held by `seq` (the useful rows of its blocks). Source:
+ * "KV缓存原理与显存估算" knowledge point 1 (useful bytes count each sequence's
+ * own length, not the block-rounded size). */
 kvc_status kvc_seq_length(kvc_pool* pool, int64_t seq, int64_t* length);
+/* Number of sequences holding `block` (0: free). Source: "KV Cache（键值缓存）"
+ * 2.3 (shared blocks are counted by reference). */
 kvc_status kvc_block_refcount(kvc_pool* pool, int64_t block, int32_t* refcount);
 /* Writes table rows (int32 [n, max_blocks], unused entries 0) and lengths
  * (int32 [n]) for the given sequences, into caller-owned host memory.
@@ -437,6 +455,11 @@ kvc_status kvc_block_refcount(kvc_pool* pool, int64_t block, int32_t* refcount);
  * from logical to physical blocks). */
 kvc_status kvc_build_block_tables(kvc_pool* pool, const int64_t* seqs, int n, int32_t* table_out,
                                   int max_blocks, int32_t* lens_out);
+/* Pool counters: free and unique (referenced) blocks, table entries, useful
+ * tokens. (Not named kvc_pool_stats: C keeps functions and typedefs in one
+ * name space, and that name is the struct's.) Source: the closing section of "KV缓存原理与显存估算" (memory counted
+ * over unique physical blocks, not table entries) and knowledge point 1
+ * (useful tokens against allocated slots). */
 kvc_status kvc_pool_get_stats(kvc_pool* pool, kvc_pool_stats* stats);
 
 /* Host helper: slots of (row, position) pairs for an existing host-side

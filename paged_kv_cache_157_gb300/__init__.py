@@ -54,6 +54,7 @@ SIGNATURES = {
     "kvc_last_error_message": (ctypes.c_char_p, []),
     "kvc_set_option": (_i32, [_i32, _i64]),
     "kvc_get_option": (_i32, [_i32, _i64p]),
+    "kvc_set_checked": (_i32, [_i32]),
     "kvc_get_error_flags": (_i32, [_vp, _u32p]),
     "kvc_append": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp]),
     "kvc_append_latent": (_i32, [_vp, _vp, _i64, _vp, _i64, _i32, _i32, _i32, _i32, _vp]),

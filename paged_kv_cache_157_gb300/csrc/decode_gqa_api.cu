@@ -1,5 +1,6 @@
 // Host side of kvc_decode_attention: argument checks, work planning,
 // workspace carve-up and launch.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -431,24 +432,54 @@ namespace {
 constexpr size_t kStaticScratchBytes = 16u << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
+// Device address of g_decode_scratch per device, with the context it was
+// looked up in: a device reset (or a destroyed and recreated primary
+// context) loads the module again, so an address from an older context is
+// stale and is looked up again.
+struct StaticScratch {
+  CUcontext ctx = nullptr;
+  void* ptr = nullptr;
+};
 std::mutex g_static_mutex;
-std::vector<void*> g_static_ptr;  // device address of g_decode_scratch, per device
+std::vector<StaticScratch> g_static;
 
-// Looks up (once per device, with that device current) the device address of
-// the scratch array. Host code must not use the symbol itself as a pointer.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static std::once_flag once;
+  static CtxGetCurrentFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  });
+  return fn;
+}
+
+// Looks up (once per device and context, with that device current) the
+// device address of the scratch array. Host code must not use the symbol
+// itself as a pointer: on the host it names a host-side stand-in.
 kvc_status static_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (get_ctx == nullptr) return fail(KVC_ERR_CUDA, "cuCtxGetCurrent is unavailable");
   std::lock_guard<std::mutex> lock(g_static_mutex);
-  if (dev >= static_cast<int>(g_static_ptr.size())) g_static_ptr.resize(dev + 1, nullptr);
-  if (g_static_ptr[dev] == nullptr) {
+  if (dev >= static_cast<int>(g_static.size())) g_static.resize(dev + 1);
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "cuCtxGetCurrent failed");
+  if (ctx == nullptr || g_static[dev].ptr == nullptr || g_static[dev].ctx != ctx) {
     void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    e = cudaGetSymbolAddress(&ptr, g_decode_scratch);  // also makes the device's primary context current
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
-    g_static_ptr[dev] = ptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "cuCtxGetCurrent failed");
+    g_static[dev].ctx = ctx;
+    g_static[dev].ptr = ptr;
   }
-  *out = g_static_ptr[dev];
+  *out = g_static[dev].ptr;
   return KVC_OK;
 }
 

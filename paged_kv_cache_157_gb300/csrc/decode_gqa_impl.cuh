@@ -659,6 +659,13 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
     s_misc[2] = 0;
   }
   fence_barrier_init();
+  // Launched right behind the previous kernel of the stream (programmatic
+  // stream serialisation: the append of this step, or whatever wrote the
+  // lengths, tables or queries on the device), the kernel becomes resident and
+  // sets up its barriers while that grid runs. Every thread then waits for
+  // the grid to finish (its writes become visible) before it reads or writes
+  // any caller buffer.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid < 2 && !p.unit_mode) {
     // Warm L2 with the block-table line this CTA most likely reads first (a
     // guess that assumes equal lengths; it only overlaps the length scan).
@@ -811,10 +818,6 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
   // warp waits for another except through the "full" barriers.
   const int n_first = total < S ? total : S;
   if (w == 0) {
-    // Launched right behind the append of this step (programmatic stream
-    // serialisation), the prologue above overlapped it; the cached rows are
-    // read only after it has finished. Every later copy follows these.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = 0; i < n_first; ++i) {
       const int src = __shfl_sync(full, w_src0, i);
       const int qo = __shfl_sync(full, w_q0, i);

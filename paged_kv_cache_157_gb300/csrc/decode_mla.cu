@@ -425,6 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // Launched behind the previous kernel of the stream (programmatic stream
+  // serialisation), the set-up above overlapped it; every thread waits for
+  // that grid to finish before it reads or writes any caller buffer.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (blockIdx.x == 0) {
     for (int b = tid; b < p.batch; b += blockDim.x) {
       const int n = __ldg(p.context_lens + b);
@@ -470,8 +474,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      // launched behind the append of this step: read cached rows only after it
-      asm volatile("griddepcontrol.wait;" ::: "memory");
       uint32_t g = 0, seg_i = 0;
       uint32_t issued[kStages] = {};
       bool q_pending = false;

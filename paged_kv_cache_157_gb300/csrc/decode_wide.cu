@@ -279,6 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // Launched behind the previous kernel of the stream (programmatic stream
+  // serialisation), the set-up above overlapped it; every thread waits for
+  // that grid to finish before it reads or writes any caller buffer.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (blockIdx.x == 0) {
     for (int b = tid; b < p.batch; b += blockDim.x) {
       const int n = __ldg(p.context_lens + b);
@@ -333,10 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     // The whole warp: lane i reads the table entry of page i of the next tile
     // before the stage is free (hiding that load), lane 0 arms the stage's
-    // barrier, then lane i issues the four copies of page i. Launched behind
-    // the append of this step, the kernel reads cached rows only once that
-    // grid has finished.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // barrier, then lane i issues the four copies of page i.
     uint32_t g = 0;
     uint32_t issued[kStages] = {};
     Segment sg;

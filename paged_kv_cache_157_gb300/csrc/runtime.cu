@@ -127,6 +127,8 @@ kvc_status kvc_set_option(kvc_option opt, int64_t value) {
   return KVC_OK;
 }
 
+kvc_status kvc_set_checked(int enabled) { return kvc_set_option(KVC_OPT_CHECKED, enabled != 0 ? 1 : 0); }
+
 kvc_status kvc_get_option(kvc_option opt, int64_t* value) {
   int o = static_cast<int>(opt);
   if (o < 0 || o > 3 || value == nullptr) return kvc::fail(KVC_ERR_INVALID_ARG, "bad option query");

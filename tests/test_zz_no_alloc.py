@@ -58,6 +58,55 @@ def test_static_scratch_matches_workspace_path_twice(kvc):
         assert kvc.get_error_flags() == 0
 
 
+def test_static_scratch_on_the_tensor_core_engine(kvc):
+    # 64 query / 8 kv heads: 8 queries per kv head, which the tensor-core
+    # kernel takes (forced here at any size); its counters and records sit in
+    # the same built-in array in a different layout.
+    for o in (kvc.OPT_BLOCKS_PER_CTA, kvc.OPT_MAX_CTAS, kvc.OPT_CHECKED):
+        kvc.set_option(o, 0)
+    kvc.set_option(kvc.OPT_GQA_ENGINE, 2)
+    try:
+        scale = 1.0 / math.sqrt(128)
+        cases = [W.gqa_case(8, 64, 8, 128, 16, [4096, 3000, 1, 17, 2500, 4096, 640, 1024], "bf16", seed=47),
+                 W.gqa_case(4, 64, 8, 128, 16, (512, 4096), "bf16", seed=48)]
+        for case in cases:
+            dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in case.items()}
+            ref = _reference(kvc, dev, scale)
+            for _ in range(2):
+                out = torch.full_like(ref, float("nan"))
+                assert _c_abi_static(kvc, dev, scale, out) == kvc.OK, kvc.raw().kvc_last_error_message()
+                torch.cuda.synchronize()
+                err = float((out - ref).abs().max())
+                assert err <= 2e-3, err
+            assert kvc.get_error_flags() == 0
+    finally:
+        kvc.set_option(kvc.OPT_GQA_ENGINE, 0)
+
+
+def test_static_scratch_after_a_call_with_a_bad_block_id(kvc):
+    # A call that meets an out-of-pool block id flags it (and leaves its output
+    # undefined); the next call with valid inputs must match the workspace path.
+    for o in (kvc.OPT_BLOCKS_PER_CTA, kvc.OPT_MAX_CTAS, kvc.OPT_CHECKED, kvc.OPT_GQA_ENGINE):
+        kvc.set_option(o, 0)
+    scale = 1.0 / math.sqrt(128)
+    case = W.gqa_case(6, 32, 8, 128, 16, [3000, 40, 1, 4096, 777, 2048], "bf16", seed=49)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in case.items()}
+    ref = _reference(kvc, dev, scale)
+    torch.cuda.synchronize()
+    assert kvc.get_error_flags() == 0
+    bad = dict(dev)
+    bad["block_tables"] = dev["block_tables"].clone()
+    bad["block_tables"][3, 10] = case["num_blocks"] + 5  # outside the pool
+    out = torch.empty_like(ref)
+    assert _c_abi_static(kvc, bad, scale, out) == kvc.OK
+    assert kvc.get_error_flags() & kvc.FLAG_BAD_BLOCK
+    out = torch.full_like(ref, float("nan"))
+    assert _c_abi_static(kvc, dev, scale, out) == kvc.OK
+    torch.cuda.synchronize()
+    assert float((out - ref).abs().max()) <= 2e-3
+    assert kvc.get_error_flags() == 0
+
+
 def test_static_scratch_refuses_oversized_shapes(kvc):
     kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, 1)  # one cache block per CTA: far more records than 16 MiB hold
     try:
