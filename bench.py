@@ -775,7 +775,8 @@ def traffic_from_profile():
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("decode_gqa_impl.cuh", "decode_gqa.h", "kvc_device.cuh", "decode_gqa_api.cu", "decode_gqa_launch.cuh"):
+    for f in ("decode_gqa_mma.cuh", "decode_gqa_impl.cuh", "decode_gqa.h", "kvc_device.cuh", "decode_gqa_api.cu",
+              "decode_gqa_mma_launch.cuh"):
         h.update(open(os.path.join(ROOT, "paged_kv_cache_157_gb300", "csrc", f), "rb").read())
     return h.hexdigest()
 
@@ -873,7 +874,7 @@ def run_kvc(args):
         "frac_of_8tbs": round(value / NOMINAL_HBM_GBS, 4),
         "seq_layer_steps_per_s": round(world * m["batch"] / (ms / 1e3), 1),
         "bytes_per_step": per_step,
-        "roofline": {"bound": "hbm", "kernel": "kvc_decode_attention (gqa_decode_kernel, split-K merge fused in)",
+        "roofline": {"bound": "hbm", "kernel": "kvc_decode_attention (gqa_mma_kernel, split-K merge fused in)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "traffic": traffic_from_profile(), "algorithmic_bytes_per_launch": dec_b,
@@ -942,9 +943,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=("main", TARGET) + VARIANTS, default="main",
                     help="time one other workload alone (prints its measurement, not the contract line)")
-    ap.add_argument("--gqa-engine", choices=("auto", "cuda-core", "tensor-core"), default="auto",
-                    help="with --workload: 'cuda-core' keeps wide query groups off the tensor-core kernel, "
-                         "'tensor-core' puts them on it at any size")
+    ap.add_argument("--gqa-engine", choices=("auto", "cuda-core", "tensor-core", "warp-mma"), default="auto",
+                    help="with --workload: 'cuda-core' forces the CUDA-core kernel, 'tensor-core' puts wide query "
+                         "groups on the tcgen05 kernel at any size, 'warp-mma' keeps them on the warp-MMA kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -952,7 +953,7 @@ def main():
         import paged_kv_cache_157_gb300 as kvc
         from paged_kv_cache_157_gb300 import build_lib
         build_lib.build()
-        kvc.set_option(kvc.OPT_GQA_ENGINE, {"auto": 0, "cuda-core": 1, "tensor-core": 2}[args.gqa_engine])
+        kvc.set_option(kvc.OPT_GQA_ENGINE, {"auto": 0, "cuda-core": 1, "tensor-core": 2, "warp-mma": 3}[args.gqa_engine])
         print(json.dumps({"workload": args.workload, "gqa_engine": args.gqa_engine,
                           **with_measured_fraction(run_variant(kvc, args.workload, flush_buffer(), args.steps))}),
               flush=True)

@@ -100,15 +100,35 @@ typedef enum kvc_option {
   KVC_OPT_BLOCKS_PER_CTA = 1,
   /* Upper bound on decode CTAs (0 = automatic, SM count x resident CTAs). */
   KVC_OPT_MAX_CTAS = 2,
-  /* GQA decode engine. The tensor-core kernel takes bf16/f16 caches,
-   * head_dim 128, block sizes 16/32/64/128, no window, and kv heads with 8 to
-   * 32 queries (qn = n_tokens x n_q_heads / n_kv_heads). 0 (default) =
-   * automatic: that kernel where it applies and the cache it may read
-   * (batch x n_kv_heads x max_blocks_per_seq x block_size rows of K and V) is
-   * at least 512 MiB / qn, else the CUDA-core kernel, whose fixed cost per
-   * call is lower; 1 = always the CUDA-core kernel; 2 = the tensor-core
-   * kernel wherever it applies, at any size. */
-  KVC_OPT_GQA_ENGINE = 3
+  /* GQA decode engine. Three kernels compute the same decode:
+   *  - the tcgen05 tensor-core kernel: bf16/f16 caches, head_dim 128, block
+   *    sizes 16/32/64/128, no window, kv heads with 8 to 32 queries (qn =
+   *    n_tokens x n_q_heads / n_kv_heads);
+   *  - the warp-MMA kernel: bf16/f16 caches, head_dim 128, block sizes that
+   *    are multiples of 16 up to 128 (every feature: windows, several new
+   *    tokens, shared prefixes);
+   *  - the CUDA-core kernel: every dtype, head size and feature.
+   * 0 (default) = automatic: the warp-MMA kernel where it applies and qn is
+   * 2 to 16; else the tensor-core kernel where it applies and the cache it
+   * may read (batch x n_kv_heads x max_blocks_per_seq x block_size rows of K
+   * and V) is at least 512 MiB / qn; else the warp-MMA kernel where it
+   * applies (qn > 32); else the CUDA-core kernel; 1 = always the CUDA-core
+   * kernel;
+   * 2 = the tensor-core kernel wherever it applies, at any size (else as 0);
+   * 3 = the warp-MMA kernel wherever it applies, else the CUDA-core kernel. */
+  KVC_OPT_GQA_ENGINE = 3,
+  /* Warp-MMA kernel work split. Each CTA streams a static range of the cache
+   * blocks; optionally a share of them is instead cut into chunks that CTAs
+   * claim as they finish, so faster SMs take more of it. Every claimed chunk
+   * that cuts a (sequence, kv-head chunk) unit leaves a partial record that
+   * the unit's last contributor merges, so small chunks trade balance for
+   * merge work at the end of the launch. DYNAMIC_SHARE: the claimed part in
+   * 1/256 of all blocks (0 = automatic, currently none; 1..255 as given; 256
+   * = none). DYNAMIC_CHUNK: blocks (of one kv-head chunk) per claimed chunk
+   * (0 = automatic, 8; N >= 1 as given, and then used at any size).
+   * Process-wide. */
+  KVC_OPT_DYNAMIC_SHARE = 4,
+  KVC_OPT_DYNAMIC_CHUNK = 5
 } kvc_option;
 kvc_status kvc_set_option(kvc_option opt, int64_t value);
 kvc_status kvc_get_option(kvc_option opt, int64_t* value);

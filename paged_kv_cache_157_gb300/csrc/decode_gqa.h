@@ -2,6 +2,7 @@
 // the host planner and the device code.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -44,6 +45,11 @@ struct GqaParams {
   const float* k_scale;  // FP8 caches: per-channel K scales [n_kv_heads, head_dim]
   const float* v_scale;  // FP8 caches: per-token V scales [num_blocks, n_kv_heads, block_size]
   float qscale;   // scale * log2(e)
+  // warp-MMA kernel: dynamic tail of the work split
+  unsigned int* sched;  // [claim counter, finished CTAs] in the workspace; zero between calls
+  int dyn_share;        // positions claimed at run time, in 1/256 of all (0: none)
+  int dyn_chunk;        // positions per claimed chunk (0: no dynamic tail)
+  int dyn_min_static;   // keep the dynamic tail only if every CTA still gets this many static positions
 };
 
 #ifndef KVC_GQA_WARPS
@@ -133,6 +139,13 @@ kvc_status wide_decode(const WideArgs& a, DeviceInfo* dev);
 template <typename T, bool EXT>
 kvc_status gqa_dispatch(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
                         int* occ);
+// Warp-MMA kernel (bf16/f16 caches, head_dim 128; tk / tv: TMA maps over the
+// K and V pools as [num_blocks * n_kv_heads * block_size rows, 128] with
+// [hc * block_size x 64] boxes and the 128-byte swizzle).
+template <typename T, bool EXT>
+kvc_status gqa_mma_dispatch(const GqaParams& p, int GH, int grid, size_t smem, const CUtensorMap& tk,
+                            const CUtensorMap& tv, cudaStream_t stream, int mode, int* occ);
+
 // FP8 e4m3 caches with bf16 queries (head_dim 64, 128 or 256).
 kvc_status gqa_dispatch_fp8(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
                             int* occ);

@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "decode_gqa.h"
+#include "decode_gqa_mma.cuh"
 #include "kvc_device.cuh"
 
 namespace kvc {
@@ -26,6 +27,8 @@ constexpr int kMaxTokens = 256;  // new tokens per sequence in one multi-token c
 
 struct GqaPlan {
   int GH = 1, n_hsub = 1, stages = 2, hc = 1, n_chunks = 1;
+  int ctas_per_sm = kMaxCtasPerSm;  // most CTAs an SM can hold with this plan's shared memory
+  int dyn_share = 0, dyn_chunk = 0;  // warp-MMA kernel: dynamic tail of the work split
   int64_t units = 0;
   size_t smem = 0;
   size_t rec_bytes_per_cta = 0;  // two records per CTA
@@ -83,6 +86,127 @@ kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, in
   pl->smem = L.total;
   pl->rec_bytes_per_cta =
       2ull * gqa_max_chunk(pl->GH) * pl->GH * (static_cast<size_t>(D) + 2) * sizeof(float);
+  return KVC_OK;
+}
+
+// Warp-MMA kernel: bf16/f16 caches, head_dim 128, block sizes that are
+// multiples of 16 up to 128, and pool rows addressable by a TMA coordinate.
+bool mma_supported(kvc_dtype dtype, int head_dim, int block_size, int64_t num_blocks, int n_kv_heads, int qn) {
+  const int64_t engine = option(KVC_OPT_GQA_ENGINE);
+  if (engine == 1) return false;
+  // One query per kv head (MHA): the CUDA-core kernel, whose two CTAs per SM
+  // read blocks shared by forked sequences close enough in time to hit in L2
+  // (measured on the 64-fork batch: 244 us against 348 us), unless forced.
+  if (qn == 1 && engine != 3) return false;
+  if (dtype != KVC_BF16 && dtype != KVC_F16) return false;
+  if (head_dim != 128 || block_size % 16 != 0 || block_size > 128) return false;
+  return num_blocks * n_kv_heads * block_size < (1ll << 31);
+}
+
+void mma_dynamic(GqaPlan* pl);
+
+#ifndef KVC_MMA_DYN_SHARE
+#define KVC_MMA_DYN_SHARE 256
+#endif
+constexpr int kDefaultDynShare = KVC_MMA_DYN_SHARE;  // 256: static ranges only
+
+// kMmaCtasPerSm CTAs per SM, each with the deepest ring that fits its share
+// of shared memory: a stage holds the K and V pages of hc kv heads of one
+// block (each a [hc * block_size x 64] box pair, at most 256 rows per box)
+// and the unit's query rows.
+kvc_status make_plan_mma(int batch, int n_q_heads, int n_kv_heads, int bs, int q_elt, int max_smem, GqaPlan* pl,
+                         int n_tok = 1) {
+  const int group = n_tok * (n_q_heads / n_kv_heads);
+  pl->GH = head_subgroup(group);
+  pl->n_hsub = group / pl->GH;
+  int hc = 1;
+  while (hc * 2 <= mma_max_chunk(pl->GH) && n_kv_heads % (hc * 2) == 0 && hc * 2 * bs <= 256) hc *= 2;
+  const int share = std::min(max_smem, (228 * 1024) / kMmaCtasPerSm - 1024);
+  int S = 0;
+  for (;;) {
+    S = 8;
+    while (S > 1 && gqa_mma_smem_layout(q_elt, pl->GH, bs, hc, S, batch).total > static_cast<size_t>(share)) --S;
+    if (S >= 3 || hc == 1) break;
+    hc /= 2;  // keep at least three stages in flight
+  }
+  while (S > 1 && gqa_mma_smem_layout(q_elt, pl->GH, bs, hc, S, batch).total > static_cast<size_t>(max_smem)) --S;
+  const GqaMmaSmem L = gqa_mma_smem_layout(q_elt, pl->GH, bs, hc, S, batch);
+  if (L.total > static_cast<size_t>(max_smem))
+    return fail(KVC_ERR_UNSUPPORTED, "block_size %d needs %zu bytes of shared memory (max %d)", bs, L.total, max_smem);
+  pl->hc = hc;
+  pl->n_chunks = n_kv_heads / hc;
+  pl->units = static_cast<int64_t>(batch) * pl->n_chunks * pl->n_hsub;
+  pl->stages = S;
+  pl->smem = L.total;
+  pl->rec_bytes_per_cta = 2ull * mma_max_chunk(pl->GH) * pl->GH * (128 + 2) * sizeof(float);
+  // an SM holds 228 KB of shared memory (1 KB of it reserved per CTA); the
+  // kernel's ~250 registers per thread allow two 128-thread CTAs at most
+  pl->ctas_per_sm = std::max(1, std::min<int>(kMmaCtasPerSm, static_cast<int>((228 * 1024) / (L.total + 1024))));
+  mma_dynamic(pl);
+  return KVC_OK;
+}
+
+// Dynamic tail of the warp-MMA work split, from the options: a quarter of
+// the positions in chunks of 8 by default; none when the caller forced a
+// block count per CTA (unless a chunk size is forced too).
+void mma_dynamic(GqaPlan* pl) {
+  const int64_t share = option(KVC_OPT_DYNAMIC_SHARE), chunk = option(KVC_OPT_DYNAMIC_CHUNK);
+  pl->dyn_share = share == 0 ? kDefaultDynShare : static_cast<int>(share);
+  pl->dyn_chunk = chunk == 0 ? 8 : static_cast<int>(chunk);
+  if (pl->dyn_share >= 256 || (option(KVC_OPT_BLOCKS_PER_CTA) > 0 && chunk == 0)) pl->dyn_share = pl->dyn_chunk = 0;
+}
+
+// Workers of the warp-MMA split: G static ranges plus at most K claimed
+// chunks, K bounded through the table width (the most the host knows about
+// the lengths).
+int64_t mma_workers(const GqaPlan& pl, int64_t G, int max_blocks) {
+  if (pl.dyn_chunk == 0) return G;
+  const int64_t n_max = pl.units * max_blocks;
+  return G + (n_max * pl.dyn_share / 256 + pl.dyn_chunk - 1) / pl.dyn_chunk;
+}
+
+// Bytes of the counter region of the warp-MMA kernel: the per-unit counters,
+// then 256 bytes holding the claim counter and the finished-CTA count.
+size_t mma_counter_bytes(int batch, int n_kv_heads, const GqaPlan& pl) {
+  return counter_bytes(batch, n_kv_heads, pl) + 256;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// TMA maps over the K and V pools as [num_blocks * n_kv_heads * block_size
+// rows, 128] with [rows_per_box x 64] boxes and the 128-byte swizzle.
+kvc_status pool_maps(const void* k_cache, const void* v_cache, int64_t num_blocks, int n_kv_heads, int block_size,
+                     int rows_per_box, kvc_dtype dtype, CUtensorMap* tk, CUtensorMap* tv) {
+  EncodeTiledFn encode = encode_tiled_fn();
+  if (encode == nullptr) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const CUtensorMapDataType dt = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(num_blocks * n_kv_heads * block_size)};
+  const cuuint64_t strides[1] = {256};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(rows_per_box)};
+  const cuuint32_t es[2] = {1, 1};
+  for (int i = 0; i < 2; ++i) {
+    CUresult r = encode(i == 0 ? tk : tv, dt, 2, const_cast<void*>(i == 0 ? k_cache : v_cache), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(KVC_ERR_CUDA, "tensor map for the %s cache: CUresult %d", i ? "V" : "K", static_cast<int>(r));
+  }
   return KVC_OK;
 }
 
@@ -156,14 +280,10 @@ kvc_status occupancy_for(int dt, const GqaParams& p, int D, const GqaPlan& pl, i
 
 }  // namespace
 
-}  // namespace kvc
-
-extern "C" {
-
-kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
-                                     int max_blocks_per_seq, size_t* bytes) {
-  using namespace kvc;
-  clear_error();
+// Workspace bytes for every engine's plan; with_dynamic = false leaves out the
+// records of the warp-MMA kernel's claimed chunks (it then splits statically).
+kvc_status decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, bool with_dynamic, size_t* bytes) {
   if (bytes == nullptr) return fail(KVC_ERR_INVALID_ARG, "bytes is NULL");
   kvc_status s = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq);
   if (s != KVC_OK) return s;
@@ -176,6 +296,17 @@ kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, i
   const int64_t G = plan_ctas(dev, kMaxCtasPerSm, static_cast<int64_t>(batch) * n_kv_heads * pl.n_hsub,
                              max_blocks_per_seq);
   *bytes = align_up(counter_bytes(batch, n_kv_heads, pl) + static_cast<size_t>(G) * pl.rec_bytes_per_cta, 256);
+  // the warp-MMA kernel's records (up to 8 query heads per warp, and the
+  // claimed chunks' records) may be larger
+  GqaPlan pm;
+  if (head_dim == 128 && block_size % 16 == 0 && block_size <= 128 &&
+      make_plan_mma(batch, n_q_heads, n_kv_heads, block_size, 2, dev->max_smem_optin, &pm) == KVC_OK) {
+    const int64_t Gm = plan_ctas(dev, pm.ctas_per_sm, pm.units, max_blocks_per_seq);
+    const int64_t Wm = with_dynamic ? mma_workers(pm, Gm, max_blocks_per_seq) : Gm;
+    *bytes = std::max(*bytes, align_up(mma_counter_bytes(batch, n_kv_heads, pm) +
+                                           static_cast<size_t>(Wm) * pm.rec_bytes_per_cta, 256));
+  }
+  clear_error();
   // the tensor-core kernel for wide groups (any dtype it takes) may need more
   // (n_q_heads here already counts every new token of a multi-token call)
   if (wide_supported(batch, n_q_heads, n_kv_heads, head_dim, block_size, 1, KVC_BF16))
@@ -183,6 +314,17 @@ kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, i
                                                             max_blocks_per_seq, 1),
                                        256));
   return KVC_OK;
+}
+
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                     int max_blocks_per_seq, size_t* bytes) {
+  kvc::clear_error();
+  return kvc::decode_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, true,
+                                     bytes);
 }
 
 }  // extern "C"
@@ -230,7 +372,15 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
 
   DeviceInfo* dev = nullptr;
   if ((s = current_device(&dev)) != KVC_OK) return s;
-  if (!fp8 && window == 0 && ex->row_div == 0 &&
+  // Engine: the warp-MMA kernel for up to 16 queries per kv head (measured
+  // faster than the tcgen05 kernel there: 260 against 270 us on the long
+  // split-K batch at 8, 118 against 125 us on the 4-token step at 16), the
+  // tcgen05 kernel for 17 to 32 (where the warp-MMA kernel would read the
+  // pages once per 16 queries), the CUDA-core kernel for the rest.
+  const int qn = n_tok * (n_q_heads / n_kv_heads);
+  const bool use_mma = !fp8 && mma_supported(dtype, head_dim, block_size, num_blocks, n_kv_heads, qn);
+  const bool force_wide = option(KVC_OPT_GQA_ENGINE) == 2;
+  if (!fp8 && window == 0 && ex->row_div == 0 && (force_wide || !use_mma || qn > 16) &&
       wide_preferred(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, n_tok, dtype)) {
     WideArgs a{};
     a.q = q;
@@ -259,9 +409,14 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   const int q_elt = static_cast<int>(dtype_size(dtype));
   const int elt = fp8 ? 1 : q_elt;
   GqaPlan pl;
-  if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, elt, q_elt, fp8 ? 4 : 0,
-                     dev->max_smem_optin, &pl, n_tok)) != KVC_OK)
+  if (use_mma) {
+    if ((s = make_plan_mma(batch, n_q_heads, n_kv_heads, block_size, q_elt, dev->max_smem_optin, &pl, n_tok)) !=
+        KVC_OK)
+      return s;
+  } else if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, elt, q_elt, fp8 ? 4 : 0,
+                            dev->max_smem_optin, &pl, n_tok)) != KVC_OK) {
     return s;
+  }
 
   GqaParams p{};
   p.q = q;
@@ -294,20 +449,52 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
 
   int occ = 1;
-  if ((s = occupancy_for(fp8 ? (ex->int8 ? -2 : -1) : static_cast<int>(dtype), p, head_dim, pl, &occ)) != KVC_OK)
+  CUtensorMap tk, tv;
+  const bool ext = uses_ext(p);
+  if (use_mma) {
+    if ((s = pool_maps(k_cache, v_cache, num_blocks, n_kv_heads, block_size, pl.hc * block_size, dtype, &tk, &tv)) !=
+        KVC_OK)
+      return s;
+    s = dtype == KVC_BF16 ? (ext ? gqa_mma_dispatch<__nv_bfloat16, true>(p, pl.GH, 0, pl.smem, tk, tv, nullptr, 1, &occ)
+                                 : gqa_mma_dispatch<__nv_bfloat16, false>(p, pl.GH, 0, pl.smem, tk, tv, nullptr, 1, &occ))
+                          : (ext ? gqa_mma_dispatch<__half, true>(p, pl.GH, 0, pl.smem, tk, tv, nullptr, 1, &occ)
+                                 : gqa_mma_dispatch<__half, false>(p, pl.GH, 0, pl.smem, tk, tv, nullptr, 1, &occ));
+    if (s != KVC_OK) return s;
+  } else if ((s = occupancy_for(fp8 ? (ex->int8 ? -2 : -1) : static_cast<int>(dtype), p, head_dim, pl, &occ)) !=
+             KVC_OK) {
     return s;
+  }
+  if (use_mma) occ = std::min(occ, pl.ctas_per_sm);  // never more records than the size query counted
   int64_t G = plan_ctas(dev, occ, pl.units, max_blocks_per_seq);
-  const size_t cbytes = counter_bytes(batch, n_kv_heads, pl);
-  G = std::min<int64_t>(G, workspace_bytes > cbytes
-                               ? static_cast<int64_t>((workspace_bytes - cbytes) / pl.rec_bytes_per_cta)
-                               : 0);
-  const int HS = gqa_max_chunk(pl.GH) * pl.GH;  // query heads per record
+  const size_t cbytes = use_mma ? mma_counter_bytes(batch, n_kv_heads, pl) : counter_bytes(batch, n_kv_heads, pl);
+  const int64_t rec_fit = workspace_bytes > cbytes
+                              ? static_cast<int64_t>((workspace_bytes - cbytes) / pl.rec_bytes_per_cta)
+                              : 0;
+  int64_t W = G;  // record slots: one pair per worker
+  if (use_mma) {
+    W = mma_workers(pl, G, max_blocks_per_seq);
+    if (W > rec_fit) {  // no room for the claimed chunks' records: static ranges only
+      pl.dyn_share = pl.dyn_chunk = 0;
+      W = G;
+    }
+  }
+  G = std::min<int64_t>(G, rec_fit);
+  W = std::max<int64_t>(W, G);
+  const int HS = (use_mma ? mma_max_chunk(pl.GH) : gqa_max_chunk(pl.GH)) * pl.GH;  // query heads per record
   int grid;
   if (G >= 1) {
     p.unit_mode = 0;
     p.counters = static_cast<unsigned int*>(workspace);
+    if (use_mma) {
+      p.sched = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + cbytes - 256);
+      p.dyn_share = pl.dyn_share;
+      p.dyn_chunk = pl.dyn_chunk;
+      // automatic split: claimed chunks only when every CTA keeps two rings'
+      // worth of static work; a forced chunk size applies at any size
+      p.dyn_min_static = option(KVC_OPT_DYNAMIC_CHUNK) > 0 ? 0 : 2 * pl.stages;
+    }
     p.rec_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + cbytes);
-    p.rec_ml = p.rec_o + static_cast<size_t>(G) * 2 * HS * head_dim;
+    p.rec_ml = p.rec_o + static_cast<size_t>(W) * 2 * HS * head_dim;
     grid = static_cast<int>(G);
   } else {
     p.unit_mode = 1;
@@ -319,13 +506,21 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   if (num_blocks * n_kv_heads >= (1ll << 31))
     return fail(KVC_ERR_UNSUPPORTED, "num_blocks x n_kv_heads must be below 2^31");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (use_mma) {
+    s = dtype == KVC_BF16 ? (ext ? gqa_mma_dispatch<__nv_bfloat16, true>(p, pl.GH, grid, pl.smem, tk, tv, st, 0, nullptr)
+                                 : gqa_mma_dispatch<__nv_bfloat16, false>(p, pl.GH, grid, pl.smem, tk, tv, st, 0, nullptr))
+                          : (ext ? gqa_mma_dispatch<__half, true>(p, pl.GH, grid, pl.smem, tk, tv, st, 0, nullptr)
+                                 : gqa_mma_dispatch<__half, false>(p, pl.GH, grid, pl.smem, tk, tv, st, 0, nullptr));
+    if (s != KVC_OK) return s;
+    return finish_call(st);
+  }
   if (fp8) {
     s = ex->int8 ? gqa_dispatch_int8(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr)
                  : gqa_dispatch_fp8(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr);
     if (s != KVC_OK) return s;
     return finish_call(st);
   }
-  const bool win = uses_ext(p);
+  const bool win = ext;
   switch (dtype) {
     case KVC_F32:
       s = win ? gqa_dispatch<float, true>(p, head_dim, pl.GH, grid, pl.smem, st, 0, nullptr)
@@ -496,9 +691,11 @@ kvc_status kvc_decode_attention_static(const void* q, const void* k_cache, const
   using namespace kvc;
   clear_error();
   if (!dtype_ok(dtype) || !dtype_ok(out_dtype)) return fail(KVC_ERR_INVALID_ARG, "unknown dtype");
+  // The least scratch these shapes need: without room for the records of
+  // claimed chunks the warp-MMA kernel splits its work statically.
   size_t need = 0;
-  kvc_status s = kvc_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                                           &need);
+  kvc_status s =
+      decode_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, false, &need);
   if (s != KVC_OK) return s;
   if (need > kStaticScratchBytes)
     return fail(KVC_ERR_WORKSPACE,
@@ -517,7 +714,7 @@ kvc_status kvc_decode_attention_static(const void* q, const void* k_cache, const
       KVC_OK)
     return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(scratch, 0, counter_bytes(batch, n_kv_heads, pl), st);
+  cudaError_t e = cudaMemsetAsync(scratch, 0, mma_counter_bytes(batch, n_kv_heads, pl), st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(decode scratch counters)");
   return kvc_decode_attention(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale,
                               n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, dtype, out, out_dtype, scratch,

@@ -39,6 +39,19 @@
 #include "decode_gqa_impl.cuh"
 
 namespace kvc {
+
+#ifndef KVC_MMA_CTAS_PER_SM
+#define KVC_MMA_CTAS_PER_SM 1
+#endif
+#ifndef KVC_MMA_WARPS
+#define KVC_MMA_WARPS 8
+#endif
+// Resident CTAs per SM the register and shared-memory budgets aim at, and the
+// consumer warps of a CTA (one kv head of the stage's block each).
+constexpr int kMmaCtasPerSm = KVC_MMA_CTAS_PER_SM;
+constexpr int kMmaWarps = KVC_MMA_WARPS;
+constexpr int kMmaThreads = (kMmaWarps + 1) * 32;  // consumer warps + one producer warp
+
 namespace wmma16 {
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -107,12 +120,6 @@ __device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* map, int 
       : "memory");
 }
 
-// Byte offset of 16-byte chunk q (0..7) of row r in a box of 128-byte rows
-// written by TMA with the 128-byte swizzle (box base 1024-byte aligned).
-__device__ __forceinline__ uint32_t swz(int r, int q) {
-  return static_cast<uint32_t>(r * 128 + ((q ^ (r & 7)) << 4));
-}
-
 }  // namespace wmma16
 
 // Per-warp state of a segment. Lane 4g + c holds, for query heads 2c and
@@ -127,35 +134,42 @@ struct MmaWarpState {
 
 // One 16-row tile of one kv head for the warp's GW query heads. kb / vb: the
 // stage's K / V box (64-dim half 0; half 1 follows at + box_bytes); row0: the
-// tile's first row in the box. PARTIAL tiles attend only rows [lo_valid,
+// tile's first row in the box. The boxes are 1024-byte aligned and written by
+// TMA with the 128-byte swizzle: 16-byte chunk q of row r sits at
+// r * 128 + ((q ^ (r & 7)) << 4). PARTIAL tiles attend only rows [lo_valid,
 // valid) and query column q only rows below vis[q & 1] of its lane.
 template <bool BF, int GW, bool PARTIAL>
 __device__ __forceinline__ void mma_tile(uint32_t kb, uint32_t vb, uint32_t box_bytes, int row0, int lo_valid,
                                          int valid, int vis0, int vis1, float qscale, MmaWarpState& st, int lane) {
   using namespace wmma16;
   const int g = lane >> 2, c = lane & 3;
+  // Swizzled chunk offsets: row r of the tile sits at r * 128 and its 16-byte
+  // chunk q at ((q ^ (r & 7)) << 4); every row a lane addresses has r & 7 =
+  // lane & 7, so for q = 2k + h the offset is 32 (k ^ s2) + 16 ((h ^ sw) & 1).
+  const int sw = lane & 7, s2 = sw >> 1;
   // ---- S^T = K . Q^T: lane l addresses row (l & 7) + 8 ((l >> 3) & 1) of
-  // the tile in dims chunk 2 (ks & 3) + (l >> 4) of half ks >> 2.
-  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  // the tile in dims chunk 2 (ks & 3) + (l >> 4) of half ks >> 2; four
+  // independent accumulator chains.
+  float sc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[j][e] = 0.f;
+  }
   {
-    const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-    const uint32_t rowk = kb + static_cast<uint32_t>(r * 128);
-    const int sw = r & 7;
+    const uint32_t rowk = kb + static_cast<uint32_t>((row0 + (lane & 7) + ((lane >> 3) & 1) * 8) * 128) +
+                          static_cast<uint32_t>((((lane >> 4) ^ sw) & 1) << 4);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const int q = ((ks & 3) << 1) + (lane >> 4);
       uint32_t a[4];
-      ldsm_x4(rowk + (ks >> 2) * box_bytes + static_cast<uint32_t>((q ^ sw) << 4), a);
-      if (ks & 1)
-        mma<BF>(sb, a, st.qb[ks][0], st.qb[ks][1]);
-      else
-        mma<BF>(sa, a, st.qb[ks][0], st.qb[ks][1]);
+      ldsm_x4(rowk + (ks >> 2) * box_bytes + static_cast<uint32_t>(((ks & 3) ^ s2) << 5), a);
+      mma<BF>(sc[ks & 3], a, st.qb[ks][0], st.qb[ks][1]);
     }
   }
   // scores in log2 units: x0 (row g, q 2c), x1 (row g, q 2c+1), x2 (row g+8, q 2c), x3 (row g+8, q 2c+1)
   float x[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) x[e] = (sa[e] + sb[e]) * qscale;
+  for (int e = 0; e < 4; ++e) x[e] = ((sc[0][e] + sc[1][e]) + (sc[2][e] + sc[3][e])) * qscale;
   const bool q0 = 2 * c < GW, q1 = 2 * c + 1 < GW;
   if (!q0) {
     x[0] = kNegInf;
@@ -220,14 +234,12 @@ __device__ __forceinline__ void mma_tile(uint32_t kb, uint32_t vb, uint32_t box_
     keep89 = ((rb >= lo_valid && rb < valid) ? 0x0000ffffu : 0u) | ((rb + 1 >= lo_valid && rb + 1 < valid) ? 0xffff0000u : 0u);
   }
   {
-    const int r = row0 + (lane & 7) + (lane >> 4) * 8;
-    const uint32_t rowv = vb + static_cast<uint32_t>(r * 128);
-    const int sw = r & 7;
+    const uint32_t rowv = vb + static_cast<uint32_t>((row0 + (lane & 7) + (lane >> 4) * 8) * 128) +
+                          static_cast<uint32_t>(((((lane >> 3) & 1) ^ sw) & 1) << 4);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int chunk = 2 * i + ((lane >> 3) & 1);
       uint32_t a[4];
-      ldsm_x4_t(rowv + (chunk >> 3) * box_bytes + static_cast<uint32_t>(((chunk & 7) ^ sw) << 4), a);
+      ldsm_x4_t(rowv + (i >> 2) * box_bytes + static_cast<uint32_t>(((i & 3) ^ s2) << 5), a);
       if (PARTIAL) {
         a[0] &= keep01;
         a[1] &= keep01;
@@ -240,12 +252,72 @@ __device__ __forceinline__ void mma_tile(uint32_t kb, uint32_t vb, uint32_t box_
   }
 }
 
-// Shared-memory carve-up of the MMA kernel (offsets from a 1024-byte aligned
-// base; the host adds 1024 bytes of slack for the alignment). A stage is
-// [K half 0][K half 1][V half 0][V half 1] (each hc * block_size rows of 128
-// bytes, swizzled) followed by the unit's query rows [hc][GH][128].
+// ------------------------------------------------------------------ work split
+//
+// The blocks of all units are laid end to end (sequence major, then kv-head
+// chunk, then head subgroup: global positions 0 .. N-1). Workers 0 .. G-1 are
+// the CTAs' static ranges over the first N0 positions, [w N0 / G, (w+1) N0 /
+// G); workers G .. G+K-1 are the chunks of C positions that tile the rest,
+// [N0 + k C, N0 + (k+1) C), claimed at run time from a counter in the
+// workspace by whichever CTA finishes first. A worker that cuts a unit leaves
+// one fp32 record per cut segment (slot 0: the segment at its range start;
+// slot 1: the one at its range end), and the last worker to count its record
+// merges them.
+struct WorkSplit {
+  int64_t N, N0, G, K;
+  int C;
+  __device__ __forceinline__ int64_t start(int64_t w) const {
+    if (w < G) return w * N0 / G;
+    const int64_t s = N0 + (w - G) * C;
+    return s < N ? s : N;
+  }
+  __device__ __forceinline__ int64_t worker_of(int64_t b) const {
+    return b < N0 ? ((b + 1) * G - 1) / N0 : G + (b - N0) / C;
+  }
+  // Workers with a non-empty range that overlap positions [u0, u0 + nb).
+  __device__ __forceinline__ int64_t contributors(int64_t u0, int nb) const {
+    const int64_t c0 = worker_of(u0), c1 = worker_of(u0 + nb - 1);
+    if (N0 >= G || c0 >= G) return c1 - c0 + 1;
+    int64_t n = 0;
+    for (int64_t x = c0; x <= c1; ++x) n += (start(x) != start(x + 1)) ? 1 : 0;
+    return n;
+  }
+  // Record of worker w for the unit starting at u0 (-1: empty range).
+  __device__ __forceinline__ int64_t record(int64_t w, int64_t u0) const {
+    const int64_t s = start(w);
+    if (s == start(w + 1)) return -1;
+    return 2 * w + (u0 > s ? 1 : 0);
+  }
+};
+
+// Splits N positions over G static ranges and a dynamic share of dyn_share /
+// 256 of the positions in chunks of dyn_chunk (dyn_chunk 0: static only). The
+// dynamic share is kept only when each CTA still gets at least min_static
+// positions of its own; every CTA computes the same split.
+__device__ __forceinline__ WorkSplit make_split(int64_t N, int64_t G, int dyn_share, int dyn_chunk, int min_static) {
+  WorkSplit s;
+  s.N = N;
+  s.G = G;
+  s.C = dyn_chunk > 0 ? dyn_chunk : 1;
+  int64_t Nd = dyn_chunk > 0 ? N * dyn_share / 256 : 0;
+  if (Nd > 0 && (N - Nd) < G * static_cast<int64_t>(min_static)) Nd = 0;
+  s.N0 = N - Nd;
+  s.K = (Nd + s.C - 1) / s.C;
+  return s;
+}
+
+// ------------------------------------------------------------ shared memory
+//
+// Offsets from a 1024-byte aligned base (the host adds 1024 bytes of slack
+// for the alignment). A stage is [K half 0][K half 1][V half 0][V half 1]
+// (each hc * block_size rows of 128 bytes, swizzled) followed by the unit's
+// query rows [hc][GH][128]; each stage has a 64-byte descriptor written by
+// the producer warp, a "full" barrier (the copies landed) and an "empty"
+// barrier (every consumer warp released it).
+constexpr int kMmaPending = 32;  // deferred merge checks per consumer warp
+
 struct GqaMmaSmem {
-  size_t box_bytes, stage_bytes, q_off, bar_off, rel_off, misc_off, scan_off, total;
+  size_t box_bytes, stage_bytes, q_off, meta_off, full_off, empty_off, iss_off, misc_off, pend_off, scan_off, total;
 };
 
 __host__ __device__ inline GqaMmaSmem gqa_mma_smem_layout(int q_elt, int GH, int block_size, int hc, int stages,
@@ -254,19 +326,121 @@ __host__ __device__ inline GqaMmaSmem gqa_mma_smem_layout(int q_elt, int GH, int
   s.box_bytes = static_cast<size_t>(hc) * block_size * 128;
   s.q_off = 4 * s.box_bytes;
   s.stage_bytes = align_up(s.q_off + static_cast<size_t>(hc) * GH * 128 * q_elt, 1024);
-  s.bar_off = static_cast<size_t>(stages) * s.stage_bytes;
-  s.rel_off = s.bar_off + static_cast<size_t>(stages) * 8;
-  s.misc_off = align_up(s.rel_off + static_cast<size_t>(stages) * 8, 16);
-  s.scan_off = s.misc_off + 16;
+  s.meta_off = static_cast<size_t>(stages) * s.stage_bytes;
+  s.full_off = s.meta_off + static_cast<size_t>(stages) * 64;
+  s.empty_off = s.full_off + static_cast<size_t>(stages) * 8;
+  s.iss_off = s.empty_off + static_cast<size_t>(stages) * 8;
+  s.misc_off = align_up(s.iss_off + static_cast<size_t>(stages) * 4, 16);
+  s.pend_off = s.misc_off + 16;
+  s.scan_off = s.pend_off + static_cast<size_t>(kMmaWarps) * kMmaPending * 16;
   s.total = s.scan_off + static_cast<size_t>(batch + 1 + 32) * 4 + 1024;
   return s;
 }
 
+
 __host__ __device__ constexpr int mma_warps_per_kvhead(int GH) { return GH > 8 ? GH / 8 : 1; }
-__host__ __device__ constexpr int mma_max_chunk(int GH) { return kGqaWarps / mma_warps_per_kvhead(GH); }
+__host__ __device__ constexpr int mma_max_chunk(int GH) { return kMmaWarps / mma_warps_per_kvhead(GH); }
+
+// Descriptor of the position a stage holds (written by the producer before it
+// arms the stage's "full" barrier).
+struct StageMeta {
+  int64_t u0;      // first global position of the unit
+  int seq;         // -1: no more work
+  int chunk, hsub, nb;
+  int jb;          // table index of the block
+  int n_rows, r0;  // cached rows of the sequence, its first visible row
+  int flags;
+  int rec;         // record index of the segment (partial segments)
+  int pad;
+};
+constexpr int kFirst = 1, kLast = 2, kSrc = 4, kWhole = 8;
+
+// One warp merges, for its GW heads of a unit (first position u0, nb blocks),
+// the records of every worker that touched it with the log-sum-exp rule and
+// writes the normalised output. Lane L owns the float4 chunks L + 32k of the
+// warp's GW x 128 outputs; RG records are read together.
+// Not inlined: it runs rarely (once per cut unit), and its registers must not
+// count against the streaming loop's.
+template <int HS, int GW, bool EXT>
+__device__ __noinline__ void merge_unit_mma(const GqaParams& p, const WorkSplit& ws, int64_t u0, int nb, int seq,
+                                            int kvh, int v0, int hoff, int lane) {
+  constexpr int D = 128;
+  constexpr int NCK = GW;  // float4 chunks per lane: (GW * 32 chunks) / 32 lanes
+  constexpr int RG = GW > 4 ? 2 : 4;
+  const int64_t c0 = ws.worker_of(u0), c1 = ws.worker_of(u0 + nb - 1);
+  const int span = static_cast<int>(c1 - c0 + 1);
+  const float* rbase = p.rec_o + static_cast<int64_t>(hoff) * D + 4 * lane;
+  float M[GW], Lp[GW];
+  float4 O[NCK];
+#pragma unroll
+  for (int h = 0; h < GW; ++h) {
+    M[h] = kNegInf;
+    Lp[h] = 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < NCK; ++k) O[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < span; base += RG) {
+    const int n = min(RG, span - base);
+    const int64_t rec = (lane < n) ? ws.record(c0 + base + lane, u0) : -1;
+    float mr[GW], lr[GW];
+#pragma unroll
+    for (int h = 0; h < GW; ++h) {
+      const float* ml = p.rec_ml + (rec * HS + hoff + h) * 2;
+      mr[h] = rec >= 0 ? __ldcg(ml) : kNegInf;
+      lr[h] = rec >= 0 ? __ldcg(ml + 1) : 0.f;
+    }
+    float4 ov[RG][NCK];
+#pragma unroll
+    for (int i = 0; i < RG; ++i) {
+      const int64_t rr = __shfl_sync(0xffffffffu, rec, i);
+#pragma unroll
+      for (int k = 0; k < NCK; ++k)
+        ov[i][k] = (i < n && rr >= 0) ? __ldcg(reinterpret_cast<const float4*>(rbase + rr * HS * D + 128 * k))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float fr[GW];
+#pragma unroll
+    for (int h = 0; h < GW; ++h) {
+      const float mn = fmaxf(M[h], warp_max(mr[h]));
+      if (mn != M[h]) {
+        const float a = (M[h] == kNegInf) ? 0.f : fast_exp2(M[h] - mn);
+        Lp[h] *= a;
+        // chunk k of lane L belongs to head (L + 32k) / 32 = k
+        O[h].x *= a;
+        O[h].y *= a;
+        O[h].z *= a;
+        O[h].w *= a;
+        M[h] = mn;
+      }
+      fr[h] = (mr[h] == kNegInf) ? 0.f : fast_exp2(mr[h] - M[h]);
+      Lp[h] += fr[h] * lr[h];
+    }
+#pragma unroll
+    for (int i = 0; i < RG; ++i) {
+#pragma unroll
+      for (int h = 0; h < GW; ++h) {
+        const float f = __shfl_sync(0xffffffffu, fr[h], i);
+        O[h].x += f * ov[i][h].x;
+        O[h].y += f * ov[i][h].y;
+        O[h].z += f * ov[i][h].z;
+        O[h].w += f * ov[i][h].w;
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < GW; ++h) {
+    const float lsum = warp_sum(Lp[h]);
+    const float inv = 1.0f / lsum;
+    if (EXT && p.lse != nullptr && lane == 0) p.lse[out_row(p, seq, kvh, v0 + h)] = M[h] + __log2f(lsum);
+    const int64_t o = EXT ? out_row(p, seq, kvh, v0 + h) * D + 4 * lane
+                          : (static_cast<int64_t>(seq) * p.n_q_heads + kvh * p.group + v0 + h) * D + 4 * lane;
+    const float v[4] = {O[h].x * inv, O[h].y * inv, O[h].z * inv, O[h].w * inv};
+    store_out_vec<4>(p.out, o, v, p.out_dtype);
+  }
+}
 
 template <typename T, int GH, bool EXT>
-__global__ void __launch_bounds__(kGqaWarps * 32, 1)
+__global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
     gqa_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const GqaParams p) {
   using namespace wmma16;
@@ -274,7 +448,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 1)
   constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
   constexpr int HW = mma_warps_per_kvhead(GH);  // warps per kv head
   constexpr int GW = GH / HW;                   // query heads per warp (MMA columns)
-  constexpr int HCM = kGqaWarps / HW;           // kv heads per CTA at most
+  constexpr int HCM = kMmaWarps / HW;           // kv heads per CTA at most
   constexpr int HS = HCM * GH;                  // query heads per record
   static_assert(GW <= 8 && GW * HW == GH, "at most 8 query heads per warp");
   extern __shared__ unsigned char smem_raw[];
@@ -292,34 +466,27 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 1)
   const int row_div = EXT ? p.row_div : 0;
   const int bs = p.block_size, S = p.stages;
   const GqaMmaSmem L = gqa_mma_smem_layout(sizeof(T), GH, bs, hc, S, p.batch);
-  uint64_t* fbar = reinterpret_cast<uint64_t*>(smem + L.bar_off);
-  unsigned int* s_rel = reinterpret_cast<unsigned int*>(smem + L.rel_off);
-  unsigned int* s_iss = s_rel + S;
-  volatile int* s_misc = reinterpret_cast<volatile int*>(smem + L.misc_off);
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta_off);
+  uint64_t* fbar = reinterpret_cast<uint64_t*>(smem + L.full_off);
+  uint64_t* ebar = reinterpret_cast<uint64_t*>(smem + L.empty_off);
+  unsigned int* s_iss = reinterpret_cast<unsigned int*>(smem + L.iss_off);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.misc_off);
   int* s_scan = reinterpret_cast<int*>(smem + L.scan_off);
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int kh = w / HW, hw = w % HW;
-  const int nact = hc * HW;
-  const bool active = w < nact;
+  const int nact = hc * HW;  // consumer warps with work
   const int B = p.batch;
-  const int tiles_per_page = bs / 16;
-  const uint32_t box_bytes = static_cast<uint32_t>(L.box_bytes);
-  const uint32_t q_bytes = static_cast<uint32_t>(hc * GH * D * sizeof(T));
-  const T* qg = static_cast<const T*>(p.q);
   const uint32_t full = 0xffffffffu;
   const int HN = p.n_chunks * p.n_hsub;
-  const bool q_contig = (GH == p.group);
 
   if (tid < S) {
-    mbar_init(fbar + tid, 1);
-    s_rel[tid] = 0u;
+    mbar_init(fbar + tid, 1);     // the producer's arrive (with the copy bytes)
+    mbar_init(ebar + tid, nact);  // one release per consumer warp
     s_iss[tid] = 0u;
   }
   if (tid == 0) {
-    s_misc[0] = 0;
-    s_misc[1] = 0;
-    s_misc[2] = 0;
+    *s_abort = 0;
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
   }
@@ -329,6 +496,15 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 1)
   // runs; every thread then waits for it (its writes become visible) before it
   // reads or writes any caller buffer.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (w == kMmaWarps && !p.unit_mode) {
+    // Warm L2 with the block-table lines this CTA most likely reads first (a
+    // guess that assumes full-length sequences; it only overlaps the scan).
+    const int64_t per_seq = static_cast<int64_t>(HN) * p.max_blocks;
+    const int64_t pos = static_cast<int64_t>(blockIdx.x) * B * per_seq / gridDim.x + 32 * lane;
+    const int64_t seq = pos / per_seq;
+    const int j = static_cast<int>((pos - seq * per_seq) % p.max_blocks);
+    if (lane < 4 && seq < B) prefetch_l2(p.block_tables + seq * p.max_blocks + j);
+  }
   scan_blocks(p.context_lens, B, bs, p.max_blocks, wnd, min_len, row_start, row_div, s_scan);  // ends with a CTA barrier
   const int64_t N = static_cast<int64_t>(HN) * s_scan[B];
   const int64_t G = gridDim.x;
@@ -339,7 +515,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 1)
     for (int b = tid; b < B; b += blockDim.x) {
       const int n = __ldg(p.context_lens + b);
       if (n < min_len || n > bs * p.max_blocks) set_flag(p.err, 0x2u);
-      if (row_div > 0 && __ldg(row_start + b / row_div) > n) set_flag(p.err, 0x2u);
+      if (row_div > 0 && __ldg(row_start + b / (row_div > 0 ? row_div : 1)) > n) set_flag(p.err, 0x2u);
       empty |= (s_scan[b + 1] == s_scan[b]) ? 1 : 0;
     }
     if (__syncthreads_or(empty) && !p.unit_mode) {
@@ -355,13 +531,17 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 1)
     }
   }
 
+  // The work split (every CTA computes the same one). In the unit mode CTA u
+  // takes unit u whole and nothing is claimed.
+  WorkSplit ws;
   int64_t lo, hi;
   if (p.unit_mode) {
+    ws = make_split(N, G, 0, 0, 1);
     const int seq = static_cast<int>(c / HN);
     const int idx = static_cast<int>(c - static_cast<int64_t>(seq) * HN);
     const int nb = s_scan[seq + 1] - s_scan[seq];
     if (nb == 0) {
-      if (active) {
+      if (w < nact) {
         const int chunk = idx / p.n_hsub, hsub = idx - chunk * p.n_hsub;
         const int kvh = chunk * hc + kh, v0 = hsub * GH + hw * GW;
         for (int i = lane; i < GW * D; i += 32) {
@@ -376,177 +556,244 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 1)
     lo = static_cast<int64_t>(HN) * s_scan[seq] + static_cast<int64_t>(idx) * nb;
     hi = lo + nb;
   } else {
-    lo = cta_range_start(c, G, N);
-    hi = cta_range_start(c + 1, G, N);
+    ws = make_split(N, G, p.dyn_share, p.dyn_chunk, p.dyn_min_static);
+    lo = ws.start(c);
+    hi = ws.start(c + 1);
   }
-  const int total = static_cast<int>(hi - lo);
-  if (total <= 0) return;  // uniform over the CTA
 
-  const uint64_t pol = policy_evict_first();
-  const uint32_t stage0 = base;  // stage s at base + s * stage_bytes
-  const uint32_t stage_bytes = static_cast<uint32_t>(L.stage_bytes);
-
-  // Positions lo + 32*win + lane, one per lane: the first row of the chunk's
-  // pages in the pool viewed as rows ((block * n_kv_heads + first kv head of
-  // the chunk) * block_size; -1 if the table entry is out of range) and, for
-  // the first block of a segment, the element offset of the unit's first
-  // query row (with several new tokens: the unit's index; -1 otherwise).
-  auto window = [&](int win, int& src, int& qoff) {
-    const int64_t pos = lo + static_cast<int64_t>(win) * 32 + lane;
-    src = -1;
-    qoff = -1;
-    if (pos < hi) {
-      const BlockPos bp = locate_block(pos, HN, s_scan, B, p.n_hsub);
-      const int j0 =
-          start_row(seq_rows(p.context_lens, bp.seq, bs, p.max_blocks, min_len), wnd, row_start, row_div, bp.seq) /
-          bs;
-      const int phys = __ldg(p.block_tables + static_cast<int64_t>(bp.seq) * p.max_blocks + j0 + bp.j);
-      if (phys >= 0 && phys < p.num_blocks) src = (phys * p.n_kv_heads + bp.chunk * hc) * bs;
-      if (pos == lo || bp.j == 0)
-        qoff = multi ? (bp.seq * p.n_chunks + bp.chunk) * p.n_hsub + bp.hsub
-                     : (bp.seq * p.n_q_heads + bp.chunk * hc * p.group + bp.hsub * GH) * D;
-    }
-  };
-  auto issue = [&](int slot, int src, int qoff) {
-    const uint32_t bytes = (src >= 0 ? 4 * box_bytes : 0u) + (qoff >= 0 ? q_bytes : 0u);
-    if (src < 0) set_flag(p.err, 0x1u);
-    atomicAdd(s_iss + slot, 1u);
-    if (bytes == 0) {
-      mbar_arrive(fbar + slot);
-      return;
-    }
-    const uint32_t dst = stage0 + static_cast<uint32_t>(slot) * stage_bytes;
-    const uint32_t bar = smem_addr(fbar + slot);
-    mbar_arrive_expect_tx(fbar + slot, bytes);
-    if (src >= 0) {
-      tma2d(dst, &tm_k, 0, src, bar, pol);
-      tma2d(dst + box_bytes, &tm_k, 64, src, bar, pol);
-      tma2d(dst + 2 * box_bytes, &tm_v, 0, src, bar, pol);
-      tma2d(dst + 3 * box_bytes, &tm_v, 64, src, bar, pol);
-    }
-    if (qoff >= 0) {
-      unsigned char* qdst = smem + static_cast<size_t>(slot) * stage_bytes + L.q_off;
-      if (multi) {
-        const int hs = qoff % p.n_hsub, rest = qoff / p.n_hsub;
-        const int ch = rest % p.n_chunks, sq = rest / p.n_chunks;
-        const uint32_t rowb = static_cast<uint32_t>(D * sizeof(T));
-        for (int h = 0; h < hc; ++h) {
-          const int kvh = ch * hc + h;
-          for (int v = hs * GH, ve = v + GH; v < ve;) {
-            const int t = v / p.group, j = v - t * p.group;
-            const int len = min(p.group - j, ve - v);
-            const int64_t row = (static_cast<int64_t>(sq) * n_tok + t) * p.n_q_heads + kvh * p.group + j;
-            bulk_g2s(qdst + (h * GH + v - hs * GH) * rowb, qg + row * D, len * rowb, fbar + slot, pol);
-            v += len;
-          }
+  if (w == kMmaWarps) {
+    // ============================================================== producer
+    // Walks its static range, then the chunks it claims, position by
+    // position: lane i describes position base + i of a window of 32 (block
+    // table entry, segment flags, record), lane 0 waits for the stage to be
+    // released, writes its descriptor and issues the copies.
+    const T* qg = static_cast<const T*>(p.q);
+    const uint64_t pol = policy_evict_first();
+    const uint32_t box_bytes = static_cast<uint32_t>(L.box_bytes);
+    const uint32_t q_bytes = static_cast<uint32_t>(hc * GH * D * sizeof(T));
+    const bool q_contig = (GH == p.group);
+    unsigned int claim = 0;
+    if (!p.unit_mode && ws.K > 0 && lane == 0) claim = atomicAdd(p.sched, 1u);  // for after the static range
+    int64_t wk = c;
+    uint32_t slot = 0, ph = 0;
+    bool ok = true;
+    for (;;) {
+      for (int64_t bpos = lo; ok && bpos < hi; bpos += 32) {
+        const int64_t pos = bpos + lane;
+        StageMeta m{};
+        int src = -1, qoff = -1;
+        if (pos < hi) {
+          const BlockPos bp = locate_block(pos, HN, s_scan, B, p.n_hsub);
+          m.seq = bp.seq;
+          m.chunk = bp.chunk;
+          m.hsub = bp.hsub;
+          m.nb = bp.nb;
+          m.u0 = pos - bp.j;
+          m.n_rows = seq_rows(p.context_lens, bp.seq, bs, p.max_blocks, min_len);
+          m.r0 = start_row(m.n_rows, wnd, row_start, row_div, bp.seq);
+          m.jb = m.r0 / bs + bp.j;
+          const int phys = __ldg(p.block_tables + static_cast<int64_t>(bp.seq) * p.max_blocks + m.jb);
+          if (phys >= 0 && phys < p.num_blocks) src = (phys * p.n_kv_heads + bp.chunk * hc) * bs;
+          const bool first = (pos == lo) || (bp.j == 0);
+          m.flags = (first ? kFirst : 0) | ((pos == hi - 1 || bp.j == bp.nb - 1) ? kLast : 0) | (src >= 0 ? kSrc : 0) |
+                    ((m.u0 >= lo && m.u0 + bp.nb <= hi) ? kWhole : 0);
+          // slot 0: the segment holding the range's first position; slot 1: a
+          // unit that starts inside the range and runs past its end
+          m.rec = static_cast<int>(2 * wk + (m.u0 > lo ? 1 : 0));
+          if (first)
+            qoff = multi ? (bp.seq * p.n_chunks + bp.chunk) * p.n_hsub + bp.hsub
+                         : (bp.seq * p.n_q_heads + bp.chunk * hc * p.group + bp.hsub * GH) * D;
         }
-      } else if (q_contig) {
-        bulk_g2s(qdst, qg + qoff, q_bytes, fbar + slot, pol);
-      } else {
-        const uint32_t rb = static_cast<uint32_t>(GH * D * sizeof(T));
-        for (int h = 0; h < hc; ++h) bulk_g2s(qdst + h * rb, qg + qoff + h * p.group * D, rb, fbar + slot, pol);
-      }
-    }
-  };
-
-  int w_src0, w_src1 = -1, w_q0, w_q1 = -1;
-  window(0, w_src0, w_q0);
-  if (total > 32) window(1, w_src1, w_q1);
-
-  const int n_first = total < S ? total : S;
-  if (w == 0) {
-    for (int i = 0; i < n_first; ++i) {
-      const int src = __shfl_sync(full, w_src0, i);
-      const int qo = __shfl_sync(full, w_q0, i);
-      if (lane == 0) issue(i, src, qo);
-    }
-  }
-  __syncwarp();
-
-  bool pend0 = false, pend1 = false;
-  unsigned int old0 = 0, old1 = 0;
-  bool aborted = false;
-  const int g8 = lane >> 2, c4 = lane & 3;
-
-  if (active) {
-    int slot = 0;
-    uint32_t par = 0, fill = 0;
-    int cpos = 0;
-    int64_t gb = lo;
-    while (gb < hi) {
-      const BlockPos sg = locate_block(gb, HN, s_scan, B, p.n_hsub);
-      const int seg_len = static_cast<int>(((sg.nb - sg.j) < (hi - gb)) ? (sg.nb - sg.j) : (hi - gb));
-      const int n_rows = seq_rows(p.context_lens, sg.seq, bs, p.max_blocks, min_len);
-      const int r0 = start_row(n_rows, wnd, row_start, row_div, sg.seq);
-      const int j0 = r0 / bs;
-      const int kvh = sg.chunk * hc + kh;
-      const int v0 = sg.hsub * GH + hw * GW;
-      const int hq0 = kvh * p.group + v0;
-      // rows at the end each of the lane's two query columns may not see (multi-token causality)
-      const int dh0 = (EXT && causal) ? tm - (v0 + 2 * c4) / p.group : 0;
-      const int dh1 = (EXT && causal) ? tm - (v0 + 2 * c4 + 1) / p.group : 0;
-
-      MmaWarpState st;
-      for (int t = 0; t < seg_len; ++t, ++cpos) {
-        if (cpos > 0 && (cpos & 31) == 0) {
-          w_src0 = w_src1;
-          w_q0 = w_q1;
-          w_src1 = -1;
-          w_q1 = -1;
-          if (cpos + 32 < total) window((cpos >> 5) + 1, w_src1, w_q1);
-        }
-        const int src = __shfl_sync(full, w_src0, cpos & 31);
-        const int cn = cpos + S;
-        const bool in_cur = (cn >> 5) == (cpos >> 5);
-        const int src_n = __shfl_sync(full, in_cur ? w_src0 : w_src1, cn & 31);
-        const int q_n = __shfl_sync(full, in_cur ? w_q0 : w_q1, cn & 31);
-        const bool ok = mbar_wait_bounded(fbar + slot, par);
-        if (__any_sync(full, !ok) || s_misc[0]) {
+        const int n = static_cast<int>(hi - bpos < 32 ? hi - bpos : 32);
+        for (int i = 0; i < n; ++i) {
+          StageMeta mi;
+          mi.u0 = __shfl_sync(full, m.u0, i);
+          mi.seq = __shfl_sync(full, m.seq, i);
+          mi.chunk = __shfl_sync(full, m.chunk, i);
+          mi.hsub = __shfl_sync(full, m.hsub, i);
+          mi.nb = __shfl_sync(full, m.nb, i);
+          mi.jb = __shfl_sync(full, m.jb, i);
+          mi.n_rows = __shfl_sync(full, m.n_rows, i);
+          mi.r0 = __shfl_sync(full, m.r0, i);
+          mi.flags = __shfl_sync(full, m.flags, i);
+          mi.rec = __shfl_sync(full, m.rec, i);
+          mi.pad = 0;
+          const int srci = __shfl_sync(full, src, i);
+          const int qo = __shfl_sync(full, qoff, i);
           if (lane == 0) {
-            set_flag(p.err, 0x8u);
-            s_misc[0] = 1;
-          }
-          aborted = true;
-          break;
-        }
-        const uint32_t stg = stage0 + static_cast<uint32_t>(slot) * stage_bytes;
-        if (t == 0) {
-          // Q^T fragments of the warp's query heads (query g of the warp, dims
-          // 16 ks + 2c (+1) and + 8 (+9)); columns beyond GW are zero.
-          const unsigned char* qs = smem + static_cast<size_t>(slot) * stage_bytes + L.q_off +
-                                    static_cast<size_t>(kh * GH + hw * GW) * D * sizeof(T);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            if (g8 < GW) {
-              const uint32_t* qr = reinterpret_cast<const uint32_t*>(qs + (g8 * D + 16 * ks + 2 * c4) * sizeof(T));
-              st.qb[ks][0] = qr[0];
-              st.qb[ks][1] = qr[4];
+            ok = mbar_wait_bounded(ebar + slot, ph ^ 1u) && !*s_abort;
+            if (ok) {
+              if (srci < 0) set_flag(p.err, 0x1u);
+              meta[slot] = mi;
+              const uint32_t bytes = (srci >= 0 ? 4 * box_bytes : 0u) + (qo >= 0 ? q_bytes : 0u);
+              s_iss[slot] += 1u;
+              if (bytes == 0) {
+                mbar_arrive(fbar + slot);
+              } else {
+                const uint32_t dst = base + static_cast<uint32_t>(slot * L.stage_bytes);
+                const uint32_t bar = smem_addr(fbar + slot);
+                mbar_arrive_expect_tx(fbar + slot, bytes);
+                if (srci >= 0) {
+                  tma2d(dst, &tm_k, 0, srci, bar, pol);
+                  tma2d(dst + box_bytes, &tm_k, 64, srci, bar, pol);
+                  tma2d(dst + 2 * box_bytes, &tm_v, 0, srci, bar, pol);
+                  tma2d(dst + 3 * box_bytes, &tm_v, 64, srci, bar, pol);
+                }
+                if (qo >= 0) {
+                  unsigned char* qdst = smem + slot * L.stage_bytes + L.q_off;
+                  if (multi) {
+                    const int hs = qo % p.n_hsub, rest = qo / p.n_hsub;
+                    const int ch = rest % p.n_chunks, sq = rest / p.n_chunks;
+                    const uint32_t rowb = static_cast<uint32_t>(D * sizeof(T));
+                    for (int h = 0; h < hc; ++h) {
+                      const int kvh = ch * hc + h;
+                      for (int v = hs * GH, ve = v + GH; v < ve;) {
+                        const int t = v / p.group, j = v - t * p.group;
+                        const int len = min(p.group - j, ve - v);
+                        const int64_t row = (static_cast<int64_t>(sq) * n_tok + t) * p.n_q_heads + kvh * p.group + j;
+                        bulk_g2s(qdst + (h * GH + v - hs * GH) * rowb, qg + row * D, len * rowb, fbar + slot, pol);
+                        v += len;
+                      }
+                    }
+                  } else if (q_contig) {
+                    bulk_g2s(qdst, qg + qo, q_bytes, fbar + slot, pol);
+                  } else {
+                    const uint32_t rb = static_cast<uint32_t>(GH * D * sizeof(T));
+                    for (int h = 0; h < hc; ++h) bulk_g2s(qdst + h * rb, qg + qo + h * p.group * D, rb, fbar + slot, pol);
+                  }
+                }
+              }
             } else {
-              st.qb[ks][0] = 0u;
-              st.qb[ks][1] = 0u;
+              set_flag(p.err, 0x8u);
+              *s_abort = 1;
             }
           }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) st.o[i][e] = 0.f;
+          ok = __shfl_sync(full, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          if (++slot == static_cast<uint32_t>(S)) {
+            slot = 0;
+            ph ^= 1u;
           }
-          // a finite start: a column that meets only masked rows keeps weight 0
-          st.m[0] = st.m[1] = -1e30f;
-          st.l[0] = st.l[1] = 0.f;
         }
-        if (src >= 0) {
+      }
+      if (!ok || p.unit_mode || ws.K == 0) break;
+      // the next chunk: the claim made a range ago; claim the one after it now
+      const int64_t k = static_cast<int64_t>(__shfl_sync(full, claim, 0));
+      if (k >= ws.K) break;
+      if (lane == 0) claim = atomicAdd(p.sched, 1u);
+      wk = G + k;
+      lo = ws.start(wk);
+      hi = ws.start(wk + 1);
+    }
+    if (lane == 0) {
+      if (ok && mbar_wait_bounded(ebar + slot, ph ^ 1u)) {
+        meta[slot].seq = -1;  // no more work
+        mbar_arrive(fbar + slot);
+      } else if (ok) {
+        set_flag(p.err, 0x8u);
+        *s_abort = 1;
+      }
+      // Every CTA makes exactly one failed claim; the last one to do so
+      // resets the claim counter for the next call.
+      if (!p.unit_mode && ws.K > 0 && atomicAdd(p.sched + 1, 1u) == static_cast<unsigned int>(G) - 1) {
+        atomicExch(p.sched, 0u);
+        atomicExch(p.sched + 1, 0u);
+      }
+    }
+  } else if (w < nact) {
+    // ============================================================== consumers
+    const int g8 = lane >> 2, c4 = lane & 3;
+    const uint32_t box_bytes = static_cast<uint32_t>(L.box_bytes);
+    uint64_t* pend = reinterpret_cast<uint64_t*>(smem + L.pend_off) + w * kMmaPending * 2;  // (u0, old) pairs
+    int n_pend = 0;
+    unsigned int last_old = 0;  // result of the newest count, written to its entry later
+    bool have_last = false;
+    // Merge check of every deferred entry: the warp whose add completed a
+    // unit's count merges its heads and resets the counter.
+    auto flush = [&]() {
+      if (have_last) {
+        if (lane == 0) pend[2 * (n_pend - 1) + 1] = last_old;
+        have_last = false;
+      }
+      __syncwarp();
+      for (int e = 0; e < n_pend; ++e) {
+        const int64_t u0 = static_cast<int64_t>(pend[2 * e]);
+        const unsigned int old = static_cast<unsigned int>(pend[2 * e + 1]);
+        const BlockPos q = locate_block(u0, HN, s_scan, B, p.n_hsub);
+        const int64_t contributors = ws.contributors(u0, q.nb);
+        const int64_t unit = (static_cast<int64_t>(q.seq) * p.n_chunks + q.chunk) * p.n_hsub + q.hsub;
+        unsigned int* ctr = p.counters + unit * nact + w;
+        if (old + 1 == static_cast<unsigned int>(contributors)) {
+          if (lane == 0) *ctr = 0u;
+          merge_unit_mma<HS, GW, EXT>(p, ws, u0, q.nb, q.seq, q.chunk * hc + kh, q.hsub * GH + hw * GW,
+                                      kh * GH + hw * GW, lane);
+        } else if (old + 1 > static_cast<unsigned int>(contributors)) {
+          if (lane == 0) {
+            set_flag(p.err, 0x10u);  // the workspace counters were not zero
+            atomicExch(ctr, 0u);
+          }
+        }
+      }
+      n_pend = 0;
+      __syncwarp();
+    };
+
+    // One pass of the outer loop per segment (the positions of one unit in
+    // one worker's range): the first position carries the unit's query rows,
+    // the last one closes the segment. The warp state lives only inside a
+    // segment, so the rare merge calls between segments cost no registers.
+    uint32_t slot = 0, ph = 0;
+    bool abort_seen = false;
+    for (;;) {
+      if (!mbar_wait_bounded(fbar + slot, ph) || *s_abort) {
+        abort_seen = true;
+        break;
+      }
+      StageMeta m = meta[slot];
+      if (m.seq < 0) break;
+      const int kvh = m.chunk * hc + kh;
+      const int v0 = m.hsub * GH + hw * GW;
+      // rows at the end each of the lane's two query columns may not see
+      const int dh0 = (EXT && causal) ? tm - (v0 + 2 * c4) / p.group : 0;
+      const int dh1 = (EXT && causal) ? tm - (v0 + 2 * c4 + 1) / p.group : 0;
+      MmaWarpState st;
+      {
+        const unsigned char* qs = smem + slot * L.stage_bytes + L.q_off +
+                                  static_cast<size_t>(kh * GH + hw * GW) * D * sizeof(T);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          if (g8 < GW) {
+            const uint32_t* qr = reinterpret_cast<const uint32_t*>(qs + (g8 * D + 16 * ks + 2 * c4) * sizeof(T));
+            st.qb[ks][0] = qr[0];
+            st.qb[ks][1] = qr[4];
+          } else {
+            st.qb[ks][0] = 0u;
+            st.qb[ks][1] = 0u;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) st.o[i][e] = 0.f;
+        }
+        st.m[0] = st.m[1] = -1e30f;  // finite: a column that meets only masked rows keeps weight 0
+        st.l[0] = st.l[1] = 0.f;
+      }
+      for (;;) {
+        if (m.flags & kSrc) {
+          const uint32_t stg = base + static_cast<uint32_t>(slot * L.stage_bytes);
           const uint32_t kb = stg, vb = stg + 2 * box_bytes;
-          const int jb = j0 + sg.j + t;
-          const int rb = n_rows - jb * bs;
+          const int j0 = m.r0 / bs;
+          const int rb = m.n_rows - m.jb * bs;  // rows from the block's first to the end
           const int vr = min(bs, rb);
-          const int lr = (jb == j0) ? r0 - j0 * bs : 0;
+          const int lr = (m.jb == j0) ? m.r0 - j0 * bs : 0;
           const int rowk = kh * bs;
+          const int tiles = bs / 16;
           if (rb - tm >= bs && lr == 0) {
-            for (int tt = 0; tt < tiles_per_page; ++tt)
+            for (int tt = 0; tt < tiles; ++tt)
               mma_tile<BF, GW, false>(kb, vb, box_bytes, rowk + tt * 16, 0, 16, 16, 16, p.qscale, st, lane);
           } else {
-            for (int tt = 0; tt < tiles_per_page; ++tt) {
+            for (int tt = 0; tt < tiles; ++tt) {
               const int valid = vr - tt * 16, lo_valid = lr - tt * 16;
               const int rt = rb - tt * 16;
               if (valid <= 0) break;
@@ -560,21 +807,23 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 1)
             }
           }
         }
+        // release the stage: every read of it fed an instruction issued before this barrier
         __syncwarp();
-        if (lane == 0) {
-          const unsigned int old = atomic_add_acq_rel_cta_smem(s_rel + slot, 1u);
-          if (old + 1 == static_cast<unsigned int>(nact) * (fill + 1) && cn < total) issue(slot, src_n, q_n);
-        }
-        __syncwarp();
-        if (++slot == S) {
+        if (lane == 0) mbar_arrive(ebar + slot);
+        if (++slot == static_cast<uint32_t>(S)) {
           slot = 0;
-          par ^= 1u;
-          ++fill;
+          ph ^= 1u;
         }
+        if (m.flags & kLast) break;
+        if (!mbar_wait_bounded(fbar + slot, ph) || *s_abort) {
+          abort_seen = true;
+          break;
+        }
+        m = meta[slot];
       }
-      if (aborted) break;
+      if (abort_seen) break;
 
-      // ---- finish the segment
+      // ---- close the segment
       float lw0 = st.l[0], lw1 = st.l[1];
 #pragma unroll
       for (int msk = 4; msk < 32; msk <<= 1) {
@@ -582,12 +831,11 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 1)
         lw1 += __shfl_xor_sync(full, lw1, msk);
       }
       const bool qv0 = 2 * c4 < GW, qv1 = 2 * c4 + 1 < GW;
-      const bool whole = (sg.j == 0 && seg_len == sg.nb);
-      if (whole) {
+      if (m.flags & kWhole) {
         const float i0 = 1.0f / lw0, i1 = 1.0f / lw1;
-        const int64_t ob0 = (EXT ? out_row(p, sg.seq, kvh, v0 + 2 * c4)
-                                 : static_cast<int64_t>(sg.seq) * p.n_q_heads + hq0 + 2 * c4) * D;
-        const int64_t ob1 = (EXT ? out_row(p, sg.seq, kvh, v0 + 2 * c4 + 1) : ob0 / D + 1) * D;
+        const int64_t ob0 = (EXT ? out_row(p, m.seq, kvh, v0 + 2 * c4)
+                                 : static_cast<int64_t>(m.seq) * p.n_q_heads + kvh * p.group + v0 + 2 * c4) * D;
+        const int64_t ob1 = EXT ? out_row(p, m.seq, kvh, v0 + 2 * c4 + 1) * D : ob0 + D;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int d0 = 16 * i + g8;
@@ -601,11 +849,12 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 1)
           }
         }
         if (EXT && p.lse != nullptr && g8 == 0) {
-          if (qv0) p.lse[out_row(p, sg.seq, kvh, v0 + 2 * c4)] = st.m[0] + __log2f(lw0);
-          if (qv1) p.lse[out_row(p, sg.seq, kvh, v0 + 2 * c4 + 1)] = st.m[1] + __log2f(lw1);
+          if (qv0) p.lse[out_row(p, m.seq, kvh, v0 + 2 * c4)] = st.m[0] + __log2f(lw0);
+          if (qv1) p.lse[out_row(p, m.seq, kvh, v0 + 2 * c4 + 1)] = st.m[1] + __log2f(lw1);
         }
       } else {
-        const int64_t rec = c * 2 + (gb == lo ? 0 : 1);
+        // record (max, sum, unnormalised output) of this warp's heads
+        const int64_t rec = m.rec;
         const int hr = kh * GH + hw * GW;
         float* ro0 = p.rec_o + (rec * HS + hr + 2 * c4) * D;
         float* ro1 = ro0 + D;
@@ -631,59 +880,34 @@ __global__ void __launch_bounds__(kGqaWarps * 32, 1)
             p.rec_ml[(rec * HS + hr + 2 * c4 + 1) * 2 + 1] = lw1;
           }
         }
+        // Count the record (one counter per unit and warp slot): the warp
+        // barrier orders the lanes' record writes before lane 0's release.
+        // The add's result is read only at the next count or at the end, so
+        // its round trip never stalls the stream.
+        if (n_pend == kMmaPending) flush();
+        if (have_last && lane == 0) pend[2 * (n_pend - 1) + 1] = last_old;
         __syncwarp();
+        const int64_t unit = (static_cast<int64_t>(m.seq) * p.n_chunks + m.chunk) * p.n_hsub + m.hsub;
         if (lane == 0) {
-          const int64_t unit = (static_cast<int64_t>(sg.seq) * p.n_chunks + sg.chunk) * p.n_hsub + sg.hsub;
-          const unsigned int old = atomic_add_acq_rel_gpu(p.counters + unit * nact + w, 1u);
-          if (gb == lo) old0 = old; else old1 = old;
+          pend[2 * n_pend] = static_cast<uint64_t>(m.u0);
+          last_old = atomic_add_acq_rel_gpu(p.counters + unit * nact + w, 1u);
         }
-        if (gb == lo) pend0 = true; else pend1 = true;
+        ++n_pend;
+        have_last = true;
       }
-      gb += seg_len;
     }
+    if (abort_seen && lane == 0) {
+      set_flag(p.err, 0x8u);
+      *s_abort = 1;
+    }
+    if (!*s_abort) flush();
   }
 
   __syncthreads();
-  const bool any_abort = s_misc[0] != 0;
-  if (active && !any_abort && (pend0 || pend1)) {
-    const BlockPos q0 = locate_block(lo, HN, s_scan, B, p.n_hsub);
-    const BlockPos q1 = locate_block(hi - 1, HN, s_scan, B, p.n_hsub);
-    const int64_t p0_u0 = lo - q0.j, p1_u0 = hi - 1 - q1.j;
-    int last = 0;
-    if (lane == 0) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        if (!(k == 0 ? pend0 : pend1)) continue;
-        const BlockPos& qq = k == 0 ? q0 : q1;
-        const int64_t u0 = k == 0 ? p0_u0 : p1_u0;
-        const int64_t c0 = worker_of_block(u0, G, N), c1 = worker_of_block(u0 + qq.nb - 1, G, N);
-        int64_t contributors = c1 - c0 + 1;
-        if (N < G) {
-          contributors = 0;
-          for (int64_t x = c0; x <= c1; ++x)
-            contributors += (worker_range_start(x, G, N) != worker_range_start(x + 1, G, N)) ? 1 : 0;
-        }
-        const int64_t unit = (static_cast<int64_t>(qq.seq) * p.n_chunks + qq.chunk) * p.n_hsub + qq.hsub;
-        unsigned int* ctr = p.counters + unit * nact + w;
-        const unsigned int old = k == 0 ? old0 : old1;
-        if (old + 1 == static_cast<unsigned int>(contributors)) {
-          last |= 1 << k;
-          *ctr = 0u;
-        } else if (old + 1 > static_cast<unsigned int>(contributors)) {
-          set_flag(p.err, 0x10u);
-          atomicExch(ctr, 0u);
-        }
-      }
-    }
-    last = __shfl_sync(full, last, 0);
-    if (last & 1)
-      merge_unit_warp<D, HS, GW, EXT>(p, p0_u0, q0.nb, G, N, q0.seq, q0.chunk * hc + kh, q0.hsub * GH + hw * GW,
-                                      kh * GH + hw * GW, lane);
-    if (last & 2)
-      merge_unit_warp<D, HS, GW, EXT>(p, p1_u0, q1.nb, G, N, q1.seq, q1.chunk * hc + kh, q1.hsub * GH + hw * GW,
-                                      kh * GH + hw * GW, lane);
-  }
-  if (any_abort && tid == 0) {
+  if (*s_abort && tid == 0) {
+    // Copies that may still be in flight must land before the CTA exits and
+    // its shared memory is reused: wait (bounded) for the latest issued fill
+    // of every stage.
     for (int x = 0; x < S; ++x) {
       const unsigned int n = s_iss[x];
       if (n > 0) (void)mbar_wait_bounded(fbar + x, (n - 1) & 1u);

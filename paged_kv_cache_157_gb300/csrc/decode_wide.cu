@@ -750,7 +750,8 @@ bool wide_preferred(int batch, int n_q_heads, int n_kv_heads, int head_dim, int 
 
 bool wide_supported(int batch, int n_q_heads, int n_kv_heads, int head_dim, int block_size, int n_tok,
                     kvc_dtype dtype) {
-  if (option(KVC_OPT_GQA_ENGINE) == 1) return false;
+  const int64_t engine = option(KVC_OPT_GQA_ENGINE);
+  if (engine == 1 || engine == 3) return false;
   if (dtype != KVC_BF16 && dtype != KVC_F16) return false;
   if (head_dim != wide::kD || batch > wide::kMaxBatch) return false;
   if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128) return false;

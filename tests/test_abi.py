@@ -47,11 +47,11 @@ def test_options_roundtrip(kvc):
         kvc.set_option(kvc.OPT_CHECKED, 2)
     with pytest.raises(kvc.KvcError):
         kvc.set_option(9, 1)
-    for e in (1, 2, 0):
+    for e in (1, 2, 3, 0):
         kvc.set_option(kvc.OPT_GQA_ENGINE, e)
         assert kvc.get_option(kvc.OPT_GQA_ENGINE) == e
     with pytest.raises(kvc.KvcError):
-        kvc.set_option(kvc.OPT_GQA_ENGINE, 3)
+        kvc.set_option(kvc.OPT_GQA_ENGINE, 4)
 
 
 def test_host_validation_before_any_device_work(kvc):

@@ -42,7 +42,8 @@ def _reference(kvc, dev, scale):
 
 
 def test_static_scratch_matches_workspace_path_twice(kvc):
-    for o in (kvc.OPT_BLOCKS_PER_CTA, kvc.OPT_MAX_CTAS, kvc.OPT_CHECKED):
+    for o in (kvc.OPT_BLOCKS_PER_CTA, kvc.OPT_MAX_CTAS, kvc.OPT_CHECKED, kvc.OPT_DYNAMIC_SHARE,
+              kvc.OPT_DYNAMIC_CHUNK):
         kvc.set_option(o, 0)
     scale = 1.0 / math.sqrt(128)
     cases = [W.gqa_case(32, 32, 8, 128, 16, (512, 4096), "bf16", seed=43),
@@ -62,7 +63,8 @@ def test_static_scratch_on_the_tensor_core_engine(kvc):
     # 64 query / 8 kv heads: 8 queries per kv head, which the tensor-core
     # kernel takes (forced here at any size); its counters and records sit in
     # the same built-in array in a different layout.
-    for o in (kvc.OPT_BLOCKS_PER_CTA, kvc.OPT_MAX_CTAS, kvc.OPT_CHECKED):
+    for o in (kvc.OPT_BLOCKS_PER_CTA, kvc.OPT_MAX_CTAS, kvc.OPT_CHECKED, kvc.OPT_DYNAMIC_SHARE,
+              kvc.OPT_DYNAMIC_CHUNK):
         kvc.set_option(o, 0)
     kvc.set_option(kvc.OPT_GQA_ENGINE, 2)
     try:
@@ -86,7 +88,8 @@ def test_static_scratch_on_the_tensor_core_engine(kvc):
 def test_static_scratch_after_a_call_with_a_bad_block_id(kvc):
     # A call that meets an out-of-pool block id flags it (and leaves its output
     # undefined); the next call with valid inputs must match the workspace path.
-    for o in (kvc.OPT_BLOCKS_PER_CTA, kvc.OPT_MAX_CTAS, kvc.OPT_CHECKED, kvc.OPT_GQA_ENGINE):
+    for o in (kvc.OPT_BLOCKS_PER_CTA, kvc.OPT_MAX_CTAS, kvc.OPT_CHECKED, kvc.OPT_GQA_ENGINE,
+              kvc.OPT_DYNAMIC_SHARE, kvc.OPT_DYNAMIC_CHUNK):
         kvc.set_option(o, 0)
     scale = 1.0 / math.sqrt(128)
     case = W.gqa_case(6, 32, 8, 128, 16, [3000, 40, 1, 4096, 777, 2048], "bf16", seed=49)
