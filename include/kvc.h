@@ -128,7 +128,16 @@ typedef enum kvc_option {
    * (0 = automatic, 8; N >= 1 as given, and then used at any size).
    * Process-wide. */
   KVC_OPT_DYNAMIC_SHARE = 4,
-  KVC_OPT_DYNAMIC_CHUNK = 5
+  KVC_OPT_DYNAMIC_CHUNK = 5,
+  /* Test hook for the failure path of the GQA decode kernels (CUDA-core and
+   * warp-MMA). 0 (default): a wait for copied data gives up after about one
+   * second. N > 0: it gives up after N polls, normally long before the data
+   * lands, so the kernel takes its abort path on a healthy GPU: it sets
+   * KVC_FLAG_TIMEOUT, stops its warps, waits (with the normal bound) for its
+   * own copies still in flight, and returns with the output undefined. After
+   * any call that set KVC_FLAG_TIMEOUT the decode workspace must be
+   * zero-filled again before its next use. Process-wide. */
+  KVC_OPT_WAIT_POLLS = 6
 } kvc_option;
 kvc_status kvc_set_option(kvc_option opt, int64_t value);
 kvc_status kvc_get_option(kvc_option opt, int64_t* value);

@@ -26,6 +26,7 @@ __all__ = [
     "F32", "F16", "BF16", "FLAG_BAD_BLOCK", "FLAG_BAD_LEN", "FLAG_BAD_SLOT", "FLAG_TIMEOUT", "FLAG_WORKSPACE",
     "new_decode_workspace",
     "OPT_CHECKED", "OPT_BLOCKS_PER_CTA", "OPT_MAX_CTAS", "OPT_GQA_ENGINE", "OPT_DYNAMIC_SHARE", "OPT_DYNAMIC_CHUNK",
+    "OPT_WAIT_POLLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,7 +35,8 @@ _LIB_PATH = os.path.join(_HERE, "libkvc.so")
 F32, F16, BF16 = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_BLOCKS, ERR_CUDA, ERR_OUT_OF_RANGE, ERR_WORKSPACE = range(7)
 FLAG_BAD_BLOCK, FLAG_BAD_LEN, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLAG_WORKSPACE = 0x1, 0x2, 0x4, 0x8, 0x10
-OPT_CHECKED, OPT_BLOCKS_PER_CTA, OPT_MAX_CTAS, OPT_GQA_ENGINE, OPT_DYNAMIC_SHARE, OPT_DYNAMIC_CHUNK = 0, 1, 2, 3, 4, 5
+OPT_CHECKED, OPT_BLOCKS_PER_CTA, OPT_MAX_CTAS, OPT_GQA_ENGINE, OPT_DYNAMIC_SHARE, OPT_DYNAMIC_CHUNK, OPT_WAIT_POLLS = \
+    0, 1, 2, 3, 4, 5, 6
 
 # Every exported symbol of include/kvc.h with (restype, argtypes).
 _vp, _i32, _i64, _f32, _sz, _u32p = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t, \

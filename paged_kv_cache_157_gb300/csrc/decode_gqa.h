@@ -50,6 +50,7 @@ struct GqaParams {
   int dyn_share;        // positions claimed at run time, in 1/256 of all (0: none)
   int dyn_chunk;        // positions per claimed chunk (0: no dynamic tail)
   int dyn_min_static;   // keep the dynamic tail only if every CTA still gets this many static positions
+  unsigned int wait_polls;  // 0: waits for copied data bounded by ~1 s; N: give up after N polls (test hook)
 };
 
 #ifndef KVC_GQA_WARPS

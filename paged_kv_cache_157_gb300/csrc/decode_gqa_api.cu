@@ -447,6 +447,7 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
+  p.wait_polls = static_cast<unsigned int>(option(KVC_OPT_WAIT_POLLS));
 
   int occ = 1;
   CUtensorMap tk, tv;
@@ -764,8 +765,12 @@ __global__ void lse_combine_kernel(const float* __restrict__ o1, const float* __
   }
 }
 
+// Workspace of the shared-prefix decode: each pass has its own decode
+// workspace (the first pass's split-K records must never land on the second
+// pass's counters, which have to be zero when it starts), then the two
+// passes' outputs and log-sum-exps.
 struct PrefixLayout {
-  size_t inner, o1, o2, l1, l2, total;
+  size_t inner1, inner2, o1, o2, l1, l2, total;
 };
 
 kvc_status prefix_layout(int batch, int group_size, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
@@ -782,8 +787,9 @@ kvc_status prefix_layout(int batch, int group_size, int n_q_heads, int n_kv_head
   if ((s = kvc_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks, &w2)) != KVC_OK)
     return s;
   const size_t rows = static_cast<size_t>(batch) * n_q_heads;
-  L->inner = 0;
-  L->o1 = align_up(std::max(w1, w2), 256);
+  L->inner1 = 0;
+  L->inner2 = align_up(w1, 256);
+  L->o1 = L->inner2 + align_up(w2, 256);
   L->o2 = L->o1 + align_up(rows * head_dim * 4, 256);
   L->l1 = L->o2 + align_up(rows * head_dim * 4, 256);
   L->l2 = L->l1 + align_up(rows * 4, 256);
@@ -845,7 +851,7 @@ kvc_status kvc_decode_attention_shared_prefix(const void* q, const void* k_cache
   e1.lse = l1;
   s = decode_impl(q, k_cache, v_cache, block_tables, group_size * max_blocks_per_seq, prefix_lens,
                   batch / group_size, scale, n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, 0, dtype, o1,
-                  KVC_F32, ws + L.inner, L.o1, stream, nullptr, nullptr, group_size, &e1);
+                  KVC_F32, ws + L.inner1, L.inner2 - L.inner1, stream, nullptr, nullptr, group_size, &e1);
   if (s != KVC_OK) return s;
   // pass 2: each sequence's own rows
   DecodeExtra e2;
@@ -853,8 +859,8 @@ kvc_status kvc_decode_attention_shared_prefix(const void* q, const void* k_cache
   e2.row_start = prefix_lens;
   e2.row_div = group_size;
   s = decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale, n_q_heads,
-                  n_kv_heads, head_dim, block_size, num_blocks, 0, dtype, o2, KVC_F32, ws + L.inner, L.o1, stream,
-                  nullptr, nullptr, 1, &e2);
+                  n_kv_heads, head_dim, block_size, num_blocks, 0, dtype, o2, KVC_F32, ws + L.inner2, L.o1 - L.inner2,
+                  stream, nullptr, nullptr, 1, &e2);
   if (s != KVC_OK) return s;
   const int64_t rows = static_cast<int64_t>(batch) * n_q_heads;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

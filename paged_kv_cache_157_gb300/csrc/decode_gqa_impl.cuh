@@ -863,7 +863,7 @@ __global__ void __launch_bounds__(kGqaWarps * 32, kGqaCtasPerSm) gqa_decode_kern
         const bool in_cur = (cn >> 5) == (cpos >> 5);
         const int src_n = __shfl_sync(full, in_cur ? w_src0 : w_src1, cn & 31);
         const int q_n = __shfl_sync(full, in_cur ? w_q0 : w_q1, cn & 31);
-        const bool ok = mbar_wait_bounded(fbar + slot, par);
+        const bool ok = mbar_wait_data(fbar + slot, par, p.wait_polls);
         if (__any_sync(full, !ok) || s_misc[0]) {
           if (lane == 0) {
             set_flag(p.err, 0x8u);

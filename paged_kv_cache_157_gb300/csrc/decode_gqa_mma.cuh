@@ -621,7 +621,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
           const int srci = __shfl_sync(full, src, i);
           const int qo = __shfl_sync(full, qoff, i);
           if (lane == 0) {
-            ok = mbar_wait_bounded(ebar + slot, ph ^ 1u) && !*s_abort;
+            ok = mbar_wait_data(ebar + slot, ph ^ 1u, p.wait_polls) && !*s_abort;
             if (ok) {
               if (srci < 0) set_flag(p.err, 0x1u);
               meta[slot] = mi;
@@ -745,7 +745,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
     uint32_t slot = 0, ph = 0;
     bool abort_seen = false;
     for (;;) {
-      if (!mbar_wait_bounded(fbar + slot, ph) || *s_abort) {
+      if (!mbar_wait_data(fbar + slot, ph, p.wait_polls) || *s_abort) {
         abort_seen = true;
         break;
       }
@@ -815,7 +815,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
           ph ^= 1u;
         }
         if (m.flags & kLast) break;
-        if (!mbar_wait_bounded(fbar + slot, ph) || *s_abort) {
+        if (!mbar_wait_data(fbar + slot, ph, p.wait_polls) || *s_abort) {
           abort_seen = true;
           break;
         }

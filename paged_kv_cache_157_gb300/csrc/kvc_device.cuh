@@ -293,6 +293,31 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Non-blocking probe of a phase (test_wait never suspends the thread, where
+// try_wait may wait a while inside the instruction).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The same wait for data a copy brings, with an optional poll limit: polls
+// == 0 keeps the bound above; polls > 0 gives up after that many
+// non-blocking probes (a test hook that makes a kernel take its abort path on
+// a healthy GPU).
+__device__ __forceinline__ bool mbar_wait_data(uint64_t* bar, uint32_t parity, uint32_t polls) {
+  if (polls == 0) return mbar_wait_bounded(bar, parity);
+  for (uint32_t i = 0; i < polls; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  return false;
+}
+
 // --------------------------------------------------------------- bulk copy
 
 // 1-D bulk copy global -> shared through the TMA unit; completion is

@@ -62,7 +62,7 @@ kvc_status current_device(DeviceInfo** out) {
   return KVC_OK;
 }
 
-static int64_t g_options[6] = {0, 0, 0, 0, 0, 0};
+static int64_t g_options[7] = {0, 0, 0, 0, 0, 0, 0};
 
 int64_t option(kvc_option opt) { return g_options[static_cast<int>(opt)]; }
 
@@ -119,12 +119,13 @@ const char* kvc_last_error_message(void) { return kvc::t_message.c_str(); }
 
 kvc_status kvc_set_option(kvc_option opt, int64_t value) {
   int o = static_cast<int>(opt);
-  if (o < 0 || o > 5) return kvc::fail(KVC_ERR_INVALID_ARG, "unknown option %d", o);
+  if (o < 0 || o > 6) return kvc::fail(KVC_ERR_INVALID_ARG, "unknown option %d", o);
   if (value < 0) return kvc::fail(KVC_ERR_INVALID_ARG, "option value must be >= 0");
   if (opt == KVC_OPT_CHECKED && value > 1) return kvc::fail(KVC_ERR_INVALID_ARG, "checked mode is 0 or 1");
   if (opt == KVC_OPT_GQA_ENGINE && value > 3) return kvc::fail(KVC_ERR_INVALID_ARG, "GQA engine is 0, 1, 2 or 3");
   if (opt == KVC_OPT_DYNAMIC_SHARE && value > 256) return kvc::fail(KVC_ERR_INVALID_ARG, "dynamic share is 0 to 256");
   if (opt == KVC_OPT_DYNAMIC_CHUNK && value > 4096) return kvc::fail(KVC_ERR_INVALID_ARG, "dynamic chunk is 0 to 4096");
+  if (opt == KVC_OPT_WAIT_POLLS && value > (1 << 20)) return kvc::fail(KVC_ERR_INVALID_ARG, "wait polls is 0 to 2^20");
   kvc::g_options[o] = value;
   return KVC_OK;
 }
@@ -133,7 +134,7 @@ kvc_status kvc_set_checked(int enabled) { return kvc_set_option(KVC_OPT_CHECKED,
 
 kvc_status kvc_get_option(kvc_option opt, int64_t* value) {
   int o = static_cast<int>(opt);
-  if (o < 0 || o > 5 || value == nullptr) return kvc::fail(KVC_ERR_INVALID_ARG, "bad option query");
+  if (o < 0 || o > 6 || value == nullptr) return kvc::fail(KVC_ERR_INVALID_ARG, "bad option query");
   *value = kvc::g_options[o];
   return KVC_OK;
 }

@@ -47,6 +47,15 @@ def test_options_roundtrip(kvc):
         kvc.set_option(kvc.OPT_CHECKED, 2)
     with pytest.raises(kvc.KvcError):
         kvc.set_option(9, 1)
+    lib = kvc.raw()
+    assert lib.kvc_set_checked(1) == kvc.OK and kvc.get_option(kvc.OPT_CHECKED) == 1
+    assert lib.kvc_set_checked(0) == kvc.OK and kvc.get_option(kvc.OPT_CHECKED) == 0
+    for o, v in ((kvc.OPT_DYNAMIC_SHARE, 256), (kvc.OPT_DYNAMIC_CHUNK, 3), (kvc.OPT_WAIT_POLLS, 5)):
+        kvc.set_option(o, v)
+        assert kvc.get_option(o) == v
+        kvc.set_option(o, 0)
+    with pytest.raises(kvc.KvcError):
+        kvc.set_option(kvc.OPT_DYNAMIC_SHARE, 257)
     for e in (1, 2, 3, 0):
         kvc.set_option(kvc.OPT_GQA_ENGINE, e)
         assert kvc.get_option(kvc.OPT_GQA_ENGINE) == e

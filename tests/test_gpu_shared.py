@@ -102,8 +102,11 @@ def test_shared_prefix_split_k_and_engines(kvc, blocks_per_cta, engine):
     assert kvc.get_error_flags() == 0
 
 
-def test_config3_shape_sampled_against_plain_decode(kvc):
-    # Llama-2-7B-shaped MHA, 8 prompts of 2048 tokens forked 8 ways + 256 private tokens: equals the plain decode
+@pytest.mark.parametrize("engine", [0, 1, 3])
+def test_config3_shape_sampled_against_plain_decode(kvc, engine):
+    # Llama-2-7B-shaped MHA, 8 prompts of 2048 tokens forked 8 ways + 256 private tokens: equals the plain decode.
+    # Each engine's first pass leaves split-K records that must not reach the second pass's counters.
+    kvc.set_option(kvc.OPT_GQA_ENGINE, engine)
     case = W.shared_case(8, 8, 2048, 256, 32, 128, 16, "f16", 44, device="cuda")
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in case.items()}
     B = 64

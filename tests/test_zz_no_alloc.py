@@ -110,6 +110,33 @@ def test_static_scratch_after_a_call_with_a_bad_block_id(kvc):
     assert kvc.get_error_flags() == 0
 
 
+def test_static_scratch_after_a_call_that_gave_up_waiting(kvc):
+    # A call whose waits give up (the KVC_OPT_WAIT_POLLS test hook) leaves the
+    # counters in the built-in scratch non-zero; the next call clears them
+    # itself and must match the workspace path.
+    for o in (kvc.OPT_BLOCKS_PER_CTA, kvc.OPT_MAX_CTAS, kvc.OPT_CHECKED, kvc.OPT_GQA_ENGINE,
+              kvc.OPT_DYNAMIC_SHARE, kvc.OPT_DYNAMIC_CHUNK, kvc.OPT_WAIT_POLLS):
+        kvc.set_option(o, 0)
+    scale = 1.0 / math.sqrt(128)
+    case = W.gqa_case(6, 32, 8, 128, 16, [3000, 40, 1, 4096, 777, 2048], "bf16", seed=50)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in case.items()}
+    ref = _reference(kvc, dev, scale)
+    torch.cuda.synchronize()
+    assert kvc.get_error_flags() == 0
+    out = torch.empty_like(ref)
+    kvc.set_option(kvc.OPT_WAIT_POLLS, 1)
+    try:
+        assert _c_abi_static(kvc, dev, scale, out) == kvc.OK
+        assert kvc.get_error_flags() & kvc.FLAG_TIMEOUT
+    finally:
+        kvc.set_option(kvc.OPT_WAIT_POLLS, 0)
+    out = torch.full_like(ref, float("nan"))
+    assert _c_abi_static(kvc, dev, scale, out) == kvc.OK
+    torch.cuda.synchronize()
+    assert float((out - ref).abs().max()) <= 2e-3
+    assert kvc.get_error_flags() == 0
+
+
 def test_static_scratch_refuses_oversized_shapes(kvc):
     kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, 1)  # one cache block per CTA: far more records than 16 MiB hold
     try:
