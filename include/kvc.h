@@ -399,8 +399,8 @@ kvc_status kvc_decode_mla_workspace_size(int batch, int n_q_heads, int d_c, int 
  * where c_t is the cached row of width d_c + d_r (keys use the whole row,
  * values its first d_c elements). The caller applies W^UV and the output
  * projection to `out`. dtype must be BF16; out_dtype F32 or BF16.
- * Supported: d_c = 512, d_r = 64, n_q_heads a multiple of 64 up to 128,
- * block_size a multiple of 64. Source: llm-compass section 2.2. */
+ * Supported: d_c = 512, d_r = 64, n_q_heads = 128, block_size a multiple of
+ * 16 up to 256, batch up to 128. Source: llm-compass section 2.2. */
 kvc_status kvc_decode_attention_mla(const void* q_absorbed, const void* latent_cache, const int32_t* block_tables,
                                     int max_blocks_per_seq, const int32_t* context_lens, int batch, float scale,
                                     int n_q_heads, int d_c, int d_r, int block_size, int64_t num_blocks,

@@ -7,30 +7,36 @@
 //     o_h = sum_t a_t c_t[0 : d_c]      (d_c = 512)
 //
 // Design (sm_103a, one CTA per SM):
-// * A CTA works on 32-token tiles and one half (256) of the 512 output
+// * A CTA works on 48-token tiles and one half (256) of the 512 output
 //   dimensions; its partner CTA (adjacent in the grid) takes the other half of
 //   the same tiles, so the latent tile is fetched from HBM once and the second
-//   read is served by L2. Both compute S = Q~ C^T in full: the O half
-//   (128 x 256 fp32), two S buffers (128 x 32 fp32), two P buffers and part
-//   of Q~ fit the 512 TMEM columns, which the whole O (128 x 512 fp32) alone
-//   would fill.
-// * Q~ [128 x 576] bf16 is split: columns 0..255 sit in TMEM (128 columns of
-//   bf16 pairs, written by the softmax warps) and feed the first 16 K steps of
-//   S as the A operand from tensor memory; columns 256..575 sit in shared
-//   memory (80 KB). That leaves room for four latent tile stages [32 x 576]
-//   (36 KB each) in the 128B-swizzled K-major layout that TMA writes and the
-//   UMMA descriptors read: a stage is held from S(t) until PV(t), and the
-//   other two stages keep the next tiles' copies in flight meanwhile.
+//   read is served by L2. Both compute S = Q~ C^T in full: the O half (128 x
+//   256 fp32) alone takes half of the 512 TMEM columns, which the whole O would
+//   fill.
+// * Tile size: a tcgen05.mma with M = 128 and K = 16 costs ~50 cycles for any
+//   N up to 64 (probe: 1276 MACs/cycle at N = 32, 2553 at N = 64, 3950 at N =
+//   256), so S, 36 MMAs per tile, costs per token in inverse proportion to
+//   the tile. 48 tokens is the largest tile whose three stages fit next to
+//   the part of Q~ kept in shared memory.
+// * TMEM (512 columns): O half at 0..255; two 48-column S/P buffers at
+//   256..351, where the softmax warps overwrite S(t) in place with P(t) as two
+//   bf16 parts (hi = bf16(p), lo = bf16(p - hi), 24 columns each, so hi + lo
+//   carries p to about 2^-17); Q~ columns 0..319 as bf16 pairs at 352..511,
+//   the A operand of the first 20 K steps of S. Q~ columns 320..575 sit in
+//   shared memory (64 KB) next to three latent tile stages [48 x 576] (54 KB
+//   each, 128B-swizzled K-major as TMA writes them and the MMA descriptors
+//   read them). A stage is held from S(t) until PV(t); with three, the next
+//   tiles' copies are in flight meanwhile. A tile may straddle two 64-token
+//   cache blocks, so it arrives as 27 boxes of 16 rows x 64 columns.
 // * Warp roles: warps 0-3 = softmax and epilogue (thread = head = TMEM lane),
 //   warp 4 = TMA producer, warp 5 = MMA issuer and TMEM owner.
-//   Per tile: S(t) = Q~ C_t^T (36 MMAs, K = 16 each, N = 32) -> softmax reads
+//   Per tile: S(t) = Q~ C_t^T (36 MMAs, K = 16 each, N = 48) -> softmax reads
 //   S from TMEM, updates the running max lazily (O in TMEM is rescaled only
 //   when the max grows by more than 2^8, after waiting for the previous PV),
-//   writes P = exp2(s - m) into TMEM as two bf16 parts (hi = bf16(p), lo =
-//   bf16(p - hi), so hi + lo carries p to about 2^-17) -> O += P_hi V_t +
-//   P_lo V_t (4 MMAs with A read from TMEM, N = 256, V = the first 512 columns
-//   of the same tile, read MN-major). S and P are double buffered and S(t+1)
-//   is queued before PV(t), so the tensor core works while the softmax runs.
+//   writes P over S -> O += P_hi V_t + P_lo V_t (6 MMAs with A read from TMEM,
+//   N = 256, V = this CTA's half of the first 512 columns of the same tile,
+//   read MN-major). S(t+1) is queued before PV(t), so the tensor core works
+//   while the softmax runs; S(t+2) reuses the buffer of P(t) once PV(t) is done.
 // * Work split: as in the GQA kernel, the tiles of all sequences are laid end
 //   to end and CTA pair c takes a contiguous range; a sequence cut by a range
 //   boundary leaves fp32 records (m, l, O) and the last contributing CTA of
@@ -57,48 +63,50 @@ constexpr int kHeads = 128;          // M of every MMA
 constexpr int kDc = 512;             // latent (value) width
 constexpr int kW = 576;              // cached row width
 constexpr int kKB = kW / 64;         // 64-element (128 B) K blocks of a row: 9
-constexpr int kTile = 32;            // tokens per tile (MMA N for S)
+constexpr int kTile = 48;            // tokens per tile (MMA N for S)
+constexpr int kBoxRows = 16;         // rows per TMA box (a box never straddles a cache block)
+constexpr int kBoxes = kTile / kBoxRows;  // boxes per 64-column block of a tile: 3
 constexpr int kHalf = kDc / 2;       // output dims per CTA: 256
-constexpr int kStages = 4;           // latent tile stages
-constexpr int kSBufs = 2;            // S buffers in TMEM
-constexpr int kPBufs = 2;            // P buffers in TMEM
+constexpr int kStages = 3;           // latent tile stages
+constexpr int kSPBufs = 2;           // S/P buffers in TMEM
 constexpr int kThreads = 192;        // 6 warps
-constexpr int kMaxBatch = 256;
+constexpr int kMaxBatch = 128;
 
-// Q~ is split: columns [0, 256) live in TMEM (the A operand of the first 16
-// K steps), columns [256, 576) in shared memory (5 blocks of 64 columns).
-constexpr int kQTmemK = 256;                          // Q~ columns held in TMEM
-constexpr int kQSmemKB0 = kQTmemK / 64;               // first 64-column block in shared memory: 4
+// Q~ is split: columns [0, 320) live in TMEM (the A operand of the first 20
+// K steps), columns [320, 576) in shared memory (4 blocks of 64 columns).
+constexpr int kQTmemK = 320;                          // Q~ columns held in TMEM
+constexpr int kQSmemKB0 = kQTmemK / 64;               // first 64-column block in shared memory: 5
 constexpr uint32_t kQSub = kHeads * 128;              // one 64-column block of Q~: 16384
-constexpr uint32_t kQBytes = (kKB - kQSmemKB0) * kQSub;  // 81920
-constexpr uint32_t kTileBytes = kTile * kW * 2;      // 36864
-constexpr uint32_t kTileSub = kTile * 128;           // one 64-column block of a tile: 4096
+constexpr uint32_t kQBytes = (kKB - kQSmemKB0) * kQSub;  // 65536
+constexpr uint32_t kTileBytes = kTile * kW * 2;      // 55296
+constexpr uint32_t kTileSub = kTile * 128;           // one 64-column block of a tile: 6144
+constexpr uint32_t kBoxBytes = kBoxRows * 128;       // one TMA box: 2048
 
-// TMEM columns: O half at 0..255, two S buffers (32 columns each) at
-// 256..319, two P buffers at 320..383 (each: the high bf16 part of the
-// weights, 16 columns = 32 bf16 per head, then the low part), Q~ columns
-// 0..255 as bf16 pairs at 384..511.
+// TMEM columns: O half at 0..255, two S/P buffers of kTile columns at
+// 256..351 (P: the high bf16 parts of the weights in the first kTile / 2
+// columns, 2 per column, then the low parts), Q~ columns 0..319 as bf16 pairs
+// at 352..511.
 constexpr uint32_t kColO = 0;
-constexpr uint32_t kColS = 256;
-constexpr uint32_t kColP = 320;
-constexpr uint32_t kColQ = 384;
+constexpr uint32_t kColSP = 256;
+constexpr uint32_t kColQ = kColSP + kSPBufs * kTile;  // 352
 constexpr uint32_t kTmemCols = 512;
+static_assert(kColQ + kQTmemK / 2 == kTmemCols, "TMEM budget");
 
-// Shared memory carve-up (offsets from a 1024-byte aligned base).
+// Shared memory carve-up (offsets from the 1024-byte aligned base of the
+// dynamic shared memory).
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffC = kOffQ + kQBytes;
 constexpr uint32_t kOffBar = kOffC + kStages * kTileBytes;
 // barrier indices
 enum {
   B_QFULL = 0, B_QEMPTY, B_CFULL0, B_CEMPTY0 = B_CFULL0 + kStages, B_SFULL0 = B_CEMPTY0 + kStages,
-  B_SEMPTY0 = B_SFULL0 + kSBufs, B_PFULL0 = B_SEMPTY0 + kSBufs, B_PEMPTY0 = B_PFULL0 + kPBufs,
-  B_OFREE = B_PEMPTY0 + kPBufs, B_FINAL, B_COUNT
+  B_PFULL0 = B_SFULL0 + kSPBufs, B_PEMPTY0 = B_PFULL0 + kSPBufs, B_OFREE = B_PEMPTY0 + kSPBufs, B_FINAL, B_COUNT
 };
 constexpr uint32_t kOffMisc = kOffBar + B_COUNT * 8;  // tmem address, abort flag, last flag
-constexpr int kMergeChunk = 64;  // record slots the merging warpgroup lists in shared memory at a time
+constexpr int kMergeChunk = 32;  // record slots the merging warpgroup lists in shared memory at a time
 constexpr uint32_t kOffRec = kOffMisc + 16;
 constexpr uint32_t kOffScan = kOffRec + kMergeChunk * 4;
-constexpr uint32_t smem_bytes(int batch) { return kOffScan + (batch + 1 + 32) * 4 + 1024; }
+constexpr uint32_t smem_bytes(int batch) { return kOffScan + (batch + 1 + 32) * 4; }
 
 struct Params {
   const __nv_bfloat16* q;  // absorbed queries [batch, 128, 576]
@@ -190,6 +198,26 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   return false;
 }
 
+// The same bound, but each probe may suspend the thread (try_wait) until the
+// phase completes or a time hint runs out: the producer and MMA-issuer warps
+// share their SM sub-partitions with softmax warps, and a spinning waiter
+// would take issue slots from them.
+__device__ __forceinline__ bool wait_phase_yield(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                 unsigned int* err) {
+  if (try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1; i < kWaitLimit; ++i) {
+    if (try_wait(bar, parity)) return true;
+    if ((i & 7u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitNs) break;
+    }
+  }
+  *abort_flag = 1;
+  set_flag(err, 0x8u);
+  return false;
+}
+
 // UMMA shared-memory descriptor: start address, leading / stride byte offsets,
 // the fixed version bits of sm_100 descriptors and the swizzle mode
 // (2 = 128B, 4 = 64B).
@@ -249,6 +277,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
@@ -388,10 +439,16 @@ struct Walker {
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
                       const Params p) {
-  extern __shared__ unsigned char smem_raw[];
-  const uint32_t raw_addr = smem_addr(smem_raw);
-  const uint32_t base = (raw_addr + 1023u) & ~1023u;
-  unsigned char* sm = smem_raw + (base - raw_addr);
+  // 1024-byte alignment (the 128B swizzle atom of TMA and UMMA) is declared,
+  // so the whole dynamic allocation is usable; a misplaced window is
+  // refused before any copy or TMEM allocation.
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t base = smem_addr(smem_raw);
+  if ((base & 1023u) != 0) {
+    if (threadIdx.x == 0) set_flag(p.err, 0x8u);
+    return;
+  }
+  unsigned char* sm = smem_raw;
   const uint32_t sQ = base + kOffQ, sC = base + kOffC;
   const uint32_t bar0 = base + kOffBar;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
@@ -410,11 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     *s_abort = 0;
     for (int i = 0; i < B_COUNT; ++i) {
       // Q~ full: the producer's copy plus the four softmax warps' TMEM stores;
-      // S empty, P full and O free: the four softmax warps; all others: one.
+      // P full and O free: the four softmax warps; all others: one.
       uint32_t c = 1;
       if (i == B_QFULL) c = 5;
-      if ((i >= B_SEMPTY0 && i < B_SEMPTY0 + kSBufs) || (i >= B_PFULL0 && i < B_PFULL0 + kPBufs) || i == B_OFREE)
-        c = 4;
+      if ((i >= B_PFULL0 && i < B_PFULL0 + kSPBufs) || i == B_OFREE) c = 4;
       mbar_init(&bars[i], c);
     }
     fence_barrier_init();
@@ -473,55 +529,85 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t g = 0, seg_i = 0;
-      uint32_t issued[kStages] = {};
-      bool q_pending = false;
-      Segment sg;
-      Walker w = walk;
-      while (!*s_abort && w.next(p, s_scan, sg)) {
-        if (sg.ntiles == 0) continue;
-        if (seg_i > 0 && !wait_phase(bar(B_QEMPTY), (seg_i - 1) & 1u, s_abort, p.err)) break;
-        arrive_expect(bar(B_QFULL), kQBytes);
-        for (int kb = kQSmemKB0; kb < kKB; ++kb)
-          tma_load_3d(sQ + (kb - kQSmemKB0) * kQSub, &tm_q, kb * 64, 0, sg.seq, bar(B_QFULL));
-        q_pending = true;
-        const int32_t* bt = p.block_tables + static_cast<int64_t>(sg.seq) * p.max_blocks;
-        bool ok = true;
-        for (int t = sg.t0; t < sg.t1; ++t, ++g) {
-          const int st = g % kStages;
-          if (g >= kStages && !wait_phase(bar(B_CEMPTY0 + st), (g / kStages - 1) & 1u, s_abort, p.err)) {
-            ok = false;
-            break;
-          }
-          const int j = (t * kTile) / p.block_size;
+    // The whole warp walks the segments; lane 0 waits and issues. A tile may
+    // straddle two cache blocks, so it arrives as 16-row boxes that each lie
+    // in one block; the source row of every box is read from the block table
+    // 32 boxes (about ten tiles) at a time, one box per lane, so a table read
+    // never sits between two tiles' copies.
+    uint32_t g = 0, seg_i = 0;
+    uint32_t issued[kStages] = {};
+    bool q_pending = false;
+    Segment sg;
+    Walker w = walk;
+    bool ok = true;
+    for (;;) {
+      // every decision below is uniform over the warp (lane 0's view of the abort flag)
+      if (__shfl_sync(0xffffffffu, *s_abort ? 1 : 0, 0) != 0 || !w.next(p, s_scan, sg)) break;
+      if (sg.ntiles == 0) continue;
+      if (lane == 0) {
+        ok = seg_i == 0 || wait_phase_yield(bar(B_QEMPTY), (seg_i - 1) & 1u, s_abort, p.err);
+        if (ok) {
+          arrive_expect(bar(B_QFULL), kQBytes);
+          for (int kb = kQSmemKB0; kb < kKB; ++kb)
+            tma_load_3d(sQ + (kb - kQSmemKB0) * kQSub, &tm_q, kb * 64, 0, sg.seq, bar(B_QFULL));
+          q_pending = true;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      const int32_t* bt = p.block_tables + static_cast<int64_t>(sg.seq) * p.max_blocks;
+      const int last_blk = (seq_rows(p.context_lens, sg.seq, p.block_size, p.max_blocks) - 1) / p.block_size;
+      int win = -1 << 30;  // first box of the window the lanes hold
+      int my_row = 0;      // source row (pool row of the box's first token) of box win + lane
+      for (int t = sg.t0; t < sg.t1; ++t, ++g) {
+        const int b0 = t * kBoxes;
+        if (b0 + kBoxes > win + 32) {
+          win = b0;
+          // Rows past the end of the sequence read its last block (they are
+          // masked out of the softmax and zeroed before PV).
+          const int tok = (win + lane) * kBoxRows;
+          const int j = min(tok / p.block_size, last_blk);
           int phys = __ldg(bt + j);
           if (phys < 0 || phys >= p.num_blocks) {
             set_flag(p.err, 0x1u);
             phys = 0;  // keep the pipeline moving on valid memory; the output is flagged
           }
-          const int row = phys * p.block_size + (t * kTile) % p.block_size;
-          arrive_expect(bar(B_CFULL0 + st), kTileBytes);
-          for (int kb = 0; kb < kKB; ++kb)
-            tma_load_2d(sC + st * kTileBytes + kb * kTileSub, &tm_c, kb * 64, row, bar(B_CFULL0 + st));
-          ++issued[st];
+          my_row = phys * p.block_size + tok % p.block_size;
         }
+        int rows[kBoxes];
+#pragma unroll
+        for (int c = 0; c < kBoxes; ++c) rows[c] = __shfl_sync(0xffffffffu, my_row, b0 - win + c);
+        const int st = g % kStages;
+        if (lane == 0) {
+          ok = g < kStages || wait_phase_yield(bar(B_CEMPTY0 + st), (g / kStages - 1) & 1u, s_abort, p.err);
+          if (ok) {
+            arrive_expect(bar(B_CFULL0 + st), kTileBytes);
+#pragma unroll
+            for (int c = 0; c < kBoxes; ++c)
+              for (int kb = 0; kb < kKB; ++kb)
+                tma_load_2d(sC + st * kTileBytes + kb * kTileSub + c * kBoxBytes, &tm_c, kb * 64, rows[c],
+                            bar(B_CFULL0 + st));
+            ++issued[st];
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        ++seg_i;
       }
-      if (*s_abort) {
-        // Copies still in flight must land before this shared memory goes away:
-        // wait (bounded) for the last phase of every barrier this warp armed.
-        for (int st = 0; st < kStages; ++st) {
-          if (issued[st] == 0) continue;
-          const uint64_t t0 = globaltimer_ns();
-          while (!try_wait(bar(B_CFULL0 + st), (issued[st] - 1) & 1u) && globaltimer_ns() - t0 < kWaitNs) {
-          }
+      if (!ok) break;
+      ++seg_i;
+    }
+    if (lane == 0 && *s_abort) {
+      // Copies still in flight must land before this shared memory goes away:
+      // wait (bounded) for the last phase of every barrier this warp armed.
+      for (int st = 0; st < kStages; ++st) {
+        if (issued[st] == 0) continue;
+        const uint64_t t0 = globaltimer_ns();
+        while (!try_wait(bar(B_CFULL0 + st), (issued[st] - 1) & 1u) && globaltimer_ns() - t0 < kWaitNs) {
         }
-        if (q_pending && seg_i > 0) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!try_wait(bar(B_QFULL), (seg_i - 1) & 1u) && globaltimer_ns() - t0 < kWaitNs) {
-          }
+      }
+      if (q_pending && seg_i > 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!try_wait(bar(B_QFULL), (seg_i - 1) & 1u) && globaltimer_ns() - t0 < kWaitNs) {
         }
       }
     }
@@ -541,16 +627,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && !*s_abort && w.next(p, s_scan, sg)) {
         if (sg.ntiles == 0) continue;
-        if (!wait_phase(bar(B_QFULL), seg_i & 1u, s_abort, p.err)) break;
+        if (!wait_phase_yield(bar(B_QFULL), seg_i & 1u, s_abort, p.err)) break;
         fence_after();
         const uint32_t g_first = g;
         // PV of global tile gi: O (+)= P_hi V + P_lo V with A = P from TMEM and
         // B = this CTA's half of the tile's first 512 columns, read MN-major.
         auto issue_pv = [&](uint32_t gi) -> bool {
-          const uint32_t pb = gi % kPBufs;
-          if (!wait_phase(bar(B_PFULL0 + pb), (gi / kPBufs) & 1u, s_abort, p.err)) return false;
+          const uint32_t pb = gi % kSPBufs;
+          if (!wait_phase_yield(bar(B_PFULL0 + pb), (gi / kSPBufs) & 1u, s_abort, p.err)) return false;
           const bool first = (gi == g_first);
-          if (first && seg_i > 0 && !wait_phase(bar(B_OFREE), (seg_i - 1) & 1u, s_abort, p.err)) return false;
+          if (first && seg_i > 0 && !wait_phase_yield(bar(B_OFREE), (seg_i - 1) & 1u, s_abort, p.err)) return false;
           fence_after();
           const uint32_t st = gi % kStages;
           const uint64_t bv0 = smem_desc(sC + st * kTileBytes + (4 * hf) * kTileSub, kTileSub, 1024, 2);
@@ -558,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int part = 0; part < 2; ++part) {  // P_hi, then P_lo, against the same V rows
 #pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks) {
-              mma_bf16_ts(tmem + kColO, tmem + kColP + pb * kTile + part * (kTile / 2) + ks * 8,
+              mma_bf16_ts(tmem + kColO, tmem + kColSP + pb * kTile + part * (kTile / 2) + ks * 8,
                           bv0 + ((ks * 2048) >> 4), id_pv, (first && part == 0 && ks == 0) ? 0u : 1u);
             }
           }
@@ -568,9 +654,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         for (int t = sg.t0; t < sg.t1 && ok; ++t, ++g) {
           const uint32_t st = g % kStages;  // latent stage
-          const uint32_t sb = g % kSBufs;   // S buffer
-          if (!wait_phase(bar(B_CFULL0 + st), (g / kStages) & 1u, s_abort, p.err)) { ok = false; break; }
-          if (g >= kSBufs && !wait_phase(bar(B_SEMPTY0 + sb), (g / kSBufs - 1) & 1u, s_abort, p.err)) {
+          const uint32_t sb = g % kSPBufs;  // S/P buffer
+          if (!wait_phase_yield(bar(B_CFULL0 + st), (g / kStages) & 1u, s_abort, p.err)) { ok = false; break; }
+          // S(g) overwrites the buffer that held P(g - 2): PV(g - 2) must be done
+          if (g >= kSPBufs && !wait_phase_yield(bar(B_PEMPTY0 + sb), (g / kSPBufs - 1) & 1u, s_abort, p.err)) {
             ok = false;
             break;
           }
@@ -579,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Descriptors advance by constant offsets (in 16-byte units) from
             // one base per operand, so each K step costs one add.
             const uint64_t b0 = smem_desc(sC + st * kTileBytes, 16, 1024, 2);
-            const uint32_t d_s = tmem + kColS + sb * kTile;
+            const uint32_t d_s = tmem + kColSP + sb * kTile;
 #pragma unroll
             for (int ks = 0; ks < kW / 16; ++ks) {
               const int kb = ks >> 2, kin = ks & 3;
@@ -631,18 +718,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_after();
       {
+        // This head's Q~ columns [0, 320): 40 16-byte loads issued in two
+        // batches (one round trip each) before the TMEM stores.
         const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(sg.seq) * kHeads + h) * kW);
-        for (int c = 0; c < kQTmemK / 2; c += 32) {
-          uint32_t r[32];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 x = __ldg(qrow + c / 4 + i);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[80];
+#pragma unroll
+          for (int i = 0; i < 20; ++i) {
+            const uint4 x = __ldg(qrow + half * 20 + i);
             r[4 * i] = x.x;
             r[4 * i + 1] = x.y;
             r[4 * i + 2] = x.z;
             r[4 * i + 3] = x.w;
           }
-          tmem_st32u(lane_addr + kColQ + c, r);
+          tmem_st32u(lane_addr + kColQ + half * 80, r);
+          tmem_st32u(lane_addr + kColQ + half * 80 + 32, r + 32);
+          tmem_st16u(lane_addr + kColQ + half * 80 + 64, r + 64);
+        }
+        // Warm L2 with the next segment's rows (this CTA's walk is known), so
+        // its start costs two L2 round trips instead of two DRAM ones.
+        Walker wn = w;
+        Segment sn;
+        if (wn.next(p, s_scan, sn) && sn.ntiles > 0) {
+          const char* nrow = reinterpret_cast<const char*>(p.q + (static_cast<int64_t>(sn.seq) * kHeads + h) * kW);
+#pragma unroll
+          for (int i = 0; i < 5; ++i) prefetch_l2(nrow + 128 * i);
         }
       }
       fence_before();
@@ -651,17 +752,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -__builtin_huge_valf(), l = 0.f;
       const uint32_t g_first = g;
       for (int t = sg.t0; t < sg.t1; ++t, ++g) {
-        const uint32_t sb = g % kSBufs, pb = g % kPBufs;
-        if (!__all_sync(0xffffffffu, wait_phase(bar(B_SFULL0 + sb), (g / kSBufs) & 1u, s_abort, p.err))) {
+        const uint32_t sb = g % kSPBufs, pb = sb;
+        if (!__all_sync(0xffffffffu, wait_phase(bar(B_SFULL0 + sb), (g / kSPBufs) & 1u, s_abort, p.err))) {
           ok = false;
           break;
         }
         fence_after();
         float s[kTile];
-        tmem_ld32(lane_addr + kColS + sb * kTile, s);
-        fence_before();
-        __syncwarp();
-        if (lane == 0) arrive(bar(B_SEMPTY0 + sb));
+        tmem_ld32(lane_addr + kColSP + sb * kTile, s);
+        tmem_ld16(lane_addr + kColSP + sb * kTile + 32, s + 32);
         const int valid = n_rows - t * kTile;
         float mt = -__builtin_huge_valf();
 #pragma unroll
@@ -669,9 +768,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           s[i] = (i < valid) ? s[i] * p.qscale : -__builtin_huge_valf();
           mt = fmaxf(mt, s[i]);
         }
-        // This P buffer was last read by PV(g - 2), long done in the steady state.
-        if (g >= kPBufs &&
-            !__all_sync(0xffffffffu, wait_phase(bar(B_PEMPTY0 + pb), (g / kPBufs - 1) & 1u, s_abort, p.err))) {
+        // This buffer's previous P was read by PV(g - 2), done before S(g) was issued.
+        if (g >= kSPBufs &&
+            !__all_sync(0xffffffffu, wait_phase(bar(B_PEMPTY0 + pb), (g / kSPBufs - 1) & 1u, s_abort, p.err))) {
           ok = false;
           break;
         }
@@ -684,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // max grew by more than 2^8)
             const uint32_t gp = g - 1;
             if (!__all_sync(0xffffffffu,
-                            wait_phase(bar(B_PEMPTY0 + gp % kPBufs), (gp / kPBufs) & 1u, s_abort, p.err))) {
+                            wait_phase(bar(B_PEMPTY0 + gp % kSPBufs), (gp / kSPBufs) & 1u, s_abort, p.err))) {
               ok = false;
               break;
             }
@@ -700,7 +799,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
           m = m_new;
         }
-        // Row h of P in TMEM: 16 columns of bf16 pairs (hi), then 16 (lo).
+        // Row h of P in TMEM, over the S it was computed from: kTile / 2
+        // columns of bf16 pairs (hi), then kTile / 2 (lo).
         uint32_t pk[kTile];
 #pragma unroll
         for (int i = 0; i < kTile / 2; ++i) {
@@ -710,7 +810,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[i] = hi;
           pk[kTile / 2 + i] = pack_bf16(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
         }
-        tmem_st32u(lane_addr + kColP + pb * kTile, pk);
+        tmem_st32u(lane_addr + kColSP + pb * kTile, pk);
+        tmem_st16u(lane_addr + kColSP + pb * kTile + 32, pk + 32);
         if (valid < kTile) {
           // Rows past the end of the sequence (the rest of its last block) may
           // hold anything, NaN included; their weight is 0, but 0 x NaN is NaN,
@@ -733,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- epilogue: wait for the last PV, read O, write output or record
       {
         const uint32_t gl = g - 1;
-        const bool got = ok && __all_sync(0xffffffffu, wait_phase(bar(B_PEMPTY0 + gl % kPBufs), (gl / kPBufs) & 1u,
+        const bool got = ok && __all_sync(0xffffffffu, wait_phase(bar(B_PEMPTY0 + gl % kSPBufs), (gl / kSPBufs) & 1u,
                                                                   s_abort, p.err));
         if (block_any128(!got || *s_abort)) {
           ok = false;
@@ -792,9 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Merge the unit's records with the log-sum-exp rule. The record
           // slots of the contributors are listed in shared memory (kMergeChunk
           // at a time, computed in parallel); pass 1 gives every head (thread
-          // h) its maximum and sum, pass 2 lets each half warp read one head's
-          // 256-float record rows as contiguous 1 KB runs and write its output
-          // row with 16-byte stores.
+          // h) its maximum and sum, pass 2 its output row.
           int* s_rec = reinterpret_cast<int*>(sm + kOffRec);
           const int span = static_cast<int>(c1 - c0 + 1);
           auto list_records = [&](int base, int nc) {
@@ -825,43 +924,95 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           const float invL = 1.0f / L;
-          const int half = lane >> 4, l16 = lane & 15;
-          for (int jj = 0; jj < 16; ++jj) {
-            const int src = 2 * jj + half;  // lane (head) of the warp this half warp serves
-            const int hj = warp * 32 + src;
-            const float Mj = __shfl_sync(0xffffffffu, M, src);
-            const float iLj = __shfl_sync(0xffffffffu, invL, src);
-            float acc[16];
+          if (span <= 4) {
+            // Pass 2, the common case (at most 4 contributors, all listed):
+            // thread h first takes f_i = 2^(m_i - M) of its own head for
+            // every record i; then each warp writes its 32 heads' rows, 4
+            // heads at a time, every load independent of the others and
+            // coalesced (lane L reads floats 4L..4L+3 and 128+4L..131+4L of a
+            // record row).
+            float f[4];
+            int rsv[4];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-            for (int base = 0; base < span; base += kMergeChunk) {
-              const int nc = min(kMergeChunk, span - base);
-              if (span > kMergeChunk) list_records(base, nc);  // uniform over the warpgroup
-#pragma unroll 2
-              for (int i = 0; i < nc; ++i) {
-                const int rs = s_rec[i];
-                if (rs < 0) continue;
-                const int64_t r = static_cast<int64_t>(rs) * kHeads + hj;
-                const float mc = __ldcg(p.rec_ml + r * 2);
-                const float4* srcp = reinterpret_cast<const float4*>(p.rec_o + r * kHalf) + l16 * 4;
-                float4 x[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) x[k] = __ldcg(srcp + k);
-                const float f = (mc == -__builtin_huge_valf()) ? 0.f : fast_exp2(mc - Mj);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  acc[4 * k] += f * x[k].x;
-                  acc[4 * k + 1] += f * x[k].y;
-                  acc[4 * k + 2] += f * x[k].z;
-                  acc[4 * k + 3] += f * x[k].w;
-                }
+            for (int i = 0; i < 4; ++i) {
+              rsv[i] = i < span ? s_rec[i] : -1;
+              f[i] = 0.f;
+              if (rsv[i] >= 0) {
+                const float mc = __ldcg(p.rec_ml + (static_cast<int64_t>(rsv[i]) * kHeads + h) * 2);
+                f[i] = (mc == -__builtin_huge_valf()) ? 0.f : fast_exp2(mc - M);
               }
             }
+            for (int hb = 0; hb < 32; hb += 4) {
+              float4 a[4][2];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] *= iLj;
-            const int64_t o = (static_cast<int64_t>(sg.seq) * kHeads + hj) * kDc + hf * kHalf + l16 * 16;
-            store_out_vec<8>(p.out, o, acc, p.out_dtype);
-            store_out_vec<8>(p.out, o + 8, acc + 8, p.out_dtype);
+              for (int k = 0; k < 4; ++k) a[k][0] = a[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if (rsv[i] < 0) continue;  // uniform: s_rec is shared
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const int hj = warp * 32 + hb + k;
+                  const float fk = __shfl_sync(0xffffffffu, f[i], hb + k);
+                  const float4* src =
+                      reinterpret_cast<const float4*>(p.rec_o + (static_cast<int64_t>(rsv[i]) * kHeads + hj) * kHalf);
+                  const float4 x0 = __ldcg(src + lane), x1 = __ldcg(src + 32 + lane);
+                  a[k][0].x += fk * x0.x;
+                  a[k][0].y += fk * x0.y;
+                  a[k][0].z += fk * x0.z;
+                  a[k][0].w += fk * x0.w;
+                  a[k][1].x += fk * x1.x;
+                  a[k][1].y += fk * x1.y;
+                  a[k][1].z += fk * x1.z;
+                  a[k][1].w += fk * x1.w;
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float iL = __shfl_sync(0xffffffffu, invL, hb + k);
+                const int64_t o = (static_cast<int64_t>(sg.seq) * kHeads + warp * 32 + hb + k) * kDc + hf * kHalf;
+                const float v0[4] = {a[k][0].x * iL, a[k][0].y * iL, a[k][0].z * iL, a[k][0].w * iL};
+                const float v1[4] = {a[k][1].x * iL, a[k][1].y * iL, a[k][1].z * iL, a[k][1].w * iL};
+                store_out_vec<4>(p.out, o + 4 * lane, v0, p.out_dtype);
+                store_out_vec<4>(p.out, o + 128 + 4 * lane, v1, p.out_dtype);
+              }
+            }
+          } else {
+            // Pass 2: thread h writes its own head's 256 outputs, 64 at a time;
+            // every record's 64-float run (256 contiguous bytes) is loaded
+            // before any is used, so one round trip serves all records.
+            for (int c = 0; c < kHalf; c += 64) {
+              float acc[64];
+#pragma unroll
+              for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+              for (int base = 0; base < span; base += kMergeChunk) {
+                const int nc = min(kMergeChunk, span - base);
+                if (span > kMergeChunk) list_records(base, nc);  // uniform over the warpgroup
+#pragma unroll 2
+                for (int i = 0; i < nc; ++i) {
+                  const int rs = s_rec[i];
+                  if (rs < 0) continue;
+                  const int64_t r = static_cast<int64_t>(rs) * kHeads + h;
+                  const float mc = __ldcg(p.rec_ml + r * 2);
+                  const float4* srcp = reinterpret_cast<const float4*>(p.rec_o + r * kHalf + c);
+                  float4 x[16];
+#pragma unroll
+                  for (int k = 0; k < 16; ++k) x[k] = __ldcg(srcp + k);
+                  const float f = (mc == -__builtin_huge_valf()) ? 0.f : fast_exp2(mc - M);
+#pragma unroll
+                  for (int k = 0; k < 16; ++k) {
+                    acc[4 * k] += f * x[k].x;
+                    acc[4 * k + 1] += f * x[k].y;
+                    acc[4 * k + 2] += f * x[k].z;
+                    acc[4 * k + 3] += f * x[k].w;
+                  }
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < 64; ++i) acc[i] *= invL;
+              const int64_t o = (static_cast<int64_t>(sg.seq) * kHeads + h) * kDc + hf * kHalf + c;
+#pragma unroll
+              for (int i = 0; i < 64; i += 8) store_out_vec<8>(p.out, o + i, acc + i, p.out_dtype);
+            }
           }
           if (tid == 0) p.counters[unit] = 0u;
         }
@@ -913,8 +1064,8 @@ kvc_status check(int batch, int n_q_heads, int d_c, int d_r, int block_size, int
   if (n_q_heads != kHeads || d_c != kDc || d_r != kW - kDc)
     return fail(KVC_ERR_UNSUPPORTED, "MLA decode supports n_q_heads 128, d_c 512, d_r 64 (got %d, %d, %d)",
                 n_q_heads, d_c, d_r);
-  if (block_size % kTile != 0 || block_size > 256)
-    return fail(KVC_ERR_UNSUPPORTED, "MLA block_size must be a multiple of 64 up to 256 (got %d)", block_size);
+  if (block_size % kBoxRows != 0 || block_size > 256)
+    return fail(KVC_ERR_UNSUPPORTED, "MLA block_size must be a multiple of 16 up to 256 (got %d)", block_size);
   if (batch > kMaxBatch) return fail(KVC_ERR_UNSUPPORTED, "MLA batch %d > %d", batch, kMaxBatch);
   return KVC_OK;
 }
@@ -981,9 +1132,12 @@ kvc_status kvc_decode_attention_mla(const void* q_absorbed, const void* latent_c
     if (r != CUDA_SUCCESS) return fail(KVC_ERR_CUDA, "tensor map for q_absorbed: CUresult %d", static_cast<int>(r));
   }
   {
+    // the latent pool as [num_blocks * block_size rows, 576] in boxes of 16
+    // rows x 64 columns (measured faster than 32- or 48-row boxes where a
+    // tile lies in one block: 248 against 276 us on the DeepSeek-V2 batch)
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mla::kW), static_cast<cuuint64_t>(num_blocks * block_size)};
     const cuuint64_t strides[1] = {mla::kW * 2ull};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(mla::kTile)};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(mla::kBoxRows)};
     const cuuint32_t es[2] = {1, 1};
     CUresult r = encode(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(latent_cache), dims, strides,
                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

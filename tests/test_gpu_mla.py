@@ -84,6 +84,18 @@ def test_mla_small(kvc, lens):
     assert kvc.get_error_flags() == 0
 
 
+@pytest.mark.parametrize("bs", [16, 32, 64, 256])
+def test_mla_tiles_across_block_boundaries(kvc, bs):
+    # 48-token tiles straddle cache blocks: lengths around tile and block edges, several block sizes
+    lens = [47, 48, 49, 95, 96, 97, 63, 64, 65, 127, 128, 129, 500]
+    case = W.mla_case(len(lens), H, D_C, D_R, bs, lens, "bf16", seed=51)
+    out, slots = run_mla(kvc, case)
+    ref = oracle_mla(case, slots)
+    err = float(np.max(np.abs(f64(out) - ref)))
+    assert err <= TOL, err
+    assert kvc.get_error_flags() == 0
+
+
 @pytest.mark.parametrize("blocks_per_cta", [1, 2, 5])
 def test_mla_forced_split(kvc, blocks_per_cta):
     kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, blocks_per_cta)
@@ -97,8 +109,8 @@ def test_mla_forced_split(kvc, blocks_per_cta):
 
 
 def test_mla_merge_of_more_than_64_records(kvc):
-    # one block per CTA pair: the 6400-row sequence is cut into 100 parts, so the merging warpgroup lists the
-    # record slots in two chunks (64 + 36); bf16 output takes the vector stores of the merge
+    # one block per CTA pair: the 6400-row sequence is cut into ~100 parts, so the merging warpgroup lists the
+    # record slots in several chunks; bf16 output takes the vector stores of the merge
     kvc.set_option(kvc.OPT_BLOCKS_PER_CTA, 1)
     lens = [6400, 300]
     case = W.mla_case(len(lens), H, D_C, D_R, 64, lens, "bf16", seed=49)
