@@ -34,6 +34,8 @@ SOURCES = [
     "decode_gqa_int8.cu",
     "decode_gqa_mma_bf16.cu",
     "decode_gqa_mma_f16.cu",
+    "decode_gqa_mma_fp8.cu",
+    "decode_gqa_mma_int8.cu",
     "decode_wide.cu",
     "decode_mla.cu",
     "pool.cpp",

@@ -147,6 +147,14 @@ template <typename T, bool EXT>
 kvc_status gqa_mma_dispatch(const GqaParams& p, int GH, int grid, size_t smem, const CUtensorMap& tk,
                             const CUtensorMap& tv, cudaStream_t stream, int mode, int* occ);
 
+// Warp-MMA kernel over one-byte caches (Q8 = 1: e4m3, 2: int8) with bf16
+// queries, head_dim 128; tk / tv: TMA maps over the code pools as
+// [num_blocks * n_kv_heads * block_size rows, 128 bytes] with
+// [hc * block_size x 128] boxes and the 128-byte swizzle.
+template <int Q8>
+kvc_status gqa_mma_dispatch_q8(const GqaParams& p, int GH, int grid, size_t smem, const CUtensorMap& tk,
+                               const CUtensorMap& tv, cudaStream_t stream, int mode, int* occ);
+
 // FP8 e4m3 caches with bf16 queries (head_dim 64, 128 or 256).
 kvc_status gqa_dispatch_fp8(const GqaParams& p, int D, int GH, int grid, size_t smem, cudaStream_t stream, int mode,
                             int* occ);

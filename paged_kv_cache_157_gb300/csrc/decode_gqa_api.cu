@@ -89,16 +89,18 @@ kvc_status make_plan(int batch, int n_q_heads, int n_kv_heads, int D, int bs, in
   return KVC_OK;
 }
 
-// Warp-MMA kernel: bf16/f16 caches, head_dim 128, block sizes that are
+// Warp-MMA kernel: bf16/f16 caches (q8 = 0) or one-byte caches with bf16
+// queries (q8 = 1: e4m3, 2: int8), head_dim 128, block sizes that are
 // multiples of 16 up to 128, and pool rows addressable by a TMA coordinate.
-bool mma_supported(kvc_dtype dtype, int head_dim, int block_size, int64_t num_blocks, int n_kv_heads, int qn) {
+bool mma_supported(kvc_dtype dtype, int head_dim, int block_size, int64_t num_blocks, int n_kv_heads, int qn,
+                   int q8 = 0) {
   const int64_t engine = option(KVC_OPT_GQA_ENGINE);
   if (engine == 1) return false;
   // One query per kv head (MHA): the CUDA-core kernel, whose two CTAs per SM
   // read blocks shared by forked sequences close enough in time to hit in L2
   // (measured on the 64-fork batch: 244 us against 348 us), unless forced.
   if (qn == 1 && engine != 3) return false;
-  if (dtype != KVC_BF16 && dtype != KVC_F16) return false;
+  if (dtype != KVC_BF16 && (dtype != KVC_F16 || q8 != 0)) return false;
   if (head_dim != 128 || block_size % 16 != 0 || block_size > 128) return false;
   return num_blocks * n_kv_heads * block_size < (1ll << 31);
 }
@@ -115,7 +117,7 @@ constexpr int kDefaultDynShare = KVC_MMA_DYN_SHARE;  // 256: static ranges only
 // block (each a [hc * block_size x 64] box pair, at most 256 rows per box)
 // and the unit's query rows.
 kvc_status make_plan_mma(int batch, int n_q_heads, int n_kv_heads, int bs, int q_elt, int max_smem, GqaPlan* pl,
-                         int n_tok = 1) {
+                         int n_tok = 1, bool q8 = false) {
   const int group = n_tok * (n_q_heads / n_kv_heads);
   pl->GH = head_subgroup(group);
   pl->n_hsub = group / pl->GH;
@@ -125,12 +127,12 @@ kvc_status make_plan_mma(int batch, int n_q_heads, int n_kv_heads, int bs, int q
   int S = 0;
   for (;;) {
     S = 8;
-    while (S > 1 && gqa_mma_smem_layout(q_elt, pl->GH, bs, hc, S, batch).total > static_cast<size_t>(share)) --S;
+    while (S > 1 && gqa_mma_smem_layout(q_elt, pl->GH, bs, hc, S, batch, q8).total > static_cast<size_t>(share)) --S;
     if (S >= 3 || hc == 1) break;
     hc /= 2;  // keep at least three stages in flight
   }
-  while (S > 1 && gqa_mma_smem_layout(q_elt, pl->GH, bs, hc, S, batch).total > static_cast<size_t>(max_smem)) --S;
-  const GqaMmaSmem L = gqa_mma_smem_layout(q_elt, pl->GH, bs, hc, S, batch);
+  while (S > 1 && gqa_mma_smem_layout(q_elt, pl->GH, bs, hc, S, batch, q8).total > static_cast<size_t>(max_smem)) --S;
+  const GqaMmaSmem L = gqa_mma_smem_layout(q_elt, pl->GH, bs, hc, S, batch, q8);
   if (L.total > static_cast<size_t>(max_smem))
     return fail(KVC_ERR_UNSUPPORTED, "block_size %d needs %zu bytes of shared memory (max %d)", bs, L.total, max_smem);
   pl->hc = hc;
@@ -190,15 +192,18 @@ EncodeTiledFn encode_tiled_fn() {
 }
 
 // TMA maps over the K and V pools as [num_blocks * n_kv_heads * block_size
-// rows, 128] with [rows_per_box x 64] boxes and the 128-byte swizzle.
+// rows, 128] with the 128-byte swizzle: 16-bit elements in [rows_per_box x 64]
+// boxes, or (one_byte) codes in [rows_per_box x 128] boxes.
 kvc_status pool_maps(const void* k_cache, const void* v_cache, int64_t num_blocks, int n_kv_heads, int block_size,
-                     int rows_per_box, kvc_dtype dtype, CUtensorMap* tk, CUtensorMap* tv) {
+                     int rows_per_box, kvc_dtype dtype, CUtensorMap* tk, CUtensorMap* tv, bool one_byte = false) {
   EncodeTiledFn encode = encode_tiled_fn();
   if (encode == nullptr) return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  const CUtensorMapDataType dt = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = one_byte            ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(num_blocks * n_kv_heads * block_size)};
-  const cuuint64_t strides[1] = {256};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(rows_per_box)};
+  const cuuint64_t strides[1] = {one_byte ? 128u : 256u};
+  const cuuint32_t box[2] = {one_byte ? 128u : 64u, static_cast<cuuint32_t>(rows_per_box)};
   const cuuint32_t es[2] = {1, 1};
   for (int i = 0; i < 2; ++i) {
     CUresult r = encode(i == 0 ? tk : tv, dt, 2, const_cast<void*>(i == 0 ? k_cache : v_cache), dims, strides, box, es,
@@ -378,7 +383,11 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   // tcgen05 kernel for 17 to 32 (where the warp-MMA kernel would read the
   // pages once per 16 queries), the CUDA-core kernel for the rest.
   const int qn = n_tok * (n_q_heads / n_kv_heads);
-  const bool use_mma = !fp8 && mma_supported(dtype, head_dim, block_size, num_blocks, n_kv_heads, qn);
+  // one-byte caches: the warp-MMA kernel for single-token full attention
+  const int q8 = fp8 ? (ex->int8 ? 2 : 1) : 0;
+  const bool use_mma =
+      (!fp8 || (window == 0 && n_tok == 1 && ex->row_div == 0 && ex->lse == nullptr)) &&
+      mma_supported(dtype, head_dim, block_size, num_blocks, n_kv_heads, qn, q8);
   const bool force_wide = option(KVC_OPT_GQA_ENGINE) == 2;
   if (!fp8 && window == 0 && ex->row_div == 0 && (force_wide || !use_mma || qn > 16) &&
       wide_preferred(batch, n_q_heads, n_kv_heads, head_dim, block_size, max_blocks_per_seq, n_tok, dtype)) {
@@ -410,8 +419,8 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   const int elt = fp8 ? 1 : q_elt;
   GqaPlan pl;
   if (use_mma) {
-    if ((s = make_plan_mma(batch, n_q_heads, n_kv_heads, block_size, q_elt, dev->max_smem_optin, &pl, n_tok)) !=
-        KVC_OK)
+    if ((s = make_plan_mma(batch, n_q_heads, n_kv_heads, block_size, q_elt, dev->max_smem_optin, &pl, n_tok,
+                           q8 != 0)) != KVC_OK)
       return s;
   } else if ((s = make_plan(batch, n_q_heads, n_kv_heads, head_dim, block_size, elt, q_elt, fp8 ? 4 : 0,
                             dev->max_smem_optin, &pl, n_tok)) != KVC_OK) {
@@ -453,10 +462,12 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   CUtensorMap tk, tv;
   const bool ext = uses_ext(p);
   if (use_mma) {
-    if ((s = pool_maps(k_cache, v_cache, num_blocks, n_kv_heads, block_size, pl.hc * block_size, dtype, &tk, &tv)) !=
-        KVC_OK)
+    if ((s = pool_maps(k_cache, v_cache, num_blocks, n_kv_heads, block_size, pl.hc * block_size, dtype, &tk, &tv,
+                       q8 != 0)) != KVC_OK)
       return s;
-    s = dtype == KVC_BF16 ? (ext ? gqa_mma_dispatch<__nv_bfloat16, true>(p, pl.GH, 0, pl.smem, tk, tv, nullptr, 1, &occ)
+    s = q8 == 1 ? gqa_mma_dispatch_q8<1>(p, pl.GH, 0, pl.smem, tk, tv, nullptr, 1, &occ)
+        : q8 == 2 ? gqa_mma_dispatch_q8<2>(p, pl.GH, 0, pl.smem, tk, tv, nullptr, 1, &occ)
+        : dtype == KVC_BF16 ? (ext ? gqa_mma_dispatch<__nv_bfloat16, true>(p, pl.GH, 0, pl.smem, tk, tv, nullptr, 1, &occ)
                                  : gqa_mma_dispatch<__nv_bfloat16, false>(p, pl.GH, 0, pl.smem, tk, tv, nullptr, 1, &occ))
                           : (ext ? gqa_mma_dispatch<__half, true>(p, pl.GH, 0, pl.smem, tk, tv, nullptr, 1, &occ)
                                  : gqa_mma_dispatch<__half, false>(p, pl.GH, 0, pl.smem, tk, tv, nullptr, 1, &occ));
@@ -508,7 +519,9 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
     return fail(KVC_ERR_UNSUPPORTED, "num_blocks x n_kv_heads must be below 2^31");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (use_mma) {
-    s = dtype == KVC_BF16 ? (ext ? gqa_mma_dispatch<__nv_bfloat16, true>(p, pl.GH, grid, pl.smem, tk, tv, st, 0, nullptr)
+    s = q8 == 1 ? gqa_mma_dispatch_q8<1>(p, pl.GH, grid, pl.smem, tk, tv, st, 0, nullptr)
+        : q8 == 2 ? gqa_mma_dispatch_q8<2>(p, pl.GH, grid, pl.smem, tk, tv, st, 0, nullptr)
+        : dtype == KVC_BF16 ? (ext ? gqa_mma_dispatch<__nv_bfloat16, true>(p, pl.GH, grid, pl.smem, tk, tv, st, 0, nullptr)
                                  : gqa_mma_dispatch<__nv_bfloat16, false>(p, pl.GH, grid, pl.smem, tk, tv, st, 0, nullptr))
                           : (ext ? gqa_mma_dispatch<__half, true>(p, pl.GH, grid, pl.smem, tk, tv, st, 0, nullptr)
                                  : gqa_mma_dispatch<__half, false>(p, pl.GH, grid, pl.smem, tk, tv, st, 0, nullptr));

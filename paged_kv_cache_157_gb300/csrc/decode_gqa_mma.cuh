@@ -30,6 +30,13 @@
 // 64 dims] boxes with the 128-byte swizzle, so every 8x8 matrix load touches
 // eight different bank groups. Work split, split-K records, the last-arriver
 // merge and the bounded waits are those of the CUDA-core kernel.
+//
+// One-byte caches (e4m3 or int8 codes with per-channel K scales and per-token
+// V scales, bf16 queries) use the same loop on f16 MMAs: every code is an f16
+// value, so each lane converts the codes it needs straight into its MMA
+// fragments (one conversion per pair of codes, no staging copy). The K scales
+// are folded into the query (q * k_scale split into f16 hi + lo), the V
+// scales into the weights; see mma_tile_q8.
 #pragma once
 
 #include <cuda.h>
@@ -118,6 +125,34 @@ __device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* map, int 
       "{%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int j) {
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+// The four one-byte codes of w as two f16 pairs: bytes 0, 1 into lo (byte 0
+// in its low half), bytes 2, 3 into hi. Q8 = 1: e4m3 codes (hardware
+// conversion, exact); Q8 = 2: int8 codes c, placed as c + 128 in the low
+// mantissa byte of the f16 1024 (1024 + c + 128, exact) minus 1152.
+template <int Q8>
+__device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (Q8 == 1) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+  } else {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140u), b = __byte_perm(u, 0x64646464u, 0x4342u);
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+  }
 }
 
 }  // namespace wmma16
@@ -252,6 +287,197 @@ __device__ __forceinline__ void mma_tile(uint32_t kb, uint32_t vb, uint32_t box_
   }
 }
 
+// Per-warp state of a segment over a one-byte cache. As MmaWarpState, but the
+// query is q * k_scale * 2^t in f16 hi + lo parts (t per segment and warp,
+// so that the largest entry lies in [2^14, 2^15)), and the output dims of
+// lane 4g + c in tile i are 16g + 2i (o[i][0], o[i][1]) and 16g + 2i + 1
+// (o[i][2], o[i][3]).
+struct Q8WarpState {
+  uint32_t qh[8][2];  // B fragments per k-step: query g, dims 32c + 4ks + {0, 1} and + {2, 3}
+  uint32_t ql[8][2];
+  float o[8][4];
+  float m[2];
+  float l[2];
+  float f;  // the weights' factor (a power of two); 0 before the segment's first tile
+};
+
+// One 16-row tile of one kv head over a one-byte cache. kb / vb: the stage's
+// K / V code boxes (128 codes per 128-byte row, 1024-byte aligned, 128-byte
+// swizzle: 16-byte chunk q of row r at r * 128 + ((q ^ (r & 7)) << 4)); row0:
+// the tile's first row (a multiple of 16); vsp: the V scales of the box's rows.
+//
+// The order of the dims inside a product is free (Q uses the same order), so
+// each lane takes whole 16-byte chunks: for S, lane 4g + c reads dims 32c ..
+// 32c + 31 of rows g and g + 8 and k-step ks uses its bytes 4ks .. 4ks + 3
+// (the MMA's k-columns 2c, 2c + 1 and 2c + 8, 2c + 9); for PV, it reads dims
+// 16g .. 16g + 15 of rows 2c, 2c + 1, 2c + 8, 2c + 9, and a byte permute
+// pairs rows 2c and 2c + 1 (and 2c + 8, 2c + 9) of one dim, the A fragment
+// V^T wants, so output tile i holds dims 16g + 2i and 16g + 2i + 1. All
+// loads of a quarter warp hit eight different bank groups.
+//
+// Weights: p * v_scale * f with f a power of two that keeps every weight
+// below 2^15, an f16 value: the lazily rescaled p reaches 2^8, so f puts the
+// largest scale of the segment's first tile in [2^6, 2^7) and drops (with a
+// rescale of O) when a later tile's largest scale reaches 2^7 / f; the sum l
+// takes the unscaled p, the segment's end divides O by f.
+template <int Q8, int GW, bool PARTIAL>
+__device__ __forceinline__ void mma_tile_q8(uint32_t kb, uint32_t vb, int row0, const float* vsp, int lo_valid,
+                                            int valid, int vis0, int vis1, float qscale, Q8WarpState& st, int lane) {
+  using namespace wmma16;
+  const int g = lane >> 2, c = lane & 3;
+  // ---- S^T = K . Q^T (hi and lo parts of Q, two accumulator chains each)
+  uint32_t kw[2][8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t row = kb + static_cast<uint32_t>((row0 + g + 8 * h) * 128);
+    const uint4 u0 = lds128(row + static_cast<uint32_t>(((2 * c) ^ g) << 4));
+    const uint4 u1 = lds128(row + static_cast<uint32_t>(((2 * c + 1) ^ g) << 4));
+    kw[h][0] = u0.x;
+    kw[h][1] = u0.y;
+    kw[h][2] = u0.z;
+    kw[h][3] = u0.w;
+    kw[h][4] = u1.x;
+    kw[h][5] = u1.y;
+    kw[h][6] = u1.z;
+    kw[h][7] = u1.w;
+  }
+  // the V codes: rows 2c, 2c + 1, 2c + 8, 2c + 9, dims 16g .. 16g + 15 (read
+  // before the scores where registers allow, to hide the load latency)
+  constexpr bool kEarlyV = GW <= 4;
+  uint4 vr[4];
+  auto load_v = [&]() {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = row0 + 2 * c + (j & 1) + 8 * (j >> 1);
+      vr[j] = lds128(vb + static_cast<uint32_t>(r * 128) + static_cast<uint32_t>((g ^ (r & 7)) << 4));
+    }
+  };
+  if constexpr (kEarlyV) load_v();
+  float sc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[j][e] = 0.f;
+  }
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    uint32_t a[4];
+    codes_to_f16x2<Q8>(kw[0][ks], a[0], a[2]);
+    codes_to_f16x2<Q8>(kw[1][ks], a[1], a[3]);
+    mma<false>(sc[ks & 1], a, st.qh[ks][0], st.qh[ks][1]);
+    mma<false>(sc[2 + (ks & 1)], a, st.ql[ks][0], st.ql[ks][1]);
+  }
+  if constexpr (!kEarlyV) load_v();
+  float x[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) x[e] = ((sc[0][e] + sc[1][e]) + (sc[2][e] + sc[3][e])) * qscale;
+  const bool q0 = 2 * c < GW, q1 = 2 * c + 1 < GW;
+  if (!q0) {
+    x[0] = kNegInf;
+    x[2] = kNegInf;
+  }
+  if (!q1) {
+    x[1] = kNegInf;
+    x[3] = kNegInf;
+  }
+  float vs0, vs1;
+  if (PARTIAL) {
+    const bool ra = g >= lo_valid && g < valid, rb = g + 8 >= lo_valid && g + 8 < valid;
+    if (!ra || g >= vis0) x[0] = kNegInf;
+    if (!ra || g >= vis1) x[1] = kNegInf;
+    if (!rb || g + 8 >= vis0) x[2] = kNegInf;
+    if (!rb || g + 8 >= vis1) x[3] = kNegInf;
+    // rows outside the range may hold anything: their scale is not used
+    vs0 = ra ? vsp[row0 + g] : 0.f;
+    vs1 = rb ? vsp[row0 + g + 8] : 0.f;
+  } else {
+    vs0 = vsp[row0 + g];
+    vs1 = vsp[row0 + g + 8];
+  }
+  // ---- the weights' factor
+  {
+    float vmax = fmaxf(vs0, vs1);
+#pragma unroll
+    for (int msk = 4; msk < 32; msk <<= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, msk));
+    if (st.f == 0.f || vmax * st.f >= 128.f) {
+      // 2^(133 - E) for vmax in [2^(E - 127), 2^(E - 126)): vmax * f in [2^6, 2^7)
+      const int e = static_cast<int>((__float_as_uint(vmax) >> 23) & 0xffu);
+      const int field = min(254, max(1, 260 - e));
+      const float nf = __uint_as_float(static_cast<uint32_t>(field) << 23);
+      if (st.f != 0.f) {
+        const float r = nf / st.f;  // both powers of two: exact
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) st.o[i][k] *= r;
+        }
+      }
+      st.f = nf;
+    }
+  }
+  // ---- online softmax (lazy rescale)
+  const bool need = x[0] > st.m[0] + 8.0f || x[2] > st.m[0] + 8.0f || x[1] > st.m[1] + 8.0f || x[3] > st.m[1] + 8.0f;
+  if (__any_sync(0xffffffffu, need)) {
+    float t0 = fmaxf(x[0], x[2]), t1 = fmaxf(x[1], x[3]);
+#pragma unroll
+    for (int msk = 4; msk < 32; msk <<= 1) {
+      t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, msk));
+      t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, msk));
+    }
+    const float n0 = fmaxf(st.m[0], t0), n1 = fmaxf(st.m[1], t1);
+    const float a0 = fast_exp2(st.m[0] - n0), a1 = fast_exp2(st.m[1] - n1);
+    const float2 a2 = make_float2(a0, a1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 u = fmul2(make_float2(st.o[i][0], st.o[i][1]), a2);
+      const float2 v = fmul2(make_float2(st.o[i][2], st.o[i][3]), a2);
+      st.o[i][0] = u.x;
+      st.o[i][1] = u.y;
+      st.o[i][2] = v.x;
+      st.o[i][3] = v.y;
+    }
+    st.l[0] *= a0;
+    st.l[1] *= a1;
+    st.m[0] = n0;
+    st.m[1] = n1;
+  }
+  const float p0 = fast_exp2(x[0] - st.m[0]), p1 = fast_exp2(x[1] - st.m[1]);
+  const float p2 = fast_exp2(x[2] - st.m[0]), p3 = fast_exp2(x[3] - st.m[1]);
+  st.l[0] += p0 + p2;
+  st.l[1] += p1 + p3;
+  const float w0 = vs0 * st.f, w1 = vs1 * st.f;
+  const float r0 = p0 * w0, r1 = p1 * w0, r2 = p2 * w1, r3 = p3 * w1;
+  const uint32_t h01 = pack2<false>(r0, r1), h23 = pack2<false>(r2, r3);
+  const float2 f01 = unpack2<false>(h01), f23 = unpack2<false>(h23);
+  const uint32_t l01 = pack2<false>(r0 - f01.x, r1 - f01.y), l23 = pack2<false>(r2 - f23.x, r3 - f23.y);
+  const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23), bl0 = movm_t(l01), bl1 = movm_t(l23);
+  // ---- O^T += V^T . P^T
+  uint32_t keep01 = 0xffffffffu, keep89 = 0xffffffffu;
+  if (PARTIAL) {
+    const int ra = 2 * c, rb = 2 * c + 8;
+    keep01 = ((ra >= lo_valid && ra < valid) ? 0x0000ffffu : 0u) | ((ra + 1 >= lo_valid && ra + 1 < valid) ? 0xffff0000u : 0u);
+    keep89 = ((rb >= lo_valid && rb < valid) ? 0x0000ffffu : 0u) | ((rb + 1 >= lo_valid && rb + 1 < valid) ? 0xffff0000u : 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    // bytes 2 (i & 1) and 2 (i & 1) + 1 of word i >> 1: dims 16g + 2i, + 1; rows interleaved
+    const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+    const uint32_t e01 = __byte_perm(word(vr[0], i >> 1), word(vr[1], i >> 1), sel);
+    const uint32_t e89 = __byte_perm(word(vr[2], i >> 1), word(vr[3], i >> 1), sel);
+    uint32_t a[4];
+    codes_to_f16x2<Q8>(e01, a[0], a[1]);
+    codes_to_f16x2<Q8>(e89, a[2], a[3]);
+    if (PARTIAL) {
+      a[0] &= keep01;
+      a[1] &= keep01;
+      a[2] &= keep89;
+      a[3] &= keep89;
+    }
+    mma<false>(st.o[i], a, bh0, bh1);
+    mma<false>(st.o[i], a, bl0, bl1);
+  }
+}
+
 // ------------------------------------------------------------------ work split
 //
 // The blocks of all units are laid end to end (sequence major, then kv-head
@@ -317,15 +543,19 @@ __device__ __forceinline__ WorkSplit make_split(int64_t N, int64_t G, int dyn_sh
 constexpr int kMmaPending = 32;  // deferred merge checks per consumer warp
 
 struct GqaMmaSmem {
-  size_t box_bytes, stage_bytes, q_off, meta_off, full_off, empty_off, iss_off, misc_off, pend_off, scan_off, total;
+  size_t box_bytes, stage_bytes, q_off, vs_off, meta_off, full_off, empty_off, iss_off, misc_off, pend_off, scan_off,
+      total;
 };
 
+// q8: one-byte caches, whose stage holds one K and one V box (128 codes per
+// row) and, after the query rows, the block's V scales [hc * block_size].
 __host__ __device__ inline GqaMmaSmem gqa_mma_smem_layout(int q_elt, int GH, int block_size, int hc, int stages,
-                                                          int batch) {
+                                                          int batch, bool q8 = false) {
   GqaMmaSmem s;
   s.box_bytes = static_cast<size_t>(hc) * block_size * 128;
-  s.q_off = 4 * s.box_bytes;
-  s.stage_bytes = align_up(s.q_off + static_cast<size_t>(hc) * GH * 128 * q_elt, 1024);
+  s.q_off = (q8 ? 2 : 4) * s.box_bytes;
+  s.vs_off = s.q_off + static_cast<size_t>(hc) * GH * 128 * q_elt;
+  s.stage_bytes = align_up(s.vs_off + (q8 ? static_cast<size_t>(hc) * block_size * 4 : 0), 1024);
   s.meta_off = static_cast<size_t>(stages) * s.stage_bytes;
   s.full_off = s.meta_off + static_cast<size_t>(stages) * 64;
   s.empty_off = s.full_off + static_cast<size_t>(stages) * 8;
@@ -439,13 +669,16 @@ __device__ __noinline__ void merge_unit_mma(const GqaParams& p, const WorkSplit&
   }
 }
 
-template <typename T, int GH, bool EXT>
+// Q8 = 0: T is the cache and query type; Q8 = 1 (e4m3) or 2 (int8): one-byte
+// caches with T (bf16) queries.
+template <typename T, int GH, bool EXT, int Q8 = 0>
 __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
     gqa_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const GqaParams p) {
   using namespace wmma16;
   constexpr int D = 128;
-  constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+  constexpr bool BF = Q8 == 0 && std::is_same<T, __nv_bfloat16>::value;
+  static_assert(Q8 == 0 || (!EXT && std::is_same<T, __nv_bfloat16>::value), "one-byte caches: bf16 queries");
   constexpr int HW = mma_warps_per_kvhead(GH);  // warps per kv head
   constexpr int GW = GH / HW;                   // query heads per warp (MMA columns)
   constexpr int HCM = kMmaWarps / HW;           // kv heads per CTA at most
@@ -465,7 +698,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
   const int32_t* row_start = EXT ? p.row_start : nullptr;
   const int row_div = EXT ? p.row_div : 0;
   const int bs = p.block_size, S = p.stages;
-  const GqaMmaSmem L = gqa_mma_smem_layout(sizeof(T), GH, bs, hc, S, p.batch);
+  const GqaMmaSmem L = gqa_mma_smem_layout(sizeof(T), GH, bs, hc, S, p.batch, Q8 != 0);
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta_off);
   uint64_t* fbar = reinterpret_cast<uint64_t*>(smem + L.full_off);
   uint64_t* ebar = reinterpret_cast<uint64_t*>(smem + L.empty_off);
@@ -571,6 +804,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
     const uint64_t pol = policy_evict_first();
     const uint32_t box_bytes = static_cast<uint32_t>(L.box_bytes);
     const uint32_t q_bytes = static_cast<uint32_t>(hc * GH * D * sizeof(T));
+    const uint32_t vs_bytes = static_cast<uint32_t>(hc * bs * 4);
     const bool q_contig = (GH == p.group);
     unsigned int claim = 0;
     if (!p.unit_mode && ws.K > 0 && lane == 0) claim = atomicAdd(p.sched, 1u);  // for after the static range
@@ -625,7 +859,8 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
             if (ok) {
               if (srci < 0) set_flag(p.err, 0x1u);
               meta[slot] = mi;
-              const uint32_t bytes = (srci >= 0 ? 4 * box_bytes : 0u) + (qo >= 0 ? q_bytes : 0u);
+              const uint32_t bytes = (srci >= 0 ? (Q8 ? 2 * box_bytes + vs_bytes : 4 * box_bytes) : 0u) +
+                                     (qo >= 0 ? q_bytes : 0u);
               s_iss[slot] += 1u;
               if (bytes == 0) {
                 mbar_arrive(fbar + slot);
@@ -634,10 +869,16 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
                 const uint32_t bar = smem_addr(fbar + slot);
                 mbar_arrive_expect_tx(fbar + slot, bytes);
                 if (srci >= 0) {
-                  tma2d(dst, &tm_k, 0, srci, bar, pol);
-                  tma2d(dst + box_bytes, &tm_k, 64, srci, bar, pol);
-                  tma2d(dst + 2 * box_bytes, &tm_v, 0, srci, bar, pol);
-                  tma2d(dst + 3 * box_bytes, &tm_v, 64, srci, bar, pol);
+                  if constexpr (Q8 != 0) {
+                    tma2d(dst, &tm_k, 0, srci, bar, pol);
+                    tma2d(dst + box_bytes, &tm_v, 0, srci, bar, pol);
+                    bulk_g2s(smem + slot * L.stage_bytes + L.vs_off, p.v_scale + srci, vs_bytes, fbar + slot, pol);
+                  } else {
+                    tma2d(dst, &tm_k, 0, srci, bar, pol);
+                    tma2d(dst + box_bytes, &tm_k, 64, srci, bar, pol);
+                    tma2d(dst + 2 * box_bytes, &tm_v, 0, srci, bar, pol);
+                    tma2d(dst + 3 * box_bytes, &tm_v, 64, srci, bar, pol);
+                  }
                 }
                 if (qo >= 0) {
                   unsigned char* qdst = smem + slot * L.stage_bytes + L.q_off;
@@ -756,20 +997,66 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
       // rows at the end each of the lane's two query columns may not see
       const int dh0 = (EXT && causal) ? tm - (v0 + 2 * c4) / p.group : 0;
       const int dh1 = (EXT && causal) ? tm - (v0 + 2 * c4 + 1) / p.group : 0;
-      MmaWarpState st;
+      std::conditional_t<Q8 != 0, Q8WarpState, MmaWarpState> st;
+      float qsc = p.qscale;
       {
         const unsigned char* qs = smem + slot * L.stage_bytes + L.q_off +
                                   static_cast<size_t>(kh * GH + hw * GW) * D * sizeof(T);
+        if constexpr (Q8 == 0) {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          if (g8 < GW) {
-            const uint32_t* qr = reinterpret_cast<const uint32_t*>(qs + (g8 * D + 16 * ks + 2 * c4) * sizeof(T));
-            st.qb[ks][0] = qr[0];
-            st.qb[ks][1] = qr[4];
-          } else {
-            st.qb[ks][0] = 0u;
-            st.qb[ks][1] = 0u;
+          for (int ks = 0; ks < 8; ++ks) {
+            if (g8 < GW) {
+              const uint32_t* qr = reinterpret_cast<const uint32_t*>(qs + (g8 * D + 16 * ks + 2 * c4) * sizeof(T));
+              st.qb[ks][0] = qr[0];
+              st.qb[ks][1] = qr[4];
+            } else {
+              st.qb[ks][0] = 0u;
+              st.qb[ks][1] = 0u;
+            }
           }
+        } else {
+          // q * k_scale over dims 32c .. 32c + 31 of query g, scaled by 2^t
+          // so that the warp's largest entry lies in [2^14, 2^15), as f16 hi + lo
+          float y[32];
+          if (g8 < GW) {
+            const uint4* qv = reinterpret_cast<const uint4*>(qs + (g8 * D + 32 * c4) * 2);
+            const float4* kv = reinterpret_cast<const float4*>(p.k_scale + static_cast<int64_t>(kvh) * D + 32 * c4);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 u = qv[j];
+              const float4 s0 = __ldg(kv + 2 * j), s1 = __ldg(kv + 2 * j + 1);
+              const uint32_t wq[4] = {u.x, u.y, u.z, u.w};
+              const float sk[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const uint32_t wv = wq[e >> 1];
+                y[8 * j + e] = __uint_as_float((e & 1) ? (wv & 0xffff0000u) : (wv << 16)) * sk[e];
+              }
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) y[e] = 0.f;
+          }
+          float amax = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(y[e]));
+#pragma unroll
+          for (int msk = 1; msk < 32; msk <<= 1) amax = fmaxf(amax, __shfl_xor_sync(full, amax, msk));
+          const int field = min(254, max(1, 268 - static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu)));
+          const float fq = __uint_as_float(static_cast<uint32_t>(field) << 23);
+          qsc = p.qscale * __uint_as_float(static_cast<uint32_t>(254 - field) << 23);  // / 2^t, exact
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float z0 = y[4 * ks + 2 * h] * fq, z1 = y[4 * ks + 2 * h + 1] * fq;
+              const uint32_t hi = pack2<false>(z0, z1);
+              const float2 fh = unpack2<false>(hi);
+              st.qh[ks][h] = hi;
+              st.ql[ks][h] = pack2<false>(z0 - fh.x, z1 - fh.y);
+            }
+          }
+          st.f = 0.f;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -782,7 +1069,18 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
       for (;;) {
         if (m.flags & kSrc) {
           const uint32_t stg = base + static_cast<uint32_t>(slot * L.stage_bytes);
-          const uint32_t kb = stg, vb = stg + 2 * box_bytes;
+          const float* vsp = reinterpret_cast<const float*>(smem + slot * L.stage_bytes + L.vs_off);
+          // one tile (PT: partial) on the kernel's cache type
+          auto tile = [&](auto pt, int row0, int lo_valid, int valid, int vis0, int vis1) {
+            constexpr bool PT = decltype(pt)::value;
+            if constexpr (Q8 == 0)
+              mma_tile<BF, GW, PT>(stg, stg + 2 * box_bytes, box_bytes, row0, lo_valid, valid, vis0, vis1, qsc, st,
+                                   lane);
+            else
+              mma_tile_q8<Q8, GW, PT>(stg, stg + box_bytes, row0, vsp, lo_valid, valid, vis0, vis1, qsc, st, lane);
+          };
+          using Full = std::integral_constant<bool, false>;
+          using Part = std::integral_constant<bool, true>;
           const int j0 = m.r0 / bs;
           const int rb = m.n_rows - m.jb * bs;  // rows from the block's first to the end
           const int vr = min(bs, rb);
@@ -790,8 +1088,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
           const int rowk = kh * bs;
           const int tiles = bs / 16;
           if (rb - tm >= bs && lr == 0) {
-            for (int tt = 0; tt < tiles; ++tt)
-              mma_tile<BF, GW, false>(kb, vb, box_bytes, rowk + tt * 16, 0, 16, 16, 16, p.qscale, st, lane);
+            for (int tt = 0; tt < tiles; ++tt) tile(Full{}, rowk + tt * 16, 0, 16, 16, 16);
           } else {
             for (int tt = 0; tt < tiles; ++tt) {
               const int valid = vr - tt * 16, lo_valid = lr - tt * 16;
@@ -799,11 +1096,10 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
               if (valid <= 0) break;
               if (lo_valid >= 16) continue;
               if (rt - tm >= 16 && lo_valid <= 0)
-                mma_tile<BF, GW, false>(kb, vb, box_bytes, rowk + tt * 16, 0, 16, 16, 16, p.qscale, st, lane);
+                tile(Full{}, rowk + tt * 16, 0, 16, 16, 16);
               else
-                mma_tile<BF, GW, true>(kb, vb, box_bytes, rowk + tt * 16, lo_valid, valid,
-                                       EXT ? min(valid, rt - dh0) : valid, EXT ? min(valid, rt - dh1) : valid,
-                                       p.qscale, st, lane);
+                tile(Part{}, rowk + tt * 16, lo_valid, valid, EXT ? min(valid, rt - dh0) : valid,
+                     EXT ? min(valid, rt - dh1) : valid);
             }
           }
         }
@@ -831,21 +1127,26 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
         lw1 += __shfl_xor_sync(full, lw1, msk);
       }
       const bool qv0 = 2 * c4 < GW, qv1 = 2 * c4 + 1 < GW;
+      // output dims of o[i][0..1] and o[i][2..3], and the one-byte path's weight factor
+      float fo = 1.f;
+      if constexpr (Q8 != 0) fo = st.f > 0.f ? 1.0f / st.f : 0.f;
+      auto dim_a = [&](int i) { return Q8 != 0 ? 16 * g8 + 2 * i : 16 * i + g8; };
+      constexpr int kDimB = Q8 != 0 ? 1 : 8;
       if (m.flags & kWhole) {
-        const float i0 = 1.0f / lw0, i1 = 1.0f / lw1;
+        const float i0 = fo / lw0, i1 = fo / lw1;
         const int64_t ob0 = (EXT ? out_row(p, m.seq, kvh, v0 + 2 * c4)
                                  : static_cast<int64_t>(m.seq) * p.n_q_heads + kvh * p.group + v0 + 2 * c4) * D;
         const int64_t ob1 = EXT ? out_row(p, m.seq, kvh, v0 + 2 * c4 + 1) * D : ob0 + D;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int d0 = 16 * i + g8;
+          const int d0 = dim_a(i);
           if (qv0) {
             store_out(p.out, ob0 + d0, st.o[i][0] * i0, p.out_dtype);
-            store_out(p.out, ob0 + d0 + 8, st.o[i][2] * i0, p.out_dtype);
+            store_out(p.out, ob0 + d0 + kDimB, st.o[i][2] * i0, p.out_dtype);
           }
           if (qv1) {
             store_out(p.out, ob1 + d0, st.o[i][1] * i1, p.out_dtype);
-            store_out(p.out, ob1 + d0 + 8, st.o[i][3] * i1, p.out_dtype);
+            store_out(p.out, ob1 + d0 + kDimB, st.o[i][3] * i1, p.out_dtype);
           }
         }
         if (EXT && p.lse != nullptr && g8 == 0) {
@@ -860,14 +1161,14 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
         float* ro1 = ro0 + D;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int d0 = 16 * i + g8;
+          const int d0 = dim_a(i);
           if (qv0) {
-            ro0[d0] = st.o[i][0];
-            ro0[d0 + 8] = st.o[i][2];
+            ro0[d0] = st.o[i][0] * fo;
+            ro0[d0 + kDimB] = st.o[i][2] * fo;
           }
           if (qv1) {
-            ro1[d0] = st.o[i][1];
-            ro1[d0 + 8] = st.o[i][3];
+            ro1[d0] = st.o[i][1] * fo;
+            ro1[d0 + kDimB] = st.o[i][3] * fo;
           }
         }
         if (g8 == 0) {

@@ -8,10 +8,10 @@
 namespace kvc {
 
 // mode 0: launch; mode 1: only report the occupancy (CTAs per SM) in *occ.
-template <typename T, int GH, bool EXT>
+template <typename T, int GH, bool EXT, int Q8 = 0>
 static kvc_status gqa_mma_run(const GqaParams& p, int grid, size_t smem, const CUtensorMap& tk, const CUtensorMap& tv,
                               cudaStream_t stream, int mode, int* occ) {
-  auto* k = gqa_mma_kernel<T, GH, EXT>;
+  auto* k = gqa_mma_kernel<T, GH, EXT, Q8>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gqa mma)");
   if (mode == 1) {
@@ -45,6 +45,20 @@ kvc_status gqa_mma_dispatch(const GqaParams& p, int GH, int grid, size_t smem, c
     case 4: return gqa_mma_run<T, 4, EXT>(p, grid, smem, tk, tv, stream, mode, occ);
     case 8: return gqa_mma_run<T, 8, EXT>(p, grid, smem, tk, tv, stream, mode, occ);
     case 16: return gqa_mma_run<T, 16, EXT>(p, grid, smem, tk, tv, stream, mode, occ);
+  }
+  return fail(KVC_ERR_UNSUPPORTED, "head subgroup %d", GH);
+}
+
+template <int Q8>
+kvc_status gqa_mma_dispatch_q8(const GqaParams& p, int GH, int grid, size_t smem, const CUtensorMap& tk,
+                               const CUtensorMap& tv, cudaStream_t stream, int mode, int* occ) {
+  using B = __nv_bfloat16;
+  switch (GH) {
+    case 1: return gqa_mma_run<B, 1, false, Q8>(p, grid, smem, tk, tv, stream, mode, occ);
+    case 2: return gqa_mma_run<B, 2, false, Q8>(p, grid, smem, tk, tv, stream, mode, occ);
+    case 4: return gqa_mma_run<B, 4, false, Q8>(p, grid, smem, tk, tv, stream, mode, occ);
+    case 8: return gqa_mma_run<B, 8, false, Q8>(p, grid, smem, tk, tv, stream, mode, occ);
+    case 16: return gqa_mma_run<B, 16, false, Q8>(p, grid, smem, tk, tv, stream, mode, occ);
   }
   return fail(KVC_ERR_UNSUPPORTED, "head subgroup %d", GH);
 }
