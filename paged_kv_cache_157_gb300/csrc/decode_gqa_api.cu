@@ -158,19 +158,20 @@ void mma_dynamic(GqaPlan* pl) {
   if (pl->dyn_share >= 256 || (option(KVC_OPT_BLOCKS_PER_CTA) > 0 && chunk == 0)) pl->dyn_share = pl->dyn_chunk = 0;
 }
 
-// Workers of the warp-MMA split: G static ranges plus at most K claimed
-// chunks, K bounded through the table width (the most the host knows about
-// the lengths).
+// Record pairs of the warp-MMA split: one per worker (G static ranges plus
+// at most K claimed chunks, K bounded through the table width, the most the
+// host knows about the lengths) and, with claimed chunks, one per unit.
 int64_t mma_workers(const GqaPlan& pl, int64_t G, int max_blocks) {
   if (pl.dyn_chunk == 0) return G;
   const int64_t n_max = pl.units * max_blocks;
-  return G + (n_max * pl.dyn_share / 256 + pl.dyn_chunk - 1) / pl.dyn_chunk;
+  return G + (n_max * pl.dyn_share / 256 + pl.dyn_chunk - 1) / pl.dyn_chunk + pl.units;
 }
 
-// Bytes of the counter region of the warp-MMA kernel: the per-unit counters,
-// then 256 bytes holding the claim counter and the finished-CTA count.
-size_t mma_counter_bytes(int batch, int n_kv_heads, const GqaPlan& pl) {
-  return counter_bytes(batch, n_kv_heads, pl) + 256;
+// Bytes ahead of the warp-MMA kernel's records: 256 holding the claim
+// counter and the finished-CTA count, then the block prefixes the decode
+// kernel leaves for its merge kernel (2 x (batch + 1) ints).
+size_t mma_counter_bytes(int batch, int, const GqaPlan&) {
+  return 256 + align_up(static_cast<size_t>(batch + 1) * 2 * 4, 256);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -498,7 +499,9 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
     p.unit_mode = 0;
     p.counters = static_cast<unsigned int*>(workspace);
     if (use_mma) {
-      p.sched = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + cbytes - 256);
+      p.sched = static_cast<unsigned int*>(workspace);
+      p.split_info = reinterpret_cast<int*>(static_cast<char*>(workspace) + 256);
+      p.split_ctas = static_cast<int>(G);
       p.dyn_share = pl.dyn_share;
       p.dyn_chunk = pl.dyn_chunk;
       // automatic split: claimed chunks only when every CTA keeps two rings'
@@ -728,7 +731,7 @@ kvc_status kvc_decode_attention_static(const void* q, const void* k_cache, const
       KVC_OK)
     return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(scratch, 0, mma_counter_bytes(batch, n_kv_heads, pl), st);
+  cudaError_t e = cudaMemsetAsync(scratch, 0, counter_bytes(batch, n_kv_heads, pl) + 256, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(decode scratch counters)");
   return kvc_decode_attention(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch, scale,
                               n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, dtype, out, out_dtype, scratch,

@@ -59,6 +59,7 @@ constexpr int kMmaCtasPerSm = KVC_MMA_CTAS_PER_SM;
 constexpr int kMmaWarps = KVC_MMA_WARPS;
 constexpr int kMmaThreads = (kMmaWarps + 1) * 32;  // consumer warps + one producer warp
 
+
 namespace wmma16 {
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -480,56 +481,144 @@ __device__ __forceinline__ void mma_tile_q8(uint32_t kb, uint32_t vb, int row0, 
 
 // ------------------------------------------------------------------ work split
 //
-// The blocks of all units are laid end to end (sequence major, then kv-head
-// chunk, then head subgroup: global positions 0 .. N-1). Workers 0 .. G-1 are
-// the CTAs' static ranges over the first N0 positions, [w N0 / G, (w+1) N0 /
-// G); workers G .. G+K-1 are the chunks of C positions that tile the rest,
-// [N0 + k C, N0 + (k+1) C), claimed at run time from a counter in the
-// workspace by whichever CTA finishes first. A worker that cuts a unit leaves
-// one fp32 record per cut segment (slot 0: the segment at its range start;
-// slot 1: the one at its range end), and the last worker to count its record
-// merges them.
-struct WorkSplit {
-  int64_t N, N0, G, K;
-  int C;
+// A unit (sequence, kv-head chunk, head subgroup) has nb cache blocks. Its
+// first nb - d blocks are static positions and its last d = nb * share / 256
+// dynamic positions; each kind is laid end to end over the units (sequence
+// major, then chunk, then subgroup): static positions 0 .. N0-1, dynamic
+// positions 0 .. Nd-1. Workers 0 .. G-1 are the CTAs' static ranges
+// [w N0 / G, (w+1) N0 / G); workers G .. G+K-1 are the chunks [k C, (k+1) C)
+// of the dynamic positions, claimed at run time from a counter in the
+// workspace by whichever CTA runs out of work first, so CTAs on SMs that
+// stream faster take more of them. With the dynamic share spread over every
+// unit's tail, a unit has a handful of contributors (the merge reads one
+// record from each). Every segment of a unit that is not the whole unit
+// leaves one fp32 record, which the merge kernel combines: worker w's slot
+// 2w holds the segment at its range start, slot 2w + 1 the one that runs
+// past its range end, and a part that lies strictly inside a range (a unit
+// whose static or dynamic blocks one worker covers, but not all its blocks)
+// goes to the unit's own slot, 2 (G + K) + 2 unit (+ 1 for the dynamic part).
+struct MmaSplit {
+  int64_t N0, Nd, G, K;
+  int C, share;  // share 0: static ranges only
+  __device__ __forceinline__ int dyn(int nb) const {
+    return static_cast<int>((static_cast<int64_t>(nb) * share) >> 8);
+  }
   __device__ __forceinline__ int64_t start(int64_t w) const {
     if (w < G) return w * N0 / G;
-    const int64_t s = N0 + (w - G) * C;
-    return s < N ? s : N;
+    const int64_t s = (w - G) * C;
+    return s < Nd ? s : Nd;
   }
-  __device__ __forceinline__ int64_t worker_of(int64_t b) const {
-    return b < N0 ? ((b + 1) * G - 1) / N0 : G + (b - N0) / C;
+  __device__ __forceinline__ int64_t end(int64_t w) const {
+    if (w < G) return (w + 1) * N0 / G;
+    const int64_t e = (w - G + 1) * C;
+    return e < Nd ? e : Nd;
   }
-  // Workers with a non-empty range that overlap positions [u0, u0 + nb).
-  __device__ __forceinline__ int64_t contributors(int64_t u0, int nb) const {
-    const int64_t c0 = worker_of(u0), c1 = worker_of(u0 + nb - 1);
-    if (N0 >= G || c0 >= G) return c1 - c0 + 1;
-    int64_t n = 0;
-    for (int64_t x = c0; x <= c1; ++x) n += (start(x) != start(x + 1)) ? 1 : 0;
-    return n;
-  }
-  // Record of worker w for the unit starting at u0 (-1: empty range).
-  __device__ __forceinline__ int64_t record(int64_t w, int64_t u0) const {
-    const int64_t s = start(w);
-    if (s == start(w + 1)) return -1;
-    return 2 * w + (u0 > s ? 1 : 0);
+  // the static worker whose range holds static position b (N0 > 0)
+  __device__ __forceinline__ int64_t static_worker(int64_t b) const { return ((b + 1) * G - 1) / N0; }
+  // record slot of worker w for the unit part that starts at u0 (in w's space)
+  // and does not lie strictly inside w's range
+  __device__ __forceinline__ int64_t record(int64_t w, int64_t u0) const { return 2 * w + (u0 > start(w) ? 1 : 0); }
+  // record slot of a unit's static (dyn = false) or dynamic part that lies
+  // strictly inside one worker's range
+  __device__ __forceinline__ int64_t interior(int64_t unit, bool dyn) const {
+    return 2 * (G + K) + 2 * unit + (dyn ? 1 : 0);
   }
 };
 
-// Splits N positions over G static ranges and a dynamic share of dyn_share /
-// 256 of the positions in chunks of dyn_chunk (dyn_chunk 0: static only). The
-// dynamic share is kept only when each CTA still gets at least min_static
-// positions of its own; every CTA computes the same split.
-__device__ __forceinline__ WorkSplit make_split(int64_t N, int64_t G, int dyn_share, int dyn_chunk, int min_static) {
-  WorkSplit s;
-  s.N = N;
+// N: all positions, Nd: the dynamic ones under `share`. The dynamic share is
+// kept only when every CTA still gets at least min_static static positions;
+// every CTA (and the merge kernel) computes the same split.
+__device__ __forceinline__ MmaSplit make_mma_split(int64_t N, int64_t Nd, int64_t G, int share, int chunk,
+                                                   int min_static) {
+  MmaSplit s;
   s.G = G;
-  s.C = dyn_chunk > 0 ? dyn_chunk : 1;
-  int64_t Nd = dyn_chunk > 0 ? N * dyn_share / 256 : 0;
-  if (Nd > 0 && (N - Nd) < G * static_cast<int64_t>(min_static)) Nd = 0;
-  s.N0 = N - Nd;
-  s.K = (Nd + s.C - 1) / s.C;
+  s.C = chunk > 0 ? chunk : 1;
+  s.share = chunk > 0 ? share : 0;
+  s.Nd = s.share > 0 ? Nd : 0;
+  if (s.Nd > 0 && N - s.Nd < G * static_cast<int64_t>(min_static)) {
+    s.share = 0;
+    s.Nd = 0;
+  }
+  s.N0 = N - s.Nd;
+  s.K = (s.Nd + s.C - 1) / s.C;
   return s;
+}
+
+// Exclusive prefix sums over the batch of d = nb * share / 256 (nb from the
+// block prefix s_scan) into s_dscan[0..B]; the whole CTA participates.
+// s_dscan needs B + 1 + 32 ints.
+__device__ inline void scan_dyn(int B, int share, const int* s_scan, int* s_dscan) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int per = (B + nt - 1) / nt;
+  const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+  auto d_of = [&](int b) {
+    return static_cast<int>((static_cast<int64_t>(s_scan[b + 1] - s_scan[b]) * share) >> 8);
+  };
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += d_of(b);
+  const int lane = tid & 31, wid = tid >> 5;
+  int v = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  int* wsum = s_dscan + B + 1;
+  if (lane == 31) wsum[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    const int nw = (nt + 31) >> 5;
+    int x = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += u;
+    }
+    if (lane < nw) wsum[lane] = x;
+  }
+  __syncthreads();
+  int run = v - local + (wid > 0 ? wsum[wid - 1] : 0);
+  for (int b = b0; b < b1; ++b) {
+    s_dscan[b] = run;
+    run += d_of(b);
+  }
+  if (b1 == B && b0 < B) s_dscan[B] = run;
+  if (B == 0 && tid == 0) s_dscan[0] = 0;
+  __syncthreads();
+}
+
+// Where static (dyn = false) or dynamic position pos lies: the unit, the
+// block index j within the unit, the unit's total blocks nb, its blocks in
+// this space cnt, and u0, the space's first position of the unit.
+struct SplitPos {
+  int64_t u0;
+  int seq, chunk, hsub, j, nb, cnt;
+};
+
+__device__ __forceinline__ SplitPos locate_split(int64_t pos, bool dyn, const MmaSplit& sp, int HN,
+                                                 const int* s_scan, const int* s_dscan, int B, int n_hsub) {
+  auto prefix = [&](int b) -> int64_t {
+    const int d = sp.share > 0 ? s_dscan[b] : 0;
+    return static_cast<int64_t>(HN) * (dyn ? d : s_scan[b] - d);
+  };
+  int a = 0, hi = B - 1;  // the last sequence whose prefix is <= pos (skips empty ones)
+  while (a < hi) {
+    const int mid = (a + hi + 1) >> 1;
+    if (prefix(mid) <= pos) a = mid; else hi = mid - 1;
+  }
+  SplitPos r;
+  r.seq = a;
+  r.nb = s_scan[a + 1] - s_scan[a];
+  const int d = sp.dyn(r.nb);
+  r.cnt = dyn ? d : r.nb - d;
+  const int r2 = static_cast<int>(pos - prefix(a));
+  const int idx = r2 / r.cnt;
+  const int jsp = r2 - idx * r.cnt;
+  r.chunk = idx / n_hsub;
+  r.hsub = idx - r.chunk * n_hsub;
+  r.j = dyn ? r.nb - d + jsp : jsp;
+  r.u0 = pos - jsp;
+  return r;
 }
 
 // ------------------------------------------------------------ shared memory
@@ -540,10 +629,9 @@ __device__ __forceinline__ WorkSplit make_split(int64_t N, int64_t G, int dyn_sh
 // query rows [hc][GH][128]; each stage has a 64-byte descriptor written by
 // the producer warp, a "full" barrier (the copies landed) and an "empty"
 // barrier (every consumer warp released it).
-constexpr int kMmaPending = 32;  // deferred merge checks per consumer warp
 
 struct GqaMmaSmem {
-  size_t box_bytes, stage_bytes, q_off, vs_off, meta_off, full_off, empty_off, iss_off, misc_off, pend_off, scan_off,
+  size_t box_bytes, stage_bytes, q_off, vs_off, meta_off, full_off, empty_off, iss_off, misc_off, scan_off, dscan_off,
       total;
 };
 
@@ -561,9 +649,9 @@ __host__ __device__ inline GqaMmaSmem gqa_mma_smem_layout(int q_elt, int GH, int
   s.empty_off = s.full_off + static_cast<size_t>(stages) * 8;
   s.iss_off = s.empty_off + static_cast<size_t>(stages) * 8;
   s.misc_off = align_up(s.iss_off + static_cast<size_t>(stages) * 4, 16);
-  s.pend_off = s.misc_off + 16;
-  s.scan_off = s.pend_off + static_cast<size_t>(kMmaWarps) * kMmaPending * 16;
-  s.total = s.scan_off + static_cast<size_t>(batch + 1 + 32) * 4 + 1024;
+  s.scan_off = s.misc_off + 16;
+  s.dscan_off = s.scan_off + static_cast<size_t>(batch + 1 + 32) * 4;
+  s.total = s.dscan_off + static_cast<size_t>(batch + 1 + 32) * 4 + 1024;
   return s;
 }
 
@@ -584,90 +672,6 @@ struct StageMeta {
   int pad;
 };
 constexpr int kFirst = 1, kLast = 2, kSrc = 4, kWhole = 8;
-
-// One warp merges, for its GW heads of a unit (first position u0, nb blocks),
-// the records of every worker that touched it with the log-sum-exp rule and
-// writes the normalised output. Lane L owns the float4 chunks L + 32k of the
-// warp's GW x 128 outputs; RG records are read together.
-// Not inlined: it runs rarely (once per cut unit), and its registers must not
-// count against the streaming loop's.
-template <int HS, int GW, bool EXT>
-__device__ __noinline__ void merge_unit_mma(const GqaParams& p, const WorkSplit& ws, int64_t u0, int nb, int seq,
-                                            int kvh, int v0, int hoff, int lane) {
-  constexpr int D = 128;
-  constexpr int NCK = GW;  // float4 chunks per lane: (GW * 32 chunks) / 32 lanes
-  constexpr int RG = GW > 4 ? 2 : 4;
-  const int64_t c0 = ws.worker_of(u0), c1 = ws.worker_of(u0 + nb - 1);
-  const int span = static_cast<int>(c1 - c0 + 1);
-  const float* rbase = p.rec_o + static_cast<int64_t>(hoff) * D + 4 * lane;
-  float M[GW], Lp[GW];
-  float4 O[NCK];
-#pragma unroll
-  for (int h = 0; h < GW; ++h) {
-    M[h] = kNegInf;
-    Lp[h] = 0.f;
-  }
-#pragma unroll
-  for (int k = 0; k < NCK; ++k) O[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int base = 0; base < span; base += RG) {
-    const int n = min(RG, span - base);
-    const int64_t rec = (lane < n) ? ws.record(c0 + base + lane, u0) : -1;
-    float mr[GW], lr[GW];
-#pragma unroll
-    for (int h = 0; h < GW; ++h) {
-      const float* ml = p.rec_ml + (rec * HS + hoff + h) * 2;
-      mr[h] = rec >= 0 ? __ldcg(ml) : kNegInf;
-      lr[h] = rec >= 0 ? __ldcg(ml + 1) : 0.f;
-    }
-    float4 ov[RG][NCK];
-#pragma unroll
-    for (int i = 0; i < RG; ++i) {
-      const int64_t rr = __shfl_sync(0xffffffffu, rec, i);
-#pragma unroll
-      for (int k = 0; k < NCK; ++k)
-        ov[i][k] = (i < n && rr >= 0) ? __ldcg(reinterpret_cast<const float4*>(rbase + rr * HS * D + 128 * k))
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float fr[GW];
-#pragma unroll
-    for (int h = 0; h < GW; ++h) {
-      const float mn = fmaxf(M[h], warp_max(mr[h]));
-      if (mn != M[h]) {
-        const float a = (M[h] == kNegInf) ? 0.f : fast_exp2(M[h] - mn);
-        Lp[h] *= a;
-        // chunk k of lane L belongs to head (L + 32k) / 32 = k
-        O[h].x *= a;
-        O[h].y *= a;
-        O[h].z *= a;
-        O[h].w *= a;
-        M[h] = mn;
-      }
-      fr[h] = (mr[h] == kNegInf) ? 0.f : fast_exp2(mr[h] - M[h]);
-      Lp[h] += fr[h] * lr[h];
-    }
-#pragma unroll
-    for (int i = 0; i < RG; ++i) {
-#pragma unroll
-      for (int h = 0; h < GW; ++h) {
-        const float f = __shfl_sync(0xffffffffu, fr[h], i);
-        O[h].x += f * ov[i][h].x;
-        O[h].y += f * ov[i][h].y;
-        O[h].z += f * ov[i][h].z;
-        O[h].w += f * ov[i][h].w;
-      }
-    }
-  }
-#pragma unroll
-  for (int h = 0; h < GW; ++h) {
-    const float lsum = warp_sum(Lp[h]);
-    const float inv = 1.0f / lsum;
-    if (EXT && p.lse != nullptr && lane == 0) p.lse[out_row(p, seq, kvh, v0 + h)] = M[h] + __log2f(lsum);
-    const int64_t o = EXT ? out_row(p, seq, kvh, v0 + h) * D + 4 * lane
-                          : (static_cast<int64_t>(seq) * p.n_q_heads + kvh * p.group + v0 + h) * D + 4 * lane;
-    const float v[4] = {O[h].x * inv, O[h].y * inv, O[h].z * inv, O[h].w * inv};
-    store_out_vec<4>(p.out, o, v, p.out_dtype);
-  }
-}
 
 // Q8 = 0: T is the cache and query type; Q8 = 1 (e4m3) or 2 (int8): one-byte
 // caches with T (bf16) queries.
@@ -705,6 +709,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
   unsigned int* s_iss = reinterpret_cast<unsigned int*>(smem + L.iss_off);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.misc_off);
   int* s_scan = reinterpret_cast<int*>(smem + L.scan_off);
+  int* s_dscan = reinterpret_cast<int*>(smem + L.dscan_off);
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int kh = w / HW, hw = w % HW;
@@ -766,10 +771,12 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
 
   // The work split (every CTA computes the same one). In the unit mode CTA u
   // takes unit u whole and nothing is claimed.
-  WorkSplit ws;
+  const int dshare = (!p.unit_mode && p.dyn_chunk > 0) ? p.dyn_share : 0;
+  scan_dyn(B, dshare, s_scan, s_dscan);  // ends with a CTA barrier
+  MmaSplit sp;
   int64_t lo, hi;
   if (p.unit_mode) {
-    ws = make_split(N, G, 0, 0, 1);
+    sp = make_mma_split(N, 0, G, 0, 0, 1);
     const int seq = static_cast<int>(c / HN);
     const int idx = static_cast<int>(c - static_cast<int64_t>(seq) * HN);
     const int nb = s_scan[seq + 1] - s_scan[seq];
@@ -789,9 +796,16 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
     lo = static_cast<int64_t>(HN) * s_scan[seq] + static_cast<int64_t>(idx) * nb;
     hi = lo + nb;
   } else {
-    ws = make_split(N, G, p.dyn_share, p.dyn_chunk, p.dyn_min_static);
-    lo = ws.start(c);
-    hi = ws.start(c + 1);
+    sp = make_mma_split(N, static_cast<int64_t>(HN) * s_dscan[B], G, dshare, p.dyn_chunk, p.dyn_min_static);
+    lo = sp.start(c);
+    hi = sp.end(c);
+    if (blockIdx.x == 0) {
+      // the block prefixes, for the merge kernel
+      for (int b = tid; b <= B; b += blockDim.x) {
+        p.split_info[b] = s_scan[b];
+        p.split_info[B + 1 + b] = s_dscan[b];
+      }
+    }
   }
 
   if (w == kMmaWarps) {
@@ -807,7 +821,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
     const uint32_t vs_bytes = static_cast<uint32_t>(hc * bs * 4);
     const bool q_contig = (GH == p.group);
     unsigned int claim = 0;
-    if (!p.unit_mode && ws.K > 0 && lane == 0) claim = atomicAdd(p.sched, 1u);  // for after the static range
+    if (!p.unit_mode && sp.K > 0 && lane == 0) claim = atomicAdd(p.sched, 1u);  // for after the static range
     int64_t wk = c;
     uint32_t slot = 0, ph = 0;
     bool ok = true;
@@ -817,23 +831,24 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
         StageMeta m{};
         int src = -1, qoff = -1;
         if (pos < hi) {
-          const BlockPos bp = locate_block(pos, HN, s_scan, B, p.n_hsub);
+          const SplitPos bp = locate_split(pos, wk >= G, sp, HN, s_scan, s_dscan, B, p.n_hsub);
           m.seq = bp.seq;
           m.chunk = bp.chunk;
           m.hsub = bp.hsub;
           m.nb = bp.nb;
-          m.u0 = pos - bp.j;
+          m.u0 = bp.u0;
           m.n_rows = seq_rows(p.context_lens, bp.seq, bs, p.max_blocks, min_len);
           m.r0 = start_row(m.n_rows, wnd, row_start, row_div, bp.seq);
           m.jb = m.r0 / bs + bp.j;
           const int phys = __ldg(p.block_tables + static_cast<int64_t>(bp.seq) * p.max_blocks + m.jb);
           if (phys >= 0 && phys < p.num_blocks) src = (phys * p.n_kv_heads + bp.chunk * hc) * bs;
-          const bool first = (pos == lo) || (bp.j == 0);
-          m.flags = (first ? kFirst : 0) | ((pos == hi - 1 || bp.j == bp.nb - 1) ? kLast : 0) | (src >= 0 ? kSrc : 0) |
-                    ((m.u0 >= lo && m.u0 + bp.nb <= hi) ? kWhole : 0);
-          // slot 0: the segment holding the range's first position; slot 1: a
-          // unit that starts inside the range and runs past its end
-          m.rec = static_cast<int>(2 * wk + (m.u0 > lo ? 1 : 0));
+          const bool first = (pos == lo) || (pos == bp.u0);
+          const bool whole = bp.cnt == bp.nb && bp.u0 >= lo && bp.u0 + bp.cnt <= hi;
+          m.flags = (first ? kFirst : 0) | ((pos == hi - 1 || pos - bp.u0 == bp.cnt - 1) ? kLast : 0) |
+                    (src >= 0 ? kSrc : 0) | (whole ? kWhole : 0);
+          const int64_t unit = static_cast<int64_t>(bp.seq) * HN + bp.chunk * p.n_hsub + bp.hsub;
+          m.rec = static_cast<int>((bp.u0 > lo && bp.u0 + bp.cnt <= hi) ? sp.interior(unit, wk >= G)
+                                                                        : sp.record(wk, bp.u0));
           if (first)
             qoff = multi ? (bp.seq * p.n_chunks + bp.chunk) * p.n_hsub + bp.hsub
                          : (bp.seq * p.n_q_heads + bp.chunk * hc * p.group + bp.hsub * GH) * D;
@@ -917,14 +932,14 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
           }
         }
       }
-      if (!ok || p.unit_mode || ws.K == 0) break;
+      if (!ok || p.unit_mode || sp.K == 0) break;
       // the next chunk: the claim made a range ago; claim the one after it now
       const int64_t k = static_cast<int64_t>(__shfl_sync(full, claim, 0));
-      if (k >= ws.K) break;
+      if (k >= sp.K) break;
       if (lane == 0) claim = atomicAdd(p.sched, 1u);
       wk = G + k;
-      lo = ws.start(wk);
-      hi = ws.start(wk + 1);
+      lo = sp.start(wk);
+      hi = sp.end(wk);
     }
     if (lane == 0) {
       if (ok && mbar_wait_bounded(ebar + slot, ph ^ 1u)) {
@@ -936,7 +951,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
       }
       // Every CTA makes exactly one failed claim; the last one to do so
       // resets the claim counter for the next call.
-      if (!p.unit_mode && ws.K > 0 && atomicAdd(p.sched + 1, 1u) == static_cast<unsigned int>(G) - 1) {
+      if (!p.unit_mode && sp.K > 0 && atomicAdd(p.sched + 1, 1u) == static_cast<unsigned int>(G) - 1) {
         atomicExch(p.sched, 0u);
         atomicExch(p.sched + 1, 0u);
       }
@@ -945,44 +960,9 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
     // ============================================================== consumers
     const int g8 = lane >> 2, c4 = lane & 3;
     const uint32_t box_bytes = static_cast<uint32_t>(L.box_bytes);
-    uint64_t* pend = reinterpret_cast<uint64_t*>(smem + L.pend_off) + w * kMmaPending * 2;  // (u0, old) pairs
-    int n_pend = 0;
-    unsigned int last_old = 0;  // result of the newest count, written to its entry later
-    bool have_last = false;
-    // Merge check of every deferred entry: the warp whose add completed a
-    // unit's count merges its heads and resets the counter.
-    auto flush = [&]() {
-      if (have_last) {
-        if (lane == 0) pend[2 * (n_pend - 1) + 1] = last_old;
-        have_last = false;
-      }
-      __syncwarp();
-      for (int e = 0; e < n_pend; ++e) {
-        const int64_t u0 = static_cast<int64_t>(pend[2 * e]);
-        const unsigned int old = static_cast<unsigned int>(pend[2 * e + 1]);
-        const BlockPos q = locate_block(u0, HN, s_scan, B, p.n_hsub);
-        const int64_t contributors = ws.contributors(u0, q.nb);
-        const int64_t unit = (static_cast<int64_t>(q.seq) * p.n_chunks + q.chunk) * p.n_hsub + q.hsub;
-        unsigned int* ctr = p.counters + unit * nact + w;
-        if (old + 1 == static_cast<unsigned int>(contributors)) {
-          if (lane == 0) *ctr = 0u;
-          merge_unit_mma<HS, GW, EXT>(p, ws, u0, q.nb, q.seq, q.chunk * hc + kh, q.hsub * GH + hw * GW,
-                                      kh * GH + hw * GW, lane);
-        } else if (old + 1 > static_cast<unsigned int>(contributors)) {
-          if (lane == 0) {
-            set_flag(p.err, 0x10u);  // the workspace counters were not zero
-            atomicExch(ctr, 0u);
-          }
-        }
-      }
-      n_pend = 0;
-      __syncwarp();
-    };
-
     // One pass of the outer loop per segment (the positions of one unit in
     // one worker's range): the first position carries the unit's query rows,
-    // the last one closes the segment. The warp state lives only inside a
-    // segment, so the rare merge calls between segments cost no registers.
+    // the last one closes the segment.
     uint32_t slot = 0, ph = 0;
     bool abort_seen = false;
     for (;;) {
@@ -1181,27 +1161,12 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
             p.rec_ml[(rec * HS + hr + 2 * c4 + 1) * 2 + 1] = lw1;
           }
         }
-        // Count the record (one counter per unit and warp slot): the warp
-        // barrier orders the lanes' record writes before lane 0's release.
-        // The add's result is read only at the next count or at the end, so
-        // its round trip never stalls the stream.
-        if (n_pend == kMmaPending) flush();
-        if (have_last && lane == 0) pend[2 * (n_pend - 1) + 1] = last_old;
-        __syncwarp();
-        const int64_t unit = (static_cast<int64_t>(m.seq) * p.n_chunks + m.chunk) * p.n_hsub + m.hsub;
-        if (lane == 0) {
-          pend[2 * n_pend] = static_cast<uint64_t>(m.u0);
-          last_old = atomic_add_acq_rel_gpu(p.counters + unit * nact + w, 1u);
-        }
-        ++n_pend;
-        have_last = true;
       }
     }
     if (abort_seen && lane == 0) {
       set_flag(p.err, 0x8u);
       *s_abort = 1;
     }
-    if (!*s_abort) flush();
   }
 
   __syncthreads();
@@ -1214,6 +1179,154 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
       if (n > 0) (void)mbar_wait_bounded(fbar + x, (n - 1) & 1u);
     }
   }
+}
+
+// ------------------------------------------------------------------ merge
+//
+// Runs after the decode kernel (launched behind it on the same stream). For
+// one unit and one head group (the GW query heads a consumer warp owns) it
+// combines the records of every segment that covered part of the unit with
+// the log-sum-exp rule, O = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r,
+// and writes the normalised output (and the LSE row). The CTA's threads form
+// NG groups of 32 GW, a thread owning dims 4 (t & 31) .. + 3 of head
+// (t mod 32 GW) / 32; group g folds records g, g + NG, ... (kMergeBatch at a
+// time, all loads of a batch in flight together), then the groups' partial
+// results are combined. Units one worker covered whole were written by the
+// decode kernel. All merges run in parallel, one small CTA each (several
+// fit next to each other on an SM, so they run in one wave).
+constexpr int kMergeBatch = 16;
+__host__ __device__ constexpr int merge_threads(int GH) {
+  return 32 * (GH / mma_warps_per_kvhead(GH)) > 128 ? 32 * (GH / mma_warps_per_kvhead(GH)) : 128;
+}
+
+template <int GH, bool EXT>
+__global__ void __launch_bounds__(merge_threads(GH)) gqa_mma_merge_kernel(const GqaParams p) {
+  constexpr int D = 128;
+  constexpr int HW = mma_warps_per_kvhead(GH);
+  constexpr int GW = GH / HW;
+  constexpr int HS = (kMmaWarps / HW) * GH;  // query heads per record
+  constexpr int TG = 32 * GW;                // threads per group
+  constexpr int NG = merge_threads(GH) / TG; // groups
+  constexpr int RR = NG * kMergeBatch;       // records per round
+  __shared__ int64_t s_rec[RR];
+  __shared__ float s_pm[NG][GW], s_pl[NG][GW];
+  __shared__ float4 s_po[NG][TG];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int B = p.batch;
+  const int HN = p.n_chunks * p.n_hsub;
+  const int nact = p.hc * HW;
+  const int unit = static_cast<int>(blockIdx.x / nact), wi = static_cast<int>(blockIdx.x % nact);
+  const int kh = wi / HW, hw = wi % HW;
+  const int seq = unit / HN, idx = unit - seq * HN;
+  const int chunk = idx / p.n_hsub, hsub = idx - chunk * p.n_hsub;
+  // the decode kernel's block prefixes over the batch (all blocks, dynamic ones)
+  const int* info = p.split_info;
+  const int pb0 = __ldcg(info + seq), pb1 = __ldcg(info + seq + 1), pbt = __ldcg(info + B);
+  const int pd0 = __ldcg(info + B + 1 + seq), pdt = __ldcg(info + 2 * B + 1);
+  const int nb = pb1 - pb0;
+  if (nb == 0) return;  // zero output, written by the decode kernel
+  const int dshare = p.dyn_chunk > 0 ? p.dyn_share : 0;
+  const MmaSplit sp = make_mma_split(static_cast<int64_t>(HN) * pbt, static_cast<int64_t>(HN) * pdt, p.split_ctas,
+                                     dshare, p.dyn_chunk, p.dyn_min_static);
+  const int d = sp.dyn(nb), s = nb - d;
+  const int64_t su0 = static_cast<int64_t>(HN) * (pb0 - (sp.share > 0 ? pd0 : 0)) + static_cast<int64_t>(idx) * s;
+  const int64_t c0 = sp.static_worker(su0), c1 = sp.static_worker(su0 + s - 1);
+  if (d == 0 && c0 == c1) return;  // one worker covered the unit whole
+  const int64_t du0 = static_cast<int64_t>(HN) * pd0 + static_cast<int64_t>(idx) * d;
+  const int64_t k0 = du0 / sp.C, k1 = d > 0 ? (du0 + d - 1) / sp.C : k0 - 1;
+  const int64_t ns = c1 - c0 + 1, R = ns + (k1 - k0 + 1);
+  // the record of contributor r (-1: an empty range). Every static range
+  // after c0 starts inside the unit (slot 2w) and, when N0 >= G, is non-empty;
+  // dynamic ranges start at k C.
+  auto record_of = [&](int64_t r) -> int64_t {
+    if (r < ns) {
+      if (r == 0) {
+        const int64_t s0 = sp.start(c0);
+        return c0 == c1 && su0 > s0 ? sp.interior(unit, false) : 2 * c0 + (su0 > s0 ? 1 : 0);
+      }
+      const int64_t wk = c0 + r;
+      return (sp.N0 >= sp.G || sp.start(wk) != sp.end(wk)) ? 2 * wk : -1;
+    }
+    const int64_t k = k0 + (r - ns);
+    const bool after = du0 > k * sp.C;
+    return k0 == k1 && after ? sp.interior(unit, true) : 2 * (sp.G + k) + (after ? 1 : 0);
+  };
+  const int t = threadIdx.x, g = t / TG, q = t - g * TG, h = q >> 5, q4 = q & 31;
+  const int hr = kh * GH + hw * GW + h;  // the head's slot in a record
+  float M = kNegInf, Ls = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t base = 0; base < R; base += RR) {
+    __syncthreads();
+    if (t < RR) s_rec[t] = base + t < R ? record_of(base + t) : -1;
+    __syncthreads();
+    float mr[kMergeBatch], lr[kMergeBatch];
+    float4 ov[kMergeBatch];
+#pragma unroll
+    for (int i = 0; i < kMergeBatch; ++i) {
+      const int64_t rec = s_rec[i * NG + g];
+      mr[i] = kNegInf;
+      lr[i] = 0.f;
+      ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (rec >= 0) {
+        const float* ml = p.rec_ml + (rec * HS + hr) * 2;
+        mr[i] = __ldcg(ml);
+        lr[i] = __ldcg(ml + 1);
+        ov[i] = __ldcg(reinterpret_cast<const float4*>(p.rec_o + (rec * HS + hr) * D) + q4);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMergeBatch; ++i) {
+      if (mr[i] == kNegInf) continue;
+      if (mr[i] > M) {
+        const float a = M == kNegInf ? 0.f : fast_exp2(M - mr[i]);
+        Ls *= a;
+        O.x *= a;
+        O.y *= a;
+        O.z *= a;
+        O.w *= a;
+        M = mr[i];
+      }
+      const float f = fast_exp2(mr[i] - M);
+      Ls += f * lr[i];
+      O.x += f * ov[i].x;
+      O.y += f * ov[i].y;
+      O.z += f * ov[i].z;
+      O.w += f * ov[i].w;
+    }
+  }
+  if (NG > 1) {
+    if (q4 == 0) {
+      s_pm[g][h] = M;
+      s_pl[g][h] = Ls;
+    }
+    s_po[g][q] = O;
+    __syncthreads();
+    if (g != 0) return;
+    float Mx = kNegInf;
+#pragma unroll
+    for (int j = 0; j < NG; ++j) Mx = fmaxf(Mx, s_pm[j][h]);
+    Ls = 0.f;
+    O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+      const float mj = s_pm[j][h];
+      if (mj == kNegInf) continue;
+      const float f = fast_exp2(mj - Mx);
+      const float4 oj = s_po[j][q];
+      Ls += f * s_pl[j][h];
+      O.x += f * oj.x;
+      O.y += f * oj.y;
+      O.z += f * oj.z;
+      O.w += f * oj.w;
+    }
+    M = Mx;
+  }
+  const int kvh = chunk * p.hc + kh, v = hsub * GH + hw * GW + h;
+  const int64_t row = EXT ? out_row(p, seq, kvh, v) : static_cast<int64_t>(seq) * p.n_q_heads + kvh * p.group + v;
+  const float inv = 1.0f / Ls;
+  const float vals[4] = {O.x * inv, O.y * inv, O.z * inv, O.w * inv};
+  store_out_vec<4>(p.out, row * D + 4 * q4, vals, p.out_dtype);
+  if (EXT && p.lse != nullptr && q4 == 0) p.lse[row] = M + __log2f(Ls);
 }
 
 }  // namespace kvc

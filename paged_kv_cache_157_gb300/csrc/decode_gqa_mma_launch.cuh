@@ -33,6 +33,20 @@ static kvc_status gqa_mma_run(const GqaParams& p, int grid, size_t smem, const C
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, k, tk, tv, p);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gqa mma)");
+  if (p.unit_mode) return KVC_OK;
+  // The merge of split units, right behind (it may be scheduled early; it
+  // waits for the decode grid before it reads anything).
+  auto* mk = gqa_mma_merge_kernel<GH, EXT>;
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3(static_cast<unsigned int>(static_cast<int64_t>(p.batch) * p.n_chunks * p.n_hsub * p.hc *
+                                                mma_warps_per_kvhead(GH)));
+  mcfg.blockDim = dim3(merge_threads(GH));
+  mcfg.dynamicSmemBytes = 0;
+  mcfg.stream = stream;
+  mcfg.attrs = attr;
+  mcfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&mcfg, mk, p);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gqa mma merge)");
   return KVC_OK;
 }
 
