@@ -874,7 +874,7 @@ def run_kvc(args):
         "frac_of_8tbs": round(value / NOMINAL_HBM_GBS, 4),
         "seq_layer_steps_per_s": round(world * m["batch"] / (ms / 1e3), 1),
         "bytes_per_step": per_step,
-        "roofline": {"bound": "hbm", "kernel": "kvc_decode_attention (gqa_mma_kernel, split-K merge fused in)",
+        "roofline": {"bound": "hbm", "kernel": "kvc_decode_attention (gqa_mma_kernel + gqa_mma_merge_kernel, timed together)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "traffic": traffic_from_profile(), "algorithmic_bytes_per_launch": dec_b,
