@@ -104,9 +104,10 @@ typedef enum kvc_option {
    *  - the tcgen05 tensor-core kernel: bf16/f16 caches, head_dim 128, block
    *    sizes 16/32/64/128, no window, kv heads with 8 to 32 queries (qn =
    *    n_tokens x n_q_heads / n_kv_heads);
-   *  - the warp-MMA kernel: bf16/f16 caches, head_dim 128, block sizes that
-   *    are multiples of 16 up to 128 (every feature: windows, several new
-   *    tokens, shared prefixes);
+   *  - the warp-MMA kernel: bf16/f16 caches, and the one-byte caches of
+   *    kvc_decode_attention_fp8 / _int8, head_dim 128, block sizes that are
+   *    multiples of 16 up to 128 (16-bit caches: every feature, windows,
+   *    several new tokens, shared prefixes);
    *  - the CUDA-core kernel: every dtype, head size and feature.
    * 0 (default) = automatic: the warp-MMA kernel where it applies and qn is
    * 2 to 16; else the tensor-core kernel where it applies and the cache it
@@ -118,15 +119,15 @@ typedef enum kvc_option {
    * 3 = the warp-MMA kernel wherever it applies, else the CUDA-core kernel. */
   KVC_OPT_GQA_ENGINE = 3,
   /* Warp-MMA kernel work split. Each CTA streams a static range of the cache
-   * blocks; optionally a share of them is instead cut into chunks that CTAs
-   * claim as they finish, so faster SMs take more of it. Every claimed chunk
-   * that cuts a (sequence, kv-head chunk) unit leaves a partial record that
-   * the unit's last contributor merges, so small chunks trade balance for
-   * merge work at the end of the launch. DYNAMIC_SHARE: the claimed part in
-   * 1/256 of all blocks (0 = automatic, currently none; 1..255 as given; 256
-   * = none). DYNAMIC_CHUNK: blocks (of one kv-head chunk) per claimed chunk
-   * (0 = automatic, 8; N >= 1 as given, and then used at any size).
-   * Process-wide. */
+   * blocks; optionally the last share of every (sequence, kv-head chunk)
+   * unit's blocks is instead cut into chunks that CTAs claim as they finish,
+   * so faster SMs take more of it. Every segment that covers part of a unit
+   * leaves a partial record, which a merge kernel launched behind the decode
+   * combines, so small chunks trade balance for records. DYNAMIC_SHARE: the
+   * claimed part in 1/256 of each unit's blocks (0 = automatic, currently
+   * none; 1..255 as given; 256 = none). DYNAMIC_CHUNK: blocks (of one
+   * kv-head chunk) per claimed chunk (0 = automatic, 8; N >= 1 as given, and
+   * then used at any size). Process-wide. */
   KVC_OPT_DYNAMIC_SHARE = 4,
   KVC_OPT_DYNAMIC_CHUNK = 5,
   /* Test hook for the failure path of the GQA decode kernels (CUDA-core and
@@ -333,10 +334,13 @@ kvc_status kvc_decode_attention_shared_prefix(const void* q, const void* k_cache
 /* FP8 KV cache decode: as kvc_decode_attention over the caches written by
  * kvc_append_fp8, attending k = e4m3value(code) * k_scale[h, d] and
  * v = e4m3value(code) * v_scale[row] (the scales fold into the query and into
- * the softmax weights, so the kernel reads one byte per cached element). q is
- * bf16 [batch, n_q_heads, head_dim]; head_dim 64, 128 or 256; k_scale and
- * v_scale 16-byte aligned. Same tables, lengths, workspace (size query:
- * kvc_decode_workspace_size) and error rules as kvc_decode_attention.
+ * the softmax weights, so the kernel reads one byte per cached element; with
+ * head_dim 128 and 2 to 16 queries per kv head the warp-MMA kernel runs the
+ * products on f16 MMAs, the codes converted exactly, the scaled query and
+ * the weights as f16 hi + lo parts). q is bf16 [batch, n_q_heads, head_dim];
+ * head_dim 64, 128 or 256; k_scale and v_scale 16-byte aligned. Same
+ * tables, lengths, workspace (size query: kvc_decode_workspace_size) and
+ * error rules as kvc_decode_attention.
  * Source: "KV-Cache——为什么AI回复越来越快" section 08 (FP8 KV cache). */
 kvc_status kvc_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                                     const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
