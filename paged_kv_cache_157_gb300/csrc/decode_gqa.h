@@ -51,8 +51,11 @@ struct GqaParams {
   int dyn_chunk;        // positions per claimed chunk (0: no dynamic tail)
   int dyn_min_static;   // keep the dynamic tail only if every CTA still gets this many static positions
   unsigned int wait_polls;  // 0: waits for copied data bounded by ~1 s; N: give up after N polls (test hook)
-  int split_ctas;           // warp-MMA kernel: CTAs of the split (its merge kernel recomputes the split)
-  int* split_info;          // warp-MMA kernel: [block prefix 0..batch][dynamic-block prefix 0..batch] for the merge
+  // warp-MMA kernel: per unit [record count R][record slots 0 .. list_cap-1], written by the worker that
+  // holds the unit's first block and read by the merge kernel; R = 0: no merge (one worker had it whole)
+  int* unit_lists;
+  int list_cap;
+  int64_t rec_slots;        // record slots in the workspace (2 per record pair)
 };
 
 #ifndef KVC_GQA_WARPS

@@ -167,11 +167,17 @@ int64_t mma_workers(const GqaPlan& pl, int64_t G, int max_blocks) {
   return G + (n_max * pl.dyn_share / 256 + pl.dyn_chunk - 1) / pl.dyn_chunk + pl.units;
 }
 
+// Contributors a unit can have at most: the G static ranges, plus the
+// claimed chunks when the split has a dynamic share.
+int64_t mma_list_cap(const GqaPlan& pl, int64_t G, int max_blocks) {
+  return pl.dyn_chunk == 0 ? G : mma_workers(pl, G, max_blocks) - pl.units;
+}
+
 // Bytes ahead of the warp-MMA kernel's records: 256 holding the claim
-// counter and the finished-CTA count, then the block prefixes the decode
-// kernel leaves for its merge kernel (2 x (batch + 1) ints).
-size_t mma_counter_bytes(int batch, int, const GqaPlan&) {
-  return 256 + align_up(static_cast<size_t>(batch + 1) * 2 * 4, 256);
+// counter and the finished-CTA count, then every unit's record list for the
+// merge kernel ([count][cap slots] ints).
+size_t mma_counter_bytes(const GqaPlan& pl, int64_t cap) {
+  return 256 + align_up(static_cast<size_t>(pl.units) * static_cast<size_t>(1 + cap) * 4, 256);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -308,8 +314,9 @@ kvc_status decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int 
   if (head_dim == 128 && block_size % 16 == 0 && block_size <= 128 &&
       make_plan_mma(batch, n_q_heads, n_kv_heads, block_size, 2, dev->max_smem_optin, &pm) == KVC_OK) {
     const int64_t Gm = plan_ctas(dev, pm.ctas_per_sm, pm.units, max_blocks_per_seq);
-    const int64_t Wm = with_dynamic ? mma_workers(pm, Gm, max_blocks_per_seq) : Gm;
-    *bytes = std::max(*bytes, align_up(mma_counter_bytes(batch, n_kv_heads, pm) +
+    if (!with_dynamic) pm.dyn_share = pm.dyn_chunk = 0;
+    const int64_t Wm = mma_workers(pm, Gm, max_blocks_per_seq);
+    *bytes = std::max(*bytes, align_up(mma_counter_bytes(pm, mma_list_cap(pm, Gm, max_blocks_per_seq)) +
                                            static_cast<size_t>(Wm) * pm.rec_bytes_per_cta, 256));
   }
   clear_error();
@@ -479,7 +486,8 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   }
   if (use_mma) occ = std::min(occ, pl.ctas_per_sm);  // never more records than the size query counted
   int64_t G = plan_ctas(dev, occ, pl.units, max_blocks_per_seq);
-  const size_t cbytes = use_mma ? mma_counter_bytes(batch, n_kv_heads, pl) : counter_bytes(batch, n_kv_heads, pl);
+  const int64_t list_cap = use_mma ? mma_list_cap(pl, G, max_blocks_per_seq) : 0;
+  const size_t cbytes = use_mma ? mma_counter_bytes(pl, list_cap) : counter_bytes(batch, n_kv_heads, pl);
   const int64_t rec_fit = workspace_bytes > cbytes
                               ? static_cast<int64_t>((workspace_bytes - cbytes) / pl.rec_bytes_per_cta)
                               : 0;
@@ -500,8 +508,8 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
     p.counters = static_cast<unsigned int*>(workspace);
     if (use_mma) {
       p.sched = static_cast<unsigned int*>(workspace);
-      p.split_info = reinterpret_cast<int*>(static_cast<char*>(workspace) + 256);
-      p.split_ctas = static_cast<int>(G);
+      p.unit_lists = reinterpret_cast<int*>(static_cast<char*>(workspace) + 256);
+      p.list_cap = static_cast<int>(list_cap);
       p.dyn_share = pl.dyn_share;
       p.dyn_chunk = pl.dyn_chunk;
       // automatic split: claimed chunks only when every CTA keeps two rings'
@@ -510,6 +518,7 @@ kvc_status decode_impl(const void* q, const void* k_cache, const void* v_cache, 
     }
     p.rec_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + cbytes);
     p.rec_ml = p.rec_o + static_cast<size_t>(W) * 2 * HS * head_dim;
+    p.rec_slots = 2 * W;
     grid = static_cast<int>(G);
   } else {
     p.unit_mode = 1;

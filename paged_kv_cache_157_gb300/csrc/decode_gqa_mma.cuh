@@ -621,6 +621,48 @@ __device__ __forceinline__ SplitPos locate_split(int64_t pos, bool dyn, const Mm
   return r;
 }
 
+// The records of one unit: its static part [su0, su0 + s) spans static
+// workers c0 .. c1, its dynamic part [du0, du0 + d) chunks k0 .. k1.
+struct UnitRecs {
+  int64_t su0, du0, c0, c1, k0, k1, ns, R;
+  bool whole;  // one worker covered the unit: no records
+};
+
+__device__ __forceinline__ UnitRecs unit_recs(int seq, int idx, const MmaSplit& sp, int HN, const int* s_scan,
+                                              const int* s_dscan) {
+  UnitRecs u;
+  const int nb = s_scan[seq + 1] - s_scan[seq];
+  const int d = sp.dyn(nb), s = nb - d;
+  const int dpre = sp.share > 0 ? s_dscan[seq] : 0;
+  u.su0 = static_cast<int64_t>(HN) * (s_scan[seq] - dpre) + static_cast<int64_t>(idx) * s;
+  u.c0 = sp.static_worker(u.su0);
+  u.c1 = sp.static_worker(u.su0 + s - 1);
+  u.du0 = static_cast<int64_t>(HN) * dpre + static_cast<int64_t>(idx) * d;
+  u.k0 = u.du0 / sp.C;
+  u.k1 = d > 0 ? (u.du0 + d - 1) / sp.C : u.k0 - 1;
+  u.ns = u.c1 - u.c0 + 1;
+  u.R = u.ns + (u.k1 - u.k0 + 1);
+  u.whole = d == 0 && u.c0 == u.c1;
+  return u;
+}
+
+// Record slot of contributor r of the unit (-1: an empty static range). Every
+// static range after c0 starts inside the unit (slot 2w) and, when N0 >= G,
+// is non-empty; dynamic chunk k starts at k C.
+__device__ __forceinline__ int64_t unit_record(const UnitRecs& u, int64_t unit, const MmaSplit& sp, int64_t r) {
+  if (r < u.ns) {
+    if (r == 0) {
+      const int64_t s0 = sp.start(u.c0);
+      return u.c0 == u.c1 && u.su0 > s0 ? sp.interior(unit, false) : 2 * u.c0 + (u.su0 > s0 ? 1 : 0);
+    }
+    const int64_t wk = u.c0 + r;
+    return (sp.N0 >= sp.G || sp.start(wk) != sp.end(wk)) ? 2 * wk : -1;
+  }
+  const int64_t k = u.k0 + (r - u.ns);
+  const bool after = u.du0 > k * sp.C;
+  return u.k0 == u.k1 && after ? sp.interior(unit, true) : 2 * (sp.G + k) + (after ? 1 : 0);
+}
+
 // ------------------------------------------------------------ shared memory
 //
 // Offsets from a 1024-byte aligned base (the host adds 1024 bytes of slack
@@ -760,6 +802,8 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
       const int rows = n_tok * p.n_q_heads * D;
       for (int b = 0; b < B; ++b) {
         if (s_scan[b + 1] != s_scan[b]) continue;
+        for (int idx = tid; idx < HN; idx += blockDim.x)  // nothing to merge
+          p.unit_lists[static_cast<int64_t>(b * HN + idx) * (1 + p.list_cap)] = 0;
         for (int idx = tid; idx < rows; idx += blockDim.x)
           store_out(p.out, static_cast<int64_t>(b) * rows + idx, 0.f, p.out_dtype);
         if (EXT && p.lse != nullptr)
@@ -799,13 +843,6 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
     sp = make_mma_split(N, static_cast<int64_t>(HN) * s_dscan[B], G, dshare, p.dyn_chunk, p.dyn_min_static);
     lo = sp.start(c);
     hi = sp.end(c);
-    if (blockIdx.x == 0) {
-      // the block prefixes, for the merge kernel
-      for (int b = tid; b <= B; b += blockDim.x) {
-        p.split_info[b] = s_scan[b];
-        p.split_info[B + 1 + b] = s_dscan[b];
-      }
-    }
   }
 
   if (w == kMmaWarps) {
@@ -869,6 +906,16 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
           mi.pad = 0;
           const int srci = __shfl_sync(full, src, i);
           const int qo = __shfl_sync(full, qoff, i);
+          if (!p.unit_mode && wk < G && mi.u0 == bpos + i) {
+            // the unit's first block: publish its record list for the merge
+            const int uidx = mi.chunk * p.n_hsub + mi.hsub;
+            const int64_t unit = static_cast<int64_t>(mi.seq) * HN + uidx;
+            const UnitRecs u = unit_recs(mi.seq, uidx, sp, HN, s_scan, s_dscan);
+            int* lst = p.unit_lists + unit * (1 + p.list_cap);
+            const int R = u.whole ? 0 : static_cast<int>(u.R < p.list_cap ? u.R : p.list_cap);
+            for (int r = lane; r < R; r += 32) lst[1 + r] = static_cast<int>(unit_record(u, unit, sp, r));
+            if (lane == 0) lst[0] = R;
+          }
           if (lane == 0) {
             ok = mbar_wait_data(ebar + slot, ph ^ 1u, p.wait_polls) && !*s_abort;
             if (ok) {
@@ -1185,15 +1232,14 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
 //
 // Runs after the decode kernel (launched behind it on the same stream). For
 // one unit and one head group (the GW query heads a consumer warp owns) it
-// combines the records of every segment that covered part of the unit with
-// the log-sum-exp rule, O = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r,
-// and writes the normalised output (and the LSE row). The CTA's threads form
-// NG groups of 32 GW, a thread owning dims 4 (t & 31) .. + 3 of head
-// (t mod 32 GW) / 32; group g folds records g, g + NG, ... (kMergeBatch at a
-// time, all loads of a batch in flight together), then the groups' partial
-// results are combined. Units one worker covered whole were written by the
-// decode kernel. All merges run in parallel, one small CTA each (several
-// fit next to each other on an SM, so they run in one wave).
+// combines the records listed for the unit (by the worker that held its
+// first block) with the log-sum-exp rule, O = sum_r 2^(m_r - M) O_r /
+// sum_r 2^(m_r - M) l_r, and writes the normalised output (and the LSE row).
+// The list is read together with its count, the records in one batch: two
+// dependent rounds of loads. The CTA's threads form NG groups of 32 GW, a
+// thread owning dims 4 (t & 31) .. + 3 of head (t mod 32 GW) / 32; group g
+// folds records g, g + NG, ..., then the groups' results are combined. All
+// merges run in parallel, one small CTA each (several fit on an SM).
 constexpr int kMergeBatch = 16;
 __host__ __device__ constexpr int merge_threads(int GH) {
   return 32 * (GH / mma_warps_per_kvhead(GH)) > 128 ? 32 * (GH / mma_warps_per_kvhead(GH)) : 128;
@@ -1208,56 +1254,35 @@ __global__ void __launch_bounds__(merge_threads(GH)) gqa_mma_merge_kernel(const 
   constexpr int TG = 32 * GW;                // threads per group
   constexpr int NG = merge_threads(GH) / TG; // groups
   constexpr int RR = NG * kMergeBatch;       // records per round
+  static_assert(RR <= merge_threads(GH), "one list entry per thread");
   __shared__ int64_t s_rec[RR];
   __shared__ float s_pm[NG][GW], s_pl[NG][GW];
   __shared__ float4 s_po[NG][TG];
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int B = p.batch;
   const int HN = p.n_chunks * p.n_hsub;
   const int nact = p.hc * HW;
   const int unit = static_cast<int>(blockIdx.x / nact), wi = static_cast<int>(blockIdx.x % nact);
   const int kh = wi / HW, hw = wi % HW;
   const int seq = unit / HN, idx = unit - seq * HN;
   const int chunk = idx / p.n_hsub, hsub = idx - chunk * p.n_hsub;
-  // the decode kernel's block prefixes over the batch (all blocks, dynamic ones)
-  const int* info = p.split_info;
-  const int pb0 = __ldcg(info + seq), pb1 = __ldcg(info + seq + 1), pbt = __ldcg(info + B);
-  const int pd0 = __ldcg(info + B + 1 + seq), pdt = __ldcg(info + 2 * B + 1);
-  const int nb = pb1 - pb0;
-  if (nb == 0) return;  // zero output, written by the decode kernel
-  const int dshare = p.dyn_chunk > 0 ? p.dyn_share : 0;
-  const MmaSplit sp = make_mma_split(static_cast<int64_t>(HN) * pbt, static_cast<int64_t>(HN) * pdt, p.split_ctas,
-                                     dshare, p.dyn_chunk, p.dyn_min_static);
-  const int d = sp.dyn(nb), s = nb - d;
-  const int64_t su0 = static_cast<int64_t>(HN) * (pb0 - (sp.share > 0 ? pd0 : 0)) + static_cast<int64_t>(idx) * s;
-  const int64_t c0 = sp.static_worker(su0), c1 = sp.static_worker(su0 + s - 1);
-  if (d == 0 && c0 == c1) return;  // one worker covered the unit whole
-  const int64_t du0 = static_cast<int64_t>(HN) * pd0 + static_cast<int64_t>(idx) * d;
-  const int64_t k0 = du0 / sp.C, k1 = d > 0 ? (du0 + d - 1) / sp.C : k0 - 1;
-  const int64_t ns = c1 - c0 + 1, R = ns + (k1 - k0 + 1);
-  // the record of contributor r (-1: an empty range). Every static range
-  // after c0 starts inside the unit (slot 2w) and, when N0 >= G, is non-empty;
-  // dynamic ranges start at k C.
-  auto record_of = [&](int64_t r) -> int64_t {
-    if (r < ns) {
-      if (r == 0) {
-        const int64_t s0 = sp.start(c0);
-        return c0 == c1 && su0 > s0 ? sp.interior(unit, false) : 2 * c0 + (su0 > s0 ? 1 : 0);
-      }
-      const int64_t wk = c0 + r;
-      return (sp.N0 >= sp.G || sp.start(wk) != sp.end(wk)) ? 2 * wk : -1;
-    }
-    const int64_t k = k0 + (r - ns);
-    const bool after = du0 > k * sp.C;
-    return k0 == k1 && after ? sp.interior(unit, true) : 2 * (sp.G + k) + (after ? 1 : 0);
-  };
-  const int t = threadIdx.x, g = t / TG, q = t - g * TG, h = q >> 5, q4 = q & 31;
+  const int* lst = p.unit_lists + static_cast<int64_t>(unit) * (1 + p.list_cap);
+  const int t = threadIdx.x;
+  // the count and the first round's entries together (entries past the count are ignored)
+  const int first = (t < RR && t < p.list_cap) ? __ldcg(lst + 1 + t) : -1;
+  int R = __ldcg(lst);
+  if (R <= 0) return;  // nothing to merge: the decode kernel wrote the output
+  R = R < p.list_cap ? R : p.list_cap;
+  const int g = t / TG, q = t - g * TG, h = q >> 5, q4 = q & 31;
   const int hr = kh * GH + hw * GW + h;  // the head's slot in a record
   float M = kNegInf, Ls = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int64_t base = 0; base < R; base += RR) {
-    __syncthreads();
-    if (t < RR) s_rec[t] = base + t < R ? record_of(base + t) : -1;
+  for (int base = 0; base < R; base += RR) {
+    if (base > 0) __syncthreads();
+    if (t < RR) {
+      const int e = base == 0 ? first : (base + t < R ? __ldcg(lst + 1 + base + t) : -1);
+      // a slot outside the workspace (a list left by a call that gave up) is skipped
+      s_rec[t] = (base + t < R && e >= 0 && e < p.rec_slots) ? e : -1;
+    }
     __syncthreads();
     float mr[kMergeBatch], lr[kMergeBatch];
     float4 ov[kMergeBatch];
