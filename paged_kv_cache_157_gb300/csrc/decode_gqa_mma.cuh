@@ -667,26 +667,30 @@ __device__ __forceinline__ int64_t unit_record(const UnitRecs& u, int64_t unit, 
 //
 // Offsets from a 1024-byte aligned base (the host adds 1024 bytes of slack
 // for the alignment). A stage is [K half 0][K half 1][V half 0][V half 1]
-// (each hc * block_size rows of 128 bytes, swizzled) followed by the unit's
-// query rows [hc][GH][128]; each stage has a 64-byte descriptor written by
-// the producer warp, a "full" barrier (the copies landed) and an "empty"
-// barrier (every consumer warp released it).
+// (each hc * block_size rows of 128 bytes, swizzled); each stage has a
+// 64-byte descriptor written by the producer warp, a "full" barrier (the
+// copies landed) and an "empty" barrier (every consumer warp released it).
+// A segment's query rows [hc][GH][128] arrive with its first stage (same
+// "full" barrier) in one of two query slots.
 
 struct GqaMmaSmem {
-  size_t box_bytes, stage_bytes, q_off, vs_off, meta_off, full_off, empty_off, iss_off, misc_off, scan_off, dscan_off,
-      total;
+  size_t box_bytes, stage_bytes, vs_off, q_off, q_slot_bytes, meta_off, full_off, empty_off, iss_off, misc_off,
+      scan_off, dscan_off, total;
 };
 
 // q8: one-byte caches, whose stage holds one K and one V box (128 codes per
-// row) and, after the query rows, the block's V scales [hc * block_size].
+// row) and the block's V scales [hc * block_size]. The query rows of a
+// segment go to one of two query slots after the ring (a segment's consumers
+// copy them into registers at its first stage).
 __host__ __device__ inline GqaMmaSmem gqa_mma_smem_layout(int q_elt, int GH, int block_size, int hc, int stages,
                                                           int batch, bool q8 = false) {
   GqaMmaSmem s;
   s.box_bytes = static_cast<size_t>(hc) * block_size * 128;
-  s.q_off = (q8 ? 2 : 4) * s.box_bytes;
-  s.vs_off = s.q_off + static_cast<size_t>(hc) * GH * 128 * q_elt;
+  s.vs_off = (q8 ? 2 : 4) * s.box_bytes;
   s.stage_bytes = align_up(s.vs_off + (q8 ? static_cast<size_t>(hc) * block_size * 4 : 0), 1024);
-  s.meta_off = static_cast<size_t>(stages) * s.stage_bytes;
+  s.q_slot_bytes = static_cast<size_t>(hc) * GH * 128 * q_elt;
+  s.q_off = static_cast<size_t>(stages) * s.stage_bytes;
+  s.meta_off = s.q_off + 2 * s.q_slot_bytes;
   s.full_off = s.meta_off + static_cast<size_t>(stages) * 64;
   s.empty_off = s.full_off + static_cast<size_t>(stages) * 8;
   s.iss_off = s.empty_off + static_cast<size_t>(stages) * 8;
@@ -711,7 +715,7 @@ struct StageMeta {
   int n_rows, r0;  // cached rows of the sequence, its first visible row
   int flags;
   int rec;         // record index of the segment (partial segments)
-  int pad;
+  int qslot;       // query slot holding the segment's query rows
 };
 constexpr int kFirst = 1, kLast = 2, kSrc = 4, kWhole = 8;
 
@@ -862,6 +866,15 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
     int64_t wk = c;
     uint32_t slot = 0, ph = 0;
     bool ok = true;
+    // Query slots: slot j was last filled with the first stage of the
+    // segment issued as position qpos_j (ring slot and phase in qsp_j).
+    // Reusing it for a new segment waits until that stage was released (its
+    // rows are in the consumers' registers by then); when S positions have
+    // been issued since, the ring order already guarantees it.
+    int64_t icount = 0;
+    int nseg = 0;
+    int64_t qpos0 = -(1ll << 40), qpos1 = -(1ll << 40);
+    uint32_t qsp0 = 0u, qsp1 = 0u;  // ring slot | phase << 16
     for (;;) {
       for (int64_t bpos = lo; ok && bpos < hi; bpos += 32) {
         const int64_t pos = bpos + lane;
@@ -903,7 +916,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
           mi.r0 = __shfl_sync(full, m.r0, i);
           mi.flags = __shfl_sync(full, m.flags, i);
           mi.rec = __shfl_sync(full, m.rec, i);
-          mi.pad = 0;
+          mi.qslot = 0;
           const int srci = __shfl_sync(full, src, i);
           const int qo = __shfl_sync(full, qoff, i);
           if (!p.unit_mode && wk < G && mi.u0 == bpos + i) {
@@ -918,7 +931,24 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
           }
           if (lane == 0) {
             ok = mbar_wait_data(ebar + slot, ph ^ 1u, p.wait_polls) && !*s_abort;
+            const int qj = nseg & 1;
+            const int64_t qp = qj ? qpos1 : qpos0;
+            const uint32_t qsp = qj ? qsp1 : qsp0;
+            if (ok && qo >= 0 && icount - qp < S)
+              ok = mbar_wait_data(ebar + (qsp & 0xffffu), qsp >> 16, p.wait_polls) && !*s_abort;
             if (ok) {
+              if (qo >= 0) {
+                ++nseg;
+                if (qj) {
+                  qpos1 = icount;
+                  qsp1 = slot | (ph << 16);
+                } else {
+                  qpos0 = icount;
+                  qsp0 = slot | (ph << 16);
+                }
+                mi.qslot = qj;
+              }
+              ++icount;
               if (srci < 0) set_flag(p.err, 0x1u);
               meta[slot] = mi;
               const uint32_t bytes = (srci >= 0 ? (Q8 ? 2 * box_bytes + vs_bytes : 4 * box_bytes) : 0u) +
@@ -943,7 +973,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
                   }
                 }
                 if (qo >= 0) {
-                  unsigned char* qdst = smem + slot * L.stage_bytes + L.q_off;
+                  unsigned char* qdst = smem + L.q_off + qj * L.q_slot_bytes;
                   if (multi) {
                     const int hs = qo % p.n_hsub, rest = qo / p.n_hsub;
                     const int ch = rest % p.n_chunks, sq = rest / p.n_chunks;
@@ -1027,7 +1057,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
       std::conditional_t<Q8 != 0, Q8WarpState, MmaWarpState> st;
       float qsc = p.qscale;
       {
-        const unsigned char* qs = smem + slot * L.stage_bytes + L.q_off +
+        const unsigned char* qs = smem + L.q_off + m.qslot * L.q_slot_bytes +
                                   static_cast<size_t>(kh * GH + hw * GW) * D * sizeof(T);
         if constexpr (Q8 == 0) {
 #pragma unroll
