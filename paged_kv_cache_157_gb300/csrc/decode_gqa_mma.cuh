@@ -503,18 +503,24 @@ struct MmaSplit {
   __device__ __forceinline__ int dyn(int nb) const {
     return static_cast<int>((static_cast<int64_t>(nb) * share) >> 8);
   }
+  // a / b for a, b >= 0, b > 0, with a 32-bit division when both fit
+  __device__ __forceinline__ static int64_t div(int64_t a, int64_t b) {
+    return (static_cast<uint64_t>(a | b) >> 32) == 0 ? static_cast<int64_t>(static_cast<uint32_t>(a) /
+                                                                             static_cast<uint32_t>(b))
+                                                     : a / b;
+  }
   __device__ __forceinline__ int64_t start(int64_t w) const {
-    if (w < G) return w * N0 / G;
+    if (w < G) return div(w * N0, G);
     const int64_t s = (w - G) * C;
     return s < Nd ? s : Nd;
   }
   __device__ __forceinline__ int64_t end(int64_t w) const {
-    if (w < G) return (w + 1) * N0 / G;
+    if (w < G) return div((w + 1) * N0, G);
     const int64_t e = (w - G + 1) * C;
     return e < Nd ? e : Nd;
   }
   // the static worker whose range holds static position b (N0 > 0)
-  __device__ __forceinline__ int64_t static_worker(int64_t b) const { return ((b + 1) * G - 1) / N0; }
+  __device__ __forceinline__ int64_t static_worker(int64_t b) const { return div((b + 1) * G - 1, N0); }
   // record slot of worker w for the unit part that starts at u0 (in w's space)
   // and does not lie strictly inside w's range
   __device__ __forceinline__ int64_t record(int64_t w, int64_t u0) const { return 2 * w + (u0 > start(w) ? 1 : 0); }
@@ -638,8 +644,8 @@ __device__ __forceinline__ UnitRecs unit_recs(int seq, int idx, const MmaSplit& 
   u.c0 = sp.static_worker(u.su0);
   u.c1 = sp.static_worker(u.su0 + s - 1);
   u.du0 = static_cast<int64_t>(HN) * dpre + static_cast<int64_t>(idx) * d;
-  u.k0 = u.du0 / sp.C;
-  u.k1 = d > 0 ? (u.du0 + d - 1) / sp.C : u.k0 - 1;
+  u.k0 = MmaSplit::div(u.du0, sp.C);
+  u.k1 = d > 0 ? MmaSplit::div(u.du0 + d - 1, sp.C) : u.k0 - 1;
   u.ns = u.c1 - u.c0 + 1;
   u.R = u.ns + (u.k1 - u.k0 + 1);
   u.whole = d == 0 && u.c0 == u.c1;
@@ -820,7 +826,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
   // The work split (every CTA computes the same one). In the unit mode CTA u
   // takes unit u whole and nothing is claimed.
   const int dshare = (!p.unit_mode && p.dyn_chunk > 0) ? p.dyn_share : 0;
-  scan_dyn(B, dshare, s_scan, s_dscan);  // ends with a CTA barrier
+  if (dshare > 0) scan_dyn(B, dshare, s_scan, s_dscan);  // ends with a CTA barrier; unused without a share
   MmaSplit sp;
   int64_t lo, hi;
   if (p.unit_mode) {
@@ -844,7 +850,8 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
     lo = static_cast<int64_t>(HN) * s_scan[seq] + static_cast<int64_t>(idx) * nb;
     hi = lo + nb;
   } else {
-    sp = make_mma_split(N, static_cast<int64_t>(HN) * s_dscan[B], G, dshare, p.dyn_chunk, p.dyn_min_static);
+    sp = make_mma_split(N, dshare > 0 ? static_cast<int64_t>(HN) * s_dscan[B] : 0, G, dshare, p.dyn_chunk,
+                        p.dyn_min_static);
     lo = sp.start(c);
     hi = sp.end(c);
   }
@@ -919,16 +926,6 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
           mi.qslot = 0;
           const int srci = __shfl_sync(full, src, i);
           const int qo = __shfl_sync(full, qoff, i);
-          if (!p.unit_mode && wk < G && mi.u0 == bpos + i) {
-            // the unit's first block: publish its record list for the merge
-            const int uidx = mi.chunk * p.n_hsub + mi.hsub;
-            const int64_t unit = static_cast<int64_t>(mi.seq) * HN + uidx;
-            const UnitRecs u = unit_recs(mi.seq, uidx, sp, HN, s_scan, s_dscan);
-            int* lst = p.unit_lists + unit * (1 + p.list_cap);
-            const int R = u.whole ? 0 : static_cast<int>(u.R < p.list_cap ? u.R : p.list_cap);
-            for (int r = lane; r < R; r += 32) lst[1 + r] = static_cast<int>(unit_record(u, unit, sp, r));
-            if (lane == 0) lst[0] = R;
-          }
           if (lane == 0) {
             ok = mbar_wait_data(ebar + slot, ph ^ 1u, p.wait_polls) && !*s_abort;
             const int qj = nseg & 1;
@@ -1003,6 +1000,17 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
           }
           ok = __shfl_sync(full, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
+          if (!p.unit_mode && wk < G && mi.u0 == bpos + i) {
+            // the unit's first block: publish its record list for the merge
+            // (after the copies are on their way)
+            const int uidx = mi.chunk * p.n_hsub + mi.hsub;
+            const int64_t unit = static_cast<int64_t>(mi.seq) * HN + uidx;
+            const UnitRecs u = unit_recs(mi.seq, uidx, sp, HN, s_scan, s_dscan);
+            int* lst = p.unit_lists + unit * (1 + p.list_cap);
+            const int R = u.whole ? 0 : static_cast<int>(u.R < p.list_cap ? u.R : p.list_cap);
+            for (int r = lane; r < R; r += 32) lst[1 + r] = static_cast<int>(unit_record(u, unit, sp, r));
+            if (lane == 0) lst[0] = R;
+          }
           if (++slot == static_cast<uint32_t>(S)) {
             slot = 0;
             ph ^= 1u;
