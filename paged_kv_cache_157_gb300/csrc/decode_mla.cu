@@ -39,8 +39,9 @@
 //   while the softmax runs; S(t+2) reuses the buffer of P(t) once PV(t) is done.
 // * Work split: as in the GQA kernel, the tiles of all sequences are laid end
 //   to end and CTA pair c takes a contiguous range; a sequence cut by a range
-//   boundary leaves fp32 records (m, l, O) and the last contributing CTA of
-//   each (sequence, half) merges them with the log-sum-exp rule.
+//   boundary leaves fp32 records (m, l, O), the CTA holding its first tile
+//   lists them, and a merge kernel launched right behind this one combines
+//   every (sequence, half) with the log-sum-exp rule, all in parallel.
 // * Every mbarrier wait is bounded; a wait that gives up sets the error word
 //   and a shared abort flag that stops every role, which then drains and
 //   frees TMEM.
@@ -103,9 +104,7 @@ enum {
   B_PFULL0 = B_SFULL0 + kSPBufs, B_PEMPTY0 = B_PFULL0 + kSPBufs, B_OFREE = B_PEMPTY0 + kSPBufs, B_FINAL, B_COUNT
 };
 constexpr uint32_t kOffMisc = kOffBar + B_COUNT * 8;  // tmem address, abort flag, last flag
-constexpr int kMergeChunk = 32;  // record slots the merging warpgroup lists in shared memory at a time
-constexpr uint32_t kOffRec = kOffMisc + 16;
-constexpr uint32_t kOffScan = kOffRec + kMergeChunk * 4;
+constexpr uint32_t kOffScan = kOffMisc + 16;
 constexpr uint32_t smem_bytes(int batch) { return kOffScan + (batch + 1 + 32) * 4; }
 
 struct Params {
@@ -115,7 +114,9 @@ struct Params {
   void* out;
   float* rec_o;   // [G * 2, 128, 256]
   float* rec_ml;  // [G * 2, 128, 2]
-  unsigned int* counters;  // [batch * 2]
+  int* unit_lists;  // per (sequence, half): [record count (0: written whole)][record slots 0 .. list_cap-1]
+  int list_cap;
+  int64_t rec_slots;
   unsigned int* err;
   int64_t num_blocks;
   int batch;
@@ -454,7 +455,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(sm + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
-  volatile int* s_last = reinterpret_cast<volatile int*>(sm + kOffMisc + 8);
   int* s_scan = reinterpret_cast<int*>(sm + kOffScan);
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
 
@@ -517,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (any_bad) {
     for (int b = 0; b < p.batch; ++b) {
       if (__ldg(p.context_lens + b) >= 1) continue;
+      if (!p.unit_mode && tid == 0) p.unit_lists[static_cast<int64_t>(b * 2 + hf) * (1 + p.list_cap)] = 0;
       for (int idx = tid; idx < kHeads * kHalf; idx += blockDim.x) {
         const int h = idx / kHalf, d = idx % kHalf;
         store_out(p.out, (static_cast<int64_t>(b) * kHeads + h) * kDc + hf * kHalf + d, 0.f, p.out_dtype);
@@ -868,154 +869,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_before();
       __syncwarp();
       if (lane == 0) arrive(bar(B_OFREE));
-      if (!whole) {
-        // count this record; the last contributor merges (softmax warpgroup only)
-        __threadfence();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (!p.unit_mode && sg.t0 == 0) {
+        // the CTA holding the unit's first tile lists its records for the merge kernel
         const int64_t c0 = pair_of(sg.u0, G, N_all), c1 = pair_of(sg.u0 + sg.ntiles - 1, G, N_all);
-        const int64_t unit = static_cast<int64_t>(sg.seq) * 2 + hf;
-        if (tid == 0) {
-          int contributors = 0;
-          for (int64_t c = c0; c <= c1; ++c)
-            contributors += (range_start(c, G, N_all) != range_start(c + 1, G, N_all)) ? 1 : 0;
-          const unsigned int old = atomicAdd(p.counters + unit, 1u);
-          *s_last = 0;
-          if (old + 1 == static_cast<unsigned int>(contributors)) {
-            *s_last = 1;
-          } else if (old + 1 > static_cast<unsigned int>(contributors)) {
-            set_flag(p.err, 0x10u);
-            atomicExch(p.counters + unit, 0u);
-          }
+        int* lst = p.unit_lists + (static_cast<int64_t>(sg.seq) * 2 + hf) * (1 + p.list_cap);
+        const int64_t span = c1 - c0 + 1;
+        const int R = whole ? 0 : static_cast<int>(span < p.list_cap ? span : p.list_cap);
+        for (int r = tid; r < R; r += 128) {
+          const int64_t c = c0 + r;
+          const int64_t f0 = range_start(c, G, N_all);
+          lst[1 + r] = (f0 == range_start(c + 1, G, N_all)) ? -1
+                                                              : static_cast<int>((c * 2 + hf) * 2 + ((sg.u0 > f0) ? 1 : 0));
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (*s_last) {
-          __threadfence();
-          // Merge the unit's records with the log-sum-exp rule. The record
-          // slots of the contributors are listed in shared memory (kMergeChunk
-          // at a time, computed in parallel); pass 1 gives every head (thread
-          // h) its maximum and sum, pass 2 its output row.
-          int* s_rec = reinterpret_cast<int*>(sm + kOffRec);
-          const int span = static_cast<int>(c1 - c0 + 1);
-          auto list_records = [&](int base, int nc) {
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // earlier readers of the list are done
-            if (tid < nc) {
-              const int64_t c = c0 + base + tid;
-              const int64_t f0 = range_start(c, G, N_all);
-              s_rec[tid] = (f0 == range_start(c + 1, G, N_all))
-                               ? -1
-                               : static_cast<int>((c * 2 + hf) * 2 + ((sg.u0 > f0) ? 1 : 0));
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-          };
-          float M = -__builtin_huge_valf(), L = 0.f;
-          for (int base = 0; base < span; base += kMergeChunk) {
-            const int nc = min(kMergeChunk, span - base);
-            list_records(base, nc);
-#pragma unroll 4
-            for (int i = 0; i < nc; ++i) {
-              const int rs = s_rec[i];
-              if (rs < 0) continue;
-              const int64_t r = static_cast<int64_t>(rs) * kHeads + h;
-              const float mc = __ldcg(p.rec_ml + r * 2), lc = __ldcg(p.rec_ml + r * 2 + 1);
-              if (mc == -__builtin_huge_valf()) continue;
-              const float mn = fmaxf(M, mc);
-              L = L * fast_exp2(M - mn) + lc * fast_exp2(mc - mn);  // M = -inf: L is 0 and stays 0
-              M = mn;
-            }
-          }
-          const float invL = 1.0f / L;
-          if (span <= 4) {
-            // Pass 2, the common case (at most 4 contributors, all listed):
-            // thread h first takes f_i = 2^(m_i - M) of its own head for
-            // every record i; then each warp writes its 32 heads' rows, 4
-            // heads at a time, every load independent of the others and
-            // coalesced (lane L reads floats 4L..4L+3 and 128+4L..131+4L of a
-            // record row).
-            float f[4];
-            int rsv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              rsv[i] = i < span ? s_rec[i] : -1;
-              f[i] = 0.f;
-              if (rsv[i] >= 0) {
-                const float mc = __ldcg(p.rec_ml + (static_cast<int64_t>(rsv[i]) * kHeads + h) * 2);
-                f[i] = (mc == -__builtin_huge_valf()) ? 0.f : fast_exp2(mc - M);
-              }
-            }
-            for (int hb = 0; hb < 32; hb += 4) {
-              float4 a[4][2];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) a[k][0] = a[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                if (rsv[i] < 0) continue;  // uniform: s_rec is shared
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const int hj = warp * 32 + hb + k;
-                  const float fk = __shfl_sync(0xffffffffu, f[i], hb + k);
-                  const float4* src =
-                      reinterpret_cast<const float4*>(p.rec_o + (static_cast<int64_t>(rsv[i]) * kHeads + hj) * kHalf);
-                  const float4 x0 = __ldcg(src + lane), x1 = __ldcg(src + 32 + lane);
-                  a[k][0].x += fk * x0.x;
-                  a[k][0].y += fk * x0.y;
-                  a[k][0].z += fk * x0.z;
-                  a[k][0].w += fk * x0.w;
-                  a[k][1].x += fk * x1.x;
-                  a[k][1].y += fk * x1.y;
-                  a[k][1].z += fk * x1.z;
-                  a[k][1].w += fk * x1.w;
-                }
-              }
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float iL = __shfl_sync(0xffffffffu, invL, hb + k);
-                const int64_t o = (static_cast<int64_t>(sg.seq) * kHeads + warp * 32 + hb + k) * kDc + hf * kHalf;
-                const float v0[4] = {a[k][0].x * iL, a[k][0].y * iL, a[k][0].z * iL, a[k][0].w * iL};
-                const float v1[4] = {a[k][1].x * iL, a[k][1].y * iL, a[k][1].z * iL, a[k][1].w * iL};
-                store_out_vec<4>(p.out, o + 4 * lane, v0, p.out_dtype);
-                store_out_vec<4>(p.out, o + 128 + 4 * lane, v1, p.out_dtype);
-              }
-            }
-          } else {
-            // Pass 2: thread h writes its own head's 256 outputs, 64 at a time;
-            // every record's 64-float run (256 contiguous bytes) is loaded
-            // before any is used, so one round trip serves all records.
-            for (int c = 0; c < kHalf; c += 64) {
-              float acc[64];
-#pragma unroll
-              for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-              for (int base = 0; base < span; base += kMergeChunk) {
-                const int nc = min(kMergeChunk, span - base);
-                if (span > kMergeChunk) list_records(base, nc);  // uniform over the warpgroup
-#pragma unroll 2
-                for (int i = 0; i < nc; ++i) {
-                  const int rs = s_rec[i];
-                  if (rs < 0) continue;
-                  const int64_t r = static_cast<int64_t>(rs) * kHeads + h;
-                  const float mc = __ldcg(p.rec_ml + r * 2);
-                  const float4* srcp = reinterpret_cast<const float4*>(p.rec_o + r * kHalf + c);
-                  float4 x[16];
-#pragma unroll
-                  for (int k = 0; k < 16; ++k) x[k] = __ldcg(srcp + k);
-                  const float f = (mc == -__builtin_huge_valf()) ? 0.f : fast_exp2(mc - M);
-#pragma unroll
-                  for (int k = 0; k < 16; ++k) {
-                    acc[4 * k] += f * x[k].x;
-                    acc[4 * k + 1] += f * x[k].y;
-                    acc[4 * k + 2] += f * x[k].z;
-                    acc[4 * k + 3] += f * x[k].w;
-                  }
-                }
-              }
-#pragma unroll
-              for (int i = 0; i < 64; ++i) acc[i] *= invL;
-              const int64_t o = (static_cast<int64_t>(sg.seq) * kHeads + h) * kDc + hf * kHalf + c;
-#pragma unroll
-              for (int i = 0; i < 64; i += 8) store_out_vec<8>(p.out, o + i, acc + i, p.out_dtype);
-            }
-          }
-          if (tid == 0) p.counters[unit] = 0u;
-        }
+        if (tid == 0) lst[0] = R;
       }
       ++seg_i;
     }
@@ -1027,6 +893,98 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 5) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
+}
+
+// ------------------------------------------------------------------ merge
+//
+// One CTA per (sequence, half, group of 8 heads), launched behind the decode
+// kernel: thread t takes dims 16 (t & 15) .. + 15 of head 8 g + t / 16 of the
+// half and folds the unit's records, listed by the CTA that held its first
+// tile, with the log-sum-exp rule (the count and the first list entries are
+// read together, then kMergeBatch records at a time; a sequence has only a
+// few contributors).
+constexpr int kMergeBatch = 4;
+constexpr int kMergeGroups = kHeads / 8;
+
+__global__ void __launch_bounds__(128) mla_merge_kernel(const Params p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int unit = static_cast<int>(blockIdx.x / kMergeGroups), hg = static_cast<int>(blockIdx.x % kMergeGroups);
+  const int seq = unit >> 1, hf = unit & 1;
+  const int t = threadIdx.x;
+  const int* lst = p.unit_lists + static_cast<int64_t>(unit) * (1 + p.list_cap);
+  const int first = (t < kMergeBatch && t < p.list_cap) ? __ldcg(lst + 1 + t) : -1;
+  int R = __ldcg(lst);
+  if (R <= 0) return;
+  R = R < p.list_cap ? R : p.list_cap;
+  __shared__ int s_rec[kMergeBatch];
+  const int h = hg * 8 + (t >> 4), q = t & 15;
+  float M = -__builtin_huge_valf(), L = 0.f;
+  float4 O[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) O[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < R; base += kMergeBatch) {
+    if (base > 0) __syncthreads();
+    if (t < kMergeBatch) {
+      const int e = base == 0 ? first : (base + t < R ? __ldcg(lst + 1 + base + t) : -1);
+      s_rec[t] = (base + t < R && e >= 0 && e < p.rec_slots) ? e : -1;
+    }
+    __syncthreads();
+    float mr[kMergeBatch], lr[kMergeBatch];
+    float4 x[kMergeBatch][4];
+#pragma unroll
+    for (int i = 0; i < kMergeBatch; ++i) {
+      const int rs = s_rec[i];
+      mr[i] = -__builtin_huge_valf();
+      lr[i] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) x[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (rs >= 0) {
+        const int64_t r = static_cast<int64_t>(rs) * kHeads + h;
+        mr[i] = __ldcg(p.rec_ml + r * 2);
+        lr[i] = __ldcg(p.rec_ml + r * 2 + 1);
+        const float4* src = reinterpret_cast<const float4*>(p.rec_o + r * kHalf) + 4 * q;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[i][k] = __ldcg(src + k);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMergeBatch; ++i) {
+      if (mr[i] == -__builtin_huge_valf()) continue;
+      if (mr[i] > M) {
+        const float sc = M == -__builtin_huge_valf() ? 0.f : fast_exp2(M - mr[i]);
+        L *= sc;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          O[k].x *= sc;
+          O[k].y *= sc;
+          O[k].z *= sc;
+          O[k].w *= sc;
+        }
+        M = mr[i];
+      }
+      const float f = fast_exp2(mr[i] - M);
+      L += f * lr[i];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        O[k].x += f * x[i][k].x;
+        O[k].y += f * x[i][k].y;
+        O[k].z += f * x[i][k].z;
+        O[k].w += f * x[i][k].w;
+      }
+    }
+  }
+  const float inv = 1.0f / L;
+  float v[16];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v[4 * k] = O[k].x * inv;
+    v[4 * k + 1] = O[k].y * inv;
+    v[4 * k + 2] = O[k].z * inv;
+    v[4 * k + 3] = O[k].w * inv;
+  }
+  const int64_t o = (static_cast<int64_t>(seq) * kHeads + h) * kDc + hf * kHalf + 16 * q;
+  store_out_vec<8>(p.out, o, v, p.out_dtype);
+  store_out_vec<8>(p.out, o + 8, v + 8, p.out_dtype);
 }
 
 // ------------------------------------------------------------------- host
@@ -1056,7 +1014,10 @@ int plan_pairs(const DeviceInfo* dev, int batch, int max_blocks, int block_size)
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(G2, 1 << 20)));
 }
 
-size_t counter_bytes(int batch) { return (static_cast<size_t>(batch) * 2 * 4 + 255) / 256 * 256; }
+// Per (sequence, half): the record count and up to G2 record slots.
+size_t list_bytes(int batch, int G2) {
+  return (static_cast<size_t>(batch) * 2 * (1 + static_cast<size_t>(G2)) * 4 + 255) / 256 * 256;
+}
 size_t record_bytes_per_pair() { return 2ull * 2 * kHeads * (kHalf + 2) * sizeof(float); }
 
 kvc_status check(int batch, int n_q_heads, int d_c, int d_r, int block_size, int max_blocks) {
@@ -1085,7 +1046,7 @@ kvc_status kvc_decode_mla_workspace_size(int batch, int n_q_heads, int d_c, int 
   DeviceInfo* dev = nullptr;
   if ((s = current_device(&dev)) != KVC_OK) return s;
   const int G2 = mla::plan_pairs(dev, batch, max_blocks_per_seq, block_size);
-  *bytes = mla::counter_bytes(batch) + static_cast<size_t>(G2) * mla::record_bytes_per_pair();
+  *bytes = mla::list_bytes(batch, G2) + static_cast<size_t>(G2) * mla::record_bytes_per_pair();
   return KVC_OK;
 }
 
@@ -1158,14 +1119,16 @@ kvc_status kvc_decode_attention_mla(const void* q_absorbed, const void* latent_c
   p.out_dtype = static_cast<int>(out_dtype);
   p.qscale = scale * 1.4426950408889634f;
   int G2 = mla::plan_pairs(dev, batch, max_blocks_per_seq, block_size);
-  const size_t cb = mla::counter_bytes(batch);
+  const size_t cb = mla::list_bytes(batch, G2);
   const int64_t fit = workspace_bytes > cb ? static_cast<int64_t>((workspace_bytes - cb) / mla::record_bytes_per_pair()) : 0;
   if (fit >= 1) {
+    p.list_cap = G2;
     G2 = static_cast<int>(std::min<int64_t>(G2, fit));
     p.unit_mode = 0;
-    p.counters = static_cast<unsigned int*>(workspace);
+    p.unit_lists = static_cast<int*>(workspace);
     p.rec_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + cb);
     p.rec_ml = p.rec_o + static_cast<size_t>(G2) * 2 * 2 * mla::kHeads * mla::kHalf;
+    p.rec_slots = static_cast<int64_t>(G2) * 4;
   } else {
     p.unit_mode = 1;
     G2 = batch;
@@ -1187,6 +1150,17 @@ kvc_status kvc_decode_attention_mla(const void* q_absorbed, const void* latent_c
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel, tq, tc, p);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(mla)");
+  if (!p.unit_mode) {
+    // the merge of split sequences, right behind (it waits for the decode grid)
+    cudaLaunchConfig_t mcfg = {};
+    mcfg.gridDim = dim3(static_cast<unsigned int>(batch) * 2 * mla::kMergeGroups);
+    mcfg.blockDim = dim3(128);
+    mcfg.stream = st;
+    mcfg.attrs = attr;
+    mcfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&mcfg, mla::mla_merge_kernel, p);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(mla merge)");
+  }
   return finish_call(st);
 }
 
