@@ -369,14 +369,24 @@ __device__ __forceinline__ int seq_rows(const int32_t* lens, int b, int bs, int 
   return n < cap ? n : cap;
 }
 
-// Exclusive prefix sums of tiles per sequence (whole CTA participates).
+// Split positions a sequence occupies ahead of its tiles. Starting a segment
+// (loading Q~, refilling the tile pipeline, writing the segment's output)
+// costs about as much as 6 tiles (per-CTA timestamps: CTA pairs whose range
+// held 1, 2 and 3 segments finished at ~186, ~198 and ~207 us on the
+// DeepSeek-V2 batch), so each sequence start counts as 6 positions of the
+// balanced split; positions that are no tile carry no work.
+constexpr int kSegCost = 6;
+
+// Exclusive prefix sums of split positions per sequence: its tiles plus
+// kSegCost (whole CTA participates).
 __device__ inline void scan_tiles(const int32_t* lens, int B, int bs, int max_blocks, int* s_scan) {
   const int tid = threadIdx.x;
   if (tid < 32) {
     int run = 0;
     for (int base = 0; base < B; base += 32) {
       const int b = base + tid;
-      const int v = b < B ? seq_tiles(lens, b, bs, max_blocks) : 0;
+      const int nt = b < B ? seq_tiles(lens, b, bs, max_blocks) : 0;
+      const int v = nt > 0 ? nt + kSegCost : 0;
       int x = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -397,7 +407,7 @@ __device__ __forceinline__ int64_t pair_of(int64_t t, int64_t G, int64_t N) { re
 // A contiguous run of tiles of one sequence handled by this CTA.
 struct Segment {
   int seq, t0, t1, ntiles;  // tiles [t0, t1) of the sequence's ntiles
-  int64_t u0;               // global index of the sequence's first tile
+  int64_t u0;               // split position of the sequence's first tile
   int which;                // record slot (0: segment starts the CTA range)
 };
 
@@ -424,8 +434,12 @@ struct Walker {
       if (s_scan[mid] <= pos) a = mid; else b = mid - 1;
     }
     sg.seq = a;
-    sg.ntiles = s_scan[a + 1] - s_scan[a];
-    sg.u0 = s_scan[a];
+    sg.u0 = s_scan[a] + kSegCost;  // the positions before it are no tiles
+    sg.ntiles = static_cast<int>(s_scan[a + 1] - sg.u0);
+    if (pos < sg.u0) {
+      pos = sg.u0;
+      if (pos >= hi) return false;
+    }
     sg.t0 = static_cast<int>(pos - sg.u0);
     const int64_t end = sg.u0 + sg.ntiles < hi ? sg.u0 + sg.ntiles : hi;
     sg.t1 = static_cast<int>(end - sg.u0);
