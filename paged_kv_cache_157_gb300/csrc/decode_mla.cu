@@ -718,52 +718,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     Segment sg;
     Walker w = walk;
     bool ok = true;
-    while (ok && w.next(p, s_scan, sg)) {
-      if (sg.ntiles == 0) continue;
-      const int n_rows = seq_rows(p.context_lens, sg.seq, p.block_size, p.max_blocks);
-      // Columns [0, 256) of this head's Q~ row go to TMEM (the A operand of the
-      // first 16 K steps of S), once the previous segment's S MMAs are done.
-      {
-        const bool got = seg_i == 0 ||
-                         __all_sync(0xffffffffu, wait_phase(bar(B_QEMPTY), (seg_i - 1) & 1u, s_abort, p.err));
-        if (block_any128(!got || *s_abort)) {
-          ok = false;
-          break;
-        }
-      }
+    // Columns [0, 320) of this head's Q~ row for segment number si (sequence
+    // seq) go to TMEM (the A operand of the first 20 K steps of S), once the
+    // previous segment's S MMAs are done: 40 16-byte loads issued in two
+    // batches (one round trip each) before the TMEM stores. Returns false on
+    // a failed wait (every warp of the group sees the same result).
+    auto load_q = [&](uint32_t si, int seq) -> bool {
+      const bool got = si == 0 || __all_sync(0xffffffffu, wait_phase(bar(B_QEMPTY), (si - 1) & 1u, s_abort, p.err));
+      if (block_any128(!got || *s_abort)) return false;
       fence_after();
-      {
-        // This head's Q~ columns [0, 320): 40 16-byte loads issued in two
-        // batches (one round trip each) before the TMEM stores.
-        const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(sg.seq) * kHeads + h) * kW);
+      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(seq) * kHeads + h) * kW);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[80];
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[80];
 #pragma unroll
-          for (int i = 0; i < 20; ++i) {
-            const uint4 x = __ldg(qrow + half * 20 + i);
-            r[4 * i] = x.x;
-            r[4 * i + 1] = x.y;
-            r[4 * i + 2] = x.z;
-            r[4 * i + 3] = x.w;
-          }
-          tmem_st32u(lane_addr + kColQ + half * 80, r);
-          tmem_st32u(lane_addr + kColQ + half * 80 + 32, r + 32);
-          tmem_st16u(lane_addr + kColQ + half * 80 + 64, r + 64);
+        for (int i = 0; i < 20; ++i) {
+          const uint4 x = __ldg(qrow + half * 20 + i);
+          r[4 * i] = x.x;
+          r[4 * i + 1] = x.y;
+          r[4 * i + 2] = x.z;
+          r[4 * i + 3] = x.w;
         }
-        // Warm L2 with the next segment's rows (this CTA's walk is known), so
-        // its start costs two L2 round trips instead of two DRAM ones.
-        Walker wn = w;
-        Segment sn;
-        if (wn.next(p, s_scan, sn) && sn.ntiles > 0) {
-          const char* nrow = reinterpret_cast<const char*>(p.q + (static_cast<int64_t>(sn.seq) * kHeads + h) * kW);
-#pragma unroll
-          for (int i = 0; i < 5; ++i) prefetch_l2(nrow + 128 * i);
-        }
+        tmem_st32u(lane_addr + kColQ + half * 80, r);
+        tmem_st32u(lane_addr + kColQ + half * 80 + 32, r + 32);
+        tmem_st16u(lane_addr + kColQ + half * 80 + 64, r + 64);
       }
       fence_before();
       __syncwarp();
       if (lane == 0) arrive(bar(B_QFULL));
+      return true;
+    };
+    bool have_q = false;  // this segment's Q~ was loaded during the previous segment's epilogue
+    while (ok && w.next(p, s_scan, sg)) {
+      if (sg.ntiles == 0) continue;
+      const int n_rows = seq_rows(p.context_lens, sg.seq, p.block_size, p.max_blocks);
+      if (!have_q && !load_q(seg_i, sg.seq)) {
+        ok = false;
+        break;
+      }
+      have_q = false;
+      // the segment after this one (this CTA's walk is known)
+      Walker wn = w;
+      Segment sn;
+      bool has_next = false;
+      while (wn.next(p, s_scan, sn)) {
+        if (sn.ntiles > 0) {
+          has_next = true;
+          break;
+        }
+      }
+      if (has_next) {
+        // warm L2 with its rows, so that its Q~ load costs L2 round trips
+        const char* nrow = reinterpret_cast<const char*>(p.q + (static_cast<int64_t>(sn.seq) * kHeads + h) * kW);
+#pragma unroll
+        for (int i = 0; i < 5; ++i) prefetch_l2(nrow + 128 * i);
+      }
       float m = -__builtin_huge_valf(), l = 0.f;
       const uint32_t g_first = g;
       for (int t = sg.t0; t < sg.t1; ++t, ++g) {
@@ -845,6 +854,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_before();
         __syncwarp();
         if (lane == 0) arrive(bar(B_PFULL0 + pb));
+      }
+      // The next segment's Q~ goes to TMEM before this epilogue, so that its
+      // first S products run while the output is read out and stored.
+      if (ok && has_next) {
+        if (!load_q(seg_i + 1, sn.seq)) {
+          ok = false;
+          break;
+        }
+        have_q = true;
       }
       // ---- epilogue: wait for the last PV, read O, write output or record
       {
