@@ -18,7 +18,7 @@ import torch
 from oracle import paged as OP
 from paged_kv_cache_157_gb300 import workloads as W
 
-from gpu_helpers import TOL, device_case, f64, max_err, oracle_decode, run_decode
+from gpu_helpers import TOL, device_case, f64, max_err, oracle_decode, oracle_decode_sampled, run_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -219,8 +219,10 @@ def test_dynamic_work_split(kvc, chunk, share, max_ctas):
 
 
 def test_dynamic_split_on_large_batch(kvc):
-    # the automatic split (a quarter of the blocks claimed in chunks of 8) on a
-    # batch large enough to use it, sampled against the oracle
+    # a quarter of every unit's blocks claimed in chunks of 8 on a large batch,
+    # three calls on one workspace (the claim counter resets itself)
+    kvc.set_option(kvc.OPT_DYNAMIC_SHARE, 64)
+    kvc.set_option(kvc.OPT_DYNAMIC_CHUNK, 8)
     case = W.gqa_case(16, 32, 8, 128, 16, (1024, 4096), "bf16", seed=117)
     dev = device_case(case)
     ws = kvc.new_decode_workspace(16, 32, 8, 128, 16, case["block_tables"].shape[1])
@@ -228,4 +230,18 @@ def test_dynamic_split_on_large_batch(kvc):
     ref = oracle_decode(case, 1.0 / math.sqrt(128))
     for o in outs:
         assert max_err(o, ref) <= TOL["bf16"]
+    assert kvc.get_error_flags() == 0
+
+
+def test_one_long_sequence_many_contributors(kvc):
+    # one sequence of 32768 rows with 8 queries per kv head: a single unit cut
+    # into every CTA's range, so its merge folds ~150 records in several rounds
+    case = W.gqa_case(1, 64, 8, 128, 16, [32768], "bf16", seed=118)
+    dev = device_case(case)
+    scale = 1.0 / math.sqrt(128)
+    out = run_decode(kvc, dev, scale)
+    ref = oracle_decode_sampled(case, scale, [(0, h) for h in (0, 7, 8, 31, 56, 63)])
+    for (i, h), r in ref.items():
+        assert float(np.max(np.abs(f64(out[i, h]) - r))) <= TOL["bf16"]
+    assert torch.isfinite(out).all()
     assert kvc.get_error_flags() == 0
