@@ -31,12 +31,14 @@ struct GqaPlan {
   int dyn_share = 0, dyn_chunk = 0;  // warp-MMA kernel: dynamic tail of the work split
   int64_t units = 0;
   size_t smem = 0;
-  size_t rec_bytes_per_cta = 0;  // two records per CTA
+  size_t rec_bytes_per_cta = 0;  // two records per CTA (per worker on the warp-MMA kernel)
 };
 
-// Workspace layout: [counters, one per unit and warp slot][record
-// outputs][record (max, sum)]. A unit of hc kv heads has hc * HW warp slots, so
-// batch * n_kv_heads * n_hsub * HW counters cover every plan.
+// Workspace layout of the CUDA-core kernel: [counters, one per unit and warp
+// slot][record outputs][record (max, sum)]. A unit of hc kv heads has hc * HW
+// warp slots, so batch * n_kv_heads * n_hsub * HW counters cover every plan.
+// (The warp-MMA kernel: [claim counter][unit record lists][records], see
+// mma_counter_bytes.)
 size_t counter_bytes(int batch, int n_kv_heads, const GqaPlan& pl) {
   return align_up(static_cast<size_t>(batch) * n_kv_heads * pl.n_hsub * gqa_warps_per_kvhead(pl.GH) * 4, 256);
 }

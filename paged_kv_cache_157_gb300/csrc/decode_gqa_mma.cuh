@@ -28,8 +28,10 @@
 // Pages reach shared memory by TMA tensor copies (a 2-D map over the pool as
 // [num_blocks * n_kv_heads * block_size rows, 128]) in [hc * block_size rows x
 // 64 dims] boxes with the 128-byte swizzle, so every 8x8 matrix load touches
-// eight different bank groups. Work split, split-K records, the last-arriver
-// merge and the bounded waits are those of the CUDA-core kernel.
+// eight different bank groups. Positions are split over the CTAs in static
+// ranges (optionally with claimed chunks at every unit's tail); segments that
+// cover part of a unit leave fp32 records, which a merge kernel launched
+// behind this one combines, all units in parallel. Every wait is bounded.
 //
 // One-byte caches (e4m3 or int8 codes with per-channel K scales and per-token
 // V scales, bf16 queries) use the same loop on f16 MMAs: every code is an f16
@@ -533,7 +535,7 @@ struct MmaSplit {
 
 // N: all positions, Nd: the dynamic ones under `share`. The dynamic share is
 // kept only when every CTA still gets at least min_static static positions;
-// every CTA (and the merge kernel) computes the same split.
+// every CTA computes the same split.
 __device__ __forceinline__ MmaSplit make_mma_split(int64_t N, int64_t Nd, int64_t G, int share, int chunk,
                                                    int min_static) {
   MmaSplit s;
