@@ -533,6 +533,25 @@ struct MmaSplit {
   }
 };
 
+// scan_blocks for a batch of at most 32 sequences: warp 0 computes the
+// exclusive prefix sums s_scan[0..B] with shuffles, and one CTA barrier
+// publishes them.
+__device__ inline void scan_blocks_warp(const int32_t* lens, int B, int bs, int max_blocks, int window, int min_len,
+                                        const int32_t* row_start, int row_div, int* s_scan) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int x = lane < B ? seq_blocks(lens, lane, bs, max_blocks, window, min_len, row_start, row_div) : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += u;
+    }
+    if (lane < B) s_scan[lane + 1] = x;
+    if (lane == 0) s_scan[0] = 0;
+  }
+  __syncthreads();
+}
+
 // N: all positions, Nd: the dynamic ones under `share`. The dynamic share is
 // kept only when every CTA still gets at least min_static static positions;
 // every CTA computes the same split.
@@ -789,15 +808,26 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
   // reads or writes any caller buffer.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (w == kMmaWarps && !p.unit_mode) {
-    // Warm L2 with the block-table lines this CTA most likely reads first (a
-    // guess that assumes full-length sequences; it only overlaps the scan).
-    const int64_t per_seq = static_cast<int64_t>(HN) * p.max_blocks;
-    const int64_t pos = static_cast<int64_t>(blockIdx.x) * B * per_seq / gridDim.x + 32 * lane;
-    const int64_t seq = pos / per_seq;
-    const int j = static_cast<int>((pos - seq * per_seq) % p.max_blocks);
-    if (lane < 4 && seq < B) prefetch_l2(p.block_tables + seq * p.max_blocks + j);
+    // Warm L2 with the block-table lines this CTA reads first, which only the
+    // scan below decides: the whole table when it is small (up to 64 KB), else
+    // a guess that assumes full-length sequences. Either overlaps the scan.
+    const int64_t entries = static_cast<int64_t>(B) * p.max_blocks;
+    if (entries <= 16384) {
+      for (int64_t e = 32 * static_cast<int64_t>(lane); e < entries; e += 32 * 32) prefetch_l2(p.block_tables + e);
+      if (lane == 0) prefetch_l2(p.block_tables + entries - 1);
+    } else {
+      const int64_t per_seq = static_cast<int64_t>(HN) * p.max_blocks;
+      const int64_t pos = static_cast<int64_t>(blockIdx.x) * B * per_seq / gridDim.x + 32 * lane;
+      const int64_t seq = pos / per_seq;
+      const int j = static_cast<int>((pos - seq * per_seq) % p.max_blocks);
+      if (lane < 4 && seq < B) prefetch_l2(p.block_tables + seq * p.max_blocks + j);
+    }
   }
-  scan_blocks(p.context_lens, B, bs, p.max_blocks, wnd, min_len, row_start, row_div, s_scan);  // ends with a CTA barrier
+  // ends with a CTA barrier; a batch of up to 32 sequences is scanned by one warp
+  if (B <= 32)
+    scan_blocks_warp(p.context_lens, B, bs, p.max_blocks, wnd, min_len, row_start, row_div, s_scan);
+  else
+    scan_blocks(p.context_lens, B, bs, p.max_blocks, wnd, min_len, row_start, row_div, s_scan);
   const int64_t N = static_cast<int64_t>(HN) * s_scan[B];
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
