@@ -56,6 +56,7 @@ struct GqaParams {
   int* unit_lists;
   int list_cap;
   int64_t rec_slots;        // record slots in the workspace (2 per record pair)
+  int pair;                 // warp-MMA kernel, one-byte caches: two cache blocks of a segment per stage
 };
 
 #ifndef KVC_GQA_WARPS

@@ -701,20 +701,24 @@ __device__ __forceinline__ int64_t unit_record(const UnitRecs& u, int64_t unit, 
 // "full" barrier) in one of two query slots.
 
 struct GqaMmaSmem {
-  size_t box_bytes, stage_bytes, vs_off, q_off, q_slot_bytes, meta_off, full_off, empty_off, iss_off, misc_off,
-      scan_off, dscan_off, total;
+  size_t box_bytes, stage_bytes, vbox_off, vs_off, q_off, q_slot_bytes, meta_off, full_off, empty_off, iss_off,
+      misc_off, scan_off, dscan_off, total;
 };
 
 // q8: one-byte caches, whose stage holds one K and one V box (128 codes per
-// row) and the block's V scales [hc * block_size]. The query rows of a
-// segment go to one of two query slots after the ring (a segment's consumers
-// copy them into registers at its first stage).
+// row) and the block's V scales [hc * block_size]; with pair, two blocks of
+// one segment (K boxes, then V boxes, then the two scale arrays, so that the
+// second block's rows follow the first's). The query rows of a segment go to
+// one of two query slots after the ring (a segment's consumers copy them into
+// registers at its first stage).
 __host__ __device__ inline GqaMmaSmem gqa_mma_smem_layout(int q_elt, int GH, int block_size, int hc, int stages,
-                                                          int batch, bool q8 = false) {
+                                                          int batch, bool q8 = false, bool pair = false) {
   GqaMmaSmem s;
+  const size_t np = (q8 && pair) ? 2 : 1;  // cache blocks per stage
   s.box_bytes = static_cast<size_t>(hc) * block_size * 128;
-  s.vs_off = (q8 ? 2 : 4) * s.box_bytes;
-  s.stage_bytes = align_up(s.vs_off + (q8 ? static_cast<size_t>(hc) * block_size * 4 : 0), 1024);
+  s.vbox_off = (q8 ? np : 2) * s.box_bytes;
+  s.vs_off = (q8 ? 2 * np : 4) * s.box_bytes;
+  s.stage_bytes = align_up(s.vs_off + (q8 ? np * hc * block_size * 4 : 0), 1024);
   s.q_slot_bytes = static_cast<size_t>(hc) * GH * 128 * q_elt;
   s.q_off = static_cast<size_t>(stages) * s.stage_bytes;
   s.meta_off = s.q_off + 2 * s.q_slot_bytes;
@@ -743,7 +747,9 @@ struct StageMeta {
   int flags;
   int rec;         // record index of the segment (partial segments)
   int qslot;       // query slot holding the segment's query rows
+  int npos;        // cache blocks in the stage (2: blocks jb and jb + 1)
 };
+static_assert(sizeof(StageMeta) <= 64, "stage descriptor slot");
 constexpr int kFirst = 1, kLast = 2, kSrc = 4, kWhole = 8;
 
 // Q8 = 0: T is the cache and query type; Q8 = 1 (e4m3) or 2 (int8): one-byte
@@ -775,7 +781,8 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
   const int32_t* row_start = EXT ? p.row_start : nullptr;
   const int row_div = EXT ? p.row_div : 0;
   const int bs = p.block_size, S = p.stages;
-  const GqaMmaSmem L = gqa_mma_smem_layout(sizeof(T), GH, bs, hc, S, p.batch, Q8 != 0);
+  const bool paired = Q8 != 0 && p.pair != 0;  // two cache blocks per stage
+  const GqaMmaSmem L = gqa_mma_smem_layout(sizeof(T), GH, bs, hc, S, p.batch, Q8 != 0, paired);
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta_off);
   uint64_t* fbar = reinterpret_cast<uint64_t*>(smem + L.full_off);
   uint64_t* ebar = reinterpret_cast<uint64_t*>(smem + L.empty_off);
@@ -943,7 +950,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
                          : (bp.seq * p.n_q_heads + bp.chunk * hc * p.group + bp.hsub * GH) * D;
         }
         const int n = static_cast<int>(hi - bpos < 32 ? hi - bpos : 32);
-        for (int i = 0; i < n; ++i) {
+        for (int i = 0; i < n;) {
           StageMeta mi;
           mi.u0 = __shfl_sync(full, m.u0, i);
           mi.seq = __shfl_sync(full, m.seq, i);
@@ -956,8 +963,22 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
           mi.flags = __shfl_sync(full, m.flags, i);
           mi.rec = __shfl_sync(full, m.rec, i);
           mi.qslot = 0;
+          mi.npos = 1;
           const int srci = __shfl_sync(full, src, i);
           const int qo = __shfl_sync(full, qoff, i);
+          // paired stages: the segment's next block (held by lane i + 1 of this
+          // window) shares the stage when both blocks are valid
+          int srcj = -1;
+          if (paired) {
+            const int nx = (i + 1) & 31;
+            const int srcn = __shfl_sync(full, src, nx);
+            const int fln = __shfl_sync(full, m.flags, nx);
+            if (i + 1 < n && !(mi.flags & kLast) && srci >= 0 && srcn >= 0) {
+              srcj = srcn;
+              mi.npos = 2;
+              mi.flags |= fln & kLast;
+            }
+          }
           if (lane == 0) {
             ok = mbar_wait_data(ebar + slot, ph ^ 1u, p.wait_polls) && !*s_abort;
             const int qj = nseg & 1;
@@ -980,8 +1001,9 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
               ++icount;
               if (srci < 0) set_flag(p.err, 0x1u);
               meta[slot] = mi;
-              const uint32_t bytes = (srci >= 0 ? (Q8 ? 2 * box_bytes + vs_bytes : 4 * box_bytes) : 0u) +
-                                     (qo >= 0 ? q_bytes : 0u);
+              const uint32_t bytes =
+                  (srci >= 0 ? (Q8 ? static_cast<uint32_t>(mi.npos) * (2 * box_bytes + vs_bytes) : 4 * box_bytes) : 0u) +
+                  (qo >= 0 ? q_bytes : 0u);
               s_iss[slot] += 1u;
               if (bytes == 0) {
                 mbar_arrive(fbar + slot);
@@ -991,9 +1013,16 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
                 mbar_arrive_expect_tx(fbar + slot, bytes);
                 if (srci >= 0) {
                   if constexpr (Q8 != 0) {
+                    const uint32_t vdst = dst + static_cast<uint32_t>(L.vbox_off);
+                    unsigned char* vsd = smem + slot * L.stage_bytes + L.vs_off;
                     tma2d(dst, &tm_k, 0, srci, bar, pol);
-                    tma2d(dst + box_bytes, &tm_v, 0, srci, bar, pol);
-                    bulk_g2s(smem + slot * L.stage_bytes + L.vs_off, p.v_scale + srci, vs_bytes, fbar + slot, pol);
+                    tma2d(vdst, &tm_v, 0, srci, bar, pol);
+                    bulk_g2s(vsd, p.v_scale + srci, vs_bytes, fbar + slot, pol);
+                    if (srcj >= 0) {
+                      tma2d(dst + box_bytes, &tm_k, 0, srcj, bar, pol);
+                      tma2d(vdst + box_bytes, &tm_v, 0, srcj, bar, pol);
+                      bulk_g2s(vsd + vs_bytes, p.v_scale + srcj, vs_bytes, fbar + slot, pol);
+                    }
                   } else {
                     tma2d(dst, &tm_k, 0, srci, bar, pol);
                     tma2d(dst + box_bytes, &tm_k, 64, srci, bar, pol);
@@ -1047,6 +1076,7 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
             slot = 0;
             ph ^= 1u;
           }
+          i += mi.npos;
         }
       }
       if (!ok || p.unit_mode || sp.K == 0) break;
@@ -1174,29 +1204,34 @@ __global__ void __launch_bounds__(kMmaThreads, kMmaCtasPerSm)
               mma_tile<BF, GW, PT>(stg, stg + 2 * box_bytes, box_bytes, row0, lo_valid, valid, vis0, vis1, qsc, st,
                                    lane);
             else
-              mma_tile_q8<Q8, GW, PT>(stg, stg + box_bytes, row0, vsp, lo_valid, valid, vis0, vis1, qsc, st, lane);
+              mma_tile_q8<Q8, GW, PT>(stg, stg + static_cast<uint32_t>(L.vbox_off), row0, vsp, lo_valid, valid, vis0,
+                                      vis1, qsc, st, lane);
           };
           using Full = std::integral_constant<bool, false>;
           using Part = std::integral_constant<bool, true>;
           const int j0 = m.r0 / bs;
-          const int rb = m.n_rows - m.jb * bs;  // rows from the block's first to the end
-          const int vr = min(bs, rb);
-          const int lr = (m.jb == j0) ? m.r0 - j0 * bs : 0;
-          const int rowk = kh * bs;
           const int tiles = bs / 16;
-          if (rb - tm >= bs && lr == 0) {
-            for (int tt = 0; tt < tiles; ++tt) tile(Full{}, rowk + tt * 16, 0, 16, 16, 16);
-          } else {
-            for (int tt = 0; tt < tiles; ++tt) {
-              const int valid = vr - tt * 16, lo_valid = lr - tt * 16;
-              const int rt = rb - tt * 16;
-              if (valid <= 0) break;
-              if (lo_valid >= 16) continue;
-              if (rt - tm >= 16 && lo_valid <= 0)
-                tile(Full{}, rowk + tt * 16, 0, 16, 16, 16);
-              else
-                tile(Part{}, rowk + tt * 16, lo_valid, valid, EXT ? min(valid, rt - dh0) : valid,
-                     EXT ? min(valid, rt - dh1) : valid);
+          // block jb + j of a paired stage: its rows follow block jb's (hc * bs rows per block)
+          for (int j = 0; j < (paired ? m.npos : 1); ++j) {
+            const int jb = m.jb + j;
+            const int rb = m.n_rows - jb * bs;  // rows from the block's first to the end
+            const int vr = min(bs, rb);
+            const int lr = (jb == j0) ? m.r0 - j0 * bs : 0;
+            const int rowk = (j * hc + kh) * bs;
+            if (rb - tm >= bs && lr == 0) {
+              for (int tt = 0; tt < tiles; ++tt) tile(Full{}, rowk + tt * 16, 0, 16, 16, 16);
+            } else {
+              for (int tt = 0; tt < tiles; ++tt) {
+                const int valid = vr - tt * 16, lo_valid = lr - tt * 16;
+                const int rt = rb - tt * 16;
+                if (valid <= 0) break;
+                if (lo_valid >= 16) continue;
+                if (rt - tm >= 16 && lo_valid <= 0)
+                  tile(Full{}, rowk + tt * 16, 0, 16, 16, 16);
+                else
+                  tile(Part{}, rowk + tt * 16, lo_valid, valid, EXT ? min(valid, rt - dh0) : valid,
+                       EXT ? min(valid, rt - dh1) : valid);
+              }
             }
           }
         }
